@@ -1,0 +1,78 @@
+"""O1: the right product computed directly from the uncompressed matrix.
+
+The grammar method reaches y = Mx exactly (up to rounding order): Lemma 2.1
+(additivity), Lemma 2.2 (rows as roots) and Theorem 2.3 of the pages' Sec. 2
+prove it, and pass-through nodes are identities (Sec. 4.2). So the oracle for
+every policy is the plain definition y[i] = (+)_j M[i][j] (x) x[j], evaluated
+one row at a time from CSR.
+
+Precision: float64 for the (+, x) semiring (the pages state agreement "within
+float precision", Sec. 6 "Correctness"); exact int64 for integer inputs;
+bitwise OR/AND for the Boolean semiring (Sec. 5).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def matvec_f64(row_ptr, col, val, x):
+    """y = Mx and b = |M||x| in float64.
+
+    ``x`` is (m,) or (m, k) (k right-hand sides, Appendix A "Batched
+    evaluation"); y and b have shape (n,) or (n, k). b is the scale the
+    float32 tolerance is stated against: |y_i - y_ref_i| <= tol * b_i.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    n = len(row_ptr) - 1
+    shape = (n,) if x.ndim == 1 else (n, x.shape[1])
+    y = np.zeros(shape, dtype=np.float64)
+    b = np.zeros(shape, dtype=np.float64)
+    for i in range(n):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        v = np.asarray(val[s:e], dtype=np.float64)
+        xs = x[np.asarray(col[s:e], dtype=np.int64)]
+        y[i] = v @ xs
+        b[i] = np.abs(v) @ np.abs(xs)
+    return y, b
+
+
+def matvec_i64(row_ptr, col, val, x):
+    """Exact integer y = Mx (int64); values and x must be integers."""
+    x = np.asarray(x, dtype=np.int64)
+    v_all = np.asarray(val)
+    if not np.all(np.floor(v_all) == v_all):
+        raise ValueError("integer product needs integer matrix values")
+    n = len(row_ptr) - 1
+    shape = (n,) if x.ndim == 1 else (n, x.shape[1])
+    y = np.zeros(shape, dtype=np.int64)
+    for i in range(n):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        v = v_all[s:e].astype(np.int64)
+        y[i] = v @ x[np.asarray(col[s:e], dtype=np.int64)]
+    return y
+
+
+def matvec_or(row_ptr, col, x):
+    """Boolean semiring (OR, AND) on 64-bit bitsets (Sec. 5).
+
+    Every stored entry is a true edge, so the leaf map is the identity on x
+    and y[i] = OR over j in row i of x[j]; an empty row gives the OR-identity 0.
+    """
+    x = np.asarray(x, dtype=np.uint64)
+    n = len(row_ptr) - 1
+    y = np.zeros(n, dtype=np.uint64)
+    for i in range(n):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        if e > s:
+            y[i] = np.bitwise_or.reduce(x[np.asarray(col[s:e], dtype=np.int64)])
+    return y
+
+
+def within_tolerance(y, y_ref, b, tol):
+    """The float32 acceptance rule: |y - y_ref| <= tol * b elementwise, and
+    y exactly 0 where b is 0 (an all-zero row or all-zero x support)."""
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - y_ref)
+    ok = err <= tol * b
+    ok &= np.where(b == 0, y == 0, True)
+    return bool(np.all(ok)), float(np.max(err / np.where(b > 0, b, 1.0))) if err.size else 0.0

@@ -1,0 +1,53 @@
+"""Boolean-semiring reachability (Sec. 5 "Beyond (+,x)").
+
+One (OR, AND) product expands a BFS frontier by one step; the pages measure a
+single pass and name the iteration to the fixpoint as the next step
+(Sec. 5, Sec. 7 item 4). Reading taken here: with y[i] = OR over out-edges
+i -> j of x[j], iterating x <- x OR y from a frontier with bit b set at source
+s_b reaches the fixpoint in which bit b of x[i] is set exactly when i can
+reach s_b (reflexively).
+"""
+from __future__ import annotations
+
+from collections import deque
+
+import numpy as np
+
+from .direct import matvec_or
+
+
+def fixpoint(row_ptr, col, x0, max_iter=1000):
+    """Iterate x <- x | (M (x) x) until it stops changing.
+
+    Returns (x, iterations), where iterations counts the products computed,
+    the last of which changed nothing. Raises if max_iter is reached first.
+    """
+    x = np.asarray(x0, dtype=np.uint64).copy()
+    for it in range(1, max_iter + 1):
+        nxt = x | matvec_or(row_ptr, col, x)
+        if np.array_equal(nxt, x):
+            return x, it
+        x = nxt
+    raise RuntimeError("fixpoint not reached")
+
+
+def reach_bfs(row_ptr, col, n, srcs):
+    """Textbook BFS on the reversed graph from every source: bit b of the
+    result at node i is set iff i reaches srcs[b] along out-edges."""
+    indeg_lists = [[] for _ in range(n)]
+    for i in range(n):
+        for e in range(int(row_ptr[i]), int(row_ptr[i + 1])):
+            indeg_lists[int(col[e])].append(i)
+    out = np.zeros(n, dtype=np.uint64)
+    for b, s in enumerate(srcs):
+        seen = np.zeros(n, dtype=bool)
+        seen[s] = True
+        q = deque([int(s)])
+        while q:
+            v = q.popleft()
+            for u in indeg_lists[v]:
+                if not seen[u]:
+                    seen[u] = True
+                    q.append(u)
+        out[seen] |= np.uint64(1) << np.uint64(b)
+    return out

@@ -1,0 +1,114 @@
+"""Plant plausible mistakes in the oracle and check that its pins notice.
+
+Each mutant replaces one oracle function by a copy with a single slip (a
+dropped term, min for max, an off-by-one, a per-edge instead of shared
+pass-through chain, AND for OR). The pin tests in test_oracle_pins.py are
+then run against the mutant and must fail. Nothing here touches a GPU.
+"""
+import numpy as np
+import pytest
+
+import test_oracle_pins as pins
+from oracle import direct, grammar, reach
+
+
+def _drop_last_term(row_ptr, col, val, x):
+    x = np.asarray(x, dtype=np.float64)
+    n = len(row_ptr) - 1
+    y = np.zeros((n,) + x.shape[1:])
+    b = np.zeros_like(y)
+    for i in range(n):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        e2 = max(s, e - 1)
+        v = np.asarray(val[s:e2], dtype=np.float64)
+        xs = x[np.asarray(col[s:e2], dtype=np.int64)]
+        y[i] = v @ xs
+        b[i] = np.abs(v) @ np.abs(xs)
+    return y, b
+
+
+def _levels_min(R):
+    lvl = np.zeros(len(R), dtype=np.int64)
+    for i in range(len(R)):
+        a, b = int(R[i][0]), int(R[i][1])
+        lvl[i] = 1 + min(lvl[a] if a >= 0 else 0, lvl[b] if b >= 0 else 0)
+    return lvl
+
+
+def _eval_w_drop_right(g, V, x):
+    R = g["R"]
+    g2 = dict(g, R=np.array([[a, a] if b < 0 else [a, b] for a, b in R], dtype=np.int64).reshape(-1, 2))
+    return _orig_eval_w(g2, V, x)
+
+
+def _complete_per_edge(R, lvl):
+    # one chain per (parent, child) edge instead of one per child
+    L = int(lvl.max()) if len(lvl) else 0
+    layers = [[] for _ in range(L)]
+    for i in range(len(R)):
+        K = int(lvl[i])
+        ch = []
+        for c in R[i]:
+            c = int(c)
+            if c < 0:
+                ch.append(('t', -c - 1))
+            elif lvl[c] == K - 1:
+                ch.append(('n', c))
+            else:
+                for k in range(int(lvl[c]) + 1, K):
+                    below = ('n', c) if k - 1 == lvl[c] else ('p', c, k - 1, i)
+                    layers[k - 1].append((('p', c, k, i), (below,)))
+                ch.append(('p', c, K - 1, i))
+        layers[K - 1].append((('n', i), tuple(ch)))
+    return layers
+
+
+def _csrv_one_based_columns(row_ptr, col, val):
+    V, rows = _orig_csrv(row_ptr, col, val)
+    return V, [[(l, j + 1) for l, j in r] for r in rows]
+
+
+def _matvec_or_and(row_ptr, col, x):
+    x = np.asarray(x, dtype=np.uint64)
+    n = len(row_ptr) - 1
+    y = np.zeros(n, dtype=np.uint64)
+    for i in range(n):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        if e > s:
+            y[i] = np.bitwise_and.reduce(x[np.asarray(col[s:e], dtype=np.int64)])
+    return y
+
+
+_orig_eval_w = grammar.eval_w
+_orig_csrv = grammar.csrv
+
+MUTANTS = [
+    ("direct.matvec_f64 drops a term", direct, "matvec_f64", _drop_last_term,
+     ["test_worked_product_matches_fig_4_2", "test_direct_matches_dense_matmul"]),
+    ("levels uses min", grammar, "levels", _levels_min,
+     ["test_worked_levels_match_eq_3_1", "test_grammar_pipeline_on_random_matrices"]),
+    ("eval_w drops the right child", grammar, "eval_w", _eval_w_drop_right,
+     ["test_worked_grammar_eval_matches_fig_4_2", "test_grammar_pipeline_on_random_matrices"]),
+    ("completion per edge", grammar, "complete", _complete_per_edge,
+     ["test_grammar_pipeline_on_random_matrices"]),
+    ("csrv columns off by one", grammar, "csrv", _csrv_one_based_columns,
+     ["test_worked_csrv_matches_eq_2_2"]),
+    ("boolean product uses AND", direct, "matvec_or", _matvec_or_and,
+     ["test_direct_or_matches_dense_boolean"]),
+]
+
+
+@pytest.mark.parametrize("name,mod,attr,fn,tests", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, mod, attr, fn, tests, monkeypatch, worked):
+    monkeypatch.setattr(mod, attr, fn)
+    if mod is direct and attr == "matvec_or":
+        monkeypatch.setattr(reach, "matvec_or", fn)
+    for t in tests:
+        f = getattr(pins, t)
+        with pytest.raises(AssertionError):
+            if "worked" in f.__code__.co_varnames[:f.__code__.co_argcount]:
+                f(worked)
+            elif f.__code__.co_argcount == 1:
+                f(1)
+            else:
+                f()

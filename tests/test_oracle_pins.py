@@ -1,0 +1,268 @@
+"""Pins for the CPU oracle, against things other than the oracle itself:
+the pages' worked example (tests/golden/worked_example.json), library
+routines (numpy dense matmul, scipy BFS), closed forms and brute force.
+
+Each test is chosen so that a plausible slip in the oracle -- a dropped term,
+a wrong index, a transposed operand, min for max -- fails at least one of
+them (tests/test_oracle_mutants.py plants such slips and checks that).
+"""
+import itertools
+
+import numpy as np
+import pytest
+import scipy.sparse as sp
+from scipy.sparse.csgraph import breadth_first_order
+
+import gcsynth
+from oracle import direct, grammar, reach
+from conftest import dense_to_csr
+
+
+# ---------------------------------------------------------------- worked example
+def test_worked_product_matches_fig_4_2(worked):
+    rp, c, v = dense_to_csr(worked["M"], np.float64)
+    y, b = direct.matvec_f64(rp, c, v, worked["x"])
+    np.testing.assert_allclose(y, worked["y"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(b, np.abs(worked["M"]) @ np.abs(worked["x"]), atol=1e-12)
+
+
+def test_worked_csrv_matches_eq_2_2(worked):
+    rp, c, v = dense_to_csr(worked["M"], np.float64)
+    V, rows = grammar.csrv(rp, c, v)
+    np.testing.assert_allclose(V, worked["V"], atol=0)
+    assert rows == worked["S"]
+
+
+def test_worked_grammar_decompresses_to_S(worked):
+    # Eqs. 2.3 + 2.4 must expand to exactly the string of Eq. 2.2
+    assert grammar.decompress(worked["grammar"]) == worked["S"]
+
+
+def test_worked_grammar_eval_matches_fig_4_2(worked):
+    g = worked["grammar"]
+    y = grammar.eval_w(g, worked["V"], worked["x"])
+    np.testing.assert_allclose(y, worked["y"], atol=1e-12)
+    rv = worked["raw"]["product"]["root_values"]
+    for name, want in rv.items():
+        got = grammar.eval_recursive(int(name[1:]) - 1, g["R"], g["term_l"], g["term_j"],
+                                     worked["V"], worked["x"])
+        assert abs(got - want) < 1e-12
+
+
+def test_worked_levels_match_eq_3_1(worked):
+    lvl = grammar.levels(worked["grammar"]["R"])
+    assert int(lvl.max()) == worked["raw"]["levels"]["L"]
+    for k, members in enumerate(worked["level_sets"], start=1):
+        assert sorted(np.nonzero(lvl == k)[0].tolist()) == sorted(members)
+
+
+def test_worked_completion_matches_sec_4_2(worked):
+    g = worked["grammar"]
+    R = g["R"]
+    lvl = grammar.levels(R)
+    pt = worked["raw"]["pass_through"]
+    u = int(pt["carried"][1:]) - 1
+    reader = int(pt["reader"][1:]) - 1
+    layers = grammar.complete(R, lvl)
+    added = [key for layer in layers for key, _ in layer if key[0] == 'p']
+    assert added == [('p', u, pt["level"])]
+    assert grammar.pass_through_count(R, lvl) == pt["count"]
+    node_children = {key: ch for layer in layers for key, ch in layer}
+    assert ('p', u, pt["level"]) in node_children[('n', reader)]
+    assert grammar.is_properly_layered(layers)
+    # widths = printed strata plus the printed pass-through at its level
+    want = [len(s) for s in worked["level_sets"]]
+    want[pt["level"] - 1] += 1
+    assert [len(layer) for layer in layers] == want
+    assert grammar.live_widths(R, lvl) == want
+    y = grammar.eval_layered(layers, g, worked["V"], worked["x"])
+    np.testing.assert_allclose(y, worked["y"], atol=1e-12)
+
+
+def test_worked_repair_is_valid(worked):
+    g = grammar.repair(worked["S"])
+    assert grammar.decompress(g) == worked["S"]
+    _assert_repair_final(g)
+    y = grammar.eval_w(g, worked["V"], worked["x"])
+    np.testing.assert_allclose(y, worked["y"], atol=1e-12)
+
+
+def test_uncompleted_grammar_is_not_properly_layered(worked):
+    # the raw Eq. 2.3 grammar has the skip edge N8 -> N4; a layering that
+    # simply drops pass-throughs must be rejected by the checker
+    R = worked["grammar"]["R"]
+    lvl = grammar.levels(R)
+    layers = [[(key, ch) for key, ch in layer if key[0] == 'n'] for layer in grammar.complete(R, lvl)]
+    bad = []
+    for layer in layers:
+        bad.append([(key, tuple(('n', c[1]) if c[0] == 'p' else c for c in ch)) for key, ch in layer])
+    assert not grammar.is_properly_layered(bad)
+
+
+# ---------------------------------------------------------------- helpers
+def _assert_repair_final(g):
+    # stop rule: no pair of adjacent symbols occurs twice in the final C
+    seen = {}
+    for row in g["C"]:
+        for i in range(len(row) - 1):
+            p = (row[i], row[i + 1])
+            seen[p] = seen.get(p, 0) + 1
+    assert all(v < 2 for v in seen.values())
+    # topological numbering and every rule referenced
+    R = g["R"]
+    used = np.zeros(len(R), dtype=bool)
+    for i, (a, b) in enumerate(R):
+        for c in (a, b):
+            if c >= 0:
+                assert c < i
+                used[c] = True
+    for row in g["C"]:
+        for s in row:
+            if s >= 0:
+                used[s] = True
+    assert used.all()
+
+
+def _random_cases():
+    for seed in range(8):
+        n = 3 + seed % 5
+        m = 4 + (seed * 3) % 7
+        rp, c, v, dense = gcsynth.random_sparse(n, m, 0.6, [1.0, 2.0, -0.5], seed)
+        yield seed, rp, c, v, dense.astype(np.float64)
+    # genotype-shaped rows (few distinct repeated rows) exercise deep grammars
+    d = gcsynth.genotype_dense(n=12, m=40, founders=3, switch=0.05, mutation=0.01, seed=3)
+    rp, c, v = gcsynth.dense_to_csr(d)
+    yield 100, rp, c, v, d.astype(np.float64)
+
+
+# ---------------------------------------------------------------- library routines
+@pytest.mark.parametrize("k", [1, 3])
+def test_direct_matches_dense_matmul(k):
+    for seed, rp, c, v, dense in _random_cases():
+        x = np.random.default_rng(seed).standard_normal((dense.shape[1], k))
+        x = x[:, 0] if k == 1 else x
+        y, b = direct.matvec_f64(rp, c, v, x)
+        np.testing.assert_allclose(y, dense @ x, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(b, np.abs(dense) @ np.abs(x), rtol=1e-12, atol=1e-12)
+
+
+def test_direct_int_matches_dense_int_matmul():
+    for seed, rp, c, v, dense in _random_cases():
+        M = np.round(dense * 2).astype(np.int64)       # integer matrix
+        rp2, c2, v2 = dense_to_csr(M, np.float64)
+        x = np.random.default_rng(seed).integers(-10**6, 10**6, dense.shape[1])
+        assert np.array_equal(direct.matvec_i64(rp2, c2, v2, x), M @ x)
+
+
+def test_direct_or_matches_dense_boolean():
+    for seed, rp, c, v, dense in _random_cases():
+        x = np.random.default_rng(seed).integers(0, 2**63, dense.shape[1], dtype=np.uint64)
+        y = direct.matvec_or(rp, c, x)
+        A = dense != 0
+        for bit in range(64):
+            xb = ((x >> np.uint64(bit)) & np.uint64(1)).astype(np.int64)
+            want = (A.astype(np.int64) @ xb) > 0
+            got = ((y >> np.uint64(bit)) & np.uint64(1)).astype(bool)
+            assert np.array_equal(got, want)
+
+
+def test_tolerance_rule():
+    ok, _ = direct.within_tolerance([1.0, 0.0], np.array([1.0, 0.0]), np.array([1.0, 0.0]), 1e-4)
+    assert ok
+    ok, _ = direct.within_tolerance([1.0, 1e-30], np.array([1.0, 0.0]), np.array([1.0, 0.0]), 1e-4)
+    assert not ok
+    ok, _ = direct.within_tolerance([1.001], np.array([1.0]), np.array([1.0]), 1e-4)
+    assert not ok
+
+
+# ---------------------------------------------------------------- brute force
+def test_grammar_pipeline_on_random_matrices():
+    for seed, rp, c, v, dense in _random_cases():
+        V, rows = grammar.csrv(rp, c, v)
+        # CSRV decodes back to the matrix
+        back = np.zeros_like(dense)
+        for i, r in enumerate(rows):
+            for l, j in r:
+                back[i, j] = V[l]
+        np.testing.assert_array_equal(back, dense)
+        g = grammar.repair(rows)
+        assert grammar.decompress(g) == rows
+        _assert_repair_final(g)
+        x = np.random.default_rng(seed + 7).standard_normal(dense.shape[1])
+        want = dense @ x
+        np.testing.assert_allclose(grammar.eval_w(g, V, x), want, atol=1e-12)
+        for i, row in enumerate(g["C"]):
+            got = sum(grammar.eval_recursive(s, g["R"], g["term_l"], g["term_j"], V, x) for s in row)
+            assert abs(got - want[i]) < 1e-12
+        lvl = grammar.levels(g["R"])
+        # Eq. 3.1 checked edge by edge: a parent is strictly above each child,
+        # and exactly one above its highest child
+        for i, (a, b) in enumerate(g["R"]):
+            ch = [lvl[s] if s >= 0 else 0 for s in (a, b)]
+            assert lvl[i] == 1 + max(ch)
+        layers = grammar.complete(g["R"], lvl)
+        assert grammar.is_properly_layered(layers)
+        widths = [len(layer) for layer in layers]
+        assert widths == grammar.live_widths(g["R"], lvl)
+        assert sum(widths) == len(g["R"]) + grammar.pass_through_count(g["R"], lvl)
+        np.testing.assert_allclose(grammar.eval_layered(layers, g, V, x), want, atol=1e-12)
+
+
+def test_exhaustive_small_binary_matrices():
+    # every 0/1 matrix of shape 3x3 through the grammar pipeline
+    x = np.array([1.5, -2.0, 0.25])
+    for bits in itertools.product([0, 1], repeat=9):
+        dense = np.array(bits, dtype=np.float64).reshape(3, 3)
+        rp, c, v = dense_to_csr(dense, np.float64)
+        V, rows = grammar.csrv(rp, c, v)
+        g = grammar.repair(rows)
+        np.testing.assert_allclose(grammar.eval_w(g, V, x) if len(V) else np.zeros(3), dense @ x, atol=1e-12)
+
+
+def test_repeated_rows_compress_to_one_root():
+    # n identical rows of length m: RePair must end with one symbol per row
+    dense = np.tile(np.arange(1, 9, dtype=np.float64), (5, 1))
+    rp, c, v = dense_to_csr(dense, np.float64)
+    V, rows = grammar.csrv(rp, c, v)
+    g = grammar.repair(rows)
+    assert all(len(r) == 1 for r in g["C"]) and len({r[0] for r in g["C"]}) == 1
+    assert len(g["R"]) == 7         # a string of 8 symbols needs 7 binary rules
+
+
+# ---------------------------------------------------------------- reachability
+def _random_graph(n, deg, seed):
+    g = np.random.default_rng(seed)
+    rows = [np.unique(g.integers(0, n, g.integers(0, deg + 1))) for _ in range(n)]
+    rp = np.zeros(n + 1, dtype=np.int64)
+    np.cumsum([len(r) for r in rows], out=rp[1:])
+    col = np.concatenate(rows).astype(np.int32) if rp[-1] else np.zeros(0, np.int32)
+    return rp, col
+
+
+def test_reach_matches_scipy_bfs():
+    for seed in range(5):
+        n = 60
+        rp, col = _random_graph(n, 2, seed)
+        srcs = np.random.default_rng(seed).choice(n, 10, replace=False)
+        x0 = gcsynth.frontier(n, srcs)
+        xs, iters = reach.fixpoint(rp, col, x0)
+        A = sp.csr_matrix((np.ones(len(col)), col, rp), shape=(n, n))
+        AT = A.T.tocsr()
+        want = np.zeros(n, dtype=np.uint64)
+        for b, s in enumerate(srcs):
+            nodes = breadth_first_order(AT, int(s), directed=True, return_predecessors=False)
+            want[nodes] |= np.uint64(1) << np.uint64(b)
+        assert np.array_equal(xs, want)
+        assert np.array_equal(reach.reach_bfs(rp, col, n, srcs), want)
+
+
+def test_reach_iterations_on_a_path():
+    # 0 -> 1 -> ... -> n-1, source n-1: n-1 products spread the bit to node 0,
+    # the n-th changes nothing
+    n = 9
+    rp = np.concatenate([np.arange(n, dtype=np.int64), [n - 1]])
+    col = np.arange(1, n, dtype=np.int32)
+    x0 = gcsynth.frontier(n, np.array([n - 1]))
+    xs, iters = reach.fixpoint(rp, col, x0)
+    assert iters == n
+    assert np.all(xs == 1)
