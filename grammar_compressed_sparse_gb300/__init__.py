@@ -1,0 +1,155 @@
+"""Grammar-compressed right products y = Mx on one GB300.
+
+The matrix is CSRV-encoded, RePair-compressed and made properly layered on
+the host (``Grammar``); ``Engine`` uploads the packed grammar into a device
+arena that torch allocates and runs the level-synchronous sweep in the
+library's sm_103a kernels. Both are thin wrappers over the C ABI in
+``include/gcsparse.h`` (``capi`` has the one-to-one bindings).
+"""
+from __future__ import annotations
+
+import hashlib
+import os
+
+import numpy as np
+
+from . import capi
+from .capi import GcError  # noqa: F401
+
+
+class Grammar:
+    """A built grammar (host). ``Grammar(n, m, row_ptr, col, val)`` runs
+    CSRV + RePair + levels + pass-through completion + packing."""
+
+    def __init__(self, n=None, m=None, row_ptr=None, col=None, val=None, *, block_rows=0,
+                 threads=0, order=0, _ptr=None):
+        self._p = _ptr if _ptr is not None else capi.gc_build(
+            n, m, row_ptr, col, val, block_rows=block_rows, threads=threads, order=order)
+
+    @classmethod
+    def load(cls, path: str) -> "Grammar":
+        return cls(_ptr=capi.gc_load(path))
+
+    def save(self, path: str):
+        capi.gc_save(self._p, path)
+
+    def stats(self) -> dict:
+        return capi.gc_stats(self._p)
+
+    def widths(self) -> np.ndarray:
+        return capi.gc_widths(self._p)
+
+    def export(self, which: str) -> np.ndarray:
+        return capi.gc_export(self._p, which)
+
+    def layout(self, policy="f32", k_max=1) -> dict:
+        return capi.gc_layout(self._p, policy, k_max)
+
+    def __del__(self):
+        p = getattr(self, "_p", None)
+        if p:
+            capi.gc_free_grammar(p)
+            self._p = None
+
+
+class Engine:
+    """A grammar resident on a CUDA device, ready for products.
+
+    The arena is one torch uint8 tensor of ``layout()["arena_bytes"]`` bytes;
+    the library never allocates device memory itself.
+    """
+
+    def __init__(self, grammar: Grammar, policy="f32", k_max=1, device="cuda", stream=None):
+        import torch
+
+        self.policy, self.k_max = policy, k_max
+        st = grammar.stats()
+        self.n, self.m = st["n"], st["m"]
+        self.layout = grammar.layout(policy, k_max)
+        self.device = torch.device(device)
+        self.arena = torch.empty(max(self.layout["arena_bytes"], 256), dtype=torch.uint8,
+                                 device=self.device)
+        self._stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self._h = capi.gc_upload(grammar._p, policy, k_max, self.arena, self.arena.numel(), self._stream)
+        self._stream.synchronize()
+
+    @property
+    def dtype(self):
+        import torch
+        return {"f32": torch.float32, "i64": torch.int64, "or": torch.int64}[self.policy]
+
+    def matvec(self, x, y=None, stream=None):
+        """y = M x for a device tensor x of shape (m,) or (m, k)."""
+        import torch
+        k = 1 if x.dim() == 1 else x.shape[1]
+        if y is None:
+            y = torch.empty((self.n,) if x.dim() == 1 else (self.n, k), dtype=x.dtype, device=x.device)
+        capi.gc_matvec(self._h, x, y, k, stream if stream is not None else self._stream)
+        return y
+
+    def matvec_host(self, x: np.ndarray, y: np.ndarray | None = None, stream=None) -> np.ndarray:
+        """Same product with host buffers (copies in and out, synchronises)."""
+        k = 1 if x.ndim == 1 else x.shape[1]
+        if y is None:
+            y = np.empty((self.n,) if x.ndim == 1 else (self.n, k), dtype=x.dtype)
+        capi.gc_matvec_host(self._h, np.ascontiguousarray(x), y, k,
+                            stream if stream is not None else self._stream)
+        return y
+
+    def reach(self, x0, max_iter=1000, stream=None):
+        """Boolean fixpoint from a device int64/uint64 bitset tensor; returns (x, iterations, status)."""
+        import torch
+        x = torch.empty_like(x0)
+        iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
+        rc = capi.gc_reach(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        return x, int(iters.item()), rc
+
+    def check(self, stream=None) -> int:
+        return capi.gc_check(self._h, stream if stream is not None else self._stream)
+
+    def launch_count(self) -> int:
+        return capi.gc_launch_count(self._h)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            capi.gc_free_handle(h)
+            self._h = None
+
+
+def _builder_fingerprint() -> str:
+    from . import build as _b
+    h = hashlib.sha256()
+    for f in _b.HOST_SOURCES + _b.HEADERS:
+        with open(os.path.join(_b.CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def cached_grammar(key: str, make_csr, cache_dir=None, **build_kwargs) -> Grammar:
+    """Build a grammar, reusing a saved copy when one exists.
+
+    ``make_csr()`` returns (n, m, row_ptr, col, val). The file name combines
+    ``key``, the build options and a hash of the builder's sources, so a
+    changed builder never reuses an old file. A file that fails to load or
+    validate is rebuilt. Set GCSPARSE_NO_CACHE=1 to always rebuild.
+    """
+    cache_dir = cache_dir or os.environ.get("GCSPARSE_CACHE",
+                                            os.path.join(os.path.expanduser("~"), ".cache", "gcsparse"))
+    tag = hashlib.sha256(repr((key, sorted(build_kwargs.items()))).encode()).hexdigest()[:16]
+    path = os.path.join(cache_dir, f"{tag}-{_builder_fingerprint()}.gcg")
+    if os.environ.get("GCSPARSE_NO_CACHE") != "1" and os.path.exists(path):
+        try:
+            return Grammar.load(path)
+        except capi.GcError:
+            pass
+    n, m, row_ptr, col, val = make_csr()
+    g = Grammar(n, m, row_ptr, col, val, **build_kwargs)
+    try:
+        os.makedirs(cache_dir, exist_ok=True)
+        tmp = path + f".tmp{os.getpid()}"
+        g.save(tmp)
+        os.replace(tmp, path)
+    except (OSError, capi.GcError):
+        pass
+    return g

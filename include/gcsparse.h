@@ -1,0 +1,243 @@
+/*
+ * gcsparse.h -- C ABI of the grammar-compressed right-product engine.
+ *
+ * The method is the one of "Right Multiplication on Grammar-Compressed
+ * Matrices: A Streaming, Memory-Bounded GPU Engine" (the pages):
+ *   - a matrix M (n x m) is CSRV-encoded (Sec. 2 "CSRV", Eqs. 2.1-2.2): the
+ *     distinct non-zero values form V, and each row becomes a string of
+ *     terminals <l, j> (value V[l] in column j);
+ *   - RePair compresses the row strings, never pairing across a row end, into
+ *     rules N_i -> A_i B_i and a final sequence C (Sec. 2 "Grammar",
+ *     Eqs. 2.3-2.4; Sec. 4.1);
+ *   - levels (Eq. 3.1) and pass-through completion (Sec. 4.2) make the
+ *     grammar properly layered (Def. 3.2), so that y = Mx is a bottom-up sweep
+ *     in which level k reads only level k-1 (Lemma 3.3, Sec. 4.3);
+ *   - the sweep needs only an associative combine, so the same schedule
+ *     evaluates (+, x) in float32, 16 right-hand sides at once (Appendix A),
+ *     exact int64, and the Boolean semiring on 64-bit bitsets (Sec. 5).
+ *
+ * Conventions
+ *   - All indices are 0-based. Sizes are int64_t unless stated.
+ *   - Every function returns a gc_status; none throws, exits or aborts.
+ *     On failure gc_last_error() gives a message (thread-local).
+ *   - Streams are cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Device work is enqueued on that stream and is asynchronous
+ *     unless the entry point says it synchronises.
+ *   - The library never allocates device memory for the product path: the
+ *     caller allocates one device arena of gc_layout().arena_bytes and
+ *     passes it to gc_upload(). Host objects (gc_grammar, gc_handle) are
+ *     library-owned and released with the matching gc_free_*.
+ */
+#ifndef GCSPARSE_H
+#define GCSPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GC_OK = 0,
+    GC_ERR_ARG = -1,              /* bad argument (null pointer, size, k, policy) */
+    GC_ERR_OOM = -2,              /* host allocation failed                        */
+    GC_ERR_CUDA = -3,             /* a CUDA runtime call failed                    */
+    GC_ERR_INVALID_GRAMMAR = -4,  /* packed grammar failed validation              */
+    GC_ERR_UNSUPPORTED = -5,      /* valid request this build cannot serve         */
+    GC_ERR_TIMEOUT = -6,          /* a device-side wait ran out (status word)      */
+    GC_ERR_NOT_CONVERGED = -7,    /* gc_reach hit max_iter before the fixpoint     */
+    GC_ERR_IO = -8                /* gc_save / gc_load file error                  */
+} gc_status;
+
+/* Leaf / combine / emit policy of the sweep (Sec. 5: any monoid homomorphism).
+ *   GC_F32_SUM  (+, x) in float32; k = 1 or k = 16 right-hand sides
+ *   GC_I64_SUM  (+, x) in exact int64; matrix values must be integers; k = 1
+ *   GC_BOOL_OR  (OR, AND) on uint64 bitsets (64 sources per word); every
+ *               stored entry must be 1 (an edge); k = 1                       */
+typedef enum { GC_F32_SUM = 0, GC_I64_SUM = 1, GC_BOOL_OR = 2 } gc_policy;
+
+typedef struct {
+    int64_t block_rows; /* 0: one grammar for all rows. >0: RePair runs on each
+                           block of block_rows rows separately (Sec. 1 "row
+                           blocks"); the blocks share one terminal table and
+                           their levels are merged, so one sweep serves all.  */
+    int32_t threads;    /* host threads for block-parallel RePair; 0 = all     */
+    int32_t order;      /* within-level node order (any order is correct,
+                           Sec. 4.3): 0 = by first column of the node's
+                           expansion (locality of child reads, default);
+                           1 = RePair creation order                          */
+} gc_build_opts;
+
+typedef struct {
+    int64_t n, m, nnz;      /* matrix shape and stored non-zeros              */
+    int64_t n_values;       /* |V|: distinct non-zero values                  */
+    int64_t n_terminals;    /* alpha: distinct terminals <l, j>               */
+    int64_t n_rules;        /* |R|: RePair nonterminals                       */
+    int64_t n_pass;         /* pass-through nodes added by completion (+pt)   */
+    int64_t n_nodes;        /* |R| + n_pass: layered nodes                    */
+    int64_t depth;          /* L: number of levels                            */
+    int64_t max_width;      /* w*: widest level = streaming-buffer length     */
+    int64_t c_len;          /* |C| without row delimiters                     */
+    int64_t n_roots;        /* rho: distinct nonterminals occurring in C      */
+    int64_t n_blocks;       /* row blocks compressed separately (1 if none)   */
+    double  repair_seconds; /* host time of CSRV + RePair                     */
+    double  layer_seconds;  /* host time of levels + completion + packing     */
+} gc_grammar_stats;
+
+/* Arrays a built grammar can hand back (for checking and serialising).      */
+typedef enum {
+    GC_A_VALUES = 0,        /* float[n_values]: V ascending                              */
+    GC_A_TERM_COL = 1,      /* int32[n_terminals]: column j of terminal t (sorted by j, l) */
+    GC_A_TERM_VIDX = 2,     /* int32[n_terminals]: value index l of terminal t           */
+    GC_A_RULES = 3,         /* int32[2*n_rules]: (A_i, B_i) per rule in creation order;
+                               a child s >= 0 is N_s, s < 0 is terminal -s-1           */
+    GC_A_C_OFF = 4,         /* int64[n+1]: row r's symbols are C[c_off[r]..c_off[r+1]) */
+    GC_A_C_SYM = 5,         /* int32[c_len]: C in the GC_A_RULES symbol encoding        */
+    GC_A_RULE_LEVEL = 6,    /* int32[n_rules]: Eq. 3.1 level of each rule               */
+    GC_A_LVL_OFF = 7,       /* int64[depth+2]: level k's packed nodes are
+                               [lvl_off[k], lvl_off[k+1]); lvl_off[0] = lvl_off[1] = 0 */
+    GC_A_NODES = 8,         /* int32[2*n_nodes]: packed child references (a, b) per node;
+                               c >= 0: slot c of level k-1's buffer; c < 0: T[-c-1]
+                               where T[0] is the combine identity and T[p+1] leaf p.
+                               A pass-through is (c, -1).                               */
+    GC_A_LVL_ROOTS = 9,     /* int64[depth+2]: number of roots of level k; a level's
+                               roots are its first nodes                                */
+    GC_A_ROOT_OFF = 10,     /* int64[depth+2]: RV slot of level k's first root          */
+    GC_A_C_REF = 11,        /* int32[c_len]: C packed: >= 0 RV slot, < 0 T[-c-1]         */
+    GC_A_NODE_ID = 12       /* int32[n_nodes]: what each packed node is: rule i >= 0, or
+                               -(u+1) for a pass-through carrying rule u                */
+} gc_array;
+
+typedef struct {
+    int64_t arena_bytes;    /* total device bytes gc_upload needs (256-B aligned parts) */
+    int64_t grammar_bytes;  /* read-only grammar arrays: nodes, level tables, leaves,
+                               V-resolved leaf values, C offsets and references        */
+    int64_t scratch_bytes;  /* T, root values RV, the two level buffers, status word   */
+    int64_t staging_bytes;  /* device copies of x and y used by gc_matvec_host          */
+    int64_t csr_bytes;      /* the same matrix as CSR: 4 B col + 4 B value per
+                               non-zero + 4 (n+1) row pointers (8 (n+1) when
+                               nnz >= 2^31), + x and y (Sec. 4.4 "Space")              */
+} gc_arena_layout;
+
+typedef struct gc_grammar gc_grammar;
+typedef struct gc_handle gc_handle;
+
+/* Thread-local message of the last failure in this thread ("" if none).     */
+const char* gc_last_error(void);
+
+/* Library version string, e.g. "gcsparse 0.1 sm_103a".                     */
+const char* gc_version(void);
+
+/*
+ * gc_build -- CSRV-encode, RePair-compress and layer a CSR matrix (host).
+ * Sec. 2 (CSRV, RePair with row boundaries), Sec. 3 (Eq. 3.1), Sec. 4.1-4.3
+ * (pass-through completion, level-major layout).
+ *   row_ptr  int64[n+1], non-decreasing, row_ptr[0] = 0
+ *   col      int32[nnz], in [0, m); a row's columns need not be sorted but
+ *            must be distinct
+ *   val      float[nnz], finite; NULL means every entry is 1. Zeros (+0/-0)
+ *            are dropped, as CSRV stores non-zeros only. Values are the same
+ *            V entry iff their float bit patterns are equal.
+ *   opts     may be NULL (defaults: one block, all threads, locality order)
+ *   out      receives a library-owned grammar; free with gc_free_grammar.
+ * Host memory only; no device is touched. Errors: GC_ERR_ARG for bad CSR,
+ * GC_ERR_OOM, GC_ERR_UNSUPPORTED when a count exceeds int32 limits.
+ */
+gc_status gc_build(int64_t n, int64_t m, const int64_t* row_ptr, const int32_t* col,
+                   const float* val, const gc_build_opts* opts, gc_grammar** out);
+
+/* Structural figures of a built grammar (Table 4.1's |R|, L, w*, +pt).      */
+gc_status gc_stats(const gc_grammar* g, gc_grammar_stats* out);
+
+/* Level widths w_1..w_L (Lemma 3.3; Sec. 4.2: width = live set).
+ * w must hold cap >= depth entries.                                          */
+gc_status gc_widths(const gc_grammar* g, int64_t* w, int64_t cap);
+
+/* Size in bytes of an exported array (see gc_array).                        */
+gc_status gc_export_size(const gc_grammar* g, gc_array which, int64_t* bytes);
+
+/* Copy an array of the grammar into dst (host memory of dst_bytes bytes).   */
+gc_status gc_export(const gc_grammar* g, gc_array which, void* dst, int64_t dst_bytes);
+
+/*
+ * gc_layout -- device bytes needed to serve products under a policy with up
+ * to k_max right-hand sides (k_max = 1 or 16 for GC_F32_SUM, 1 otherwise).
+ * GC_ERR_UNSUPPORTED if the grammar's values do not fit the policy (non-
+ * integer values for GC_I64_SUM, values other than 1 for GC_BOOL_OR).
+ */
+gc_status gc_layout(const gc_grammar* g, gc_policy policy, int32_t k_max, gc_arena_layout* out);
+
+/*
+ * gc_upload -- copy the packed grammar into a caller-owned device arena and
+ * return a handle for products.
+ *   arena        device pointer, 256-byte aligned, arena_bytes >= the
+ *                gc_layout() figure for the same policy and k_max. It must
+ *                outlive the handle; the library does not free it.
+ *   stream       the copies are enqueued on it; the call returns after they
+ *                are enqueued and the host-side validation (every child index
+ *                within the level below, every terminal within alpha, every C
+ *                reference within rho / alpha) has passed.
+ * The handle keeps host copies of the level tables; the grammar may be freed
+ * after the upload's copies completed (synchronise the stream first).
+ * One product at a time per handle: the level buffers are shared by calls.
+ */
+gc_status gc_upload(const gc_grammar* g, gc_policy policy, int32_t k_max, void* arena,
+                    int64_t arena_bytes, void* stream, gc_handle** out);
+
+/*
+ * gc_matvec -- y = M x on the device (Lemmas 2.1-2.2, Theorem 2.3, Sec. 4.3,
+ * Appendix A for k > 1). Asynchronous on stream.
+ *   x   device, m*k elements, row-major (x[j*k + c] is column j of input c)
+ *       float for GC_F32_SUM, int64_t for GC_I64_SUM, uint64_t for GC_BOOL_OR
+ *   y   device, n*k elements, row-major, same element type; fully written
+ *       (a row with no non-zeros gets the combine identity: 0)
+ *   k   1, or 16 with GC_F32_SUM when the handle was uploaded with k_max 16
+ * x and y must not overlap the arena. Deterministic: the same x gives the same
+ * y bit for bit (fixed summation order, no atomics).
+ */
+gc_status gc_matvec(gc_handle* h, const void* x, void* y, int32_t k, void* stream);
+
+/*
+ * gc_matvec_host -- the same product with x and y in HOST memory: copies x
+ * into the arena's staging area, runs gc_matvec, copies y back and
+ * synchronises the stream before returning. Host buffers should be pinned
+ * for full copy speed (pageable memory works but is slower).
+ */
+gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t k,
+                         void* stream);
+
+/*
+ * gc_reach -- Boolean-semiring fixpoint x <- x OR (M (x) x) from x0 until it
+ * stops changing (Sec. 5; the pages stop at one pass and name the fixpoint as
+ * the next step, Sec. 7 item 4). Requires GC_BOOL_OR and n == m.
+ *   x0, x    device uint64_t[n]; bit b of x[i] ends set iff node i reaches a
+ *            node whose bit b is set in x0. x may equal x0 (in place).
+ *   iters    device int32_t[1]: products performed, the last of which changed
+ *            nothing; -1 if max_iter was reached first (gc_check then returns
+ *            GC_ERR_NOT_CONVERGED).
+ * Synchronises the stream once per product to read the changed flag.
+ */
+gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
+                   int32_t* iters, void* stream);
+
+/* Synchronise the stream and return the device status word of the handle
+ * (GC_OK, GC_ERR_TIMEOUT, GC_ERR_NOT_CONVERGED, GC_ERR_INVALID_GRAMMAR).
+ * The word is cleared after it is read.                                     */
+gc_status gc_check(gc_handle* h, void* stream);
+
+/* Number of kernel launches the most recent gc_matvec on h enqueued.        */
+gc_status gc_launch_count(const gc_handle* h, int64_t* launches);
+
+/* Serialise / restore a built grammar (host file, little-endian, versioned). */
+gc_status gc_save(const gc_grammar* g, const char* path);
+gc_status gc_load(const char* path, gc_grammar** out);
+
+void gc_free_grammar(gc_grammar* g);
+void gc_free_handle(gc_handle* h);   /* host object only; not the arena */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCSPARSE_H */

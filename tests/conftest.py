@@ -69,3 +69,26 @@ def dense_to_csr(M, dtype=np.float32):
     np.cumsum((M != 0).sum(1), out=row_ptr[1:])
     r, c = np.nonzero(M)
     return row_ptr, c.astype(np.int32), M[r, c].astype(dtype)
+
+
+@pytest.fixture(scope="session")
+def gcs():
+    """The product package with its library built (compiles on first use)."""
+    from grammar_compressed_sparse_gb300 import build
+    build.build()
+    import grammar_compressed_sparse_gb300 as pkg
+    return pkg
+
+
+def export_all(G):
+    names = ["values", "term_col", "term_vidx", "rules", "c_off", "c_sym", "rule_level", "lvl_off",
+             "nodes", "lvl_roots", "root_off", "c_ref", "node_id"]
+    return {a: G.export(a) for a in names}
+
+
+def oracle_grammar(ex):
+    """The builder's raw SLP in the oracle's representation."""
+    R = ex["rules"].reshape(-1, 2).astype(np.int64)
+    c_off = ex["c_off"]
+    C = [ex["c_sym"][c_off[r]:c_off[r + 1]].astype(np.int64).tolist() for r in range(len(c_off) - 1)]
+    return dict(R=R, C=C, term_l=ex["term_vidx"].astype(np.int64), term_j=ex["term_col"].astype(np.int64))

@@ -1,0 +1,244 @@
+"""Host builder (CSRV, RePair, levels, completion, packing) checked against
+the oracle on the CPU, through the C ABI. No GPU needed."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import gcsynth
+from conftest import ROOT, dense_to_csr, export_all, oracle_grammar
+from oracle import direct, grammar
+from packed_emulator import emulate
+
+
+def _cases():
+    for seed in range(6):
+        n = 4 + seed * 3
+        m = 5 + seed * 4
+        rp, c, v, dense = gcsynth.random_sparse(n, m, 0.5, [1.0, 2.0, -0.5, 3.25], seed)
+        yield f"rand{seed}", rp, c, v
+    for seed, (n, m, F) in enumerate([(30, 200, 3), (64, 500, 5), (200, 300, 8)]):
+        d = gcsynth.genotype_dense(n=n, m=m, founders=F, switch=0.02, mutation=0.005, seed=seed)
+        rp, c, v = gcsynth.dense_to_csr(d)
+        yield f"geno{n}x{m}", rp, c, v
+
+
+CASES = list(_cases())
+
+
+def check_grammar(G, rp, c, v, n, m, block_rows=0):
+    ex = export_all(G)
+    st = G.stats()
+    og = oracle_grammar(ex)
+    V, rows = grammar.csrv(rp, c, v)
+    # CSRV: same dictionary; terminal table is the sorted set of used <l, j>
+    np.testing.assert_array_equal(ex["values"].astype(np.float64), V.astype(np.float32).astype(np.float64))
+    # O3: decompression reproduces S
+    assert grammar.decompress(og) == rows
+    # RePair end state: no pair of adjacent symbols repeats in C, topological numbering
+    # (per row block when blocks are compressed separately)
+    seen = {}
+    for r, row in enumerate(og["C"]):
+        blk = r // block_rows if block_rows else 0
+        for i in range(len(row) - 1):
+            key = (blk, row[i], row[i + 1])
+            seen[key] = seen.get(key, 0) + 1
+    assert all(cnt < 2 for cnt in seen.values())
+    for i, (a, b) in enumerate(og["R"]):
+        assert (a < 0 or a < i) and (b < 0 or b < i)
+    # O4: Eq. 3.1 levels, live-set widths, pass-through count
+    lvl = grammar.levels(og["R"])
+    np.testing.assert_array_equal(ex["rule_level"], lvl)
+    assert st["depth"] == (int(lvl.max()) if len(lvl) else 0)
+    np.testing.assert_array_equal(G.widths(), grammar.live_widths(og["R"], lvl))
+    assert st["n_pass"] == grammar.pass_through_count(og["R"], lvl)
+    assert st["n_nodes"] == st["n_rules"] + st["n_pass"]
+    # packed nodes are the oracle's completed grammar, level by level
+    layers = grammar.complete(og["R"], lvl)
+    node_id = ex["node_id"]
+    lo = ex["lvl_off"]
+    nodes = ex["nodes"].reshape(-1, 2)
+    roots = {s for row in og["C"] for s in row if s >= 0}
+    for k in range(1, st["depth"] + 1):
+        ids = node_id[lo[k]:lo[k + 1]]
+        want = sorted([key[1] if key[0] == 'n' else -(key[1] + 1) for key, _ in layers[k - 1]])
+        assert sorted(ids.tolist()) == want
+        nr = int(ex["lvl_roots"][k])
+        assert all(i >= 0 and i in roots for i in ids[:nr])
+        assert not any(i >= 0 and i in roots for i in ids[nr:])
+        prev_ids = node_id[lo[k - 1]:lo[k]] if k > 1 else np.zeros(0, np.int32)
+        for q, i in enumerate(ids):
+            a, b = nodes[lo[k] + q]
+            kids = [int(og["R"][i][0]), int(og["R"][i][1])] if i >= 0 else [-i - 1]
+            refs = [a, b] if i >= 0 else [a]
+            if i < 0:
+                assert b == -1
+            for kid, ref in zip(kids, refs):
+                if kid < 0:
+                    assert ref == kid - 1           # terminal t -> T[t+1]
+                else:
+                    assert ref >= 0
+                    assert prev_ids[ref] in (kid, -(kid + 1))
+    # values: packed emulator and W-array sweep against the direct product
+    x = np.random.default_rng(1).standard_normal(m)
+    y_ref, b = direct.matvec_f64(rp, c, v, x)
+    np.testing.assert_allclose(grammar.eval_w(og, ex["values"], x), y_ref, rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(emulate(ex, x), y_ref, rtol=1e-9, atol=1e-9)
+    X = np.random.default_rng(2).standard_normal((m, 3))
+    np.testing.assert_allclose(emulate(ex, X), direct.matvec_f64(rp, c, v, X)[0], rtol=1e-9, atol=1e-9)
+    return ex
+
+
+def test_library_exports_every_header_symbol(gcs):
+    text = open(os.path.join(ROOT, "include", "gcsparse.h")).read()
+    declared = set(re.findall(r"^\s*(?:gc_status|void|const char\*)\s+(gc_\w+)\s*\(", text, re.M))
+    assert declared, "no declarations parsed"
+    import ctypes
+    lib = ctypes.CDLL(gcs.capi._build.LIB)
+    for name in sorted(declared):
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert declared == set(gcs.capi.EXPORTED)
+
+
+def test_worked_example_builds(gcs, worked):
+    rp, c, v = dense_to_csr(worked["M"], np.float32)
+    G = gcs.Grammar(8, 7, rp, c, v)
+    ex = check_grammar(G, rp, c, v, 8, 7)
+    y = emulate(ex, worked["x"])
+    np.testing.assert_allclose(y, worked["y"], rtol=1e-6)
+    st = G.stats()
+    assert st["n_values"] == 4 and st["n_terminals"] == 12
+
+
+@pytest.mark.parametrize("name,rp,c,v", CASES, ids=[cs[0] for cs in CASES])
+def test_builder_matches_oracle(gcs, name, rp, c, v):
+    n, m = len(rp) - 1, int(c.max()) + 3
+    G = gcs.Grammar(n, m, rp, c, v)
+    check_grammar(G, rp, c, v, n, m)
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("block_rows", [0, 7, 64])
+def test_blocks_and_orders(gcs, order, block_rows):
+    d = gcsynth.genotype_dense(n=150, m=400, founders=6, switch=0.01, mutation=0.005, seed=11)
+    rp, c, v = gcsynth.dense_to_csr(d)
+    G = gcs.Grammar(150, 400, rp, c, v, block_rows=block_rows, order=order)
+    ex = check_grammar(G, rp, c, v, 150, 400, block_rows)
+    st = G.stats()
+    assert st["n_blocks"] == (1 if block_rows == 0 else -(-150 // block_rows))
+    if block_rows:
+        # no rule is shared across blocks: each block's rows use its own rules
+        og = oracle_grammar(ex)
+        owner = {}
+        for r, row in enumerate(og["C"]):
+            blk = r // block_rows
+            stack = [s for s in row if s >= 0]
+            while stack:
+                s = stack.pop()
+                assert owner.setdefault(s, blk) == blk
+                stack.extend(int(z) for z in og["R"][s] if z >= 0)
+
+
+def test_integer_and_boolean_values(gcs):
+    # graph-like 0/1 matrix, built with val = NULL (every entry 1)
+    rp, col = gcsynth.copy_model_graph(nodes=300, n0=10, d0=12, p_edit=0.1, seed=5)
+    G = gcs.Grammar(300, 300, rp, col, None)
+    ex = export_all(G)
+    assert ex["values"].tolist() == [1.0]
+    x = np.random.default_rng(0).integers(0, 2**63, 300, dtype=np.uint64)
+    np.testing.assert_array_equal(emulate(ex, x, "or"), direct.matvec_or(rp, col, x))
+    xi = np.random.default_rng(1).integers(-1000, 1000, 300)
+    np.testing.assert_array_equal(emulate(ex, xi, "i64"),
+                                  direct.matvec_i64(rp, col, np.ones(len(col)), xi))
+    for pol in ("f32", "i64", "or"):
+        lay = G.layout(pol, 1)
+        assert lay["arena_bytes"] >= lay["grammar_bytes"] + lay["scratch_bytes"]
+    with pytest.raises(gcs.GcError):
+        G.layout("f32", 3)
+
+
+def test_policy_value_checks(gcs):
+    rp, c, v, _ = gcsynth.random_sparse(10, 10, 0.5, [0.5, 2.0], 3)
+    G = gcs.Grammar(10, 10, rp, c, v)
+    with pytest.raises(gcs.GcError, match="UNSUPPORTED"):
+        G.layout("i64", 1)
+    with pytest.raises(gcs.GcError, match="UNSUPPORTED"):
+        G.layout("or", 1)
+    rp, c, v, _ = gcsynth.random_sparse(10, 10, 0.5, [1.0, 2.0], 3)
+    G = gcs.Grammar(10, 10, rp, c, v)
+    G.layout("i64", 1)
+    with pytest.raises(gcs.GcError, match="UNSUPPORTED"):
+        G.layout("or", 1)
+
+
+@pytest.mark.parametrize("bad", ["row_ptr", "col_range", "dup", "nan", "inf"])
+def test_bad_csr_is_rejected(gcs, bad):
+    rp = np.array([0, 2, 3], dtype=np.int64)
+    c = np.array([0, 2, 1], dtype=np.int32)
+    v = np.array([1.0, 2.0, 3.0], dtype=np.float32)
+    if bad == "row_ptr":
+        rp = np.array([0, 3, 2], dtype=np.int64)
+    elif bad == "col_range":
+        c = np.array([0, 5, 1], dtype=np.int32)
+    elif bad == "dup":
+        c = np.array([1, 1, 1], dtype=np.int32)
+    elif bad == "nan":
+        v[1] = np.nan
+    elif bad == "inf":
+        v[1] = np.inf
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.Grammar(2, 3, rp, c, v)
+
+
+def test_zeros_unsorted_and_degenerate(gcs):
+    # stored zeros are dropped; unsorted rows are ordered by column
+    rp = np.array([0, 3, 3, 5], dtype=np.int64)
+    c = np.array([2, 0, 1, 1, 0], dtype=np.int32)
+    v = np.array([1.5, 0.0, -0.0, 1.5, 2.0], dtype=np.float32)
+    G = gcs.Grammar(3, 3, rp, c, v)
+    ex = export_all(G)
+    x = np.array([1.0, 2.0, 4.0])
+    dense = np.zeros((3, 3))
+    for r in range(3):
+        for q in range(rp[r], rp[r + 1]):
+            dense[r, c[q]] = v[q]
+    np.testing.assert_allclose(emulate(ex, x), dense @ x)
+    # empty matrix, all-empty rows, a single non-zero, no repetition at all
+    for n, m, rp, c, v in [
+        (0, 0, np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32)),
+        (4, 6, np.zeros(5, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32)),
+        (3, 3, np.array([0, 0, 1, 1], np.int64), np.array([2], np.int32), np.array([5.0], np.float32)),
+        (2, 4, np.array([0, 2, 4], np.int64), np.array([0, 1, 2, 3], np.int32),
+         np.array([1, 2, 3, 4], np.float32)),
+    ]:
+        G = gcs.Grammar(n, m, rp, c, v)
+        st = G.stats()
+        assert st["n"] == n
+        ex = export_all(G)
+        x = np.arange(1, m + 1, dtype=np.float64)
+        dense = np.zeros((n, m))
+        for r in range(n):
+            for q in range(rp[r], rp[r + 1]):
+                dense[r, c[q]] = v[q]
+        np.testing.assert_allclose(emulate(ex, x), dense @ x)
+        assert G.layout("f32", 1)["arena_bytes"] > 0
+
+
+def test_save_load_roundtrip(gcs, tmp_path):
+    d = gcsynth.genotype_dense(n=40, m=120, founders=4, switch=0.02, mutation=0.01, seed=2)
+    rp, c, v = gcsynth.dense_to_csr(d)
+    G = gcs.Grammar(40, 120, rp, c, v)
+    p = str(tmp_path / "g.bin")
+    G.save(p)
+    H = gcs.Grammar.load(p)
+    a, b = export_all(G), export_all(H)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
+    assert G.stats()["n_nodes"] == H.stats()["n_nodes"]
+    with open(p, "r+b") as f:
+        f.truncate(100)
+    with pytest.raises(gcs.GcError, match="GC_ERR_IO"):
+        gcs.Grammar.load(p)
+    with pytest.raises(gcs.GcError, match="GC_ERR_IO"):
+        gcs.Grammar.load(str(tmp_path / "missing.bin"))

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA sweep through the C ABI against the CPU oracle.
+
+Tolerance for float32 (+, x): |y_i - y_ref_i| <= 1e-4 * (|M||x|)_i with y_i
+exactly 0 where (|M||x|)_i = 0, y_ref in float64 (oracle.direct). Integer
+and Boolean policies must match bit for bit.
+"""
+import numpy as np
+import pytest
+
+import gcsynth
+from conftest import dense_to_csr
+from oracle import direct, reach
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return t
+
+
+def _dev(torch, a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def f32_product(gcs, torch, G, x, k_max=1):
+    eng = gcs.Engine(G, "f32", k_max)
+    y = eng.matvec(_dev(torch, x.astype(np.float32)))
+    torch.cuda.synchronize()
+    assert eng.check() == 0
+    return y.cpu().numpy(), eng
+
+
+def assert_f32_parity(y, rp, c, v, x):
+    y_ref, b = direct.matvec_f64(rp, c, v, x.astype(np.float32))
+    ok, worst = direct.within_tolerance(y, y_ref, b, TOL)
+    assert ok, f"max scaled error {worst:.3e} > {TOL}"
+    return worst
+
+
+def _small_cases():
+    for seed in range(4):
+        rp, c, v, _ = gcsynth.random_sparse(5 + 7 * seed, 6 + 9 * seed, 0.5, [1.0, 2.0, -0.5, 3.25], seed)
+        yield f"rand{seed}", len(rp) - 1, 6 + 9 * seed, rp, c, v
+    d = gcsynth.genotype_dense(n=300, m=900, founders=6, switch=0.01, mutation=0.005, seed=4)
+    rp, c, v = gcsynth.dense_to_csr(d)
+    yield "geno300x900", 300, 900, rp, c, v
+
+
+SMALL = list(_small_cases())
+
+
+def test_worked_example_f32(gcs, torch, worked):
+    rp, c, v = dense_to_csr(worked["M"], np.float32)
+    G = gcs.Grammar(8, 7, rp, c, v)
+    y, _ = f32_product(gcs, torch, G, worked["x"])
+    b = np.abs(worked["M"]) @ np.abs(worked["x"])
+    assert np.all(np.abs(y - worked["y"]) <= TOL * b)
+    assert_f32_parity(y, rp, c, v, worked["x"])
+
+
+@pytest.mark.parametrize("name,n,m,rp,c,v", SMALL, ids=[s[0] for s in SMALL])
+def test_small_f32_k1_and_k16(gcs, torch, name, n, m, rp, c, v):
+    G = gcs.Grammar(n, m, rp, c, v)
+    x = np.random.default_rng(3).standard_normal(m).astype(np.float32)
+    y, eng = f32_product(gcs, torch, G, x, k_max=16)
+    assert_f32_parity(y, rp, c, v, x)
+    X = np.random.default_rng(4).standard_normal((m, 16)).astype(np.float32)
+    Y = eng.matvec(_dev(torch, X)).cpu().numpy()
+    for col in range(16):
+        assert_f32_parity(Y[:, col], rp, c, v, X[:, col])
+
+
+@pytest.mark.parametrize("name,n,m,rp,c,v", SMALL, ids=[s[0] for s in SMALL])
+def test_small_i64_exact(gcs, torch, name, n, m, rp, c, v):
+    vi = np.round(v * 4).astype(np.float32)          # integer-valued matrix
+    keep = vi != 0
+    rp2 = np.concatenate([[0], np.cumsum([keep[rp[i]:rp[i + 1]].sum() for i in range(n)])]).astype(np.int64)
+    c2, vi = c[keep], vi[keep]
+    G = gcs.Grammar(n, m, rp2, c2, vi)
+    x = np.random.default_rng(5).integers(-10**9, 10**9, m)
+    eng = gcs.Engine(G, "i64", 1)
+    y = eng.matvec(_dev(torch, x)).cpu().numpy()
+    np.testing.assert_array_equal(y, direct.matvec_i64(rp2, c2, vi, x))
+
+
+def test_genotype_small_config(gcs, torch):
+    cfg = gcsynth.GENO_SMALL
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    G = gcs.Grammar(cfg["n"], cfg["m"], rp, c, v)
+    st = G.stats()
+    assert st["depth"] > 3 and st["n_pass"] > 0
+    x = gcsynth.beta(cfg["m"], seed=0)
+    y, eng = f32_product(gcs, torch, G, x, k_max=16)
+    assert_f32_parity(y, rp, c, v, x)
+    # deterministic: the same input gives the same bits
+    y2 = eng.matvec(_dev(torch, x)).cpu().numpy()
+    np.testing.assert_array_equal(y, y2)
+    # host-buffer entry point gives the same bits
+    np.testing.assert_array_equal(eng.matvec_host(x), y)
+    X = gcsynth.beta(cfg["m"], seed=1, k=16)
+    Y = eng.matvec(_dev(torch, X)).cpu().numpy()
+    y_ref, b = direct.matvec_f64(rp, c, v, X)
+    ok, worst = direct.within_tolerance(Y, y_ref, b, TOL)
+    assert ok, worst
+    np.testing.assert_array_equal(eng.matvec_host(X), Y)
+    # integer policy on the same matrix, exact
+    xi = np.random.default_rng(9).integers(-1000, 1000, cfg["m"])
+    ei = gcs.Engine(G, "i64", 1)
+    np.testing.assert_array_equal(ei.matvec(_dev(torch, xi)).cpu().numpy(),
+                                  direct.matvec_i64(rp, c, v, xi))
+
+
+def test_genotype_wide_slice(gcs, torch):
+    # 600 rows of the 50,000-variant generator: many tiles per level, ragged tails
+    cfg = dict(gcsynth.GENO_MEDIUM, n=600)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    G = gcs.Grammar(600, cfg["m"], rp, c, v)
+    x = gcsynth.beta(cfg["m"], seed=7)
+    y, _ = f32_product(gcs, torch, G, x)
+    assert_f32_parity(y, rp, c, v, x)
+
+
+def test_boolean_product_and_fixpoint(gcs, torch):
+    N = 3000
+    rp, col = gcsynth.copy_model_graph(nodes=N, n0=20, d0=15, p_edit=0.05, seed=1)
+    G = gcs.Grammar(N, N, rp, col, None)
+    eng = gcs.Engine(G, "or", 1)
+    x = np.random.default_rng(2).integers(0, 2**63, N, dtype=np.uint64)
+    y = eng.matvec(_dev(torch, x.view(np.int64))).cpu().numpy().view(np.uint64)
+    np.testing.assert_array_equal(y, direct.matvec_or(rp, col, x))
+    srcs = gcsynth.sources(N, 64, seed=0)
+    x0 = gcsynth.frontier(N, srcs)
+    xs, iters, rc = eng.reach(_dev(torch, x0.view(np.int64)))
+    assert rc == 0
+    want, want_iters = reach.fixpoint(rp, col, x0)
+    np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint64), want)
+    assert iters == want_iters
+    # not converged within one product: status and iteration count say so
+    xs1, iters1, rc1 = eng.reach(_dev(torch, x0.view(np.int64)), max_iter=1)
+    assert rc1 == gcs.capi.GC_ERR_NOT_CONVERGED and iters1 == -1
+    assert eng.check() == gcs.capi.GC_ERR_NOT_CONVERGED
+    assert eng.check() == 0          # the status word is cleared once read
+
+
+def test_edge_cases(gcs, torch):
+    cases = [
+        (4, 6, np.zeros(5, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32)),      # all rows empty
+        (3, 3, np.array([0, 0, 1, 1], np.int64), np.array([2], np.int32), np.array([5.0], np.float32)),
+        (2, 4, np.array([0, 2, 4], np.int64), np.array([0, 1, 2, 3], np.int32),
+         np.array([1, 2, 3, 4], np.float32)),                                             # no rules (L = 0)
+        (1, 1, np.array([0, 1], np.int64), np.array([0], np.int32), np.array([-2.5], np.float32)),
+    ]
+    for n, m, rp, c, v in cases:
+        G = gcs.Grammar(n, m, rp, c, v)
+        x = np.arange(1, m + 1, dtype=np.float32)
+        y, _ = f32_product(gcs, torch, G, x)
+        assert_f32_parity(y, rp, c, v, x)
+    # long rows made of bare terminals plus one repeated row: C-heavy emit
+    rp, c, v, _ = gcsynth.random_sparse(40, 3000, 0.4, [1.0, -1.0, 0.5], 8)
+    G = gcs.Grammar(40, 3000, rp, c, v)
+    x = np.random.default_rng(1).standard_normal(3000).astype(np.float32)
+    y, _ = f32_product(gcs, torch, G, x)
+    assert_f32_parity(y, rp, c, v, x)
+
+
+def test_argument_errors(gcs, torch):
+    rp, c, v, _ = gcsynth.random_sparse(20, 30, 0.5, [1.0, 2.0], 0)
+    G = gcs.Grammar(20, 30, rp, c, v)
+    eng = gcs.Engine(G, "f32", 1)
+    X = torch.zeros((30, 16), device="cuda")
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        eng.matvec(X)                                 # k = 16 on a k_max = 1 handle
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_reach(eng._h, X, X, 5, X)        # reach needs the OR policy
+    arena = torch.empty(G.layout("f32", 1)["arena_bytes"] + 512, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_upload(G._p, "f32", 1, arena.data_ptr() + 16, arena.numel() - 16)
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_upload(G._p, "f32", 1, arena, 1024)
