@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -92,67 +93,140 @@ def compulsory_bytes(st, k, alpha):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """SM clock and throttle reasons sampled DURING the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML directly (libnvidia-ml, read-only queries) from a thread about
+    every millisecond, because a timed region of a few milliseconds is far
+    shorter than nvidia-smi's sampling period; nvidia-smi is the fallback.
+    """
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index):
         self.index = index
-        self.proc = None
+        self.samples = []
+        self.max_mhz = None
+        self._stop = False
+        self._thread = None
+        self._nvml = None
+        self._smi = None
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        return lib, h, get_reasons
+
+    def _loop(self):
+        import ctypes
+        lib, h, get_reasons = self._nvml
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(0.001)
 
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            self._nvml = self._open_nvml()
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+            while not self.samples and self._thread.is_alive():   # first sample before timing starts
+                time.sleep(0.0005)
+        except (OSError, AttributeError):
+            self._nvml = None
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}", "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._smi = None
         return self
 
     def __exit__(self, *a):
-        self.out = ""
-        if self.proc:
-            self.proc.terminate()
+        if self._thread is not None:
+            time.sleep(0.002)   # one more sample at the end of the region
+            self._stop = True
+            self._thread.join(timeout=2)
+        if self._smi is not None:
+            self._smi.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self._smi.communicate(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self._smi.kill()
+                out, _ = self._smi.communicate()
+            for r in out.strip().splitlines():
+                f = [x.strip() for x in r.split(",")]
+                try:
+                    self.samples.append((int(float(f[0])), int(f[2], 16)))
+                    self.max_mhz = int(float(f[1]))
+                except (ValueError, IndexError):
+                    pass
 
     def summary(self):
-        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.count(",") >= 8]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        mhz = [c for c, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(name for bit, name in self.REASONS.items() if bits & bit)
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
-def cpu_oracle_rate(gen, k, seconds, rows_cap=None):
-    """Products per second of the CPU oracle on a bounded sample of rows."""
-    from threadpoolctl import threadpool_limits
+ORACLE_SAMPLE_ROWS = 2000
 
+
+def _oracle_sample(workload, seconds, steps):
+    """Runs in a child process whose BLAS is limited to one thread. Generates
+    the first ORACLE_SAMPLE_ROWS rows of the workload's matrix once, then for
+    each of ``steps`` steps runs the oracle's float64 direct product over
+    blocks of 250 of those rows until ``seconds`` pass; prints, per step, the
+    rows done and the time, as JSON."""
     from oracle import direct
-    rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=rows_cap or gen["n"]))
+    wl = WORKLOADS[workload]
+    gen, k = wl["gen"], wl["k"]
+    rows = min(gen["n"], ORACLE_SAMPLE_ROWS)
+    rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=rows))
     x = gcsynth.beta(gen["m"], seed=0, k=k)
-    n = len(rp) - 1
-    done_rows = 0
-    t0 = time.perf_counter()
-    with threadpool_limits(limits=1):
+    out = []
+    for _ in range(steps):
+        done_rows = 0
+        t0 = time.perf_counter()
         while time.perf_counter() - t0 < seconds:
-            a = done_rows % n
-            b = min(n, a + 250)
+            a = done_rows % rows
+            b = min(rows, a + 250)
             direct.matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
             done_rows += b - a
-    el = time.perf_counter() - t0
-    products = done_rows / gen["n"]
-    return products / el, {"rows": done_rows, "seconds": round(el, 3), "cores": 1}
+        out.append({"rows": done_rows, "seconds": time.perf_counter() - t0})
+    print(json.dumps(out), flush=True)
+
+
+def cpu_oracle_rates(workload, seconds, steps=1):
+    """Products per second of the CPU oracle, one figure per step, each step
+    a bounded sample (``seconds``) of the workload's rows; timed in a child
+    process with one BLAS / OpenMP thread."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample",
+                          "--workload", workload, "--cpu-seconds", str(seconds), "--steps", str(steps)],
+                         env=env, capture_output=True, text=True, check=True).stdout
+    recs = json.loads(out.strip().splitlines()[-1])
+    n = WORKLOADS[workload]["gen"]["n"]
+    return [(r["rows"] / n) / r["seconds"] for r in recs], recs
 
 
 def run_reference(args):
@@ -162,12 +236,9 @@ def run_reference(args):
     wl = WORKLOADS[args.workload]
     gen, k = wl["gen"], wl["k"]
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
-    rates = []
-    for i in range(args.warmup + args.steps):
-        r, info = cpu_oracle_rate(gen, k, per_step)
-        if i >= args.warmup:
-            rates.append(r)
-    value = statistics.mean(rates)
+    rates, _ = cpu_oracle_rates(args.workload, per_step, args.warmup + args.steps)
+    rates = rates[args.warmup:]
+    value = len(rates) / sum(1.0 / r for r in rates)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "matvec/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -175,7 +246,8 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "n": gen["n"], "m": gen["m"], "k": k},
         "cpu_baseline": {"value": value, "unit": "matvec/s", "cores": 1, "kind": "oracle",
-                         "sample": f"float64 CSR rows in blocks of 250, about {per_step:.1f} s per step"},
+                         "sample": f"float64 direct product over the first {ORACLE_SAMPLE_ROWS} rows "
+                                   f"in blocks of 250, {per_step:.1f} s per step, scaled to whole products"},
         "e2e": {"value": value, "unit": "matvec/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -301,10 +373,11 @@ def run_ours(args):
     footprint = lay["grammar_bytes"] + lay["scratch_bytes"] + 4 * k * (gen["m"] + gen["n"])
     cpu = None
     if not args.no_cpu_baseline:
-        r, info = cpu_oracle_rate(gen, k, args.cpu_seconds)
-        cpu = {"value": r, "unit": "matvec/s", "cores": info["cores"], "kind": "oracle",
-               "sample": f"{info['rows']} rows ({info['rows'] / gen['n']:.2f} products) of the same "
-                         f"matrix in {info['seconds']} s, float64, one BLAS thread"}
+        rates, recs = cpu_oracle_rates(args.workload, args.cpu_seconds)
+        cpu = {"value": rates[0], "unit": "matvec/s", "cores": 1, "kind": "oracle",
+               "sample": f"{recs[0]['rows']} rows ({recs[0]['rows'] / gen['n']:.2f} products) of the "
+                         f"first {ORACLE_SAMPLE_ROWS} rows of the same matrix in {recs[0]['seconds']:.1f} s, "
+                         "float64, one BLAS thread"}
     line = {
         "metric": METRIC, "value": value, "unit": "matvec/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
@@ -339,7 +412,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.oracle_sample:
+        _oracle_sample(args.workload, args.cpu_seconds, args.steps)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -11,10 +11,23 @@ from __future__ import annotations
 import hashlib
 import os
 
+import importlib
+
 import numpy as np
 
-from . import capi
-from .capi import GcError  # noqa: F401
+
+def __getattr__(name):
+    # The binding loads libgcsparse.so; it is imported on first use so that
+    # the ``build`` submodule can run before the library exists. Without the
+    # library every product entry point raises ImportError (no fallback).
+    if name in ("capi", "GcError"):
+        mod = importlib.import_module(".capi", __name__)
+        return mod if name == "capi" else mod.GcError
+    raise AttributeError(name)
+
+
+def _capi():
+    return importlib.import_module(".capi", __name__)
 
 
 class Grammar:
@@ -23,32 +36,35 @@ class Grammar:
 
     def __init__(self, n=None, m=None, row_ptr=None, col=None, val=None, *, block_rows=0,
                  threads=0, order=0, _ptr=None):
-        self._p = _ptr if _ptr is not None else capi.gc_build(
+        self._p = _ptr if _ptr is not None else _capi().gc_build(
             n, m, row_ptr, col, val, block_rows=block_rows, threads=threads, order=order)
 
     @classmethod
     def load(cls, path: str) -> "Grammar":
-        return cls(_ptr=capi.gc_load(path))
+        return cls(_ptr=_capi().gc_load(path))
 
     def save(self, path: str):
-        capi.gc_save(self._p, path)
+        _capi().gc_save(self._p, path)
 
     def stats(self) -> dict:
-        return capi.gc_stats(self._p)
+        return _capi().gc_stats(self._p)
 
     def widths(self) -> np.ndarray:
-        return capi.gc_widths(self._p)
+        return _capi().gc_widths(self._p)
 
     def export(self, which: str) -> np.ndarray:
-        return capi.gc_export(self._p, which)
+        return _capi().gc_export(self._p, which)
 
     def layout(self, policy="f32", k_max=1) -> dict:
-        return capi.gc_layout(self._p, policy, k_max)
+        return _capi().gc_layout(self._p, policy, k_max)
 
     def __del__(self):
         p = getattr(self, "_p", None)
         if p:
-            capi.gc_free_grammar(p)
+            try:
+                _capi().gc_free_grammar(p)
+            except Exception:   # interpreter shutdown
+                pass
             self._p = None
 
 
@@ -70,7 +86,7 @@ class Engine:
         self.arena = torch.empty(max(self.layout["arena_bytes"], 256), dtype=torch.uint8,
                                  device=self.device)
         self._stream = stream if stream is not None else torch.cuda.current_stream(self.device)
-        self._h = capi.gc_upload(grammar._p, policy, k_max, self.arena, self.arena.numel(), self._stream)
+        self._h = _capi().gc_upload(grammar._p, policy, k_max, self.arena, self.arena.numel(), self._stream)
         self._stream.synchronize()
 
     @property
@@ -84,7 +100,7 @@ class Engine:
         k = 1 if x.dim() == 1 else x.shape[1]
         if y is None:
             y = torch.empty((self.n,) if x.dim() == 1 else (self.n, k), dtype=x.dtype, device=x.device)
-        capi.gc_matvec(self._h, x, y, k, stream if stream is not None else self._stream)
+        _capi().gc_matvec(self._h, x, y, k, stream if stream is not None else self._stream)
         return y
 
     def matvec_host(self, x: np.ndarray, y: np.ndarray | None = None, stream=None) -> np.ndarray:
@@ -92,7 +108,7 @@ class Engine:
         k = 1 if x.ndim == 1 else x.shape[1]
         if y is None:
             y = np.empty((self.n,) if x.ndim == 1 else (self.n, k), dtype=x.dtype)
-        capi.gc_matvec_host(self._h, np.ascontiguousarray(x), y, k,
+        _capi().gc_matvec_host(self._h, np.ascontiguousarray(x), y, k,
                             stream if stream is not None else self._stream)
         return y
 
@@ -101,19 +117,30 @@ class Engine:
         import torch
         x = torch.empty_like(x0)
         iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
-        rc = capi.gc_reach(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        rc = _capi().gc_reach(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
         return x, int(iters.item()), rc
 
     def check(self, stream=None) -> int:
-        return capi.gc_check(self._h, stream if stream is not None else self._stream)
+        return _capi().gc_check(self._h, stream if stream is not None else self._stream)
 
     def launch_count(self) -> int:
-        return capi.gc_launch_count(self._h)
+        return _capi().gc_launch_count(self._h)
+
+    @property
+    def schedule(self) -> str:
+        return "persistent" if _capi().gc_get_schedule(self._h) == 0 else "per_level"
+
+    @schedule.setter
+    def schedule(self, name: str):
+        _capi().gc_set_schedule(self._h, {"persistent": 0, "per_level": 1}[name])
 
     def __del__(self):
         h = getattr(self, "_h", None)
         if h:
-            capi.gc_free_handle(h)
+            try:
+                _capi().gc_free_handle(h)
+            except Exception:   # interpreter shutdown
+                pass
             self._h = None
 
 
@@ -141,7 +168,7 @@ def cached_grammar(key: str, make_csr, cache_dir=None, **build_kwargs) -> Gramma
     if os.environ.get("GCSPARSE_NO_CACHE") != "1" and os.path.exists(path):
         try:
             return Grammar.load(path)
-        except capi.GcError:
+        except _capi().GcError:
             pass
     n, m, row_ptr, col, val = make_csr()
     g = Grammar(n, m, row_ptr, col, val, **build_kwargs)
@@ -150,6 +177,6 @@ def cached_grammar(key: str, make_csr, cache_dir=None, **build_kwargs) -> Gramma
         tmp = path + f".tmp{os.getpid()}"
         g.save(tmp)
         os.replace(tmp, path)
-    except (OSError, capi.GcError):
+    except (OSError, _capi().GcError):
         pass
     return g

@@ -29,6 +29,7 @@ STATUS_NAMES = {0: "GC_OK", -1: "GC_ERR_ARG", -2: "GC_ERR_OOM", -3: "GC_ERR_CUDA
                 -7: "GC_ERR_NOT_CONVERGED", -8: "GC_ERR_IO"}
 
 GC_F32_SUM, GC_I64_SUM, GC_BOOL_OR = 0, 1, 2
+GC_SCHED_PERSISTENT, GC_SCHED_PER_LEVEL = 0, 1
 POLICIES = {"f32": GC_F32_SUM, "i64": GC_I64_SUM, "or": GC_BOOL_OR}
 
 ARRAYS = {  # gc_array enum -> numpy dtype
@@ -79,6 +80,9 @@ _sig = {
     "gc_reach": ([_vp, _vp, _vp, _i32, _vp, _vp], ctypes.c_int),
     "gc_check": ([_vp, _vp], ctypes.c_int),
     "gc_launch_count": ([_vp, ctypes.POINTER(_i64)], ctypes.c_int),
+    "gc_set_schedule": ([_vp, _i32], ctypes.c_int),
+    "gc_get_schedule": ([_vp, ctypes.POINTER(_i32)], ctypes.c_int),
+    "gc_debug_inject": ([_vp, _i32, _i64], ctypes.c_int),
     "gc_save": ([_vp, ctypes.c_char_p], ctypes.c_int),
     "gc_load": ([ctypes.c_char_p, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_free_grammar": ([_vp], None),
@@ -194,6 +198,20 @@ def gc_launch_count(h) -> int:
     v = _i64()
     _check(_lib.gc_launch_count(h, ctypes.byref(v)), "gc_launch_count")
     return v.value
+
+
+def gc_set_schedule(h, schedule: int):
+    _check(_lib.gc_set_schedule(h, schedule), "gc_set_schedule")
+
+
+def gc_get_schedule(h) -> int:
+    v = _i32()
+    _check(_lib.gc_get_schedule(h, ctypes.byref(v)), "gc_get_schedule")
+    return v.value
+
+
+def gc_debug_inject(h, what: int, timeout_cycles: int):
+    _check(_lib.gc_debug_inject(h, what, timeout_cycles), "gc_debug_inject")
 
 
 def gc_save(g, path: str):

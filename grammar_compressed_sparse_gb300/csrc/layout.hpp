@@ -1,60 +1,75 @@
 // Device arena layout of an uploaded grammar (host-side arithmetic only; used
 // by gc_layout and gc_upload). Every part starts on a 256-byte boundary.
 //
-//   read-only grammar            nodes        int2[N]        (a, b) child refs
-//                                lvl_off      int64[L+2]
-//                                lvl_roots    int64[L+2]
-//                                root_off     int64[L+2]
-//                                leaf_col     int32[alpha]
-//                                leaf_val     policy[alpha]  V[l] of each leaf (none for OR)
-//                                c_off        int32[n+1]
-//                                c_ref        int32[|C|]
-//   scratch (overwritten)        T            value[alpha+1]  T[0] identity
-//                                RV           value[rho]      root values
-//                                buf0, buf1   value[w*]       level ping-pong
-//                                status       256 B           device status word, flags
-//   staging (host-buffer calls)  xs           value[m]
-//                                ys           value[n]
+//   read-only grammar   nodes     int2[sum of padded widths]  (a, b) child refs,
+//                                 each level starting on a 16-node (128 B)
+//                                 boundary and padded to a multiple of 16
+//                       levels    int64[4 (L+2)]   per level k: padded start,
+//                                 width, number of roots, RV slot of the first root
+//                       V         policy[|V|]      value dictionary
+//                       c_off     int32[n+1]
+//                       c_ref     int32[|C|]
+//   scratch             RV        value[rho]       root values
+//                       buf0/1    value[w*]        level ping-pong buffers
+//                       status    256 B            status word, fixpoint flag,
+//                                                  grid-barrier arrival counter
+//   staging             xs        value[m]         x / y copies for the
+//                       ys        value[n]         host-buffer entry point
 // "value" is k_max elements of the policy's type (float, int64, uint64).
+//
+// Device child references (rewritten from the packed T-index form at upload):
+//   c >= 0    slot c of the previous level's buffer
+//   c == -1   the combine identity (second child of a pass-through)
+//   c <= -2   leaf q = -c - 2 = (column << vbits) | value index: the leaf value
+//             V[l] (x) x[j] is evaluated in the sweep, no terminal array.
 #pragma once
 
 #include "common.hpp"
 
 namespace gcs {
 
+constexpr int64_t kNodeAlign = 16;   // nodes per 128-byte bulk-copy granule
+
 struct DevLayout {
-    int64_t nodes, lvl_off, lvl_roots, root_off, leaf_col, leaf_val, c_off, c_ref;
-    int64_t T, RV, buf0, buf1, status, xs, ys;
+    int64_t nodes, levels, V, c_off, c_ref;
+    int64_t RV, buf0, buf1, status, xs, ys;
     int64_t total, grammar_bytes, scratch_bytes, staging_bytes;
     int64_t value_bytes;   // bytes of one node value (k_max elements)
-    int64_t leaf_bytes;    // bytes of one leaf value
+    int64_t n_nodes_padded;
+    int32_t vbits;         // bits of the value index inside a leaf code
 };
 
 inline int64_t policy_elem_bytes(gc_policy p) { return p == GC_F32_SUM ? 4 : 8; }
 
 inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
+inline int64_t pad_nodes(int64_t w) { return (w + kNodeAlign - 1) / kNodeAlign * kNodeAlign; }
+
+inline int32_t value_bits(int64_t n_values) {
+    int32_t b = 0;
+    while (((int64_t)1 << b) < n_values) ++b;
+    return b;
+}
+
 inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     DevLayout d{};
-    const int64_t N = g.n_nodes(), L = g.L, A = g.alpha(), C = (int64_t)g.c_ref.size();
+    const int64_t L = g.L, C = (int64_t)g.c_ref.size();
     d.value_bytes = policy_elem_bytes(p) * k_max;
-    d.leaf_bytes = p == GC_BOOL_OR ? 0 : policy_elem_bytes(p);
+    d.vbits = value_bits((int64_t)g.V.size());
+    d.n_nodes_padded = 0;
+    for (int64_t k = 1; k <= L; ++k) d.n_nodes_padded += pad_nodes(g.lvl_off[k + 1] - g.lvl_off[k]);
     int64_t o = 0;
     auto take = [&](int64_t bytes) {
         int64_t at = o;
         o = align256(o + bytes);
         return at;
     };
-    d.nodes = take(8 * N);
-    d.lvl_off = take(8 * (L + 2));
-    d.lvl_roots = take(8 * (L + 2));
-    d.root_off = take(8 * (L + 2));
-    d.leaf_col = take(4 * A);
-    d.leaf_val = take(d.leaf_bytes * A);
+    d.nodes = take(8 * d.n_nodes_padded);
+    d.levels = take(8 * 4 * (L + 2));
+    d.V = take(policy_elem_bytes(p) * std::max<int64_t>(1, (int64_t)g.V.size()));
     d.c_off = take(4 * (g.n + 1));
     d.c_ref = take(4 * C);
     d.grammar_bytes = o;
-    d.T = take(d.value_bytes * (A + 1));
     d.RV = take(d.value_bytes * g.n_roots);
     const int64_t w = g.max_width();
     d.buf0 = take(d.value_bytes * w);
@@ -81,6 +96,8 @@ inline void check_policy(const Grammar& g, gc_policy p, int32_t k_max) {
         for (float v : g.V)
             if (v != 1.0f) fail(GC_ERR_UNSUPPORTED, "GC_BOOL_OR needs every stored entry to be 1");
     if ((int64_t)g.c_ref.size() >= INT32_MAX) fail(GC_ERR_UNSUPPORTED, "|C| >= 2^31");
+    if ((((int64_t)g.m) << value_bits((int64_t)g.V.size())) + 2 > INT32_MAX)
+        fail(GC_ERR_UNSUPPORTED, "columns x distinct values too large for 31-bit leaf codes");
 }
 
 }  // namespace gcs

@@ -8,8 +8,9 @@
 //          (Appendix A batched product; 64 B per node, four float4 lanes)
 //   I64   (+, x) exact int64                            V = int64,  LPN = 1
 //   OR    (OR, AND) on 64 sources per uint64 word       V = uint64, LPN = 1
-// The leaf map is T[p] = V[l_p] (x) x[j_p]; the combine identity fills T[0]
-// (0 for sums, all-zero bits for OR: the semiring zero, Sec. 5).
+// The leaf map is V[l] (x) x[j] for the terminal <l, j>, evaluated where the
+// sweep reads the terminal; the combine identity (0 for sums, all-zero bits
+// for OR: the semiring zero, Sec. 5) stands in for a missing child.
 #pragma once
 
 #include <cstdint>
@@ -22,8 +23,10 @@ struct PolF32 {
     using Leaf = float;
     static constexpr int LPN = 1;
     __device__ __forceinline__ static V identity() { return 0.0f; }
-    __device__ __forceinline__ static V combine(V a, V b) { return a + b; }
-    __device__ __forceinline__ static V leaf(const Leaf* lv, int64_t p, V x) { return lv[p] * x; }
+    // explicitly rounded: no FMA contraction, so every kernel that evaluates
+    // the same node gets the same bits
+    __device__ __forceinline__ static V combine(V a, V b) { return __fadd_rn(a, b); }
+    __device__ __forceinline__ static V leaf(Leaf v, V x) { return __fmul_rn(v, x); }
 };
 
 struct PolF32x16 {
@@ -32,11 +35,10 @@ struct PolF32x16 {
     static constexpr int LPN = 4;
     __device__ __forceinline__ static V identity() { return make_float4(0.f, 0.f, 0.f, 0.f); }
     __device__ __forceinline__ static V combine(V a, V b) {
-        return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
     }
-    __device__ __forceinline__ static V leaf(const Leaf* lv, int64_t p, V x) {
-        float s = lv[p];
-        return make_float4(s * x.x, s * x.y, s * x.z, s * x.w);
+    __device__ __forceinline__ static V leaf(Leaf s, V x) {
+        return make_float4(__fmul_rn(s, x.x), __fmul_rn(s, x.y), __fmul_rn(s, x.z), __fmul_rn(s, x.w));
     }
 };
 
@@ -46,16 +48,16 @@ struct PolI64 {
     static constexpr int LPN = 1;
     __device__ __forceinline__ static V identity() { return 0; }
     __device__ __forceinline__ static V combine(V a, V b) { return a + b; }
-    __device__ __forceinline__ static V leaf(const Leaf* lv, int64_t p, V x) { return lv[p] * x; }
+    __device__ __forceinline__ static V leaf(Leaf v, V x) { return v * x; }
 };
 
 struct PolOr {
     using V = unsigned long long;
-    using Leaf = unsigned long long;   // unused: every stored entry is 1
+    using Leaf = unsigned long long;   // every stored entry is 1: AND with all-ones
     static constexpr int LPN = 1;
     __device__ __forceinline__ static V identity() { return 0ull; }
     __device__ __forceinline__ static V combine(V a, V b) { return a | b; }
-    __device__ __forceinline__ static V leaf(const Leaf*, int64_t, V x) { return x; }
+    __device__ __forceinline__ static V leaf(Leaf, V x) { return x; }
 };
 
 }  // namespace gcs

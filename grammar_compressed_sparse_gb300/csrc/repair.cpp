@@ -5,19 +5,26 @@
 // precedes its parent (the topological numbering of Eq. 2.3).
 //
 // Data structures (after Larsson and Moffat's linear-time RePair):
-//   seq/nxt/prv      the working sequence with links over live positions;
-//                    a row end is a DELIM position, a replaced right symbol
-//                    becomes EMPTY and is unlinked
-//   pid[i]           id of the pair that starts at live position i (or -1)
-//   onext/oprev      each pair's occurrences, threaded through positions
-//   pair records     (a, b, freq, first occurrence, bucket links)
-//   buckets          frequency buckets 2..B plus one unsorted list above B
+//   Pos[i]     one record per position of the working sequence: its symbol
+//              (a row end is DELIM, a replaced right symbol EMPTY), links to
+//              the neighbouring live positions, the id of the pair starting
+//              here, and this occurrence's links in that pair's list
+//   Pair[id]   (a, b, frequency, first occurrence, queue links)
+//   queues     FIFO per frequency 2..B plus one list above B
 // Because a row never holds the same symbol twice (its symbols cover disjoint
 // column ranges), occurrences never overlap. Every pair created while
 // replacing (a, b) by N contains N, so new pairs are found through two small
 // per-round maps keyed by the neighbour symbol; no global pair hash is needed
-// after the initial count, and decrements go through pid[].
+// after the initial count, and decrements go through Pos[i].pid.
+//
+// The main loop is bound by memory latency, so each record fits one cache
+// line and a round first collects the pair's occurrences, then walks them
+// with a three-stage software prefetch (the position; its neighbours; their
+// list neighbours and pair records).
+#include <sys/mman.h>
+
 #include <cstring>
+#include <memory>
 #include <numeric>
 
 #include "common.hpp"
@@ -31,6 +38,52 @@ namespace {
 
 constexpr int32_t DELIM = -1;
 constexpr int32_t EMPTY = -2;
+
+struct Pos {
+    int32_t seq, nxt, prv, pid, onext, oprev;
+};
+struct alignas(32) PairRec {
+    int32_t a, b, freq, head, qp, qn, qb, pad;
+};
+
+template <class T>
+inline void prefetch(const T* p) {
+    __builtin_prefetch(p, 1, 3);
+}
+
+// Fixed-capacity array in anonymous memory, backed by transparent huge pages
+// where the kernel allows it: the random accesses of the main loop would
+// otherwise miss the TLB on almost every step. Pages are zero until touched.
+template <class T>
+class HugeArray {
+public:
+    HugeArray() = default;
+    explicit HugeArray(size_t n) { reset(n); }
+    HugeArray(const HugeArray&) = delete;
+    HugeArray& operator=(const HugeArray&) = delete;
+    ~HugeArray() { release(); }
+    void reset(size_t n) {
+        release();
+        bytes_ = std::max<size_t>(n * sizeof(T), 1);
+        void* p = mmap(nullptr, bytes_, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+        if (p == MAP_FAILED) throw std::bad_alloc();
+        madvise(p, bytes_, MADV_HUGEPAGE);
+        p_ = static_cast<T*>(p);
+        cap_ = n;
+    }
+    T* get() const { return p_; }
+    T& operator[](size_t i) const { return p_[i]; }
+    size_t capacity() const { return cap_; }
+
+private:
+    void release() {
+        if (p_) munmap(p_, bytes_);
+        p_ = nullptr;
+        cap_ = 0;
+    }
+    T* p_ = nullptr;
+    size_t bytes_ = 0, cap_ = 0;
+};
 
 // int32 -> int32 map cleared in O(1) by a generation stamp.
 struct StampMap {
@@ -51,7 +104,7 @@ struct StampMap {
             gen = 1;
         }
     }
-    // returns slot; found tells whether the key was present
+    // slot of key k; found tells whether it is present
     size_t slot(int32_t k, bool& found) {
         size_t p = ((uint32_t)k * 0x9E3779B1u) & mask;
         while (stamp[p] == gen) {
@@ -81,23 +134,27 @@ public:
                  "a RePair block holds more than 2^31-2 symbols; compress in row blocks (block_rows)");
         ns_ = (int32_t)ns;
         rows_ = r1 - r0;
-        seq_.resize(ns_);
+        S_.reset((size_t)ns_ + 1);
+        // ids are recycled, so records in use never exceed all ever created:
+        // the initial pairs (<= ns) plus two per replacement (<= 2 ns)
+        P_.reset(3 * (size_t)ns_ + 2);
         row_start_.resize((size_t)rows_);
         int64_t p = 0;
         for (int64_t r = r0; r < r1; ++r) {
             row_start_[r - r0] = (int32_t)p;
-            for (int64_t e = s.row_off[r]; e < s.row_off[r + 1]; ++e) seq_[p++] = s.sym[e];
-            seq_[p++] = DELIM;
+            for (int64_t e = s.row_off[r]; e < s.row_off[r + 1]; ++e) S_[p++].seq = s.sym[e];
+            S_[p++].seq = DELIM;
         }
-        nxt_.resize(ns_);
-        prv_.resize(ns_);
+        Pos* S = S_.get();
+#pragma omp parallel for schedule(static)
         for (int32_t i = 0; i < ns_; ++i) {
-            nxt_[i] = i + 1;
-            prv_[i] = i - 1;
+            S[i].nxt = i + 1;
+            S[i].prv = i - 1;
+            S[i].pid = -1;
+            S[i].onext = -1;
+            S[i].oprev = -1;
         }
-        pid_.assign(ns_, -1);
-        onext_.assign(ns_, -1);
-        oprev_.assign(ns_, -1);
+        S[ns_] = Pos{DELIM, ns_, ns_ - 1, -1, -1, -1};   // sentinel read by prefetches
         int64_t b = 2;
         while (b * b < ns) ++b;
         B_ = (int32_t)std::max<int64_t>(b, 2);
@@ -109,10 +166,11 @@ public:
     Slp run() {
         count_initial_pairs();
         for (;;) {
-            int32_t p = pop_max();
+            const int32_t p = pop_max();
             if (p < 0) break;
             replace(p);
         }
+        const Pos* S = S_.get();
         Slp out;
         out.rule_a.resize(ra_.size());
         out.rule_b.resize(rb_.size());
@@ -123,13 +181,13 @@ public:
         out.c_off.assign((size_t)rows_ + 1, 0);
         for (int64_t r = 0; r < rows_; ++r) {
             int64_t c = 0;
-            for (int32_t q = row_start_[r]; seq_[q] != DELIM; q = nxt_[q]) ++c;
+            for (int32_t q = row_start_[r]; S[q].seq != DELIM; q = S[q].nxt) ++c;
             out.c_off[r + 1] = out.c_off[r] + c;
         }
         out.c_sym.resize((size_t)out.c_off[rows_]);
         for (int64_t r = 0; r < rows_; ++r) {
             int64_t o = out.c_off[r];
-            for (int32_t q = row_start_[r]; seq_[q] != DELIM; q = nxt_[q]) out.c_sym[o++] = to_export(seq_[q]);
+            for (int32_t q = row_start_[r]; S[q].seq != DELIM; q = S[q].nxt) out.c_sym[o++] = to_export(S[q].seq);
         }
         return out;
     }
@@ -138,15 +196,15 @@ private:
     int32_t alpha_;
     int32_t ns_ = 0;
     int64_t rows_ = 0;
-    std::vector<int32_t> seq_, nxt_, prv_, pid_, onext_, oprev_, row_start_;
-    // pair records
-    std::vector<int32_t> pa_, pb_, pf_, ph_, qp_, qn_, free_;
-    // buckets
+    HugeArray<Pos> S_;
+    std::vector<int32_t> row_start_;
+    HugeArray<PairRec> P_;
+    int32_t np_ = 0;   // pair records in use
+    std::vector<int32_t> free_;
     int32_t B_ = 2, maxb_ = 0;
-    std::vector<int32_t> bucket_, btail_, qb_;
-    std::vector<int32_t> fresh_;   // pairs created in the current round
-    // rules in internal symbols
-    std::vector<int32_t> ra_, rb_;
+    std::vector<int32_t> bucket_, btail_;
+    std::vector<int32_t> fresh_, occ_;
+    std::vector<int32_t> ra_, rb_;   // rules in internal symbols
     StampMap lmap_, rmap_;
 
     int32_t to_export(int32_t s) const { return s < alpha_ ? -(s + 1) : s - alpha_; }
@@ -156,102 +214,89 @@ private:
         if (!free_.empty()) {
             id = free_.back();
             free_.pop_back();
-            pa_[id] = a;
-            pb_[id] = b;
-            pf_[id] = 0;
-            ph_[id] = -1;
-            qp_[id] = qn_[id] = -1;
-            qb_[id] = -1;
         } else {
-            if (pa_.size() >= (size_t)INT32_MAX) fail(GC_ERR_UNSUPPORTED, "too many pairs");
-            id = (int32_t)pa_.size();
-            pa_.push_back(a);
-            pb_.push_back(b);
-            pf_.push_back(0);
-            ph_.push_back(-1);
-            qp_.push_back(-1);
-            qn_.push_back(-1);
-            qb_.push_back(-1);
+            if ((size_t)np_ >= P_.capacity()) fail(GC_ERR_UNSUPPORTED, "pair table full");
+            id = np_++;
         }
+        P_[id] = PairRec{a, b, 0, -1, -1, -1, -1, 0};
         fresh_.push_back(id);
         return id;
     }
 
     // ---- occurrence lists
     void occ_push(int32_t id, int32_t pos) {
-        int32_t h = ph_[id];
-        onext_[pos] = h;
-        oprev_[pos] = -1;
-        if (h >= 0) oprev_[h] = pos;
-        ph_[id] = pos;
+        Pos* S = S_.get();
+        const int32_t h = P_[id].head;
+        S[pos].onext = h;
+        S[pos].oprev = -1;
+        if (h >= 0) S[h].oprev = pos;
+        P_[id].head = pos;
     }
     void occ_remove(int32_t id, int32_t pos) {
-        int32_t a = oprev_[pos], b = onext_[pos];
-        if (a >= 0) onext_[a] = b; else ph_[id] = b;
-        if (b >= 0) oprev_[b] = a;
-        onext_[pos] = oprev_[pos] = -1;
+        Pos* S = S_.get();
+        const int32_t a = S[pos].oprev, b = S[pos].onext;
+        if (a >= 0) S[a].onext = b; else P_[id].head = b;
+        if (b >= 0) S[b].oprev = a;
     }
 
-    // ---- frequency buckets: FIFO queues per frequency 2..B, one list above B.
+    // ---- frequency queues: FIFO per frequency 2..B, one list above B.
     // Ties between equally frequent pairs go to the oldest pair (the pages
     // leave the tie-break open). Older pairs hold shallower symbols, so over a
     // repeated segment this pairs neighbours level by level and keeps the
     // grammar's depth near log2 of the segment length; a newest-first order
     // instead grows left-deep chains.
-    // Decrements are lazy: a pair stays in the bucket it was filed in (which
+    // Decrements are lazy: a pair stays in the queue it was filed in (which
     // is then >= its frequency) and is re-filed when it reaches the front.
     // Increments only ever happen to the pairs created in the current round
     // (they all contain the new symbol); those are filed once, after it.
     int32_t list_of(int32_t f) const { return f > B_ ? B_ + 1 : f; }
     void pq_insert(int32_t id) {
-        const int32_t l = list_of(pf_[id]);
+        PairRec& r = P_[id];
+        const int32_t l = list_of(r.freq);
         const int32_t t = btail_[l];
-        qp_[id] = t;
-        qn_[id] = -1;
-        if (t >= 0) qn_[t] = id; else bucket_[l] = id;
+        r.qp = t;
+        r.qn = -1;
+        if (t >= 0) P_[t].qn = id; else bucket_[l] = id;
         btail_[l] = id;
-        qb_[id] = l;
+        r.qb = l;
         if (l <= B_ && l > maxb_) maxb_ = l;
     }
     void pq_unlink(int32_t id) {
-        const int32_t l = qb_[id];
-        const int32_t a = qp_[id], b = qn_[id];
-        if (a >= 0) qn_[a] = b; else bucket_[l] = b;
-        if (b >= 0) qp_[b] = a; else btail_[l] = a;
-        qp_[id] = qn_[id] = -1;
-        qb_[id] = -1;
+        PairRec& r = P_[id];
+        const int32_t l = r.qb;
+        if (r.qp >= 0) P_[r.qp].qn = r.qn; else bucket_[l] = r.qn;
+        if (r.qn >= 0) P_[r.qn].qp = r.qp; else btail_[l] = r.qp;
+        r.qp = r.qn = -1;
+        r.qb = -1;
     }
-    // Takes id out of the queue; returns true if it is still a candidate.
+    // Takes id out of its queue; true if it is still a candidate (freq >= 2).
     bool settle(int32_t id) {
         pq_unlink(id);
-        if (pf_[id] >= 2) return true;
-        if (pf_[id] == 0) free_.push_back(id);
+        if (P_[id].freq >= 2) return true;
+        if (P_[id].freq == 0) free_.push_back(id);
         return false;
     }
     int32_t pop_max() {
         // above B: exact maximum by scan, re-filing entries that fell to <= B
-        for (;;) {
-            int32_t best = -1;
-            for (int32_t q = bucket_[B_ + 1]; q >= 0;) {
-                const int32_t nx = qn_[q];
-                if (pf_[q] <= B_) {
-                    if (settle(q)) pq_insert(q);
-                } else if (best < 0 || pf_[q] > pf_[best]) {
-                    best = q;
-                }
-                q = nx;
+        int32_t best = -1;
+        for (int32_t q = bucket_[B_ + 1]; q >= 0;) {
+            const int32_t nx = P_[q].qn;
+            if (P_[q].freq <= B_) {
+                if (settle(q)) pq_insert(q);
+            } else if (best < 0 || P_[q].freq > P_[best].freq) {
+                best = q;
             }
-            if (best >= 0) {
-                pq_unlink(best);
-                return best;
-            }
-            break;
+            q = nx;
+        }
+        if (best >= 0) {
+            pq_unlink(best);
+            return best;
         }
         for (;;) {
             while (maxb_ >= 2 && bucket_[maxb_] < 0) --maxb_;
             if (maxb_ < 2) return -1;
             const int32_t id = bucket_[maxb_];
-            if (pf_[id] == maxb_) {
+            if (P_[id].freq == maxb_) {
                 pq_unlink(id);
                 return id;
             }
@@ -260,25 +305,26 @@ private:
     }
     void inc(int32_t id, int32_t pos) {   // only pairs created in this round
         occ_push(id, pos);
-        ++pf_[id];
+        ++P_[id].freq;
     }
     void dec(int32_t id, int32_t pos) {
         occ_remove(id, pos);
-        if (--pf_[id] == 0 && qb_[id] < 0) free_.push_back(id);
+        if (--P_[id].freq == 0 && P_[id].qb < 0) free_.push_back(id);
     }
 
     // Initial digram count, grouped by left symbol (parallel over groups).
     void count_initial_pairs() {
+        Pos* S = S_.get();
         const int32_t A = alpha_;
         std::vector<int64_t> cnt((size_t)A + 1, 0);
         for (int32_t i = 0; i + 1 < ns_; ++i)
-            if (seq_[i] >= 0 && seq_[i + 1] >= 0) ++cnt[seq_[i] + 1];
+            if (S[i].seq >= 0 && S[i + 1].seq >= 0) ++cnt[S[i].seq + 1];
         for (int32_t a = 0; a < A; ++a) cnt[a + 1] += cnt[a];
-        std::vector<int32_t> grp((size_t)cnt[A]);
+        std::unique_ptr<int32_t[]> grp(new int32_t[(size_t)cnt[A] + 1]);
         {
             std::vector<int64_t> w(cnt.begin(), cnt.end() - 1);
             for (int32_t i = 0; i + 1 < ns_; ++i)
-                if (seq_[i] >= 0 && seq_[i + 1] >= 0) grp[w[seq_[i]]++] = i;
+                if (S[i].seq >= 0 && S[i + 1].seq >= 0) grp[w[S[i].seq]++] = i;
         }
         // distinct right symbols per group -> local pair ids
         std::vector<int32_t> ndist((size_t)A + 1, 0);
@@ -293,97 +339,129 @@ private:
                 int32_t d = 0;
                 for (int64_t q = g0; q < g1; ++q) {
                     const int32_t pos = grp[q];
-                    const int32_t bsym = seq_[pos + 1];
+                    const int32_t bsym = S[pos + 1].seq;
                     bool f;
-                    size_t s = m.slot(bsym, f);
-                    if (!f) m.put(s, bsym, d++);
-                    pid_[pos] = m.val[s];
+                    const size_t sl = m.slot(bsym, f);
+                    if (!f) m.put(sl, bsym, d++);
+                    S[pos].pid = m.val[sl];
                 }
                 ndist[a + 1] = d;
             }
         }
         for (int32_t a = 0; a < A; ++a) ndist[a + 1] += ndist[a];
         const int32_t np = ndist[A];
-        pa_.resize(np);
-        pb_.resize(np);
-        pf_.assign(np, 0);
-        ph_.assign(np, -1);
-        qp_.assign(np, -1);
-        qn_.assign(np, -1);
-        qb_.assign(np, -1);
+        np_ = np;
+#pragma omp parallel for schedule(static)
+        for (int32_t id = 0; id < np; ++id) P_[id] = PairRec{0, 0, 0, -1, -1, -1, -1, 0};
         // global ids, records, occurrence lists (each group owns its positions)
 #pragma omp parallel for schedule(dynamic, 256)
         for (int32_t a = 0; a < A; ++a) {
             for (int64_t q = cnt[a]; q < cnt[a + 1]; ++q) {
-                int32_t pos = grp[q];
-                int32_t id = ndist[a] + pid_[pos];
-                pid_[pos] = id;
-                pa_[id] = a;
-                pb_[id] = seq_[pos + 1];
-                ++pf_[id];
-                int32_t h = ph_[id];
-                onext_[pos] = h;
-                if (h >= 0) oprev_[h] = pos;
-                ph_[id] = pos;
+                const int32_t pos = grp[q];
+                const int32_t id = ndist[a] + S[pos].pid;
+                S[pos].pid = id;
+                PairRec& r = P_[id];
+                r.a = a;
+                r.b = S[pos + 1].seq;
+                ++r.freq;
+                const int32_t h = r.head;
+                S[pos].onext = h;
+                if (h >= 0) S[h].oprev = pos;
+                r.head = pos;
             }
         }
         for (int32_t id = 0; id < np; ++id)
-            if (pf_[id] >= 2) pq_insert(id);
+            if (P_[id].freq >= 2) pq_insert(id);
     }
 
     void replace(int32_t p) {
-        const int32_t a = pa_[p], b = pb_[p];
+        Pos* S = S_.get();
+        const int32_t a = P_[p].a, b = P_[p].b;
         if ((int64_t)alpha_ + (int64_t)ra_.size() >= INT32_MAX)
             fail(GC_ERR_UNSUPPORTED, "more than 2^31-1 symbols");
         const int32_t N = alpha_ + (int32_t)ra_.size();
         ra_.push_back(a);
         rb_.push_back(b);
-        lmap_.prepare((size_t)pf_[p]);
-        rmap_.prepare((size_t)pf_[p]);
+        // Every occurrence of p is consumed this round, so its list is only
+        // read (the positions are re-threaded into new lists as they go).
+        occ_.clear();
+        for (int32_t q = P_[p].head; q >= 0; q = S[q].onext) occ_.push_back(q);
+        P_[p].head = -1;
+        lmap_.prepare(occ_.size());
+        rmap_.prepare(occ_.size());
         fresh_.clear();
-        while (ph_[p] >= 0) {
-            const int32_t i = ph_[p];
-            occ_remove(p, i);
-            const int32_t j = nxt_[i];
-            if (j >= ns_ || seq_[i] != a || seq_[j] != b) continue;   // cannot happen; defensive
-            const int32_t xp = prv_[i];
-            const int32_t yp = nxt_[j];
-            const bool hx = xp >= 0 && seq_[xp] >= 0;
-            const bool hy = yp < ns_ && seq_[yp] >= 0;
-            if (hx) dec(pid_[xp], xp);
-            if (hy) dec(pid_[j], j);
-            seq_[i] = N;
-            seq_[j] = EMPTY;
-            pid_[j] = -1;
-            nxt_[i] = yp;
-            if (yp < ns_) prv_[yp] = i;
+        const int64_t K = (int64_t)occ_.size();
+        constexpr int64_t D = 6;
+        for (int64_t t = 0; t < K; ++t) {
+            if (t + 3 * D < K) prefetch(&S[occ_[t + 3 * D]]);
+            if (t + 2 * D < K) {
+                const Pos& s2 = S[occ_[t + 2 * D]];
+                if (s2.prv >= 0) prefetch(&S[s2.prv]);
+                prefetch(&S[s2.nxt]);
+            }
+            if (t + D < K) {
+                const Pos& s1 = S[occ_[t + D]];
+                if (s1.prv >= 0) {
+                    const Pos& sx = S[s1.prv];
+                    if (sx.onext >= 0) prefetch(&S[sx.onext]);
+                    if (sx.oprev >= 0) prefetch(&S[sx.oprev]);
+                    if (sx.pid >= 0) prefetch(&P_[sx.pid]);
+                }
+                const Pos& sj = S[s1.nxt];
+                if (sj.onext >= 0) prefetch(&S[sj.onext]);
+                if (sj.oprev >= 0) prefetch(&S[sj.oprev]);
+                if (sj.pid >= 0) prefetch(&P_[sj.pid]);
+                if (sj.nxt < ns_) prefetch(&S[sj.nxt]);
+            }
+            const int32_t i = occ_[t];
+            const int32_t j = S[i].nxt;
+            if (j >= ns_ || S[i].seq != a || S[j].seq != b) continue;   // cannot happen; defensive
+            const int32_t xp = S[i].prv;
+            const int32_t yp = S[j].nxt;
+            const bool hx = xp >= 0 && S[xp].seq >= 0;
+            const bool hy = yp < ns_ && S[yp].seq >= 0;
+            if (hx) dec(S[xp].pid, xp);
+            if (hy) dec(S[j].pid, j);
+            S[i].seq = N;
+            S[j].seq = EMPTY;
+            S[j].pid = -1;
+            S[i].nxt = yp;
+            if (yp < ns_) S[yp].prv = i;
             if (hx) {
-                const int32_t x = seq_[xp];
+                const int32_t x = S[xp].seq;
                 bool f;
-                size_t s = lmap_.slot(x, f);
+                const size_t sl = lmap_.slot(x, f);
                 int32_t id;
-                if (f) id = lmap_.val[s];
-                else { id = new_pair(x, N); lmap_.put(s, x, id); }
-                pid_[xp] = id;
+                if (f) {
+                    id = lmap_.val[sl];
+                } else {
+                    id = new_pair(x, N);
+                    lmap_.put(sl, x, id);
+                }
+                S[xp].pid = id;
                 inc(id, xp);
             }
             if (hy) {
-                const int32_t y = seq_[yp];
+                const int32_t y = S[yp].seq;
                 bool f;
-                size_t s = rmap_.slot(y, f);
+                const size_t sl = rmap_.slot(y, f);
                 int32_t id;
-                if (f) id = rmap_.val[s];
-                else { id = new_pair(N, y); rmap_.put(s, y, id); }
-                pid_[i] = id;
+                if (f) {
+                    id = rmap_.val[sl];
+                } else {
+                    id = new_pair(N, y);
+                    rmap_.put(sl, y, id);
+                }
+                S[i].pid = id;
                 inc(id, i);
             } else {
-                pid_[i] = -1;
+                S[i].pid = -1;
             }
         }
-        pf_[p] = 0;
+        P_[p].freq = 0;
         free_.push_back(p);
         for (int32_t id : fresh_)
-            if (pf_[id] >= 2) pq_insert(id);
+            if (P_[id].freq >= 2) pq_insert(id);
         fresh_.clear();
     }
 };

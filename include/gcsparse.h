@@ -214,20 +214,47 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
  *   x0, x    device uint64_t[n]; bit b of x[i] ends set iff node i reaches a
  *            node whose bit b is set in x0. x may equal x0 (in place).
  *   iters    device int32_t[1]: products performed, the last of which changed
- *            nothing; -1 if max_iter was reached first (gc_check then returns
- *            GC_ERR_NOT_CONVERGED).
+ *            nothing; -1 if max_iter was reached first.
+ * Returns GC_ERR_NOT_CONVERGED (and records it in the status word, which
+ * gc_check reports once) if max_iter products did not reach the fixpoint.
  * Synchronises the stream once per product to read the changed flag.
  */
 gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
                    int32_t* iters, void* stream);
 
 /* Synchronise the stream and return the device status word of the handle
- * (GC_OK, GC_ERR_TIMEOUT, GC_ERR_NOT_CONVERGED, GC_ERR_INVALID_GRAMMAR).
- * The word is cleared after it is read.                                     */
+ * (GC_OK, GC_ERR_TIMEOUT, GC_ERR_NOT_CONVERGED). The word is cleared after it
+ * is read. While a GC_ERR_TIMEOUT is unread, products are skipped (y is not
+ * written): a timed-out grid barrier leaves its counter part-way, and
+ * gc_check restarts it.                                                     */
 gc_status gc_check(gc_handle* h, void* stream);
 
 /* Number of kernel launches the most recent gc_matvec on h enqueued.        */
 gc_status gc_launch_count(const gc_handle* h, int64_t* launches);
+
+/* Schedules of the sweep (the same values either way, bit for bit):
+ *   GC_SCHED_PERSISTENT  one cooperative kernel per product, levels separated
+ *                        by a grid barrier with bounded waits (default; used
+ *                        when the device supports cooperative launch)
+ *   GC_SCHED_PER_LEVEL   one kernel per level plus one emit kernel, the
+ *                        launch sequence of Listing 1 of the pages          */
+enum { GC_SCHED_PERSISTENT = 0, GC_SCHED_PER_LEVEL = 1 };
+gc_status gc_set_schedule(gc_handle* h, int32_t schedule);
+/* The schedule products actually use (PER_LEVEL when cooperative launch is
+ * unavailable).                                                             */
+gc_status gc_get_schedule(const gc_handle* h, int32_t* schedule);
+
+/*
+ * gc_debug_inject -- failure injection for tests; never faults the GPU.
+ *   what 0: normal operation. what 1: in the next persistent products, CTA 0
+ *   skips its first grid-barrier arrival, so every other CTA's bounded wait
+ *   runs out after timeout_cycles SM clock cycles; the kernel then sets the
+ *   status word to GC_ERR_TIMEOUT and returns. gc_check reports it, clears
+ *   it and resets the barrier state; products are skipped (y left unwritten)
+ *   while a failure is unread.
+ * timeout_cycles also sets the wait limit for what 0 (default 4e9 cycles).
+ */
+gc_status gc_debug_inject(gc_handle* h, int32_t what, int64_t timeout_cycles);
 
 /* Serialise / restore a built grammar (host file, little-endian, versioned). */
 gc_status gc_save(const gc_grammar* g, const char* path);

@@ -57,14 +57,16 @@ def matvec_or(row_ptr, col, x):
 
     Every stored entry is a true edge, so the leaf map is the identity on x
     and y[i] = OR over j in row i of x[j]; an empty row gives the OR-identity 0.
+    (numpy's OR-reduction over each row's slice of x[col], so that graphs with
+    10^8 edges finish in seconds.)
     """
     x = np.asarray(x, dtype=np.uint64)
+    row_ptr = np.asarray(row_ptr, dtype=np.int64)
     n = len(row_ptr) - 1
     y = np.zeros(n, dtype=np.uint64)
-    for i in range(n):
-        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
-        if e > s:
-            y[i] = np.bitwise_or.reduce(x[np.asarray(col[s:e], dtype=np.int64)])
+    nonempty = row_ptr[1:] > row_ptr[:-1]
+    if nonempty.any():
+        y[nonempty] = np.bitwise_or.reduceat(x[np.asarray(col, dtype=np.int64)], row_ptr[:-1][nonempty])
     return y
 
 

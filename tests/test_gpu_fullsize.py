@@ -1,0 +1,85 @@
+"""Full-size parity, in the launch configuration bench.py times.
+
+* 10,000 x 50,000 genotype matrix (2.3e8 non-zeros, one grammar): every row of
+  y = G beta against the float64 oracle, persistent schedule; a 16-wide product.
+* 2,000,000-node copy-model graph (about 2e8 edges): the Boolean product and the
+  reachability fixpoint from 64 sources, bit for bit against the oracle.
+
+Grammars are built once per session (RePair takes a minute or two of host
+time) and reused through the grammar cache when present.
+"""
+import numpy as np
+import pytest
+
+import gcsynth
+from oracle import direct, reach
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return t
+
+
+@pytest.fixture(scope="module")
+def medium(gcs):
+    gen = gcsynth.GENO_MEDIUM
+    rp, c, v = gcsynth.genotype_csr(**gen)
+    G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: (gen["n"], gen["m"], rp, c, v))
+    return gen, rp, c, v, G
+
+
+def test_medium_single_vector_all_rows(gcs, torch, medium):
+    gen, rp, c, v, G = medium
+    st = G.stats()
+    assert st["nnz"] == rp[-1] and st["depth"] >= 10
+    eng = gcs.Engine(G, "f32", 1)
+    assert eng.schedule == "persistent"
+    for seed in (0, 99):
+        x = gcsynth.beta(gen["m"], seed=seed)
+        y = eng.matvec(torch.from_numpy(x).cuda()).cpu().numpy()
+        assert eng.check() == 0
+        y_ref, b = direct.matvec_f64(rp, c, v, x)
+        ok, worst = direct.within_tolerance(y, y_ref, b, TOL)
+        assert ok, f"seed {seed}: max scaled error {worst:.3e}"
+    # footprint below the CSR of the same matrix
+    lay = G.layout("f32", 1)
+    assert lay["grammar_bytes"] + lay["scratch_bytes"] < lay["csr_bytes"]
+
+
+def test_medium_sixteen_vectors(gcs, torch, medium):
+    gen, rp, c, v, G = medium
+    eng = gcs.Engine(G, "f32", 16)
+    X = gcsynth.beta(gen["m"], seed=0, k=16)
+    Y = eng.matvec(torch.from_numpy(X).cuda()).cpu().numpy()
+    rows = np.arange(0, gen["n"], 7)              # every 7th row, all 16 columns
+    for r in rows[:600]:
+        s, e = rp[r], rp[r + 1]
+        ref = np.asarray(v[s:e], np.float64) @ X[c[s:e]].astype(np.float64)
+        bnd = np.abs(np.asarray(v[s:e], np.float64)) @ np.abs(X[c[s:e]].astype(np.float64))
+        assert np.all(np.abs(Y[r] - ref) <= TOL * bnd)
+
+
+def test_graph_fixpoint(gcs, torch):
+    gp = gcsynth.GRAPH
+    rp, col = gcsynth.copy_model_graph(**gp)
+    N = gp["nodes"]
+    G = gcs.cached_grammar(f"graph:{sorted(gp.items())}", lambda: (N, N, rp, col, None))
+    st = G.stats()
+    assert st["nnz"] == len(col) > 1.5e8
+    eng = gcs.Engine(G, "or", 1)
+    x = np.random.default_rng(0).integers(0, 2**63, N, dtype=np.uint64)
+    y = eng.matvec(torch.from_numpy(x.view(np.int64)).cuda()).cpu().numpy().view(np.uint64)
+    np.testing.assert_array_equal(y, direct.matvec_or(rp, col, x))
+    x0 = gcsynth.frontier(N, gcsynth.sources(N, gp["sources"], gp["seed"]))
+    xs, iters, rc = eng.reach(torch.from_numpy(x0.view(np.int64)).cuda())
+    assert rc == 0
+    want, want_iters = reach.fixpoint(rp, col, x0)
+    assert iters == want_iters
+    np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint64), want)

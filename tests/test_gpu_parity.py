@@ -186,3 +186,52 @@ def test_argument_errors(gcs, torch):
         gcs.capi.gc_upload(G._p, "f32", 1, arena.data_ptr() + 16, arena.numel() - 16)
     with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
         gcs.capi.gc_upload(G._p, "f32", 1, arena, 1024)
+
+
+def test_schedules_agree_bit_for_bit(gcs, torch):
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    G = gcs.Grammar(300, cfg["m"], rp, c, v)
+    eng = gcs.Engine(G, "f32", 16)
+    assert eng.schedule == "persistent"          # cooperative launch on this GPU
+    x = _dev(torch, gcsynth.beta(cfg["m"], seed=3))
+    y_p = eng.matvec(x).cpu().numpy()
+    assert eng.launch_count() == 1
+    X = _dev(torch, gcsynth.beta(cfg["m"], seed=4, k=16))
+    Y_p = eng.matvec(X).cpu().numpy()
+    eng.schedule = "per_level"
+    assert eng.schedule == "per_level"
+    y_l = eng.matvec(x).cpu().numpy()
+    assert eng.launch_count() == G.stats()["depth"] + 1
+    Y_l = eng.matvec(X).cpu().numpy()
+    np.testing.assert_array_equal(y_p, y_l)
+    np.testing.assert_array_equal(Y_p, Y_l)
+    assert_f32_parity(y_p, rp, c, v, gcsynth.beta(cfg["m"], seed=3))
+
+
+def test_barrier_timeout_is_reported_not_hung(gcs, torch):
+    # CTA 0 skips its first barrier arrival; every other CTA's bounded wait
+    # runs out (about a millisecond), the kernel returns with GC_ERR_TIMEOUT
+    cfg = dict(gcsynth.GENO_MEDIUM, n=200)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    G = gcs.Grammar(200, cfg["m"], rp, c, v)
+    eng = gcs.Engine(G, "f32", 1)
+    x = _dev(torch, gcsynth.beta(cfg["m"], seed=5))
+    y_ok = eng.matvec(x).cpu().numpy()
+    gcs.capi.gc_debug_inject(eng._h, 1, 2_000_000)
+    y = torch.full((200,), float("nan"), device="cuda")
+    eng.matvec(x, y)
+    torch.cuda.synchronize()
+    assert eng.check() == gcs.capi.GC_ERR_TIMEOUT
+    assert eng.check() == 0
+    # while a timeout is unread, products are skipped
+    gcs.capi.gc_debug_inject(eng._h, 1, 2_000_000)
+    eng.matvec(x, y)
+    y2 = torch.full((200,), float("nan"), device="cuda")
+    gcs.capi.gc_debug_inject(eng._h, 0, 4_000_000_000)
+    eng.matvec(x, y2)
+    assert torch.isnan(y2).all()
+    assert eng.check() == gcs.capi.GC_ERR_TIMEOUT
+    # after the check the same handle computes correctly again
+    np.testing.assert_array_equal(eng.matvec(x).cpu().numpy(), y_ok)
+    assert eng.check() == 0
