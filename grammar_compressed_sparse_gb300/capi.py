@@ -77,6 +77,7 @@ _sig = {
     "gc_upload": ([_vp, ctypes.c_int, _i32, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_matvec": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
     "gc_matvec_host": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
+    "gc_matvec_static": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
     "gc_reach": ([_vp, _vp, _vp, _i32, _vp, _vp], ctypes.c_int),
     "gc_check": ([_vp, _vp], ctypes.c_int),
     "gc_launch_count": ([_vp, ctypes.POINTER(_i64)], ctypes.c_int),
@@ -180,6 +181,13 @@ def gc_matvec(h, x, y, k=1, stream=None):
 
 def gc_matvec_host(h, x, y, k=1, stream=None):
     _check(_lib.gc_matvec_host(h, _addr(x), _addr(y), k, _stream(stream)), "gc_matvec_host")
+
+
+def gc_matvec_static(h, x, y, k=1, stream=None):
+    _check(_lib.gc_matvec_static(h, _addr(x), _addr(y), k, _stream(stream)), "gc_matvec_static")
+
+
+GC_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def gc_reach(h, x0, x, max_iter, iters, stream=None) -> int:

@@ -34,6 +34,7 @@
 
 #include <cstring>
 #include <memory>
+#include <mutex>
 
 #include "common.hpp"
 #include "layout.hpp"
@@ -644,6 +645,86 @@ void put(cudaStream_t st, char* arena, int64_t off, const T* p, size_t count) {
     cuda_check(cudaMemcpyAsync(arena + off, p, count * sizeof(T), cudaMemcpyHostToDevice, st), "upload copy");
 }
 
+// ---------------------------------------------------------------- fixed scratch
+// Scratch for gc_matvec_static: callers that cannot allocate device memory at
+// the point of the call still get a product. Every GPU that loads the library
+// holds this array until the process exits; every call shares it.
+constexpr int64_t kStaticScratchBytes = GC_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch per device, looked up once with that
+// device current (the host-side name is only a stand-in for it).
+constexpr int kMaxDevices = 64;
+static unsigned char* g_static_ptr[kMaxDevices] = {};
+static std::mutex g_static_mu;
+
+unsigned char* static_scratch_on_current_device() {
+    int dev = 0;
+    cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) fail(GC_ERR_UNSUPPORTED, "device index beyond the fixed-scratch table");
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        cuda_check(cudaGetSymbolAddress(&p, g_static_scratch), "cudaGetSymbolAddress(fixed scratch)");
+        g_static_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+    return g_static_ptr[dev];
+}
+
+// Bytes of fixed scratch a product with k right-hand sides needs: status
+// block, root values, two level buffers (same parts as the arena's scratch).
+int64_t static_scratch_need(const gc_handle* h, int32_t k) {
+    const int64_t vb = policy_elem_bytes(h->policy) * k;
+    return 256 + align256(vb * h->n_roots) + 2 * align256(vb * h->max_width);
+}
+
+// One product whose scratch is the fixed array: the same kernels and order of
+// evaluation as run_product, with RV, the level buffers, the status word and
+// the barrier counter pointed into g_static_scratch.
+template <class P>
+void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, unsigned char* scratch) {
+    using V = typename P::V;
+    SweepArgs<P> a = make_args<P>(h, x, y);
+    const int64_t vb = (int64_t)sizeof(V) * P::LPN;
+    a.status = reinterpret_cast<int32_t*>(scratch);
+    a.bar = reinterpret_cast<unsigned long long*>(scratch + 64);
+    a.bar_base = 0;
+    a.rv = reinterpret_cast<V*>(scratch + 256);
+    a.buf0 = reinterpret_cast<V*>(scratch + 256 + align256(vb * h->n_roots));
+    a.buf1 = reinterpret_cast<V*>(scratch + 256 + align256(vb * h->n_roots) + align256(vb * h->max_width));
+    a.inject = 0;
+    // the array keeps the previous call's contents: start from a clear status
+    // word and barrier counter
+    cuda_check(cudaMemsetAsync(scratch, 0, 256, st), "fixed scratch clear");
+    int64_t launches = 0;
+    int grid = 0;
+    if (h->schedule == 0 && h->coop) grid = sweep_grid<P>(h);
+    if (grid > 0) {
+        const size_t smem = (size_t)kStages * Tile<P>::NODES * sizeof(int2);
+        void* args[] = {&a};
+        cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P>, dim3(grid), dim3(kSweepThreads), args,
+                                               smem, st),
+                   "sweep launch");
+        launches = 1;
+    } else {
+        a.grid_levels = (int32_t)h->L;
+        for (int k = 1; k <= h->L; ++k) {
+            const int64_t w = h->lv[LV_W * (h->L + 2) + k];
+            if (w == 0) continue;
+            level_kernel<P><<<grid_for(w * P::LPN, kLevelThreads * kNodesPerThread, h->sms), kLevelThreads, 0, st>>>(
+                a, k);
+            ++launches;
+        }
+        if (h->n > 0) {
+            const int64_t rows_per_block = h->emit_group == 0 ? 1 : (kSweepThreads / 32) * (32 / h->emit_group);
+            emit_kernel<P><<<grid_for(h->n, (int)rows_per_block, h->sms, 8), kSweepThreads, 0, st>>>(a);
+            ++launches;
+        }
+    }
+    cuda_check(cudaGetLastError(), "kernel launch");
+    h->launches = launches;
+}
+
 // device leaf code of terminal p: -((col << vbits | vidx) + 2)
 inline int32_t leaf_ref(const Grammar& g, int32_t p, int32_t vbits) {
     const int64_t q = ((int64_t)g.term_col[p] << vbits) | g.term_vidx[p];
@@ -871,6 +952,37 @@ gc_status gc_debug_inject(gc_handle* h, int32_t what, int64_t timeout_cycles) {
         h->inject = what;
         h->timeout_cycles = timeout_cycles;
     });
+}
+
+gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void* stream) {
+    gc_status rc = GC_OK;
+    gc_status g = guard([&] {
+        if (!h) fail(GC_ERR_ARG, "null handle");
+        if ((!x && h->m > 0) || (!y && h->n > 0)) fail(GC_ERR_ARG, "null x or y");
+        check_k(h, k);
+        const int64_t need = static_scratch_need(h, k);
+        if (need > kStaticScratchBytes)
+            fail(GC_ERR_UNSUPPORTED, "gc_matvec_static: this grammar needs " + std::to_string(need) +
+                                         " bytes of scratch; the fixed array holds " +
+                                         std::to_string(kStaticScratchBytes));
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        unsigned char* scratch = static_scratch_on_current_device();
+        switch (h->policy) {
+            case GC_F32_SUM:
+                if (k == 1) run_product_static<PolF32>(h, x, y, st, scratch);
+                else run_product_static<PolF32x16>(h, x, y, st, scratch);
+                break;
+            case GC_I64_SUM: run_product_static<PolI64>(h, x, y, st, scratch); break;
+            case GC_BOOL_OR: run_product_static<PolOr>(h, x, y, st, scratch); break;
+        }
+        int32_t s = 0;
+        cuda_check(cudaMemcpyAsync(&s, scratch, 4, cudaMemcpyDeviceToHost, st), "fixed scratch status read");
+        cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+        rc = (gc_status)s;
+    });
+    if (g != GC_OK) return g;
+    if (rc != GC_OK) set_last_error("gc_matvec_static: a device-side wait ran out");
+    return rc;
 }
 
 void gc_free_handle(gc_handle* h) { delete h; }

@@ -256,6 +256,33 @@ gc_status gc_get_schedule(const gc_handle* h, int32_t* schedule);
  */
 gc_status gc_debug_inject(gc_handle* h, int32_t what, int64_t timeout_cycles);
 
+/*
+ * gc_matvec_static -- y = M x without any device memory for scratch.
+ * The pages have no counterpart; this is a library convenience. It serves
+ * callers that cannot call cudaMalloc (or any allocator) where the product
+ * runs: a process whose device memory is fully reserved up front, or code
+ * that only receives input and output buffers. The product's scratch -- the
+ * root values, the two level buffers, the status word and the grid-barrier
+ * counter -- lives in one fixed array compiled into the library, of
+ * GC_STATIC_SCRATCH_BYTES bytes, that every GPU which loads the library holds
+ * until the process exits. The handle's grammar (gc_upload) and x are the
+ * inputs, y the output, as for gc_matvec; the handle's own scratch is unused.
+ *   Size limit: a product needs 256 + RV + 2 level buffers bytes (rho and w*
+ *   values of k elements each, each part rounded up to 256 bytes); a larger
+ *   request returns GC_ERR_UNSUPPORTED with the sizes in gc_last_error().
+ *   Set-up: the first call on a device, with that device current, looks up
+ *   the array's device address (cudaGetSymbolAddress) once; make that first
+ *   call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents; the call clears the status word and barrier counter itself.
+ *   Calls that overlap on the GPU (other streams, other threads) race on it.
+ *   Allocation: no cudaMalloc, cudaFree or allocating library routine.
+ *   Returns after the product completed (it synchronises the stream), with
+ *   GC_ERR_TIMEOUT if a device-side wait ran out.
+ */
+#define GC_STATIC_SCRATCH_BYTES (32ll << 20)
+gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void* stream);
+
 /* Serialise / restore a built grammar (host file, little-endian, versioned). */
 gc_status gc_save(const gc_grammar* g, const char* path);
 gc_status gc_load(const char* path, gc_grammar** out);
