@@ -2,34 +2,35 @@
 // arena, and the streaming bottom-up sweep of Sec. 4.3 of the pages ("Right
 // Multiplication on Grammar-Compressed Matrices"), written for sm_103a.
 //
-//   level combine   for k = 1..L: cur[t] = cv(a_t) (+) cv(b_t), where
-//                   cv(c) = prev[c] for c >= 0, the identity for c = -1, and
-//                   the leaf V[l] (x) x[j] for a terminal <l, j>; the level's
-//                   roots (its first nodes) are also written to RV, the
-//                   emit-on-the-spot capture (Listing 1, Lemma 3.3)
-//   row emit        y[r] = (+) over row r's symbols of RV[c] or the leaf value
-//                   (Lemma 2.2; a row of C may hold several symbols and bare
-//                   terminals)
+//   leaf table      T[0] = identity, T[p+1] = V[l_p] (x) x[j_p]          (Sec. 4.3)
+//   level combine   for k = 1..L: cur[t] = cv(a_t) (+) cv(b_t) with one load
+//                   per child from the previous level's buffer, which has T
+//                   in front (see layout.hpp); the level's roots (its first
+//                   nodes) are also written to RV, the emit-on-the-spot
+//                   capture                                  (Listing 1, Lemma 3.3)
+//   row emit        y[r] = (+) over row r's symbols of RV / T entries   (Lemma 2.2)
 //
-// Differences from the pages' design, for this GPU:
-//   * one persistent cooperative kernel per product instead of two launches
-//     per level; levels are separated by a grid barrier whose waits are
-//     bounded (a wait that runs out sets the status word and the kernel
-//     returns);
-//   * each CTA streams its tiles of child pairs from HBM into shared memory
-//     with cp.async.bulk (an mbarrier-tracked, three-stage pipeline with an
-//     L2 evict-first hint) and keeps issuing across level barriers, since the
-//     pairs do not depend on values; the child values are gathered from the
-//     L2-resident level buffers, eight nodes per thread with all loads issued
-//     first;
-//   * leaves are evaluated where they are read (the pages' own future-work
-//     item, Sec. 7 item 3), so there is no terminal array and no leaf phase;
+// Schedule (differences from the pages' two launches per level, for this GPU):
+//   * one persistent cooperative kernel per product, two CTAs of 512 threads
+//     per SM; levels are separated by a grid barrier whose waits are bounded
+//     (a wait that runs out sets the status word and the kernel returns);
+//   * within a level every warp works on its own chunks of 128 nodes
+//     (4 per lane, coalesced), with no block-wide synchronisation, and loads
+//     the next chunk's child pairs -- possibly of the next level, since pairs
+//     do not depend on values -- before gathering the current chunk's
+//     children, so node-stream latency hides behind gathers and barriers;
+//   * level 1 evaluates its (all-terminal) children in the sweep while the
+//     grid writes the three T copies, so T costs no phase of its own;
+//   * child values are gathered through L1/L2 (the grid barrier's gpu-scope
+//     acquire orders them after the writers); root values are stored with an
+//     L2 evict-last policy so the emit finds them in L2; the node and C
+//     streams are loaded evict-first;
 //   * the narrow top levels run on one CTA with block-level barriers;
 //   * the pages emit with atomicAdd into y; here each row is reduced by a
 //     fixed group of threads in a fixed order: deterministic, no atomics.
-// A second schedule launches one kernel per level plus one emit kernel; it
-// computes every value with the same device functions (bit-identical y) and
-// serves as the reference point for the persistent one.
+// A second schedule launches one kernel per level plus one emit kernel with
+// the same device functions (bit-identical y): the launch sequence of
+// Listing 1, kept as the reference point for the persistent one.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -43,7 +44,7 @@
 struct gc_handle {
     gc_policy policy = GC_F32_SUM;
     int32_t k_max = 1;
-    int64_t n = 0, m = 0, L = 0, n_roots = 0, c_len = 0, max_width = 0;
+    int64_t n = 0, m = 0, L = 0, n_roots = 0, c_len = 0, max_width = 0, alpha = 0;
     std::vector<int64_t> lv;      // host copy of the level table, 4 (L+2)
     char* arena = nullptr;
     gcs::DevLayout lay{};
@@ -61,10 +62,9 @@ struct gc_handle {
 namespace gcs {
 namespace {
 
-constexpr int kSweepThreads = 512;   // persistent kernel: one CTA of 512 per SM
-constexpr int kLevelThreads = 256;   // per-level schedule
-constexpr int kStages = 3;
-constexpr int kNodesPerThread = 8;
+constexpr int kThreads = 512;        // every kernel: 16 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kU = 4;                // nodes (or node lanes) per thread per chunk
 constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3;
 
 void cuda_check(cudaError_t e, const char* what) {
@@ -72,49 +72,14 @@ void cuda_check(cudaError_t e, const char* what) {
 }
 
 template <class P>
-struct Tile {
-    static constexpr int NODES = kSweepThreads * kNodesPerThread / P::LPN;   // nodes per bulk copy
+struct Chunk {
+    static constexpr int NPW = 32 / P::LPN;          // nodes per warp row
+    static constexpr int NODES = NPW * kU;           // nodes per warp chunk
+    static constexpr int TAIL = NODES * kWarps * 2;  // widest level left to one CTA
 };
 
 // ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ uint64_t l2_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-// global -> shared bulk copy (16-byte aligned, size a multiple of 16)
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-        : "memory");
-}
-__device__ __forceinline__ void atom_add_release(unsigned long long* p, unsigned long long v) {
+__device__ __forceinline__ void red_add_release(unsigned long long* p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
@@ -124,16 +89,26 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
 }
 __device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
 
-// L2-only loads / stores for values written during the kernel (L1 is not
-// coherent across SMs)
-__device__ __forceinline__ float ldv(const float* p) { return __ldcg(p); }
-__device__ __forceinline__ float4 ldv(const float4* p) { return __ldcg(p); }
-__device__ __forceinline__ long long ldv(const long long* p) { return __ldcg(p); }
-__device__ __forceinline__ unsigned long long ldv(const unsigned long long* p) { return __ldcg(p); }
-__device__ __forceinline__ void stv(float* p, float v) { __stcg(p, v); }
-__device__ __forceinline__ void stv(float4* p, float4 v) { __stcg(p, v); }
-__device__ __forceinline__ void stv(long long* p, long long v) { __stcg(p, v); }
-__device__ __forceinline__ void stv(unsigned long long* p, unsigned long long v) { __stcg(p, v); }
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// stores that ask L2 to keep the line (root values, read again by the emit)
+__device__ __forceinline__ void st_keep(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep(float4* p, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void st_keep(long long* p, long long v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_keep(unsigned long long* p, unsigned long long v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(pol) : "memory");
+}
 
 __device__ __forceinline__ float shfl_x(float v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
 __device__ __forceinline__ long long shfl_x(long long v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
@@ -151,13 +126,16 @@ struct SweepArgs {
     const int2* nodes;
     const int64_t* lv;        // level table: 4 rows of L+2
     int32_t L, L2, grid_levels;
+    int64_t TB;               // leaf-table block length (values)
+    int64_t alpha;
     const typename P::Leaf* Vd;
+    const int32_t* leaf;      // leaf code per terminal
     int32_t vbits;
     const V* x;
     V* y;
-    V* buf0;
+    V* buf0;                  // [T | level values]
     V* buf1;
-    V* rv;
+    V* rv;                    // [T | root values]
     const int32_t* c_off;
     const int32_t* c_ref;
     int64_t n;
@@ -171,72 +149,95 @@ struct SweepArgs {
     __device__ __forceinline__ int64_t lvl(int row, int k) const { return __ldg(lv + (int64_t)row * L2 + k); }
 };
 
-// value of child reference c (lane `lane` of the node value)
+// V[l] (x) x[j] for a leaf code (column << vbits | value index)
 template <class P>
-__device__ __forceinline__ typename P::V child(int32_t c, int lane, const typename P::V* prev,
-                                               const SweepArgs<P>& a) {
-    if (c >= 0) return ldv(prev + (int64_t)c * P::LPN + lane);
-    if (c == -1) return P::identity();
-    const uint32_t q = (uint32_t)(-(c + 2));
+__device__ __forceinline__ typename P::V leaf_value(int32_t code, int part, const SweepArgs<P>& a) {
+    const uint32_t q = (uint32_t)code;
     const uint32_t col = q >> a.vbits, vi = q & ((1u << a.vbits) - 1u);
-    return P::leaf(__ldg(a.Vd + vi), __ldg(a.x + (int64_t)col * P::LPN + lane));
+    return P::leaf(__ldg(a.Vd + vi), __ldg(a.x + (int64_t)col * P::LPN + part));
 }
 
-// Combine cnt nodes (pairs at src, from shared memory or, with kGlobal,
-// streamed from global) into cur[base ..], capturing roots into rv.
-template <class P, int NT, bool kGlobal>
-__device__ __forceinline__ void combine_block(const int2* src, int32_t cnt, int64_t base, int64_t nroots,
-                                              const typename P::V* prev, typename P::V* cur, typename P::V* rv,
-                                              const SweepArgs<P>& a) {
+// The three leaf-table copies (in front of buf0, buf1 and RV), grid-stride.
+template <class P>
+__device__ void write_leaf_tables(const SweepArgs<P>& a, int64_t tid, int64_t nthreads) {
     using V = typename P::V;
-    constexpr int NPP = NT / P::LPN;
-    constexpr int U = kNodesPerThread;
-    const int lane = threadIdx.x % P::LPN;
-    const int sub = threadIdx.x / P::LPN;
-    int2 ab[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int i = u * NPP + sub;
-        ab[u] = i < cnt ? (kGlobal ? __ldcs(src + i) : src[i]) : make_int2(-1, -1);
+    const int64_t total = (a.alpha + 1) * P::LPN;
+    for (int64_t i = tid; i < total; i += nthreads) {
+        const int64_t p = i / P::LPN;
+        const int part = (int)(i % P::LPN);
+        const V v = p == 0 ? P::identity() : leaf_value<P>(__ldg(a.leaf + (p - 1)), part, a);
+        a.buf0[i] = v;
+        a.buf1[i] = v;
+        a.rv[i] = v;
     }
-    V va[U], vb[U];
+}
+
+// Loads the child pairs of chunk c of level k (this warp's lanes).
+template <class P>
+__device__ __forceinline__ void load_chunk(const SweepArgs<P>& a, int k, int64_t c, int2 (&ab)[kU]) {
+    constexpr int NPW = Chunk<P>::NPW;
+    const int lane = threadIdx.x & 31;
+    const int64_t w = a.lvl(LV_W, k);
+    const int2* src = a.nodes + a.lvl(LV_START, k);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        va[u] = child<P>(ab[u].x, lane, prev, a);
-        vb[u] = child<P>(ab[u].y, lane, prev, a);
+    for (int u = 0; u < kU; ++u) {
+        const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
+        ab[u] = node < w ? __ldcs(src + node) : make_int2(0, 0);
+    }
+}
+
+// Combines chunk c of level k from its prefetched child pairs.
+template <class P>
+__device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int64_t c, const int2 (&ab)[kU],
+                                              uint64_t keep) {
+    using V = typename P::V;
+    constexpr int NPW = Chunk<P>::NPW;
+    const int lane = threadIdx.x & 31;
+    const int part = lane % P::LPN;
+    const int64_t w = a.lvl(LV_W, k), nroots = a.lvl(LV_ROOTS, k);
+    const V* prev = (k & 1) ? a.buf0 : a.buf1;
+    V* cur = ((k & 1) ? a.buf1 : a.buf0) + a.TB * P::LPN;
+    V* rv = a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN;
+    V va[kU], vb[kU];
+    if (k == 1) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
+            va[u] = node < w ? leaf_value<P>(ab[u].x, part, a) : P::identity();
+            vb[u] = node < w ? leaf_value<P>(ab[u].y, part, a) : P::identity();
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            va[u] = prev[(int64_t)ab[u].x * P::LPN + part];
+            vb[u] = prev[(int64_t)ab[u].y * P::LPN + part];
+        }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int i = u * NPP + sub;
-        if (i < cnt) {
+    for (int u = 0; u < kU; ++u) {
+        const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
+        if (node < w) {
             const V v = P::combine(va[u], vb[u]);
-            const int64_t g = base + i;
-            stv(cur + g * P::LPN + lane, v);
-            if (g < nroots) stv(rv + g * P::LPN + lane, v);
+            cur[node * P::LPN + part] = v;
+            if (node < nroots) st_keep(rv + node * P::LPN + part, v, keep);
         }
     }
 }
 
 // ---------------------------------------------------------------- row emit
-template <class P>
-__device__ __forceinline__ typename P::V emit_value(int32_t c, int lane, const SweepArgs<P>& a) {
-    if (c >= 0) return ldv(a.rv + (int64_t)c * P::LPN + lane);
-    return child<P>(c, lane, nullptr, a);   // leaf (or identity for -1)
-}
-
 constexpr int kEmitBatch = 4;
 
 // G threads per row (G divides 32); warps walk rows in lockstep so the
 // shuffles always see the full warp. Thread gl sums its symbols q = s+gl,
 // s+gl+G, ... in order, then the group reduces by a fixed butterfly.
-template <class P, int NT, int G>
+template <class P, int G>
 __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     using V = typename P::V;
     constexpr int RPW = 32 / G;
     const int lane = threadIdx.x & 31;
     const int gl = lane % G;
-    const int64_t warp = block * (NT / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = nblocks * (NT / 32);
+    const int64_t warp = block * kWarps + (threadIdx.x >> 5);
+    const int64_t nwarps = nblocks * kWarps;
     for (int64_t base = warp * RPW; base < a.n; base += nwarps * RPW) {
         const int64_t row = base + lane / G;
         V acc[P::LPN];
@@ -247,12 +248,12 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
             for (int32_t q0 = s + gl; q0 < e; q0 += G * kEmitBatch) {
                 int32_t c[kEmitBatch];
 #pragma unroll
-                for (int u = 0; u < kEmitBatch; ++u) c[u] = q0 + u * G < e ? __ldcs(a.c_ref + q0 + u * G) : -1;
+                for (int u = 0; u < kEmitBatch; ++u) c[u] = q0 + u * G < e ? __ldcs(a.c_ref + q0 + u * G) : 0;
                 V v[kEmitBatch][P::LPN];
 #pragma unroll
                 for (int u = 0; u < kEmitBatch; ++u)
 #pragma unroll
-                    for (int l = 0; l < P::LPN; ++l) v[u][l] = emit_value<P>(c[u], l, a);
+                    for (int l = 0; l < P::LPN; ++l) v[u][l] = a.rv[(int64_t)c[u] * P::LPN + l];
 #pragma unroll
                 for (int u = 0; u < kEmitBatch; ++u)
 #pragma unroll
@@ -270,25 +271,25 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
 }
 
 // One CTA per row, for long rows of C.
-template <class P, int NT>
+template <class P>
 __device__ void emit_ctas(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     using V = typename P::V;
-    __shared__ V red[NT / 32][P::LPN];
+    __shared__ V red[kWarps][P::LPN];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int64_t row = block; row < a.n; row += nblocks) {
         V acc[P::LPN];
 #pragma unroll
         for (int l = 0; l < P::LPN; ++l) acc[l] = P::identity();
         const int32_t s = __ldg(a.c_off + row), e = __ldg(a.c_off + row + 1);
-        for (int32_t q0 = s + threadIdx.x; q0 < e; q0 += NT * kEmitBatch) {
+        for (int32_t q0 = s + threadIdx.x; q0 < e; q0 += kThreads * kEmitBatch) {
             int32_t c[kEmitBatch];
 #pragma unroll
-            for (int u = 0; u < kEmitBatch; ++u) c[u] = q0 + u * NT < e ? __ldcs(a.c_ref + q0 + u * NT) : -1;
+            for (int u = 0; u < kEmitBatch; ++u) c[u] = q0 + u * kThreads < e ? __ldcs(a.c_ref + q0 + u * kThreads) : 0;
             V v[kEmitBatch][P::LPN];
 #pragma unroll
             for (int u = 0; u < kEmitBatch; ++u)
 #pragma unroll
-                for (int l = 0; l < P::LPN; ++l) v[u][l] = emit_value<P>(c[u], l, a);
+                for (int l = 0; l < P::LPN; ++l) v[u][l] = a.rv[(int64_t)c[u] * P::LPN + l];
 #pragma unroll
             for (int u = 0; u < kEmitBatch; ++u)
 #pragma unroll
@@ -304,31 +305,32 @@ __device__ void emit_ctas(const SweepArgs<P>& a, int64_t block, int64_t nblocks)
         __syncthreads();
         if (threadIdx.x < P::LPN) {
             V t = red[0][threadIdx.x];
-            for (int w = 1; w < NT / 32; ++w) t = P::combine(t, red[w][threadIdx.x]);
+            for (int w = 1; w < kWarps; ++w) t = P::combine(t, red[w][threadIdx.x]);
             a.y[row * P::LPN + threadIdx.x] = t;
         }
         __syncthreads();
     }
 }
 
-template <class P, int NT>
+template <class P>
 __device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     switch (a.emit_group) {
-        case 0: emit_ctas<P, NT>(a, block, nblocks); break;
-        case 1: emit_groups<P, NT, 1>(a, block, nblocks); break;
-        case 2: emit_groups<P, NT, 2>(a, block, nblocks); break;
-        case 4: emit_groups<P, NT, 4>(a, block, nblocks); break;
-        case 8: emit_groups<P, NT, 8>(a, block, nblocks); break;
-        case 16: emit_groups<P, NT, 16>(a, block, nblocks); break;
-        default: emit_groups<P, NT, 32>(a, block, nblocks); break;
+        case 0: emit_ctas<P>(a, block, nblocks); break;
+        case 1: emit_groups<P, 1>(a, block, nblocks); break;
+        case 2: emit_groups<P, 2>(a, block, nblocks); break;
+        case 4: emit_groups<P, 4>(a, block, nblocks); break;
+        case 8: emit_groups<P, 8>(a, block, nblocks); break;
+        case 16: emit_groups<P, 16>(a, block, nblocks); break;
+        default: emit_groups<P, 32>(a, block, nblocks); break;
     }
 }
 
-// ---------------------------------------------------------------- waits
-// Grid barrier: arrival counter that only grows; barrier j of this launch
-// completes when it reaches (bar_base + j + 1) * gridDim.x. A wait gives up
-// after a.timeout cycles (or when another CTA already reported a failure),
-// sets the status word and returns false.
+// ---------------------------------------------------------------- grid barrier
+// Arrival counter that only grows; barrier j of this launch completes when it
+// reaches (bar_base + j + 1) * gridDim.x. A wait gives up after a.timeout
+// cycles (or when another CTA already reported a timeout), sets the status
+// word and returns false. The acquire at gpu scope, followed by the block
+// barrier, orders every thread's later loads after the other CTAs' writes.
 template <class P>
 __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
     __shared__ int s_ok;
@@ -338,7 +340,7 @@ __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
         const bool skip = a.inject == 1 && blockIdx.x == 0 && j == 0;   // test-only
         if (!skip) {
             __threadfence();
-            atom_add_release(a.bar, 1ull);
+            red_add_release(a.bar, 1ull);
         }
         const unsigned long long target = (a.bar_base + j + 1) * (unsigned long long)gridDim.x;
         const long long t0 = clock64();
@@ -364,165 +366,90 @@ __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
     return s_ok != 0;
 }
 
-// Bounded wait for a bulk copy to land; false (status set) if it does not.
-template <class P>
-__device__ bool stage_wait(const SweepArgs<P>& a, uint64_t* bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > a.timeout) {
-            atomicCAS(a.status, 0, (int32_t)GC_ERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
 // ---------------------------------------------------------------- persistent sweep
 template <class P>
-__global__ void __launch_bounds__(kSweepThreads, 1) sweep_kernel(const SweepArgs<P> a) {
-    using V = typename P::V;
-    constexpr int TILE = Tile<P>::NODES;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    int2* stage = reinterpret_cast<int2*>(smem_raw);
-    __shared__ __align__(8) uint64_t bars[kStages];
-    __shared__ int s_ok;
-
+__global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a) {
     // an unread earlier timeout left the barrier counter part-way: do nothing
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
-    const int64_t G = gridDim.x, b = blockIdx.x;
     const int Lg = a.grid_levels;
-    auto ntiles = [&](int k) { return (a.lvl(LV_W, k) + TILE - 1) / TILE; };
-    // (level, tile) iterators over this CTA's tiles b, b+G, ... of levels 1..Lg
-    auto norm = [&](int& k, int64_t& t) {
-        while (k <= Lg && t >= ntiles(k)) {
+    const int64_t GW = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const uint64_t keep = l2_evict_last();
+    auto nchunks = [&](int k) { return (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES; };
+    auto norm = [&](int& k, int64_t& c) {
+        while (k <= Lg && c >= nchunks(k)) {
             ++k;
-            t = b;
+            c = gw;
         }
     };
-    const uint64_t pol = l2_evict_first();
-    auto issue = [&](int k, int64_t t, int s) {
-        const int64_t node0 = t * TILE;
-        const int64_t cnt = min((int64_t)TILE, a.lvl(LV_W, k) - node0);
-        const uint32_t bytes = (uint32_t)(((cnt + kNodeAlign - 1) / kNodeAlign) * kNodeAlign * 8);
-        mbar_expect_tx(&bars[s], bytes);
-        bulk_g2s(stage + (int64_t)s * TILE, a.nodes + a.lvl(LV_START, k) + node0, bytes, &bars[s], pol);
-    };
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
+    write_leaf_tables<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
 
-    int pk = 1, ck = 1;
-    int64_t pt = b, ct = b;
-    norm(pk, pt);
-    norm(ck, ct);
-    int inflight = 0;   // meaningful in thread 0
-    if (threadIdx.x == 0)
-        for (int s = 0; s < kStages && pk <= Lg; ++s) {
-            issue(pk, pt, s);
-            ++inflight;
-            pt += G;
-            norm(pk, pt);
-        }
-    uint32_t parity = 0;
-    int slot = 0;
+    int kn = 1;
+    int64_t cn = gw;
+    norm(kn, cn);
+    int2 nab[kU];
+    if (kn <= Lg) load_chunk<P>(a, kn, cn, nab);
     unsigned long long nbar = 0;
-    bool ok = true;
-
-    for (int k = 1; k <= Lg && ok; ++k) {
-        if (k > 1 && !(ok = grid_sync(a, nbar++))) break;
-        const V* prev = (k & 1) ? a.buf0 : a.buf1;
-        V* cur = (k & 1) ? a.buf1 : a.buf0;
-        const int64_t w = a.lvl(LV_W, k), nroots = a.lvl(LV_ROOTS, k);
-        V* rv = a.rv + a.lvl(LV_ROFF, k) * P::LPN;
-        while (ck == k) {
-            const int got = stage_wait(a, &bars[slot], (parity >> slot) & 1u);
-            if (!__syncthreads_and(got)) {
-                ok = false;
-                break;
-            }
-            parity ^= 1u << slot;
-            const int64_t node0 = ct * TILE;
-            combine_block<P, kSweepThreads, false>(stage + (int64_t)slot * TILE, (int32_t)min((int64_t)TILE, w - node0),
-                                                   node0, nroots, prev, cur, rv, a);
-            __syncthreads();   // every thread is done with this stage
-            if (threadIdx.x == 0) {
-                --inflight;
-                if (pk <= Lg) {
-                    issue(pk, pt, slot);
-                    ++inflight;
-                    pt += G;
-                    norm(pk, pt);
-                }
-            }
-            ct += G;
-            norm(ck, ct);
-            slot = slot + 1 == kStages ? 0 : slot + 1;
+    for (int k = 1; k <= Lg; ++k) {
+        if (k > 1 && !grid_sync(a, nbar++)) return;
+        while (kn == k) {
+            int2 ab[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) ab[u] = nab[u];
+            const int64_t c = cn;
+            cn += GW;
+            norm(kn, cn);
+            if (kn <= Lg) load_chunk<P>(a, kn, cn, nab);   // next chunk, maybe of a later level
+            combine_chunk<P>(a, k, c, ab, keep);
         }
     }
-
-    if (!ok) {
-        // leave no bulk copy writing into shared memory after the CTA exits
-        if (threadIdx.x == 0) {
-            for (int i = 0, s = slot; i < inflight; ++i, s = s + 1 == kStages ? 0 : s + 1) {
-                const long long t0 = clock64();
-                while (!mbar_try_wait(&bars[s], (parity >> s) & 1u) && clock64() - t0 < a.timeout) {
-                }
-                parity ^= 1u << s;
-            }
-        }
-        __syncthreads();
-        return;
-    }
-
     // narrow top levels: CTA 0 alone, block barriers only
     if (Lg < a.L) {
         if (!grid_sync(a, nbar++)) return;
-        if (b == 0) {
-            constexpr int CH = kSweepThreads * kNodesPerThread / P::LPN;
+        if (blockIdx.x == 0) {
+            const int w0 = threadIdx.x >> 5;
             for (int k = Lg + 1; k <= a.L; ++k) {
-                const V* prev = (k & 1) ? a.buf0 : a.buf1;
-                V* cur = (k & 1) ? a.buf1 : a.buf0;
-                const int64_t w = a.lvl(LV_W, k), nroots = a.lvl(LV_ROOTS, k);
-                const int2* src = a.nodes + a.lvl(LV_START, k);
-                V* rv = a.rv + a.lvl(LV_ROFF, k) * P::LPN;
-                for (int64_t c0 = 0; c0 < w; c0 += CH)
-                    combine_block<P, kSweepThreads, true>(src + c0, (int32_t)min((int64_t)CH, w - c0), c0, nroots,
-                                                          prev, cur, rv, a);
+                for (int64_t c = w0; c < nchunks(k); c += kWarps) {
+                    int2 ab[kU];
+                    load_chunk<P>(a, k, c, ab);
+                    combine_chunk<P>(a, k, c, ab, keep);
+                }
                 __syncthreads();
             }
         }
     }
     if (!grid_sync(a, nbar++)) return;
-    emit_rows<P, kSweepThreads>(a, b, G);
-    (void)s_ok;
+    emit_rows<P>(a, blockIdx.x, gridDim.x);
 }
 
 // ---------------------------------------------------------------- per-level schedule
 template <class P>
-__global__ void __launch_bounds__(kLevelThreads) level_kernel(const SweepArgs<P> a, int k) {
-    constexpr int CH = kLevelThreads * kNodesPerThread / P::LPN;
-    const typename P::V* prev = (k & 1) ? a.buf0 : a.buf1;
-    typename P::V* cur = (k & 1) ? a.buf1 : a.buf0;
-    const int64_t w = a.lvl(LV_W, k), nroots = a.lvl(LV_ROOTS, k);
-    const int2* src = a.nodes + a.lvl(LV_START, k);
-    typename P::V* rv = a.rv + a.lvl(LV_ROFF, k) * P::LPN;
-    for (int64_t c0 = (int64_t)blockIdx.x * CH; c0 < w; c0 += (int64_t)gridDim.x * CH)
-        combine_block<P, kLevelThreads, true>(src + c0, (int32_t)min((int64_t)CH, w - c0), c0, nroots, prev, cur, rv,
-                                              a);
+__global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a, int k) {
+    const int64_t GW = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const uint64_t keep = l2_evict_last();
+    if (k <= 1) write_leaf_tables<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    if (k < 1) return;
+    const int64_t nc = (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES;
+    int2 nab[kU];
+    if (gw < nc) load_chunk<P>(a, k, gw, nab);
+    for (int64_t c = gw; c < nc; c += GW) {
+        int2 ab[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) ab[u] = nab[u];
+        if (c + GW < nc) load_chunk<P>(a, k, c + GW, nab);
+        combine_chunk<P>(a, k, c, ab, keep);
+    }
 }
 
-// Same block size as the persistent kernel, so both schedules reduce every
-// row in the same order.
 template <class P>
-__global__ void __launch_bounds__(kSweepThreads) emit_kernel(const SweepArgs<P> a) {
-    emit_rows<P, kSweepThreads>(a, blockIdx.x, gridDim.x);
+__global__ void __launch_bounds__(kThreads, 2) emit_kernel(const SweepArgs<P> a) {
+    emit_rows<P>(a, blockIdx.x, gridDim.x);
 }
 
 // x |= y elementwise; sets *changed if any word changed (Boolean fixpoint step).
-__global__ void __launch_bounds__(kLevelThreads)
+__global__ void __launch_bounds__(kThreads)
 or_update_kernel(unsigned long long* __restrict__ x, const unsigned long long* __restrict__ y, int64_t n,
                  int32_t* __restrict__ changed) {
     int ch = 0;
@@ -537,8 +464,8 @@ or_update_kernel(unsigned long long* __restrict__ x, const unsigned long long* _
 }
 
 // ---------------------------------------------------------------- host side
-int grid_for(int64_t items, int threads, int sms, int per_sm = 8) {
-    int64_t g = (items + threads - 1) / threads;
+int grid_for(int64_t items, int per_block, int sms, int per_sm = 2) {
+    int64_t g = (items + per_block - 1) / per_block;
     const int64_t cap = (int64_t)sms * per_sm;
     if (g > cap) g = cap;
     return (int)(g < 1 ? 1 : g);
@@ -555,7 +482,10 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.L = (int32_t)h->L;
     a.L2 = (int32_t)h->L + 2;
     a.grid_levels = h->grid_levels;
+    a.TB = d.TB;
+    a.alpha = h->alpha;
     a.Vd = reinterpret_cast<const typename P::Leaf*>(ar + d.V);
+    a.leaf = reinterpret_cast<const int32_t*>(ar + d.leaf);
     a.vbits = d.vbits;
     a.x = static_cast<const V*>(x);
     a.y = static_cast<V*>(y);
@@ -574,48 +504,60 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     return a;
 }
 
+// CTAs the persistent kernel can keep resident (at most two per SM; 0 if none)
 template <class P>
 int sweep_grid(const gc_handle* h) {
-    const size_t smem = (size_t)kStages * Tile<P>::NODES * sizeof(int2);
-    cuda_check(cudaFuncSetAttribute(sweep_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-               "sweep smem attribute");
     int per_sm = 0;
-    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel<P>, kSweepThreads, smem),
+    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel<P>, kThreads, 0),
                "sweep occupancy");
-    return per_sm >= 1 ? h->sms : 0;   // one CTA per SM
+    return std::min(per_sm, 2) * h->sms;
+}
+
+int64_t barriers_per_product(const gc_handle* h) {
+    const int Lg = h->grid_levels;
+    return std::max(Lg - 1, 0) + (Lg < h->L ? 1 : 0) + 1;
+}
+
+// Enqueues one product with the arguments in a (persistent kernel when the
+// device allows, else one kernel per level). Returns the launch count.
+template <class P>
+int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st) {
+    int grid = 0;
+    if (h->schedule == 0 && h->coop) grid = sweep_grid<P>(h);
+    int64_t launches = 0;
+    if (grid > 0) {
+        void* args[] = {&a};
+        cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P>, dim3(grid), dim3(kThreads), args, 0, st),
+                   "sweep launch");
+        launches = 1;
+    } else {
+        a.grid_levels = (int32_t)h->L;
+        // level 1 also writes the leaf tables; with no levels a table-only launch
+        const int64_t w1 = h->L >= 1 ? h->lv[LV_W * (h->L + 2) + 1] : 0;
+        const int64_t items = std::max<int64_t>(w1, (h->alpha + 1) * P::LPN);
+        level_kernel<P><<<grid_for(items, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, h->L >= 1 ? 1 : 0);
+        ++launches;
+        for (int k = 2; k <= h->L; ++k) {
+            const int64_t w = h->lv[LV_W * (h->L + 2) + k];
+            level_kernel<P><<<grid_for(w, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, k);
+            ++launches;
+        }
+        if (h->n > 0) {
+            const int64_t rows_per_block = h->emit_group == 0 ? 1 : kWarps * (32 / h->emit_group);
+            emit_kernel<P><<<grid_for(h->n, (int)rows_per_block, h->sms, 4), kThreads, 0, st>>>(a);
+            ++launches;
+        }
+    }
+    cuda_check(cudaGetLastError(), "kernel launch");
+    return launches;
 }
 
 template <class P>
 void run_product(gc_handle* h, const void* x, void* y, cudaStream_t st) {
     SweepArgs<P> a = make_args<P>(h, x, y);
-    int64_t launches = 0;
-    int grid = 0;
-    if (h->schedule == 0 && h->coop) grid = sweep_grid<P>(h);
-    if (grid > 0) {
-        const size_t smem = (size_t)kStages * Tile<P>::NODES * sizeof(int2);
-        void* args[] = {&a};
-        cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P>, dim3(grid), dim3(kSweepThreads), args,
-                                               smem, st),
-                   "sweep launch");
-        const int Lg = h->grid_levels;
-        h->bar_base += (unsigned long long)(std::max(Lg - 1, 0) + (Lg < h->L ? 1 : 0) + 1);
-        launches = 1;
-    } else {
-        a.grid_levels = (int32_t)h->L;
-        for (int k = 1; k <= h->L; ++k) {
-            const int64_t w = h->lv[LV_W * (h->L + 2) + k];
-            if (w == 0) continue;
-            level_kernel<P><<<grid_for(w * P::LPN, kLevelThreads * kNodesPerThread, h->sms), kLevelThreads, 0, st>>>(
-                a, k);
-            ++launches;
-        }
-        if (h->n > 0) {
-            const int64_t rows_per_block = h->emit_group == 0 ? 1 : (kSweepThreads / 32) * (32 / h->emit_group);
-            emit_kernel<P><<<grid_for(h->n, (int)rows_per_block, h->sms, 8), kSweepThreads, 0, st>>>(a);
-            ++launches;
-        }
-    }
-    cuda_check(cudaGetLastError(), "kernel launch");
+    const bool persistent = h->schedule == 0 && h->coop;
+    const int64_t launches = launch_product<P>(h, a, st);
+    if (persistent && launches == 1) h->bar_base += (unsigned long long)barriers_per_product(h);
     h->launches = launches;
 }
 
@@ -672,63 +614,33 @@ unsigned char* static_scratch_on_current_device() {
 }
 
 // Bytes of fixed scratch a product with k right-hand sides needs: status
-// block, root values, two level buffers (same parts as the arena's scratch).
+// block, [T | root values], two [T | level] buffers (the arena's scratch parts).
 int64_t static_scratch_need(const gc_handle* h, int32_t k) {
     const int64_t vb = policy_elem_bytes(h->policy) * k;
-    return 256 + align256(vb * h->n_roots) + 2 * align256(vb * h->max_width);
+    const int64_t TB = h->lay.TB;
+    return 256 + align256(vb * (TB + h->n_roots)) + 2 * align256(vb * (TB + h->max_width));
 }
 
 // One product whose scratch is the fixed array: the same kernels and order of
-// evaluation as run_product, with RV, the level buffers, the status word and
+// evaluation as gc_matvec, with RV, the level buffers, the status word and
 // the barrier counter pointed into g_static_scratch.
 template <class P>
 void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, unsigned char* scratch) {
     using V = typename P::V;
     SweepArgs<P> a = make_args<P>(h, x, y);
     const int64_t vb = (int64_t)sizeof(V) * P::LPN;
+    const int64_t rv_bytes = align256(vb * (a.TB + h->n_roots)), buf_bytes = align256(vb * (a.TB + h->max_width));
     a.status = reinterpret_cast<int32_t*>(scratch);
     a.bar = reinterpret_cast<unsigned long long*>(scratch + 64);
     a.bar_base = 0;
     a.rv = reinterpret_cast<V*>(scratch + 256);
-    a.buf0 = reinterpret_cast<V*>(scratch + 256 + align256(vb * h->n_roots));
-    a.buf1 = reinterpret_cast<V*>(scratch + 256 + align256(vb * h->n_roots) + align256(vb * h->max_width));
+    a.buf0 = reinterpret_cast<V*>(scratch + 256 + rv_bytes);
+    a.buf1 = reinterpret_cast<V*>(scratch + 256 + rv_bytes + buf_bytes);
     a.inject = 0;
     // the array keeps the previous call's contents: start from a clear status
     // word and barrier counter
     cuda_check(cudaMemsetAsync(scratch, 0, 256, st), "fixed scratch clear");
-    int64_t launches = 0;
-    int grid = 0;
-    if (h->schedule == 0 && h->coop) grid = sweep_grid<P>(h);
-    if (grid > 0) {
-        const size_t smem = (size_t)kStages * Tile<P>::NODES * sizeof(int2);
-        void* args[] = {&a};
-        cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P>, dim3(grid), dim3(kSweepThreads), args,
-                                               smem, st),
-                   "sweep launch");
-        launches = 1;
-    } else {
-        a.grid_levels = (int32_t)h->L;
-        for (int k = 1; k <= h->L; ++k) {
-            const int64_t w = h->lv[LV_W * (h->L + 2) + k];
-            if (w == 0) continue;
-            level_kernel<P><<<grid_for(w * P::LPN, kLevelThreads * kNodesPerThread, h->sms), kLevelThreads, 0, st>>>(
-                a, k);
-            ++launches;
-        }
-        if (h->n > 0) {
-            const int64_t rows_per_block = h->emit_group == 0 ? 1 : (kSweepThreads / 32) * (32 / h->emit_group);
-            emit_kernel<P><<<grid_for(h->n, (int)rows_per_block, h->sms, 8), kSweepThreads, 0, st>>>(a);
-            ++launches;
-        }
-    }
-    cuda_check(cudaGetLastError(), "kernel launch");
-    h->launches = launches;
-}
-
-// device leaf code of terminal p: -((col << vbits | vidx) + 2)
-inline int32_t leaf_ref(const Grammar& g, int32_t p, int32_t vbits) {
-    const int64_t q = ((int64_t)g.term_col[p] << vbits) | g.term_vidx[p];
-    return (int32_t)(-(q + 2));
+    h->launches = launch_product<P>(h, a, st);
 }
 
 }  // namespace
@@ -756,6 +668,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         h->n = g.n;
         h->m = g.m;
         h->L = g.L;
+        h->alpha = g.alpha();
         h->n_roots = g.n_roots;
         h->c_len = (int64_t)g.c_ref.size();
         h->max_width = g.max_width();
@@ -776,14 +689,20 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         }
         // levels narrow enough for one CTA finish the sweep there (when two or more)
         const int64_t L = g.L;
-        const int64_t tail_w = (int64_t)kSweepThreads * kNodesPerThread / (policy == GC_F32_SUM && k_max == 16 ? 4 : 1);
+        const int64_t tail_w = (policy == GC_F32_SUM && k_max == 16) ? Chunk<PolF32x16>::TAIL : Chunk<PolF32>::TAIL;
         int64_t first_narrow = L + 1;
         while (first_narrow > 1 && g.lvl_off[first_narrow] - g.lvl_off[first_narrow - 1] <= tail_w) --first_narrow;
         h->grid_levels = (int)(L - first_narrow + 1 >= 2 ? first_narrow - 1 : L);
 
-        // level table and nodes with leaf codes, each level padded to 16 nodes
+        // level table; level 1 with leaf codes, later levels with indices into [T | buffer]
+        auto leaf_code = [&](int32_t p) { return (int32_t)(((int64_t)g.term_col[p] << d.vbits) | g.term_vidx[p]); };
+        auto ref = [&](int32_t c) -> int32_t {   // packed reference -> [T | buffer] index
+            if (c >= 0) return (int32_t)(d.TB + c);
+            if (c == -1) return 0;
+            return -c - 1;                         // terminal p = -c-2 -> T[p+1]
+        };
         h->lv.assign((size_t)(4 * (L + 2)), 0);
-        std::vector<int32_t> nodes((size_t)(2 * d.n_nodes_padded), -1);
+        std::vector<int32_t> nodes((size_t)(2 * d.n_nodes_padded), 0);
         int64_t start = 0;
         for (int64_t k = 1; k <= L; ++k) {
             const int64_t w = g.lvl_off[k + 1] - g.lvl_off[k];
@@ -794,15 +713,15 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             for (int64_t q = 0; q < w; ++q)
                 for (int t = 0; t < 2; ++t) {
                     const int32_t c = g.nodes[2 * (g.lvl_off[k] + q) + t];
-                    nodes[2 * (start + q) + t] = c <= -2 ? leaf_ref(g, -c - 2, d.vbits) : c;
+                    if (k == 1 && c > -2) fail(GC_ERR_INVALID_GRAMMAR, "a level-1 node has a non-terminal child");
+                    nodes[2 * (start + q) + t] = k == 1 ? leaf_code(-c - 2) : ref(c);
                 }
             start += pad_nodes(w);
         }
+        std::vector<int32_t> leaf((size_t)g.alpha());
+        for (int64_t p = 0; p < g.alpha(); ++p) leaf[p] = leaf_code((int32_t)p);
         std::vector<int32_t> cref(g.c_ref.size());
-        for (size_t e = 0; e < cref.size(); ++e) {
-            const int32_t c = g.c_ref[e];
-            cref[e] = c <= -2 ? leaf_ref(g, -c - 2, d.vbits) : c;
-        }
+        for (size_t e = 0; e < cref.size(); ++e) cref[e] = ref(g.c_ref[e]);
         std::vector<int32_t> co(g.slp.c_off.size());
         for (size_t r = 0; r < co.size(); ++r) co[r] = (int32_t)g.slp.c_off[r];
 
@@ -816,6 +735,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             for (size_t i = 0; i < v.size(); ++i) v[i] = policy == GC_BOOL_OR ? ~0ll : (long long)g.V[i];
             put(st, a, d.V, v.data(), v.size());
         }
+        put(st, a, d.leaf, leaf.data(), leaf.size());
         put(st, a, d.c_off, co.data(), co.size());
         put(st, a, d.c_ref, cref.data(), cref.size());
         cuda_check(cudaMemsetAsync(a + d.status, 0, 256, st), "status clear");
@@ -873,7 +793,7 @@ gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_it
             dispatch_product(h, xv, yv, 1, st);
             launches += h->launches;
             if (n > 0) {
-                or_update_kernel<<<grid_for(n, kLevelThreads, h->sms), kLevelThreads, 0, st>>>(xv, yv, n, changed);
+                or_update_kernel<<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(xv, yv, n, changed);
                 ++launches;
             }
             cuda_check(cudaGetLastError(), "kernel launch");

@@ -1,41 +1,49 @@
 // Device arena layout of an uploaded grammar (host-side arithmetic only; used
 // by gc_layout and gc_upload). Every part starts on a 256-byte boundary.
 //
-//   read-only grammar   nodes     int2[sum of padded widths]  (a, b) child refs,
+//   read-only grammar   nodes     int2[sum of padded widths]  child references,
 //                                 each level starting on a 16-node (128 B)
 //                                 boundary and padded to a multiple of 16
 //                       levels    int64[4 (L+2)]   per level k: padded start,
 //                                 width, number of roots, RV slot of the first root
 //                       V         policy[|V|]      value dictionary
+//                       leaf      int32[alpha]     leaf code of terminal p
 //                       c_off     int32[n+1]
 //                       c_ref     int32[|C|]
-//   scratch             RV        value[rho]       root values
-//                       buf0/1    value[w*]        level ping-pong buffers
+//   scratch             RVX       value[TB + rho]  leaf table T, then root values
+//                       buf0X     value[TB + w*]   leaf table T, then a level's
+//                       buf1X     value[TB + w*]   values (the two streaming buffers)
 //                       status    256 B            status word, fixpoint flag,
 //                                                  grid-barrier arrival counter
 //   staging             xs        value[m]         x / y copies for the
 //                       ys        value[n]         host-buffer entry point
-// "value" is k_max elements of the policy's type (float, int64, uint64).
+// "value" is k_max elements of the policy's type (float, int64, uint64);
+// TB = alpha + 1 rounded up to a multiple of 64 values.
 //
-// Device child references (rewritten from the packed T-index form at upload):
-//   c >= 0    slot c of the previous level's buffer
-//   c == -1   the combine identity (second child of a pass-through)
-//   c <= -2   leaf q = -c - 2 = (column << vbits) | value index: the leaf value
-//             V[l] (x) x[j] is evaluated in the sweep, no terminal array.
+// Leaf table: T[0] is the combine identity and T[p+1] = V[l_p] (x) x[j_p] for
+// terminal p = <l_p, j_p> (Sec. 4.3's T). Its three copies sit in front of
+// each buffer, so that one index space covers both: a child or C reference is
+//   0            the identity (second child of a pass-through)
+//   p + 1        terminal p
+//   TB + s       slot s of the previous level (nodes) or root slot s (C)
+// and every read is a single load, without a branch. Level 1, whose children
+// are all terminals, instead stores leaf codes (column << vbits | value index)
+// and evaluates its leaves in the sweep while the T copies are being written.
 #pragma once
 
 #include "common.hpp"
 
 namespace gcs {
 
-constexpr int64_t kNodeAlign = 16;   // nodes per 128-byte bulk-copy granule
+constexpr int64_t kNodeAlign = 16;   // nodes per 128-byte granule
 
 struct DevLayout {
-    int64_t nodes, levels, V, c_off, c_ref;
+    int64_t nodes, levels, V, leaf, c_off, c_ref;
     int64_t RV, buf0, buf1, status, xs, ys;
     int64_t total, grammar_bytes, scratch_bytes, staging_bytes;
     int64_t value_bytes;   // bytes of one node value (k_max elements)
     int64_t n_nodes_padded;
+    int64_t TB;            // leaf-table block length in values
     int32_t vbits;         // bits of the value index inside a leaf code
 };
 
@@ -51,11 +59,14 @@ inline int32_t value_bits(int64_t n_values) {
     return b;
 }
 
+inline int64_t leaf_block(int64_t alpha) { return (alpha + 1 + 63) / 64 * 64; }
+
 inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     DevLayout d{};
-    const int64_t L = g.L, C = (int64_t)g.c_ref.size();
+    const int64_t L = g.L, C = (int64_t)g.c_ref.size(), A = g.alpha();
     d.value_bytes = policy_elem_bytes(p) * k_max;
     d.vbits = value_bits((int64_t)g.V.size());
+    d.TB = leaf_block(A);
     d.n_nodes_padded = 0;
     for (int64_t k = 1; k <= L; ++k) d.n_nodes_padded += pad_nodes(g.lvl_off[k + 1] - g.lvl_off[k]);
     int64_t o = 0;
@@ -67,13 +78,14 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.nodes = take(8 * d.n_nodes_padded);
     d.levels = take(8 * 4 * (L + 2));
     d.V = take(policy_elem_bytes(p) * std::max<int64_t>(1, (int64_t)g.V.size()));
+    d.leaf = take(4 * A);
     d.c_off = take(4 * (g.n + 1));
     d.c_ref = take(4 * C);
     d.grammar_bytes = o;
-    d.RV = take(d.value_bytes * g.n_roots);
+    d.RV = take(d.value_bytes * (d.TB + g.n_roots));
     const int64_t w = g.max_width();
-    d.buf0 = take(d.value_bytes * w);
-    d.buf1 = take(d.value_bytes * w);
+    d.buf0 = take(d.value_bytes * (d.TB + w));
+    d.buf1 = take(d.value_bytes * (d.TB + w));
     d.status = take(256);
     d.scratch_bytes = o - d.grammar_bytes;
     d.xs = take(d.value_bytes * g.m);
@@ -96,8 +108,10 @@ inline void check_policy(const Grammar& g, gc_policy p, int32_t k_max) {
         for (float v : g.V)
             if (v != 1.0f) fail(GC_ERR_UNSUPPORTED, "GC_BOOL_OR needs every stored entry to be 1");
     if ((int64_t)g.c_ref.size() >= INT32_MAX) fail(GC_ERR_UNSUPPORTED, "|C| >= 2^31");
-    if ((((int64_t)g.m) << value_bits((int64_t)g.V.size())) + 2 > INT32_MAX)
+    if ((((int64_t)g.m) << value_bits((int64_t)g.V.size())) >= INT32_MAX)
         fail(GC_ERR_UNSUPPORTED, "columns x distinct values too large for 31-bit leaf codes");
+    if (leaf_block(g.alpha()) + std::max(g.max_width(), g.n_roots) >= INT32_MAX)
+        fail(GC_ERR_UNSUPPORTED, "leaf table plus level width exceeds 31-bit indices");
 }
 
 }  // namespace gcs
