@@ -44,6 +44,7 @@ WORKLOADS = {
     "geno_10k_50k": dict(gen=gcsynth.GENO_MEDIUM, k=1),
     "geno_10k_50k_k16": dict(gen=gcsynth.GENO_MEDIUM, k=16),
     "geno_1k_2k": dict(gen=gcsynth.GENO_SMALL, k=1),
+    "graph_2m": dict(graph=gcsynth.GRAPH, k=1),
 }
 L2_FLUSH_BYTES = 512 << 20
 
@@ -83,13 +84,18 @@ def make_csr(gen):
     return gen["n"], gen["m"], rp, c, v
 
 
-def compulsory_bytes(st, k, alpha):
+def make_graph(gp):
+    rp, col = gcsynth.copy_model_graph(**gp)
+    return gp["nodes"], gp["nodes"], rp, col, None
+
+
+def compulsory_bytes(st, k, elem=4):
     """Algorithmic bytes of one product: every array the sweep must read or
-    write once -- child pairs of all layered nodes (8 B), leaf records (col +
-    value, 8 B), level tables, C offsets and references (4 B), x and y."""
+    write once -- child pairs of all layered nodes (8 B), one leaf code per
+    terminal (4 B), the level table, C offsets and references (4 B), x and y."""
     L = st["depth"]
-    return (8 * st["n_nodes"] + 8 * alpha + 3 * 8 * (L + 2) + 4 * (st["n"] + 1)
-            + 4 * st["c_len"] + 4 * k * (st["m"] + st["n"]))
+    return (8 * st["n_nodes"] + 4 * st["n_terminals"] + 4 * 8 * (L + 2) + 4 * (st["n"] + 1)
+            + 4 * st["c_len"] + elem * k * (st["m"] + st["n"]))
 
 
 class ClockSampler:
@@ -287,19 +293,31 @@ def run_ours(args):
     import grammar_compressed_sparse_gb300 as gcs
 
     wl = WORKLOADS[args.workload]
-    gen, k = wl["gen"], wl["k"]
+    k = wl["k"]
+    graph = "graph" in wl
     t0 = time.perf_counter()
-    G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: make_csr(gen))
+    if graph:
+        gp = wl["graph"]
+        gen = dict(n=gp["nodes"], m=gp["nodes"])
+        G = gcs.cached_grammar(f"graph:{sorted(gp.items())}", lambda: make_graph(gp))
+    else:
+        gen = wl["gen"]
+        G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: make_csr(gen))
     build_s = time.perf_counter() - t0
     st = G.stats()
-    alpha = st["n_terminals"]
-    eng = gcs.Engine(G, "f32", k, device=dev)
+    policy, elem = ("or", 8) if graph else ("f32", 4)
+    eng = gcs.Engine(G, policy, k, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     nvec = args.warmup + args.steps
-    xs = [torch.from_numpy(gcsynth.beta(gen["m"], seed=(rank * 1000 + i) % 100, k=k)).to(dev)
-          for i in range(min(nvec, 100))]
-    y = torch.empty((gen["n"],) if k == 1 else (gen["n"], k), dtype=torch.float32, device=dev)
+    if graph:
+        xs = [torch.from_numpy(np.random.default_rng(rank * 1000 + i).integers(
+            0, 2**63, gen["m"], dtype=np.int64)).to(dev) for i in range(min(nvec, 8))]
+        y = torch.empty(gen["n"], dtype=torch.int64, device=dev)
+    else:
+        xs = [torch.from_numpy(gcsynth.beta(gen["m"], seed=(rank * 1000 + i) % 100, k=k)).to(dev)
+              for i in range(min(nvec, 100))]
+        y = torch.empty((gen["n"],) if k == 1 else (gen["n"], k), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(i, timed_events=None):
@@ -336,10 +354,9 @@ def run_ours(args):
         total_s = float(t.item())
     value = world * args.steps / total_s
 
-    # end to end through the host-buffer entry point (pinned beta in, y out)
-    xh = [torch.from_numpy(gcsynth.beta(gen["m"], seed=i % 100, k=k)).pin_memory().numpy()
-          for i in range(min(nvec, 8))]
-    yh = torch.empty(y.shape, dtype=torch.float32).pin_memory().numpy()
+    # end to end through the host-buffer entry point (pinned x in, y out)
+    xh = [xx.cpu().pin_memory().numpy() for xx in xs[:8]]
+    yh = torch.empty(y.shape, dtype=y.dtype).pin_memory().numpy()
     for i in range(args.warmup):
         eng.matvec_host(xh[i % len(xh)], yh, stream=stream)
     e2e_t = 0.0
@@ -355,24 +372,41 @@ def run_ours(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e = world * args.steps / float(t.item())
 
+    # Boolean workload: the reachability fixpoint from 64 sources, timed once
+    fixpoint = None
+    if graph:
+        x0 = gcsynth.frontier(gen["n"], gcsynth.sources(gen["n"], gp["sources"], gp["seed"]))
+        x0d = torch.from_numpy(x0.view(np.int64)).to(dev)
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        _, iters, rc = eng.reach(x0d)
+        fixpoint = {"iterations": iters, "seconds": round(time.perf_counter() - t1, 5), "status": rc}
+
     if rank != 0:
         return
     # parity spot check of the last product against the oracle, 200 rows
     from oracle import direct
     y_last = y.cpu().numpy()
-    rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=200))
-    xl = gcsynth.beta(gen["m"], seed=(args.warmup + args.steps - 1) % len(xs) % 100, k=k)
-    y_ref, bnd = direct.matvec_f64(rp, c, v, xl)
-    ok, worst = direct.within_tolerance(y_last[:200], y_ref, bnd, 1e-4)
+    if graph:
+        x_last = xs[(args.warmup + args.steps - 1) % len(xs)].cpu().numpy().view(np.uint64)
+        rp, col = gcsynth.copy_model_graph(**gp)
+        y_ref = direct.matvec_or(rp, col, x_last)
+        ok = bool(np.array_equal(y_last.view(np.uint64), y_ref))
+        worst = 0.0 if ok else float("inf")
+    else:
+        rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=200))
+        xl = gcsynth.beta(gen["m"], seed=(args.warmup + args.steps - 1) % len(xs) % 100, k=k)
+        y_ref, bnd = direct.matvec_f64(rp, c, v, xl)
+        ok, worst = direct.within_tolerance(y_last[:200], y_ref, bnd, 1e-4)
 
     peak, peak_src = peaks()
-    bytes_step = compulsory_bytes(st, k, alpha)
+    bytes_step = compulsory_bytes(st, k, elem)
     mean_s = total_s / args.steps
     achieved = bytes_step / mean_s / 1e9
     lay = eng.layout
-    footprint = lay["grammar_bytes"] + lay["scratch_bytes"] + 4 * k * (gen["m"] + gen["n"])
+    footprint = lay["grammar_bytes"] + lay["scratch_bytes"] + elem * k * (gen["m"] + gen["n"])
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not graph:
         rates, recs = cpu_oracle_rates(args.workload, args.cpu_seconds)
         cpu = {"value": rates[0], "unit": "matvec/s", "cores": 1, "kind": "oracle",
                "sample": f"{recs[0]['rows']} rows ({recs[0]['rows'] / gen['n']:.2f} products) of the "
@@ -381,10 +415,11 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "matvec/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u64" if graph else "f32", "data": "synthetic",
         "config": {"workload": args.workload, "n": gen["n"], "m": gen["m"], "k": k,
-                   "founders": gen["founders"], "switch": gen["switch"], "mutation": gen["mutation"],
+                   **({"graph": "copy model, 64-bit source bitsets"} if graph else
+                      {"founders": gen["founders"], "switch": gen["switch"], "mutation": gen["mutation"]}),
                    "l2": "flushed before every step (512 MB write, outside the events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -393,8 +428,10 @@ def run_ours(args):
                      "kernel": "whole product (leaf gather + level combines + row emit)",
                      "algorithmic_bytes_per_launch": bytes_step},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": 4 * k * gen["m"],
-                "d2h_bytes_per_step": 4 * k * gen["n"]},
+        "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": elem * k * gen["m"],
+                "d2h_bytes_per_step": elem * k * gen["n"]},
+        "vectors_per_s": value * k,
+        "fixpoint": fixpoint,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "grammar": {"depth": st["depth"], "max_width": st["max_width"], "rules": st["n_rules"],

@@ -40,6 +40,31 @@ class Grammar:
             n, m, row_ptr, col, val, block_rows=block_rows, threads=threads, order=order)
 
     @classmethod
+    def from_row_blocks(cls, n, m, block_rows, make_block, workers=1, threads=0, order=0) -> "Grammar":
+        """Streaming build: ``make_block(r0, r1)`` returns the CSR (row_ptr
+        from 0, col, val) of rows [r0, r1); each block is compressed as soon
+        as it is made, ``workers`` blocks at a time (threads; the generator
+        and the library release the GIL)."""
+        from concurrent.futures import ThreadPoolExecutor
+        capi = _capi()
+        b = capi.gc_builder_create(n, m, threads=threads, order=order)
+        try:
+            def one(r0):
+                r1 = min(n, r0 + block_rows)
+                rp, col, val = make_block(r0, r1)
+                capi.gc_builder_add_rows(b, r0, rp, col, val)
+            starts = list(range(0, n, block_rows)) if n else []
+            if workers > 1:
+                with ThreadPoolExecutor(workers) as ex:
+                    list(ex.map(one, starts))
+            else:
+                for r0 in starts:
+                    one(r0)
+            return cls(_ptr=capi.gc_builder_finish(b))
+        finally:
+            capi.gc_builder_free(b)
+
+    @classmethod
     def load(cls, path: str) -> "Grammar":
         return cls(_ptr=_capi().gc_load(path))
 

@@ -87,6 +87,10 @@ _sig = {
     "gc_save": ([_vp, ctypes.c_char_p], ctypes.c_int),
     "gc_load": ([ctypes.c_char_p, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_free_grammar": ([_vp], None),
+    "gc_builder_create": ([_i64, _i64, ctypes.POINTER(BuildOpts), ctypes.POINTER(_vp)], ctypes.c_int),
+    "gc_builder_add_rows": ([_vp, _i64, _i64, _vp, _vp, _vp], ctypes.c_int),
+    "gc_builder_finish": ([_vp, ctypes.POINTER(_vp)], ctypes.c_int),
+    "gc_builder_free": ([_vp], None),
     "gc_free_handle": ([_vp], None),
 }
 for _name, (_args, _res) in _sig.items():
@@ -230,6 +234,31 @@ def gc_load(path: str) -> int:
     out = _vp()
     _check(_lib.gc_load(path.encode(), ctypes.byref(out)), "gc_load")
     return out.value
+
+
+def gc_builder_create(n, m, threads=0, order=0) -> int:
+    out = _vp()
+    opts = BuildOpts(0, threads, order)
+    _check(_lib.gc_builder_create(n, m, ctypes.byref(opts), ctypes.byref(out)), "gc_builder_create")
+    return out.value
+
+
+def gc_builder_add_rows(b, r0, row_ptr, col, val=None):
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    col = np.ascontiguousarray(col, dtype=np.int32)
+    val = None if val is None else np.ascontiguousarray(val, dtype=np.float32)
+    _check(_lib.gc_builder_add_rows(b, r0, len(row_ptr) - 1, _addr(row_ptr), _addr(col), _addr(val)),
+           "gc_builder_add_rows")
+
+
+def gc_builder_finish(b) -> int:
+    out = _vp()
+    _check(_lib.gc_builder_finish(b, ctypes.byref(out)), "gc_builder_finish")
+    return out.value
+
+
+def gc_builder_free(b):
+    _lib.gc_builder_free(b)
 
 
 def gc_free_grammar(g):

@@ -4,6 +4,7 @@
 #include <cstring>
 #include <exception>
 #include <memory>
+#include <mutex>
 
 #include "common.hpp"
 #include "layout.hpp"
@@ -15,6 +16,12 @@
 namespace gcs {
 
 static thread_local std::string g_last_error;
+
+static int32_t value_bits_host(int64_t n_values) {
+    int32_t b = 0;
+    while (((int64_t)1 << b) < n_values) ++b;
+    return b;
+}
 
 void set_last_error(const std::string& msg) { g_last_error = msg; }
 
@@ -153,6 +160,78 @@ void fields(IO& io, G& g) {
     io.vec(g.nodes);
     io.vec(g.node_id);
     io.vec(g.c_ref);
+}
+
+// One compressed row block of a streaming build: its own value dictionary,
+// terminal table and SLP (terminals in the block's local numbering).
+struct Block {
+    int64_t r0 = 0, rows = 0;
+    std::vector<float> V;
+    std::vector<int32_t> term_col, term_vidx;
+    Slp slp;
+};
+
+// Merges row blocks (sorted by first row, covering [0, n)) into one grammar:
+// one value dictionary (sorted union), one terminal table (sorted union of
+// <l, j>), rules numbered block after block, C rows in row order.
+void merge_blocks(std::vector<Block>& blocks, Grammar& g) {
+    std::vector<float> V;
+    for (auto& b : blocks) V.insert(V.end(), b.V.begin(), b.V.end());
+    std::sort(V.begin(), V.end());
+    V.erase(std::unique(V.begin(), V.end(), [](float x, float y) {
+                uint32_t a, c;
+                std::memcpy(&a, &x, 4);
+                std::memcpy(&c, &y, 4);
+                return a == c;
+            }),
+            V.end());
+    const int32_t vb = value_bits_host((int64_t)V.size());
+    auto vglob = [&](const Block& b, int32_t l) {
+        return (int32_t)(std::lower_bound(V.begin(), V.end(), b.V[l]) - V.begin());
+    };
+    std::vector<uint64_t> keys;
+    for (auto& b : blocks)
+        for (size_t t = 0; t < b.term_col.size(); ++t)
+            keys.push_back(((uint64_t)(uint32_t)b.term_col[t] << vb) | (uint64_t)vglob(b, b.term_vidx[t]));
+    std::sort(keys.begin(), keys.end());
+    keys.erase(std::unique(keys.begin(), keys.end()), keys.end());
+    if ((int64_t)keys.size() > INT32_MAX - 2) fail(GC_ERR_UNSUPPORTED, "more than 2^31-3 distinct terminals");
+    g.V = V;
+    g.term_col.resize(keys.size());
+    g.term_vidx.resize(keys.size());
+    for (size_t t = 0; t < keys.size(); ++t) {
+        g.term_col[t] = (int32_t)(keys[t] >> vb);
+        g.term_vidx[t] = (int32_t)(keys[t] & ((1ull << vb) - 1ull));
+    }
+    int64_t R = 0, C = 0;
+    for (auto& b : blocks) {
+        R += (int64_t)b.slp.rule_a.size();
+        C += (int64_t)b.slp.c_sym.size();
+    }
+    if (R >= INT32_MAX) fail(GC_ERR_UNSUPPORTED, "more than 2^31-1 rules over all blocks");
+    Slp& out = g.slp;
+    out.rule_a.reserve((size_t)R);
+    out.rule_b.reserve((size_t)R);
+    out.c_sym.reserve((size_t)C);
+    out.c_off.assign(1, 0);
+    int32_t base = 0;
+    for (auto& b : blocks) {
+        std::vector<int32_t> tmap(b.term_col.size());
+        for (size_t t = 0; t < tmap.size(); ++t) {
+            const uint64_t key = ((uint64_t)(uint32_t)b.term_col[t] << vb) | (uint64_t)vglob(b, b.term_vidx[t]);
+            tmap[t] = (int32_t)(std::lower_bound(keys.begin(), keys.end(), key) - keys.begin());
+        }
+        auto shift = [&](int32_t c) { return c >= 0 ? c + base : -(tmap[-c - 1] + 1); };
+        for (size_t i = 0; i < b.slp.rule_a.size(); ++i) {
+            out.rule_a.push_back(shift(b.slp.rule_a[i]));
+            out.rule_b.push_back(shift(b.slp.rule_b[i]));
+        }
+        const int64_t c0 = (int64_t)out.c_sym.size();
+        for (int32_t c : b.slp.c_sym) out.c_sym.push_back(shift(c));
+        for (size_t r = 1; r < b.slp.c_off.size(); ++r) out.c_off.push_back(c0 + b.slp.c_off[r]);
+        base += (int32_t)b.slp.rule_a.size();
+        b = Block();   // release the block as soon as it is merged
+    }
 }
 
 }  // namespace
@@ -315,5 +394,91 @@ gc_status gc_load(const char* path, gc_grammar** out) {
 }
 
 void gc_free_grammar(gc_grammar* g) { delete g; }
+
+}  // extern "C"
+
+struct gc_builder {
+    int64_t n = 0, m = 0;
+    gc_build_opts opts{0, 0, 0};
+    std::mutex mu;
+    std::vector<gcs::Block> blocks;
+    int64_t rows_added = 0;
+    double seconds = 0;
+};
+
+extern "C" {
+
+gc_status gc_builder_create(int64_t n, int64_t m, const gc_build_opts* opts, gc_builder** out) {
+    return guard([&] {
+        if (!out) fail(GC_ERR_ARG, "null output pointer");
+        if (n < 0 || m < 0) fail(GC_ERR_ARG, "negative matrix shape");
+        auto b = std::make_unique<gc_builder>();
+        b->n = n;
+        b->m = m;
+        if (opts) b->opts = *opts;
+        if (b->opts.order != 0 && b->opts.order != 1) fail(GC_ERR_ARG, "order must be 0 or 1");
+        *out = b.release();
+    });
+}
+
+gc_status gc_builder_add_rows(gc_builder* b, int64_t r0, int64_t rows, const int64_t* row_ptr, const int32_t* col,
+                              const float* val) {
+    return guard([&] {
+        if (!b) fail(GC_ERR_ARG, "null builder");
+        if (r0 < 0 || rows < 0 || r0 + rows > b->n) fail(GC_ERR_ARG, "row block outside [0, n)");
+        const double t0 = now_seconds();
+        Block blk;
+        blk.r0 = r0;
+        blk.rows = rows;
+        {
+            Csrv s = csrv_encode(rows, b->m, row_ptr, col, val, b->opts.threads);
+            blk.slp = repair(s, 0, rows);
+            blk.V = std::move(s.V);
+            blk.term_col = std::move(s.term_col);
+            blk.term_vidx = std::move(s.term_vidx);
+        }
+        const double dt = now_seconds() - t0;
+        std::lock_guard<std::mutex> lock(b->mu);
+        for (auto& o : b->blocks)
+            if (r0 < o.r0 + o.rows && o.r0 < r0 + rows) fail(GC_ERR_ARG, "row blocks overlap");
+        b->blocks.push_back(std::move(blk));
+        b->rows_added += rows;
+        b->seconds += dt;
+    });
+}
+
+gc_status gc_builder_finish(gc_builder* b, gc_grammar** out) {
+    return guard([&] {
+        if (!b || !out) fail(GC_ERR_ARG, "null argument");
+        *out = nullptr;
+        std::lock_guard<std::mutex> lock(b->mu);
+        if (b->rows_added != b->n) fail(GC_ERR_ARG, "row blocks do not cover all n rows");
+        std::sort(b->blocks.begin(), b->blocks.end(), [](const Block& x, const Block& y) { return x.r0 < y.r0; });
+        auto G = std::make_unique<gc_grammar>();
+        Grammar& g = G->g;
+        g.n = b->n;
+        g.m = b->m;
+        g.n_blocks = (int64_t)b->blocks.size();
+        const double t0 = now_seconds();
+        merge_blocks(b->blocks, g);
+        b->blocks.clear();
+        g.nnz = 0;
+        g.repair_seconds = b->seconds + (now_seconds() - t0);
+        layer_and_pack(g, b->opts.order);
+        validate_packed(g);
+        // stored non-zeros: the expansion lengths of C
+        {
+            std::vector<int64_t> len(g.slp.rule_a.size());
+            for (size_t i = 0; i < len.size(); ++i) {
+                const int32_t a = g.slp.rule_a[i], c = g.slp.rule_b[i];
+                len[i] = (a >= 0 ? len[a] : 1) + (c >= 0 ? len[c] : 1);
+            }
+            for (int32_t c : g.slp.c_sym) g.nnz += c >= 0 ? len[c] : 1;
+        }
+        *out = G.release();
+    });
+}
+
+void gc_builder_free(gc_builder* b) { delete b; }
 
 }  // extern "C"

@@ -8,26 +8,33 @@
 //                   in front (see layout.hpp); the level's roots (its first
 //                   nodes) are also written to RV, the emit-on-the-spot
 //                   capture                                  (Listing 1, Lemma 3.3)
-//   row emit        y[r] = (+) over row r's symbols of RV / T entries   (Lemma 2.2)
+//   row emit        y[r] = (+) over row r's symbols of C               (Lemma 2.2),
+//                   in one of two modes (layout.hpp): long rows are reduced
+//                   level by level in chunks, straight from the level buffer
+//                   right after the level is computed (emit on the spot,
+//                   Sec. 4.3) and summed per row at the end; short rows read
+//                   root values captured into RV
 //
 // Schedule (differences from the pages' two launches per level, for this GPU):
 //   * one persistent cooperative kernel per product, two CTAs of 512 threads
 //     per SM; levels are separated by a grid barrier whose waits are bounded
 //     (a wait that runs out sets the status word and the kernel returns);
-//   * within a level every warp works on its own chunks of 128 nodes
-//     (4 per lane, coalesced), with no block-wide synchronisation, and loads
+//   * within a level every warp works on its own chunks of nodes (128
+//     one-lane values, 4 per lane; or 16 four-lane values, 2 per lane),
+//     coalesced, with no block-wide synchronisation, and loads
 //     the next chunk's child pairs -- possibly of the next level, since pairs
 //     do not depend on values -- before gathering the current chunk's
 //     children, so node-stream latency hides behind gathers and barriers;
 //   * level 1 evaluates its (all-terminal) children in the sweep while the
-//     grid writes the three T copies, so T costs no phase of its own;
+//     grid writes the T copies, so T costs no phase of its own;
 //   * child values are gathered through L1/L2 (the grid barrier's gpu-scope
-//     acquire orders them after the writers); root values are stored with an
-//     L2 evict-last policy so the emit finds them in L2; the node and C
-//     streams are loaded evict-first;
-//   * the narrow top levels run on one CTA with block-level barriers;
-//   * the pages emit with atomicAdd into y; here each row is reduced by a
-//     fixed group of threads in a fixed order: deterministic, no atomics.
+//     acquire orders them after the writers); the node and C streams are
+//     loaded evict-first; root values for RV are stored evict-last;
+//   * the narrow top levels run on one CTA with block-level barriers, in a
+//     small buffer pair of their own, so that the other CTAs can reduce the
+//     C chunks of the last wide level meanwhile;
+//   * the pages emit with atomicAdd into y; here every partial sum has a
+//     fixed order: deterministic, no atomics.
 // A second schedule launches one kernel per level plus one emit kernel with
 // the same device functions (bit-identical y): the launch sequence of
 // Listing 1, kept as the reference point for the persistent one.
@@ -49,11 +56,11 @@ struct gc_handle {
     char* arena = nullptr;
     gcs::DevLayout lay{};
     int sms = 1;
-    int emit_group = 32;          // threads per row in the emit; 0 = one CTA per row
+    int emit_group = 32;          // row emit: threads per row; 0 = level emit
     int schedule = 0;             // 0 persistent (if cooperative launch works), 1 per level
     int coop = 0;                 // device supports cooperative launch
     int grid_levels = 0;          // levels 1..grid_levels use the whole grid
-    unsigned long long bar_base = 0;
+    unsigned long long bar_base = 0;   // barrier arrivals of all earlier persistent launches
     long long timeout_cycles = 4000000000LL;
     int32_t inject = 0;           // test-only: 1 = CTA 0 skips its first barrier arrival
     int64_t launches = 0;
@@ -64,18 +71,20 @@ namespace {
 
 constexpr int kThreads = 512;        // every kernel: 16 warps
 constexpr int kWarps = kThreads / 32;
-constexpr int kU = 4;                // nodes (or node lanes) per thread per chunk
-constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3;
+constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3, LV_ECH = 4, LV_TOFF = 5, LV_ROWS = 6;
 
 void cuda_check(cudaError_t e, const char* what) {
     if (e != cudaSuccess) fail(GC_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// A warp's chunk: U rows of NPW nodes, LPN lanes per node. Sixteen-wide
+// values (64 B a node) take two rows, so that a lane's pairs and child values
+// stay in registers.
 template <class P>
 struct Chunk {
+    static constexpr int U = P::LPN == 1 ? 4 : 2;    // nodes per lane
     static constexpr int NPW = 32 / P::LPN;          // nodes per warp row
-    static constexpr int NODES = NPW * kU;           // nodes per warp chunk
-    static constexpr int TAIL = NODES * kWarps * 2;  // widest level left to one CTA
+    static constexpr int NODES = NPW * U;            // nodes per warp chunk
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -124,7 +133,7 @@ template <class P>
 struct SweepArgs {
     using V = typename P::V;
     const int2* nodes;
-    const int64_t* lv;        // level table: 4 rows of L+2
+    const int64_t* lv;        // level table: LV_ROWS rows of L+2
     int32_t L, L2, grid_levels;
     int64_t TB;               // leaf-table block length (values)
     int64_t alpha;
@@ -135,11 +144,18 @@ struct SweepArgs {
     V* y;
     V* buf0;                  // [T | level values]
     V* buf1;
-    V* rv;                    // [T | root values]
-    const int32_t* c_off;
+    V* rv;                    // row emit: [T | root values]
+    const int32_t* c_off;     // row emit: C in row order
     const int32_t* c_ref;
+    const int4* echunk;       // level emit: (start, length, id, 0) per chunk
+    const int32_t* cref;      //   C grouped by level, then row
+    const int32_t* row_ech;   //   row r's chunk ids
+    const int32_t* late_off;  //   row r's references into the tail levels
+    const int32_t* late_ref;
+    V* esum;                  //   chunk sums
+    V* tbuf;                  // the narrow top levels' values, level after level
     int64_t n;
-    int32_t emit_group;
+    int32_t emit_group;       // 0: level emit; G: row emit with G lanes per row
     int32_t* status;
     unsigned long long* bar;
     unsigned long long bar_base;
@@ -157,7 +173,7 @@ __device__ __forceinline__ typename P::V leaf_value(int32_t code, int part, cons
     return P::leaf(__ldg(a.Vd + vi), __ldg(a.x + (int64_t)col * P::LPN + part));
 }
 
-// The three leaf-table copies (in front of buf0, buf1 and RV), grid-stride.
+// The leaf-table copies in front of buf0, buf1 (and RV in the row emit), grid-stride.
 template <class P>
 __device__ void write_leaf_tables(const SweepArgs<P>& a, int64_t tid, int64_t nthreads) {
     using V = typename P::V;
@@ -168,154 +184,218 @@ __device__ void write_leaf_tables(const SweepArgs<P>& a, int64_t tid, int64_t nt
         const V v = p == 0 ? P::identity() : leaf_value<P>(__ldg(a.leaf + (p - 1)), part, a);
         a.buf0[i] = v;
         a.buf1[i] = v;
-        a.rv[i] = v;
+        if (a.emit_group != 0) a.rv[i] = v;   // RV exists in the row emit only
     }
 }
 
 // Loads the child pairs of chunk c of level k (this warp's lanes).
 template <class P>
-__device__ __forceinline__ void load_chunk(const SweepArgs<P>& a, int k, int64_t c, int2 (&ab)[kU]) {
+__device__ __forceinline__ void load_chunk(const SweepArgs<P>& a, int k, int64_t c, int2 (&ab)[Chunk<P>::U]) {
     constexpr int NPW = Chunk<P>::NPW;
     const int lane = threadIdx.x & 31;
     const int64_t w = a.lvl(LV_W, k);
     const int2* src = a.nodes + a.lvl(LV_START, k);
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < Chunk<P>::U; ++u) {
         const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
         ab[u] = node < w ? __ldcs(src + node) : make_int2(0, 0);
     }
 }
 
-// Combines chunk c of level k from its prefetched child pairs.
-template <class P>
-__device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int64_t c, const int2 (&ab)[kU],
-                                              uint64_t keep) {
+// Combines chunk c of level k from its prefetched child pairs. prev is the
+// [T | level k-1] index space; with kTail, references past T into level k-1
+// come from prev_tail instead (a narrow level kept in the tail buffers). The
+// values go to cur[t]; roots also to rv[t] when rv is given.
+template <class P, bool kTail>
+__device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int64_t c, const int2 (&ab)[Chunk<P>::U],
+                                              const typename P::V* prev, const typename P::V* prev_tail,
+                                              typename P::V* cur, typename P::V* rv, uint64_t keep) {
     using V = typename P::V;
     constexpr int NPW = Chunk<P>::NPW;
     const int lane = threadIdx.x & 31;
     const int part = lane % P::LPN;
     const int64_t w = a.lvl(LV_W, k), nroots = a.lvl(LV_ROOTS, k);
-    const V* prev = (k & 1) ? a.buf0 : a.buf1;
-    V* cur = ((k & 1) ? a.buf1 : a.buf0) + a.TB * P::LPN;
-    V* rv = a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN;
-    V va[kU], vb[kU];
+    V va[Chunk<P>::U], vb[Chunk<P>::U];
     if (k == 1) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
+        for (int u = 0; u < Chunk<P>::U; ++u) {
             const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
             va[u] = node < w ? leaf_value<P>(ab[u].x, part, a) : P::identity();
             vb[u] = node < w ? leaf_value<P>(ab[u].y, part, a) : P::identity();
         }
     } else {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            va[u] = prev[(int64_t)ab[u].x * P::LPN + part];
-            vb[u] = prev[(int64_t)ab[u].y * P::LPN + part];
+        for (int u = 0; u < Chunk<P>::U; ++u) {
+            if (kTail && prev_tail != nullptr) {
+                const int64_t xa = ab[u].x, xb = ab[u].y;
+                va[u] = xa >= a.TB ? prev_tail[(xa - a.TB) * P::LPN + part] : prev[xa * P::LPN + part];
+                vb[u] = xb >= a.TB ? prev_tail[(xb - a.TB) * P::LPN + part] : prev[xb * P::LPN + part];
+            } else {
+                va[u] = prev[(int64_t)ab[u].x * P::LPN + part];
+                vb[u] = prev[(int64_t)ab[u].y * P::LPN + part];
+            }
         }
     }
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < Chunk<P>::U; ++u) {
         const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
         if (node < w) {
             const V v = P::combine(va[u], vb[u]);
             cur[node * P::LPN + part] = v;
-            if (node < nroots) st_keep(rv + node * P::LPN + part, v, keep);
+            if (rv != nullptr && node < nroots) st_keep(rv + node * P::LPN + part, v, keep);
         }
     }
+}
+
+// Buffer pointers of grid level k: [T | level k-1] in, level k's values out.
+template <class P>
+struct LevelIO {
+    const typename P::V* prev;
+    typename P::V* cur;
+    typename P::V* rv;
+};
+template <class P>
+__device__ __forceinline__ LevelIO<P> level_io(const SweepArgs<P>& a, int k) {
+    LevelIO<P> io;
+    io.prev = (k & 1) ? a.buf0 : a.buf1;
+    io.cur = ((k & 1) ? a.buf1 : a.buf0) + a.TB * P::LPN;
+    io.rv = a.emit_group != 0 ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;
+    return io;
+}
+
+// Buffer pointers of tail level k > Lg: T from either full buffer, level k-1
+// from its full buffer (k-1 == Lg) or from the tail buffer, level k's values
+// into the tail buffer.
+template <class P>
+struct TailIO {
+    const typename P::V* prev;
+    const typename P::V* prev_tail;   // nullptr: level k-1 is in prev
+    typename P::V* cur;
+    typename P::V* rv;
+};
+template <class P>
+__device__ __forceinline__ TailIO<P> tail_io(const SweepArgs<P>& a, int k) {
+    TailIO<P> io;
+    io.prev = (k & 1) ? a.buf0 : a.buf1;
+    io.prev_tail = k - 1 > a.grid_levels ? a.tbuf + a.lvl(LV_TOFF, k - 1) * P::LPN : nullptr;
+    io.cur = a.tbuf + a.lvl(LV_TOFF, k) * P::LPN;
+    io.rv = a.emit_group != 0 ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;
+    return io;
 }
 
 // ---------------------------------------------------------------- row emit
-constexpr int kEmitBatch = 4;
 
-// G threads per row (G divides 32); warps walk rows in lockstep so the
-// shuffles always see the full warp. Thread gl sums its symbols q = s+gl,
-// s+gl+G, ... in order, then the group reduces by a fixed butterfly.
+// S symbol slots of LPN lanes each per row, S = min(G, 32 / LPN) (G divides
+// 32); warps walk rows in lockstep so the shuffles always see the full warp.
+// Lane (slot, part) sums part `part` of the row's symbols q = s+slot,
+// s+slot+S, ... in order, then the group reduces the slots by a fixed butterfly.
 template <class P, int G>
 __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     using V = typename P::V;
-    constexpr int RPW = 32 / G;
+    constexpr int S = G < 32 / P::LPN ? G : 32 / P::LPN;
+    constexpr int GG = S * P::LPN;                     // lanes per row
+    constexpr int RPW = 32 / GG;                       // rows per warp
+    constexpr int BATCH = P::LPN == 1 ? 4 : 2;         // symbols loaded together per lane
     const int lane = threadIdx.x & 31;
-    const int gl = lane % G;
+    const int gl = lane % GG;
+    const int slot = gl / P::LPN, part = gl % P::LPN;
     const int64_t warp = block * kWarps + (threadIdx.x >> 5);
     const int64_t nwarps = nblocks * kWarps;
     for (int64_t base = warp * RPW; base < a.n; base += nwarps * RPW) {
-        const int64_t row = base + lane / G;
-        V acc[P::LPN];
-#pragma unroll
-        for (int l = 0; l < P::LPN; ++l) acc[l] = P::identity();
+        const int64_t row = base + lane / GG;
+        V acc = P::identity();
         if (row < a.n) {
             const int32_t s = __ldg(a.c_off + row), e = __ldg(a.c_off + row + 1);
-            for (int32_t q0 = s + gl; q0 < e; q0 += G * kEmitBatch) {
-                int32_t c[kEmitBatch];
+            for (int32_t q0 = s + slot; q0 < e; q0 += S * BATCH) {
+                int32_t c[BATCH];
 #pragma unroll
-                for (int u = 0; u < kEmitBatch; ++u) c[u] = q0 + u * G < e ? __ldcs(a.c_ref + q0 + u * G) : 0;
-                V v[kEmitBatch][P::LPN];
+                for (int u = 0; u < BATCH; ++u) c[u] = q0 + u * S < e ? __ldcs(a.c_ref + q0 + u * S) : 0;
+                V v[BATCH];
 #pragma unroll
-                for (int u = 0; u < kEmitBatch; ++u)
+                for (int u = 0; u < BATCH; ++u) v[u] = a.rv[(int64_t)c[u] * P::LPN + part];
 #pragma unroll
-                    for (int l = 0; l < P::LPN; ++l) v[u][l] = a.rv[(int64_t)c[u] * P::LPN + l];
-#pragma unroll
-                for (int u = 0; u < kEmitBatch; ++u)
-#pragma unroll
-                    for (int l = 0; l < P::LPN; ++l) acc[l] = P::combine(acc[l], v[u][l]);
+                for (int u = 0; u < BATCH; ++u) acc = P::combine(acc, v[u]);
             }
         }
 #pragma unroll
-        for (int msk = G / 2; msk >= 1; msk >>= 1)
-#pragma unroll
-            for (int l = 0; l < P::LPN; ++l) acc[l] = P::combine(acc[l], shfl_x(acc[l], msk));
-        if (row < a.n && gl == 0)
-#pragma unroll
-            for (int l = 0; l < P::LPN; ++l) a.y[row * P::LPN + l] = acc[l];
+        for (int msk = GG / 2; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
+        if (row < a.n && slot == 0) a.y[row * P::LPN + part] = acc;
     }
 }
 
-// One CTA per row, for long rows of C.
+// Level emit: chunk j holds references cref[start .. start+len) of one
+// (level, row), len <= kEmitChunk. A warp takes 32/LPN references at a time,
+// LPN lanes each; lane (slot, part) sums part `part` of references slot,
+// slot + 32/LPN, ... in order, the warp reduces the slots by a fixed
+// butterfly, and the sum goes to esum[id]. base is the [T | level] index space
+// of the chunk's level; with tb, level references past T come from that tail
+// buffer instead.
+constexpr int kEmitChunk = (int)kEmitChunkSyms;
+
 template <class P>
-__device__ void emit_ctas(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
+__device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, const typename P::V* base,
+                                           const typename P::V* tb) {
     using V = typename P::V;
-    __shared__ V red[kWarps][P::LPN];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int64_t row = block; row < a.n; row += nblocks) {
-        V acc[P::LPN];
+    constexpr int NS = 32 / P::LPN;            // reference slots per warp row
+    constexpr int PER = kEmitChunk / NS;       // references per lane
+    constexpr int B = P::LPN == 1 ? PER : 4;   // references loaded together
+    const int lane = threadIdx.x & 31;
+    const int part = lane % P::LPN, slot = lane / P::LPN;
+    const int4 ch = __ldg(a.echunk + j);
+    V acc = P::identity();
 #pragma unroll
-        for (int l = 0; l < P::LPN; ++l) acc[l] = P::identity();
-        const int32_t s = __ldg(a.c_off + row), e = __ldg(a.c_off + row + 1);
-        for (int32_t q0 = s + threadIdx.x; q0 < e; q0 += kThreads * kEmitBatch) {
-            int32_t c[kEmitBatch];
+    for (int u0 = 0; u0 < PER; u0 += B) {
+        if (u0 * NS >= ch.y) break;            // the same for the whole warp
+        int32_t r[B];
 #pragma unroll
-            for (int u = 0; u < kEmitBatch; ++u) c[u] = q0 + u * kThreads < e ? __ldcs(a.c_ref + q0 + u * kThreads) : 0;
-            V v[kEmitBatch][P::LPN];
+        for (int u = 0; u < B; ++u) {
+            const int idx = (u0 + u) * NS + slot;
+            r[u] = idx < ch.y ? __ldcs(a.cref + ch.x + idx) : 0;
+        }
+        V v[B];
 #pragma unroll
-            for (int u = 0; u < kEmitBatch; ++u)
-#pragma unroll
-                for (int l = 0; l < P::LPN; ++l) v[u][l] = a.rv[(int64_t)c[u] * P::LPN + l];
-#pragma unroll
-            for (int u = 0; u < kEmitBatch; ++u)
-#pragma unroll
-                for (int l = 0; l < P::LPN; ++l) acc[l] = P::combine(acc[l], v[u][l]);
+        for (int u = 0; u < B; ++u) {
+            const int64_t c = r[u];
+            v[u] = (tb != nullptr && c >= a.TB) ? tb[(c - a.TB) * P::LPN + part] : base[c * P::LPN + part];
         }
 #pragma unroll
-        for (int msk = 16; msk >= 1; msk >>= 1)
+        for (int u = 0; u < B; ++u) acc = P::combine(acc, v[u]);
+    }
 #pragma unroll
-            for (int l = 0; l < P::LPN; ++l) acc[l] = P::combine(acc[l], shfl_x(acc[l], msk));
-        if (lane == 0)
-#pragma unroll
-            for (int l = 0; l < P::LPN; ++l) red[wid][l] = acc[l];
-        __syncthreads();
-        if (threadIdx.x < P::LPN) {
-            V t = red[0][threadIdx.x];
-            for (int w = 1; w < kWarps; ++w) t = P::combine(t, red[w][threadIdx.x]);
-            a.y[row * P::LPN + threadIdx.x] = t;
-        }
-        __syncthreads();
+    for (int msk = 16; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
+    if (slot == 0) a.esum[(int64_t)ch.z * P::LPN + part] = acc;
+}
+
+// The chunks of level k (0 = bare terminals), spread over warps gwarp, gwarp +
+// nwarps, ...
+template <class P>
+__device__ void emit_level(const SweepArgs<P>& a, int k, const typename P::V* base, const typename P::V* tb,
+                           int64_t gwarp, int64_t nwarps) {
+    const int64_t j1 = a.lvl(LV_ECH, k + 1);
+    for (int64_t j = a.lvl(LV_ECH, k) + gwarp; j < j1; j += nwarps) emit_chunk<P>(a, j, base, tb);
+}
+
+// y[r] = row r's chunk sums added in chunk-id order, then its references into
+// the tail levels in C order (identity for an empty row)
+template <class P>
+__device__ void emit_final(const SweepArgs<P>& a, int64_t tid, int64_t nthreads) {
+    using V = typename P::V;
+    for (int64_t i = tid; i < a.n * P::LPN; i += nthreads) {
+        const int64_t row = i / P::LPN;
+        const int l = (int)(i % P::LPN);
+        V acc = P::identity();
+        for (int32_t c = __ldg(a.row_ech + row); c < __ldg(a.row_ech + row + 1); ++c)
+            acc = P::combine(acc, a.esum[(int64_t)c * P::LPN + l]);
+        for (int32_t q = __ldg(a.late_off + row); q < __ldg(a.late_off + row + 1); ++q)
+            acc = P::combine(acc, a.tbuf[(int64_t)__ldg(a.late_ref + q) * P::LPN + l]);
+        a.y[i] = acc;
     }
 }
 
+// Row emit: groups of G lanes per row (emit_group = G).
 template <class P>
 __device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     switch (a.emit_group) {
-        case 0: emit_ctas<P>(a, block, nblocks); break;
         case 1: emit_groups<P, 1>(a, block, nblocks); break;
         case 2: emit_groups<P, 2>(a, block, nblocks); break;
         case 4: emit_groups<P, 4>(a, block, nblocks); break;
@@ -326,8 +406,9 @@ __device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks)
 }
 
 // ---------------------------------------------------------------- grid barrier
-// Arrival counter that only grows; barrier j of this launch completes when it
-// reaches (bar_base + j + 1) * gridDim.x. A wait gives up after a.timeout
+// Arrival counter that only grows; bar_base is its value when the launch
+// starts, and barrier j of this launch completes when it reaches
+// bar_base + (j + 1) * gridDim.x. A wait gives up after a.timeout
 // cycles (or when another CTA already reported a timeout), sets the status
 // word and returns false. The acquire at gpu scope, followed by the block
 // barrier, orders every thread's later loads after the other CTAs' writes.
@@ -342,7 +423,7 @@ __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
             __threadfence();
             red_add_release(a.bar, 1ull);
         }
-        const unsigned long long target = (a.bar_base + j + 1) * (unsigned long long)gridDim.x;
+        const unsigned long long target = a.bar_base + (j + 1) * (unsigned long long)gridDim.x;
         const long long t0 = clock64();
         unsigned it = 0;
         while (ld_acquire(a.bar) < target) {
@@ -384,43 +465,56 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
     };
 
     write_leaf_tables<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    const bool lemit = a.emit_group == 0;
 
     int kn = 1;
     int64_t cn = gw;
     norm(kn, cn);
-    int2 nab[kU];
+    int2 nab[Chunk<P>::U];
     if (kn <= Lg) load_chunk<P>(a, kn, cn, nab);
     unsigned long long nbar = 0;
     for (int k = 1; k <= Lg; ++k) {
         if (k > 1 && !grid_sync(a, nbar++)) return;
+        const LevelIO<P> io = level_io<P>(a, k);
         while (kn == k) {
-            int2 ab[kU];
+            int2 ab[Chunk<P>::U];
 #pragma unroll
-            for (int u = 0; u < kU; ++u) ab[u] = nab[u];
+            for (int u = 0; u < Chunk<P>::U; ++u) ab[u] = nab[u];
             const int64_t c = cn;
             cn += GW;
             norm(kn, cn);
             if (kn <= Lg) load_chunk<P>(a, kn, cn, nab);   // next chunk, maybe of a later level
-            combine_chunk<P>(a, k, c, ab, keep);
+            combine_chunk<P, false>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
         }
-    }
-    // narrow top levels: CTA 0 alone, block barriers only
-    if (Lg < a.L) {
-        if (!grid_sync(a, nbar++)) return;
-        if (blockIdx.x == 0) {
-            const int w0 = threadIdx.x >> 5;
-            for (int k = Lg + 1; k <= a.L; ++k) {
-                for (int64_t c = w0; c < nchunks(k); c += kWarps) {
-                    int2 ab[kU];
-                    load_chunk<P>(a, k, c, ab);
-                    combine_chunk<P>(a, k, c, ab, keep);
-                }
-                __syncthreads();
-            }
+        if (lemit && k >= 2) {   // level k-1 is complete and still in its buffer
+            emit_level<P>(a, k - 1, io.prev, nullptr, gw, GW);
+            if (k == 2) emit_level<P>(a, 0, a.buf0, nullptr, gw, GW);
         }
     }
     if (!grid_sync(a, nbar++)) return;
-    emit_rows<P>(a, blockIdx.x, gridDim.x);
+    // what is left of the level emit: level Lg, and the terminals if no phase took them
+    const bool tail = Lg < a.L;
+    const int64_t skip = (tail && gridDim.x > 1) ? kWarps : 0;   // CTA 0 runs the tail
+    if (lemit && gw >= skip) {
+        if (Lg >= 1) emit_level<P>(a, Lg, (Lg & 1) ? a.buf1 : a.buf0, nullptr, gw - skip, GW - skip);
+        if (Lg < 2) emit_level<P>(a, 0, a.buf0, nullptr, gw - skip, GW - skip);
+    }
+    // narrow top levels: CTA 0 alone, block barriers only, into the tail buffer
+    if (tail && blockIdx.x == 0) {
+        const int w0 = threadIdx.x >> 5;
+        for (int k = Lg + 1; k <= a.L; ++k) {
+            const TailIO<P> io = tail_io<P>(a, k);
+            for (int64_t c = w0; c < nchunks(k); c += kWarps) {
+                int2 ab[Chunk<P>::U];
+                load_chunk<P>(a, k, c, ab);
+                combine_chunk<P, true>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, keep);
+            }
+            __syncthreads();
+        }
+    }
+    if (!grid_sync(a, nbar++)) return;
+    if (lemit) emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    else emit_rows<P>(a, blockIdx.x, gridDim.x);
 }
 
 // ---------------------------------------------------------------- per-level schedule
@@ -432,20 +526,40 @@ __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a
     if (k <= 1) write_leaf_tables<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
     if (k < 1) return;
     const int64_t nc = (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES;
-    int2 nab[kU];
+    const bool tail = k > a.grid_levels;
+    const LevelIO<P> io = level_io<P>(a, k);
+    const TailIO<P> tio = tail_io<P>(a, k);
+    int2 nab[Chunk<P>::U];
     if (gw < nc) load_chunk<P>(a, k, gw, nab);
     for (int64_t c = gw; c < nc; c += GW) {
-        int2 ab[kU];
+        int2 ab[Chunk<P>::U];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) ab[u] = nab[u];
+        for (int u = 0; u < Chunk<P>::U; ++u) ab[u] = nab[u];
         if (c + GW < nc) load_chunk<P>(a, k, c + GW, nab);
-        combine_chunk<P>(a, k, c, ab, keep);
+        if (tail) combine_chunk<P, true>(a, k, c, ab, tio.prev, tio.prev_tail, tio.cur, tio.rv, keep);
+        else combine_chunk<P, false>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
+    }
+    // level k-1 (a wide one) is complete and still in its buffer
+    if (a.emit_group == 0 && k >= 2) {
+        if (k - 1 <= a.grid_levels) emit_level<P>(a, k - 1, io.prev, nullptr, gw, GW);
+        if (k == 2) emit_level<P>(a, 0, a.buf0, nullptr, gw, GW);
     }
 }
 
+// phase 0: what is left of the level emit (level L when it is a wide one,
+// terminals if L < 2), or the whole row emit; phase 1: the level emit's row sums
 template <class P>
-__global__ void __launch_bounds__(kThreads, 2) emit_kernel(const SweepArgs<P> a) {
-    emit_rows<P>(a, blockIdx.x, gridDim.x);
+__global__ void __launch_bounds__(kThreads, 2) emit_kernel(const SweepArgs<P> a, int phase) {
+    const int64_t GW = (int64_t)gridDim.x * kWarps;
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (a.emit_group != 0) {
+        emit_rows<P>(a, blockIdx.x, gridDim.x);
+    } else if (phase == 0) {
+        if (a.L >= 1 && a.grid_levels == a.L) emit_level<P>(a, a.L, (a.L & 1) ? a.buf1 : a.buf0, nullptr, gw, GW);
+        if (a.L < 2) emit_level<P>(a, 0, a.buf0, nullptr, gw, GW);
+    } else {
+        emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    }
 }
 
 // x |= y elementwise; sets *changed if any word changed (Boolean fixpoint step).
@@ -480,7 +594,7 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.nodes = reinterpret_cast<const int2*>(ar + d.nodes);
     a.lv = reinterpret_cast<const int64_t*>(ar + d.levels);
     a.L = (int32_t)h->L;
-    a.L2 = (int32_t)h->L + 2;
+    a.L2 = (int32_t)h->L + 2;   // row stride of the level table
     a.grid_levels = h->grid_levels;
     a.TB = d.TB;
     a.alpha = h->alpha;
@@ -494,6 +608,13 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.rv = reinterpret_cast<V*>(ar + d.RV);
     a.c_off = reinterpret_cast<const int32_t*>(ar + d.c_off);
     a.c_ref = reinterpret_cast<const int32_t*>(ar + d.c_ref);
+    a.echunk = reinterpret_cast<const int4*>(ar + d.echunk);
+    a.cref = reinterpret_cast<const int32_t*>(ar + d.cref);
+    a.row_ech = reinterpret_cast<const int32_t*>(ar + d.row_ech);
+    a.late_off = reinterpret_cast<const int32_t*>(ar + d.late_off);
+    a.late_ref = reinterpret_cast<const int32_t*>(ar + d.late_ref);
+    a.esum = reinterpret_cast<V*>(ar + d.esum);
+    a.tbuf = reinterpret_cast<V*>(ar + d.tbuf);
     a.n = h->n;
     a.emit_group = h->emit_group;
     a.status = reinterpret_cast<int32_t*>(ar + d.status);
@@ -514,16 +635,16 @@ int sweep_grid(const gc_handle* h) {
 }
 
 int64_t barriers_per_product(const gc_handle* h) {
-    const int Lg = h->grid_levels;
-    return std::max(Lg - 1, 0) + (Lg < h->L ? 1 : 0) + 1;
+    return std::max(h->grid_levels - 1, 0) + 2;
 }
 
 // Enqueues one product with the arguments in a (persistent kernel when the
 // device allows, else one kernel per level). Returns the launch count.
 template <class P>
-int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st) {
+int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, int* grid_out = nullptr) {
     int grid = 0;
     if (h->schedule == 0 && h->coop) grid = sweep_grid<P>(h);
+    if (grid_out) *grid_out = grid;
     int64_t launches = 0;
     if (grid > 0) {
         void* args[] = {&a};
@@ -531,7 +652,6 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st) {
                    "sweep launch");
         launches = 1;
     } else {
-        a.grid_levels = (int32_t)h->L;
         // level 1 also writes the leaf tables; with no levels a table-only launch
         const int64_t w1 = h->L >= 1 ? h->lv[LV_W * (h->L + 2) + 1] : 0;
         const int64_t items = std::max<int64_t>(w1, (h->alpha + 1) * P::LPN);
@@ -542,10 +662,13 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st) {
             level_kernel<P><<<grid_for(w, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, k);
             ++launches;
         }
-        if (h->n > 0) {
-            const int64_t rows_per_block = h->emit_group == 0 ? 1 : kWarps * (32 / h->emit_group);
-            emit_kernel<P><<<grid_for(h->n, (int)rows_per_block, h->sms, 4), kThreads, 0, st>>>(a);
+        if (h->n > 0 && h->emit_group != 0) {
+            emit_kernel<P><<<grid_for(h->n, kWarps * (32 / h->emit_group), h->sms, 4), kThreads, 0, st>>>(a, 0);
             ++launches;
+        } else if (h->n > 0) {
+            emit_kernel<P><<<grid_for(h->lay.n_echunks, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 0);
+            emit_kernel<P><<<grid_for(h->n * P::LPN, kThreads, h->sms, 4), kThreads, 0, st>>>(a, 1);
+            launches += 2;
         }
     }
     cuda_check(cudaGetLastError(), "kernel launch");
@@ -555,9 +678,9 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st) {
 template <class P>
 void run_product(gc_handle* h, const void* x, void* y, cudaStream_t st) {
     SweepArgs<P> a = make_args<P>(h, x, y);
-    const bool persistent = h->schedule == 0 && h->coop;
-    const int64_t launches = launch_product<P>(h, a, st);
-    if (persistent && launches == 1) h->bar_base += (unsigned long long)barriers_per_product(h);
+    int grid = 0;
+    const int64_t launches = launch_product<P>(h, a, st, &grid);
+    if (grid > 0) h->bar_base += (unsigned long long)barriers_per_product(h) * (unsigned long long)grid;
     h->launches = launches;
 }
 
@@ -613,33 +736,54 @@ unsigned char* static_scratch_on_current_device() {
     return g_static_ptr[dev];
 }
 
-// Bytes of fixed scratch a product with k right-hand sides needs: status
-// block, [T | root values], two [T | level] buffers (the arena's scratch parts).
-int64_t static_scratch_need(const gc_handle* h, int32_t k) {
+// Offsets of the scratch parts inside the fixed array for a product with k
+// right-hand sides, in the arena's order: buffers, tail buffers, level-emit
+// sums or RV, then the status block.
+struct StaticParts {
+    int64_t buf0, buf1, esum, tbuf, rv, status, total;
+};
+StaticParts static_parts(const gc_handle* h, int32_t k) {
+    const DevLayout& d = h->lay;
     const int64_t vb = policy_elem_bytes(h->policy) * k;
-    const int64_t TB = h->lay.TB;
-    return 256 + align256(vb * (TB + h->n_roots)) + 2 * align256(vb * (TB + h->max_width));
+    StaticParts s{};
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    s.buf0 = take(vb * (d.TB + h->max_width));
+    s.buf1 = take(vb * (d.TB + h->max_width));
+    s.tbuf = take(vb * d.tail_total);
+    if (d.level_emit) s.esum = take(vb * d.n_echunks);
+    else s.rv = take(vb * (d.TB + h->n_roots));
+    s.status = take(256);
+    s.total = o;
+    return s;
 }
 
+int64_t static_scratch_need(const gc_handle* h, int32_t k) { return static_parts(h, k).total; }
+
 // One product whose scratch is the fixed array: the same kernels and order of
-// evaluation as gc_matvec, with RV, the level buffers, the status word and
-// the barrier counter pointed into g_static_scratch.
+// evaluation as gc_matvec, with the level buffers, emit sums or RV, status
+// word and barrier counter pointed into g_static_scratch.
 template <class P>
 void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, unsigned char* scratch) {
     using V = typename P::V;
     SweepArgs<P> a = make_args<P>(h, x, y);
-    const int64_t vb = (int64_t)sizeof(V) * P::LPN;
-    const int64_t rv_bytes = align256(vb * (a.TB + h->n_roots)), buf_bytes = align256(vb * (a.TB + h->max_width));
-    a.status = reinterpret_cast<int32_t*>(scratch);
-    a.bar = reinterpret_cast<unsigned long long*>(scratch + 64);
+    const StaticParts sp = static_parts(h, P::LPN * (int32_t)(sizeof(V) / policy_elem_bytes(h->policy)));
+    a.buf0 = reinterpret_cast<V*>(scratch + sp.buf0);
+    a.buf1 = reinterpret_cast<V*>(scratch + sp.buf1);
+    a.esum = reinterpret_cast<V*>(scratch + sp.esum);
+    a.tbuf = reinterpret_cast<V*>(scratch + sp.tbuf);
+    a.rv = reinterpret_cast<V*>(scratch + sp.rv);
+    a.status = reinterpret_cast<int32_t*>(scratch + sp.status);
+    a.bar = reinterpret_cast<unsigned long long*>(scratch + sp.status + 64);
     a.bar_base = 0;
-    a.rv = reinterpret_cast<V*>(scratch + 256);
-    a.buf0 = reinterpret_cast<V*>(scratch + 256 + rv_bytes);
-    a.buf1 = reinterpret_cast<V*>(scratch + 256 + rv_bytes + buf_bytes);
     a.inject = 0;
     // the array keeps the previous call's contents: start from a clear status
     // word and barrier counter
-    cuda_check(cudaMemsetAsync(scratch, 0, 256, st), "fixed scratch clear");
+    cuda_check(cudaMemsetAsync(scratch + sp.status, 0, 256, st), "fixed scratch clear");
     h->launches = launch_product<P>(h, a, st);
 }
 
@@ -674,25 +818,16 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         h->max_width = g.max_width();
         h->arena = static_cast<char*>(arena);
         h->lay = d;
-        int dev = 0;
-        cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
-        cuda_check(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
-        cuda_check(cudaDeviceGetAttribute(&h->coop, cudaDevAttrCooperativeLaunch, dev), "cooperative attribute");
-        // emit group: about one symbol per thread per pass, capped at a CTA
+        // emit: rows averaging 128 symbols or more are reduced level by level
+        // (emit_group 0); shorter rows by groups of about one lane per symbol
         const double avg = g.n > 0 ? (double)h->c_len / (double)g.n : 0.0;
-        if (avg >= 128) {
-            h->emit_group = 0;
-        } else {
-            int G = 1;
-            while (G < 32 && G < avg) G <<= 1;
-            h->emit_group = G;
-        }
+        int G = 1;
+        while (G < 32 && G < avg) G <<= 1;
+        h->emit_group = d.level_emit ? 0 : G;
         // levels narrow enough for one CTA finish the sweep there (when two or more)
         const int64_t L = g.L;
-        const int64_t tail_w = (policy == GC_F32_SUM && k_max == 16) ? Chunk<PolF32x16>::TAIL : Chunk<PolF32>::TAIL;
-        int64_t first_narrow = L + 1;
-        while (first_narrow > 1 && g.lvl_off[first_narrow] - g.lvl_off[first_narrow - 1] <= tail_w) --first_narrow;
-        h->grid_levels = (int)(L - first_narrow + 1 >= 2 ? first_narrow - 1 : L);
+        h->grid_levels = (int)d.grid_levels;
+        const std::vector<int64_t> toff = tail_offsets(g, d.grid_levels);
 
         // level table; level 1 with leaf codes, later levels with indices into [T | buffer]
         auto leaf_code = [&](int32_t p) { return (int32_t)(((int64_t)g.term_col[p] << d.vbits) | g.term_vidx[p]); };
@@ -701,7 +836,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             if (c == -1) return 0;
             return -c - 1;                         // terminal p = -c-2 -> T[p+1]
         };
-        h->lv.assign((size_t)(4 * (L + 2)), 0);
+        h->lv.assign((size_t)(LV_ROWS * (L + 2)), 0);
         std::vector<int32_t> nodes((size_t)(2 * d.n_nodes_padded), 0);
         int64_t start = 0;
         for (int64_t k = 1; k <= L; ++k) {
@@ -710,6 +845,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             h->lv[LV_W * (L + 2) + k] = w;
             h->lv[LV_ROOTS * (L + 2) + k] = g.lvl_roots[k];
             h->lv[LV_ROFF * (L + 2) + k] = g.root_off[k];
+            h->lv[LV_TOFF * (L + 2) + k] = toff[k];
             for (int64_t q = 0; q < w; ++q)
                 for (int t = 0; t < 2; ++t) {
                     const int32_t c = g.nodes[2 * (g.lvl_off[k] + q) + t];
@@ -720,11 +856,26 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         }
         std::vector<int32_t> leaf((size_t)g.alpha());
         for (int64_t p = 0; p < g.alpha(); ++p) leaf[p] = leaf_code((int32_t)p);
-        std::vector<int32_t> cref(g.c_ref.size());
-        for (size_t e = 0; e < cref.size(); ++e) cref[e] = ref(g.c_ref[e]);
-        std::vector<int32_t> co(g.slp.c_off.size());
-        for (size_t r = 0; r < co.size(); ++r) co[r] = (int32_t)g.slp.c_off[r];
+        EmitPlan plan;
+        std::vector<int32_t> cref, co;
+        if (d.level_emit) {
+            plan = plan_level_emit(g, d.TB, d.grid_levels);
+            if ((int64_t)plan.echunk.size() != 4 * d.n_echunks || (int64_t)plan.late_ref.size() != d.n_late)
+                fail(GC_ERR_INVALID_GRAMMAR, "emit plan does not match the layout");
+            validate_emit_plan(plan, g, d.TB, d.grid_levels);
+            for (int64_t k = 0; k <= L + 1; ++k) h->lv[LV_ECH * (L + 2) + k] = plan.ech[k];
+        } else {
+            cref.resize(g.c_ref.size());
+            for (size_t e = 0; e < cref.size(); ++e) cref[e] = ref(g.c_ref[e]);
+            co.resize(g.slp.c_off.size());
+            for (size_t r = 0; r < co.size(); ++r) co[r] = (int32_t)g.slp.c_off[r];
+        }
 
+        // every host-side array is built and checked; now the device
+        int dev = 0;
+        cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+        cuda_check(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+        cuda_check(cudaDeviceGetAttribute(&h->coop, cudaDevAttrCooperativeLaunch, dev), "cooperative attribute");
         char* a = h->arena;
         put(st, a, d.nodes, nodes.data(), nodes.size());
         put(st, a, d.levels, h->lv.data(), h->lv.size());
@@ -736,8 +887,16 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             put(st, a, d.V, v.data(), v.size());
         }
         put(st, a, d.leaf, leaf.data(), leaf.size());
-        put(st, a, d.c_off, co.data(), co.size());
-        put(st, a, d.c_ref, cref.data(), cref.size());
+        if (d.level_emit) {
+            put(st, a, d.cref, plan.cref.data(), plan.cref.size());
+            put(st, a, d.echunk, plan.echunk.data(), plan.echunk.size());
+            put(st, a, d.row_ech, plan.row_ech.data(), plan.row_ech.size());
+            put(st, a, d.late_off, plan.late_off.data(), plan.late_off.size());
+            put(st, a, d.late_ref, plan.late_ref.data(), plan.late_ref.size());
+        } else {
+            put(st, a, d.c_off, co.data(), co.size());
+            put(st, a, d.c_ref, cref.data(), cref.size());
+        }
         cuda_check(cudaMemsetAsync(a + d.status, 0, 256, st), "status clear");
         cuda_check(cudaStreamSynchronize(st), "upload synchronize");
         *out = h.release();
@@ -896,7 +1055,8 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
             case GC_BOOL_OR: run_product_static<PolOr>(h, x, y, st, scratch); break;
         }
         int32_t s = 0;
-        cuda_check(cudaMemcpyAsync(&s, scratch, 4, cudaMemcpyDeviceToHost, st), "fixed scratch status read");
+        cuda_check(cudaMemcpyAsync(&s, scratch + static_parts(h, k).status, 4, cudaMemcpyDeviceToHost, st),
+                   "fixed scratch status read");
         cuda_check(cudaStreamSynchronize(st), "stream synchronize");
         rc = (gc_status)s;
     });

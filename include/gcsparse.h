@@ -147,6 +147,25 @@ const char* gc_version(void);
 gc_status gc_build(int64_t n, int64_t m, const int64_t* row_ptr, const int32_t* col,
                    const float* val, const gc_build_opts* opts, gc_grammar** out);
 
+/*
+ * Streaming build in row blocks, for matrices too large to hand over as one
+ * CSR (Sec. 1: row blocks compressed separately). gc_builder_add_rows
+ * CSRV-encodes and RePair-compresses one block of rows [r0, r0 + rows) right
+ * away and keeps only its grammar; it may be called concurrently from several
+ * threads with different blocks. gc_builder_finish merges the blocks (one
+ * value dictionary, one terminal table, rules numbered block after block)
+ * and layers and packs the result like gc_build; it fails with GC_ERR_ARG
+ * unless the blocks cover [0, n) exactly once. The block CSR follows the
+ * gc_build rules with row_ptr[0] = 0. The builder is freed by
+ * gc_builder_free (also after finish).
+ */
+typedef struct gc_builder gc_builder;
+gc_status gc_builder_create(int64_t n, int64_t m, const gc_build_opts* opts, gc_builder** out);
+gc_status gc_builder_add_rows(gc_builder* b, int64_t r0, int64_t rows, const int64_t* row_ptr,
+                              const int32_t* col, const float* val);
+gc_status gc_builder_finish(gc_builder* b, gc_grammar** out);
+void gc_builder_free(gc_builder* b);
+
 /* Structural figures of a built grammar (Table 4.1's |R|, L, w*, +pt).      */
 gc_status gc_stats(const gc_grammar* g, gc_grammar_stats* out);
 

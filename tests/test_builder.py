@@ -172,6 +172,27 @@ def test_policy_value_checks(gcs):
         G.layout("or", 1)
 
 
+@pytest.mark.parametrize("k_max", [1, 16])
+def test_device_plans_pass_host_checks(gcs, k_max):
+    # gc_upload builds and checks every device array on the host (node codes,
+    # level-emit chunks, references into the narrow top levels) before its
+    # first CUDA call; without a GPU it must get that far and stop there
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU")
+    cfg = dict(gcsynth.GENO_MEDIUM, n=150, m=20000)
+    slice_ = gcs.Grammar(150, 20000, *gcsynth.genotype_csr(**cfg))         # level emit, with a tail
+    w = slice_.widths()
+    assert slice_.stats()["c_len"] >= 128 * 150 and w[-1] <= 1024 and w[-2] <= 1024
+    rp, c, v, _ = gcsynth.random_sparse(40, 3000, 0.4, [1.0, -1.0, 0.5], 8)
+    heavy = gcs.Grammar(40, 3000, rp, c, v)                                 # level emit, few levels
+    small = gcs.Grammar(1000, 2000, *gcsynth.genotype_csr(**gcsynth.GENO_SMALL))   # row emit
+    for G in (slice_, heavy, small):
+        lay = G.layout("f32", k_max)
+        with pytest.raises(gcs.GcError, match="GC_ERR_CUDA"):
+            gcs.capi.gc_upload(G._p, "f32", k_max, 256, lay["arena_bytes"])
+
+
 @pytest.mark.parametrize("bad", ["row_ptr", "col_range", "dup", "nan", "inf"])
 def test_bad_csr_is_rejected(gcs, bad):
     rp = np.array([0, 2, 3], dtype=np.int64)
@@ -242,3 +263,39 @@ def test_save_load_roundtrip(gcs, tmp_path):
         gcs.Grammar.load(p)
     with pytest.raises(gcs.GcError, match="GC_ERR_IO"):
         gcs.Grammar.load(str(tmp_path / "missing.bin"))
+
+
+@pytest.mark.parametrize("workers", [1, 3])
+def test_streaming_row_blocks_match_block_build(gcs, workers):
+    d = gcsynth.genotype_dense(n=130, m=300, founders=5, switch=0.01, mutation=0.005, seed=21)
+    rp, c, v = gcsynth.dense_to_csr(d)
+
+    def make_block(r0, r1):
+        return rp[r0:r1 + 1] - rp[r0], c[rp[r0]:rp[r1]], v[rp[r0]:rp[r1]]
+
+    S = gcs.Grammar.from_row_blocks(130, 300, 32, make_block, workers=workers)
+    B = gcs.Grammar(130, 300, rp, c, v, block_rows=32)
+    a, b = export_all(S), export_all(B)
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    st = S.stats()
+    assert st["n_blocks"] == 5 and st["nnz"] == rp[-1]
+    check_grammar(S, rp, c, v, 130, 300, 32)
+
+
+def test_streaming_builder_rejects_gaps_and_overlaps(gcs):
+    capi = gcs.capi
+    rp = np.array([0, 1], dtype=np.int64)
+    c = np.array([0], dtype=np.int32)
+    v = np.array([1.0], dtype=np.float32)
+    b = capi.gc_builder_create(3, 2)
+    try:
+        capi.gc_builder_add_rows(b, 0, rp, c, v)
+        with pytest.raises(gcs.GcError, match="overlap"):
+            capi.gc_builder_add_rows(b, 0, rp, c, v)
+        with pytest.raises(gcs.GcError, match="cover"):
+            capi.gc_builder_finish(b)
+        with pytest.raises(gcs.GcError, match="outside"):
+            capi.gc_builder_add_rows(b, 3, rp, c, v)
+    finally:
+        capi.gc_builder_free(b)

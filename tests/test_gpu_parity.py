@@ -202,7 +202,8 @@ def test_schedules_agree_bit_for_bit(gcs, torch):
     eng.schedule = "per_level"
     assert eng.schedule == "per_level"
     y_l = eng.matvec(x).cpu().numpy()
-    assert eng.launch_count() == G.stats()["depth"] + 1
+    # one kernel per level, then the emit (one kernel, or chunks + row sums)
+    assert G.stats()["depth"] + 1 <= eng.launch_count() <= G.stats()["depth"] + 2
     Y_l = eng.matvec(X).cpu().numpy()
     np.testing.assert_array_equal(y_p, y_l)
     np.testing.assert_array_equal(Y_p, Y_l)
