@@ -56,7 +56,7 @@ struct gc_handle {
     char* arena = nullptr;
     gcs::DevLayout lay{};
     int sms = 1;
-    int emit_group = 32;          // row emit: threads per row; 0 = level emit
+    int emit_group = 32;          // row emit: threads per row (0 in the chunked emits)
     int schedule = 0;             // 0 persistent (if cooperative launch works), 1 per level
     int coop = 0;                 // device supports cooperative launch
     int grid_levels = 0;          // levels 1..grid_levels use the whole grid
@@ -71,7 +71,10 @@ namespace {
 
 constexpr int kThreads = 512;        // every kernel: 16 warps
 constexpr int kWarps = kThreads / 32;
-constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3, LV_ECH = 4, LV_TOFF = 5, LV_ROWS = 6;
+constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3, LV_ECH = 4, LV_TOFF = 5;
+constexpr int LV_ROWS = (int)kLevelRows;
+static_assert(LV_TOFF < LV_ROWS, "level table rows");
+
 
 void cuda_check(cudaError_t e, const char* what) {
     if (e != cudaSuccess) fail(GC_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
@@ -97,6 +100,8 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
     return v;
 }
 __device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ uint64_t l2_evict_last() {
     uint64_t pol;
@@ -154,8 +159,10 @@ struct SweepArgs {
     const int32_t* late_ref;
     V* esum;                  //   chunk sums
     V* tbuf;                  // the narrow top levels' values, level after level
+    int64_t tail_total;       // nodes of the tail levels (padded)
     int64_t n;
-    int32_t emit_group;       // 0: level emit; G: row emit with G lanes per row
+    int32_t emode;            // EmitMode
+    int32_t emit_group;       // row emit: G lanes per row
     int32_t* status;
     unsigned long long* bar;
     unsigned long long bar_base;
@@ -184,7 +191,7 @@ __device__ void write_leaf_tables(const SweepArgs<P>& a, int64_t tid, int64_t nt
         const V v = p == 0 ? P::identity() : leaf_value<P>(__ldg(a.leaf + (p - 1)), part, a);
         a.buf0[i] = v;
         a.buf1[i] = v;
-        if (a.emit_group != 0) a.rv[i] = v;   // RV exists in the row emit only
+        if (a.emode != EMIT_LEVEL) a.rv[i] = v;   // RV exists in the chunk and row emits
     }
 }
 
@@ -259,7 +266,7 @@ __device__ __forceinline__ LevelIO<P> level_io(const SweepArgs<P>& a, int k) {
     LevelIO<P> io;
     io.prev = (k & 1) ? a.buf0 : a.buf1;
     io.cur = ((k & 1) ? a.buf1 : a.buf0) + a.TB * P::LPN;
-    io.rv = a.emit_group != 0 ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;
+    io.rv = a.emode != EMIT_LEVEL ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;
     return io;
 }
 
@@ -274,12 +281,12 @@ struct TailIO {
     typename P::V* rv;
 };
 template <class P>
-__device__ __forceinline__ TailIO<P> tail_io(const SweepArgs<P>& a, int k) {
+__device__ __forceinline__ TailIO<P> tail_io(const SweepArgs<P>& a, int k, typename P::V* tb) {
     TailIO<P> io;
     io.prev = (k & 1) ? a.buf0 : a.buf1;
-    io.prev_tail = k - 1 > a.grid_levels ? a.tbuf + a.lvl(LV_TOFF, k - 1) * P::LPN : nullptr;
-    io.cur = a.tbuf + a.lvl(LV_TOFF, k) * P::LPN;
-    io.rv = a.emit_group != 0 ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;
+    io.prev_tail = k - 1 > a.grid_levels ? tb + a.lvl(LV_TOFF, k - 1) * P::LPN : nullptr;
+    io.cur = tb + a.lvl(LV_TOFF, k) * P::LPN;
+    io.rv = a.emode == EMIT_ROWS ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;   // late refs read tbuf
     return io;
 }
 
@@ -323,18 +330,16 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
     }
 }
 
-// Level emit: chunk j holds references cref[start .. start+len) of one
-// (level, row), len <= kEmitChunk. A warp takes 32/LPN references at a time,
-// LPN lanes each; lane (slot, part) sums part `part` of references slot,
-// slot + 32/LPN, ... in order, the warp reduces the slots by a fixed
-// butterfly, and the sum goes to esum[id]. base is the [T | level] index space
-// of the chunk's level; with tb, level references past T come from that tail
-// buffer instead.
+// Level and chunk emit: chunk j holds references cref[start .. start+len) of
+// one row (and one level, in the level emit), len <= kEmitChunk. A warp takes
+// 32/LPN references at a time, LPN lanes each; lane (slot, part) sums part
+// `part` of references slot, slot + 32/LPN, ... in order, the warp reduces the
+// slots by a fixed butterfly, and the sum goes to esum[id]. base is the index
+// space of the references: [T | level buffer] or [T | RV].
 constexpr int kEmitChunk = (int)kEmitChunkSyms;
 
 template <class P>
-__device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, const typename P::V* base,
-                                           const typename P::V* tb) {
+__device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, const typename P::V* base) {
     using V = typename P::V;
     constexpr int NS = 32 / P::LPN;            // reference slots per warp row
     constexpr int PER = kEmitChunk / NS;       // references per lane
@@ -355,8 +360,7 @@ __device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, con
         V v[B];
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            const int64_t c = r[u];
-            v[u] = (tb != nullptr && c >= a.TB) ? tb[(c - a.TB) * P::LPN + part] : base[c * P::LPN + part];
+            v[u] = base[(int64_t)r[u] * P::LPN + part];
         }
 #pragma unroll
         for (int u = 0; u < B; ++u) acc = P::combine(acc, v[u]);
@@ -366,13 +370,57 @@ __device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, con
     if (slot == 0) a.esum[(int64_t)ch.z * P::LPN + part] = acc;
 }
 
-// The chunks of level k (0 = bare terminals), spread over warps gwarp, gwarp +
-// nwarps, ...
+// Chunks j0 <= j < j1, spread over warps gwarp, gwarp + nwarps, ... For
+// one-lane 4-byte values a warp overlaps its chunks: it issues the current chunk's
+// gathers, then the next chunk's references and the header after that, and
+// only then waits; each chunk is reduced exactly as emit_chunk does.
 template <class P>
-__device__ void emit_level(const SweepArgs<P>& a, int k, const typename P::V* base, const typename P::V* tb,
-                           int64_t gwarp, int64_t nwarps) {
-    const int64_t j1 = a.lvl(LV_ECH, k + 1);
-    for (int64_t j = a.lvl(LV_ECH, k) + gwarp; j < j1; j += nwarps) emit_chunk<P>(a, j, base, tb);
+__device__ void emit_chunks(const SweepArgs<P>& a, int64_t j0, int64_t j1, const typename P::V* base, int64_t gwarp,
+                            int64_t nwarps) {
+    using V = typename P::V;
+    if constexpr (P::LPN != 1 || sizeof(V) != 4) {
+        for (int64_t j = j0 + gwarp; j < j1; j += nwarps) emit_chunk<P>(a, j, base);
+    } else {
+        constexpr int PER = kEmitChunk / 32;
+        const int lane = threadIdx.x & 31;
+        int64_t j = j0 + gwarp;
+        if (j >= j1) return;
+        auto refs = [&](const int4& ch, int32_t (&r)[PER]) {
+#pragma unroll
+            for (int u = 0; u < PER; ++u) r[u] = u * 32 + lane < ch.y ? __ldcs(a.cref + ch.x + u * 32 + lane) : 0;
+        };
+        int4 ch = __ldg(a.echunk + j);
+        int32_t r[PER];
+        refs(ch, r);
+        int4 chn = j + nwarps < j1 ? __ldg(a.echunk + j + nwarps) : make_int4(0, 0, 0, 0);
+        for (;;) {
+            V v[PER];
+#pragma unroll
+            for (int u = 0; u < PER; ++u) v[u] = base[r[u]];
+            const int64_t jn = j + nwarps;
+            int4 chnn = make_int4(0, 0, 0, 0);
+            if (jn < j1) {
+                refs(chn, r);
+                if (jn + nwarps < j1) chnn = __ldg(a.echunk + jn + nwarps);
+            }
+            V acc = P::identity();
+#pragma unroll
+            for (int u = 0; u < PER; ++u) acc = P::combine(acc, v[u]);
+#pragma unroll
+            for (int msk = 16; msk >= 1; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
+            if (lane == 0) a.esum[ch.z] = acc;
+            if (jn >= j1) break;
+            j = jn;
+            ch = chn;
+            chn = chnn;
+        }
+    }
+}
+
+// The chunks of level k (0 = bare terminals).
+template <class P>
+__device__ void emit_level(const SweepArgs<P>& a, int k, const typename P::V* base, int64_t gwarp, int64_t nwarps) {
+    emit_chunks<P>(a, a.lvl(LV_ECH, k), a.lvl(LV_ECH, k + 1), base, gwarp, nwarps);
 }
 
 // y[r] = row r's chunk sums added in chunk-id order, then its references into
@@ -456,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const uint64_t keep = l2_evict_last();
+    const bool tail = Lg < a.L;
+    const bool tail_cta = tail && blockIdx.x == 0;
     auto nchunks = [&](int k) { return (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES; };
     auto norm = [&](int& k, int64_t& c) {
         while (k <= Lg && c >= nchunks(k)) {
@@ -464,8 +514,15 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
         }
     };
 
+    // CTA 0 asks L2 for the tail's node pairs (levels Lg+1..L, contiguous at
+    // the end of the node array) while the grid sweeps the wide levels
+    if (tail_cta) {
+        const int2* src = a.nodes + a.lvl(LV_START, Lg + 1);
+        for (int64_t i = (int64_t)threadIdx.x * 16; i < a.tail_total; i += (int64_t)kThreads * 16) prefetch_l2(src + i);
+    }
+
     write_leaf_tables<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
-    const bool lemit = a.emit_group == 0;
+    const bool lemit = a.emode == EMIT_LEVEL;
 
     int kn = 1;
     int64_t cn = gw;
@@ -487,23 +544,28 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
             combine_chunk<P, false>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
         }
         if (lemit && k >= 2) {   // level k-1 is complete and still in its buffer
-            emit_level<P>(a, k - 1, io.prev, nullptr, gw, GW);
-            if (k == 2) emit_level<P>(a, 0, a.buf0, nullptr, gw, GW);
+            emit_level<P>(a, k - 1, io.prev, gw, GW);
+            if (k == 2) emit_level<P>(a, 0, a.buf0, gw, GW);
         }
     }
     if (!grid_sync(a, nbar++)) return;
-    // what is left of the level emit: level Lg, and the terminals if no phase took them
-    const bool tail = Lg < a.L;
-    const int64_t skip = (tail && gridDim.x > 1) ? kWarps : 0;   // CTA 0 runs the tail
-    if (lemit && gw >= skip) {
-        if (Lg >= 1) emit_level<P>(a, Lg, (Lg & 1) ? a.buf1 : a.buf0, nullptr, gw - skip, GW - skip);
-        if (Lg < 2) emit_level<P>(a, 0, a.buf0, nullptr, gw - skip, GW - skip);
+    // while CTA 0 runs the tail, the others reduce what is left of the level
+    // emit (level Lg, and the terminals if no phase took them), or of the
+    // chunk emit
+    const int64_t skip = (tail && gridDim.x > 1) ? kWarps : 0;
+    if (gw >= skip) {
+        if (lemit) {
+            if (Lg >= 1) emit_level<P>(a, Lg, (Lg & 1) ? a.buf1 : a.buf0, gw - skip, GW - skip);
+            if (Lg < 2) emit_level<P>(a, 0, a.buf0, gw - skip, GW - skip);
+        } else if (a.emode == EMIT_CHUNK) {
+            emit_level<P>(a, 0, a.rv, gw - skip, GW - skip);
+        }
     }
     // narrow top levels: CTA 0 alone, block barriers only, into the tail buffer
-    if (tail && blockIdx.x == 0) {
+    if (tail_cta) {
         const int w0 = threadIdx.x >> 5;
         for (int k = Lg + 1; k <= a.L; ++k) {
-            const TailIO<P> io = tail_io<P>(a, k);
+            const TailIO<P> io = tail_io<P>(a, k, a.tbuf);
             for (int64_t c = w0; c < nchunks(k); c += kWarps) {
                 int2 ab[Chunk<P>::U];
                 load_chunk<P>(a, k, c, ab);
@@ -513,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
         }
     }
     if (!grid_sync(a, nbar++)) return;
-    if (lemit) emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    if (a.emode != EMIT_ROWS) emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
     else emit_rows<P>(a, blockIdx.x, gridDim.x);
 }
 
@@ -528,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a
     const int64_t nc = (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES;
     const bool tail = k > a.grid_levels;
     const LevelIO<P> io = level_io<P>(a, k);
-    const TailIO<P> tio = tail_io<P>(a, k);
+    const TailIO<P> tio = tail_io<P>(a, k, a.tbuf);
     int2 nab[Chunk<P>::U];
     if (gw < nc) load_chunk<P>(a, k, gw, nab);
     for (int64_t c = gw; c < nc; c += GW) {
@@ -540,23 +602,26 @@ __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a
         else combine_chunk<P, false>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
     }
     // level k-1 (a wide one) is complete and still in its buffer
-    if (a.emit_group == 0 && k >= 2) {
-        if (k - 1 <= a.grid_levels) emit_level<P>(a, k - 1, io.prev, nullptr, gw, GW);
-        if (k == 2) emit_level<P>(a, 0, a.buf0, nullptr, gw, GW);
+    if (a.emode == EMIT_LEVEL && k >= 2) {
+        if (k - 1 <= a.grid_levels) emit_level<P>(a, k - 1, io.prev, gw, GW);
+        if (k == 2) emit_level<P>(a, 0, a.buf0, gw, GW);
     }
 }
 
 // phase 0: what is left of the level emit (level L when it is a wide one,
-// terminals if L < 2), or the whole row emit; phase 1: the level emit's row sums
+// terminals if L < 2), every chunk of the chunk emit, or the whole row emit;
+// phase 1: the chunked emits' row sums
 template <class P>
-__global__ void __launch_bounds__(kThreads, 2) emit_kernel(const SweepArgs<P> a, int phase) {
+__global__ void __launch_bounds__(kThreads, 1) emit_kernel(const SweepArgs<P> a, int phase) {
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (a.emit_group != 0) {
+    if (a.emode == EMIT_ROWS) {
         emit_rows<P>(a, blockIdx.x, gridDim.x);
+    } else if (phase == 0 && a.emode == EMIT_CHUNK) {
+        emit_level<P>(a, 0, a.rv, gw, GW);
     } else if (phase == 0) {
-        if (a.L >= 1 && a.grid_levels == a.L) emit_level<P>(a, a.L, (a.L & 1) ? a.buf1 : a.buf0, nullptr, gw, GW);
-        if (a.L < 2) emit_level<P>(a, 0, a.buf0, nullptr, gw, GW);
+        if (a.L >= 1 && a.grid_levels == a.L) emit_level<P>(a, a.L, (a.L & 1) ? a.buf1 : a.buf0, gw, GW);
+        if (a.L < 2) emit_level<P>(a, 0, a.buf0, gw, GW);
     } else {
         emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
     }
@@ -615,7 +680,9 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.late_ref = reinterpret_cast<const int32_t*>(ar + d.late_ref);
     a.esum = reinterpret_cast<V*>(ar + d.esum);
     a.tbuf = reinterpret_cast<V*>(ar + d.tbuf);
+    a.tail_total = d.tail_total;
     a.n = h->n;
+    a.emode = d.emit;
     a.emit_group = h->emit_group;
     a.status = reinterpret_cast<int32_t*>(ar + d.status);
     a.bar = reinterpret_cast<unsigned long long*>(ar + d.status + 64);
@@ -662,7 +729,7 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, int
             level_kernel<P><<<grid_for(w, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, k);
             ++launches;
         }
-        if (h->n > 0 && h->emit_group != 0) {
+        if (h->n > 0 && h->lay.emit == EMIT_ROWS) {
             emit_kernel<P><<<grid_for(h->n, kWarps * (32 / h->emit_group), h->sms, 4), kThreads, 0, st>>>(a, 0);
             ++launches;
         } else if (h->n > 0) {
@@ -755,8 +822,8 @@ StaticParts static_parts(const gc_handle* h, int32_t k) {
     s.buf0 = take(vb * (d.TB + h->max_width));
     s.buf1 = take(vb * (d.TB + h->max_width));
     s.tbuf = take(vb * d.tail_total);
-    if (d.level_emit) s.esum = take(vb * d.n_echunks);
-    else s.rv = take(vb * (d.TB + h->n_roots));
+    if (d.chunked()) s.esum = take(vb * d.n_echunks);
+    if (d.has_rv()) s.rv = take(vb * (d.TB + h->n_roots));
     s.status = take(256);
     s.total = o;
     return s;
@@ -818,12 +885,11 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         h->max_width = g.max_width();
         h->arena = static_cast<char*>(arena);
         h->lay = d;
-        // emit: rows averaging 128 symbols or more are reduced level by level
-        // (emit_group 0); shorter rows by groups of about one lane per symbol
+        // row emit: groups of about one lane per symbol (rows average < 128)
         const double avg = g.n > 0 ? (double)h->c_len / (double)g.n : 0.0;
         int G = 1;
         while (G < 32 && G < avg) G <<= 1;
-        h->emit_group = d.level_emit ? 0 : G;
+        h->emit_group = d.emit == EMIT_ROWS ? G : 0;
         // levels narrow enough for one CTA finish the sweep there (when two or more)
         const int64_t L = g.L;
         h->grid_levels = (int)d.grid_levels;
@@ -858,11 +924,12 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         for (int64_t p = 0; p < g.alpha(); ++p) leaf[p] = leaf_code((int32_t)p);
         EmitPlan plan;
         std::vector<int32_t> cref, co;
-        if (d.level_emit) {
-            plan = plan_level_emit(g, d.TB, d.grid_levels);
+        if (d.chunked()) {
+            const bool by_level = d.emit == EMIT_LEVEL;
+            plan = plan_emit(g, d.TB, d.grid_levels, by_level);
             if ((int64_t)plan.echunk.size() != 4 * d.n_echunks || (int64_t)plan.late_ref.size() != d.n_late)
                 fail(GC_ERR_INVALID_GRAMMAR, "emit plan does not match the layout");
-            validate_emit_plan(plan, g, d.TB, d.grid_levels);
+            validate_emit_plan(plan, g, d.TB, d.grid_levels, by_level);
             for (int64_t k = 0; k <= L + 1; ++k) h->lv[LV_ECH * (L + 2) + k] = plan.ech[k];
         } else {
             cref.resize(g.c_ref.size());
@@ -887,7 +954,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             put(st, a, d.V, v.data(), v.size());
         }
         put(st, a, d.leaf, leaf.data(), leaf.size());
-        if (d.level_emit) {
+        if (d.chunked()) {
             put(st, a, d.cref, plan.cref.data(), plan.cref.size());
             put(st, a, d.echunk, plan.echunk.data(), plan.echunk.size());
             put(st, a, d.row_ech, plan.row_ech.data(), plan.row_ech.size());

@@ -9,8 +9,9 @@
 //                                 offset in the tail buffer
 //                       V         policy[|V|]      value dictionary
 //                       leaf      int32[alpha]     leaf code of terminal p
-//     level emit:       cref      int32[|C|]       C grouped by the level of its
-//                                                  symbol, then by row (wide levels)
+//     level / chunk     cref      int32[early]     C without the references to
+//     emit:                                        the tail levels: by level, then
+//                                                  row (level emit); by row (chunk)
 //                       echunk    int4[chunks]     (start, length, id, 0) per chunk
 //                       row_ech   int32[n+1]       row r's chunk ids
 //                       late_off  int32[n+1]       row r's references into the
@@ -21,8 +22,8 @@
 //                       buf1X     value[TB + w*]   values (the two streaming buffers)
 //                       tbuf      value[tail]      the narrow top levels' values,
 //                                                  level after level
-//     level emit:       esum      value[chunks]    chunk sums
-//     row emit:         RVX       value[TB + rho]  leaf table T, then root values
+//     level / chunk:    esum      value[chunks]    chunk sums
+//     chunk / row:      RVX       value[TB + rho]  leaf table T, then root values
 //                       status    256 B            status word, fixpoint flag,
 //                                                  grid-barrier arrival counter
 //   staging             xs        value[m]         x / y copies for the
@@ -44,16 +45,22 @@
 // (each at most tail_nodes wide, two or more of them) form the tail, computed
 // by one CTA into the tail buffer, where they all stay until the product ends.
 //
-// Emit modes (Lemma 2.2, y[r] = sum of row r's symbols of C):
-//   level emit  rows of C average 128 symbols or more. The references to
-//               terminals and wide levels are grouped by level, then row;
-//               chunks of at most 512 references of one (level, row) are
-//               reduced right after their level is computed, straight from
-//               that level's buffer (the pages' emit on the spot). A last pass
-//               adds each row's chunk sums in order, then its references into
-//               the tail, which are few.
-//   row emit    shorter rows: roots are also stored to RV when their level is
-//               computed, and rows are reduced at the end, a few lanes per row.
+// Emit modes (Lemma 2.2, y[r] = sum of row r's symbols of C). C's references
+// to the tail levels ("late" references, few) are kept per row and added by
+// the last pass, from the tail buffer; the others are "early" references.
+//   level emit  rows of C average 128 symbols or more, 16-wide values. Early
+//               references are grouped by level, then row; chunks of at most
+//               512 references of one (level, row) are reduced right after
+//               their level is computed, straight from that level's buffer
+//               (the pages' emit on the spot). A last pass adds each row's
+//               chunk sums in order, then its late references.
+//   chunk emit  rows average 128 symbols or more, one-wide values: roots are
+//               also stored to RV when their level is computed (RV stays in
+//               L2), and the early references, in row order and cut into
+//               chunks of at most 512 of one row, are reduced from RV while
+//               one CTA computes the tail levels; a last pass as above.
+//   row emit    shorter rows: roots are stored to RV, and rows are reduced at
+//               the end, a few lanes per row.
 #pragma once
 
 #include "common.hpp"
@@ -62,11 +69,14 @@ namespace gcs {
 
 constexpr int64_t kNodeAlign = 16;        // nodes per 128-byte granule
 constexpr int64_t kEmitChunkSyms = 512;   // references per emit chunk
-constexpr int64_t kLevelEmitMinAvg = 128; // average |C| per row for the level emit
+constexpr int64_t kLongRowAvg = 128;      // average |C| per row for chunked emits
+constexpr int64_t kLevelRows = 6;         // rows of the level table
+
+enum EmitMode : int32_t { EMIT_LEVEL = 0, EMIT_CHUNK = 1, EMIT_ROWS = 2 };
 
 struct DevLayout {
     int64_t nodes, levels, V, leaf;
-    int64_t cref, echunk, row_ech;        // level emit
+    int64_t cref, echunk, row_ech;        // level and chunk emit
     int64_t late_off, late_ref;
     int64_t c_off, c_ref;                 // row emit
     int64_t buf0, buf1, esum, tbuf, RV, status, xs, ys;
@@ -79,7 +89,10 @@ struct DevLayout {
     int64_t tail_total;    // nodes of the tail buffer (levels Lg+1..L, padded)
     int64_t TB;            // leaf-table block length in values
     int32_t vbits;         // bits of the value index inside a leaf code
-    bool level_emit;
+    EmitMode emit;
+
+    bool chunked() const { return emit != EMIT_ROWS; }
+    bool has_rv() const { return emit != EMIT_LEVEL; }
 };
 
 inline int64_t policy_elem_bytes(gc_policy p) { return p == GC_F32_SUM ? 4 : 8; }
@@ -96,8 +109,9 @@ inline int32_t value_bits(int64_t n_values) {
 
 inline int64_t leaf_block(int64_t alpha) { return (alpha + 1 + 63) / 64 * 64; }
 
-inline bool uses_level_emit(const Grammar& g) {
-    return g.n > 0 && (int64_t)g.c_ref.size() >= kLevelEmitMinAvg * g.n;
+inline EmitMode emit_mode(const Grammar& g, int32_t k_max) {
+    const bool long_rows = g.n > 0 && (int64_t)g.c_ref.size() >= kLongRowAvg * g.n;
+    return !long_rows ? EMIT_ROWS : k_max == 1 ? EMIT_CHUNK : EMIT_LEVEL;
 }
 
 inline int64_t tail_width(int32_t k_max) { return k_max == 16 ? 1024 : 4096; }
@@ -123,10 +137,11 @@ inline std::vector<int64_t> tail_offsets(const Grammar& g, int64_t Lg) {
     return t;
 }
 
-// Level of the symbol behind each packed C reference (0 for a terminal), its
-// index in that level's [T | buffer] space, and the per-level, per-row chunks
-// of the references to levels 0..Lg; references to the tail levels are kept
-// per row as tail-buffer indices.
+// Chunks of C's early references (terminals and levels 1..Lg): with by_level,
+// grouped by the level of their symbol and indexed into that level's
+// [T | buffer] space, in chunks of one (level, row); otherwise in row order,
+// indexed into [T | RV], in chunks of one row (all in group 0). References to
+// the tail levels are kept per row as tail-buffer indices.
 struct EmitPlan {
     std::vector<int32_t> cref;      // grouped by (level, row), as [T | buffer] indices
     std::vector<int32_t> echunk;    // 4 per chunk: start, length, id, 0 (level-major)
@@ -143,23 +158,25 @@ inline int64_t ref_level(const Grammar& g, int32_t c) {
            g.root_off.begin() - 1;
 }
 
-inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
+inline EmitPlan plan_emit(const Grammar& g, int64_t TB, int64_t Lg, bool by_level) {
     const int64_t L = g.L, n = g.n;
     const std::vector<int64_t>& co = g.slp.c_off;
     const std::vector<int64_t> toff = tail_offsets(g, Lg);
     const size_t C = g.c_ref.size();
     std::vector<int32_t> lev(C), pos(C);
+    std::vector<char> early(C);
     EmitPlan p;
     p.late_off.assign((size_t)n + 1, 0);
     for (int64_t r = 0; r < n; ++r) {
         for (int64_t e = co[r]; e < co[r + 1]; ++e) {
             const int32_t c = g.c_ref[e];
             const int64_t k = ref_level(g, c);
-            lev[e] = (int32_t)k;
+            early[e] = k <= Lg;
+            lev[e] = by_level ? (int32_t)k : 0;
             if (c < 0) {
                 pos[e] = -c - 1;   // terminal p = -c-2 -> T[p+1]
             } else if (k <= Lg) {
-                pos[e] = (int32_t)(TB + c - g.root_off[k]);
+                pos[e] = (int32_t)(by_level ? TB + c - g.root_off[k] : TB + c);
             } else {
                 p.late_ref.push_back((int32_t)(toff[k] + c - g.root_off[k]));
             }
@@ -169,14 +186,14 @@ inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
     // counting sort of the wide references by level, stable in row-major order
     std::vector<int64_t> cnt((size_t)Lg + 2, 0);
     for (size_t e = 0; e < C; ++e)
-        if (lev[e] <= Lg) ++cnt[lev[e] + 1];
+        if (early[e]) ++cnt[lev[e] + 1];
     for (int64_t k = 0; k <= Lg; ++k) cnt[k + 1] += cnt[k];
     p.cref.resize((size_t)cnt[Lg + 1]);
     std::vector<int64_t> at(cnt.begin(), cnt.end() - 1);
     std::vector<int32_t> row_of(p.cref.size());
     for (int64_t r = 0; r < n; ++r)
         for (int64_t e = co[r]; e < co[r + 1]; ++e) {
-            if (lev[e] > Lg) continue;
+            if (!early[e]) continue;
             const int64_t d = at[lev[e]]++;
             p.cref[d] = pos[e];
             row_of[d] = (int32_t)r;
@@ -221,7 +238,7 @@ inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
 // chunk lies inside cref and holds references of its own level only (T for
 // level 0, that level's roots otherwise), chunk ids are a permutation that
 // row_ech splits by row, and every tail reference lies inside the tail buffer.
-inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, int64_t Lg) {
+inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, int64_t Lg, bool by_level) {
     const int64_t n = g.n, L = g.L, nch = (int64_t)p.echunk.size() / 4;
     const std::vector<int64_t> toff = tail_offsets(g, Lg);
     auto bad = [](const char* what) { fail(GC_ERR_INVALID_GRAMMAR, std::string("emit plan: ") + what); };
@@ -231,15 +248,20 @@ inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, 
         bad("tail reference ranges");
     std::vector<char> seen((size_t)nch, 0);
     for (int64_t k = 0; k <= L; ++k) {
-        if (p.ech[k + 1] < p.ech[k] || (k > Lg && p.ech[k + 1] != p.ech[k])) bad("level chunk ranges");
-        const int64_t lo = k == 0 ? 0 : TB, hi = k == 0 ? g.alpha() + 1 : TB + g.lvl_roots[k];
+        if (p.ech[k + 1] < p.ech[k] || ((k > Lg || (!by_level && k > 0)) && p.ech[k + 1] != p.ech[k]))
+            bad("level chunk ranges");
+        // terminals (level 0), one level's roots (by level), or terminals and
+        // the roots of levels 1..Lg in RV (row order)
+        const int64_t t_hi = k == 0 ? g.alpha() + 1 : 0;
+        const int64_t r_hi = TB + (!by_level ? g.root_off[Lg + 1] : k == 0 ? 0 : g.lvl_roots[k]);
+        auto ok = [&](int64_t v) { return (v >= 0 && v < t_hi) || (v >= TB && v < r_hi); };
         for (int64_t j = p.ech[k]; j < p.ech[k + 1]; ++j) {
             const int64_t st = p.echunk[4 * j], len = p.echunk[4 * j + 1], id = p.echunk[4 * j + 2];
             if (st < 0 || len < 1 || len > kEmitChunkSyms || st + len > (int64_t)p.cref.size()) bad("chunk extent");
             if (id < 0 || id >= nch || seen[id]) bad("chunk ids");
             seen[id] = 1;
             for (int64_t e = st; e < st + len; ++e)
-                if (p.cref[e] < lo || p.cref[e] >= hi) bad("reference outside its level");
+                if (!ok(p.cref[e])) bad("reference outside its level");
         }
     }
     for (int64_t r = 0; r < n; ++r)
@@ -248,12 +270,12 @@ inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, 
         if (t < 0 || t >= toff[L + 1]) bad("tail reference outside the tail buffer");
 }
 
-// Sizes of plan_level_emit's arrays, counted without building the plan:
+// Sizes of plan_emit's arrays, counted without building the plan:
 // chunks, wide references and tail references.
 struct EmitCounts {
     int64_t chunks = 0, wide = 0, late = 0;
 };
-inline EmitCounts count_level_emit(const Grammar& g, int64_t Lg) {
+inline EmitCounts count_emit(const Grammar& g, int64_t Lg, bool by_level) {
     const int64_t n = g.n;
     const std::vector<int64_t>& co = g.slp.c_off;
     std::vector<int64_t> per((size_t)Lg + 1, 0);
@@ -262,8 +284,8 @@ inline EmitCounts count_level_emit(const Grammar& g, int64_t Lg) {
         std::fill(per.begin(), per.end(), 0);
         for (int64_t e = co[r]; e < co[r + 1]; ++e) {
             const int64_t k = ref_level(g, g.c_ref[e]);
-            if (k <= Lg) ++per[k];
-            else ++t.late;
+            if (k > Lg) ++t.late;
+            else ++per[by_level ? k : 0];
         }
         for (int64_t k = 0; k <= Lg; ++k) {
             t.chunks += (per[k] + kEmitChunkSyms - 1) / kEmitChunkSyms;
@@ -279,14 +301,14 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.value_bytes = policy_elem_bytes(p) * k_max;
     d.vbits = value_bits((int64_t)g.V.size());
     d.TB = leaf_block(A);
-    d.level_emit = uses_level_emit(g);
+    d.emit = emit_mode(g, k_max);
     d.tail_nodes = tail_width(k_max);
     d.grid_levels = grid_level_count(g, d.tail_nodes);
     d.tail_total = tail_offsets(g, d.grid_levels)[L + 1];
     d.n_nodes_padded = 0;
     for (int64_t k = 1; k <= L; ++k) d.n_nodes_padded += pad_nodes(g.lvl_off[k + 1] - g.lvl_off[k]);
     EmitCounts ec;
-    if (d.level_emit) ec = count_level_emit(g, d.grid_levels);
+    if (d.chunked()) ec = count_emit(g, d.grid_levels, d.emit == EMIT_LEVEL);
     d.n_echunks = ec.chunks;
     d.n_late = ec.late;
     int64_t o = 0;
@@ -296,10 +318,10 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
         return at;
     };
     d.nodes = take(8 * d.n_nodes_padded);
-    d.levels = take(8 * 6 * (L + 2));
+    d.levels = take(8 * kLevelRows * (L + 2));
     d.V = take(policy_elem_bytes(p) * std::max<int64_t>(1, (int64_t)g.V.size()));
     d.leaf = take(4 * A);
-    if (d.level_emit) {
+    if (d.chunked()) {
         d.cref = take(4 * ec.wide);
         d.echunk = take(16 * d.n_echunks);
         d.row_ech = take(4 * (g.n + 1));
@@ -314,8 +336,8 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.buf0 = take(d.value_bytes * (d.TB + w));
     d.buf1 = take(d.value_bytes * (d.TB + w));
     d.tbuf = take(d.value_bytes * d.tail_total);
-    if (d.level_emit) d.esum = take(d.value_bytes * d.n_echunks);
-    else d.RV = take(d.value_bytes * (d.TB + g.n_roots));
+    if (d.chunked()) d.esum = take(d.value_bytes * d.n_echunks);
+    if (d.has_rv()) d.RV = take(d.value_bytes * (d.TB + g.n_roots));
     d.status = take(256);
     d.scratch_bytes = o - d.grammar_bytes;
     d.xs = take(d.value_bytes * g.m);
