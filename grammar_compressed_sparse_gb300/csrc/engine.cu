@@ -132,6 +132,11 @@ __device__ __forceinline__ unsigned long long shfl_x(unsigned long long v, int m
 __device__ __forceinline__ float4 shfl_x(float4 v, int m) {
     return make_float4(shfl_x(v.x, m), shfl_x(v.y, m), shfl_x(v.z, m), shfl_x(v.w, m));
 }
+__device__ __forceinline__ float shfl_up(float v, int d) { return __shfl_up_sync(0xffffffffu, v, d); }
+__device__ __forceinline__ long long shfl_up(long long v, int d) { return __shfl_up_sync(0xffffffffu, v, d); }
+__device__ __forceinline__ unsigned long long shfl_up(unsigned long long v, int d) {
+    return __shfl_up_sync(0xffffffffu, v, d);
+}
 
 // ---------------------------------------------------------------- arguments
 template <class P>
@@ -154,7 +159,15 @@ struct SweepArgs {
     const int32_t* c_ref;
     const int4* echunk;       // level emit: (start, length, id, 0) per chunk
     const int32_t* cref;      //   C grouped by level, then row
-    const int32_t* row_ech;   //   row r's chunk ids
+    const uint4* sref;        // slice emit: offsets into slices of [T | RV], 256 a tile
+    const uint8_t* sflag;     //   segment starts, one bit per reference
+    const int32_t* tile_sid;  //   first segment start of each tile
+    const int32_t* row_pos;   //   segment start of each of a row's sums (nullptr: level emit)
+    const int32_t* sx0;       //   first value of each slice
+    const int32_t* stile;     //   tile range of each slice
+    const int32_t* sorder;    //   slices, heaviest first
+    int64_t slice, nslices;   //   most values a slice holds, slices
+    const int32_t* row_ech;   // level / slice emit: row r's chunk / segment ids
     const int32_t* late_off;  //   row r's references into the tail levels
     const int32_t* late_ref;
     V* esum;                  //   chunk sums
@@ -206,6 +219,20 @@ __device__ __forceinline__ void load_chunk(const SweepArgs<P>& a, int k, int64_t
     for (int u = 0; u < Chunk<P>::U; ++u) {
         const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
         ab[u] = node < w ? __ldcs(src + node) : make_int2(0, 0);
+    }
+}
+
+// Same, from node pairs staged elsewhere (shared memory): src holds level k.
+template <class P>
+__device__ __forceinline__ void load_chunk_staged(const SweepArgs<P>& a, int k, int64_t c, const int2* src,
+                                                  int2 (&ab)[Chunk<P>::U]) {
+    constexpr int NPW = Chunk<P>::NPW;
+    const int lane = threadIdx.x & 31;
+    const int64_t w = a.lvl(LV_W, k);
+#pragma unroll
+    for (int u = 0; u < Chunk<P>::U; ++u) {
+        const int64_t node = c * Chunk<P>::NODES + u * NPW + lane / P::LPN;
+        ab[u] = node < w ? src[node] : make_int2(0, 0);
     }
 }
 
@@ -423,20 +450,40 @@ __device__ void emit_level(const SweepArgs<P>& a, int k, const typename P::V* ba
     emit_chunks<P>(a, a.lvl(LV_ECH, k), a.lvl(LV_ECH, k + 1), base, gwarp, nwarps);
 }
 
-// y[r] = row r's chunk sums added in chunk-id order, then its references into
-// the tail levels in C order (identity for an empty row)
+// y[r] = row r's chunk (or segment) sums, then its references into the tail
+// levels: one warp per row, LPN lanes per item; lane (slot, part) adds part
+// `part` of items slot, slot + 32/LPN, ... of the row's list [chunk sums |
+// tail references] in order, and the warp reduces the slots by a fixed
+// butterfly (identity for an empty row). The slice emit's sums sit at their
+// segment starts, found through row_pos.
 template <class P>
-__device__ void emit_final(const SweepArgs<P>& a, int64_t tid, int64_t nthreads) {
+__device__ void emit_final(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps) {
     using V = typename P::V;
-    for (int64_t i = tid; i < a.n * P::LPN; i += nthreads) {
-        const int64_t row = i / P::LPN;
-        const int l = (int)(i % P::LPN);
+    constexpr int NS = 32 / P::LPN;
+    const int lane = threadIdx.x & 31;
+    const int part = lane % P::LPN, slot = lane / P::LPN;
+    for (int64_t row = gwarp; row < a.n; row += nwarps) {
+        const int32_t c0 = __ldg(a.row_ech + row), c1 = __ldg(a.row_ech + row + 1);
+        const int32_t q0 = __ldg(a.late_off + row), q1 = __ldg(a.late_off + row + 1);
+        const int32_t nc = c1 - c0, total = nc + (q1 - q0);
         V acc = P::identity();
-        for (int32_t c = __ldg(a.row_ech + row); c < __ldg(a.row_ech + row + 1); ++c)
-            acc = P::combine(acc, a.esum[(int64_t)c * P::LPN + l]);
-        for (int32_t q = __ldg(a.late_off + row); q < __ldg(a.late_off + row + 1); ++q)
-            acc = P::combine(acc, a.tbuf[(int64_t)__ldg(a.late_ref + q) * P::LPN + l]);
-        a.y[i] = acc;
+        constexpr int B = P::LPN == 1 ? 8 : 4;   // items a lane loads together
+        for (int32_t i0 = 0; i0 < total; i0 += B * NS) {
+            V v[B];
+#pragma unroll
+            for (int u = 0; u < B; ++u) {
+                const int32_t i = i0 + u * NS + slot;
+                const int64_t e = i < nc ? (a.row_pos ? (int64_t)__ldg(a.row_pos + c0 + i) : (int64_t)(c0 + i)) : 0;
+                v[u] = i >= total ? P::identity()
+                       : i < nc   ? a.esum[e * P::LPN + part]
+                                  : a.tbuf[(int64_t)__ldg(a.late_ref + q0 + (i - nc)) * P::LPN + part];
+            }
+#pragma unroll
+            for (int u = 0; u < B; ++u) acc = P::combine(acc, v[u]);
+        }
+#pragma unroll
+        for (int msk = 16; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
+        if (slot == 0) a.y[row * P::LPN + part] = acc;
     }
 }
 
@@ -516,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
 
     // CTA 0 asks L2 for the tail's node pairs (levels Lg+1..L, contiguous at
     // the end of the node array) while the grid sweeps the wide levels
-    if (tail_cta) {
+    if (tail_cta && a.emode != EMIT_SLICE) {
         const int2* src = a.nodes + a.lvl(LV_START, Lg + 1);
         for (int64_t i = (int64_t)threadIdx.x * 16; i < a.tail_total; i += (int64_t)kThreads * 16) prefetch_l2(src + i);
     }
@@ -548,17 +595,16 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
             if (k == 2) emit_level<P>(a, 0, a.buf0, gw, GW);
         }
     }
+    // slice emit: the second kernel takes the tail, the emit and the row pass
+    if (a.emode == EMIT_SLICE) return;
     if (!grid_sync(a, nbar++)) return;
     // while CTA 0 runs the tail, the others reduce what is left of the level
-    // emit (level Lg, and the terminals if no phase took them), or of the
-    // chunk emit
+    // emit (level Lg, and the terminals if no phase took them)
     const int64_t skip = (tail && gridDim.x > 1) ? kWarps : 0;
     if (gw >= skip) {
         if (lemit) {
             if (Lg >= 1) emit_level<P>(a, Lg, (Lg & 1) ? a.buf1 : a.buf0, gw - skip, GW - skip);
             if (Lg < 2) emit_level<P>(a, 0, a.buf0, gw - skip, GW - skip);
-        } else if (a.emode == EMIT_CHUNK) {
-            emit_level<P>(a, 0, a.rv, gw - skip, GW - skip);
         }
     }
     // narrow top levels: CTA 0 alone, block barriers only, into the tail buffer
@@ -575,8 +621,170 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
         }
     }
     if (!grid_sync(a, nbar++)) return;
-    if (a.emode != EMIT_ROWS) emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+    if (a.emode != EMIT_ROWS) emit_final<P>(a, gw, GW);
     else emit_rows<P>(a, blockIdx.x, gridDim.x);
+}
+
+// ---------------------------------------------------------------- slice emit
+constexpr int kSliceThreads = 1024;
+
+// The narrow top levels on one CTA of kSliceThreads, with block barriers only:
+// node pairs and values in shared memory when both fit in `room` bytes, else
+// pairs and values in global memory; the values end in the tail buffer.
+template <class P>
+__device__ void slice_tail(const SweepArgs<P>& a, unsigned char* smem, int64_t room) {
+    using V = typename P::V;
+    const int Lg = a.grid_levels;
+    const int w0 = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const bool staged = (int64_t)(8 + sizeof(V) * P::LPN) * a.tail_total <= room;
+    int2* tp = reinterpret_cast<int2*>(smem);
+    V* tv = staged ? reinterpret_cast<V*>(tp + a.tail_total) : a.tbuf;
+    if (staged) {
+        const int2* src = a.nodes + a.lvl(LV_START, Lg + 1);
+        for (int64_t i = threadIdx.x; i < a.tail_total; i += blockDim.x) tp[i] = __ldcs(src + i);
+        __syncthreads();
+    }
+    for (int k = Lg + 1; k <= a.L; ++k) {
+        const TailIO<P> io = tail_io<P>(a, k, tv);
+        const int64_t nc = (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES;
+        for (int64_t c = w0; c < nc; c += nw) {
+            int2 ab[Chunk<P>::U];
+            if (staged) load_chunk_staged<P>(a, k, c, tp + a.lvl(LV_TOFF, k), ab);
+            else load_chunk<P>(a, k, c, ab);
+            combine_chunk<P, true>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, 0);
+        }
+        __syncthreads();
+    }
+    if (staged)
+        for (int64_t i = threadIdx.x; i < a.tail_total * P::LPN; i += blockDim.x) a.tbuf[i] = tv[i];
+}
+
+// One tile of a slice, on one warp: lane l holds references 8l .. 8l+7 (their
+// offsets o, their segment-start bits f). A lane adds its references in order,
+// closing the runs that start and end inside it; a segmented scan over the
+// lanes (Hillis-Steele, fixed order) carries each open run into the lane where
+// the next segment starts, which closes it, and lane 31 closes the run open at
+// the tile's end. The sum of the tile's k-th segment start goes to
+// esum[base + k] (padding included: nothing reads it).
+template <class P>
+__device__ __forceinline__ void tile_sums(const SweepArgs<P>& a, int64_t base, uint4 o, uint32_t f,
+                                          const typename P::V* sv) {
+    using V = typename P::V;
+    const int lane = threadIdx.x & 31;
+    const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+    V v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = sv[(w[i / 2] >> (16 * (i % 2))) & 0xffffu];
+    // segment starts before this lane, and in all lanes up to this one
+    const int nf = __popc(f);
+    int incl = nf;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += t;
+    }
+    const int before = incl - nf;
+    // runs inside the lane
+    V cur = P::identity(), head = P::identity();
+    bool open_head = true;
+    int k = before - 1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if ((f >> i) & 1u) {
+            if (open_head) {
+                head = cur;
+                open_head = false;
+            } else {
+                a.esum[base + k] = cur;
+            }
+            ++k;
+            cur = P::identity();
+        }
+        cur = P::combine(cur, v[i]);
+    }
+    // segmented inclusive scan of (lane holds a start, sum of its last run)
+    bool F = f != 0u;
+    V X = cur;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const bool Fp = __shfl_up_sync(0xffffffffu, F, d);
+        const V Xp = shfl_up(X, d);
+        if (lane >= d) {
+            if (!F) X = P::combine(Xp, X);
+            F = F || Fp;
+        }
+    }
+    // the run open at this lane's start: the scan one lane down
+    const V carry = shfl_up(X, 1);
+    if (f != 0u && before >= 1) a.esum[base + before - 1] = P::combine(lane >= 1 ? carry : P::identity(), head);
+    if (lane == 31 && incl >= 1) a.esum[base + incl - 1] = X;
+}
+
+// Slice s of [T | RV] into shared memory, then its tiles, one warp each; a
+// warp loads its next tile's offsets, starts and first start index before
+// reducing the current one.
+template <class P>
+__device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) {
+    using V = typename P::V;
+    // values [x0, x1) in 16-byte units (x0 is a multiple of 256 values; the
+    // last unit may run up to 15 bytes past x1, inside RV's padded allocation)
+    const int64_t x0 = __ldg(a.sx0 + s), x1 = __ldg(a.sx0 + s + 1);
+    const int64_t n16 = ((x1 - x0) * (int64_t)sizeof(V) + 15) / 16;
+    const int4* src = reinterpret_cast<const int4*>(a.rv + x0);
+    int4* dst = reinterpret_cast<int4*>(sv);
+#pragma unroll 4
+    for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+    __syncthreads();
+    if constexpr (P::LPN == 1) {
+        const int lane = threadIdx.x & 31;
+        const int64_t nw = blockDim.x >> 5;
+        const int64_t t1 = __ldg(a.stile + s + 1);
+        int64_t t = __ldg(a.stile + s) + (threadIdx.x >> 5);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        uint32_t f = 0;
+        int32_t sb = 0;
+        if (t < t1) {
+            o = __ldcs(a.sref + t * 32 + lane);
+            f = __ldcs(a.sflag + t * 32 + lane);
+            sb = __ldg(a.tile_sid + t);
+        }
+        while (t < t1) {
+            const int64_t tn = t + nw;
+            uint4 on = make_uint4(0, 0, 0, 0);
+            uint32_t fn = 0;
+            int32_t sbn = 0;
+            if (tn < t1) {
+                on = __ldcs(a.sref + tn * 32 + lane);
+                fn = __ldcs(a.sflag + tn * 32 + lane);
+                sbn = __ldg(a.tile_sid + tn);
+            }
+            tile_sums<P>(a, sb, o, f, sv);
+            t = tn;
+            o = on;
+            f = fn;
+            sb = sbn;
+        }
+    }
+    __syncthreads();
+}
+
+// After the wide levels: slices on every CTA (CTA 0 runs the tail first when
+// the launch is cooperative and has more than one CTA; then it only waits),
+// and, cooperative, a grid barrier and the row pass.
+template <class P>
+__global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs<P> a, int coop) {
+    using V = typename P::V;
+    extern __shared__ __align__(16) unsigned char slice_smem[];
+    if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
+    const bool tail = coop && a.grid_levels < a.L;
+    if (tail && blockIdx.x == 0) slice_tail<P>(a, slice_smem, (int64_t)a.slice * (int64_t)sizeof(V));
+    const int64_t first = tail && gridDim.x > 1 ? 1 : 0;
+    if (blockIdx.x >= first)
+        for (int64_t i = blockIdx.x - first; i < a.nslices; i += gridDim.x - first)
+            slice_sums<P>(a, __ldg(a.sorder + i), reinterpret_cast<V*>(slice_smem));
+    if (!coop) return;
+    if (!grid_sync(a, 0)) return;
+    emit_final<P>(a, ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, ((int64_t)gridDim.x * blockDim.x) >> 5);
 }
 
 // ---------------------------------------------------------------- per-level schedule
@@ -617,13 +825,11 @@ __global__ void __launch_bounds__(kThreads, 1) emit_kernel(const SweepArgs<P> a,
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (a.emode == EMIT_ROWS) {
         emit_rows<P>(a, blockIdx.x, gridDim.x);
-    } else if (phase == 0 && a.emode == EMIT_CHUNK) {
-        emit_level<P>(a, 0, a.rv, gw, GW);
     } else if (phase == 0) {
         if (a.L >= 1 && a.grid_levels == a.L) emit_level<P>(a, a.L, (a.L & 1) ? a.buf1 : a.buf0, gw, GW);
         if (a.L < 2) emit_level<P>(a, 0, a.buf0, gw, GW);
     } else {
-        emit_final<P>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads);
+        emit_final<P>(a, gw, GW);
     }
 }
 
@@ -676,6 +882,15 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.echunk = reinterpret_cast<const int4*>(ar + d.echunk);
     a.cref = reinterpret_cast<const int32_t*>(ar + d.cref);
     a.row_ech = reinterpret_cast<const int32_t*>(ar + d.row_ech);
+    a.sref = reinterpret_cast<const uint4*>(ar + d.sref);
+    a.sflag = reinterpret_cast<const uint8_t*>(ar + d.sflag);
+    a.tile_sid = reinterpret_cast<const int32_t*>(ar + d.tile_sid);
+    a.row_pos = d.emit == EMIT_SLICE ? reinterpret_cast<const int32_t*>(ar + d.row_pos) : nullptr;
+    a.sx0 = reinterpret_cast<const int32_t*>(ar + d.sx0);
+    a.stile = reinterpret_cast<const int32_t*>(ar + d.stile);
+    a.sorder = reinterpret_cast<const int32_t*>(ar + d.sorder);
+    a.slice = d.slice;
+    a.nslices = d.n_slices;
     a.late_off = reinterpret_cast<const int32_t*>(ar + d.late_off);
     a.late_ref = reinterpret_cast<const int32_t*>(ar + d.late_ref);
     a.esum = reinterpret_cast<V*>(ar + d.esum);
@@ -701,23 +916,64 @@ int sweep_grid(const gc_handle* h) {
     return std::min(per_sm, 2) * h->sms;
 }
 
-int64_t barriers_per_product(const gc_handle* h) {
-    return std::max(h->grid_levels - 1, 0) + 2;
+// Grid barriers one CTA of the persistent sweep passes: one per level after
+// the first, then (unless the slice kernel takes over) one before the tail and
+// one before the row pass.
+int64_t sweep_barriers(const gc_handle* h) {
+    return std::max(h->grid_levels - 1, 0) + (h->lay.emit == EMIT_SLICE ? 0 : 2);
 }
 
-// Enqueues one product with the arguments in a (persistent kernel when the
-// device allows, else one kernel per level). Returns the launch count.
+// Shared memory of the slice kernel: one slice of values.
 template <class P>
-int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, int* grid_out = nullptr) {
-    int grid = 0;
-    if (h->schedule == 0 && h->coop) grid = sweep_grid<P>(h);
-    if (grid_out) *grid_out = grid;
+int64_t slice_smem(const gc_handle* h) {
+    return h->lay.slice * (int64_t)sizeof(typename P::V);
+}
+
+// CTAs of the cooperative slice kernel (one per SM; 0 if it cannot be resident).
+template <class P>
+int slice_grid(const gc_handle* h) {
+    const int64_t smem = slice_smem<P>(h);
+    cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem),
+               "slice shared memory");
+    int per_sm = 0;
+    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, slice_kernel<P>, kSliceThreads, (size_t)smem),
+               "slice occupancy");
+    return per_sm >= 1 ? h->sms : 0;
+}
+
+// Enqueues one product with the arguments in a (persistent kernels when the
+// device allows, else one kernel per level). Returns the launch count and
+// adds the grid-barrier arrivals of the cooperative launches to *arrivals;
+// a.bar_base is the barrier counter's value when the first launch starts.
+template <class P>
+int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals) {
+    const bool slice = h->lay.emit == EMIT_SLICE;
+    int grid = 0, grid2 = 0;
+    if (h->schedule == 0 && h->coop) {
+        grid = sweep_grid<P>(h);
+        if (slice && grid > 0) grid2 = slice_grid<P>(h);
+        if (slice && grid2 == 0) grid = 0;
+    }
     int64_t launches = 0;
+    *arrivals = 0;
     if (grid > 0) {
         void* args[] = {&a};
         cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P>, dim3(grid), dim3(kThreads), args, 0, st),
                    "sweep launch");
         launches = 1;
+        *arrivals = (unsigned long long)sweep_barriers(h) * (unsigned long long)grid;
+        if (slice) {
+            SweepArgs<P> b = a;
+            b.bar_base = a.bar_base + *arrivals;
+            int coop = 1;
+            void* args2[] = {&b, &coop};
+            cuda_check(cudaLaunchCooperativeKernel((const void*)slice_kernel<P>, dim3(grid2), dim3(kSliceThreads),
+                                                   args2, (size_t)slice_smem<P>(h), st),
+                       "slice launch");
+            ++launches;
+            *arrivals += (unsigned long long)grid2;
+        }
     } else {
         // level 1 also writes the leaf tables; with no levels a table-only launch
         const int64_t w1 = h->L >= 1 ? h->lv[LV_W * (h->L + 2) + 1] : 0;
@@ -733,8 +989,17 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, int
             emit_kernel<P><<<grid_for(h->n, kWarps * (32 / h->emit_group), h->sms, 4), kThreads, 0, st>>>(a, 0);
             ++launches;
         } else if (h->n > 0) {
-            emit_kernel<P><<<grid_for(h->lay.n_echunks, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 0);
-            emit_kernel<P><<<grid_for(h->n * P::LPN, kThreads, h->sms, 4), kThreads, 0, st>>>(a, 1);
+            if (slice) {
+                const int64_t smem = slice_smem<P>(h);
+                cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                           "slice shared memory");
+                const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>(h->lay.n_slices, h->sms));
+                slice_kernel<P><<<g2, kSliceThreads, (size_t)smem, st>>>(a, 0);
+            } else {
+                emit_kernel<P><<<grid_for(h->lay.n_echunks, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 0);
+            }
+            emit_kernel<P><<<grid_for(h->n, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 1);
             launches += 2;
         }
     }
@@ -745,10 +1010,9 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, int
 template <class P>
 void run_product(gc_handle* h, const void* x, void* y, cudaStream_t st) {
     SweepArgs<P> a = make_args<P>(h, x, y);
-    int grid = 0;
-    const int64_t launches = launch_product<P>(h, a, st, &grid);
-    if (grid > 0) h->bar_base += (unsigned long long)barriers_per_product(h) * (unsigned long long)grid;
-    h->launches = launches;
+    unsigned long long arrivals = 0;
+    h->launches = launch_product<P>(h, a, st, &arrivals);
+    h->bar_base += arrivals;
 }
 
 void dispatch_product(gc_handle* h, const void* x, void* y, int32_t k, cudaStream_t st) {
@@ -822,7 +1086,7 @@ StaticParts static_parts(const gc_handle* h, int32_t k) {
     s.buf0 = take(vb * (d.TB + h->max_width));
     s.buf1 = take(vb * (d.TB + h->max_width));
     s.tbuf = take(vb * d.tail_total);
-    if (d.chunked()) s.esum = take(vb * d.n_echunks);
+    if (d.chunked()) s.esum = take(vb * d.n_esum);
     if (d.has_rv()) s.rv = take(vb * (d.TB + h->n_roots));
     s.status = take(256);
     s.total = o;
@@ -851,7 +1115,8 @@ void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, u
     // the array keeps the previous call's contents: start from a clear status
     // word and barrier counter
     cuda_check(cudaMemsetAsync(scratch + sp.status, 0, 256, st), "fixed scratch clear");
-    h->launches = launch_product<P>(h, a, st);
+    unsigned long long arrivals = 0;
+    h->launches = launch_product<P>(h, a, st, &arrivals);
 }
 
 }  // namespace
@@ -923,14 +1188,21 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         std::vector<int32_t> leaf((size_t)g.alpha());
         for (int64_t p = 0; p < g.alpha(); ++p) leaf[p] = leaf_code((int32_t)p);
         EmitPlan plan;
+        SlicePlan sp;
         std::vector<int32_t> cref, co;
-        if (d.chunked()) {
-            const bool by_level = d.emit == EMIT_LEVEL;
-            plan = plan_emit(g, d.TB, d.grid_levels, by_level);
-            if ((int64_t)plan.echunk.size() != 4 * d.n_echunks || (int64_t)plan.late_ref.size() != d.n_late)
+        if (d.emit == EMIT_LEVEL) {
+            plan = plan_level_emit(g, d.TB, d.grid_levels);
+            if ((int64_t)plan.echunk.size() != 4 * d.n_echunks || (int64_t)plan.late_ref.size() != d.n_late ||
+                (int64_t)plan.cref.size() != d.n_early)
                 fail(GC_ERR_INVALID_GRAMMAR, "emit plan does not match the layout");
-            validate_emit_plan(plan, g, d.TB, d.grid_levels, by_level);
+            validate_emit_plan(plan, g, d.TB, d.grid_levels);
             for (int64_t k = 0; k <= L + 1; ++k) h->lv[LV_ECH * (L + 2) + k] = plan.ech[k];
+        } else if (d.emit == EMIT_SLICE) {
+            sp = plan_slice_emit(g, d.TB, d.grid_levels, d.slice);
+            if (sp.nids != d.n_echunks || (int64_t)sp.late_ref.size() != d.n_late || sp.ntiles != d.n_tiles ||
+                (int64_t)sp.tsid.size() != d.n_starts || sp.nslices != d.n_slices)
+                fail(GC_ERR_INVALID_GRAMMAR, "slice plan does not match the layout");
+            validate_slice_plan(sp, g, d.TB, d.grid_levels);
         } else {
             cref.resize(g.c_ref.size());
             for (size_t e = 0; e < cref.size(); ++e) cref[e] = ref(g.c_ref[e]);
@@ -954,12 +1226,23 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             put(st, a, d.V, v.data(), v.size());
         }
         put(st, a, d.leaf, leaf.data(), leaf.size());
-        if (d.chunked()) {
+        if (d.emit == EMIT_LEVEL) {
             put(st, a, d.cref, plan.cref.data(), plan.cref.size());
             put(st, a, d.echunk, plan.echunk.data(), plan.echunk.size());
             put(st, a, d.row_ech, plan.row_ech.data(), plan.row_ech.size());
             put(st, a, d.late_off, plan.late_off.data(), plan.late_off.size());
             put(st, a, d.late_ref, plan.late_ref.data(), plan.late_ref.size());
+        } else if (d.emit == EMIT_SLICE) {
+            put(st, a, d.sref, sp.sref.data(), sp.sref.size());
+            put(st, a, d.sflag, sp.sflag.data(), sp.sflag.size());
+            put(st, a, d.tile_sid, sp.tile_sid.data(), sp.tile_sid.size());
+            put(st, a, d.row_pos, sp.row_pos.data(), sp.row_pos.size());
+            put(st, a, d.sx0, sp.x0.data(), sp.x0.size());
+            put(st, a, d.stile, sp.stile.data(), sp.stile.size());
+            put(st, a, d.sorder, sp.sorder.data(), sp.sorder.size());
+            put(st, a, d.row_ech, sp.row_seg.data(), sp.row_seg.size());
+            put(st, a, d.late_off, sp.late_off.data(), sp.late_off.size());
+            put(st, a, d.late_ref, sp.late_ref.data(), sp.late_ref.size());
         } else {
             put(st, a, d.c_off, co.data(), co.size());
             put(st, a, d.c_ref, cref.data(), cref.size());

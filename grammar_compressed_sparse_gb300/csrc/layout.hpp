@@ -9,11 +9,21 @@
 //                                 offset in the tail buffer
 //                       V         policy[|V|]      value dictionary
 //                       leaf      int32[alpha]     leaf code of terminal p
-//     level / chunk     cref      int32[early]     C without the references to
-//     emit:                                        the tail levels: by level, then
-//                                                  row (level emit); by row (chunk)
+//     level emit:       cref      int32[early]     C without the references to
+//                                                  the tail levels, by level, then row
 //                       echunk    int4[chunks]     (start, length, id, 0) per chunk
-//                       row_ech   int32[n+1]       row r's chunk ids
+//     slice emit:       sref      uint16[256 tiles] offsets into slices of [T | RV],
+//                                                  in tiles of 256 references
+//                       sflag     uint8[32 tiles]  bit i of byte j: reference 8j+i
+//                                                  of the tile starts a segment
+//                       tile_sid  int32[tiles+1]   first segment start of each tile
+//                       row_pos   int32[ids]       for each id (a row's segments and
+//                                                  pieces in slice order), the index
+//                                                  of its segment start
+//                       sx0       int32[slices+1]  first value of each slice
+//                       stile     int32[slices+1]  tile range of each slice
+//                       sorder    int32[slices]    slices by decreasing tile count
+//     level / slice:    row_ech   int32[n+1]       row r's chunk / segment ids
 //                       late_off  int32[n+1]       row r's references into the
 //                       late_ref  int32[late]      narrow top levels (tail indices)
 //     row emit:         c_off     int32[n+1]
@@ -22,8 +32,9 @@
 //                       buf1X     value[TB + w*]   values (the two streaming buffers)
 //                       tbuf      value[tail]      the narrow top levels' values,
 //                                                  level after level
-//     level / chunk:    esum      value[chunks]    chunk sums
-//     chunk / row:      RVX       value[TB + rho]  leaf table T, then root values
+//     level / slice:    esum      value[chunks     chunk sums, or one sum per
+//                                       / starts]  segment start
+//     slice / row:      RVX       value[TB + rho]  leaf table T, then root values
 //                       status    256 B            status word, fixpoint flag,
 //                                                  grid-barrier arrival counter
 //   staging             xs        value[m]         x / y copies for the
@@ -54,11 +65,15 @@
 //               their level is computed, straight from that level's buffer
 //               (the pages' emit on the spot). A last pass adds each row's
 //               chunk sums in order, then its late references.
-//   chunk emit  rows average 128 symbols or more, one-wide values: roots are
-//               also stored to RV when their level is computed (RV stays in
-//               L2), and the early references, in row order and cut into
-//               chunks of at most 512 of one row, are reduced from RV while
-//               one CTA computes the tail levels; a last pass as above.
+//   slice emit  rows average 128 symbols or more, one-wide values: roots are
+//               also stored to RV when their level is computed. After the wide
+//               levels, a second kernel cuts [T | RV] into slices that fit a
+//               CTA's shared memory; each CTA loads a slice and sums, for
+//               every row, that row's references into the slice (a segment,
+//               in C order), reading shared memory instead of scattered global
+//               lines. One CTA computes the tail levels meanwhile; a last pass
+//               adds each row's segment sums in slice order, then its late
+//               references.
 //   row emit    shorter rows: roots are stored to RV, and rows are reduced at
 //               the end, a few lanes per row.
 #pragma once
@@ -72,18 +87,29 @@ constexpr int64_t kEmitChunkSyms = 512;   // references per emit chunk
 constexpr int64_t kLongRowAvg = 128;      // average |C| per row for chunked emits
 constexpr int64_t kLevelRows = 6;         // rows of the level table
 
-enum EmitMode : int32_t { EMIT_LEVEL = 0, EMIT_CHUNK = 1, EMIT_ROWS = 2 };
+enum EmitMode : int32_t { EMIT_LEVEL = 0, EMIT_SLICE = 1, EMIT_ROWS = 2 };
+
+constexpr int64_t kSliceBytes = 192 << 10;   // shared memory of one slice
+constexpr int64_t kSliceTarget = 144;         // slices the references are spread over, at least
+constexpr int64_t kSliceRefsMin = 16384;      // a slice may always take this many references
+constexpr int64_t kSliceStep = 256;           // slices start on multiples of this many values
+inline int64_t slice_len(int64_t value_bytes) { return std::min<int64_t>(kSliceBytes / value_bytes, 65536); }
 
 struct DevLayout {
     int64_t nodes, levels, V, leaf;
-    int64_t cref, echunk, row_ech;        // level and chunk emit
-    int64_t late_off, late_ref;
+    int64_t cref, echunk;                 // level emit
+    int64_t sref, sflag, tile_sid, row_pos, sx0, stile, sorder;   // slice emit
+    int64_t row_ech, late_off, late_ref;  // level and slice emit
     int64_t c_off, c_ref;                 // row emit
     int64_t buf0, buf1, esum, tbuf, RV, status, xs, ys;
     int64_t total, grammar_bytes, scratch_bytes, staging_bytes;
     int64_t value_bytes;   // bytes of one node value (k_max elements)
     int64_t n_nodes_padded;
-    int64_t n_echunks, n_late;
+    int64_t n_echunks, n_late;   // chunk or segment ids; late references
+    int64_t n_early;             // level emit: early references
+    int64_t slice, n_slices;     // slice emit: most values a slice holds, slices,
+    int64_t n_tiles, n_starts;   //   tiles, segment starts
+    int64_t n_esum;              // level emit: chunks; slice emit: segment starts
     int64_t tail_nodes;    // widest level the single-CTA tail takes
     int64_t grid_levels;   // Lg: levels 1..Lg use the whole grid
     int64_t tail_total;    // nodes of the tail buffer (levels Lg+1..L, padded)
@@ -91,7 +117,7 @@ struct DevLayout {
     int32_t vbits;         // bits of the value index inside a leaf code
     EmitMode emit;
 
-    bool chunked() const { return emit != EMIT_ROWS; }
+    bool chunked() const { return emit != EMIT_ROWS; }   // chunk or segment sums, esum
     bool has_rv() const { return emit != EMIT_LEVEL; }
 };
 
@@ -111,7 +137,7 @@ inline int64_t leaf_block(int64_t alpha) { return (alpha + 1 + 63) / 64 * 64; }
 
 inline EmitMode emit_mode(const Grammar& g, int32_t k_max) {
     const bool long_rows = g.n > 0 && (int64_t)g.c_ref.size() >= kLongRowAvg * g.n;
-    return !long_rows ? EMIT_ROWS : k_max == 1 ? EMIT_CHUNK : EMIT_LEVEL;
+    return !long_rows ? EMIT_ROWS : k_max == 1 ? EMIT_SLICE : EMIT_LEVEL;
 }
 
 inline int64_t tail_width(int32_t k_max) { return k_max == 16 ? 1024 : 4096; }
@@ -137,11 +163,10 @@ inline std::vector<int64_t> tail_offsets(const Grammar& g, int64_t Lg) {
     return t;
 }
 
-// Chunks of C's early references (terminals and levels 1..Lg): with by_level,
+// Level emit: chunks of C's early references (terminals and levels 1..Lg),
 // grouped by the level of their symbol and indexed into that level's
-// [T | buffer] space, in chunks of one (level, row); otherwise in row order,
-// indexed into [T | RV], in chunks of one row (all in group 0). References to
-// the tail levels are kept per row as tail-buffer indices.
+// [T | buffer] space, in chunks of one (level, row). References to the tail
+// levels are kept per row as tail-buffer indices.
 struct EmitPlan {
     std::vector<int32_t> cref;      // grouped by (level, row), as [T | buffer] indices
     std::vector<int32_t> echunk;    // 4 per chunk: start, length, id, 0 (level-major)
@@ -158,42 +183,47 @@ inline int64_t ref_level(const Grammar& g, int32_t c) {
            g.root_off.begin() - 1;
 }
 
-inline EmitPlan plan_emit(const Grammar& g, int64_t TB, int64_t Lg, bool by_level) {
-    const int64_t L = g.L, n = g.n;
+// Row r's references into the tail levels (levels > Lg), as tail-buffer indices.
+inline void plan_late(const Grammar& g, int64_t Lg, std::vector<int32_t>& off, std::vector<int32_t>& ref) {
     const std::vector<int64_t>& co = g.slp.c_off;
     const std::vector<int64_t> toff = tail_offsets(g, Lg);
-    const size_t C = g.c_ref.size();
-    std::vector<int32_t> lev(C), pos(C);
-    std::vector<char> early(C);
-    EmitPlan p;
-    p.late_off.assign((size_t)n + 1, 0);
-    for (int64_t r = 0; r < n; ++r) {
+    off.assign((size_t)g.n + 1, 0);
+    ref.clear();
+    for (int64_t r = 0; r < g.n; ++r) {
         for (int64_t e = co[r]; e < co[r + 1]; ++e) {
             const int32_t c = g.c_ref[e];
             const int64_t k = ref_level(g, c);
-            early[e] = k <= Lg;
-            lev[e] = by_level ? (int32_t)k : 0;
-            if (c < 0) {
-                pos[e] = -c - 1;   // terminal p = -c-2 -> T[p+1]
-            } else if (k <= Lg) {
-                pos[e] = (int32_t)(by_level ? TB + c - g.root_off[k] : TB + c);
-            } else {
-                p.late_ref.push_back((int32_t)(toff[k] + c - g.root_off[k]));
-            }
+            if (k > Lg) ref.push_back((int32_t)(toff[k] + c - g.root_off[k]));
         }
-        p.late_off[r + 1] = (int32_t)p.late_ref.size();
+        off[r + 1] = (int32_t)ref.size();
     }
-    // counting sort of the wide references by level, stable in row-major order
+}
+
+inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
+    const int64_t L = g.L, n = g.n;
+    const std::vector<int64_t>& co = g.slp.c_off;
+    const size_t C = g.c_ref.size();
+    EmitPlan p;
+    plan_late(g, Lg, p.late_off, p.late_ref);
+    std::vector<int32_t> lev(C), pos(C);
+    for (size_t e = 0; e < C; ++e) {
+        const int32_t c = g.c_ref[e];
+        const int64_t k = ref_level(g, c);
+        lev[e] = (int32_t)k;
+        pos[e] = c < 0 ? -c - 1                                   // terminal p = -c-2 -> T[p+1]
+                       : (int32_t)(TB + c - g.root_off[k]);
+    }
+    // counting sort of the early references by level, stable in row-major order
     std::vector<int64_t> cnt((size_t)Lg + 2, 0);
     for (size_t e = 0; e < C; ++e)
-        if (early[e]) ++cnt[lev[e] + 1];
+        if (lev[e] <= Lg) ++cnt[lev[e] + 1];
     for (int64_t k = 0; k <= Lg; ++k) cnt[k + 1] += cnt[k];
     p.cref.resize((size_t)cnt[Lg + 1]);
     std::vector<int64_t> at(cnt.begin(), cnt.end() - 1);
     std::vector<int32_t> row_of(p.cref.size());
     for (int64_t r = 0; r < n; ++r)
         for (int64_t e = co[r]; e < co[r + 1]; ++e) {
-            if (!early[e]) continue;
+            if (lev[e] > Lg) continue;
             const int64_t d = at[lev[e]]++;
             p.cref[d] = pos[e];
             row_of[d] = (int32_t)r;
@@ -234,26 +264,259 @@ inline EmitPlan plan_emit(const Grammar& g, int64_t TB, int64_t Lg, bool by_leve
     return p;
 }
 
+// Slice emit: the early references as [T | RV] indices x. Slices are runs of
+// values [x0[s], x0[s+1]) that start on multiples of kSliceStep, at most S
+// values wide, and close before they would take more than max(kSliceRefsMin,
+// early references / kSliceTarget) references; slice s holds offset x - x0[s]. Within a slice the references
+// keep row-major C order, so a row's references into it form one segment.
+// A slice's segments are packed, in order, into tiles of kTileRefs references
+// (32 lanes x 8): a segment that does not fit in the rest of a tile starts a
+// new one (the rest is padding, a segment with id -1), and one longer than a
+// tile is cut into tile-long pieces, ceil(length / kTileRefs) of them. Every segment or piece gets its own id,
+// in (row, slice, piece) order, so a row's sums are contiguous.
+constexpr int64_t kTileRefs = 256;
+
+struct SlicePlan {
+    int64_t S = 0, nslices = 0, ntiles = 0, nids = 0;
+    std::vector<int32_t> x0;        // nslices+1
+    std::vector<int32_t> stile;     // nslices+1
+    std::vector<int32_t> sorder;    // nslices: slices by decreasing tile count
+    std::vector<uint16_t> sref;     // kTileRefs per tile
+    std::vector<uint8_t> sflag;     // kTileRefs/8 per tile
+    std::vector<int32_t> tsid;      // one per segment start: its id (-1: padding)
+    std::vector<int32_t> tile_sid;  // ntiles+1
+    std::vector<int32_t> row_seg;   // n+1: row r's ids
+    std::vector<int32_t> row_pos;   // nids: segment start of each id
+    std::vector<int32_t> late_off, late_ref;
+};
+
+// [T | RV] index of an early reference (terminal or root of levels 1..Lg).
+inline int64_t slice_index(int64_t TB, int32_t c) { return c < 0 ? -c - 1 : TB + c; }
+
+// Slice boundaries from the references' counts per kSliceStep values.
+inline std::vector<int32_t> slice_bounds(const Grammar& g, int64_t TB, int64_t Lg, int64_t S) {
+    const int64_t X = TB + (Lg >= 1 ? g.root_off[Lg + 1] : 0);   // early references lie below X
+    const int64_t nb = (X + kSliceStep - 1) / kSliceStep;
+    std::vector<int64_t> cnt((size_t)nb, 0);
+    for (int32_t c : g.c_ref)
+        if (ref_level(g, c) <= Lg) ++cnt[slice_index(TB, c) / kSliceStep];
+    int64_t total = 0;
+    for (int64_t c : cnt) total += c;
+    const int64_t cap = std::max<int64_t>(kSliceRefsMin, (total + kSliceTarget - 1) / kSliceTarget);
+    std::vector<int32_t> x0{0};
+    int64_t refs = 0, width = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+        if (width > 0 && (width + kSliceStep > S || refs + cnt[b] > cap)) {
+            x0.push_back((int32_t)(b * kSliceStep));
+            refs = width = 0;
+        }
+        refs += cnt[b];
+        width += kSliceStep;
+    }
+    if (nb > 0) x0.push_back((int32_t)X);
+    return x0;
+}
+
+inline int64_t slice_of(const std::vector<int32_t>& x0, int64_t x) {
+    return std::upper_bound(x0.begin() + 1, x0.end(), (int32_t)x) - x0.begin() - 1;
+}
+
+// Segments of the early references: for each slice, (row, first, length) in
+// row order, with the references' offsets in `off` (slice by slice).
+struct SliceSegments {
+    std::vector<int32_t> x0;
+    std::vector<int64_t> sseg;                 // nslices+1
+    std::vector<int32_t> seg_row;
+    std::vector<int64_t> seg_first, seg_len;   // into off
+    std::vector<uint16_t> off;
+};
+
+inline SliceSegments slice_segments(const Grammar& g, int64_t TB, int64_t Lg, int64_t S, bool with_offsets) {
+    const std::vector<int64_t>& co = g.slp.c_off;
+    const size_t C = g.c_ref.size();
+    SliceSegments z;
+    z.x0 = slice_bounds(g, TB, Lg, S);
+    const int64_t NS = (int64_t)z.x0.size() - 1;
+    std::vector<int32_t> sl(C, -1);   // slice of each early reference, -1 for late ones
+    for (size_t e = 0; e < C; ++e)
+        if (ref_level(g, g.c_ref[e]) <= Lg) sl[e] = (int32_t)slice_of(z.x0, slice_index(TB, g.c_ref[e]));
+    std::vector<int64_t> last((size_t)NS, -1), nref((size_t)NS + 1, 0), nseg((size_t)NS + 1, 0);
+    for (int64_t r = 0; r < g.n; ++r)
+        for (int64_t e = co[r]; e < co[r + 1]; ++e) {
+            if (sl[e] < 0) continue;
+            ++nref[sl[e] + 1];
+            if (last[sl[e]] != r) {
+                last[sl[e]] = r;
+                ++nseg[sl[e] + 1];
+            }
+        }
+    for (int64_t s = 0; s < NS; ++s) {
+        nref[s + 1] += nref[s];
+        nseg[s + 1] += nseg[s];
+    }
+    z.sseg = nseg;
+    z.seg_row.assign((size_t)nseg[NS], 0);
+    z.seg_first.assign((size_t)nseg[NS], 0);
+    z.seg_len.assign((size_t)nseg[NS], 0);
+    if (with_offsets) z.off.resize((size_t)nref[NS]);
+    std::vector<int64_t> at_ref(nref.begin(), nref.end() - 1), at_seg(nseg.begin(), nseg.end() - 1);
+    std::fill(last.begin(), last.end(), -1);
+    for (int64_t r = 0; r < g.n; ++r)
+        for (int64_t e = co[r]; e < co[r + 1]; ++e) {
+            if (sl[e] < 0) continue;
+            const int32_t s = sl[e];
+            if (last[s] != r) {
+                last[s] = r;
+                z.seg_row[at_seg[s]] = (int32_t)r;
+                z.seg_first[at_seg[s]] = at_ref[s];
+                ++at_seg[s];
+            }
+            ++z.seg_len[at_seg[s] - 1];
+            if (with_offsets) z.off[at_ref[s]] = (uint16_t)(slice_index(TB, g.c_ref[e]) - z.x0[s]);
+            ++at_ref[s];
+        }
+    return z;
+}
+
+// Tiles and ids of the packing described above, from a slice's segment lengths.
+struct TileCounts {
+    int64_t tiles = 0, starts = 0, ids = 0;
+};
+inline TileCounts count_tiles(const SliceSegments& z) {
+    TileCounts t;
+    const int64_t NS = (int64_t)z.x0.size() - 1;
+    for (int64_t s = 0; s < NS; ++s) {
+        int64_t fill = kTileRefs;   // no open tile yet
+        for (int64_t j = z.sseg[s]; j < z.sseg[s + 1]; ++j)
+            for (int64_t left = z.seg_len[j]; left > 0;) {
+                if (fill == kTileRefs || (fill > 0 && left > kTileRefs - fill)) {
+                    if (fill > 0 && fill < kTileRefs) ++t.starts;   // padding closes the tile
+                    ++t.tiles;
+                    fill = 0;
+                }
+                const int64_t take = std::min(left, kTileRefs - fill);
+                ++t.starts;
+                ++t.ids;
+                fill += take;
+                left -= take;
+            }
+        if (fill > 0 && fill < kTileRefs) ++t.starts;
+    }
+    return t;
+}
+
+inline SlicePlan plan_slice_emit(const Grammar& g, int64_t TB, int64_t Lg, int64_t S) {
+    const int64_t n = g.n;
+    SliceSegments z = slice_segments(g, TB, Lg, S, true);
+    SlicePlan p;
+    p.S = S;
+    p.x0 = z.x0;
+    p.nslices = (int64_t)z.x0.size() - 1;
+    plan_late(g, Lg, p.late_off, p.late_ref);
+    const int64_t NS = p.nslices;
+    // ids: per row, its pieces in (slice, piece) order
+    std::vector<int64_t> row_ids((size_t)n + 1, 0);
+    for (int64_t j = 0; j < (int64_t)z.seg_row.size(); ++j)
+        row_ids[z.seg_row[j] + 1] += (z.seg_len[j] + kTileRefs - 1) / kTileRefs;
+    for (int64_t r = 0; r < n; ++r) row_ids[r + 1] += row_ids[r];
+    p.row_seg.assign(row_ids.begin(), row_ids.end());
+    p.nids = row_ids[n];
+    std::vector<int64_t> next_id(row_ids.begin(), row_ids.end() - 1);
+    // slices in order: each row's pieces are met in (slice, piece) order
+    p.stile.assign((size_t)NS + 1, 0);
+    int64_t fill = kTileRefs;
+    auto open_tile = [&]() {
+        if (fill > 0 && fill < kTileRefs) {   // pad the open tile: one start with id -1
+            p.sflag[(p.ntiles - 1) * (kTileRefs / 8) + fill / 8] |= (uint8_t)(1u << (fill % 8));
+            p.tsid.push_back(-1);
+        }
+        p.sref.resize(p.sref.size() + kTileRefs, 0);
+        p.sflag.resize(p.sflag.size() + kTileRefs / 8, 0);
+        p.tile_sid.push_back((int32_t)p.tsid.size());
+        ++p.ntiles;
+        fill = 0;
+    };
+    for (int64_t s = 0; s < NS; ++s) {
+        p.stile[s] = p.ntiles;
+        fill = kTileRefs;
+        for (int64_t j = z.sseg[s]; j < z.sseg[s + 1]; ++j) {
+            int64_t q = z.seg_first[j];
+            for (int64_t left = z.seg_len[j]; left > 0;) {
+                if (fill == kTileRefs || (fill > 0 && left > kTileRefs - fill)) open_tile();
+                const int64_t take = std::min(left, kTileRefs - fill);
+                const int64_t base = (p.ntiles - 1) * kTileRefs + fill;
+                p.sflag[(p.ntiles - 1) * (kTileRefs / 8) + fill / 8] |= (uint8_t)(1u << (fill % 8));
+                p.tsid.push_back((int32_t)next_id[z.seg_row[j]]++);
+                for (int64_t i = 0; i < take; ++i) p.sref[base + i] = z.off[q + i];
+                q += take;
+                fill += take;
+                left -= take;
+            }
+        }
+        if (fill > 0 && fill < kTileRefs) {   // pad the slice's last tile
+            p.sflag[(p.ntiles - 1) * (kTileRefs / 8) + fill / 8] |= (uint8_t)(1u << (fill % 8));
+            p.tsid.push_back(-1);
+        }
+    }
+    p.stile[NS] = p.ntiles;
+    p.tile_sid.push_back((int32_t)p.tsid.size());
+    p.row_pos.assign((size_t)p.nids, -1);
+    for (size_t k = 0; k < p.tsid.size(); ++k)
+        if (p.tsid[k] >= 0) p.row_pos[p.tsid[k]] = (int32_t)k;
+    // processing order: heaviest slices first, so that CTAs taking a second
+    // slice take light ones
+    p.sorder.resize((size_t)NS);
+    for (int64_t i = 0; i < NS; ++i) p.sorder[i] = (int32_t)i;
+    std::stable_sort(p.sorder.begin(), p.sorder.end(), [&](int32_t a, int32_t b) {
+        return p.stile[a + 1] - p.stile[a] > p.stile[b + 1] - p.stile[b];
+    });
+    return p;
+}
+
+// Counts of plan_slice_emit's arrays, without building it.
+struct SliceCounts {
+    int64_t slices = 0, tiles = 0, starts = 0, ids = 0, late = 0;
+};
+inline SliceCounts count_slice_emit(const Grammar& g, int64_t TB, int64_t Lg, int64_t S) {
+    const SliceSegments z = slice_segments(g, TB, Lg, S, false);
+    const TileCounts t = count_tiles(z);
+    SliceCounts c;
+    c.slices = (int64_t)z.x0.size() - 1;
+    c.tiles = t.tiles;
+    c.starts = t.starts;
+    c.ids = t.ids;
+    for (int32_t r : g.c_ref)
+        if (ref_level(g, r) > Lg) ++c.late;
+    return c;
+}
+
 // Checks a plan against the grammar before it reaches the device: every
 // chunk lies inside cref and holds references of its own level only (T for
 // level 0, that level's roots otherwise), chunk ids are a permutation that
 // row_ech splits by row, and every tail reference lies inside the tail buffer.
-inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, int64_t Lg, bool by_level) {
-    const int64_t n = g.n, L = g.L, nch = (int64_t)p.echunk.size() / 4;
+inline void check_late(const std::vector<int32_t>& off, const std::vector<int32_t>& ref, const Grammar& g,
+                       int64_t Lg, const char* what) {
     const std::vector<int64_t> toff = tail_offsets(g, Lg);
+    auto bad = [&](const char* why) { fail(GC_ERR_INVALID_GRAMMAR, std::string(what) + ": " + why); };
+    if ((int64_t)off.size() != g.n + 1 || off[0] != 0 || off[g.n] != (int64_t)ref.size()) bad("tail reference ranges");
+    for (int64_t r = 0; r < g.n; ++r)
+        if (off[r + 1] < off[r]) bad("tail reference ranges decrease");
+    for (int32_t t : ref)
+        if (t < 0 || t >= toff[g.L + 1]) bad("tail reference outside the tail buffer");
+}
+
+inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, int64_t Lg) {
+    const int64_t n = g.n, L = g.L, nch = (int64_t)p.echunk.size() / 4;
     auto bad = [](const char* what) { fail(GC_ERR_INVALID_GRAMMAR, std::string("emit plan: ") + what); };
     if ((int64_t)p.ech.size() != L + 2 || p.ech[0] != 0 || p.ech[L + 1] != nch) bad("level chunk ranges");
     if ((int64_t)p.row_ech.size() != n + 1 || p.row_ech[0] != 0 || p.row_ech[n] != nch) bad("row chunk ranges");
-    if ((int64_t)p.late_off.size() != n + 1 || p.late_off[0] != 0 || p.late_off[n] != (int64_t)p.late_ref.size())
-        bad("tail reference ranges");
+    check_late(p.late_off, p.late_ref, g, Lg, "emit plan");
     std::vector<char> seen((size_t)nch, 0);
     for (int64_t k = 0; k <= L; ++k) {
-        if (p.ech[k + 1] < p.ech[k] || ((k > Lg || (!by_level && k > 0)) && p.ech[k + 1] != p.ech[k]))
-            bad("level chunk ranges");
-        // terminals (level 0), one level's roots (by level), or terminals and
-        // the roots of levels 1..Lg in RV (row order)
+        if (p.ech[k + 1] < p.ech[k] || (k > Lg && p.ech[k + 1] != p.ech[k])) bad("level chunk ranges");
+        // terminals (level 0) or level k's roots in its buffer
         const int64_t t_hi = k == 0 ? g.alpha() + 1 : 0;
-        const int64_t r_hi = TB + (!by_level ? g.root_off[Lg + 1] : k == 0 ? 0 : g.lvl_roots[k]);
+        const int64_t r_hi = TB + (k == 0 ? 0 : g.lvl_roots[k]);
         auto ok = [&](int64_t v) { return (v >= 0 && v < t_hi) || (v >= TB && v < r_hi); };
         for (int64_t j = p.ech[k]; j < p.ech[k + 1]; ++j) {
             const int64_t st = p.echunk[4 * j], len = p.echunk[4 * j + 1], id = p.echunk[4 * j + 2];
@@ -265,27 +528,80 @@ inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, 
         }
     }
     for (int64_t r = 0; r < n; ++r)
-        if (p.row_ech[r + 1] < p.row_ech[r] || p.late_off[r + 1] < p.late_off[r]) bad("row ranges decrease");
-    for (int32_t t : p.late_ref)
-        if (t < 0 || t >= toff[L + 1]) bad("tail reference outside the tail buffer");
+        if (p.row_ech[r + 1] < p.row_ech[r]) bad("row ranges decrease");
 }
 
-// Sizes of plan_emit's arrays, counted without building the plan:
-// chunks, wide references and tail references.
+// Same for a slice plan: slice bounds and tile ranges are consistent, every
+// tile starts a segment at its first reference, its starts match its ids,
+// every id is -1 or names one esum slot exactly once, every reference of a
+// real segment names a T entry or a root of levels 1..Lg inside its slice,
+// and row_seg covers the ids.
+inline void validate_slice_plan(const SlicePlan& p, const Grammar& g, int64_t TB, int64_t Lg) {
+    const int64_t n = g.n, NS = p.nslices, S = p.S, NT = p.ntiles;
+    auto bad = [](const char* what) { fail(GC_ERR_INVALID_GRAMMAR, std::string("slice plan: ") + what); };
+    if (S < 1 || S > 65536 || (int64_t)p.x0.size() != NS + 1 || (int64_t)p.stile.size() != NS + 1) bad("slice size");
+    if ((int64_t)p.sref.size() != NT * kTileRefs || (int64_t)p.sflag.size() != NT * (kTileRefs / 8) ||
+        (int64_t)p.tile_sid.size() != NT + 1 || p.tile_sid[0] != 0 || p.tile_sid[NT] != (int64_t)p.tsid.size())
+        bad("tile arrays");
+    if ((int64_t)p.row_seg.size() != n + 1 || p.row_seg[0] != 0 || p.row_seg[n] != p.nids) bad("row id ranges");
+    for (int64_t r = 0; r < n; ++r)
+        if (p.row_seg[r + 1] < p.row_seg[r]) bad("row id ranges decrease");
+    check_late(p.late_off, p.late_ref, g, Lg, "slice plan");
+    const int64_t x_hi = TB + (Lg >= 1 ? g.root_off[Lg + 1] : 0);
+    std::vector<char> seen((size_t)p.nids, 0);
+    if (p.stile[0] != 0 || p.stile[NS] != NT) bad("slice tile ranges");
+    for (int64_t s = 0; s < NS; ++s) {
+        if (p.x0[s] % kSliceStep != 0 || p.x0[s + 1] <= p.x0[s] || p.x0[s + 1] - p.x0[s] > S) bad("slice bounds");
+        if (p.stile[s + 1] < p.stile[s]) bad("slice tile ranges decrease");
+        for (int64_t t = p.stile[s]; t < p.stile[s + 1]; ++t) {
+            if (!(p.sflag[t * (kTileRefs / 8)] & 1u)) bad("tile does not start a segment");
+            int64_t k = p.tile_sid[t] - 1, id = -1;
+            for (int64_t i = 0; i < kTileRefs; ++i) {
+                if (p.sflag[t * (kTileRefs / 8) + i / 8] & (1u << (i % 8))) {
+                    if (++k >= p.tile_sid[t + 1]) bad("tile starts exceed its ids");
+                    id = p.tsid[k];
+                    if (id < -1 || id >= p.nids || (id >= 0 && seen[id])) bad("segment ids");
+                    if (id >= 0) seen[id] = 1;
+                }
+                if (id < 0) continue;   // padding
+                const int64_t x = p.x0[s] + p.sref[t * kTileRefs + i];
+                if (x >= p.x0[s + 1] || !((x >= 0 && x <= g.alpha()) || (x >= TB && x < x_hi)))
+                    bad("reference outside its slice, T and RV");
+            }
+            if (k + 1 != p.tile_sid[t + 1]) bad("tile starts and ids differ");
+        }
+    }
+    for (int64_t i = 0; i < p.nids; ++i)
+        if (!seen[i]) bad("an id is never written");
+    if ((int64_t)p.sorder.size() != NS) bad("slice order");
+    {
+        std::vector<char> sseen((size_t)NS, 0);
+        for (int32_t v : p.sorder) {
+            if (v < 0 || v >= NS || sseen[v]) bad("slice order");
+            sseen[v] = 1;
+        }
+    }
+    if ((int64_t)p.row_pos.size() != p.nids) bad("row positions");
+    for (int64_t i = 0; i < p.nids; ++i)
+        if (p.row_pos[i] < 0 || p.row_pos[i] >= (int64_t)p.tsid.size() || p.tsid[p.row_pos[i]] != i)
+            bad("row positions");
+}
+
+// Counts of plan_level_emit's arrays, without building it: chunks, early
+// references and tail references.
 struct EmitCounts {
     int64_t chunks = 0, wide = 0, late = 0;
 };
-inline EmitCounts count_emit(const Grammar& g, int64_t Lg, bool by_level) {
-    const int64_t n = g.n;
+inline EmitCounts count_level_emit(const Grammar& g, int64_t Lg) {
     const std::vector<int64_t>& co = g.slp.c_off;
     std::vector<int64_t> per((size_t)Lg + 1, 0);
     EmitCounts t;
-    for (int64_t r = 0; r < n; ++r) {
+    for (int64_t r = 0; r < g.n; ++r) {
         std::fill(per.begin(), per.end(), 0);
         for (int64_t e = co[r]; e < co[r + 1]; ++e) {
             const int64_t k = ref_level(g, g.c_ref[e]);
             if (k > Lg) ++t.late;
-            else ++per[by_level ? k : 0];
+            else ++per[k];
         }
         for (int64_t k = 0; k <= Lg; ++k) {
             t.chunks += (per[k] + kEmitChunkSyms - 1) / kEmitChunkSyms;
@@ -308,9 +624,23 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.n_nodes_padded = 0;
     for (int64_t k = 1; k <= L; ++k) d.n_nodes_padded += pad_nodes(g.lvl_off[k + 1] - g.lvl_off[k]);
     EmitCounts ec;
-    if (d.chunked()) ec = count_emit(g, d.grid_levels, d.emit == EMIT_LEVEL);
-    d.n_echunks = ec.chunks;
-    d.n_late = ec.late;
+    SliceCounts sc;
+    if (d.emit == EMIT_LEVEL) {
+        ec = count_level_emit(g, d.grid_levels);
+        d.n_echunks = ec.chunks;
+        d.n_esum = ec.chunks;
+        d.n_late = ec.late;
+        d.n_early = ec.wide;
+    } else if (d.emit == EMIT_SLICE) {
+        d.slice = slice_len(d.value_bytes);
+        sc = count_slice_emit(g, d.TB, d.grid_levels, d.slice);
+        d.n_slices = sc.slices;
+        d.n_tiles = sc.tiles;
+        d.n_starts = sc.starts;
+        d.n_echunks = sc.ids;
+        d.n_esum = sc.starts;
+        d.n_late = sc.late;
+    }
     int64_t o = 0;
     auto take = [&](int64_t bytes) {
         int64_t at = o;
@@ -321,9 +651,19 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.levels = take(8 * kLevelRows * (L + 2));
     d.V = take(policy_elem_bytes(p) * std::max<int64_t>(1, (int64_t)g.V.size()));
     d.leaf = take(4 * A);
-    if (d.chunked()) {
-        d.cref = take(4 * ec.wide);
+    if (d.emit == EMIT_LEVEL) {
+        d.cref = take(4 * d.n_early);
         d.echunk = take(16 * d.n_echunks);
+    } else if (d.emit == EMIT_SLICE) {
+        d.sref = take(2 * kTileRefs * d.n_tiles);
+        d.sflag = take(kTileRefs / 8 * d.n_tiles);
+        d.tile_sid = take(4 * (d.n_tiles + 1));
+        d.row_pos = take(4 * d.n_echunks);
+        d.sx0 = take(4 * (d.n_slices + 1));
+        d.stile = take(4 * (d.n_slices + 1));
+        d.sorder = take(4 * d.n_slices);
+    }
+    if (d.chunked()) {
         d.row_ech = take(4 * (g.n + 1));
         d.late_off = take(4 * (g.n + 1));
         d.late_ref = take(4 * d.n_late);
@@ -336,7 +676,7 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.buf0 = take(d.value_bytes * (d.TB + w));
     d.buf1 = take(d.value_bytes * (d.TB + w));
     d.tbuf = take(d.value_bytes * d.tail_total);
-    if (d.chunked()) d.esum = take(d.value_bytes * d.n_echunks);
+    if (d.chunked()) d.esum = take(d.value_bytes * d.n_esum);
     if (d.has_rv()) d.RV = take(d.value_bytes * (d.TB + g.n_roots));
     d.status = take(256);
     d.scratch_bytes = o - d.grammar_bytes;
