@@ -44,6 +44,7 @@ WORKLOADS = {
     "geno_10k_50k": dict(gen=gcsynth.GENO_MEDIUM, k=1),
     "geno_10k_50k_k16": dict(gen=gcsynth.GENO_MEDIUM, k=16),
     "geno_1k_2k": dict(gen=gcsynth.GENO_SMALL, k=1),
+    "geno_50k_200k": dict(gen=gcsynth.GENO_LARGE, k=1),
     "graph_2m": dict(graph=gcsynth.GRAPH, k=1),
 }
 L2_FLUSH_BYTES = 512 << 20
@@ -82,6 +83,18 @@ def peaks():
 def make_csr(gen):
     rp, c, v = gcsynth.genotype_csr(**gen)
     return gen["n"], gen["m"], rp, c, v
+
+
+def make_blocked(gcs, gen):
+    """Streaming build of a row-blocked genotype matrix: each block of
+    ``block_rows`` rows is generated and compressed on its own, several at a
+    time (a block's CSR and RePair peak near 22 bytes per matrix entry)."""
+    mem = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    per_block = 22 * gen["block_rows"] * gen["m"]
+    workers = max(1, min(os.cpu_count() or 1, int(0.75 * mem // per_block), 8))
+    return gcs.Grammar.from_row_blocks(gen["n"], gen["m"], gen["block_rows"],
+                                       lambda r0, r1: gcsynth.genotype_csr(**gen, r0=r0, r1=r1),
+                                       workers=workers)
 
 
 def make_graph(gp):
@@ -302,7 +315,10 @@ def run_ours(args):
         G = gcs.cached_grammar(f"graph:{sorted(gp.items())}", lambda: make_graph(gp))
     else:
         gen = wl["gen"]
-        G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: make_csr(gen))
+        if "block_rows" in gen:
+            G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", None, build=lambda: make_blocked(gcs, gen))
+        else:
+            G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: make_csr(gen))
     build_s = time.perf_counter() - t0
     st = G.stats()
     policy, elem = ("or", 8) if graph else ("f32", 4)

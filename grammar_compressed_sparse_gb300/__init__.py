@@ -178,13 +178,14 @@ def _builder_fingerprint() -> str:
     return h.hexdigest()[:16]
 
 
-def cached_grammar(key: str, make_csr, cache_dir=None, **build_kwargs) -> Grammar:
+def cached_grammar(key: str, make_csr, cache_dir=None, build=None, **build_kwargs) -> Grammar:
     """Build a grammar, reusing a saved copy when one exists.
 
-    ``make_csr()`` returns (n, m, row_ptr, col, val). The file name combines
-    ``key``, the build options and a hash of the builder's sources, so a
-    changed builder never reuses an old file. A file that fails to load or
-    validate is rebuilt. Set GCSPARSE_NO_CACHE=1 to always rebuild.
+    ``make_csr()`` returns (n, m, row_ptr, col, val); alternatively
+    ``build()`` returns the Grammar itself (a streaming build). The file name
+    combines ``key``, the build options and a hash of the builder's sources,
+    so a changed builder never reuses an old file. A file that fails to load
+    or validate is rebuilt. Set GCSPARSE_NO_CACHE=1 to always rebuild.
     """
     cache_dir = cache_dir or os.environ.get("GCSPARSE_CACHE",
                                             os.path.join(os.path.expanduser("~"), ".cache", "gcsparse"))
@@ -195,8 +196,11 @@ def cached_grammar(key: str, make_csr, cache_dir=None, **build_kwargs) -> Gramma
             return Grammar.load(path)
         except _capi().GcError:
             pass
-    n, m, row_ptr, col, val = make_csr()
-    g = Grammar(n, m, row_ptr, col, val, **build_kwargs)
+    if build is not None:
+        g = build()
+    else:
+        n, m, row_ptr, col, val = make_csr()
+        g = Grammar(n, m, row_ptr, col, val, **build_kwargs)
     try:
         os.makedirs(cache_dir, exist_ok=True)
         tmp = path + f".tmp{os.getpid()}"

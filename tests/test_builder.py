@@ -193,6 +193,44 @@ def test_device_plans_pass_host_checks(gcs, k_max):
             gcs.capi.gc_upload(G._p, "f32", k_max, 256, lay["arena_bytes"])
 
 
+def test_slice_plan_and_tile_reduction(gcs, tmp_path):
+    # tests/native/slice_plan_check.cpp rebuilds the slice emit's plan for each
+    # matrix and replays the device's tile reduction on the CPU (lane runs and
+    # the segmented lane scan), against direct row sums over random values
+    import struct
+    import subprocess
+    from grammar_compressed_sparse_gb300 import build as gbuild
+    gbuild.build()
+    objs = [os.path.join(gbuild.BUILD, f + ".o") for f in gbuild.HOST_SOURCES]
+    exe = str(tmp_path / "slice_plan_check")
+    subprocess.run(["g++", "-O2", "-std=c++17", "-fopenmp", "-I", gbuild.INCLUDE, "-I", gbuild.CSRC,
+                    os.path.join(ROOT, "tests", "native", "slice_plan_check.cpp"), *objs, "-o", exe],
+                   check=True, capture_output=True)
+    files = []
+
+    def dump(name, n, m, rp, c, v):
+        path = str(tmp_path / name)
+        with open(path, "wb") as f:
+            f.write(struct.pack("qqq", n, m, int(rp[-1])))
+            f.write(np.asarray(rp, np.int64).tobytes())
+            f.write(np.asarray(c, np.int32).tobytes())
+            f.write(np.asarray(v, np.float32).tobytes())
+        files.append(path)
+
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    dump("slice300.bin", 300, cfg["m"], *gcsynth.genotype_csr(**cfg))                  # long segments
+    dump("small.bin", 1000, 2000, *gcsynth.genotype_csr(**gcsynth.GENO_SMALL))         # one or two slices
+    rp, c, v, _ = gcsynth.random_sparse(40, 3000, 0.4, [1.0, -1.0, 0.5], 8)
+    dump("heavy.bin", 40, 3000, rp, c, v)                                               # bare terminals
+    d = np.zeros((9, 700), np.float32)
+    d[:, ::3] = 1.0
+    d[4, 1::3] = 2.0                                                                     # one row much longer
+    dump("dense.bin", 9, 700, *dense_to_csr(d, np.float32))
+    out = subprocess.run([exe, *files], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.strip().endswith("OK")
+
+
 @pytest.mark.parametrize("bad", ["row_ptr", "col_range", "dup", "nan", "inf"])
 def test_bad_csr_is_rejected(gcs, bad):
     rp = np.array([0, 2, 3], dtype=np.int64)
