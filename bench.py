@@ -218,18 +218,30 @@ def _oracle_sample(workload, seconds, steps):
     rows done and the time, as JSON."""
     from oracle import direct
     wl = WORKLOADS[workload]
-    gen, k = wl["gen"], wl["k"]
-    rows = min(gen["n"], ORACLE_SAMPLE_ROWS)
-    rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=rows))
-    x = gcsynth.beta(gen["m"], seed=0, k=k)
+    k = wl["k"]
+    if "graph" in wl:
+        gp = wl["graph"]
+        rp, c = gcsynth.copy_model_graph(**gp)
+        rows = min(gp["nodes"], ORACLE_SAMPLE_ROWS * 100)
+        rp, c = rp[:rows + 1], c[:rp[rows]]
+        x = np.random.default_rng(0).integers(0, 2**63, gp["nodes"], dtype=np.uint64)
+        product = lambda a, b: direct.matvec_or(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], x)
+        block = 25000
+    else:
+        gen = wl["gen"]
+        rows = min(gen["n"], ORACLE_SAMPLE_ROWS)
+        rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=rows))
+        x = gcsynth.beta(gen["m"], seed=0, k=k)
+        product = lambda a, b: direct.matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
+        block = 250
     out = []
     for _ in range(steps):
         done_rows = 0
         t0 = time.perf_counter()
         while time.perf_counter() - t0 < seconds:
             a = done_rows % rows
-            b = min(rows, a + 250)
-            direct.matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
+            b = min(rows, a + block)
+            product(a, b)
             done_rows += b - a
         out.append({"rows": done_rows, "seconds": time.perf_counter() - t0})
     print(json.dumps(out), flush=True)
@@ -244,8 +256,17 @@ def cpu_oracle_rates(workload, seconds, steps=1):
                           "--workload", workload, "--cpu-seconds", str(seconds), "--steps", str(steps)],
                          env=env, capture_output=True, text=True, check=True).stdout
     recs = json.loads(out.strip().splitlines()[-1])
-    n = WORKLOADS[workload]["gen"]["n"]
+    wl = WORKLOADS[workload]
+    n = wl["graph"]["nodes"] if "graph" in wl else wl["gen"]["n"]
     return [(r["rows"] / n) / r["seconds"] for r in recs], recs
+
+
+def oracle_sample_text(workload):
+    wl = WORKLOADS[workload]
+    if "graph" in wl:
+        return (f"Boolean OR product of the first {min(wl['graph']['nodes'], ORACLE_SAMPLE_ROWS * 100)} rows "
+                "(64 sources per word) in blocks of 25,000")
+    return f"float64 direct product over the first {ORACLE_SAMPLE_ROWS} rows in blocks of 250"
 
 
 def run_reference(args):
@@ -253,7 +274,8 @@ def run_reference(args):
     if rank != 0:
         return
     wl = WORKLOADS[args.workload]
-    gen, k = wl["gen"], wl["k"]
+    k = wl["k"]
+    gen = dict(n=wl["graph"]["nodes"], m=wl["graph"]["nodes"]) if "graph" in wl else wl["gen"]
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
     rates, _ = cpu_oracle_rates(args.workload, per_step, args.warmup + args.steps)
     rates = rates[args.warmup:]
@@ -262,11 +284,11 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "matvec/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "vs_baseline": None, "dtype": "u64" if "graph" in wl else "f64", "data": "synthetic",
         "config": {"workload": args.workload, "n": gen["n"], "m": gen["m"], "k": k},
         "cpu_baseline": {"value": value, "unit": "matvec/s", "cores": 1, "kind": "oracle",
-                         "sample": f"float64 direct product over the first {ORACLE_SAMPLE_ROWS} rows "
-                                   f"in blocks of 250, {per_step:.1f} s per step, scaled to whole products"},
+                         "sample": f"{oracle_sample_text(args.workload)}, {per_step:.1f} s per step, "
+                                   "scaled to whole products"},
         "e2e": {"value": value, "unit": "matvec/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -422,12 +444,12 @@ def run_ours(args):
     lay = eng.layout
     footprint = lay["grammar_bytes"] + lay["scratch_bytes"] + elem * k * (gen["m"] + gen["n"])
     cpu = None
-    if not args.no_cpu_baseline and not graph:
+    if not args.no_cpu_baseline:
         rates, recs = cpu_oracle_rates(args.workload, args.cpu_seconds)
         cpu = {"value": rates[0], "unit": "matvec/s", "cores": 1, "kind": "oracle",
-               "sample": f"{recs[0]['rows']} rows ({recs[0]['rows'] / gen['n']:.2f} products) of the "
-                         f"first {ORACLE_SAMPLE_ROWS} rows of the same matrix in {recs[0]['seconds']:.1f} s, "
-                         "float64, one BLAS thread"}
+               "sample": f"{recs[0]['rows']} rows ({recs[0]['rows'] / gen['n']:.3f} products) of the same "
+                         f"matrix in {recs[0]['seconds']:.1f} s: {oracle_sample_text(args.workload)}, "
+                         "one BLAS thread"}
     line = {
         "metric": METRIC, "value": value, "unit": "matvec/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
@@ -441,7 +463,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profile_traffic(f"sweep:{args.workload}"),
-                     "kernel": "whole product (leaf gather + level combines + row emit)",
+                     "kernel": ("whole product: sweep_kernel + slice_kernel" if launches_per_step == 2
+                                else "whole product: sweep_kernel"),
                      "algorithmic_bytes_per_launch": bytes_step},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": elem * k * gen["m"],

@@ -720,11 +720,13 @@ __device__ __forceinline__ void tile_sums(const SweepArgs<P>& a, int64_t base, u
     if (lane == 31 && incl >= 1) a.esum[base + incl - 1] = X;
 }
 
-// Slice s of [T | RV] into shared memory, then its tiles, one warp each; a
-// warp loads its next tile's offsets, starts and first start index before
-// reducing the current one.
+// Slice s of [T | RV] into shared memory, then its tiles: a warp claims tiles
+// from a counter in shared memory (so the CTA's warps finish together) and
+// loads its next tile's offsets, starts and first start index before reducing
+// the current one.
 template <class P>
 __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) {
+    __shared__ int32_t next_tile;
     using V = typename P::V;
     // values [x0, x1) in 16-byte units (x0 is a multiple of 256 values; the
     // last unit may run up to 15 bytes past x1, inside RV's padded allocation)
@@ -734,12 +736,18 @@ __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) 
     int4* dst = reinterpret_cast<int4*>(sv);
 #pragma unroll 4
     for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+    const int64_t t0 = __ldg(a.stile + s), nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) next_tile = (int32_t)nw;
     __syncthreads();
     if constexpr (P::LPN == 1) {
         const int lane = threadIdx.x & 31;
-        const int64_t nw = blockDim.x >> 5;
         const int64_t t1 = __ldg(a.stile + s + 1);
-        int64_t t = __ldg(a.stile + s) + (threadIdx.x >> 5);
+        auto claim = [&]() {
+            int32_t i = 0;
+            if (lane == 0) i = atomicAdd(&next_tile, 1);
+            return t0 + __shfl_sync(0xffffffffu, i, 0);
+        };
+        int64_t t = t0 + (threadIdx.x >> 5);
         uint4 o = make_uint4(0, 0, 0, 0);
         uint32_t f = 0;
         int32_t sb = 0;
@@ -749,7 +757,7 @@ __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) 
             sb = __ldg(a.tile_sid + t);
         }
         while (t < t1) {
-            const int64_t tn = t + nw;
+            const int64_t tn = claim();
             uint4 on = make_uint4(0, 0, 0, 0);
             uint32_t fn = 0;
             int32_t sbn = 0;
@@ -780,8 +788,13 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
     if (tail && blockIdx.x == 0) slice_tail<P>(a, slice_smem, (int64_t)a.slice * (int64_t)sizeof(V));
     const int64_t first = tail && gridDim.x > 1 ? 1 : 0;
     if (blockIdx.x >= first)
-        for (int64_t i = blockIdx.x - first; i < a.nslices; i += gridDim.x - first)
+        // slices heaviest first, dealt out in snake order: round r goes to the
+        // CTAs in reverse when r is odd
+        for (int64_t r = 0, g = gridDim.x - first, c = blockIdx.x - first;; ++r) {
+            const int64_t i = r * g + ((r & 1) ? g - 1 - c : c);
+            if (i >= a.nslices) break;
             slice_sums<P>(a, __ldg(a.sorder + i), reinterpret_cast<V*>(slice_smem));
+        }
     if (!coop) return;
     if (!grid_sync(a, 0)) return;
     emit_final<P>(a, ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, ((int64_t)gridDim.x * blockDim.x) >> 5);
