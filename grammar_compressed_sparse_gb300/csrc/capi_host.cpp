@@ -337,7 +337,7 @@ gc_status gc_layout(const gc_grammar* gg, gc_policy policy, int32_t k_max, gc_ar
         if (!gg || !out) fail(GC_ERR_ARG, "null argument");
         const Grammar& g = gg->g;
         check_policy(g, policy, k_max);
-        const DevLayout d = device_layout(g, policy, k_max);
+        const DevLayout d = device_layout(device_view(g, emit_mode(g, k_max) == EMIT_LEVEL), policy, k_max);
         gc_arena_layout l{};
         l.arena_bytes = d.total;
         l.grammar_bytes = d.grammar_bytes;

@@ -64,6 +64,10 @@ struct Grammar {
     std::vector<int32_t> node_id;          // n_nodes: rule i, or -(u+1) pass-through of u
     std::vector<int32_t> c_ref;            // |C|: >= 0 RV slot, < 0 T[-c-1]
     int64_t n_pass = 0, n_roots = 0, n_blocks = 1;
+    // device view only (see device_view in layout.hpp): carried nodes per
+    // level (roots, others) and the first carry slot of each level
+    std::vector<int64_t> carry_roots, carry_rest, carry_off;
+    int64_t n_carry = 0;
     double repair_seconds = 0, layer_seconds = 0;
 
     int64_t n_rules() const { return (int64_t)slp.rule_a.size(); }

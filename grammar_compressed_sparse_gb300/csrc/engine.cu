@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <type_traits>
 #include <memory>
 #include <mutex>
 
@@ -51,7 +52,7 @@
 struct gc_handle {
     gc_policy policy = GC_F32_SUM;
     int32_t k_max = 1;
-    int64_t n = 0, m = 0, L = 0, n_roots = 0, c_len = 0, max_width = 0, alpha = 0;
+    int64_t n = 0, m = 0, L = 0, n_roots = 0, c_len = 0, max_width = 0, alpha = 0, n_carry = 0;
     std::vector<int64_t> lv;      // host copy of the level table, 4 (L+2)
     char* arena = nullptr;
     gcs::DevLayout lay{};
@@ -72,8 +73,11 @@ namespace {
 constexpr int kThreads = 512;        // every kernel: 16 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3, LV_ECH = 4, LV_TOFF = 5;
+constexpr int LV_CR = 6, LV_CN = 7, LV_COFF = 8;   // carried roots, carried others, first carry slot
 constexpr int LV_ROWS = (int)kLevelRows;
-static_assert(LV_TOFF < LV_ROWS, "level table rows");
+static_assert(LV_COFF < LV_ROWS, "level table rows");
+// device index of carry slot s: kCarryBase + s (above every [T | buffer] index)
+constexpr int32_t kCarryBase = 1 << 30;
 
 
 void cuda_check(cudaError_t e, const char* what) {
@@ -172,6 +176,7 @@ struct SweepArgs {
     const int32_t* late_ref;
     V* esum;                  //   chunk sums
     V* tbuf;                  // the narrow top levels' values, level after level
+    V* carry;                 // values of nodes read two or more levels up
     int64_t tail_total;       // nodes of the tail levels (padded)
     int64_t n;
     int32_t emode;            // EmitMode
@@ -240,7 +245,7 @@ __device__ __forceinline__ void load_chunk_staged(const SweepArgs<P>& a, int k, 
 // [T | level k-1] index space; with kTail, references past T into level k-1
 // come from prev_tail instead (a narrow level kept in the tail buffers). The
 // values go to cur[t]; roots also to rv[t] when rv is given.
-template <class P, bool kTail>
+template <class P, bool kTail, bool kC>
 __device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int64_t c, const int2 (&ab)[Chunk<P>::U],
                                               const typename P::V* prev, const typename P::V* prev_tail,
                                               typename P::V* cur, typename P::V* rv, uint64_t keep) {
@@ -258,17 +263,29 @@ __device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int6
             vb[u] = node < w ? leaf_value<P>(ab[u].y, part, a) : P::identity();
         }
     } else {
+        // a child is a carry slot (index >= kCarryBase), a slot of level k-1
+        // (in the tail buffer with kTail, past T), or a T entry
+        auto child = [&](int32_t x) -> V {
+            if (kC && x >= kCarryBase) return a.carry[(int64_t)(x - kCarryBase) * P::LPN + part];
+            if (kTail && prev_tail != nullptr && x >= a.TB) return prev_tail[(int64_t)(x - a.TB) * P::LPN + part];
+            return prev[(int64_t)x * P::LPN + part];
+        };
 #pragma unroll
         for (int u = 0; u < Chunk<P>::U; ++u) {
-            if (kTail && prev_tail != nullptr) {
-                const int64_t xa = ab[u].x, xb = ab[u].y;
-                va[u] = xa >= a.TB ? prev_tail[(xa - a.TB) * P::LPN + part] : prev[xa * P::LPN + part];
-                vb[u] = xb >= a.TB ? prev_tail[(xb - a.TB) * P::LPN + part] : prev[xb * P::LPN + part];
-            } else {
-                va[u] = prev[(int64_t)ab[u].x * P::LPN + part];
-                vb[u] = prev[(int64_t)ab[u].y * P::LPN + part];
-            }
+            va[u] = child(ab[u].x);
+            vb[u] = child(ab[u].y);
         }
+    }
+    // carried nodes (kC): the first cr roots and the cn nodes after the roots,
+    // in carry slots from coff on (level sizes fit 32 bits); read levels later,
+    // so kept in L2
+    [[maybe_unused]] int32_t cr = 0, cn = 0, nr = 0;
+    [[maybe_unused]] V* carry = nullptr;
+    if constexpr (kC) {
+        cr = (int32_t)a.lvl(LV_CR, k);
+        cn = (int32_t)a.lvl(LV_CN, k);
+        nr = (int32_t)nroots;
+        carry = a.carry + a.lvl(LV_COFF, k) * P::LPN;
     }
 #pragma unroll
     for (int u = 0; u < Chunk<P>::U; ++u) {
@@ -277,6 +294,11 @@ __device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int6
             const V v = P::combine(va[u], vb[u]);
             cur[node * P::LPN + part] = v;
             if (rv != nullptr && node < nroots) st_keep(rv + node * P::LPN + part, v, keep);
+            if constexpr (kC) {
+                const int32_t t = (int32_t)node;
+                const int32_t cs = t < cr ? t : (t >= nr && t - nr < cn) ? cr + (t - nr) : -1;
+                if (cs >= 0) st_keep(carry + (int64_t)cs * P::LPN + part, v, keep);
+            }
         }
     }
 }
@@ -543,7 +565,7 @@ __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
 }
 
 // ---------------------------------------------------------------- persistent sweep
-template <class P>
+template <class P, bool kC>
 __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a) {
     // an unread earlier timeout left the barrier counter part-way: do nothing
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
@@ -588,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
             cn += GW;
             norm(kn, cn);
             if (kn <= Lg) load_chunk<P>(a, kn, cn, nab);   // next chunk, maybe of a later level
-            combine_chunk<P, false>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
+            combine_chunk<P, false, kC>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
         }
         if (lemit && k >= 2) {   // level k-1 is complete and still in its buffer
             emit_level<P>(a, k - 1, io.prev, gw, GW);
@@ -615,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
             for (int64_t c = w0; c < nchunks(k); c += kWarps) {
                 int2 ab[Chunk<P>::U];
                 load_chunk<P>(a, k, c, ab);
-                combine_chunk<P, true>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, keep);
+                combine_chunk<P, true, kC>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, keep);
             }
             __syncthreads();
         }
@@ -631,11 +653,12 @@ constexpr int kSliceThreads = 1024;
 // The narrow top levels on one CTA of kSliceThreads, with block barriers only:
 // node pairs and values in shared memory when both fit in `room` bytes, else
 // pairs and values in global memory; the values end in the tail buffer.
-template <class P>
+template <class P, bool kC>
 __device__ void slice_tail(const SweepArgs<P>& a, unsigned char* smem, int64_t room) {
     using V = typename P::V;
     const int Lg = a.grid_levels;
     const int w0 = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const uint64_t keep = l2_evict_last();
     const bool staged = (int64_t)(8 + sizeof(V) * P::LPN) * a.tail_total <= room;
     int2* tp = reinterpret_cast<int2*>(smem);
     V* tv = staged ? reinterpret_cast<V*>(tp + a.tail_total) : a.tbuf;
@@ -651,7 +674,7 @@ __device__ void slice_tail(const SweepArgs<P>& a, unsigned char* smem, int64_t r
             int2 ab[Chunk<P>::U];
             if (staged) load_chunk_staged<P>(a, k, c, tp + a.lvl(LV_TOFF, k), ab);
             else load_chunk<P>(a, k, c, ab);
-            combine_chunk<P, true>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, 0);
+            combine_chunk<P, true, kC>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, keep);
         }
         __syncthreads();
     }
@@ -779,13 +802,13 @@ __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) 
 // After the wide levels: slices on every CTA (CTA 0 runs the tail first when
 // the launch is cooperative and has more than one CTA; then it only waits),
 // and, cooperative, a grid barrier and the row pass.
-template <class P>
+template <class P, bool kC>
 __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs<P> a, int coop) {
     using V = typename P::V;
     extern __shared__ __align__(16) unsigned char slice_smem[];
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
     const bool tail = coop && a.grid_levels < a.L;
-    if (tail && blockIdx.x == 0) slice_tail<P>(a, slice_smem, (int64_t)a.slice * (int64_t)sizeof(V));
+    if (tail && blockIdx.x == 0) slice_tail<P, kC>(a, slice_smem, (int64_t)a.slice * (int64_t)sizeof(V));
     const int64_t first = tail && gridDim.x > 1 ? 1 : 0;
     if (blockIdx.x >= first)
         // slices heaviest first, dealt out in snake order: round r goes to the
@@ -801,7 +824,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
 }
 
 // ---------------------------------------------------------------- per-level schedule
-template <class P>
+template <class P, bool kC>
 __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a, int k) {
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -819,8 +842,8 @@ __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a
 #pragma unroll
         for (int u = 0; u < Chunk<P>::U; ++u) ab[u] = nab[u];
         if (c + GW < nc) load_chunk<P>(a, k, c + GW, nab);
-        if (tail) combine_chunk<P, true>(a, k, c, ab, tio.prev, tio.prev_tail, tio.cur, tio.rv, keep);
-        else combine_chunk<P, false>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
+        if (tail) combine_chunk<P, true, kC>(a, k, c, ab, tio.prev, tio.prev_tail, tio.cur, tio.rv, keep);
+        else combine_chunk<P, false, kC>(a, k, c, ab, io.prev, nullptr, io.cur, io.rv, keep);
     }
     // level k-1 (a wide one) is complete and still in its buffer
     if (a.emode == EMIT_LEVEL && k >= 2) {
@@ -908,6 +931,7 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.late_ref = reinterpret_cast<const int32_t*>(ar + d.late_ref);
     a.esum = reinterpret_cast<V*>(ar + d.esum);
     a.tbuf = reinterpret_cast<V*>(ar + d.tbuf);
+    a.carry = reinterpret_cast<V*>(ar + d.carry);
     a.tail_total = d.tail_total;
     a.n = h->n;
     a.emode = d.emit;
@@ -921,10 +945,10 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
 }
 
 // CTAs the persistent kernel can keep resident (at most two per SM; 0 if none)
-template <class P>
+template <class P, bool kC>
 int sweep_grid(const gc_handle* h) {
     int per_sm = 0;
-    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel<P>, kThreads, 0),
+    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sweep_kernel<P, kC>, kThreads, 0),
                "sweep occupancy");
     return std::min(per_sm, 2) * h->sms;
 }
@@ -943,14 +967,14 @@ int64_t slice_smem(const gc_handle* h) {
 }
 
 // CTAs of the cooperative slice kernel (one per SM; 0 if it cannot be resident).
-template <class P>
+template <class P, bool kC>
 int slice_grid(const gc_handle* h) {
     const int64_t smem = slice_smem<P>(h);
-    cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P, kC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)smem),
                "slice shared memory");
     int per_sm = 0;
-    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, slice_kernel<P>, kSliceThreads, (size_t)smem),
+    cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, slice_kernel<P, kC>, kSliceThreads, (size_t)smem),
                "slice occupancy");
     return per_sm >= 1 ? h->sms : 0;
 }
@@ -959,20 +983,20 @@ int slice_grid(const gc_handle* h) {
 // device allows, else one kernel per level). Returns the launch count and
 // adds the grid-barrier arrivals of the cooperative launches to *arrivals;
 // a.bar_base is the barrier counter's value when the first launch starts.
-template <class P>
-int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals) {
+template <class P, bool kC>
+int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals) {
     const bool slice = h->lay.emit == EMIT_SLICE;
     int grid = 0, grid2 = 0;
     if (h->schedule == 0 && h->coop) {
-        grid = sweep_grid<P>(h);
-        if (slice && grid > 0) grid2 = slice_grid<P>(h);
+        grid = sweep_grid<P, kC>(h);
+        if (slice && grid > 0) grid2 = slice_grid<P, kC>(h);
         if (slice && grid2 == 0) grid = 0;
     }
     int64_t launches = 0;
     *arrivals = 0;
     if (grid > 0) {
         void* args[] = {&a};
-        cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P>, dim3(grid), dim3(kThreads), args, 0, st),
+        cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P, kC>, dim3(grid), dim3(kThreads), args, 0, st),
                    "sweep launch");
         launches = 1;
         *arrivals = (unsigned long long)sweep_barriers(h) * (unsigned long long)grid;
@@ -981,7 +1005,7 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, uns
             b.bar_base = a.bar_base + *arrivals;
             int coop = 1;
             void* args2[] = {&b, &coop};
-            cuda_check(cudaLaunchCooperativeKernel((const void*)slice_kernel<P>, dim3(grid2), dim3(kSliceThreads),
+            cuda_check(cudaLaunchCooperativeKernel((const void*)slice_kernel<P, kC>, dim3(grid2), dim3(kSliceThreads),
                                                    args2, (size_t)slice_smem<P>(h), st),
                        "slice launch");
             ++launches;
@@ -991,11 +1015,11 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, uns
         // level 1 also writes the leaf tables; with no levels a table-only launch
         const int64_t w1 = h->L >= 1 ? h->lv[LV_W * (h->L + 2) + 1] : 0;
         const int64_t items = std::max<int64_t>(w1, (h->alpha + 1) * P::LPN);
-        level_kernel<P><<<grid_for(items, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, h->L >= 1 ? 1 : 0);
+        level_kernel<P, kC><<<grid_for(items, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, h->L >= 1 ? 1 : 0);
         ++launches;
         for (int k = 2; k <= h->L; ++k) {
             const int64_t w = h->lv[LV_W * (h->L + 2) + k];
-            level_kernel<P><<<grid_for(w, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, k);
+            level_kernel<P, kC><<<grid_for(w, Chunk<P>::NODES * kWarps, h->sms), kThreads, 0, st>>>(a, k);
             ++launches;
         }
         if (h->n > 0 && h->lay.emit == EMIT_ROWS) {
@@ -1004,11 +1028,11 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, uns
         } else if (h->n > 0) {
             if (slice) {
                 const int64_t smem = slice_smem<P>(h);
-                cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P>,
+                cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P, kC>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
                            "slice shared memory");
                 const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>(h->lay.n_slices, h->sms));
-                slice_kernel<P><<<g2, kSliceThreads, (size_t)smem, st>>>(a, 0);
+                slice_kernel<P, kC><<<g2, kSliceThreads, (size_t)smem, st>>>(a, 0);
             } else {
                 emit_kernel<P><<<grid_for(h->lay.n_echunks, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 0);
             }
@@ -1018,6 +1042,16 @@ int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, uns
     }
     cuda_check(cudaGetLastError(), "kernel launch");
     return launches;
+}
+
+// Carry slots exist only for the device view of 16-wide handles (float32);
+// the other policies are built without them.
+template <class P>
+int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals) {
+    if constexpr (std::is_same<P, PolF32>::value || std::is_same<P, PolF32x16>::value)
+        if (h->n_carry > 0) return launch_product_as<P, true>(h, a, st, arrivals);
+    if (h->n_carry > 0) fail(GC_ERR_UNSUPPORTED, "carry slots for a policy built without them");
+    return launch_product_as<P, false>(h, a, st, arrivals);
 }
 
 template <class P>
@@ -1084,7 +1118,7 @@ unsigned char* static_scratch_on_current_device() {
 // right-hand sides, in the arena's order: buffers, tail buffers, level-emit
 // sums or RV, then the status block.
 struct StaticParts {
-    int64_t buf0, buf1, esum, tbuf, rv, status, total;
+    int64_t buf0, buf1, esum, tbuf, carry, rv, status, total;
 };
 StaticParts static_parts(const gc_handle* h, int32_t k) {
     const DevLayout& d = h->lay;
@@ -1099,6 +1133,7 @@ StaticParts static_parts(const gc_handle* h, int32_t k) {
     s.buf0 = take(vb * (d.TB + h->max_width));
     s.buf1 = take(vb * (d.TB + h->max_width));
     s.tbuf = take(vb * d.tail_total);
+    s.carry = take(vb * std::max<int64_t>(1, h->n_carry));
     if (d.chunked()) s.esum = take(vb * d.n_esum);
     if (d.has_rv()) s.rv = take(vb * (d.TB + h->n_roots));
     s.status = take(256);
@@ -1120,6 +1155,7 @@ void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, u
     a.buf1 = reinterpret_cast<V*>(scratch + sp.buf1);
     a.esum = reinterpret_cast<V*>(scratch + sp.esum);
     a.tbuf = reinterpret_cast<V*>(scratch + sp.tbuf);
+    a.carry = reinterpret_cast<V*>(scratch + sp.carry);
     a.rv = reinterpret_cast<V*>(scratch + sp.rv);
     a.status = reinterpret_cast<int32_t*>(scratch + sp.status);
     a.bar = reinterpret_cast<unsigned long long*>(scratch + sp.status + 64);
@@ -1145,9 +1181,10 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         if (!gg || !out) fail(GC_ERR_ARG, "null grammar or output pointer");
         if (!arena) fail(GC_ERR_ARG, "null arena");
         if (reinterpret_cast<uintptr_t>(arena) % 256 != 0) fail(GC_ERR_ARG, "arena must be 256-byte aligned");
-        const Grammar& g = gg->g;
-        check_policy(g, policy, k_max);
-        validate_packed(g);
+        check_policy(gg->g, policy, k_max);
+        validate_packed(gg->g);
+        const Grammar g = device_view(gg->g, emit_mode(gg->g, k_max) == EMIT_LEVEL);   // carry slots for 16-wide values
+        validate_device_view(g);
         const DevLayout d = device_layout(g, policy, k_max);
         if (arena_bytes < d.total) fail(GC_ERR_ARG, "arena smaller than gc_layout().arena_bytes");
         cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1161,6 +1198,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         h->n_roots = g.n_roots;
         h->c_len = (int64_t)g.c_ref.size();
         h->max_width = g.max_width();
+        h->n_carry = g.n_carry;
         h->arena = static_cast<char*>(arena);
         h->lay = d;
         // row emit: groups of about one lane per symbol (rows average < 128)
@@ -1175,10 +1213,12 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
 
         // level table; level 1 with leaf codes, later levels with indices into [T | buffer]
         auto leaf_code = [&](int32_t p) { return (int32_t)(((int64_t)g.term_col[p] << d.vbits) | g.term_vidx[p]); };
-        auto ref = [&](int32_t c) -> int32_t {   // packed reference -> [T | buffer] index
+        const int64_t A = g.alpha();
+        auto ref = [&](int32_t c) -> int32_t {   // device-view reference -> device index
             if (c >= 0) return (int32_t)(d.TB + c);
             if (c == -1) return 0;
-            return -c - 1;                         // terminal p = -c-2 -> T[p+1]
+            if (c >= -(A + 1)) return -c - 1;      // terminal p = -c-2 -> T[p+1]
+            return kCarryBase + (int32_t)carry_slot(c, A);
         };
         h->lv.assign((size_t)(LV_ROWS * (L + 2)), 0);
         std::vector<int32_t> nodes((size_t)(2 * d.n_nodes_padded), 0);
@@ -1190,6 +1230,9 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             h->lv[LV_ROOTS * (L + 2) + k] = g.lvl_roots[k];
             h->lv[LV_ROFF * (L + 2) + k] = g.root_off[k];
             h->lv[LV_TOFF * (L + 2) + k] = toff[k];
+            h->lv[LV_CR * (L + 2) + k] = g.carry_roots[k];
+            h->lv[LV_CN * (L + 2) + k] = g.carry_rest[k];
+            h->lv[LV_COFF * (L + 2) + k] = g.carry_off[k];
             for (int64_t q = 0; q < w; ++q)
                 for (int t = 0; t < 2; ++t) {
                     const int32_t c = g.nodes[2 * (g.lvl_off[k] + q) + t];

@@ -4,9 +4,10 @@
 //   read-only grammar   nodes     int2[sum of padded widths]  child references,
 //                                 each level starting on a 16-node (128 B)
 //                                 boundary and padded to a multiple of 16
-//                       levels    int64[6 (L+2)]   per level k: padded start,
+//                       levels    int64[9 (L+2)]   per level k: padded start,
 //                                 width, roots, first RV slot, first emit chunk,
-//                                 offset in the tail buffer
+//                                 offset in the tail buffer, carried roots,
+//                                 carried other nodes, first carry slot
 //                       V         policy[|V|]      value dictionary
 //                       leaf      int32[alpha]     leaf code of terminal p
 //     level emit:       cref      int32[early]     C without the references to
@@ -32,6 +33,8 @@
 //                       buf1X     value[TB + w*]   values (the two streaming buffers)
 //                       tbuf      value[tail]      the narrow top levels' values,
 //                                                  level after level
+//                       carry     value[carried]   values of the nodes read two or
+//                                                  more levels up (device view)
 //     level / slice:    esum      value[chunks     chunk sums, or one sum per
 //                                       / starts]  segment start
 //     slice / row:      RVX       value[TB + rho]  leaf table T, then root values
@@ -85,7 +88,7 @@ namespace gcs {
 constexpr int64_t kNodeAlign = 16;        // nodes per 128-byte granule
 constexpr int64_t kEmitChunkSyms = 512;   // references per emit chunk
 constexpr int64_t kLongRowAvg = 128;      // average |C| per row for chunked emits
-constexpr int64_t kLevelRows = 6;         // rows of the level table
+constexpr int64_t kLevelRows = 9;         // rows of the level table
 
 enum EmitMode : int32_t { EMIT_LEVEL = 0, EMIT_SLICE = 1, EMIT_ROWS = 2 };
 
@@ -101,7 +104,7 @@ struct DevLayout {
     int64_t sref, sflag, tile_sid, row_pos, sx0, stile, sorder;   // slice emit
     int64_t row_ech, late_off, late_ref;  // level and slice emit
     int64_t c_off, c_ref;                 // row emit
-    int64_t buf0, buf1, esum, tbuf, RV, status, xs, ys;
+    int64_t buf0, buf1, esum, tbuf, carry, RV, status, xs, ys;
     int64_t total, grammar_bytes, scratch_bytes, staging_bytes;
     int64_t value_bytes;   // bytes of one node value (k_max elements)
     int64_t n_nodes_padded;
@@ -138,6 +141,166 @@ inline int64_t leaf_block(int64_t alpha) { return (alpha + 1 + 63) / 64 * 64; }
 inline EmitMode emit_mode(const Grammar& g, int32_t k_max) {
     const bool long_rows = g.n > 0 && (int64_t)g.c_ref.size() >= kLongRowAvg * g.n;
     return !long_rows ? EMIT_ROWS : k_max == 1 ? EMIT_SLICE : EMIT_LEVEL;
+}
+
+// Device view of a layered grammar. The pages' pass-through nodes (Sec. 4.2)
+// copy a value one level up; a chain of them carries a rule u to its highest
+// parent. With carry slots (used for 16-wide values, whose level buffers do
+// not stay in L2, so each copy costs a DRAM round trip) the device does not
+// execute the copies: every rule a parent reads two or more levels above it
+// (u has pass-throughs) stores its value once, when its level is computed,
+// into a carry slot, and parents read the slot where the layered grammar
+// reads u's chain element. Without carry slots (one-wide values, whose copies
+// read the level just written, in L2) the view is the layered grammar itself. x (+) identity = x for every
+// policy, so the values are the same; the node stream shrinks by the
+// pass-throughs. Each level lists its roots first (carried ones first), then
+// its other rules (carried ones first), each group in the packed order, so a
+// level's carried nodes are two runs of positions and their carry slots
+// follow from position. Child references: >= 0 a slot of the level below,
+// -2 - p terminal p, below -1 - alpha a carry slot (carry_ref / carry_slot).
+inline int32_t carry_ref(int64_t slot, int64_t alpha) { return (int32_t)(-(alpha + 2) - slot); }
+inline int64_t carry_slot(int32_t c, int64_t alpha) { return -(int64_t)c - (alpha + 2); }
+
+inline Grammar device_view(const Grammar& g, bool carry) {
+    const int64_t L = g.L, R = g.n_rules(), A = g.alpha();
+    Grammar d;
+    if (!carry) {
+        d.n = g.n;
+        d.m = g.m;
+        d.nnz = g.nnz;
+        d.L = L;
+        d.V = g.V;
+        d.term_col = g.term_col;
+        d.term_vidx = g.term_vidx;
+        d.slp.c_off = g.slp.c_off;
+        d.lvl_off = g.lvl_off;
+        d.lvl_roots = g.lvl_roots;
+        d.root_off = g.root_off;
+        d.n_roots = g.n_roots;
+        d.nodes = g.nodes;
+        d.node_id = g.node_id;
+        d.c_ref = g.c_ref;
+        d.carry_roots.assign((size_t)L + 2, 0);
+        d.carry_rest.assign((size_t)L + 2, 0);
+        d.carry_off.assign((size_t)L + 2, 0);
+        return d;
+    }
+    d.n = g.n;
+    d.m = g.m;
+    d.nnz = g.nnz;
+    d.L = L;
+    d.V = g.V;
+    d.term_col = g.term_col;
+    d.term_vidx = g.term_vidx;
+    d.slp.c_off = g.slp.c_off;
+    d.lvl_roots = g.lvl_roots;
+    d.root_off = g.root_off;
+    d.n_roots = g.n_roots;
+    std::vector<char> carried((size_t)R, 0);
+    for (int32_t id : g.node_id)
+        if (id < 0) carried[-(int64_t)id - 1] = 1;
+    std::vector<int32_t> pos((size_t)R, -1), cslot((size_t)R, -1);
+    d.lvl_off.assign((size_t)L + 2, 0);
+    d.carry_roots.assign((size_t)L + 2, 0);
+    d.carry_rest.assign((size_t)L + 2, 0);
+    d.carry_off.assign((size_t)L + 2, 0);
+    d.node_id.reserve((size_t)R);
+    int64_t off = 0, coff = 0;
+    for (int64_t k = 1; k <= L; ++k) {
+        d.lvl_off[k] = off;
+        d.carry_off[k] = coff;
+        const int64_t q0 = g.lvl_off[k], qr = q0 + g.lvl_roots[k], q1 = g.lvl_off[k + 1];
+        auto take = [&](int64_t a, int64_t b, bool want_carried, int64_t& count) {
+            for (int64_t q = a; q < b; ++q) {
+                const int32_t u = g.node_id[q];
+                if (u < 0 || (bool)carried[u] != want_carried) continue;   // pass-throughs are dropped
+                pos[u] = (int32_t)(off - d.lvl_off[k]);
+                if (want_carried) cslot[u] = (int32_t)coff++;
+                d.node_id.push_back(u);
+                ++off;
+                ++count;
+            }
+        };
+        int64_t cr = 0, cn = 0, rest = 0;
+        take(q0, qr, true, cr);
+        take(q0, qr, false, rest);
+        take(qr, q1, true, cn);
+        take(qr, q1, false, rest);
+        d.carry_roots[k] = cr;
+        d.carry_rest[k] = cn;
+    }
+    d.lvl_off[L + 1] = off;
+    d.carry_off[L + 1] = coff;
+    d.n_carry = coff;
+    if (coff >= (int64_t)INT32_MAX - A - 2) fail(GC_ERR_UNSUPPORTED, "too many carried nodes for 31-bit references");
+    // children: a rule at level k reads level k-1 slots; a host chain element
+    // there stands for its rule's carry slot
+    d.nodes.assign((size_t)2 * off, 0);
+    for (int64_t k = 1; k <= L; ++k)
+        for (int64_t i = d.lvl_off[k]; i < d.lvl_off[k + 1]; ++i) {
+            const int32_t u = d.node_id[i];
+            const int32_t kids[2] = {g.slp.rule_a[u], g.slp.rule_b[u]};
+            for (int t = 0; t < 2; ++t) {
+                const int32_t c = kids[t];
+                int32_t ref;
+                if (c < 0) {
+                    ref = c - 1;                                   // terminal -c-1 -> -2 - p
+                } else if (g.rule_level[c] == k - 1) {
+                    ref = pos[c];
+                } else {
+                    if (cslot[c] < 0) fail(GC_ERR_INVALID_GRAMMAR, "a rule skips levels without a carry slot");
+                    ref = carry_ref(cslot[c], A);
+                }
+                d.nodes[2 * i + t] = ref;
+            }
+        }
+    // C's root slots in the new order
+    d.c_ref.resize(g.c_ref.size());
+    for (size_t e = 0; e < g.c_ref.size(); ++e) {
+        const int32_t c = g.c_ref[e];
+        if (c < 0) {
+            d.c_ref[e] = c;
+            continue;
+        }
+        const int64_t k = std::upper_bound(g.root_off.begin() + 1, g.root_off.begin() + L + 2, (int64_t)c) -
+                          g.root_off.begin() - 1;
+        const int32_t u = g.node_id[g.lvl_off[k] + (c - g.root_off[k])];
+        d.c_ref[e] = (int32_t)(g.root_off[k] + pos[u]);
+    }
+    return d;
+}
+
+// Checks a device view: every child of a level-k node is a terminal, a slot
+// of level k-1, the identity (a pass-through's second child) or the carry slot
+// of a rule at least two levels down; carried runs lie inside their levels; C
+// names terminals and roots.
+inline void validate_device_view(const Grammar& d) {
+    const int64_t L = d.L, A = d.alpha();
+    auto bad = [](const char* what) { fail(GC_ERR_INVALID_GRAMMAR, std::string("device view: ") + what); };
+    if ((int64_t)d.lvl_off.size() != L + 2 || (int64_t)d.carry_off.size() != L + 2 ||
+        d.lvl_off[L + 1] * 2 != (int64_t)d.nodes.size() || d.carry_off[L + 1] != d.n_carry)
+        bad("level tables");
+    std::vector<int64_t> slot_level((size_t)d.n_carry, 0);
+    for (int64_t k = 1; k <= L; ++k) {
+        const int64_t w = d.lvl_off[k + 1] - d.lvl_off[k];
+        if (w < 0 || d.lvl_roots[k] > w || d.carry_roots[k] > d.lvl_roots[k] ||
+            d.lvl_roots[k] + d.carry_rest[k] > w || d.carry_off[k + 1] - d.carry_off[k] != d.carry_roots[k] + d.carry_rest[k])
+            bad("level sizes");
+        for (int64_t s = d.carry_off[k]; s < d.carry_off[k + 1]; ++s) slot_level[s] = k;
+    }
+    for (int64_t k = 1; k <= L; ++k) {
+        const int64_t wprev = k > 1 ? d.lvl_off[k] - d.lvl_off[k - 1] : 0;
+        for (int64_t i = 2 * d.lvl_off[k]; i < 2 * d.lvl_off[k + 1]; ++i) {
+            const int32_t c = d.nodes[i];
+            const bool ok = c >= 0                 ? c < wprev
+                            : c == -1              ? (i & 1) == 1 && k >= 2
+                            : c >= -(A + 1)        ? true
+                            : (carry_slot(c, A) < d.n_carry && slot_level[carry_slot(c, A)] < k - 1);
+            if (!ok || (k == 1 && c > -2) || (k == 1 && c < -(A + 1))) bad("child reference out of range");
+        }
+    }
+    for (int32_t c : d.c_ref)
+        if (c >= 0 ? c >= d.n_roots : (-(int64_t)c - 1) > A) bad("C reference out of range");
 }
 
 inline int64_t tail_width(int32_t k_max) { return k_max == 16 ? 1024 : 4096; }
@@ -611,6 +774,7 @@ inline EmitCounts count_level_emit(const Grammar& g, int64_t Lg) {
     return t;
 }
 
+// Sizes of the arena for the device view g (device_view) of a grammar.
 inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     DevLayout d{};
     const int64_t L = g.L, C = (int64_t)g.c_ref.size(), A = g.alpha();
@@ -676,6 +840,7 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.buf0 = take(d.value_bytes * (d.TB + w));
     d.buf1 = take(d.value_bytes * (d.TB + w));
     d.tbuf = take(d.value_bytes * d.tail_total);
+    d.carry = take(d.value_bytes * std::max<int64_t>(1, g.n_carry));
     if (d.chunked()) d.esum = take(d.value_bytes * d.n_esum);
     if (d.has_rv()) d.RV = take(d.value_bytes * (d.TB + g.n_roots));
     d.status = take(256);

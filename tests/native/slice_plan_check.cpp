@@ -1,10 +1,16 @@
-// Checks the slice emit's plan and its tile reduction on the CPU: builds the
-// plan the library uploads for each input matrix, replays the per-lane runs
-// and the segmented lane scan that tile_sums performs on the device (over
-// random values standing in for [T | RV]), and compares every row's sum of
-// segment sums with the direct sum of the row's early references. Also checks
-// that every segment start is written exactly once and that the counts used
-// to size the arena match the plan.
+// Checks two host-side constructions of the device path on the CPU.
+//
+// check_view: evaluates the device view of the grammar (pass-throughs replaced
+// by carry slots, levels compacted, C's roots renumbered) level by level from a
+// random x, exactly as the sweep reads it, and compares y with the direct
+// product of the input CSR matrix.
+//
+// check_slices: builds the slice plan the library uploads, replays the
+// per-lane runs and the segmented lane scan that tile_sums performs on the
+// device (over random values standing in for [T | RV]), and compares every
+// row's sum of segment sums with the direct sum of the row's early
+// references. Also checks that every segment start is written exactly once
+// and that the counts used to size the arena match the plan.
 //
 // Input files: int64 n, m, nnz; int64 row_ptr[n+1]; int32 col[nnz];
 // float32 val[nnz]. Exit status 0 when every check holds.
@@ -18,7 +24,59 @@
 
 using namespace gcs;
 
-static int check(const Grammar& g, int64_t value_bytes, int64_t tail_nodes) {
+static int check_view(const Grammar& host, const Grammar& g, const std::vector<int64_t>& rp,
+                      const std::vector<int32_t>& col, const std::vector<float>& val) {
+    validate_device_view(g);
+    const int64_t A = g.alpha(), L = g.L;
+    std::mt19937_64 rng(7);
+    std::uniform_real_distribution<double> U(-1, 1);
+    std::vector<double> x((size_t)g.m);
+    for (double& v : x) v = U(rng);
+    std::vector<double> T((size_t)A);
+    for (int64_t p = 0; p < A; ++p) T[p] = (double)g.V[g.term_vidx[p]] * x[g.term_col[p]];
+    std::vector<std::vector<double>> lv((size_t)L + 1);
+    std::vector<double> carry((size_t)std::max<int64_t>(1, g.n_carry));
+    for (int64_t k = 1; k <= L; ++k) {
+        const int64_t w = g.lvl_off[k + 1] - g.lvl_off[k];
+        lv[k].assign((size_t)w, 0);
+        auto child = [&](int32_t c) -> double {
+            if (c >= 0) return lv[k - 1][c];
+            if (c == -1) return 0.0;   // a pass-through's identity
+            if (c >= -(A + 1)) return T[-c - 2];
+            return carry[carry_slot(c, A)];
+        };
+        for (int64_t t = 0; t < w; ++t) {
+            const double v = child(g.nodes[2 * (g.lvl_off[k] + t)]) + child(g.nodes[2 * (g.lvl_off[k] + t) + 1]);
+            lv[k][t] = v;
+            const int64_t cr = g.carry_roots[k], cn = g.carry_rest[k], nr = g.lvl_roots[k];
+            const int64_t cs = t < cr ? t : (t >= nr && t - nr < cn) ? cr + (t - nr) : -1;
+            if (cs >= 0) carry[g.carry_off[k] + cs] = v;
+        }
+    }
+    double worst = 0;
+    for (int64_t r = 0; r < g.n; ++r) {
+        double got = 0, want = 0, mag = 0;
+        for (int64_t e = g.slp.c_off[r]; e < g.slp.c_off[r + 1]; ++e) {
+            const int32_t c = g.c_ref[e];
+            if (c < 0) {
+                got += T[-c - 2];
+            } else {
+                const int64_t k = ref_level(g, c);
+                got += lv[k][c - g.root_off[k]];
+            }
+        }
+        for (int64_t e = rp[r]; e < rp[r + 1]; ++e) {
+            want += (double)val[e] * x[col[e]];
+            mag += std::fabs((double)val[e] * x[col[e]]);
+        }
+        worst = std::max(worst, std::fabs(got - want) / (mag + 1e-300));
+    }
+    std::printf("view: n %ld nodes %ld (layered %ld) carried %ld  max scaled |y difference| %.3g\n", (long)g.n,
+                (long)g.lvl_off[L + 1], (long)host.n_nodes(), (long)g.n_carry, worst);
+    return worst < 1e-12 ? 0 : 1;
+}
+
+static int check_slices(const Grammar& g, int64_t value_bytes, int64_t tail_nodes) {
     const int64_t TB = leaf_block(g.alpha());
     const int64_t Lg = grid_level_count(g, tail_nodes);
     const int64_t S = slice_len(value_bytes);
@@ -132,8 +190,10 @@ int main(int argc, char** argv) {
         std::fclose(fp);
         gc_grammar* gg = nullptr;
         if (gc_build(n, m, rp.data(), col.data(), v.data(), nullptr, &gg) != GC_OK) return 2;
+        for (bool carry : {true, false}) bad |= check_view(gg->g, device_view(gg->g, carry), rp, col, v);
+        const Grammar dv = device_view(gg->g, false);
         for (int64_t vb : {4, 8})
-            for (int64_t tail : {4096, 1024}) bad |= check(gg->g, vb, tail);
+            for (int64_t tail : {4096, 1024}) bad |= check_slices(dv, vb, tail);
         gc_free_grammar(gg);
     }
     std::printf(bad ? "FAIL\n" : "OK\n");
