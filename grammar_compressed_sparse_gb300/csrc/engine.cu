@@ -357,11 +357,22 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
     const int slot = gl / P::LPN, part = gl % P::LPN;
     const int64_t warp = block * kWarps + (threadIdx.x >> 5);
     const int64_t nwarps = nblocks * kWarps;
+    // the next rows' C ranges are loaded before the current rows are reduced
+    int64_t row = warp * RPW + lane / GG;
+    int32_t s = 0, e = 0;
+    if (row < a.n) {
+        s = __ldg(a.c_off + row);
+        e = __ldg(a.c_off + row + 1);
+    }
     for (int64_t base = warp * RPW; base < a.n; base += nwarps * RPW) {
-        const int64_t row = base + lane / GG;
+        const int64_t nrow = row + nwarps * RPW;
+        int32_t ns = 0, ne = 0;
+        if (nrow < a.n) {
+            ns = __ldg(a.c_off + nrow);
+            ne = __ldg(a.c_off + nrow + 1);
+        }
         V acc = P::identity();
         if (row < a.n) {
-            const int32_t s = __ldg(a.c_off + row), e = __ldg(a.c_off + row + 1);
             for (int32_t q0 = s + slot; q0 < e; q0 += S * BATCH) {
                 int32_t c[BATCH];
 #pragma unroll
@@ -376,6 +387,9 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
 #pragma unroll
         for (int msk = GG / 2; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
         if (row < a.n && slot == 0) a.y[row * P::LPN + part] = acc;
+        row = nrow;
+        s = ns;
+        e = ne;
     }
 }
 
@@ -419,51 +433,11 @@ __device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, con
     if (slot == 0) a.esum[(int64_t)ch.z * P::LPN + part] = acc;
 }
 
-// Chunks j0 <= j < j1, spread over warps gwarp, gwarp + nwarps, ... For
-// one-lane 4-byte values a warp overlaps its chunks: it issues the current chunk's
-// gathers, then the next chunk's references and the header after that, and
-// only then waits; each chunk is reduced exactly as emit_chunk does.
+// Chunks j0 <= j < j1, spread over warps gwarp, gwarp + nwarps, ...
 template <class P>
 __device__ void emit_chunks(const SweepArgs<P>& a, int64_t j0, int64_t j1, const typename P::V* base, int64_t gwarp,
                             int64_t nwarps) {
-    using V = typename P::V;
-    if constexpr (P::LPN != 1 || sizeof(V) != 4) {
-        for (int64_t j = j0 + gwarp; j < j1; j += nwarps) emit_chunk<P>(a, j, base);
-    } else {
-        constexpr int PER = kEmitChunk / 32;
-        const int lane = threadIdx.x & 31;
-        int64_t j = j0 + gwarp;
-        if (j >= j1) return;
-        auto refs = [&](const int4& ch, int32_t (&r)[PER]) {
-#pragma unroll
-            for (int u = 0; u < PER; ++u) r[u] = u * 32 + lane < ch.y ? __ldcs(a.cref + ch.x + u * 32 + lane) : 0;
-        };
-        int4 ch = __ldg(a.echunk + j);
-        int32_t r[PER];
-        refs(ch, r);
-        int4 chn = j + nwarps < j1 ? __ldg(a.echunk + j + nwarps) : make_int4(0, 0, 0, 0);
-        for (;;) {
-            V v[PER];
-#pragma unroll
-            for (int u = 0; u < PER; ++u) v[u] = base[r[u]];
-            const int64_t jn = j + nwarps;
-            int4 chnn = make_int4(0, 0, 0, 0);
-            if (jn < j1) {
-                refs(chn, r);
-                if (jn + nwarps < j1) chnn = __ldg(a.echunk + jn + nwarps);
-            }
-            V acc = P::identity();
-#pragma unroll
-            for (int u = 0; u < PER; ++u) acc = P::combine(acc, v[u]);
-#pragma unroll
-            for (int msk = 16; msk >= 1; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
-            if (lane == 0) a.esum[ch.z] = acc;
-            if (jn >= j1) break;
-            j = jn;
-            ch = chn;
-            chn = chnn;
-        }
-    }
+    for (int64_t j = j0 + gwarp; j < j1; j += nwarps) emit_chunk<P>(a, j, base);
 }
 
 // The chunks of level k (0 = bare terminals).
@@ -1201,10 +1175,13 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         h->n_carry = g.n_carry;
         h->arena = static_cast<char*>(arena);
         h->lay = d;
-        // row emit: groups of about one lane per symbol (rows average < 128)
+        // row emit (rows average < 128 symbols): G lanes per row, so that a
+        // lane loads about one batch of a row's symbols (4 one-lane values, 2
+        // four-lane ones) and a warp reduces 32 / G rows at a time
         const double avg = g.n > 0 ? (double)h->c_len / (double)g.n : 0.0;
+        const int batch = k_max == 16 ? 2 : 4;
         int G = 1;
-        while (G < 32 && G < avg) G <<= 1;
+        while (G < 32 && G * batch < avg) G <<= 1;
         h->emit_group = d.emit == EMIT_ROWS ? G : 0;
         // levels narrow enough for one CTA finish the sweep there (when two or more)
         const int64_t L = g.L;
