@@ -62,6 +62,7 @@ struct gc_handle {
     int coop = 0;                 // device supports cooperative launch
     int grid_levels = 0;          // levels 1..grid_levels use the whole grid
     unsigned long long bar_base = 0;   // barrier arrivals of all earlier persistent launches
+    unsigned long long tbar_base = 0;  // arrivals on the slice kernel's tail-group counter
     long long timeout_cycles = 4000000000LL;
     int32_t inject = 0;           // test-only: 1 = CTA 0 skips its first barrier arrival
     int64_t launches = 0;
@@ -184,6 +185,9 @@ struct SweepArgs {
     int32_t* status;
     unsigned long long* bar;
     unsigned long long bar_base;
+    unsigned long long* tbar;        // slice emit: the tail group's arrival counter
+    unsigned long long tbar_base;
+    int32_t tail_group;              //   CTAs of the slice kernel that run the tail
     long long timeout;
     int32_t inject;
 
@@ -503,21 +507,24 @@ __device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks)
 // cycles (or when another CTA already reported a timeout), sets the status
 // word and returns false. The acquire at gpu scope, followed by the block
 // barrier, orders every thread's later loads after the other CTAs' writes.
+// Barrier j of `members` CTAs on the arrival counter bar, whose value was
+// base when the launch started.
 template <class P>
-__device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
+__device__ bool sync_on(const SweepArgs<P>& a, unsigned long long* bar, unsigned long long base, unsigned long long j,
+                        unsigned long long members) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        const bool skip = a.inject == 1 && blockIdx.x == 0 && j == 0;   // test-only
+        const bool skip = a.inject == 1 && blockIdx.x == 0 && j == 0 && bar == a.bar;   // test-only
         if (!skip) {
             __threadfence();
-            red_add_release(a.bar, 1ull);
+            red_add_release(bar, 1ull);
         }
-        const unsigned long long target = a.bar_base + (j + 1) * (unsigned long long)gridDim.x;
+        const unsigned long long target = base + (j + 1) * members;
         const long long t0 = clock64();
         unsigned it = 0;
-        while (ld_acquire(a.bar) < target) {
+        while (ld_acquire(bar) < target) {
             if ((++it & 63u) == 0) {
                 if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) {
                     ok = 0;
@@ -536,6 +543,11 @@ __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+template <class P>
+__device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
+    return sync_on<P>(a, a.bar, a.bar_base, j, gridDim.x);
 }
 
 // ---------------------------------------------------------------- persistent sweep
@@ -623,37 +635,52 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
 
 // ---------------------------------------------------------------- slice emit
 constexpr int kSliceThreads = 1024;
+constexpr int kTailGroup = 16;   // CTAs of the slice kernel that run the tail
 
-// The narrow top levels on one CTA of kSliceThreads, with block barriers only:
-// node pairs and values in shared memory when both fit in `room` bytes, else
-// pairs and values in global memory; the values end in the tail buffer.
+// The narrow top levels on the slice kernel's first `group` CTAs, chunks
+// dealt over their warps, a barrier of the group between levels (on its own
+// counter), values in the tail buffer. As in the sweep, a warp loads its next
+// chunk's child pairs, possibly of the next level, before gathering the
+// current chunk's children.
 template <class P, bool kC>
-__device__ void slice_tail(const SweepArgs<P>& a, unsigned char* smem, int64_t room) {
-    using V = typename P::V;
+__device__ bool slice_tail(const SweepArgs<P>& a, int64_t group) {
     const int Lg = a.grid_levels;
-    const int w0 = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int32_t nw = (int32_t)(group * (blockDim.x >> 5)), w0 = (int32_t)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
     const uint64_t keep = l2_evict_last();
-    const bool staged = (int64_t)(8 + sizeof(V) * P::LPN) * a.tail_total <= room;
-    int2* tp = reinterpret_cast<int2*>(smem);
-    V* tv = staged ? reinterpret_cast<V*>(tp + a.tail_total) : a.tbuf;
-    if (staged) {
-        const int2* src = a.nodes + a.lvl(LV_START, Lg + 1);
-        for (int64_t i = threadIdx.x; i < a.tail_total; i += blockDim.x) tp[i] = __ldcs(src + i);
-        __syncthreads();
-    }
+    auto nchunks = [&](int k) { return (int32_t)((a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES); };
+    auto norm = [&](int& k, int32_t& c) {
+        while (k <= a.L && c >= nchunks(k)) {
+            ++k;
+            c = w0;
+        }
+    };
+    int kn = Lg + 1;
+    int32_t cn = w0;
+    norm(kn, cn);
+    int2 nab[Chunk<P>::U];
+    if (kn <= a.L) load_chunk<P>(a, kn, cn, nab);
+    unsigned long long j = 0;
     for (int k = Lg + 1; k <= a.L; ++k) {
-        const TailIO<P> io = tail_io<P>(a, k, tv);
-        const int64_t nc = (a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES;
-        for (int64_t c = w0; c < nc; c += nw) {
+        if (k > Lg + 1) {
+            if (group > 1) {
+                if (!sync_on<P>(a, a.tbar, a.tbar_base, j++, (unsigned long long)group)) return false;
+            } else {
+                __syncthreads();
+            }
+        }
+        const TailIO<P> io = tail_io<P>(a, k, a.tbuf);
+        while (kn == k) {
             int2 ab[Chunk<P>::U];
-            if (staged) load_chunk_staged<P>(a, k, c, tp + a.lvl(LV_TOFF, k), ab);
-            else load_chunk<P>(a, k, c, ab);
+#pragma unroll
+            for (int u = 0; u < Chunk<P>::U; ++u) ab[u] = nab[u];
+            const int32_t c = cn;
+            cn += nw;
+            norm(kn, cn);
+            if (kn <= a.L) load_chunk<P>(a, kn, cn, nab);
             combine_chunk<P, true, kC>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, keep);
         }
-        __syncthreads();
     }
-    if (staged)
-        for (int64_t i = threadIdx.x; i < a.tail_total * P::LPN; i += blockDim.x) a.tbuf[i] = tv[i];
+    return true;
 }
 
 // One tile of a slice, on one warp: lane l holds references 8l .. 8l+7 (their
@@ -782,8 +809,11 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
     extern __shared__ __align__(16) unsigned char slice_smem[];
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
     const bool tail = coop && a.grid_levels < a.L;
-    if (tail && blockIdx.x == 0) slice_tail<P, kC>(a, slice_smem, (int64_t)a.slice * (int64_t)sizeof(V));
-    const int64_t first = tail && gridDim.x > 1 ? 1 : 0;
+    // the first tail_group CTAs run the tail (all of them when the grid is
+    // that small), the others the slices
+    const int64_t group = !tail ? 0 : gridDim.x > a.tail_group ? a.tail_group : gridDim.x;
+    if (tail && blockIdx.x < group && !slice_tail<P, kC>(a, group)) return;
+    const int64_t first = group < gridDim.x ? group : 0;
     if (blockIdx.x >= first)
         // slices heaviest first, dealt out in snake order: round r goes to the
         // CTAs in reverse when r is odd
@@ -912,9 +942,12 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.emit_group = h->emit_group;
     a.status = reinterpret_cast<int32_t*>(ar + d.status);
     a.bar = reinterpret_cast<unsigned long long*>(ar + d.status + 64);
+    a.tbar = reinterpret_cast<unsigned long long*>(ar + d.status + 128);
+    a.tbar_base = h->tbar_base;
     a.bar_base = h->bar_base;
     a.timeout = h->timeout_cycles;
     a.inject = h->inject;
+    a.tail_group = 1;
     return a;
 }
 
@@ -958,7 +991,8 @@ int slice_grid(const gc_handle* h) {
 // adds the grid-barrier arrivals of the cooperative launches to *arrivals;
 // a.bar_base is the barrier counter's value when the first launch starts.
 template <class P, bool kC>
-int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals) {
+int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals,
+                          unsigned long long* tail_arrivals) {
     const bool slice = h->lay.emit == EMIT_SLICE;
     int grid = 0, grid2 = 0;
     if (h->schedule == 0 && h->coop) {
@@ -968,6 +1002,7 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
     }
     int64_t launches = 0;
     *arrivals = 0;
+    *tail_arrivals = 0;
     if (grid > 0) {
         void* args[] = {&a};
         cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P, kC>, dim3(grid), dim3(kThreads), args, 0, st),
@@ -977,6 +1012,7 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
         if (slice) {
             SweepArgs<P> b = a;
             b.bar_base = a.bar_base + *arrivals;
+            b.tail_group = std::min(kTailGroup, grid2);
             int coop = 1;
             void* args2[] = {&b, &coop};
             cuda_check(cudaLaunchCooperativeKernel((const void*)slice_kernel<P, kC>, dim3(grid2), dim3(kSliceThreads),
@@ -984,6 +1020,8 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
                        "slice launch");
             ++launches;
             *arrivals += (unsigned long long)grid2;
+            if (b.tail_group > 1 && h->L > h->grid_levels)   // tail-group barriers between tail levels
+                *tail_arrivals = (unsigned long long)(h->L - h->grid_levels - 1) * (unsigned long long)b.tail_group;
         }
     } else {
         // level 1 also writes the leaf tables; with no levels a table-only launch
@@ -1021,19 +1059,21 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
 // Carry slots exist only for the device view of 16-wide handles (float32);
 // the other policies are built without them.
 template <class P>
-int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals) {
+int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals,
+                       unsigned long long* tail_arrivals) {
     if constexpr (std::is_same<P, PolF32>::value || std::is_same<P, PolF32x16>::value)
-        if (h->n_carry > 0) return launch_product_as<P, true>(h, a, st, arrivals);
+        if (h->n_carry > 0) return launch_product_as<P, true>(h, a, st, arrivals, tail_arrivals);
     if (h->n_carry > 0) fail(GC_ERR_UNSUPPORTED, "carry slots for a policy built without them");
-    return launch_product_as<P, false>(h, a, st, arrivals);
+    return launch_product_as<P, false>(h, a, st, arrivals, tail_arrivals);
 }
 
 template <class P>
 void run_product(gc_handle* h, const void* x, void* y, cudaStream_t st) {
     SweepArgs<P> a = make_args<P>(h, x, y);
-    unsigned long long arrivals = 0;
-    h->launches = launch_product<P>(h, a, st, &arrivals);
+    unsigned long long arrivals = 0, tail_arrivals = 0;
+    h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals);
     h->bar_base += arrivals;
+    h->tbar_base += tail_arrivals;
 }
 
 void dispatch_product(gc_handle* h, const void* x, void* y, int32_t k, cudaStream_t st) {
@@ -1134,12 +1174,14 @@ void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, u
     a.status = reinterpret_cast<int32_t*>(scratch + sp.status);
     a.bar = reinterpret_cast<unsigned long long*>(scratch + sp.status + 64);
     a.bar_base = 0;
+    a.tbar = reinterpret_cast<unsigned long long*>(scratch + sp.status + 128);
+    a.tbar_base = 0;
     a.inject = 0;
     // the array keeps the previous call's contents: start from a clear status
     // word and barrier counter
     cuda_check(cudaMemsetAsync(scratch + sp.status, 0, 256, st), "fixed scratch clear");
-    unsigned long long arrivals = 0;
-    h->launches = launch_product<P>(h, a, st, &arrivals);
+    unsigned long long arrivals = 0, tail_arrivals = 0;
+    h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals);
 }
 
 }  // namespace
@@ -1376,6 +1418,7 @@ gc_status gc_check(gc_handle* h, void* stream) {
             cuda_check(cudaMemsetAsync(h->arena + h->lay.status, 0, 256, st), "status clear");
             cuda_check(cudaStreamSynchronize(st), "stream synchronize");
             h->bar_base = 0;
+            h->tbar_base = 0;
         }
         rc = (gc_status)s;
     });

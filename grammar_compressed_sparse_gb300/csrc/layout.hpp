@@ -38,8 +38,8 @@
 //     level / slice:    esum      value[chunks     chunk sums, or one sum per
 //                                       / starts]  segment start
 //     slice / row:      RVX       value[TB + rho]  leaf table T, then root values
-//                       status    256 B            status word, fixpoint flag,
-//                                                  grid-barrier arrival counter
+//                       status    256 B            status word, fixpoint flag, grid-
+//                                                  barrier and tail-group arrival counters
 //   staging             xs        value[m]         x / y copies for the
 //                       ys        value[n]         host-buffer entry point
 // "value" is k_max elements of the policy's type (float, int64, uint64);
@@ -57,7 +57,9 @@
 //
 // Levels 1..Lg are wide and use the whole grid; the narrow levels above them
 // (each at most tail_nodes wide, two or more of them) form the tail, computed
-// by one CTA into the tail buffer, where they all stay until the product ends.
+// into the tail buffer, where they all stay until the product ends: by one CTA
+// in the level and row emits, by a group of CTAs beside the slices in the
+// slice emit (whose tail takes wider levels).
 //
 // Emit modes (Lemma 2.2, y[r] = sum of row r's symbols of C). C's references
 // to the tail levels ("late" references, few) are kept per row and added by
@@ -304,6 +306,9 @@ inline void validate_device_view(const Grammar& d) {
 }
 
 inline int64_t tail_width(int32_t k_max) { return k_max == 16 ? 1024 : 4096; }
+// the slice emit's tail runs on a group of CTAs beside the slices, so it
+// takes the levels up to this width
+constexpr int64_t kSliceTailNodes = 65536;
 
 // Lg: the narrow levels at the top (each at most tail_nodes wide) form the
 // tail when there are two or more of them; otherwise every level is wide.
@@ -782,7 +787,7 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     d.vbits = value_bits((int64_t)g.V.size());
     d.TB = leaf_block(A);
     d.emit = emit_mode(g, k_max);
-    d.tail_nodes = tail_width(k_max);
+    d.tail_nodes = d.emit == EMIT_SLICE ? kSliceTailNodes : tail_width(k_max);
     d.grid_levels = grid_level_count(g, d.tail_nodes);
     d.tail_total = tail_offsets(g, d.grid_levels)[L + 1];
     d.n_nodes_padded = 0;

@@ -193,7 +193,7 @@ int main(int argc, char** argv) {
         for (bool carry : {true, false}) bad |= check_view(gg->g, device_view(gg->g, carry), rp, col, v);
         const Grammar dv = device_view(gg->g, false);
         for (int64_t vb : {4, 8})
-            for (int64_t tail : {4096, 1024}) bad |= check_slices(dv, vb, tail);
+            for (int64_t tail : {kSliceTailNodes, (int64_t)4096, (int64_t)1024}) bad |= check_slices(dv, vb, tail);
         gc_free_grammar(gg);
     }
     std::printf(bad ? "FAIL\n" : "OK\n");
