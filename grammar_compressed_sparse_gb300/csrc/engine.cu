@@ -487,6 +487,85 @@ __device__ void emit_final(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps)
     }
 }
 
+// The row pass of the slice kernel, split around its grid barrier. Which sums
+// and tail values a row adds (its sum positions and late references) does not
+// depend on the slices, so plan_rows reads them for the warp's first R rows
+// before the barrier, as indices: e >= 0 a sum, e <= -2 tail value -2 - e,
+// -1 nothing. finish_rows then only gathers; rows with more than B * NS items
+// and rows past the first R go through emit_final's loop.
+template <int R, int B>
+struct RowPlan {
+    int32_t e[R][B];
+    int32_t total[R];
+};
+
+template <class P, int R, int B>
+__device__ void plan_rows(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps, RowPlan<R, B>& pl) {
+    constexpr int NS = 32 / P::LPN;
+    const int slot = (threadIdx.x & 31) / P::LPN;
+    int32_t c0[R], nc[R], q0[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int64_t row = gwarp + j * nwarps;
+        if (row < a.n) {
+            c0[j] = __ldg(a.row_ech + row);
+            nc[j] = __ldg(a.row_ech + row + 1) - c0[j];
+            q0[j] = __ldg(a.late_off + row);
+            pl.total[j] = nc[j] + (__ldg(a.late_off + row + 1) - q0[j]);
+        } else {
+            c0[j] = nc[j] = q0[j] = pl.total[j] = 0;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int32_t i = u * NS + slot;
+            pl.e[j][u] = i >= pl.total[j] ? -1
+                         : i < nc[j]      ? (a.row_pos ? __ldg(a.row_pos + c0[j] + i) : c0[j] + i)
+                                          : -2 - __ldg(a.late_ref + q0[j] + (i - nc[j]));
+        }
+}
+
+template <class P, int R, int B>
+__device__ void finish_rows(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps, const RowPlan<R, B>& pl) {
+    using V = typename P::V;
+    constexpr int NS = 32 / P::LPN;
+    const int lane = threadIdx.x & 31;
+    const int part = lane % P::LPN, slot = lane / P::LPN;
+    V v[R][B];
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int32_t e = pl.e[j][u];
+            v[j][u] = e == -1 ? P::identity()
+                      : e >= 0 ? a.esum[(int64_t)e * P::LPN + part]
+                               : a.tbuf[(int64_t)(-2 - e) * P::LPN + part];
+        }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int64_t row = gwarp + j * nwarps;
+        if (row >= a.n) break;
+        V acc = v[j][0];
+#pragma unroll
+        for (int u = 1; u < B; ++u) acc = P::combine(acc, v[j][u]);
+        if (pl.total[j] > B * NS) {   // the rest of a long row
+            const int32_t c0 = __ldg(a.row_ech + row), nc = __ldg(a.row_ech + row + 1) - c0;
+            const int32_t q0 = __ldg(a.late_off + row);
+            for (int32_t i = B * NS + slot; i < pl.total[j]; i += NS) {
+                const V w = i < nc ? a.esum[(a.row_pos ? (int64_t)__ldg(a.row_pos + c0 + i) : (int64_t)(c0 + i)) * P::LPN + part]
+                                   : a.tbuf[(int64_t)__ldg(a.late_ref + q0 + (i - nc)) * P::LPN + part];
+                acc = P::combine(acc, w);
+            }
+        }
+#pragma unroll
+        for (int msk = 16; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
+        if (slot == 0) a.y[row * P::LPN + part] = acc;
+    }
+    if (gwarp + R * nwarps < a.n) emit_final<P>(a, gwarp + R * nwarps, nwarps);
+}
+
 // Row emit: groups of G lanes per row (emit_group = G).
 template <class P>
 __device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
@@ -800,9 +879,9 @@ __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) 
     __syncthreads();
 }
 
-// After the wide levels: slices on every CTA (CTA 0 runs the tail first when
-// the launch is cooperative and has more than one CTA; then it only waits),
-// and, cooperative, a grid barrier and the row pass.
+// After the wide levels: slices on every CTA (when the launch is cooperative,
+// the first tail_group CTAs run the tail instead), and, cooperative, the row
+// plan, a grid barrier and the row pass.
 template <class P, bool kC>
 __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs<P> a, int coop) {
     using V = typename P::V;
@@ -823,8 +902,17 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
             slice_sums<P>(a, __ldg(a.sorder + i), reinterpret_cast<V*>(slice_smem));
         }
     if (!coop) return;
-    if (!grid_sync(a, 0)) return;
-    emit_final<P>(a, ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, ((int64_t)gridDim.x * blockDim.x) >> 5);
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, GW = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    if constexpr (P::LPN == 1) {
+        constexpr int R = sizeof(V) <= 4 ? 3 : 2;
+        RowPlan<R, 8> pl;
+        plan_rows<P>(a, gw, GW, pl);
+        if (!grid_sync(a, 0)) return;
+        finish_rows<P>(a, gw, GW, pl);
+    } else {
+        if (!grid_sync(a, 0)) return;
+        emit_final<P>(a, gw, GW);
+    }
 }
 
 // ---------------------------------------------------------------- per-level schedule
