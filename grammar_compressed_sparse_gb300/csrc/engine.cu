@@ -188,6 +188,7 @@ struct SweepArgs {
     unsigned long long* tbar;        // slice emit: the tail group's arrival counter
     unsigned long long tbar_base;
     int32_t tail_group;              //   CTAs of the slice kernel that run the tail
+    int32_t tail_solo;               //   first tail level CTA 0 runs alone (L + 1: none)
     long long timeout;
     int32_t inject;
 
@@ -629,6 +630,16 @@ __device__ bool grid_sync(const SweepArgs<P>& a, unsigned long long j) {
     return sync_on<P>(a, a.bar, a.bar_base, j, gridDim.x);
 }
 
+// Arrival at a barrier of bar without waiting for it (a CTA that has no work
+// after it, but whose writes the waiting CTAs read).
+__device__ __forceinline__ void arrive_on(unsigned long long* bar) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_add_release(bar, 1ull);
+    }
+}
+
 // ---------------------------------------------------------------- persistent sweep
 template <class P, bool kC>
 __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a) {
@@ -718,15 +729,19 @@ constexpr int kTailGroup = 16;   // CTAs of the slice kernel that run the tail
 
 // The narrow top levels on the slice kernel's first `group` CTAs, chunks
 // dealt over their warps, a barrier of the group between levels (on its own
-// counter), values in the tail buffer. As in the sweep, a warp loads its next
-// chunk's child pairs, possibly of the next level, before gathering the
-// current chunk's children.
+// counter), values in the tail buffer. From level a.tail_solo on (at most one
+// chunk per warp of a CTA) CTA 0 goes on alone with block barriers: the other
+// CTAs arrive at the barrier before that level and leave. As in the sweep, a
+// warp loads its next chunk's child pairs, possibly of the next level, before
+// gathering the current chunk's children.
 template <class P, bool kC>
 __device__ bool slice_tail(const SweepArgs<P>& a, int64_t group) {
-    const int Lg = a.grid_levels;
-    const int32_t nw = (int32_t)(group * (blockDim.x >> 5)), w0 = (int32_t)(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+    const int Lg = a.grid_levels, ks = a.tail_solo;
+    const int32_t wpc = (int32_t)(blockDim.x >> 5), nw = (int32_t)group * wpc;
+    const int32_t w0 = (int32_t)blockIdx.x * wpc + (int32_t)(threadIdx.x >> 5);
     const uint64_t keep = l2_evict_last();
     auto nchunks = [&](int k) { return (int32_t)((a.lvl(LV_W, k) + Chunk<P>::NODES - 1) / Chunk<P>::NODES); };
+    auto stride = [&](int k) { return k < ks ? nw : wpc; };
     auto norm = [&](int& k, int32_t& c) {
         while (k <= a.L && c >= nchunks(k)) {
             ++k;
@@ -741,7 +756,11 @@ __device__ bool slice_tail(const SweepArgs<P>& a, int64_t group) {
     unsigned long long j = 0;
     for (int k = Lg + 1; k <= a.L; ++k) {
         if (k > Lg + 1) {
-            if (group > 1) {
+            if (group > 1 && k <= ks) {
+                if (k == ks && blockIdx.x != 0) {
+                    arrive_on(a.tbar);
+                    return true;
+                }
                 if (!sync_on<P>(a, a.tbar, a.tbar_base, j++, (unsigned long long)group)) return false;
             } else {
                 __syncthreads();
@@ -753,7 +772,7 @@ __device__ bool slice_tail(const SweepArgs<P>& a, int64_t group) {
 #pragma unroll
             for (int u = 0; u < Chunk<P>::U; ++u) ab[u] = nab[u];
             const int32_t c = cn;
-            cn += nw;
+            cn += stride(kn);
             norm(kn, cn);
             if (kn <= a.L) load_chunk<P>(a, kn, cn, nab);
             combine_chunk<P, true, kC>(a, k, c, ab, io.prev, io.prev_tail, io.cur, io.rv, keep);
@@ -905,7 +924,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, GW = ((int64_t)gridDim.x * blockDim.x) >> 5;
     if constexpr (P::LPN == 1) {
         constexpr int R = sizeof(V) <= 4 ? 3 : 2;
-        RowPlan<R, 8> pl;
+        RowPlan<R, 10> pl;
         plan_rows<P>(a, gw, GW, pl);
         if (!grid_sync(a, 0)) return;
         finish_rows<P>(a, gw, GW, pl);
@@ -1036,6 +1055,7 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.timeout = h->timeout_cycles;
     a.inject = h->inject;
     a.tail_group = 1;
+    a.tail_solo = h->L + 1;
     return a;
 }
 
@@ -1101,6 +1121,12 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
             SweepArgs<P> b = a;
             b.bar_base = a.bar_base + *arrivals;
             b.tail_group = std::min(kTailGroup, grid2);
+            // the top levels of at most one chunk per warp of a CTA run on CTA 0 alone
+            const int64_t solo_nodes = (int64_t)Chunk<P>::NODES * (kSliceThreads / 32);
+            int ks = h->L + 1;
+            while (ks - 1 > h->grid_levels && h->lv[LV_W * (h->L + 2) + ks - 1] <= solo_nodes) --ks;
+            b.tail_solo = ks;
+            if (ks == h->grid_levels + 1) b.tail_group = 1;
             int coop = 1;
             void* args2[] = {&b, &coop};
             cuda_check(cudaLaunchCooperativeKernel((const void*)slice_kernel<P, kC>, dim3(grid2), dim3(kSliceThreads),
@@ -1108,8 +1134,9 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
                        "slice launch");
             ++launches;
             *arrivals += (unsigned long long)grid2;
-            if (b.tail_group > 1 && h->L > h->grid_levels)   // tail-group barriers between tail levels
-                *tail_arrivals = (unsigned long long)(h->L - h->grid_levels - 1) * (unsigned long long)b.tail_group;
+            if (b.tail_group > 1 && h->L > h->grid_levels)   // group barriers before tail levels Lg+2 .. min(ks, L)
+                *tail_arrivals = (unsigned long long)(std::min<int64_t>(b.tail_solo, h->L) - h->grid_levels - 1) *
+                                 (unsigned long long)b.tail_group;
         }
     } else {
         // level 1 also writes the leaf tables; with no levels a table-only launch

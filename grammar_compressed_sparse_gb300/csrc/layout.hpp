@@ -95,8 +95,8 @@ constexpr int64_t kLevelRows = 9;         // rows of the level table
 enum EmitMode : int32_t { EMIT_LEVEL = 0, EMIT_SLICE = 1, EMIT_ROWS = 2 };
 
 constexpr int64_t kSliceBytes = 192 << 10;   // shared memory of one slice
-constexpr int64_t kSliceTarget = 144;         // slices the references are spread over, at least
-constexpr int64_t kSliceRefsMin = 16384;      // a slice may always take this many references
+constexpr int64_t kSliceTarget = 136;         // slices per round: a 152-SM part's CTAs less the tail group's 16
+constexpr int64_t kSliceValueCost = 4;        // staged values that cost as much as one reference
 constexpr int64_t kSliceStep = 256;           // slices start on multiples of this many values
 inline int64_t slice_len(int64_t value_bytes) { return std::min<int64_t>(kSliceBytes / value_bytes, 65536); }
 
@@ -434,14 +434,15 @@ inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
 
 // Slice emit: the early references as [T | RV] indices x. Slices are runs of
 // values [x0[s], x0[s+1]) that start on multiples of kSliceStep, at most S
-// values wide, and close before they would take more than max(kSliceRefsMin,
-// early references / kSliceTarget) references; slice s holds offset x - x0[s]. Within a slice the references
+// values wide, with their costs balanced (slice_bounds); slice s holds offset
+// x - x0[s]. Within a slice the references
 // keep row-major C order, so a row's references into it form one segment.
-// A slice's segments are packed, in order, into tiles of kTileRefs references
-// (32 lanes x 8): a segment that does not fit in the rest of a tile starts a
-// new one (the rest is padding, a segment with id -1), and one longer than a
-// tile is cut into tile-long pieces, ceil(length / kTileRefs) of them. Every segment or piece gets its own id,
-// in (row, slice, piece) order, so a row's sums are contiguous.
+// A slice's segments are packed back to back, in order, into tiles of
+// kTileRefs references (32 lanes x 8): a segment that runs past the end of a
+// tile goes on in the next one as a new piece, and only the slice's last tile
+// is padded (the rest is a segment with id -1), so a slice of R references
+// takes ceil(R / kTileRefs) tiles. Every piece gets its own id, in (row,
+// slice, piece) order, so a row's sums are contiguous.
 constexpr int64_t kTileRefs = 256;
 
 struct SlicePlan {
@@ -461,26 +462,44 @@ struct SlicePlan {
 // [T | RV] index of an early reference (terminal or root of levels 1..Lg).
 inline int64_t slice_index(int64_t TB, int32_t c) { return c < 0 ? -c - 1 : TB + c; }
 
-// Slice boundaries from the references' counts per kSliceStep values.
+// Slice boundaries from the references' counts per kSliceStep values. A
+// slice's cost is its references plus its values / kSliceValueCost (the
+// staging); slices are cut greedily at the smallest cost cap that gives at
+// most kSliceTarget * r slices (r rounds of slices over the CTAs).
 inline std::vector<int32_t> slice_bounds(const Grammar& g, int64_t TB, int64_t Lg, int64_t S) {
     const int64_t X = TB + (Lg >= 1 ? g.root_off[Lg + 1] : 0);   // early references lie below X
     const int64_t nb = (X + kSliceStep - 1) / kSliceStep;
-    std::vector<int64_t> cnt((size_t)nb, 0);
+    std::vector<int64_t> cost((size_t)nb, kSliceStep / kSliceValueCost);
     for (int32_t c : g.c_ref)
-        if (ref_level(g, c) <= Lg) ++cnt[slice_index(TB, c) / kSliceStep];
-    int64_t total = 0;
-    for (int64_t c : cnt) total += c;
-    const int64_t cap = std::max<int64_t>(kSliceRefsMin, (total + kSliceTarget - 1) / kSliceTarget);
-    std::vector<int32_t> x0{0};
-    int64_t refs = 0, width = 0;
-    for (int64_t b = 0; b < nb; ++b) {
-        if (width > 0 && (width + kSliceStep > S || refs + cnt[b] > cap)) {
-            x0.push_back((int32_t)(b * kSliceStep));
-            refs = width = 0;
+        if (ref_level(g, c) <= Lg) ++cost[slice_index(TB, c) / kSliceStep];
+    auto cut = [&](int64_t cap, std::vector<int32_t>* x0) {
+        int64_t count = nb > 0 ? 1 : 0, sum = 0, width = 0;
+        for (int64_t b = 0; b < nb; ++b) {
+            if (width > 0 && (width + kSliceStep > S || sum + cost[b] > cap)) {
+                if (x0) x0->push_back((int32_t)(b * kSliceStep));
+                ++count;
+                sum = width = 0;
+            }
+            sum += cost[b];
+            width += kSliceStep;
         }
-        refs += cnt[b];
-        width += kSliceStep;
+        return count;
+    };
+    int64_t total = 0;
+    for (int64_t c : cost) total += c;
+    // one round more than the S-value limit alone needs, so that the costs can
+    // be balanced (in one round, slices full of values leave the few others
+    // all the densely referenced values)
+    const int64_t fewest = cut(total, nullptr);
+    const int64_t target = kSliceTarget * ((fewest + kSliceTarget - 1) / kSliceTarget + 1);
+    int64_t lo = 1, hi = std::max<int64_t>(total, 1);   // cut(hi) <= target
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (cut(mid, nullptr) <= target) hi = mid;
+        else lo = mid + 1;
     }
+    std::vector<int32_t> x0{0};
+    cut(hi, &x0);
     if (nb > 0) x0.push_back((int32_t)X);
     return x0;
 }
@@ -550,25 +569,27 @@ inline SliceSegments slice_segments(const Grammar& g, int64_t TB, int64_t Lg, in
 struct TileCounts {
     int64_t tiles = 0, starts = 0, ids = 0;
 };
-inline TileCounts count_tiles(const SliceSegments& z) {
+// Pieces of each segment under that packing (pieces[j] for segment j).
+inline TileCounts count_tiles(const SliceSegments& z, std::vector<int32_t>* pieces = nullptr) {
     TileCounts t;
     const int64_t NS = (int64_t)z.x0.size() - 1;
+    if (pieces) pieces->assign(z.seg_len.size(), 0);
     for (int64_t s = 0; s < NS; ++s) {
         int64_t fill = kTileRefs;   // no open tile yet
         for (int64_t j = z.sseg[s]; j < z.sseg[s + 1]; ++j)
             for (int64_t left = z.seg_len[j]; left > 0;) {
-                if (fill == kTileRefs || (fill > 0 && left > kTileRefs - fill)) {
-                    if (fill > 0 && fill < kTileRefs) ++t.starts;   // padding closes the tile
+                if (fill == kTileRefs) {
                     ++t.tiles;
                     fill = 0;
                 }
                 const int64_t take = std::min(left, kTileRefs - fill);
                 ++t.starts;
                 ++t.ids;
+                if (pieces) ++(*pieces)[j];
                 fill += take;
                 left -= take;
             }
-        if (fill > 0 && fill < kTileRefs) ++t.starts;
+        if (fill > 0 && fill < kTileRefs) ++t.starts;   // padding of the slice's last tile
     }
     return t;
 }
@@ -583,9 +604,10 @@ inline SlicePlan plan_slice_emit(const Grammar& g, int64_t TB, int64_t Lg, int64
     plan_late(g, Lg, p.late_off, p.late_ref);
     const int64_t NS = p.nslices;
     // ids: per row, its pieces in (slice, piece) order
+    std::vector<int32_t> pieces;
+    count_tiles(z, &pieces);
     std::vector<int64_t> row_ids((size_t)n + 1, 0);
-    for (int64_t j = 0; j < (int64_t)z.seg_row.size(); ++j)
-        row_ids[z.seg_row[j] + 1] += (z.seg_len[j] + kTileRefs - 1) / kTileRefs;
+    for (int64_t j = 0; j < (int64_t)z.seg_row.size(); ++j) row_ids[z.seg_row[j] + 1] += pieces[j];
     for (int64_t r = 0; r < n; ++r) row_ids[r + 1] += row_ids[r];
     p.row_seg.assign(row_ids.begin(), row_ids.end());
     p.nids = row_ids[n];
@@ -594,10 +616,6 @@ inline SlicePlan plan_slice_emit(const Grammar& g, int64_t TB, int64_t Lg, int64
     p.stile.assign((size_t)NS + 1, 0);
     int64_t fill = kTileRefs;
     auto open_tile = [&]() {
-        if (fill > 0 && fill < kTileRefs) {   // pad the open tile: one start with id -1
-            p.sflag[(p.ntiles - 1) * (kTileRefs / 8) + fill / 8] |= (uint8_t)(1u << (fill % 8));
-            p.tsid.push_back(-1);
-        }
         p.sref.resize(p.sref.size() + kTileRefs, 0);
         p.sflag.resize(p.sflag.size() + kTileRefs / 8, 0);
         p.tile_sid.push_back((int32_t)p.tsid.size());
@@ -610,7 +628,7 @@ inline SlicePlan plan_slice_emit(const Grammar& g, int64_t TB, int64_t Lg, int64
         for (int64_t j = z.sseg[s]; j < z.sseg[s + 1]; ++j) {
             int64_t q = z.seg_first[j];
             for (int64_t left = z.seg_len[j]; left > 0;) {
-                if (fill == kTileRefs || (fill > 0 && left > kTileRefs - fill)) open_tile();
+                if (fill == kTileRefs) open_tile();
                 const int64_t take = std::min(left, kTileRefs - fill);
                 const int64_t base = (p.ntiles - 1) * kTileRefs + fill;
                 p.sflag[(p.ntiles - 1) * (kTileRefs / 8) + fill / 8] |= (uint8_t)(1u << (fill % 8));
