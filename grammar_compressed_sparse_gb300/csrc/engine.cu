@@ -921,14 +921,17 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
             slice_sums<P>(a, __ldg(a.sorder + i), reinterpret_cast<V*>(slice_smem));
         }
     if (!coop) return;
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, GW = ((int64_t)gridDim.x * blockDim.x) >> 5;
     if constexpr (P::LPN == 1) {
+        // rows on the slice CTAs only: the tail's CTAs reach the barrier last
+        const int64_t wpc = blockDim.x >> 5;
+        const int64_t gw = (int64_t)(blockIdx.x - first) * wpc + (threadIdx.x >> 5), GW = (gridDim.x - first) * wpc;
         constexpr int R = sizeof(V) <= 4 ? 3 : 2;
         RowPlan<R, 10> pl;
-        plan_rows<P>(a, gw, GW, pl);
+        if (blockIdx.x >= first) plan_rows<P>(a, gw, GW, pl);
         if (!grid_sync(a, 0)) return;
-        finish_rows<P>(a, gw, GW, pl);
+        if (blockIdx.x >= first) finish_rows<P>(a, gw, GW, pl);
     } else {
+        const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, GW = ((int64_t)gridDim.x * blockDim.x) >> 5;
         if (!grid_sync(a, 0)) return;
         emit_final<P>(a, gw, GW);
     }
