@@ -12,11 +12,12 @@ pages) that it follows.
 
 Modules
   direct   O1: y = Mx straight from the uncompressed rows (fp64 / exact int /
-           boolean OR), plus the error scale b = |M||x|.
+           boolean OR / float32 min-plus), plus the error scale b = |M||x|.
   grammar  CSRV encoding, a naive RePair, decompression, the W-array grammar
-           evaluation, levels (Eq. 3.1), pass-through completion and live-set
-           widths (Def. 3.2, Lemma 3.3, Sec. 4.2).
-  reach    Boolean-semiring fixpoint x <- x OR (M (x) x) and textbook BFS.
+           evaluation (sum and min-plus), levels (Eq. 3.1), pass-through
+           completion and live-set widths (Def. 3.2, Lemma 3.3, Sec. 4.2).
+  reach    Boolean-semiring fixpoint x <- x OR (M (x) x), textbook BFS, and the
+           tropical fixpoint x <- min(x, M (x) x) (Bellman-Ford).
 
 Parity status: every public function here is pinned by a ``-m "not gpu"``
 test against the pages' worked example, a library routine or brute force

@@ -171,6 +171,30 @@ def eval_w(g, V, x):
     return y
 
 
+def eval_w_minplus(g, V, x):
+    """Theorem 2.3's sweep over the tropical semiring (Sec. 5: the schedule
+    needs only an associative combine): W[i] = min(cv(A_i), cv(B_i)) in rule
+    order, cv(N_j) = W[j], cv(<l,j>) = V[l] + x[j] rounded to float32; then
+    y[r] is the min of cv over row r's symbols in C, +inf for an empty row.
+    ``x`` is (m,) or (m, k)."""
+    x = np.asarray(x, dtype=np.float32)
+    V = np.asarray(V, dtype=np.float32)
+    R, tl, tj = g["R"], g["term_l"], g["term_j"]
+    k_shape = () if x.ndim == 1 else (x.shape[1],)
+    W = np.full((len(R),) + k_shape, np.inf, dtype=np.float32)
+
+    def cv(s):
+        return W[s] if s >= 0 else V[tl[-s - 1]] + x[tj[-s - 1]]
+
+    for i in range(len(R)):
+        W[i] = np.minimum(cv(int(R[i][0])), cv(int(R[i][1])))
+    y = np.full((len(g["C"]),) + k_shape, np.inf, dtype=np.float32)
+    for r, row in enumerate(g["C"]):
+        for s in row:
+            y[r] = np.minimum(y[r], cv(int(s)))
+    return y
+
+
 # ----------------------------------------------------------------------------
 # Levels (Sec. 3, Eq. 3.1) and pass-through completion (Sec. 4.2)
 # ----------------------------------------------------------------------------

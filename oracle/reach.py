@@ -6,6 +6,13 @@ single pass and name the iteration to the fixpoint as the next step
 i -> j of x[j], iterating x <- x OR y from a frontier with bit b set at source
 s_b reaches the fixpoint in which bit b of x[i] is set exactly when i can
 reach s_b (reflexively).
+
+The tropical semiring (min, +) gives single-source shortest paths the same
+way (Sec. 5: a pass is one Bellman-Ford edge relaxation): iterating
+x <- min(x, M (x) x) from x0 (0 at the sources, +inf elsewhere) reaches the
+fixpoint x[i] = min over sources s of (length of a shortest path i -> s along
+out-edges, M[i][j] the length of edge i -> j) + x0[s], when no cycle has
+negative length.
 """
 from __future__ import annotations
 
@@ -13,7 +20,7 @@ from collections import deque
 
 import numpy as np
 
-from .direct import matvec_or
+from .direct import matvec_minplus, matvec_or
 
 
 def fixpoint(row_ptr, col, x0, max_iter=1000):
@@ -25,6 +32,21 @@ def fixpoint(row_ptr, col, x0, max_iter=1000):
     x = np.asarray(x0, dtype=np.uint64).copy()
     for it in range(1, max_iter + 1):
         nxt = x | matvec_or(row_ptr, col, x)
+        if np.array_equal(nxt, x):
+            return x, it
+        x = nxt
+    raise RuntimeError("fixpoint not reached")
+
+
+def sssp_fixpoint(row_ptr, col, val, x0, max_iter=1000):
+    """Iterate x <- min(x, M (x) x) in float32 until it stops changing.
+
+    Returns (x, iterations), iterations counting the products computed, the
+    last of which changed nothing. Raises if max_iter is reached first.
+    """
+    x = np.asarray(x0, dtype=np.float32).copy()
+    for it in range(1, max_iter + 1):
+        nxt = np.minimum(x, matvec_minplus(row_ptr, col, val, x))
         if np.array_equal(nxt, x):
             return x, it
         x = nxt

@@ -79,6 +79,32 @@ def _matvec_or_and(row_ptr, col, x):
     return y
 
 
+def _minplus_with(reduce_op, empty, leaf):
+    def f(row_ptr, col, val, x):
+        x = np.asarray(x, dtype=np.float32)
+        n = len(row_ptr) - 1
+        y = np.full((n,) + x.shape[1:], empty, dtype=np.float32)
+        for i in range(n):
+            s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+            if e > s:
+                v = np.asarray(val[s:e], dtype=np.float32)
+                xs = x[np.asarray(col[s:e], dtype=np.int64)]
+                y[i] = reduce_op(leaf(v if x.ndim == 1 else v[:, None], xs), axis=0)
+        return y
+    return f
+
+
+def _sssp_without_keeping_x(row_ptr, col, val, x0, max_iter=1000):
+    # x <- M (x) x, forgetting min(x, .): the sources lose their own distance
+    x = np.asarray(x0, dtype=np.float32).copy()
+    for it in range(1, max_iter + 1):
+        nxt = direct.matvec_minplus(row_ptr, col, val, x)
+        if np.array_equal(nxt, x):
+            return x, it
+        x = nxt
+    return x, max_iter
+
+
 _orig_eval_w = grammar.eval_w
 _orig_csrv = grammar.csrv
 
@@ -95,6 +121,17 @@ MUTANTS = [
      ["test_worked_csrv_matches_eq_2_2"]),
     ("boolean product uses AND", direct, "matvec_or", _matvec_or_and,
      ["test_direct_or_matches_dense_boolean"]),
+    ("min-plus product uses max", direct, "matvec_minplus",
+     _minplus_with(np.max, np.inf, lambda v, x: v + x),
+     ["test_minplus_matches_fp64_rounded_once", "test_minplus_closed_forms_on_worked_example"]),
+    ("min-plus empty row gives 0", direct, "matvec_minplus",
+     _minplus_with(np.min, 0.0, lambda v, x: v + x),
+     ["test_minplus_matches_fp64_rounded_once"]),
+    ("min-plus leaf multiplies", direct, "matvec_minplus",
+     _minplus_with(np.min, np.inf, lambda v, x: v * x),
+     ["test_minplus_matches_fp64_rounded_once", "test_minplus_closed_forms_on_worked_example"]),
+    ("shortest-path fixpoint drops min(x, .)", reach, "sssp_fixpoint", _sssp_without_keeping_x,
+     ["test_sssp_matches_scipy_dijkstra", "test_sssp_iterations_on_a_path"]),
 ]
 
 
@@ -103,6 +140,8 @@ def test_pins_catch_mutant(name, mod, attr, fn, tests, monkeypatch, worked):
     monkeypatch.setattr(mod, attr, fn)
     if mod is direct and attr == "matvec_or":
         monkeypatch.setattr(reach, "matvec_or", fn)
+    if mod is direct and attr == "matvec_minplus":
+        monkeypatch.setattr(reach, "matvec_minplus", fn)
     for t in tests:
         f = getattr(pins, t)
         with pytest.raises(AssertionError):

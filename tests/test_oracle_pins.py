@@ -11,7 +11,7 @@ import itertools
 import numpy as np
 import pytest
 import scipy.sparse as sp
-from scipy.sparse.csgraph import breadth_first_order
+from scipy.sparse.csgraph import breadth_first_order, dijkstra
 
 import gcsynth
 from oracle import direct, grammar, reach
@@ -266,3 +266,119 @@ def test_reach_iterations_on_a_path():
     xs, iters = reach.fixpoint(rp, col, x0)
     assert iters == n
     assert np.all(xs == 1)
+
+
+# ---------------------------------------------------------------- tropical (min, +)
+def _minplus_cases():
+    """The random cases, plus one with empty rows and a column no row uses."""
+    yield from _random_cases()
+    dense = np.zeros((6, 5))
+    dense[0, [1, 3]] = [2.0, -1.5]
+    dense[2, 0] = 4.0
+    dense[3, [0, 1, 3]] = [1.0, 1.0, 7.25]
+    dense[5, 3] = -3.0
+    rp, c, v = dense_to_csr(dense, np.float64)
+    yield 200, rp, c, v, dense
+
+
+def _minplus_fp64_rounded_once(dense, x):
+    # every sum in float64, one rounding to float32 at the end, dense loops:
+    # rounding is monotone, so min commutes with it, and a float64 sum of two
+    # float32 numbers rounded to float32 is the correctly rounded float32 sum
+    # (double rounding is harmless for + when 53 >= 2 * 24 + 2)
+    n, m = dense.shape
+    k = 1 if x.ndim == 1 else x.shape[1]
+    xx = x.reshape(m, k)
+    out = np.empty((n, k), dtype=np.float32)
+    for i in range(n):
+        for c in range(k):
+            best = float("inf")
+            for j in range(m):
+                if dense[i, j] != 0:
+                    best = min(best, float(np.float32(dense[i, j])) + float(xx[j, c]))
+            out[i, c] = np.float32(best)
+    return out.reshape(n) if x.ndim == 1 else out
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_minplus_matches_fp64_rounded_once(k):
+    for seed, rp, c, v, dense in _minplus_cases():
+        g = np.random.default_rng(seed + 11)
+        # wide dynamic range, so that a float32 sum often rounds
+        x = (g.standard_normal((dense.shape[1], k)) * 10.0 ** g.uniform(-6, 6, (dense.shape[1], k)))
+        x = x.astype(np.float32)
+        x = x[:, 0] if k == 1 else x
+        got = direct.matvec_minplus(rp, c, v, x)
+        want = _minplus_fp64_rounded_once(dense, x)
+        assert got.dtype == np.float32
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_minplus_closed_forms_on_worked_example(worked):
+    M = worked["M"]
+    rp, c, v = dense_to_csr(M, np.float64)
+    nz = M != 0
+    rowmin = np.array([M[i, nz[i]].min() for i in range(M.shape[0])], dtype=np.float32)
+    m = M.shape[1]
+    # x = 0: each row's smallest stored value
+    assert np.array_equal(direct.matvec_minplus(rp, c, v, np.zeros(m, np.float32)), rowmin)
+    # x = 2.5 everywhere: shifted by 2.5 (exact: the values are small dyadics)
+    assert np.array_equal(direct.matvec_minplus(rp, c, v, np.full(m, 2.5, np.float32)), rowmin + np.float32(2.5))
+    # x = +inf everywhere: nothing reachable
+    assert np.all(np.isinf(direct.matvec_minplus(rp, c, v, np.full(m, np.inf, np.float32))))
+    # one finite column j0 (the rest +inf): exactly the rows that store j0
+    for j0 in range(m):
+        x = np.full(m, np.inf, np.float32)
+        x[j0] = -100.0
+        y = direct.matvec_minplus(rp, c, v, x)
+        want = np.where(nz[:, j0], M[:, j0].astype(np.float32) - np.float32(100.0), np.float32(np.inf))
+        assert np.array_equal(y, want)
+
+
+def test_minplus_grammar_sweep_matches_direct(worked):
+    rp, c, v = dense_to_csr(worked["M"], np.float64)
+    x = np.random.default_rng(5).standard_normal(worked["M"].shape[1]).astype(np.float32)
+    assert np.array_equal(grammar.eval_w_minplus(worked["grammar"], worked["V"], x),
+                          direct.matvec_minplus(rp, c, v, x))
+    for seed, rp, c, v, dense in _minplus_cases():
+        V, rows = grammar.csrv(rp, c, v)
+        g = grammar.repair(rows)
+        x = np.random.default_rng(seed + 3).standard_normal((dense.shape[1], 2)).astype(np.float32)
+        want = _minplus_fp64_rounded_once(dense, x)
+        got = grammar.eval_w_minplus(g, V, x) if len(V) else np.full((dense.shape[0], 2), np.inf, np.float32)
+        assert np.array_equal(got, want)
+
+
+def _weighted_graph(n, deg, seed):
+    rp, col = _random_graph(n, deg, seed)
+    w = np.random.default_rng(seed + 1).integers(1, 10, len(col)).astype(np.float32)
+    return rp, col, w
+
+
+def test_sssp_matches_scipy_dijkstra():
+    # integer edge lengths: every path length is exact in float32
+    for seed in range(5):
+        n = 80
+        rp, col, w = _weighted_graph(n, 3, seed)
+        srcs = np.random.default_rng(seed).choice(n, 4, replace=False)
+        x0 = np.full(n, np.inf, np.float32)
+        x0[srcs] = 0.0
+        xs, iters = reach.sssp_fixpoint(rp, col, w, x0)
+        A = sp.csr_matrix((w.astype(np.float64), col, rp), shape=(n, n))
+        # distance i -> s along out-edges = distance s -> i in the transpose
+        want = dijkstra(A.T.tocsr(), directed=True, indices=srcs, min_only=True)
+        assert np.array_equal(xs.astype(np.float64), want)
+
+
+def test_sssp_iterations_on_a_path():
+    # 0 -> 1 -> ... -> n-1 with lengths 1..n-1, source n-1 at distance 0:
+    # x*[i] = sum of the lengths from i on; n-1 products, then one unchanged
+    n = 9
+    rp = np.concatenate([np.arange(n, dtype=np.int64), [n - 1]])
+    col = np.arange(1, n, dtype=np.int32)
+    w = np.arange(1, n, dtype=np.float32)
+    x0 = np.full(n, np.inf, np.float32)
+    x0[n - 1] = 0.0
+    xs, iters = reach.sssp_fixpoint(rp, col, w, x0)
+    assert iters == n
+    assert np.array_equal(xs, np.array([w[i:].sum() for i in range(n)], dtype=np.float32))
