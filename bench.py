@@ -19,6 +19,13 @@ products / the slowest rank's time.
 --impl reference times the CPU oracle (float64 direct product over the CSR
 rows, one BLAS thread) on the same workload; each step is a bounded sample
 of rows, scaled to products per second.
+
+Other workloads (--workload): the same matrix with 16 right-hand sides, the
+small and the row-blocked 50,000 x 200,000 genotype matrices, the
+2,000,000-node copy-model graph under the Boolean policy (with the
+reachability fixpoint) and, with the "_minplus" suffix, the tropical policy
+on the genotype matrix and on the graph (with the shortest-path fixpoint,
+unit edge lengths).
 """
 from __future__ import annotations
 
@@ -46,6 +53,9 @@ WORKLOADS = {
     "geno_1k_2k": dict(gen=gcsynth.GENO_SMALL, k=1),
     "geno_50k_200k": dict(gen=gcsynth.GENO_LARGE, k=1),
     "graph_2m": dict(graph=gcsynth.GRAPH, k=1),
+    # tropical (min, +): one Bellman-Ford relaxation per product
+    "geno_10k_50k_minplus": dict(gen=gcsynth.GENO_MEDIUM, k=1, policy="minplus"),
+    "graph_2m_minplus": dict(graph=gcsynth.GRAPH, k=1, policy="minplus"),
 }
 L2_FLUSH_BYTES = 512 << 20
 
@@ -219,20 +229,29 @@ def _oracle_sample(workload, seconds, steps):
     from oracle import direct
     wl = WORKLOADS[workload]
     k = wl["k"]
+    minplus = wl.get("policy") == "minplus"
     if "graph" in wl:
         gp = wl["graph"]
         rp, c = gcsynth.copy_model_graph(**gp)
         rows = min(gp["nodes"], ORACLE_SAMPLE_ROWS * 100)
         rp, c = rp[:rows + 1], c[:rp[rows]]
-        x = np.random.default_rng(0).integers(0, 2**63, gp["nodes"], dtype=np.uint64)
-        product = lambda a, b: direct.matvec_or(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], x)
+        if minplus:
+            x = gcsynth.beta(gp["nodes"], seed=0)
+            ones = np.ones(len(c), np.float32)
+            product = lambda a, b: direct.matvec_minplus(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], ones[rp[a]:rp[b]], x)
+        else:
+            x = np.random.default_rng(0).integers(0, 2**63, gp["nodes"], dtype=np.uint64)
+            product = lambda a, b: direct.matvec_or(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], x)
         block = 25000
     else:
         gen = wl["gen"]
         rows = min(gen["n"], ORACLE_SAMPLE_ROWS)
         rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=rows))
         x = gcsynth.beta(gen["m"], seed=0, k=k)
-        product = lambda a, b: direct.matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
+        if minplus:
+            product = lambda a, b: direct.matvec_minplus(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
+        else:
+            product = lambda a, b: direct.matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
         block = 250
     out = []
     for _ in range(steps):
@@ -263,10 +282,19 @@ def cpu_oracle_rates(workload, seconds, steps=1):
 
 def oracle_sample_text(workload):
     wl = WORKLOADS[workload]
+    minplus = wl.get("policy") == "minplus"
     if "graph" in wl:
-        return (f"Boolean OR product of the first {min(wl['graph']['nodes'], ORACLE_SAMPLE_ROWS * 100)} rows "
-                "(64 sources per word) in blocks of 25,000")
-    return f"float64 direct product over the first {ORACLE_SAMPLE_ROWS} rows in blocks of 250"
+        what = "float32 min-plus product" if minplus else "Boolean OR product"
+        return (f"{what} of the first {min(wl['graph']['nodes'], ORACLE_SAMPLE_ROWS * 100)} rows "
+                + ("" if minplus else "(64 sources per word) ") + "in blocks of 25,000")
+    what = "float32 min-plus" if minplus else "float64 direct"
+    return f"{what} product over the first {ORACLE_SAMPLE_ROWS} rows in blocks of 250"
+
+
+def workload_policy(wl):
+    """(policy, element bytes, dtype name) of a workload."""
+    pol = wl.get("policy", "or" if "graph" in wl else "f32")
+    return pol, (8 if pol in ("or", "i64") else 4), {"or": "u64", "i64": "i64", "f32": "f32", "minplus": "f32"}[pol]
 
 
 def run_reference(args):
@@ -284,7 +312,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "matvec/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u64" if "graph" in wl else "f64", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32" if wl.get("policy") == "minplus" else ("u64" if "graph" in wl else "f64"),
+        "data": "synthetic",
         "config": {"workload": args.workload, "n": gen["n"], "m": gen["m"], "k": k},
         "cpu_baseline": {"value": value, "unit": "matvec/s", "cores": 1, "kind": "oracle",
                          "sample": f"{oracle_sample_text(args.workload)}, {per_step:.1f} s per step, "
@@ -343,12 +372,13 @@ def run_ours(args):
             G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: make_csr(gen))
     build_s = time.perf_counter() - t0
     st = G.stats()
-    policy, elem = ("or", 8) if graph else ("f32", 4)
+    policy, elem, dtype_name = workload_policy(wl)
+    minplus = policy == "minplus"
     eng = gcs.Engine(G, policy, k, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     nvec = args.warmup + args.steps
-    if graph:
+    if graph and not minplus:
         xs = [torch.from_numpy(np.random.default_rng(rank * 1000 + i).integers(
             0, 2**63, gen["m"], dtype=np.int64)).to(dev) for i in range(min(nvec, 8))]
         y = torch.empty(gen["n"], dtype=torch.int64, device=dev)
@@ -410,26 +440,44 @@ def run_ours(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e = world * args.steps / float(t.item())
 
-    # Boolean workload: the reachability fixpoint from 64 sources, timed once
+    # graph workloads: the reachability (Boolean) or shortest-path (min-plus)
+    # fixpoint from 64 sources, timed once
     fixpoint = None
     if graph:
-        x0 = gcsynth.frontier(gen["n"], gcsynth.sources(gen["n"], gp["sources"], gp["seed"]))
-        x0d = torch.from_numpy(x0.view(np.int64)).to(dev)
+        srcs = gcsynth.sources(gen["n"], gp["sources"], gp["seed"])
+        if minplus:
+            x0d = torch.from_numpy(gcsynth.frontier_distances(gen["n"], srcs)).to(dev)
+        else:
+            x0d = torch.from_numpy(gcsynth.frontier(gen["n"], srcs).view(np.int64)).to(dev)
         torch.cuda.synchronize(dev)
         t1 = time.perf_counter()
-        _, iters, rc = eng.reach(x0d)
-        fixpoint = {"iterations": iters, "seconds": round(time.perf_counter() - t1, 5), "status": rc}
+        _, iters, rc = (eng.sssp if minplus else eng.reach)(x0d)
+        fixpoint = {"kind": "shortest paths, unit lengths" if minplus else "reachability, 64-bit source bitsets",
+                    "iterations": iters, "seconds": round(time.perf_counter() - t1, 5), "status": rc}
 
     if rank != 0:
         return
     # parity spot check of the last product against the oracle, 200 rows
     from oracle import direct
     y_last = y.cpu().numpy()
-    if graph:
+    if graph and minplus:
+        x_last = xs[(args.warmup + args.steps - 1) % len(xs)].cpu().numpy()
+        rp, col = gcsynth.copy_model_graph(**gp)
+        rp, col = rp[:201], col[:rp[200]]
+        y_ref = direct.matvec_minplus(rp, col, np.ones(len(col), np.float32), x_last)
+        ok = bool(np.array_equal(y_last[:200].view(np.uint32), y_ref.view(np.uint32)))
+        worst = 0.0 if ok else float("inf")
+    elif graph:
         x_last = xs[(args.warmup + args.steps - 1) % len(xs)].cpu().numpy().view(np.uint64)
         rp, col = gcsynth.copy_model_graph(**gp)
         y_ref = direct.matvec_or(rp, col, x_last)
         ok = bool(np.array_equal(y_last.view(np.uint64), y_ref))
+        worst = 0.0 if ok else float("inf")
+    elif minplus:
+        rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=200))
+        xl = gcsynth.beta(gen["m"], seed=(args.warmup + args.steps - 1) % len(xs) % 100, k=k)
+        y_ref = direct.matvec_minplus(rp, c, v, xl)
+        ok = bool(np.array_equal(y_last[:200].view(np.uint32), y_ref.view(np.uint32)))
         worst = 0.0 if ok else float("inf")
     else:
         rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=200))
@@ -454,9 +502,11 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "matvec/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u64" if graph else "f32", "data": "synthetic",
+        "dtype": dtype_name, "data": "synthetic",
         "config": {"workload": args.workload, "n": gen["n"], "m": gen["m"], "k": k,
-                   **({"graph": "copy model, 64-bit source bitsets"} if graph else
+                   "policy": policy,
+                   **({"graph": "copy model, unit edge lengths" if minplus else "copy model, 64-bit source bitsets"}
+                      if graph else
                       {"founders": gen["founders"], "switch": gen["switch"], "mutation": gen["mutation"]}),
                    "l2": "flushed before every step (512 MB write, outside the events)",
                    "parallelism": f"replicas x{world}"},

@@ -155,6 +155,23 @@ def frontier(nodes: int, srcs: np.ndarray) -> np.ndarray:
     return x
 
 
+def target_lengths(col: np.ndarray, nodes: int, seed: int, hi: int = 9) -> np.ndarray:
+    """Edge lengths for shortest-path workloads, as float32: edge i -> j gets
+    the length of its target j, an integer drawn uniformly from 1..hi per node.
+    Copied adjacency lists keep their (column, length) pairs, so a copy-model
+    graph stays as repetitive as without lengths; integer lengths keep every
+    path length exact in float32 below 2^24."""
+    per_node = np.random.default_rng(seed).integers(1, hi + 1, nodes)
+    return per_node[np.asarray(col, dtype=np.int64)].astype(np.float32)
+
+
+def frontier_distances(nodes: int, srcs: np.ndarray) -> np.ndarray:
+    """float32 distances before the first relaxation: 0 at the sources, +inf elsewhere."""
+    x = np.full(nodes, np.inf, dtype=np.float32)
+    x[np.asarray(srcs, dtype=np.int64)] = 0.0
+    return x
+
+
 def random_sparse(n: int, m: int, density: float, values, seed: int):
     """Small seeded sparse matrix as CSR with values drawn from ``values``.
 

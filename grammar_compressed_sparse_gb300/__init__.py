@@ -117,7 +117,7 @@ class Engine:
     @property
     def dtype(self):
         import torch
-        return {"f32": torch.float32, "i64": torch.int64, "or": torch.int64}[self.policy]
+        return {"f32": torch.float32, "i64": torch.int64, "or": torch.int64, "minplus": torch.float32}[self.policy]
 
     def matvec(self, x, y=None, stream=None):
         """y = M x for a device tensor x of shape (m,) or (m, k)."""
@@ -143,6 +143,15 @@ class Engine:
         x = torch.empty_like(x0)
         iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
         rc = _capi().gc_reach(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        return x, int(iters.item()), rc
+
+    def sssp(self, x0, max_iter=1000, stream=None):
+        """Tropical fixpoint x <- min(x, M (x) x) from a device float32 tensor
+        (0 at the sources, +inf elsewhere); returns (x, iterations, status)."""
+        import torch
+        x = torch.empty_like(x0)
+        iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
+        rc = _capi().gc_sssp(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
         return x, int(iters.item()), rc
 
     def check(self, stream=None) -> int:

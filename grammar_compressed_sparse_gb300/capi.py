@@ -28,9 +28,9 @@ STATUS_NAMES = {0: "GC_OK", -1: "GC_ERR_ARG", -2: "GC_ERR_OOM", -3: "GC_ERR_CUDA
                 -4: "GC_ERR_INVALID_GRAMMAR", -5: "GC_ERR_UNSUPPORTED", -6: "GC_ERR_TIMEOUT",
                 -7: "GC_ERR_NOT_CONVERGED", -8: "GC_ERR_IO"}
 
-GC_F32_SUM, GC_I64_SUM, GC_BOOL_OR = 0, 1, 2
+GC_F32_SUM, GC_I64_SUM, GC_BOOL_OR, GC_F32_MIN_PLUS = 0, 1, 2, 3
 GC_SCHED_PERSISTENT, GC_SCHED_PER_LEVEL = 0, 1
-POLICIES = {"f32": GC_F32_SUM, "i64": GC_I64_SUM, "or": GC_BOOL_OR}
+POLICIES = {"f32": GC_F32_SUM, "i64": GC_I64_SUM, "or": GC_BOOL_OR, "minplus": GC_F32_MIN_PLUS}
 
 ARRAYS = {  # gc_array enum -> numpy dtype
     "values": (0, np.float32), "term_col": (1, np.int32), "term_vidx": (2, np.int32),
@@ -79,6 +79,7 @@ _sig = {
     "gc_matvec_host": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
     "gc_matvec_static": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
     "gc_reach": ([_vp, _vp, _vp, _i32, _vp, _vp], ctypes.c_int),
+    "gc_sssp": ([_vp, _vp, _vp, _i32, _vp, _vp], ctypes.c_int),
     "gc_check": ([_vp, _vp], ctypes.c_int),
     "gc_launch_count": ([_vp, ctypes.POINTER(_i64)], ctypes.c_int),
     "gc_set_schedule": ([_vp, _i32], ctypes.c_int),
@@ -199,6 +200,14 @@ def gc_reach(h, x0, x, max_iter, iters, stream=None) -> int:
     rc = _lib.gc_reach(h, _addr(x0), _addr(x), max_iter, _addr(iters), _stream(stream))
     if rc not in (GC_OK, GC_ERR_NOT_CONVERGED):
         raise GcError(rc, "gc_reach")
+    return rc
+
+
+def gc_sssp(h, x0, x, max_iter, iters, stream=None) -> int:
+    """Returns the status (GC_OK or GC_ERR_NOT_CONVERGED); raises on anything else."""
+    rc = _lib.gc_sssp(h, _addr(x0), _addr(x), max_iter, _addr(iters), _stream(stream))
+    if rc not in (GC_OK, GC_ERR_NOT_CONVERGED):
+        raise GcError(rc, "gc_sssp")
     return rc
 
 

@@ -983,13 +983,24 @@ __global__ void __launch_bounds__(kThreads, 1) emit_kernel(const SweepArgs<P> a,
     }
 }
 
-// x |= y elementwise; sets *changed if any word changed (Boolean fixpoint step).
+// x = x (+) y elementwise (OR for reachability, min for shortest paths);
+// sets *changed if any element changed (one fixpoint step).
+struct OrUpdate {
+    using T = unsigned long long;
+    __device__ __forceinline__ static T apply(T u, T v) { return u | v; }
+};
+struct MinUpdate {
+    using T = float;
+    __device__ __forceinline__ static T apply(T u, T v) { return fminf(u, v); }
+};
+
+template <class U>
 __global__ void __launch_bounds__(kThreads)
-or_update_kernel(unsigned long long* __restrict__ x, const unsigned long long* __restrict__ y, int64_t n,
-                 int32_t* __restrict__ changed) {
+update_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y, int64_t n,
+              int32_t* __restrict__ changed) {
     int ch = 0;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const unsigned long long u = x[i], v = u | y[i];
+        const typename U::T u = x[i], v = U::apply(u, y[i]);
         if (v != u) {
             x[i] = v;
             ch = 1;
@@ -1174,12 +1185,12 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
     return launches;
 }
 
-// Carry slots exist only for the device view of 16-wide handles (float32);
-// the other policies are built without them.
+// Carry slots exist only for the device view of 16-wide handles (the float32
+// policies); the other policies are built without them.
 template <class P>
 int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals,
                        unsigned long long* tail_arrivals) {
-    if constexpr (std::is_same<P, PolF32>::value || std::is_same<P, PolF32x16>::value)
+    if constexpr (std::is_same<typename P::Leaf, float>::value)
         if (h->n_carry > 0) return launch_product_as<P, true>(h, a, st, arrivals, tail_arrivals);
     if (h->n_carry > 0) fail(GC_ERR_UNSUPPORTED, "carry slots for a policy built without them");
     return launch_product_as<P, false>(h, a, st, arrivals, tail_arrivals);
@@ -1202,11 +1213,15 @@ void dispatch_product(gc_handle* h, const void* x, void* y, int32_t k, cudaStrea
             break;
         case GC_I64_SUM: run_product<PolI64>(h, x, y, st); break;
         case GC_BOOL_OR: run_product<PolOr>(h, x, y, st); break;
+        case GC_F32_MIN_PLUS:
+            if (k == 1) run_product<PolMinPlus>(h, x, y, st);
+            else run_product<PolMinPlusx16>(h, x, y, st);
+            break;
     }
 }
 
 void check_k(const gc_handle* h, int32_t k) {
-    if (h->policy == GC_F32_SUM) {
+    if (policy_is_f32(h->policy)) {
         if (k != 1 && k != 16) fail(GC_ERR_ARG, "k must be 1 or 16");
         if (k > h->k_max) fail(GC_ERR_ARG, "k exceeds the k_max the handle was uploaded with");
     } else if (k != 1) {
@@ -1218,6 +1233,51 @@ template <class T>
 void put(cudaStream_t st, char* arena, int64_t off, const T* p, size_t count) {
     if (count == 0) return;
     cuda_check(cudaMemcpyAsync(arena + off, p, count * sizeof(T), cudaMemcpyHostToDevice, st), "upload copy");
+}
+
+// x <- x (+) (M (x) x) from x0 until nothing changes, at most max_iter
+// products; the product's y lives in the arena's staging area. Writes the
+// product count (or -1) to iters on the device. Returns false if max_iter
+// was reached first (the status word then says GC_ERR_NOT_CONVERGED).
+template <class U>
+bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32_t max_iter, int32_t* iters,
+                  cudaStream_t st) {
+    using T = typename U::T;
+    const int64_t n = h->n;
+    T* yv = reinterpret_cast<T*>(h->arena + h->lay.ys);
+    int32_t* status = reinterpret_cast<int32_t*>(h->arena + h->lay.status);
+    int32_t* changed = status + 1;
+    if (x != x0 && n > 0)
+        cuda_check(cudaMemcpyAsync(x, x0, n * sizeof(T), cudaMemcpyDeviceToDevice, st), "x0 copy");
+    int32_t it = 0, done = 0;
+    int64_t launches = 0;
+    while (it < max_iter) {
+        ++it;
+        cuda_check(cudaMemsetAsync(changed, 0, 4, st), "flag clear");
+        dispatch_product(h, x, yv, 1, st);
+        launches += h->launches;
+        if (n > 0) {
+            update_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, changed);
+            ++launches;
+        }
+        cuda_check(cudaGetLastError(), "kernel launch");
+        int32_t c = 0;
+        cuda_check(cudaMemcpyAsync(&c, changed, 4, cudaMemcpyDeviceToHost, st), "flag read");
+        cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+        if (!c) {
+            done = 1;
+            break;
+        }
+    }
+    h->launches = launches;
+    int32_t result = done ? it : -1;
+    cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
+    if (!done) {
+        int32_t sw = GC_ERR_NOT_CONVERGED;
+        cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
+    }
+    cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+    return done != 0;
 }
 
 // ---------------------------------------------------------------- fixed scratch
@@ -1411,7 +1471,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         char* a = h->arena;
         put(st, a, d.nodes, nodes.data(), nodes.size());
         put(st, a, d.levels, h->lv.data(), h->lv.size());
-        if (policy == GC_F32_SUM) {
+        if (policy_is_f32(policy)) {
             put(st, a, d.V, g.V.data(), g.V.size());
         } else {
             std::vector<long long> v(g.V.size());
@@ -1479,46 +1539,28 @@ gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_it
         if (h->policy != GC_BOOL_OR) fail(GC_ERR_ARG, "gc_reach needs the GC_BOOL_OR policy");
         if (h->n != h->m) fail(GC_ERR_ARG, "gc_reach needs a square matrix");
         if (max_iter < 1) fail(GC_ERR_ARG, "max_iter must be >= 1");
-        cudaStream_t st = static_cast<cudaStream_t>(stream);
-        const int64_t n = h->n;
-        unsigned long long* xv = reinterpret_cast<unsigned long long*>(x);
-        unsigned long long* yv = reinterpret_cast<unsigned long long*>(h->arena + h->lay.ys);
-        int32_t* status = reinterpret_cast<int32_t*>(h->arena + h->lay.status);
-        int32_t* changed = status + 1;
-        if (x != x0 && n > 0)
-            cuda_check(cudaMemcpyAsync(x, x0, n * 8, cudaMemcpyDeviceToDevice, st), "x0 copy");
-        int32_t it = 0, done = 0;
-        int64_t launches = 0;
-        while (it < max_iter) {
-            ++it;
-            cuda_check(cudaMemsetAsync(changed, 0, 4, st), "flag clear");
-            dispatch_product(h, xv, yv, 1, st);
-            launches += h->launches;
-            if (n > 0) {
-                or_update_kernel<<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(xv, yv, n, changed);
-                ++launches;
-            }
-            cuda_check(cudaGetLastError(), "kernel launch");
-            int32_t c = 0;
-            cuda_check(cudaMemcpyAsync(&c, changed, 4, cudaMemcpyDeviceToHost, st), "flag read");
-            cuda_check(cudaStreamSynchronize(st), "stream synchronize");
-            if (!c) {
-                done = 1;
-                break;
-            }
-        }
-        h->launches = launches;
-        int32_t result = done ? it : -1;
-        cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
-        if (!done) {
-            int32_t s = GC_ERR_NOT_CONVERGED;
-            cuda_check(cudaMemcpyAsync(status, &s, 4, cudaMemcpyHostToDevice, st), "status write");
+        if (!run_fixpoint<OrUpdate>(h, reinterpret_cast<const unsigned long long*>(x0),
+                                    reinterpret_cast<unsigned long long*>(x), max_iter, iters,
+                                    static_cast<cudaStream_t>(stream)))
             rc = GC_ERR_NOT_CONVERGED;
-        }
-        cuda_check(cudaStreamSynchronize(st), "stream synchronize");
     });
     if (g != GC_OK) return g;
     if (rc != GC_OK) set_last_error("gc_reach: max_iter reached before the fixpoint");
+    return rc;
+}
+
+gc_status gc_sssp(gc_handle* h, const float* x0, float* x, int32_t max_iter, int32_t* iters, void* stream) {
+    gc_status rc = GC_OK;
+    gc_status g = guard([&] {
+        if (!h || !x0 || !x || !iters) fail(GC_ERR_ARG, "null argument");
+        if (h->policy != GC_F32_MIN_PLUS) fail(GC_ERR_ARG, "gc_sssp needs the GC_F32_MIN_PLUS policy");
+        if (h->n != h->m) fail(GC_ERR_ARG, "gc_sssp needs a square matrix");
+        if (max_iter < 1) fail(GC_ERR_ARG, "max_iter must be >= 1");
+        if (!run_fixpoint<MinUpdate>(h, x0, x, max_iter, iters, static_cast<cudaStream_t>(stream)))
+            rc = GC_ERR_NOT_CONVERGED;
+    });
+    if (g != GC_OK) return g;
+    if (rc != GC_OK) set_last_error("gc_sssp: max_iter reached before the fixpoint");
     return rc;
 }
 
@@ -1597,6 +1639,10 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
                 break;
             case GC_I64_SUM: run_product_static<PolI64>(h, x, y, st, scratch); break;
             case GC_BOOL_OR: run_product_static<PolOr>(h, x, y, st, scratch); break;
+            case GC_F32_MIN_PLUS:
+                if (k == 1) run_product_static<PolMinPlus>(h, x, y, st, scratch);
+                else run_product_static<PolMinPlusx16>(h, x, y, st, scratch);
+                break;
         }
         int32_t s = 0;
         cuda_check(cudaMemcpyAsync(&s, scratch + static_parts(h, k).status, 4, cudaMemcpyDeviceToHost, st),

@@ -126,7 +126,8 @@ struct DevLayout {
     bool has_rv() const { return emit != EMIT_LEVEL; }
 };
 
-inline int64_t policy_elem_bytes(gc_policy p) { return p == GC_F32_SUM ? 4 : 8; }
+inline bool policy_is_f32(gc_policy p) { return p == GC_F32_SUM || p == GC_F32_MIN_PLUS; }
+inline int64_t policy_elem_bytes(gc_policy p) { return policy_is_f32(p) ? 4 : 8; }
 
 inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
@@ -877,9 +878,10 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
 
 // Checks a (policy, k) request against the grammar's values.
 inline void check_policy(const Grammar& g, gc_policy p, int32_t k_max) {
-    if (p != GC_F32_SUM && p != GC_I64_SUM && p != GC_BOOL_OR) fail(GC_ERR_ARG, "unknown policy");
-    if (p == GC_F32_SUM ? (k_max != 1 && k_max != 16) : k_max != 1)
-        fail(GC_ERR_ARG, "k_max must be 1 (or 16 for GC_F32_SUM)");
+    if (p != GC_F32_SUM && p != GC_I64_SUM && p != GC_BOOL_OR && p != GC_F32_MIN_PLUS)
+        fail(GC_ERR_ARG, "unknown policy");
+    if (policy_is_f32(p) ? (k_max != 1 && k_max != 16) : k_max != 1)
+        fail(GC_ERR_ARG, "k_max must be 1 (or 16 for the float32 policies)");
     if (p == GC_I64_SUM)
         for (float v : g.V)
             if (v != (float)(int64_t)v || v > 9.0e15f || v < -9.0e15f)

@@ -8,9 +8,12 @@
 //          (Appendix A batched product; 64 B per node, four float4 lanes)
 //   I64   (+, x) exact int64                            V = int64,  LPN = 1
 //   OR    (OR, AND) on 64 sources per uint64 word       V = uint64, LPN = 1
+//   MinPlus   tropical (min, +) float32, one right-hand side      V = float
+//   MinPlusx16 the same on 16 right-hand sides                      V = float4
 // The leaf map is V[l] (x) x[j] for the terminal <l, j>, evaluated where the
 // sweep reads the terminal; the combine identity (0 for sums, all-zero bits
-// for OR: the semiring zero, Sec. 5) stands in for a missing child.
+// for OR, +inf for min: the semiring zero, Sec. 5) stands in for a missing
+// child.
 #pragma once
 
 #include <cstdint>
@@ -58,6 +61,34 @@ struct PolOr {
     __device__ __forceinline__ static V identity() { return 0ull; }
     __device__ __forceinline__ static V combine(V a, V b) { return a | b; }
     __device__ __forceinline__ static V leaf(Leaf, V x) { return x; }
+};
+
+// Tropical: min is exact and each leaf sum is rounded once, so every order of
+// evaluation gives the same bits. A leaf sum is never -0 (stored values are
+// non-zero), so min never has to choose between two zeros.
+struct PolMinPlus {
+    using V = float;
+    using Leaf = float;
+    static constexpr int LPN = 1;
+    __device__ __forceinline__ static V identity() { return __int_as_float(0x7f800000); }
+    __device__ __forceinline__ static V combine(V a, V b) { return fminf(a, b); }
+    __device__ __forceinline__ static V leaf(Leaf v, V x) { return __fadd_rn(v, x); }
+};
+
+struct PolMinPlusx16 {
+    using V = float4;
+    using Leaf = float;
+    static constexpr int LPN = 4;
+    __device__ __forceinline__ static V identity() {
+        const float inf = __int_as_float(0x7f800000);
+        return make_float4(inf, inf, inf, inf);
+    }
+    __device__ __forceinline__ static V combine(V a, V b) {
+        return make_float4(fminf(a.x, b.x), fminf(a.y, b.y), fminf(a.z, b.z), fminf(a.w, b.w));
+    }
+    __device__ __forceinline__ static V leaf(Leaf s, V x) {
+        return make_float4(__fadd_rn(s, x.x), __fadd_rn(s, x.y), __fadd_rn(s, x.z), __fadd_rn(s, x.w));
+    }
 };
 
 }  // namespace gcs

@@ -51,11 +51,17 @@ typedef enum {
 } gc_status;
 
 /* Leaf / combine / emit policy of the sweep (Sec. 5: any monoid homomorphism).
- *   GC_F32_SUM  (+, x) in float32; k = 1 or k = 16 right-hand sides
- *   GC_I64_SUM  (+, x) in exact int64; matrix values must be integers; k = 1
- *   GC_BOOL_OR  (OR, AND) on uint64 bitsets (64 sources per word); every
- *               stored entry must be 1 (an edge); k = 1                       */
-typedef enum { GC_F32_SUM = 0, GC_I64_SUM = 1, GC_BOOL_OR = 2 } gc_policy;
+ *   GC_F32_SUM       (+, x) in float32; k = 1 or k = 16 right-hand sides
+ *   GC_I64_SUM       (+, x) in exact int64; matrix values must be integers; k = 1
+ *   GC_BOOL_OR       (OR, AND) on uint64 bitsets (64 sources per word); every
+ *                    stored entry must be 1 (an edge); k = 1
+ *   GC_F32_MIN_PLUS  tropical (min, +) in float32 (Sec. 5: one product is one
+ *                    Bellman-Ford edge relaxation): y[i] = min over stored
+ *                    M[i][j] of M[i][j] + x[j], each sum rounded to float32,
+ *                    +inf for a row with no stored entry; min is exact, so y
+ *                    is the same bit for bit whatever the order. x must hold
+ *                    no NaN. k = 1 or k = 16                                 */
+typedef enum { GC_F32_SUM = 0, GC_I64_SUM = 1, GC_BOOL_OR = 2, GC_F32_MIN_PLUS = 3 } gc_policy;
 
 typedef struct {
     int64_t block_rows; /* 0: one grammar for all rows. >0: RePair runs on each
@@ -181,7 +187,8 @@ gc_status gc_export(const gc_grammar* g, gc_array which, void* dst, int64_t dst_
 
 /*
  * gc_layout -- device bytes needed to serve products under a policy with up
- * to k_max right-hand sides (k_max = 1 or 16 for GC_F32_SUM, 1 otherwise).
+ * to k_max right-hand sides (k_max = 1 or 16 for GC_F32_SUM and
+ * GC_F32_MIN_PLUS, 1 otherwise).
  * GC_ERR_UNSUPPORTED if the grammar's values do not fit the policy (non-
  * integer values for GC_I64_SUM, values other than 1 for GC_BOOL_OR).
  */
@@ -208,10 +215,13 @@ gc_status gc_upload(const gc_grammar* g, gc_policy policy, int32_t k_max, void* 
  * gc_matvec -- y = M x on the device (Lemmas 2.1-2.2, Theorem 2.3, Sec. 4.3,
  * Appendix A for k > 1). Asynchronous on stream.
  *   x   device, m*k elements, row-major (x[j*k + c] is column j of input c)
- *       float for GC_F32_SUM, int64_t for GC_I64_SUM, uint64_t for GC_BOOL_OR
+ *       float for GC_F32_SUM and GC_F32_MIN_PLUS, int64_t for GC_I64_SUM,
+ *       uint64_t for GC_BOOL_OR
  *   y   device, n*k elements, row-major, same element type; fully written
- *       (a row with no non-zeros gets the combine identity: 0)
- *   k   1, or 16 with GC_F32_SUM when the handle was uploaded with k_max 16
+ *       (a row with no non-zeros gets the combine identity: 0, or +inf for
+ *       GC_F32_MIN_PLUS)
+ *   k   1, or 16 with GC_F32_SUM / GC_F32_MIN_PLUS when the handle was
+ *       uploaded with k_max 16
  * x and y must not overlap the arena. Deterministic: the same x gives the same
  * y bit for bit (fixed summation order, no atomics).
  */
@@ -240,6 +250,28 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
  */
 gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
                    int32_t* iters, void* stream);
+
+/*
+ * gc_sssp -- tropical-semiring fixpoint x <- min(x, M (x) x) from x0 until it
+ * stops changing: Bellman-Ford relaxation to the end (Sec. 5 measures one
+ * pass, one edge relaxation, and names the iteration to the shortest-path
+ * fixpoint as the next step, Sec. 7 item 4). Requires GC_F32_MIN_PLUS and
+ * n == m; M[i][j] is the length of edge i -> j.
+ *   x0, x    device float[n]; x[i] ends as min over nodes s of (length of a
+ *            shortest path i -> s along out-edges) + x0[s], +inf if none
+ *            (x0 = 0 at the sources, +inf elsewhere: distance to the nearest
+ *            source). Sums round to float32 at every relaxation, so with
+ *            non-integer lengths x is the float32 Bellman-Ford result, not
+ *            the exact distance. x may equal x0 (in place). No negative cycle
+ *            may be reachable: the iteration would not end before max_iter.
+ *   iters    device int32_t[1]: products performed, the last of which changed
+ *            nothing; -1 if max_iter was reached first.
+ * Returns GC_ERR_NOT_CONVERGED (also recorded in the status word) if
+ * max_iter products did not reach the fixpoint. Synchronises the stream once
+ * per product to read the changed flag.
+ */
+gc_status gc_sssp(gc_handle* h, const float* x0, float* x, int32_t max_iter, int32_t* iters,
+                  void* stream);
 
 /* Synchronise the stream and return the device status word of the handle
  * (GC_OK, GC_ERR_TIMEOUT, GC_ERR_NOT_CONVERGED). The word is cleared after it

@@ -2,7 +2,8 @@
 packing, not the oracle): it reads exactly the arrays the device reads and
 evaluates them the way the kernels do -- T[0] identity, T[p+1] leaf values,
 one buffer per level read through signed child references, roots captured
-into RV, then the row sums over C -- in float64 (or int64 / uint64 OR).
+into RV, then the row sums over C -- in float64 (or int64 / uint64 OR /
+float32 min-plus).
 """
 import numpy as np
 
@@ -16,6 +17,14 @@ def emulate(ex, x, mode="f64"):
         ident = np.uint64(0)
         comb = np.bitwise_or
         dt = np.uint64
+    elif mode == "minplus":
+        dt = np.float32
+        x = np.asarray(x, dtype=dt)
+        v = ex["values"].astype(dt)[ex["term_vidx"]]
+        xs = x[ex["term_col"]]
+        leaf = (v[:, None] + xs) if x.ndim == 2 else v + xs
+        ident = dt(np.inf)
+        comb = np.minimum
     else:
         dt = np.int64 if mode == "i64" else np.float64
         x = np.asarray(x, dtype=dt)

@@ -151,11 +151,30 @@ def test_integer_and_boolean_values(gcs):
     xi = np.random.default_rng(1).integers(-1000, 1000, 300)
     np.testing.assert_array_equal(emulate(ex, xi, "i64"),
                                   direct.matvec_i64(rp, col, np.ones(len(col)), xi))
-    for pol in ("f32", "i64", "or"):
+    xf = np.random.default_rng(2).standard_normal(300).astype(np.float32)
+    assert np.array_equal(emulate(ex, xf, "minplus"), direct.matvec_minplus(rp, col, np.ones(len(col)), xf))
+    for pol in ("f32", "i64", "or", "minplus"):
         lay = G.layout(pol, 1)
         assert lay["arena_bytes"] >= lay["grammar_bytes"] + lay["scratch_bytes"]
     with pytest.raises(gcs.GcError):
         G.layout("f32", 3)
+
+
+def test_minplus_packed_layout_matches_oracle(gcs):
+    # the tropical policy reads the same packed arrays; min is exact, so the
+    # packed evaluation equals the direct product bit for bit, k = 1 and 16
+    d = gcsynth.genotype_dense(n=120, m=300, founders=5, switch=0.01, mutation=0.005, seed=4)
+    rp, c, v = gcsynth.dense_to_csr(d)
+    G = gcs.Grammar(120, 300, rp, c, v)
+    ex = export_all(G)
+    g = np.random.default_rng(9)
+    for x in (g.standard_normal(300).astype(np.float32), g.standard_normal((300, 16)).astype(np.float32)):
+        assert np.array_equal(emulate(ex, x, "minplus"), direct.matvec_minplus(rp, c, v, x))
+    for k_max in (1, 16):
+        lay = G.layout("minplus", k_max)
+        assert lay == G.layout("f32", k_max)     # same value width as the float32 sum
+    with pytest.raises(gcs.GcError):
+        G.layout("minplus", 4)
 
 
 def test_policy_value_checks(gcs):
@@ -188,9 +207,10 @@ def test_device_plans_pass_host_checks(gcs, k_max):
     heavy = gcs.Grammar(40, 3000, rp, c, v)                                 # level emit, few levels
     small = gcs.Grammar(1000, 2000, *gcsynth.genotype_csr(**gcsynth.GENO_SMALL))   # row emit
     for G in (slice_, heavy, small):
-        lay = G.layout("f32", k_max)
-        with pytest.raises(gcs.GcError, match="GC_ERR_CUDA"):
-            gcs.capi.gc_upload(G._p, "f32", k_max, 256, lay["arena_bytes"])
+        for pol in ("f32", "minplus"):
+            lay = G.layout(pol, k_max)
+            with pytest.raises(gcs.GcError, match="GC_ERR_CUDA"):
+                gcs.capi.gc_upload(G._p, pol, k_max, 256, lay["arena_bytes"])
 
 
 def test_slice_plan_and_tile_reduction(gcs, tmp_path):

@@ -4,6 +4,9 @@
   y = G beta against the float64 oracle, persistent schedule; a 16-wide product.
 * 2,000,000-node copy-model graph (about 2e8 edges): the Boolean product and the
   reachability fixpoint from 64 sources, bit for bit against the oracle.
+* The tropical (min, +) policy on both: every row of the genotype product, and
+  the shortest-path fixpoint (unit lengths: hop distance to the nearest of the
+  64 sources), bit for bit.
 
 Grammars are built once per session (RePair takes a minute or two of host
 time) and reused through the grammar cache when present.
@@ -83,3 +86,34 @@ def test_graph_fixpoint(gcs, torch):
     want, want_iters = reach.fixpoint(rp, col, x0)
     assert iters == want_iters
     np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint64), want)
+
+
+def _same_bits(a, b):
+    return np.array_equal(np.ascontiguousarray(a, np.float32).view(np.uint32),
+                          np.ascontiguousarray(b, np.float32).view(np.uint32))
+
+
+def test_medium_minplus_all_rows(gcs, torch, medium):
+    gen, rp, c, v, G = medium
+    eng = gcs.Engine(G, "minplus", 1)
+    x = gcsynth.beta(gen["m"], seed=0)
+    y = eng.matvec(torch.from_numpy(x).cuda()).cpu().numpy()
+    assert eng.check() == 0
+    assert _same_bits(y, direct.matvec_minplus(rp, c, v, x))
+
+
+def test_graph_shortest_paths(gcs, torch):
+    gp = gcsynth.GRAPH
+    rp, col = gcsynth.copy_model_graph(**gp)
+    N = gp["nodes"]
+    G = gcs.cached_grammar(f"graph:{sorted(gp.items())}", lambda: (N, N, rp, col, None))
+    eng = gcs.Engine(G, "minplus", 1)
+    ones = np.ones(len(col), np.float32)
+    x0 = gcsynth.frontier_distances(N, gcsynth.sources(N, gp["sources"], gp["seed"]))
+    y = eng.matvec(torch.from_numpy(x0).cuda()).cpu().numpy()
+    assert _same_bits(y, direct.matvec_minplus(rp, col, ones, x0))
+    xs, iters, rc = eng.sssp(torch.from_numpy(x0).cuda())
+    assert rc == 0
+    want, want_iters = reach.sssp_fixpoint(rp, col, ones, x0)
+    assert iters == want_iters
+    assert _same_bits(xs.cpu().numpy(), want)
