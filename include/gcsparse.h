@@ -313,14 +313,17 @@ gc_status gc_debug_inject(gc_handle* h, int32_t what, int64_t timeout_cycles);
  * callers that cannot call cudaMalloc (or any allocator) where the product
  * runs: a process whose device memory is fully reserved up front, or code
  * that only receives input and output buffers. The product's scratch -- the
- * root values, the two level buffers, the status word and the grid-barrier
- * counter -- lives in one fixed array compiled into the library, of
- * GC_STATIC_SCRATCH_BYTES bytes, that every GPU which loads the library holds
- * until the process exits. The handle's grammar (gc_upload) and x are the
- * inputs, y the output, as for gc_matvec; the handle's own scratch is unused.
- *   Size limit: a product needs 256 + RV + 2 level buffers bytes (rho and w*
- *   values of k elements each, each part rounded up to 256 bytes); a larger
- *   request returns GC_ERR_UNSUPPORTED with the sizes in gc_last_error().
+ * two level buffers, the tail buffer of the narrow top levels, the carry
+ * slots, the emit's chunk or segment sums, the root values, the status word
+ * and the grid-barrier counters -- lives in one fixed array compiled into the
+ * library, of GC_STATIC_SCRATCH_BYTES bytes, that every GPU which loads the
+ * library holds until the process exits. The handle's grammar (gc_upload) and
+ * x are the inputs, y the output, as for gc_matvec; the handle's own scratch
+ * is unused.
+ *   Size limit: a product needs the sum of those parts for k values a node
+ *   (each part rounded up to 256 bytes; about the handle's gc_layout
+ *   scratch_bytes); a larger request returns GC_ERR_UNSUPPORTED with the
+ *   sizes in gc_last_error().
  *   Set-up: the first call on a device, with that device current, looks up
  *   the array's device address (cudaGetSymbolAddress) once; make that first
  *   call before any stream capture.
