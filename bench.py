@@ -20,7 +20,7 @@ products / the slowest rank's time.
 rows, one BLAS thread) on the same workload; each step is a bounded sample
 of rows, scaled to products per second.
 
-Other workloads (--workload): the same matrix with 16 right-hand sides, the
+Other workloads (--workload): the same matrix with 16, 64 or 256 right-hand sides, the
 small and the row-blocked 50,000 x 200,000 genotype matrices, the
 2,000,000-node copy-model graph under the Boolean policy (with the
 reachability fixpoint) and, with the "_minplus" suffix, the tropical policy
@@ -50,6 +50,8 @@ METRIC = "matvecs/s and effective HBM GB/s (% of roofline) for y=Gβ on one GB30
 WORKLOADS = {
     "geno_10k_50k": dict(gen=gcsynth.GENO_MEDIUM, k=1),
     "geno_10k_50k_k16": dict(gen=gcsynth.GENO_MEDIUM, k=16),
+    "geno_10k_50k_k64": dict(gen=gcsynth.GENO_MEDIUM, k=64),
+    "geno_10k_50k_k256": dict(gen=gcsynth.GENO_MEDIUM, k=256),
     "geno_1k_2k": dict(gen=gcsynth.GENO_SMALL, k=1),
     "geno_50k_200k": dict(gen=gcsynth.GENO_LARGE, k=1),
     "graph_2m": dict(graph=gcsynth.GRAPH, k=1),

@@ -85,12 +85,12 @@ void cuda_check(cudaError_t e, const char* what) {
     if (e != cudaSuccess) fail(GC_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-// A warp's chunk: U rows of NPW nodes, LPN lanes per node. Sixteen-wide
-// values (64 B a node) take two rows, so that a lane's pairs and child values
-// stay in registers.
+// A warp's chunk: U rows of NPW nodes, LPN lanes per node. Values of 16 bytes
+// a lane take two rows, of 32 bytes one, so that a lane's pairs and child
+// values stay in registers.
 template <class P>
 struct Chunk {
-    static constexpr int U = P::LPN == 1 ? 4 : 2;    // nodes per lane
+    static constexpr int U = sizeof(typename P::V) <= 8 ? 4 : sizeof(typename P::V) <= 16 ? 2 : 1;   // nodes per lane
     static constexpr int NPW = 32 / P::LPN;          // nodes per warp row
     static constexpr int NODES = NPW * U;            // nodes per warp chunk
 };
@@ -136,6 +136,18 @@ __device__ __forceinline__ unsigned long long shfl_x(unsigned long long v, int m
 }
 __device__ __forceinline__ float4 shfl_x(float4 v, int m) {
     return make_float4(shfl_x(v.x, m), shfl_x(v.y, m), shfl_x(v.z, m), shfl_x(v.w, m));
+}
+__device__ __forceinline__ F8 shfl_x(F8 v, int m) { return F8{shfl_x(v.lo, m), shfl_x(v.hi, m)}; }
+// read-only loads of x: __ldg, and two 16-byte ones for the eight-float value
+template <class T>
+__device__ __forceinline__ T ldg_value(const T* p) { return __ldg(p); }
+__device__ __forceinline__ F8 ldg_value(const F8* p) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+    return F8{__ldg(q), __ldg(q + 1)};
+}
+__device__ __forceinline__ void st_keep(F8* p, F8 v, uint64_t pol) {
+    st_keep(&p->lo, v.lo, pol);
+    st_keep(&p->hi, v.hi, pol);
 }
 __device__ __forceinline__ float shfl_up(float v, int d) { return __shfl_up_sync(0xffffffffu, v, d); }
 __device__ __forceinline__ long long shfl_up(long long v, int d) { return __shfl_up_sync(0xffffffffu, v, d); }
@@ -200,7 +212,7 @@ template <class P>
 __device__ __forceinline__ typename P::V leaf_value(int32_t code, int part, const SweepArgs<P>& a) {
     const uint32_t q = (uint32_t)code;
     const uint32_t col = q >> a.vbits, vi = q & ((1u << a.vbits) - 1u);
-    return P::leaf(__ldg(a.Vd + vi), __ldg(a.x + (int64_t)col * P::LPN + part));
+    return P::leaf(__ldg(a.Vd + vi), ldg_value(a.x + (int64_t)col * P::LPN + part));
 }
 
 // The leaf-table copies in front of buf0, buf1 (and RV in the row emit), grid-stride.
@@ -356,7 +368,7 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
     constexpr int S = G < 32 / P::LPN ? G : 32 / P::LPN;
     constexpr int GG = S * P::LPN;                     // lanes per row
     constexpr int RPW = 32 / GG;                       // rows per warp
-    constexpr int BATCH = P::LPN == 1 ? 4 : 2;         // symbols loaded together per lane
+    constexpr int BATCH = sizeof(V) <= 8 ? 4 : 2;      // symbols loaded together per lane
     const int lane = threadIdx.x & 31;
     const int gl = lane % GG;
     const int slot = gl / P::LPN, part = gl % P::LPN;
@@ -411,14 +423,12 @@ __device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, con
     using V = typename P::V;
     constexpr int NS = 32 / P::LPN;            // reference slots per warp row
     constexpr int PER = kEmitChunk / NS;       // references per lane
-    constexpr int B = P::LPN == 1 ? PER : 4;   // references loaded together
+    constexpr int B = sizeof(V) <= 8 ? PER : 4;   // references loaded together
     const int lane = threadIdx.x & 31;
     const int part = lane % P::LPN, slot = lane / P::LPN;
     const int4 ch = __ldg(a.echunk + j);
     V acc = P::identity();
-#pragma unroll
-    for (int u0 = 0; u0 < PER; u0 += B) {
-        if (u0 * NS >= ch.y) break;            // the same for the whole warp
+    auto batch = [&](int u0) {
         int32_t r[B];
 #pragma unroll
         for (int u = 0; u < B; ++u) {
@@ -432,6 +442,16 @@ __device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, con
         }
 #pragma unroll
         for (int u = 0; u < B; ++u) acc = P::combine(acc, v[u]);
+    };
+    if constexpr (PER / B <= 8) {
+#pragma unroll
+        for (int u0 = 0; u0 < PER; u0 += B) {
+            if (u0 * NS >= ch.y) break;            // the same for the whole warp
+            batch(u0);
+        }
+    } else {   // wide values: few slots per warp row, so many batches
+#pragma unroll 1
+        for (int u0 = 0; u0 < PER && u0 * NS < ch.y; u0 += B) batch(u0);
     }
 #pragma unroll
     for (int msk = 16; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
@@ -468,7 +488,7 @@ __device__ void emit_final(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps)
         const int32_t q0 = __ldg(a.late_off + row), q1 = __ldg(a.late_off + row + 1);
         const int32_t nc = c1 - c0, total = nc + (q1 - q0);
         V acc = P::identity();
-        constexpr int B = P::LPN == 1 ? 8 : 4;   // items a lane loads together
+        constexpr int B = sizeof(V) <= 8 ? 8 : 4;   // items a lane loads together
         for (int32_t i0 = 0; i0 < total; i0 += B * NS) {
             V v[B];
 #pragma unroll
@@ -850,6 +870,7 @@ template <class P>
 __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) {
     __shared__ int32_t next_tile;
     using V = typename P::V;
+    static_assert(kScalarPolicy<P>, "the slice emit serves one-lane scalar values");
     // values [x0, x1) in 16-byte units (x0 is a multiple of 256 values; the
     // last unit may run up to 15 bytes past x1, inside RV's padded allocation)
     const int64_t x0 = __ldg(a.sx0 + s), x1 = __ldg(a.sx0 + s + 1);
@@ -861,7 +882,7 @@ __device__ void slice_sums(const SweepArgs<P>& a, int64_t s, typename P::V* sv) 
     const int64_t t0 = __ldg(a.stile + s), nw = blockDim.x >> 5;
     if (threadIdx.x == 0) next_tile = (int32_t)nw;
     __syncthreads();
-    if constexpr (P::LPN == 1) {
+    {
         const int lane = threadIdx.x & 31;
         const int64_t t1 = __ldg(a.stile + s + 1);
         auto claim = [&]() {
@@ -921,7 +942,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
             slice_sums<P>(a, __ldg(a.sorder + i), reinterpret_cast<V*>(slice_smem));
         }
     if (!coop) return;
-    if constexpr (P::LPN == 1) {
+    {
         // rows on the slice CTAs only: the tail's CTAs reach the barrier last
         const int64_t wpc = blockDim.x >> 5;
         const int64_t gw = (int64_t)(blockIdx.x - first) * wpc + (threadIdx.x >> 5), GW = (gridDim.x - first) * wpc;
@@ -930,10 +951,6 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
         if (blockIdx.x >= first) plan_rows<P>(a, gw, GW, pl);
         if (!grid_sync(a, 0)) return;
         if (blockIdx.x >= first) finish_rows<P>(a, gw, GW, pl);
-    } else {
-        const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5, GW = ((int64_t)gridDim.x * blockDim.x) >> 5;
-        if (!grid_sync(a, 0)) return;
-        emit_final<P>(a, gw, GW);
     }
 }
 
@@ -1116,10 +1133,13 @@ template <class P, bool kC>
 int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals,
                           unsigned long long* tail_arrivals) {
     const bool slice = h->lay.emit == EMIT_SLICE;
+    // the slice emit (k_max = 1 handles) serves one-lane values only
+    if (slice && !kScalarPolicy<P>) fail(GC_ERR_ARG, "a multi-vector product on a one-vector handle");
     int grid = 0, grid2 = 0;
     if (h->schedule == 0 && h->coop) {
         grid = sweep_grid<P, kC>(h);
-        if (slice && grid > 0) grid2 = slice_grid<P, kC>(h);
+        if constexpr (kScalarPolicy<P>)
+            if (slice && grid > 0) grid2 = slice_grid<P, kC>(h);
         if (slice && grid2 == 0) grid = 0;
     }
     int64_t launches = 0;
@@ -1131,7 +1151,7 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
                    "sweep launch");
         launches = 1;
         *arrivals = (unsigned long long)sweep_barriers(h) * (unsigned long long)grid;
-        if (slice) {
+        if constexpr (kScalarPolicy<P>) if (slice) {
             SweepArgs<P> b = a;
             b.bar_base = a.bar_base + *arrivals;
             b.tail_group = std::min(kTailGroup, grid2);
@@ -1167,16 +1187,15 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
             emit_kernel<P><<<grid_for(h->n, kWarps * (32 / h->emit_group), h->sms, 4), kThreads, 0, st>>>(a, 0);
             ++launches;
         } else if (h->n > 0) {
-            if (slice) {
+            if constexpr (kScalarPolicy<P>) if (slice) {
                 const int64_t smem = slice_smem<P>(h);
                 cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P, kC>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
                            "slice shared memory");
                 const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>(h->lay.n_slices, h->sms));
                 slice_kernel<P, kC><<<g2, kSliceThreads, (size_t)smem, st>>>(a, 0);
-            } else {
-                emit_kernel<P><<<grid_for(h->lay.n_echunks, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 0);
             }
+            if (!slice) emit_kernel<P><<<grid_for(h->lay.n_echunks, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 0);
             emit_kernel<P><<<grid_for(h->n, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 1);
             launches += 2;
         }
@@ -1205,12 +1224,29 @@ void run_product(gc_handle* h, const void* x, void* y, cudaStream_t st) {
     h->tbar_base += tail_arrivals;
 }
 
+// The float32 sum at k right-hand sides (k one of kF32Widths; checked before).
+template <template <class> class Run, class... Args>
+void for_f32_width(int32_t k, Args&&... args) {
+    switch (k) {
+        case 1: Run<PolF32>::go(args...); break;
+        case 4: Run<PolF32xN<1>>::go(args...); break;
+        case 8: Run<PolF32xN<2>>::go(args...); break;
+        case 16: Run<PolF32xN<4>>::go(args...); break;
+        case 32: Run<PolF32xN<8>>::go(args...); break;
+        case 64: Run<PolF32xN<16>>::go(args...); break;
+        case 128: Run<PolF32xN<32>>::go(args...); break;
+        case 256: Run<PolF32x256>::go(args...); break;
+        default: fail(GC_ERR_ARG, "unsupported k");
+    }
+}
+template <class P>
+struct RunProduct {
+    static void go(gc_handle* h, const void* x, void* y, cudaStream_t st) { run_product<P>(h, x, y, st); }
+};
+
 void dispatch_product(gc_handle* h, const void* x, void* y, int32_t k, cudaStream_t st) {
     switch (h->policy) {
-        case GC_F32_SUM:
-            if (k == 1) run_product<PolF32>(h, x, y, st);
-            else run_product<PolF32x16>(h, x, y, st);
-            break;
+        case GC_F32_SUM: for_f32_width<RunProduct>(k, h, x, y, st); break;
         case GC_I64_SUM: run_product<PolI64>(h, x, y, st); break;
         case GC_BOOL_OR: run_product<PolOr>(h, x, y, st); break;
         case GC_F32_MIN_PLUS:
@@ -1220,13 +1256,11 @@ void dispatch_product(gc_handle* h, const void* x, void* y, int32_t k, cudaStrea
     }
 }
 
+// k: a width the policy supports (policy_width_ok), at most the handle's
+// k_max (its buffers hold k_max values a node).
 void check_k(const gc_handle* h, int32_t k) {
-    if (policy_is_f32(h->policy)) {
-        if (k != 1 && k != 16) fail(GC_ERR_ARG, "k must be 1 or 16");
-        if (k > h->k_max) fail(GC_ERR_ARG, "k exceeds the k_max the handle was uploaded with");
-    } else if (k != 1) {
-        fail(GC_ERR_ARG, "k must be 1 for this policy");
-    }
+    if (!policy_width_ok(h->policy, k)) fail(GC_ERR_ARG, "k is not a width this policy supports");
+    if (k > h->k_max) fail(GC_ERR_ARG, "k exceeds the k_max the handle was uploaded with");
 }
 
 template <class T>
@@ -1362,6 +1396,13 @@ void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, u
     h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals);
 }
 
+template <class P>
+struct RunStatic {
+    static void go(gc_handle* h, const void* x, void* y, cudaStream_t st, unsigned char* scratch) {
+        run_product_static<P>(h, x, y, st, scratch);
+    }
+};
+
 }  // namespace
 }  // namespace gcs
 
@@ -1399,7 +1440,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         // lane loads about one batch of a row's symbols (4 one-lane values, 2
         // four-lane ones) and a warp reduces 32 / G rows at a time
         const double avg = g.n > 0 ? (double)h->c_len / (double)g.n : 0.0;
-        const int batch = k_max == 16 ? 2 : 4;
+        const int batch = k_max == 1 ? 4 : 2;
         int G = 1;
         while (G < 32 && G * batch < avg) G <<= 1;
         h->emit_group = d.emit == EMIT_ROWS ? G : 0;
@@ -1633,10 +1674,7 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
         cudaStream_t st = static_cast<cudaStream_t>(stream);
         unsigned char* scratch = static_scratch_on_current_device();
         switch (h->policy) {
-            case GC_F32_SUM:
-                if (k == 1) run_product_static<PolF32>(h, x, y, st, scratch);
-                else run_product_static<PolF32x16>(h, x, y, st, scratch);
-                break;
+            case GC_F32_SUM: for_f32_width<RunStatic>(k, h, x, y, st, scratch); break;
             case GC_I64_SUM: run_product_static<PolI64>(h, x, y, st, scratch); break;
             case GC_BOOL_OR: run_product_static<PolOr>(h, x, y, st, scratch); break;
             case GC_F32_MIN_PLUS:

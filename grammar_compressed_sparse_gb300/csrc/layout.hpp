@@ -127,6 +127,14 @@ struct DevLayout {
 };
 
 inline bool policy_is_f32(gc_policy p) { return p == GC_F32_SUM || p == GC_F32_MIN_PLUS; }
+// Right-hand sides a node's value may hold: the float32 sum takes the batch
+// widths of Appendix A (1, 4, 8, ..., 256), the tropical policy 1 or 16, the
+// exact and Boolean policies one.
+inline bool policy_width_ok(gc_policy p, int64_t k) {
+    if (p == GC_F32_SUM) return k == 1 || k == 4 || k == 8 || k == 16 || k == 32 || k == 64 || k == 128 || k == 256;
+    if (p == GC_F32_MIN_PLUS) return k == 1 || k == 16;
+    return k == 1;
+}
 inline int64_t policy_elem_bytes(gc_policy p) { return policy_is_f32(p) ? 4 : 8; }
 
 inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
@@ -306,7 +314,9 @@ inline void validate_device_view(const Grammar& d) {
         if (c >= 0 ? c >= d.n_roots : (-(int64_t)c - 1) > A) bad("C reference out of range");
 }
 
-inline int64_t tail_width(int32_t k_max) { return k_max == 16 ? 1024 : 4096; }
+// widest level of the tail that one CTA finishes: 4,096 one-lane values,
+// 16 KB of values a level for wider ones (1,024 16-wide values), at least 256
+inline int64_t tail_width(int32_t k_max) { return k_max == 1 ? 4096 : std::max<int64_t>(256, 16384 / k_max); }
 // the slice emit's tail runs on a group of CTAs beside the slices, so it
 // takes the levels up to this width
 constexpr int64_t kSliceTailNodes = 65536;
@@ -880,8 +890,8 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
 inline void check_policy(const Grammar& g, gc_policy p, int32_t k_max) {
     if (p != GC_F32_SUM && p != GC_I64_SUM && p != GC_BOOL_OR && p != GC_F32_MIN_PLUS)
         fail(GC_ERR_ARG, "unknown policy");
-    if (policy_is_f32(p) ? (k_max != 1 && k_max != 16) : k_max != 1)
-        fail(GC_ERR_ARG, "k_max must be 1 (or 16 for the float32 policies)");
+    if (!policy_width_ok(p, k_max))
+        fail(GC_ERR_ARG, "k_max must be 1, or 4, 8, ..., 256 for GC_F32_SUM, or 16 for GC_F32_MIN_PLUS");
     if (p == GC_I64_SUM)
         for (float v : g.V)
             if (v != (float)(int64_t)v || v > 9.0e15f || v < -9.0e15f)

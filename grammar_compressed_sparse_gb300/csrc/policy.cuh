@@ -4,8 +4,10 @@
 //
 // A node value is LPN lanes of type V:
 //   F32   (+, x) float32, one right-hand side          V = float,  LPN = 1
-//   F32x16 (+, x) float32, 16 right-hand sides          V = float4, LPN = 4
-//          (Appendix A batched product; 64 B per node, four float4 lanes)
+//   F32xN  (+, x) float32, k = 4 LPN right-hand sides   V = float4, LPN = k / 4
+//          (Appendix A batched product: k = 4 .. 128; F32x16 is LPN = 4,
+//          64 B per node in four float4 lanes)
+//   F32x256 (+, x) float32, 256 right-hand sides        V = F8 (8 floats), LPN = 32
 //   I64   (+, x) exact int64                            V = int64,  LPN = 1
 //   OR    (OR, AND) on 64 sources per uint64 word       V = uint64, LPN = 1
 //   MinPlus   tropical (min, +) float32, one right-hand side      V = float
@@ -32,10 +34,11 @@ struct PolF32 {
     __device__ __forceinline__ static V leaf(Leaf v, V x) { return __fmul_rn(v, x); }
 };
 
-struct PolF32x16 {
+template <int LPN_>
+struct PolF32xN {
     using V = float4;
     using Leaf = float;
-    static constexpr int LPN = 4;
+    static constexpr int LPN = LPN_;
     __device__ __forceinline__ static V identity() { return make_float4(0.f, 0.f, 0.f, 0.f); }
     __device__ __forceinline__ static V combine(V a, V b) {
         return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
@@ -44,6 +47,30 @@ struct PolF32x16 {
         return make_float4(__fmul_rn(s, x.x), __fmul_rn(s, x.y), __fmul_rn(s, x.z), __fmul_rn(s, x.w));
     }
 };
+
+using PolF32x16 = PolF32xN<4>;
+
+// Eight floats of a 256-wide value: one lane's part (32 lanes a node).
+struct __align__(16) F8 {
+    float4 lo, hi;
+};
+
+struct PolF32x256 {
+    using V = F8;
+    using Leaf = float;
+    static constexpr int LPN = 32;
+    __device__ __forceinline__ static V identity() {
+        return F8{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    }
+    __device__ __forceinline__ static V combine(V a, V b) {
+        return F8{PolF32x16::combine(a.lo, b.lo), PolF32x16::combine(a.hi, b.hi)};
+    }
+    __device__ __forceinline__ static V leaf(Leaf s, V x) { return F8{PolF32x16::leaf(s, x.lo), PolF32x16::leaf(s, x.hi)}; }
+};
+
+// Values of one scalar per node (one lane): the slice emit serves only these.
+template <class P>
+constexpr bool kScalarPolicy = P::LPN == 1 && sizeof(typename P::V) <= 8;
 
 struct PolI64 {
     using V = long long;

@@ -158,6 +158,17 @@ def test_integer_and_boolean_values(gcs):
         assert lay["arena_bytes"] >= lay["grammar_bytes"] + lay["scratch_bytes"]
     with pytest.raises(gcs.GcError):
         G.layout("f32", 3)
+    # the float32 sum takes the batch widths 1, 4, 8, ..., 256; the buffers
+    # grow with the width, the grammar does not
+    lays = {k: G.layout("f32", k) for k in (1, 4, 8, 16, 32, 64, 128, 256)}
+    assert len({lay["grammar_bytes"] for k, lay in lays.items() if k > 1}) == 1
+    assert lays[256]["scratch_bytes"] > lays[64]["scratch_bytes"] > lays[16]["scratch_bytes"]
+    for bad in (2, 12, 512):
+        with pytest.raises(gcs.GcError):
+            G.layout("f32", bad)
+    for bad in (4, 64):
+        with pytest.raises(gcs.GcError):
+            G.layout("minplus", bad)
 
 
 def test_minplus_packed_layout_matches_oracle(gcs):
@@ -191,7 +202,7 @@ def test_policy_value_checks(gcs):
         G.layout("or", 1)
 
 
-@pytest.mark.parametrize("k_max", [1, 16])
+@pytest.mark.parametrize("k_max", [1, 16, 256])
 def test_device_plans_pass_host_checks(gcs, k_max):
     # gc_upload builds and checks every device array on the host (node codes,
     # level-emit chunks, references into the narrow top levels) before its
@@ -207,7 +218,7 @@ def test_device_plans_pass_host_checks(gcs, k_max):
     heavy = gcs.Grammar(40, 3000, rp, c, v)                                 # level emit, few levels
     small = gcs.Grammar(1000, 2000, *gcsynth.genotype_csr(**gcsynth.GENO_SMALL))   # row emit
     for G in (slice_, heavy, small):
-        for pol in ("f32", "minplus"):
+        for pol in ("f32", "minplus") if k_max <= 16 else ("f32",):
             lay = G.layout(pol, k_max)
             with pytest.raises(gcs.GcError, match="GC_ERR_CUDA"):
                 gcs.capi.gc_upload(G._p, pol, k_max, 256, lay["arena_bytes"])

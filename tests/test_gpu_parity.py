@@ -236,3 +236,45 @@ def test_barrier_timeout_is_reported_not_hung(gcs, torch):
     # after the check the same handle computes correctly again
     np.testing.assert_array_equal(eng.matvec(x).cpu().numpy(), y_ok)
     assert eng.check() == 0
+
+
+@pytest.mark.parametrize("k", [4, 8, 32, 64, 128, 256])
+def test_batch_widths(gcs, torch, k):
+    # Appendix A's batched product at every width the float32 sum takes:
+    # a slice of the 50,000-variant generator (level emit, carry slots, a
+    # tail) and a short-row genotype matrix (row emit); every row and column
+    # against the float64 oracle, both schedules bit for bit, the
+    # allocation-free entry point bit for bit, and a one-vector product on
+    # the same handle
+    cfg = dict(gcsynth.GENO_MEDIUM, n=200)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    d = gcsynth.genotype_dense(n=300, m=900, founders=6, switch=0.01, mutation=0.005, seed=4)
+    rp2, c2, v2 = gcsynth.dense_to_csr(d)
+    for n, m, rp_, c_, v_ in ((200, cfg["m"], rp, c, v), (300, 900, rp2, c2, v2)):
+        G = gcs.Grammar(n, m, rp_, c_, v_)
+        eng = gcs.Engine(G, "f32", k)
+        X = gcsynth.beta(m, seed=k, k=k)
+        Xd = _dev(torch, X)
+        Y = eng.matvec(Xd).cpu().numpy()
+        assert eng.check() == 0
+        y_ref, b = direct.matvec_f64(rp_, c_, v_, X)
+        ok, worst = direct.within_tolerance(Y, y_ref, b, TOL)
+        assert ok, f"k={k} n={n}: max scaled error {worst:.3e}"
+        eng.schedule = "per_level"
+        np.testing.assert_array_equal(eng.matvec(Xd).cpu().numpy(), Y)
+        eng.schedule = "persistent"
+        if eng.layout["scratch_bytes"] < gcs.capi.GC_STATIC_SCRATCH_BYTES // 2:
+            Ys = torch.empty((n, k), dtype=torch.float32, device="cuda")
+            gcs.capi.gc_matvec_static(eng._h, Xd, Ys, k)
+            np.testing.assert_array_equal(Ys.cpu().numpy(), Y)
+        x1 = gcsynth.beta(m, seed=1)
+        y1 = eng.matvec(_dev(torch, x1)).cpu().numpy()
+        assert_f32_parity(y1, rp_, c_, v_, x1)
+    # a narrower supported width runs on the wide handle; other widths are refused
+    if k >= 8:
+        Xn = _dev(torch, gcsynth.beta(m, seed=2, k=4))
+        Yn = eng.matvec(Xn).cpu().numpy()
+        y_ref, b = direct.matvec_f64(rp_, c_, v_, gcsynth.beta(m, seed=2, k=4))
+        assert direct.within_tolerance(Yn, y_ref, b, TOL)[0]
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        eng.matvec(torch.zeros((m, 12), device="cuda"))
