@@ -12,9 +12,11 @@ pages) that it follows.
 
 Modules
   direct   O1: y = Mx straight from the uncompressed rows (fp64 / exact int /
-           boolean OR / float32 min-plus), plus the error scale b = |M||x|.
+           boolean OR / float32 min-plus), plus the error scale b = |M||x|;
+           the left product x = M^T y with b = |M|^T |y|.
   grammar  CSRV encoding, a naive RePair, decompression, the W-array grammar
-           evaluation (sum and min-plus), levels (Eq. 3.1), pass-through
+           evaluation (sum and min-plus), the top-down left product, levels
+           (Eq. 3.1), pass-through
            completion and live-set widths (Def. 3.2, Lemma 3.3, Sec. 4.2).
   reach    Boolean-semiring fixpoint x <- x OR (M (x) x), textbook BFS, and the
            tropical fixpoint x <- min(x, M (x) x) (Bellman-Ford).

@@ -97,6 +97,26 @@ def matvec_minplus(row_ptr, col, val, x):
     return y
 
 
+def left_matvec_f64(row_ptr, col, val, y, m):
+    """The left product x^T = y^T M, i.e. x = M^T y, and b = |M|^T |y| in
+    float64 (the dual product; the pages leave it to future work, Sec. 8).
+
+    x[j] = sum over the stored entries M[i][j] of M[i][j] * y[i], one row at a
+    time: row i adds M[i][j] * y[i] to x[j] for each of its columns j. ``y``
+    is (n,); x and b have shape (m,).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    x = np.zeros(m, dtype=np.float64)
+    b = np.zeros(m, dtype=np.float64)
+    for i in range(len(row_ptr) - 1):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        cols = np.asarray(col[s:e], dtype=np.int64)
+        v = np.asarray(val[s:e], dtype=np.float64)
+        np.add.at(x, cols, v * y[i])
+        np.add.at(b, cols, np.abs(v) * abs(y[i]))
+    return x, b
+
+
 def within_tolerance(y, y_ref, b, tol):
     """The float32 acceptance rule: |y - y_ref| <= tol * b elementwise, and
     y exactly 0 where b is 0 (an all-zero row or all-zero x support)."""

@@ -195,6 +195,39 @@ def eval_w_minplus(g, V, x):
     return y
 
 
+def eval_left(g, V, y, m):
+    """The left product x = M^T y from the grammar, top-down, in float64: a
+    symbol's weight is the sum of y over its occurrences in the rows'
+    expansions. Row r gives each symbol of its C row the weight y[r]; rules
+    are visited in reverse creation order (every parent before its
+    children, since a rule only names earlier rules), and N_i -> A B adds
+    N_i's weight to A and to B; a terminal <l, j> then adds V[l] times its
+    weight to x[j]. The reverse reading of Lemmas 2.1-2.2."""
+    y = np.asarray(y, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    R, tl, tj = g["R"], g["term_l"], g["term_j"]
+    wr = np.zeros(len(R))
+    wt = np.zeros(len(tl))
+    for r, row in enumerate(g["C"]):
+        for s in row:
+            s = int(s)
+            if s >= 0:
+                wr[s] += y[r]
+            else:
+                wt[-s - 1] += y[r]
+    for i in range(len(R) - 1, -1, -1):
+        for c in R[i]:
+            c = int(c)
+            if c >= 0:
+                wr[c] += wr[i]
+            else:
+                wt[-c - 1] += wr[i]
+    x = np.zeros(m)
+    for t in range(len(tl)):
+        x[tj[t]] += V[tl[t]] * wt[t]
+    return x
+
+
 # ----------------------------------------------------------------------------
 # Levels (Sec. 3, Eq. 3.1) and pass-through completion (Sec. 4.2)
 # ----------------------------------------------------------------------------

@@ -105,7 +105,33 @@ def _sssp_without_keeping_x(row_ptr, col, val, x0, max_iter=1000):
     return x, max_iter
 
 
+def _left_untransposed(row_ptr, col, val, y, m):
+    # x[i] += M[i][j] * y[j]: the right product's indexing, read as the left
+    y = np.asarray(y, dtype=np.float64)
+    x = np.zeros(m)
+    b = np.zeros(m)
+    for i in range(len(row_ptr) - 1):
+        for e in range(int(row_ptr[i]), int(row_ptr[i + 1])):
+            j = int(col[e])
+            if i < m and j < len(y):
+                x[i] += float(val[e]) * y[j]
+                b[i] += abs(float(val[e]) * y[j])
+    return x, b
+
+
+def _eval_left_forward_order(g, V, y, m):
+    # rules visited in creation order: children before parents, so a parent's
+    # weight has not arrived when it is passed on
+    g2 = dict(g, R=g["R"][::-1].copy())
+    n_r = len(g["R"])
+    remap = lambda s: n_r - 1 - s if s >= 0 else s
+    g2["R"] = np.array([[remap(int(a)), remap(int(b))] for a, b in g["R"][::-1]], dtype=np.int64).reshape(-1, 2)
+    g2["C"] = [[remap(int(s)) for s in row] for row in g["C"]]
+    return _orig_eval_left(g2, V, y, m)
+
+
 _orig_eval_w = grammar.eval_w
+_orig_eval_left = grammar.eval_left
 _orig_csrv = grammar.csrv
 
 MUTANTS = [
@@ -130,6 +156,10 @@ MUTANTS = [
     ("min-plus leaf multiplies", direct, "matvec_minplus",
      _minplus_with(np.min, np.inf, lambda v, x: v * x),
      ["test_minplus_matches_fp64_rounded_once", "test_minplus_closed_forms_on_worked_example"]),
+    ("left product not transposed", direct, "left_matvec_f64", _left_untransposed,
+     ["test_left_matches_dense_transposed_matmul", "test_left_closed_forms_on_worked_example"]),
+    ("left grammar sweep children first", grammar, "eval_left", _eval_left_forward_order,
+     ["test_left_grammar_sweep_matches_dense"]),
     ("shortest-path fixpoint drops min(x, .)", reach, "sssp_fixpoint", _sssp_without_keeping_x,
      ["test_sssp_matches_scipy_dijkstra", "test_sssp_iterations_on_a_path"]),
 ]

@@ -382,3 +382,44 @@ def test_sssp_iterations_on_a_path():
     xs, iters = reach.sssp_fixpoint(rp, col, w, x0)
     assert iters == n
     assert np.array_equal(xs, np.array([w[i:].sum() for i in range(n)], dtype=np.float32))
+
+
+# ---------------------------------------------------------------- left product x = M^T y
+def test_left_matches_dense_transposed_matmul():
+    for seed, rp, c, v, dense in _random_cases():
+        y = np.random.default_rng(seed + 21).standard_normal(dense.shape[0])
+        x, b = direct.left_matvec_f64(rp, c, v, y, dense.shape[1])
+        np.testing.assert_allclose(x, dense.T @ y, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(b, np.abs(dense).T @ np.abs(y), rtol=1e-12, atol=1e-12)
+
+
+def test_left_closed_forms_on_worked_example(worked):
+    M = worked["M"]
+    rp, c, v = dense_to_csr(M, np.float64)
+    n, m = M.shape
+    # y = e_r picks row r of M; y = 1 gives the column sums
+    for r in range(n):
+        y = np.zeros(n)
+        y[r] = 1.0
+        x, _ = direct.left_matvec_f64(rp, c, v, y, m)
+        assert np.array_equal(x, M[r])
+    x, _ = direct.left_matvec_f64(rp, c, v, np.ones(n), m)
+    assert np.array_equal(x, M.sum(axis=0))
+    # duality: y . (M x) == (M^T y) . x
+    g = np.random.default_rng(3)
+    xv, yv = g.standard_normal(m), g.standard_normal(n)
+    lhs = yv @ direct.matvec_f64(rp, c, v, xv)[0]
+    rhs = direct.left_matvec_f64(rp, c, v, yv, m)[0] @ xv
+    assert abs(lhs - rhs) < 1e-12
+
+
+def test_left_grammar_sweep_matches_dense(worked):
+    M = worked["M"]
+    y = np.random.default_rng(4).standard_normal(M.shape[0])
+    np.testing.assert_allclose(grammar.eval_left(worked["grammar"], worked["V"], y, M.shape[1]), M.T @ y,
+                               rtol=0, atol=1e-12)
+    for seed, rp, c, v, dense in _random_cases():
+        V, rows = grammar.csrv(rp, c, v)
+        g = grammar.repair(rows)
+        y = np.random.default_rng(seed + 5).standard_normal(dense.shape[0])
+        np.testing.assert_allclose(grammar.eval_left(g, V, y, dense.shape[1]), dense.T @ y, rtol=0, atol=1e-12)
