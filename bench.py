@@ -25,7 +25,9 @@ small and the row-blocked 50,000 x 200,000 genotype matrices, the
 2,000,000-node copy-model graph under the Boolean policy (with the
 reachability fixpoint) and, with the "_minplus" suffix, the tropical policy
 on the genotype matrix and on the graph (with the shortest-path fixpoint,
-unit edge lengths).
+unit edge lengths), and the left product x = M^T y on the genotype matrix
+("_left": a step is one left product; its algorithmic bytes are the plan's
+arrays, each read once, plus y and x).
 """
 from __future__ import annotations
 
@@ -57,6 +59,8 @@ WORKLOADS = {
     "graph_2m": dict(graph=gcsynth.GRAPH, k=1),
     # tropical (min, +): one Bellman-Ford relaxation per product
     "geno_10k_50k_minplus": dict(gen=gcsynth.GENO_MEDIUM, k=1, policy="minplus"),
+    # the left product x = M^T y (float32, one vector)
+    "geno_10k_50k_left": dict(gen=gcsynth.GENO_MEDIUM, k=1, op="left"),
     "graph_2m_minplus": dict(graph=gcsynth.GRAPH, k=1, policy="minplus"),
 }
 L2_FLUSH_BYTES = 512 << 20
@@ -252,6 +256,10 @@ def _oracle_sample(workload, seconds, steps):
         x = gcsynth.beta(gen["m"], seed=0, k=k)
         if minplus:
             product = lambda a, b: direct.matvec_minplus(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
+        elif wl.get("op") == "left":
+            yv = gcsynth.beta(gen["n"], seed=0)
+            product = lambda a, b: direct.left_matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]],
+                                                          yv[a:b], gen["m"])
         else:
             product = lambda a, b: direct.matvec_f64(rp[a:b + 1] - rp[a], c[rp[a]:rp[b]], v[rp[a]:rp[b]], x)
         block = 250
@@ -289,7 +297,8 @@ def oracle_sample_text(workload):
         what = "float32 min-plus product" if minplus else "Boolean OR product"
         return (f"{what} of the first {min(wl['graph']['nodes'], ORACLE_SAMPLE_ROWS * 100)} rows "
                 + ("" if minplus else "(64 sources per word) ") + "in blocks of 25,000")
-    what = "float32 min-plus" if minplus else "float64 direct"
+    what = ("float32 min-plus" if minplus else "float64 direct left (M^T y)" if wl.get("op") == "left"
+            else "float64 direct")
     return f"{what} product over the first {ORACLE_SAMPLE_ROWS} rows in blocks of 250"
 
 
@@ -342,6 +351,33 @@ def profile_traffic(kernel_key):
     return rec.get("dram_bytes_per_launch") if rec.get("engine_sha") == h else None
 
 
+class LeftAdapter:
+    """The left product behind the calls the timing loop makes: input y
+    (n values), output x (m values); the host-buffer form copies pinned y in
+    and x out around gc_left_matvec and synchronises."""
+
+    def __init__(self, gcs, G, dev, torch):
+        self.eng = gcs.LeftEngine(G, device=dev)
+        self.layout = self.eng.layout
+        self._torch = torch
+        self._yd = torch.empty(self.eng.n, dtype=torch.float32, device=dev)
+        self._xd = torch.empty(self.eng.m, dtype=torch.float32, device=dev)
+
+    def matvec(self, y, x, stream=None):
+        self.eng.matvec(y, x, stream=stream)
+
+    def matvec_host(self, yh, xh, stream=None):
+        torch = self._torch
+        with torch.cuda.stream(stream):
+            self._yd.copy_(torch.from_numpy(yh), non_blocking=True)
+            self.eng.matvec(self._yd, self._xd, stream=stream)
+            torch.from_numpy(xh).copy_(self._xd, non_blocking=True)
+        stream.synchronize()
+
+    def launch_count(self):
+        return self.eng.launch_count()
+
+
 def run_ours(args):
     import torch
 
@@ -376,8 +412,11 @@ def run_ours(args):
     st = G.stats()
     policy, elem, dtype_name = workload_policy(wl)
     minplus = policy == "minplus"
-    eng = gcs.Engine(G, policy, k, device=dev)
+    left = wl.get("op") == "left"
     stream = torch.cuda.current_stream(dev)
+    eng = LeftAdapter(gcs, G, dev, torch) if left else gcs.Engine(G, policy, k, device=dev)
+    # the left product reads n values and writes m
+    n_in, n_out = (gen["n"], gen["m"]) if left else (gen["m"], gen["n"])
 
     nvec = args.warmup + args.steps
     if graph and not minplus:
@@ -385,9 +424,9 @@ def run_ours(args):
             0, 2**63, gen["m"], dtype=np.int64)).to(dev) for i in range(min(nvec, 8))]
         y = torch.empty(gen["n"], dtype=torch.int64, device=dev)
     else:
-        xs = [torch.from_numpy(gcsynth.beta(gen["m"], seed=(rank * 1000 + i) % 100, k=k)).to(dev)
+        xs = [torch.from_numpy(gcsynth.beta(n_in, seed=(rank * 1000 + i) % 100, k=k)).to(dev)
               for i in range(min(nvec, 100))]
-        y = torch.empty((gen["n"],) if k == 1 else (gen["n"], k), dtype=torch.float32, device=dev)
+        y = torch.empty((n_out,) if k == 1 else (n_out, k), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(i, timed_events=None):
@@ -475,6 +514,17 @@ def run_ours(args):
         y_ref = direct.matvec_or(rp, col, x_last)
         ok = bool(np.array_equal(y_last.view(np.uint64), y_ref))
         worst = 0.0 if ok else float("inf")
+    elif left:
+        # one more product with y zero past the first 200 rows: x is then the
+        # left product of those rows alone
+        rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=200))
+        y200 = np.zeros(gen["n"], np.float32)
+        y200[:200] = gcsynth.beta(200, seed=123)
+        xd = torch.empty(gen["m"], dtype=torch.float32, device=dev)
+        eng.matvec(torch.from_numpy(y200).to(dev), xd, stream=stream)
+        torch.cuda.synchronize(dev)
+        x_ref, bnd = direct.left_matvec_f64(rp, c, v, y200[:200], gen["m"])
+        ok, worst = direct.within_tolerance(xd.cpu().numpy(), x_ref, bnd, 1e-4)
     elif minplus:
         rp, c, v = gcsynth.genotype_csr(**dict(gen, r1=200))
         xl = gcsynth.beta(gen["m"], seed=(args.warmup + args.steps - 1) % len(xs) % 100, k=k)
@@ -488,11 +538,13 @@ def run_ours(args):
         ok, worst = direct.within_tolerance(y_last[:200], y_ref, bnd, 1e-4)
 
     peak, peak_src = peaks()
-    bytes_step = compulsory_bytes(st, k, elem)
+    bytes_step = (eng.layout["grammar_bytes"] + 4 * (gen["n"] + gen["m"])) if left else compulsory_bytes(st, k, elem)
     mean_s = total_s / args.steps
     achieved = bytes_step / mean_s / 1e9
     lay = eng.layout
     footprint = lay["grammar_bytes"] + lay["scratch_bytes"] + elem * k * (gen["m"] + gen["n"])
+    kernel_name = ("whole left product: left_step_kernel x (depth + 3)" if left else
+                   "whole product: sweep_kernel + slice_kernel" if launches_per_step == 2 else "whole product: sweep_kernel")
     cpu = None
     if not args.no_cpu_baseline:
         rates, recs = cpu_oracle_rates(args.workload, args.cpu_seconds)
@@ -506,7 +558,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_name, "data": "synthetic",
         "config": {"workload": args.workload, "n": gen["n"], "m": gen["m"], "k": k,
-                   "policy": policy,
+                   "policy": policy, **({"op": "left: x = M^T y"} if left else {}),
                    **({"graph": "copy model, unit edge lengths" if minplus else "copy model, 64-bit source bitsets"}
                       if graph else
                       {"founders": gen["founders"], "switch": gen["switch"], "mutation": gen["mutation"]}),
@@ -515,12 +567,11 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profile_traffic(f"sweep:{args.workload}"),
-                     "kernel": ("whole product: sweep_kernel + slice_kernel" if launches_per_step == 2
-                                else "whole product: sweep_kernel"),
+                     "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": bytes_step},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": elem * k * gen["m"],
-                "d2h_bytes_per_step": elem * k * gen["n"]},
+        "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": elem * k * n_in,
+                "d2h_bytes_per_step": elem * k * n_out},
         "vectors_per_s": value * k,
         "fixpoint": fixpoint,
         "gpu_launches": launches_per_step * args.steps,

@@ -178,6 +178,43 @@ class Engine:
             self._h = None
 
 
+class LeftEngine:
+    """The left product x = M^T y of a grammar resident on a CUDA device
+    (float32, one right-hand side; gc_left_* of the C ABI). The arena is one
+    torch uint8 tensor; the library allocates no device memory itself."""
+
+    def __init__(self, grammar: Grammar, device="cuda", stream=None):
+        import torch
+
+        st = grammar.stats()
+        self.n, self.m = st["n"], st["m"]
+        self.layout = _capi().gc_left_layout(grammar._p)
+        self.device = torch.device(device)
+        self.arena = torch.empty(max(self.layout["arena_bytes"], 256), dtype=torch.uint8, device=self.device)
+        self._stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self._h = _capi().gc_left_upload(grammar._p, self.arena, self.arena.numel(), self._stream)
+
+    def matvec(self, y, x=None, stream=None):
+        """x = M^T y for a device float32 tensor y of shape (n,)."""
+        import torch
+        if x is None:
+            x = torch.empty(self.m, dtype=torch.float32, device=y.device)
+        _capi().gc_left_matvec(self._h, y, x, stream if stream is not None else self._stream)
+        return x
+
+    def launch_count(self) -> int:
+        return _capi().gc_left_launch_count(self._h)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            try:
+                _capi().gc_free_left_handle(h)
+            except Exception:   # interpreter shutdown
+                pass
+            self._h = None
+
+
 def _builder_fingerprint() -> str:
     from . import build as _b
     h = hashlib.sha256()

@@ -93,6 +93,11 @@ _sig = {
     "gc_builder_finish": ([_vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_builder_free": ([_vp], None),
     "gc_free_handle": ([_vp], None),
+    "gc_left_layout": ([_vp, ctypes.POINTER(ArenaLayout)], ctypes.c_int),
+    "gc_left_upload": ([_vp, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
+    "gc_left_matvec": ([_vp, _vp, _vp, _vp], ctypes.c_int),
+    "gc_left_launch_count": ([_vp, ctypes.POINTER(_i64)], ctypes.c_int),
+    "gc_free_left_handle": ([_vp], None),
 }
 for _name, (_args, _res) in _sig.items():
     _f = getattr(_lib, _name)
@@ -276,3 +281,29 @@ def gc_free_grammar(g):
 
 def gc_free_handle(h):
     _lib.gc_free_handle(h)
+
+
+def gc_left_layout(g) -> dict:
+    lay = ArenaLayout()
+    _check(_lib.gc_left_layout(g, ctypes.byref(lay)), "gc_left_layout")
+    return {f: getattr(lay, f) for f, _ in ArenaLayout._fields_}
+
+
+def gc_left_upload(g, arena, arena_bytes, stream=None) -> int:
+    h = _vp()
+    _check(_lib.gc_left_upload(g, _addr(arena), arena_bytes, _stream(stream), ctypes.byref(h)), "gc_left_upload")
+    return h.value
+
+
+def gc_left_matvec(h, y, x, stream=None):
+    _check(_lib.gc_left_matvec(h, _addr(y), _addr(x), _stream(stream)), "gc_left_matvec")
+
+
+def gc_left_launch_count(h) -> int:
+    v = _i64()
+    _check(_lib.gc_left_launch_count(h, ctypes.byref(v)), "gc_left_launch_count")
+    return v.value
+
+
+def gc_free_left_handle(h):
+    _lib.gc_free_left_handle(h)

@@ -1,0 +1,249 @@
+// Device side of the left product x = M^T y (x^T = y^T M) over the packed,
+// properly layered grammar: the pull-based top-down sweep planned in
+// left.hpp. The pages name left multiplication by pull-based reduction as
+// future work (Sec. 8); this is its plainest reading: every value is a sum
+// the reading thread gathers (no atomics, no scatter), the level sets run in
+// stream order L, L-1, ..., 1, and each sum has a fixed order, so x is the
+// same bit for bit on every run.
+//
+// One kernel serves every step: a grid of warps walks the step's tasks; a
+// LIGHT task sums up to 32 segments, one per lane, each in order from its
+// initial value; a HEAVY task sums one segment over the warp (lane l takes
+// items l, l + 32, ... in order, then a fixed xor butterfly) and adds it to
+// the initial value. Float32, each addition and product rounded separately.
+#include <cuda_runtime.h>
+
+#include <memory>
+#include <string>
+
+#include "common.hpp"
+#include "layout.hpp"
+#include "left.hpp"
+
+struct gc_left_handle {
+    int64_t n = 0, m = 0, L = 0, N = 0, rho = 0, alpha = 0;
+    std::vector<int64_t> lvl_off, lvl_roots, root_off, task_off;
+    char* arena = nullptr;
+    int sms = 1;
+    int64_t launches = 0;
+    // arena offsets
+    int64_t soff, srow, poff, pref, toff, tref, coff, vidx, V, seg, task, RS, W, TIN, total, grammar_bytes;
+};
+
+namespace gcs {
+namespace {
+
+constexpr int kLeftThreads = 256;
+
+// What one step reads and writes: segment g covers references
+// ref[off[g] .. off[g+1]) (ref == nullptr: the references are the indices
+// themselves); item i is scale(i) * src[i] (scale only for the columns).
+struct LeftStep {
+    const int32_t* off;
+    const int32_t* ref;
+    const float* src;
+    const int32_t* vidx;   // columns: terminal -> value index, else nullptr
+    const float* V;
+    // initial value of segment g: init[g - init_base] when init_base <= g <
+    // init_base + init_count, else 0
+    const float* init;
+    int64_t init_base, init_count, init_shift;
+    float* out;            // out[g - out_base]
+    int64_t out_base;
+};
+
+__device__ __forceinline__ float left_item(const LeftStep& s, int32_t q) {
+    const int32_t i = s.ref ? __ldg(s.ref + q) : q;
+    const float v = s.src[i];
+    return s.vidx ? __fmul_rn(__ldg(s.V + __ldg(s.vidx + i)), v) : v;
+}
+
+__device__ __forceinline__ float left_init(const LeftStep& s, int32_t g) {
+    const int64_t r = (int64_t)g - s.init_base;
+    return (s.init && r >= 0 && r < s.init_count) ? s.init[r + s.init_shift] : 0.0f;
+}
+
+__global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep s, const int32_t* __restrict__ task,
+                                                                 const int32_t* __restrict__ seg, int64_t t0,
+                                                                 int64_t t1) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kLeftThreads / 32);
+    for (int64_t t = t0 + (int64_t)blockIdx.x * (kLeftThreads / 32) + (threadIdx.x >> 5); t < t1; t += warps) {
+        const int32_t first = __ldg(task + 2 * t), cnt = __ldg(task + 2 * t + 1);
+        if (cnt > 0) {   // LIGHT: one segment per lane
+            if (lane < cnt) {
+                const int32_t g = __ldg(seg + first + lane);
+                float acc = left_init(s, g);
+                const int32_t q1 = __ldg(s.off + g + 1);
+                for (int32_t q = __ldg(s.off + g); q < q1; ++q) acc = __fadd_rn(acc, left_item(s, q));
+                s.out[g - s.out_base] = acc;
+            }
+        } else {         // HEAVY: one segment over the warp
+            const int32_t g = __ldg(seg + first);
+            const int32_t q1 = __ldg(s.off + g + 1);
+            float acc = 0.0f;
+            for (int32_t q = __ldg(s.off + g) + lane; q < q1; q += 32) acc = __fadd_rn(acc, left_item(s, q));
+#pragma unroll
+            for (int msk = 16; msk >= 1; msk >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, msk));
+            if (lane == 0) s.out[g - s.out_base] = __fadd_rn(left_init(s, g), acc);
+        }
+    }
+}
+
+void cuda_ok(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) fail(GC_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Arena parts, 256-byte aligned: the plan's arrays (read-only), then the
+// seed sums RS, the node weights W and the terminal sums TIN.
+void left_layout(const LeftPlan& p, gc_left_handle& h) {
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        const int64_t at = o;
+        o = align256(o + std::max<int64_t>(bytes, 4));
+        return at;
+    };
+    h.soff = take(4 * (int64_t)p.soff.size());
+    h.srow = take(4 * (int64_t)p.srow.size());
+    h.poff = take(4 * (int64_t)p.poff.size());
+    h.pref = take(4 * (int64_t)p.pref.size());
+    h.toff = take(4 * (int64_t)p.toff.size());
+    h.tref = take(4 * (int64_t)p.tref.size());
+    h.coff = take(4 * (int64_t)p.coff.size());
+    h.vidx = take(4 * (int64_t)p.term_vidx.size());
+    h.V = take(4 * (int64_t)p.V.size());
+    h.seg = take(4 * (int64_t)p.seg.size());
+    h.task = take(4 * (int64_t)p.task.size());
+    h.grammar_bytes = o;
+    h.RS = take(4 * (p.rho + p.alpha));
+    h.W = take(4 * p.N);
+    h.TIN = take(4 * p.alpha);
+    h.total = o;
+}
+
+template <class T>
+void put(cudaStream_t st, char* arena, int64_t off, const std::vector<T>& v) {
+    if (v.empty()) return;
+    cuda_ok(cudaMemcpyAsync(arena + off, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice, st), "left upload copy");
+}
+
+}  // namespace
+}  // namespace gcs
+
+using namespace gcs;
+
+extern "C" {
+
+gc_status gc_left_layout(const gc_grammar* gg, gc_arena_layout* out) {
+    return guard([&] {
+        if (!gg || !out) fail(GC_ERR_ARG, "null argument");
+        const Grammar& g = gg->g;
+        validate_packed(g);
+        const LeftPlan p = plan_left(g);
+        gc_left_handle h;
+        left_layout(p, h);
+        gc_arena_layout l{};
+        l.arena_bytes = h.total;
+        l.grammar_bytes = h.grammar_bytes;
+        l.scratch_bytes = h.total - h.grammar_bytes;
+        l.staging_bytes = 0;
+        const int64_t rp = g.nnz >= INT32_MAX ? 8 * (g.n + 1) : 4 * (g.n + 1);
+        l.csr_bytes = 8 * g.nnz + rp + 4 * (g.n + g.m);
+        *out = l;
+    });
+}
+
+gc_status gc_left_upload(const gc_grammar* gg, void* arena, int64_t arena_bytes, void* stream, gc_left_handle** out) {
+    return guard([&] {
+        if (!gg || !out) fail(GC_ERR_ARG, "null grammar or output pointer");
+        if (!arena) fail(GC_ERR_ARG, "null arena");
+        if (reinterpret_cast<uintptr_t>(arena) % 256 != 0) fail(GC_ERR_ARG, "arena must be 256-byte aligned");
+        const Grammar& g = gg->g;
+        validate_packed(g);
+        const LeftPlan p = plan_left(g);
+        validate_left_plan(p);
+        auto h = std::make_unique<gc_left_handle>();
+        left_layout(p, *h);
+        if (arena_bytes < h->total) fail(GC_ERR_ARG, "arena smaller than gc_left_layout().arena_bytes");
+        h->n = p.n;
+        h->m = p.m;
+        h->L = p.L;
+        h->N = p.N;
+        h->rho = p.rho;
+        h->alpha = p.alpha;
+        h->lvl_off = p.lvl_off;
+        h->lvl_roots = p.lvl_roots;
+        h->root_off = p.root_off;
+        h->task_off = p.task_off;
+        h->arena = static_cast<char*>(arena);
+        int dev = 0;
+        cuda_ok(cudaGetDevice(&dev), "cudaGetDevice");
+        cuda_ok(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        char* a = h->arena;
+        put(st, a, h->soff, p.soff);
+        put(st, a, h->srow, p.srow);
+        put(st, a, h->poff, p.poff);
+        put(st, a, h->pref, p.pref);
+        put(st, a, h->toff, p.toff);
+        put(st, a, h->tref, p.tref);
+        put(st, a, h->coff, p.coff);
+        put(st, a, h->vidx, p.term_vidx);
+        put(st, a, h->V, p.V);
+        put(st, a, h->seg, p.seg);
+        put(st, a, h->task, p.task);
+        cuda_ok(cudaStreamSynchronize(st), "left upload synchronize");
+        *out = h.release();
+    });
+}
+
+gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream) {
+    return guard([&] {
+        if (!h) fail(GC_ERR_ARG, "null handle");
+        if ((!y && h->n > 0) || (!x && h->m > 0)) fail(GC_ERR_ARG, "null y or x");
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        char* a = h->arena;
+        auto I = [&](int64_t off) { return reinterpret_cast<const int32_t*>(a + off); };
+        auto F = [&](int64_t off) { return reinterpret_cast<float*>(a + off); };
+        const int32_t* task = I(h->task);
+        const int32_t* seg = I(h->seg);
+        int64_t launches = 0;
+        auto run = [&](const LeftStep& s, int64_t set) {
+            const int64_t t0 = h->task_off[set], t1 = h->task_off[set + 1];
+            if (t1 <= t0) return;
+            const int64_t wpb = kLeftThreads / 32;
+            const int64_t grid = std::min<int64_t>((t1 - t0 + wpb - 1) / wpb, (int64_t)h->sms * 8);
+            left_step_kernel<<<(unsigned)grid, kLeftThreads, 0, st>>>(s, task, seg, t0, t1);
+            ++launches;
+        };
+        // seed: RS[s] = sum of y over C's references to s
+        run(LeftStep{I(h->soff), I(h->srow), static_cast<const float*>(y), nullptr, nullptr, nullptr, 0, 0, 0,
+                     F(h->RS), 0},
+            0);
+        // levels, top first: W[u] = RS[root slot] (roots) + sum of the parents' W
+        for (int64_t k = h->L; k >= 1; --k)
+            run(LeftStep{I(h->poff), I(h->pref), F(h->W), nullptr, nullptr, F(h->RS), h->lvl_off[k], h->lvl_roots[k],
+                         h->root_off[k], F(h->W), 0},
+                k);
+        // terminals: TIN[p] = RS[rho + p] + sum of the W of the nodes naming p
+        run(LeftStep{I(h->toff), I(h->tref), F(h->W), nullptr, nullptr, F(h->RS), 0, h->alpha, h->rho, F(h->TIN), 0},
+            h->L + 1);
+        // columns: x[j] = sum over column j's terminals of V[l] * TIN[p]
+        run(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), reinterpret_cast<const float*>(a + h->V), nullptr, 0,
+                     0, 0, static_cast<float*>(x), 0},
+            h->L + 2);
+        cuda_ok(cudaGetLastError(), "left kernel launch");
+        h->launches = launches;
+    });
+}
+
+gc_status gc_left_launch_count(const gc_left_handle* h, int64_t* launches) {
+    return guard([&] {
+        if (!h || !launches) fail(GC_ERR_ARG, "null argument");
+        *launches = h->launches;
+    });
+}
+
+void gc_free_left_handle(gc_left_handle* h) { delete h; }
+
+}  // extern "C"

@@ -128,6 +128,7 @@ typedef struct {
 
 typedef struct gc_grammar gc_grammar;
 typedef struct gc_handle gc_handle;
+typedef struct gc_left_handle gc_left_handle;
 
 /* Thread-local message of the last failure in this thread ("" if none).     */
 const char* gc_last_error(void);
@@ -336,6 +337,45 @@ gc_status gc_debug_inject(gc_handle* h, int32_t what, int64_t timeout_cycles);
  */
 #define GC_STATIC_SCRATCH_BYTES (32ll << 20)
 gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void* stream);
+
+/*
+ * Left product x^T = y^T M, i.e. x = M^T y, in float32 (one right-hand side):
+ * the dual of gc_matvec over the same grammar. The pages name left
+ * multiplication by pull-based reduction as future work (Sec. 8); here it is
+ * a top-down sweep over the properly layered grammar in which every value is
+ * a sum its reader gathers, in a fixed order (no atomics):
+ *   RS[s]  = sum of y[r] over row r's references to s in C (root slots and
+ *            terminals),
+ *   W[u]   = RS[u's slot] (roots) + sum of W over u's parents, level L first
+ *            (every parent of a level-k node is at level k + 1, Def. 3.2),
+ *   x[j]   = sum over the terminals <l, j> of V[l] * (RS + sum of W over the
+ *            nodes naming the terminal).
+ * Long sums run over a warp with a fixed butterfly, so each is at most about
+ * 64 + count / 32 + 5 additions deep. Deterministic: the same y gives the
+ * same x bit for bit.
+ *
+ * gc_left_layout -- device bytes a left handle needs (grammar_bytes: the
+ *   parent, seed and column lists and the task tables; scratch_bytes: RS, W
+ *   and the terminal sums; staging_bytes 0; csr_bytes as in gc_layout for
+ *   k = 1). Builds the plan on the host to size it.
+ * gc_left_upload -- builds and checks the plan on the host (every reference
+ *   within its list, every parent one level up, every segment in exactly one
+ *   task), then copies it into a caller-owned arena (device, 256-byte
+ *   aligned, at least arena_bytes, outliving the handle), enqueued on stream,
+ *   and synchronises the stream. The grammar may be freed afterwards.
+ * gc_left_matvec -- x = M^T y, asynchronous on stream: y device float[n], x
+ *   device float[m], fully written (a column no row uses gets 0); L + 3
+ *   kernel launches in stream order. One product at a time per handle (W is
+ *   shared). x and y must not overlap the arena.
+ * gc_left_launch_count -- kernel launches of the last gc_left_matvec.
+ * gc_free_left_handle -- host object only; not the arena.
+ */
+gc_status gc_left_layout(const gc_grammar* g, gc_arena_layout* out);
+gc_status gc_left_upload(const gc_grammar* g, void* arena, int64_t arena_bytes, void* stream,
+                         gc_left_handle** out);
+gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream);
+gc_status gc_left_launch_count(const gc_left_handle* h, int64_t* launches);
+void gc_free_left_handle(gc_left_handle* h);
 
 /* Serialise / restore a built grammar (host file, little-endian, versioned). */
 gc_status gc_save(const gc_grammar* g, const char* path);

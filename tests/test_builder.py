@@ -368,3 +368,56 @@ def test_streaming_builder_rejects_gaps_and_overlaps(gcs):
             capi.gc_builder_add_rows(b, 3, rp, c, v)
     finally:
         capi.gc_builder_free(b)
+
+
+def test_left_plan_replays_to_the_transpose(gcs, tmp_path):
+    # tests/native/left_plan_check.cpp builds the left product's plan, checks
+    # it, and replays its warp tasks on the CPU exactly as left_step_kernel
+    # runs them (float32 and float64) against a direct M^T y
+    import struct
+    import subprocess
+    from grammar_compressed_sparse_gb300 import build as gbuild
+    gbuild.build()
+    objs = [os.path.join(gbuild.BUILD, f + ".o") for f in gbuild.HOST_SOURCES]
+    exe = str(tmp_path / "left_plan_check")
+    subprocess.run(["g++", "-O2", "-std=c++17", "-fopenmp", "-I", gbuild.INCLUDE, "-I", gbuild.CSRC,
+                    os.path.join(ROOT, "tests", "native", "left_plan_check.cpp"), *objs, "-o", exe],
+                   check=True, capture_output=True)
+    files = []
+
+    def dump(name, n, m, rp, c, v):
+        path = str(tmp_path / name)
+        with open(path, "wb") as f:
+            f.write(struct.pack("qqq", n, m, int(rp[-1])))
+            f.write(np.asarray(rp, np.int64).tobytes())
+            f.write(np.asarray(c, np.int32).tobytes())
+            f.write(np.asarray(v, np.float32).tobytes())
+        files.append(path)
+
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    dump("slice300.bin", 300, cfg["m"], *gcsynth.genotype_csr(**cfg))
+    dump("small.bin", 1000, 2000, *gcsynth.genotype_csr(**gcsynth.GENO_SMALL))
+    rp, c, v, _ = gcsynth.random_sparse(40, 3000, 0.4, [1.0, -1.0, 0.5], 8)
+    dump("heavy.bin", 40, 3000, rp, c, v)
+    rp, col = gcsynth.copy_model_graph(nodes=3000, n0=20, d0=15, p_edit=0.05, seed=1)
+    dump("graph.bin", 3000, 3000, rp, col, gcsynth.target_lengths(col, 3000, seed=2))
+    d = np.zeros((400, 50), np.float32)
+    d[:, 7] = 1.0                         # one column in every row: long parent lists
+    d[::2, 11] = 2.0
+    dump("column.bin", 400, 50, *dense_to_csr(d, np.float32))
+    dump("empty.bin", 4, 6, np.zeros(5, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32))
+    dump("norules.bin", 2, 4, np.array([0, 2, 4], np.int64), np.array([0, 1, 2, 3], np.int32),
+         np.array([1, 2, 3, 4], np.float32))
+    out = subprocess.run([exe, *files], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.strip().endswith("OK")
+
+
+def test_left_layout_sizes(gcs):
+    d = gcsynth.genotype_dense(n=120, m=300, founders=5, switch=0.01, mutation=0.005, seed=4)
+    G = gcs.Grammar(120, 300, *gcsynth.dense_to_csr(d))
+    lay = gcs.capi.gc_left_layout(G._p)
+    st = G.stats()
+    # W holds one float per layered node; RS one per root slot and terminal
+    assert lay["scratch_bytes"] >= 4 * (st["n_nodes"] + st["n_roots"] + 2 * st["n_terminals"])
+    assert lay["arena_bytes"] == lay["grammar_bytes"] + lay["scratch_bytes"] and lay["staging_bytes"] == 0

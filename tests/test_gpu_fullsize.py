@@ -4,6 +4,8 @@
   y = G beta against the float64 oracle, persistent schedule; a 16-wide product.
 * 2,000,000-node copy-model graph (about 2e8 edges): the Boolean product and the
   reachability fixpoint from 64 sources, bit for bit against the oracle.
+* The left product x = M^T y on the genotype matrix: every column against the
+  float64 oracle.
 * The tropical (min, +) policy on both: every row of the genotype product, and
   the shortest-path fixpoint (unit lengths: hop distance to the nearest of the
   64 sources), bit for bit.
@@ -117,3 +119,13 @@ def test_graph_shortest_paths(gcs, torch):
     want, want_iters = reach.sssp_fixpoint(rp, col, ones, x0)
     assert iters == want_iters
     assert _same_bits(xs.cpu().numpy(), want)
+
+
+def test_medium_left_all_columns(gcs, torch, medium):
+    gen, rp, c, v, G = medium
+    eng = gcs.LeftEngine(G)
+    y = gcsynth.beta(gen["n"], seed=5)
+    x = eng.matvec(torch.from_numpy(y).cuda()).cpu().numpy()
+    x_ref, b = direct.left_matvec_f64(rp, c, v, y, gen["m"])
+    ok, worst = direct.within_tolerance(x, x_ref, b, TOL)
+    assert ok, f"max scaled error {worst:.3e}"

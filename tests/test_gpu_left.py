@@ -1,0 +1,106 @@
+"""GPU parity for the left product x = M^T y (gc_left_* through the C ABI).
+
+The pages name left multiplication by pull-based reduction as future work
+(Sec. 8). Tolerance as for the right product: |x_j - x_ref_j| <= 1e-4 *
+(|M|^T |y|)_j with x_j exactly 0 where that bound is 0, x_ref in float64
+(oracle.direct.left_matvec_f64). Determinism: the same y gives the same x
+bit for bit.
+"""
+import numpy as np
+import pytest
+
+import gcsynth
+from conftest import dense_to_csr
+from oracle import direct
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return t
+
+
+def left_parity(gcs, torch, n, m, rp, c, v, seed=0, y=None):
+    G = gcs.Grammar(n, m, rp, c, v)
+    eng = gcs.LeftEngine(G)
+    if y is None:
+        y = np.random.default_rng(seed).standard_normal(n).astype(np.float32)
+    yd = torch.from_numpy(y).cuda()
+    x = eng.matvec(yd).cpu().numpy()
+    x_ref, b = direct.left_matvec_f64(rp, c, v, y, m)
+    ok, worst = direct.within_tolerance(x, x_ref, b, TOL)
+    assert ok, f"max scaled error {worst:.3e}"
+    np.testing.assert_array_equal(eng.matvec(yd).cpu().numpy(), x)       # deterministic
+    assert eng.launch_count() == G.stats()["depth"] + 3
+    return x, eng
+
+
+def test_worked_example_left(gcs, torch, worked):
+    rp, c, v = dense_to_csr(worked["M"], np.float32)
+    for r in range(8):                   # y = e_r picks row r
+        y = np.zeros(8, np.float32)
+        y[r] = 1.0
+        x, _ = left_parity(gcs, torch, 8, 7, rp, c, v, y=y)
+        np.testing.assert_array_equal(x, worked["M"][r].astype(np.float32))
+    left_parity(gcs, torch, 8, 7, rp, c, v, seed=1)
+
+
+def test_small_and_genotype_left(gcs, torch):
+    for seed in range(3):
+        rp, c, v, _ = gcsynth.random_sparse(5 + 9 * seed, 7 + 11 * seed, 0.5, [1.0, 2.0, -0.5, 3.25], seed)
+        left_parity(gcs, torch, len(rp) - 1, 7 + 11 * seed, rp, c, v, seed=seed)
+    cfg = gcsynth.GENO_SMALL
+    left_parity(gcs, torch, cfg["n"], cfg["m"], *gcsynth.genotype_csr(**cfg), seed=3)
+    cfg = dict(gcsynth.GENO_MEDIUM, n=600)
+    left_parity(gcs, torch, 600, cfg["m"], *gcsynth.genotype_csr(**cfg), seed=4)
+    rp, c, v, _ = gcsynth.random_sparse(40, 3000, 0.4, [1.0, -1.0, 0.5], 8)   # bare terminals in C
+    left_parity(gcs, torch, 40, 3000, rp, c, v, seed=5)
+
+
+def test_graph_left(gcs, torch):
+    N = 3000
+    rp, col = gcsynth.copy_model_graph(nodes=N, n0=20, d0=15, p_edit=0.05, seed=1)
+    left_parity(gcs, torch, N, N, rp, col, gcsynth.target_lengths(col, N, seed=2), seed=6)
+
+
+def test_long_parent_lists_left(gcs, torch):
+    # one column in every row and rows of two kinds: warp-wide (HEAVY) sums
+    d = np.zeros((3000, 64), np.float32)
+    d[:, 7] = 1.0
+    d[::2, 11] = 2.0
+    d[1::3, 40] = -0.5
+    left_parity(gcs, torch, 3000, 64, *dense_to_csr(d, np.float32), seed=7)
+
+
+def test_edge_cases_left(gcs, torch):
+    cases = [
+        (4, 6, np.zeros(5, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32)),      # all rows empty
+        (3, 3, np.array([0, 0, 1, 1], np.int64), np.array([2], np.int32), np.array([5.0], np.float32)),
+        (2, 4, np.array([0, 2, 4], np.int64), np.array([0, 1, 2, 3], np.int32),
+         np.array([1, 2, 3, 4], np.float32)),                                             # no rules (L = 0)
+        (1, 1, np.array([0, 1], np.int64), np.array([0], np.int32), np.array([-2.5], np.float32)),
+    ]
+    for i, (n, m, rp, c, v) in enumerate(cases):
+        x, _ = left_parity(gcs, torch, n, m, rp, c, v, seed=10 + i)
+    x, _ = left_parity(gcs, torch, 4, 6, *cases[0][2:], seed=1)
+    assert np.all(x == 0)
+
+
+def test_left_argument_errors(gcs, torch):
+    rp, c, v, _ = gcsynth.random_sparse(20, 30, 0.5, [1.0, 2.0], 0)
+    G = gcs.Grammar(20, 30, rp, c, v)
+    lay = gcs.capi.gc_left_layout(G._p)
+    arena = torch.empty(lay["arena_bytes"] + 512, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_left_upload(G._p, arena.data_ptr() + 16, arena.numel() - 16)    # misaligned
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_left_upload(G._p, arena, 256)                                   # too small
+    eng = gcs.LeftEngine(G)
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_left_matvec(eng._h, None, torch.zeros(30, device="cuda"))
