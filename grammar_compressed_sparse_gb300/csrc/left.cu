@@ -7,10 +7,12 @@
 // same bit for bit on every run.
 //
 // One kernel serves every step: a grid of warps walks the step's tasks; a
-// LIGHT task sums up to 32 segments, one per lane, each in order from its
-// initial value; a HEAVY task sums one segment over the warp (lane l takes
-// items l, l + 32, ... in order, then a fixed xor butterfly) and adds it to
-// the initial value. Float32, each addition and product rounded separately.
+// LIGHT task sums up to 32 consecutive segments, one per lane, each in order
+// from its initial value (items loaded four at a time, added in order; a
+// segment too long for one lane is left to its HEAVY task); a HEAVY task sums
+// one segment over the warp (lane l takes items l, l + 32, ... in order, then
+// a fixed xor butterfly) and adds it to the initial value. Float32, each
+// addition and product rounded separately.
 #include <cuda_runtime.h>
 
 #include <memory>
@@ -27,7 +29,7 @@ struct gc_left_handle {
     int sms = 1;
     int64_t launches = 0;
     // arena offsets
-    int64_t soff, srow, poff, pref, toff, tref, coff, vidx, V, seg, task, RS, W, TIN, total, grammar_bytes;
+    int64_t soff, srow, poff, pref, toff, tref, coff, vidx, V, task, RS, W, TIN, total, grammar_bytes;
 };
 
 namespace gcs {
@@ -64,22 +66,27 @@ __device__ __forceinline__ float left_init(const LeftStep& s, int32_t g) {
 }
 
 __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep s, const int32_t* __restrict__ task,
-                                                                 const int32_t* __restrict__ seg, int64_t t0,
-                                                                 int64_t t1) {
+                                                                 int64_t t0, int64_t t1) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kLeftThreads / 32);
     for (int64_t t = t0 + (int64_t)blockIdx.x * (kLeftThreads / 32) + (threadIdx.x >> 5); t < t1; t += warps) {
         const int32_t first = __ldg(task + 2 * t), cnt = __ldg(task + 2 * t + 1);
         if (cnt > 0) {   // LIGHT: one segment per lane
-            if (lane < cnt) {
-                const int32_t g = __ldg(seg + first + lane);
+            const int32_t g = first + lane;
+            const int32_t q0 = lane < cnt ? __ldg(s.off + g) : 0, q1 = lane < cnt ? __ldg(s.off + g + 1) : 0;
+            if (lane < cnt && q1 - q0 <= kLeftLightMax) {
                 float acc = left_init(s, g);
-                const int32_t q1 = __ldg(s.off + g + 1);
-                for (int32_t q = __ldg(s.off + g); q < q1; ++q) acc = __fadd_rn(acc, left_item(s, q));
+                int32_t q = q0;
+                for (; q + 4 <= q1; q += 4) {
+                    const float v0 = left_item(s, q), v1 = left_item(s, q + 1), v2 = left_item(s, q + 2),
+                                v3 = left_item(s, q + 3);
+                    acc = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(acc, v0), v1), v2), v3);
+                }
+                for (; q < q1; ++q) acc = __fadd_rn(acc, left_item(s, q));
                 s.out[g - s.out_base] = acc;
             }
         } else {         // HEAVY: one segment over the warp
-            const int32_t g = __ldg(seg + first);
+            const int32_t g = first;
             const int32_t q1 = __ldg(s.off + g + 1);
             float acc = 0.0f;
             for (int32_t q = __ldg(s.off + g) + lane; q < q1; q += 32) acc = __fadd_rn(acc, left_item(s, q));
@@ -112,7 +119,6 @@ void left_layout(const LeftPlan& p, gc_left_handle& h) {
     h.coff = take(4 * (int64_t)p.coff.size());
     h.vidx = take(4 * (int64_t)p.term_vidx.size());
     h.V = take(4 * (int64_t)p.V.size());
-    h.seg = take(4 * (int64_t)p.seg.size());
     h.task = take(4 * (int64_t)p.task.size());
     h.grammar_bytes = o;
     h.RS = take(4 * (p.rho + p.alpha));
@@ -190,7 +196,6 @@ gc_status gc_left_upload(const gc_grammar* gg, void* arena, int64_t arena_bytes,
         put(st, a, h->coff, p.coff);
         put(st, a, h->vidx, p.term_vidx);
         put(st, a, h->V, p.V);
-        put(st, a, h->seg, p.seg);
         put(st, a, h->task, p.task);
         cuda_ok(cudaStreamSynchronize(st), "left upload synchronize");
         *out = h.release();
@@ -206,14 +211,13 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
         auto I = [&](int64_t off) { return reinterpret_cast<const int32_t*>(a + off); };
         auto F = [&](int64_t off) { return reinterpret_cast<float*>(a + off); };
         const int32_t* task = I(h->task);
-        const int32_t* seg = I(h->seg);
         int64_t launches = 0;
         auto run = [&](const LeftStep& s, int64_t set) {
             const int64_t t0 = h->task_off[set], t1 = h->task_off[set + 1];
             if (t1 <= t0) return;
             const int64_t wpb = kLeftThreads / 32;
             const int64_t grid = std::min<int64_t>((t1 - t0 + wpb - 1) / wpb, (int64_t)h->sms * 8);
-            left_step_kernel<<<(unsigned)grid, kLeftThreads, 0, st>>>(s, task, seg, t0, t1);
+            left_step_kernel<<<(unsigned)grid, kLeftThreads, 0, st>>>(s, task, t0, t1);
             ++launches;
         };
         // seed: RS[s] = sum of y over C's references to s

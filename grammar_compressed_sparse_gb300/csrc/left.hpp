@@ -19,10 +19,11 @@
 //   columns  x[j]   = sum over the terminals p = <l, j> of V[l] * TIN[p]
 //
 // Each step is a set of segments (a sum over a list of references). A warp
-// task reduces either up to 32 short segments, one per lane, in order
-// (LIGHT: at most kLeftLightMax items each), or one long segment over all 32
-// lanes: lane l sums items l, l + 32, ... in order, then the lanes combine by
-// a fixed butterfly (HEAVY). So no sum is a sequential chain longer than
+// task reduces either up to 32 consecutive segments, one per lane, each in
+// order (LIGHT; a lane whose segment holds more than kLeftLightMax items
+// leaves it to a HEAVY task), or one long segment over all 32 lanes: lane l
+// sums items l, l + 32, ... in order, then the lanes combine by a fixed
+// butterfly (HEAVY). So no sum is a sequential chain longer than
 // kLeftLightMax + count / 32 + 5 additions.
 #pragma once
 
@@ -51,39 +52,30 @@ struct LeftPlan {
     std::vector<int32_t> coff;
     std::vector<int32_t> term_vidx;
     std::vector<float> V;
-    // warp tasks of every set: (first index into seg, count > 0 LIGHT, or
-    // -1 HEAVY for the one segment seg[first]); set s owns
-    // tasks[task_off[s] .. task_off[s+1]) and its segment ids in seg
-    std::vector<int32_t> seg;
+    // warp tasks of every set: (first segment, count > 0: LIGHT over
+    // segments first .. first + count - 1; -1: HEAVY for segment first); set
+    // s owns tasks[task_off[s] .. task_off[s+1])
     std::vector<int32_t> task;      // 2 per task
     std::vector<int64_t> task_off;  // L+4
     int64_t n_tasks() const { return (int64_t)task.size() / 2; }
 };
 
-// Tasks of one segment set: light segments (count <= kLeftLightMax) in
-// their natural order, 32 to a task, then one task per heavy segment.
+// Tasks of one segment set: the segments in runs of 32 (LIGHT; their heavy
+// segments, over kLeftLightMax items, skipped), then one task per heavy
+// segment.
+inline bool left_heavy(const std::vector<int32_t>& off, int64_t s) {
+    return (int64_t)off[s + 1] - off[s] > kLeftLightMax;
+}
 inline void left_tasks(LeftPlan& p, int64_t first, int64_t count, const std::vector<int32_t>& off) {
-    std::vector<int32_t> heavy;
-    int32_t open = -1;
-    for (int64_t s = first; s < first + count; ++s) {
-        const int64_t c = (int64_t)off[s + 1] - off[s];
-        if (c > kLeftLightMax) {
-            heavy.push_back((int32_t)s);
-            continue;
-        }
-        if (open < 0 || p.task[2 * open + 1] == 32) {
-            open = (int32_t)(p.task.size() / 2);
-            p.task.push_back((int32_t)p.seg.size());
-            p.task.push_back(0);
-        }
-        p.seg.push_back((int32_t)s);
-        ++p.task[2 * open + 1];
+    for (int64_t s = first; s < first + count; s += 32) {
+        p.task.push_back((int32_t)s);
+        p.task.push_back((int32_t)std::min<int64_t>(32, first + count - s));
     }
-    for (int32_t s : heavy) {
-        p.task.push_back((int32_t)p.seg.size());
-        p.task.push_back(-1);
-        p.seg.push_back(s);
-    }
+    for (int64_t s = first; s < first + count; ++s)
+        if (left_heavy(off, s)) {
+            p.task.push_back((int32_t)s);
+            p.task.push_back(-1);
+        }
 }
 
 // CSR by counting: for keys key[e] < nkeys, the values val[e] grouped by key,
@@ -216,12 +208,12 @@ inline void validate_left_plan(const LeftPlan& p) {
         for (int64_t t = p.task_off[s]; t < p.task_off[s + 1]; ++t) {
             const int32_t first = p.task[2 * t], cnt = p.task[2 * t + 1];
             const int32_t k = cnt < 0 ? 1 : cnt;
-            if (cnt == 0 || cnt > 32 || cnt < -1 || first < 0 || (int64_t)first + k > (int64_t)p.seg.size())
-                bad("task");
+            if (cnt == 0 || cnt > 32 || cnt < -1 || first < lo || (int64_t)first + k > hi) bad("task");
             for (int32_t i = 0; i < k; ++i) {
-                const int32_t sg = p.seg[first + i];
-                if (sg < lo || sg >= hi || seen[sg - lo]++) bad("task segment");
-                if (cnt > 0 && off[sg + 1] - off[sg] > kLeftLightMax) bad("light segment too long");
+                const int32_t sg = first + i;
+                const bool heavy = left_heavy(off, sg);
+                if (cnt < 0 && !heavy) bad("heavy task on a short segment");
+                if ((cnt < 0) == heavy && seen[sg - lo]++) bad("segment summed twice");
             }
         }
         for (int32_t c : seen)

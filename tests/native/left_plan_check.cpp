@@ -1,6 +1,7 @@
 // Checks the left product's host plan (left.hpp) on the CPU: builds it for a
 // matrix, validates it, and replays its tasks the way left_step_kernel does
-// (LIGHT: one segment per lane, in order from its initial value; HEAVY: 32
+// (LIGHT: one segment per lane of a run of 32, in order from its initial
+// value, segments over kLeftLightMax items left to their HEAVY task; HEAVY: 32
 // lane partial sums in order, then the xor butterfly, added to the initial
 // value), in float32 with every operation rounded separately and again in
 // float64. Compares x with a direct M^T y: the float64 replay within 1e-9,
@@ -29,13 +30,14 @@ static std::vector<T> replay(const LeftPlan& p, const std::vector<T>& y) {
             const int32_t first = p.task[2 * t], cnt = p.task[2 * t + 1];
             if (cnt > 0) {
                 for (int32_t l = 0; l < cnt; ++l) {
-                    const int32_t g = p.seg[first + l];
+                    const int32_t g = first + l;
+                    if (off[g + 1] - off[g] > kLeftLightMax) continue;   // its HEAVY task sums it
                     T acc = init(g);
                     for (int32_t q = off[g]; q < off[g + 1]; ++q) acc = acc + item(q);
                     store(g, acc);
                 }
             } else {
-                const int32_t g = p.seg[first];
+                const int32_t g = first;
                 T lane[32];
                 for (int l = 0; l < 32; ++l) {
                     lane[l] = T(0);

@@ -37,7 +37,8 @@ def left_parity(gcs, torch, n, m, rp, c, v, seed=0, y=None):
     ok, worst = direct.within_tolerance(x, x_ref, b, TOL)
     assert ok, f"max scaled error {worst:.3e}"
     np.testing.assert_array_equal(eng.matvec(yd).cpu().numpy(), x)       # deterministic
-    assert eng.launch_count() == G.stats()["depth"] + 3
+    # seed, one step per level, terminals, columns; steps with nothing to sum are skipped
+    assert 1 <= eng.launch_count() <= G.stats()["depth"] + 3
     return x, eng
 
 
@@ -88,8 +89,9 @@ def test_edge_cases_left(gcs, torch):
     ]
     for i, (n, m, rp, c, v) in enumerate(cases):
         x, _ = left_parity(gcs, torch, n, m, rp, c, v, seed=10 + i)
-    x, _ = left_parity(gcs, torch, 4, 6, *cases[0][2:], seed=1)
+    x, eng = left_parity(gcs, torch, 4, 6, *cases[0][2:], seed=1)
     assert np.all(x == 0)
+    assert eng.launch_count() == 1          # only the columns step has segments
 
 
 def test_left_argument_errors(gcs, torch):
