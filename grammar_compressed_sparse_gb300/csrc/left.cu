@@ -13,6 +13,11 @@
 // one segment over the warp (lane l takes items l, l + 32, ... in order, then
 // a fixed xor butterfly) and adds it to the initial value. Float32, each
 // addition and product rounded separately.
+//
+// The L + 3 steps are one CUDA graph per handle, a chain of kernel nodes
+// built on the first product; later products update the two nodes that read
+// y and write x when those pointers change, and launch the graph, which
+// spares the per-launch gaps of a stream of short dependent kernels.
 #include <cuda_runtime.h>
 
 #include <memory>
@@ -30,6 +35,17 @@ struct gc_left_handle {
     int64_t launches = 0;
     // arena offsets
     int64_t soff, srow, poff, pref, toff, tref, coff, vidx, V, task, RS, W, TIN, total, grammar_bytes;
+    // the steps as a graph: its kernel nodes and the step set of each
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<cudaGraphNode_t> nodes;
+    std::vector<int64_t> node_set;
+    const void* y_last = nullptr;
+    void* x_last = nullptr;
+    ~gc_left_handle() {
+        if (exec) cudaGraphExecDestroy(exec);
+        if (graph) cudaGraphDestroy(graph);
+    }
 };
 
 namespace gcs {
@@ -127,6 +143,62 @@ void left_layout(const LeftPlan& p, gc_left_handle& h) {
     h.total = o;
 }
 
+// One step of a product: its arguments and launch shape.
+struct StepLaunch {
+    LeftStep s;
+    const int32_t* task;
+    int64_t t0, t1, set;
+    unsigned grid;
+};
+
+// The product's steps in order (steps with no task left out).
+std::vector<StepLaunch> left_steps(const gc_left_handle* h, const void* y, void* x) {
+    char* a = h->arena;
+    auto I = [&](int64_t off) { return reinterpret_cast<const int32_t*>(a + off); };
+    auto F = [&](int64_t off) { return reinterpret_cast<float*>(a + off); };
+    std::vector<StepLaunch> out;
+    auto add = [&](const LeftStep& s, int64_t set) {
+        const int64_t t0 = h->task_off[set], t1 = h->task_off[set + 1];
+        if (t1 <= t0) return;
+        const int64_t wpb = kLeftThreads / 32;
+        const int64_t grid = std::min<int64_t>((t1 - t0 + wpb - 1) / wpb, (int64_t)h->sms * 8);
+        out.push_back(StepLaunch{s, I(h->task), t0, t1, set, (unsigned)grid});
+    };
+    // seed: RS[s] = sum of y over C's references to s
+    add(LeftStep{I(h->soff), I(h->srow), static_cast<const float*>(y), nullptr, nullptr, nullptr, 0, 0, 0, F(h->RS), 0},
+        0);
+    // levels, top first: W[u] = RS[root slot] (roots) + sum of the parents' W
+    for (int64_t k = h->L; k >= 1; --k)
+        add(LeftStep{I(h->poff), I(h->pref), F(h->W), nullptr, nullptr, F(h->RS), h->lvl_off[k], h->lvl_roots[k],
+                     h->root_off[k], F(h->W), 0},
+            k);
+    // terminals: TIN[p] = RS[rho + p] + sum of the W of the nodes naming p
+    add(LeftStep{I(h->toff), I(h->tref), F(h->W), nullptr, nullptr, F(h->RS), 0, h->alpha, h->rho, F(h->TIN), 0},
+        h->L + 1);
+    // columns: x[j] = sum over column j's terminals of V[l] * TIN[p]
+    add(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), reinterpret_cast<const float*>(a + h->V), nullptr, 0, 0,
+                 0, static_cast<float*>(x), 0},
+        h->L + 2);
+    return out;
+}
+
+// Kernel-node parameters of a step; args holds the argument pointers and
+// must live until the call that takes the parameters returns.
+cudaKernelNodeParams node_params(StepLaunch& l, void* (&args)[4]) {
+    args[0] = &l.s;
+    args[1] = &l.task;
+    args[2] = &l.t0;
+    args[3] = &l.t1;
+    cudaKernelNodeParams kp{};
+    kp.func = reinterpret_cast<void*>(left_step_kernel);
+    kp.gridDim = dim3(l.grid);
+    kp.blockDim = dim3(kLeftThreads);
+    kp.sharedMemBytes = 0;
+    kp.kernelParams = args;
+    kp.extra = nullptr;
+    return kp;
+}
+
 template <class T>
 void put(cudaStream_t st, char* arena, int64_t off, const std::vector<T>& v) {
     if (v.empty()) return;
@@ -207,37 +279,38 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
         if (!h) fail(GC_ERR_ARG, "null handle");
         if ((!y && h->n > 0) || (!x && h->m > 0)) fail(GC_ERR_ARG, "null y or x");
         cudaStream_t st = static_cast<cudaStream_t>(stream);
-        char* a = h->arena;
-        auto I = [&](int64_t off) { return reinterpret_cast<const int32_t*>(a + off); };
-        auto F = [&](int64_t off) { return reinterpret_cast<float*>(a + off); };
-        const int32_t* task = I(h->task);
-        int64_t launches = 0;
-        auto run = [&](const LeftStep& s, int64_t set) {
-            const int64_t t0 = h->task_off[set], t1 = h->task_off[set + 1];
-            if (t1 <= t0) return;
-            const int64_t wpb = kLeftThreads / 32;
-            const int64_t grid = std::min<int64_t>((t1 - t0 + wpb - 1) / wpb, (int64_t)h->sms * 8);
-            left_step_kernel<<<(unsigned)grid, kLeftThreads, 0, st>>>(s, task, t0, t1);
-            ++launches;
-        };
-        // seed: RS[s] = sum of y over C's references to s
-        run(LeftStep{I(h->soff), I(h->srow), static_cast<const float*>(y), nullptr, nullptr, nullptr, 0, 0, 0,
-                     F(h->RS), 0},
-            0);
-        // levels, top first: W[u] = RS[root slot] (roots) + sum of the parents' W
-        for (int64_t k = h->L; k >= 1; --k)
-            run(LeftStep{I(h->poff), I(h->pref), F(h->W), nullptr, nullptr, F(h->RS), h->lvl_off[k], h->lvl_roots[k],
-                         h->root_off[k], F(h->W), 0},
-                k);
-        // terminals: TIN[p] = RS[rho + p] + sum of the W of the nodes naming p
-        run(LeftStep{I(h->toff), I(h->tref), F(h->W), nullptr, nullptr, F(h->RS), 0, h->alpha, h->rho, F(h->TIN), 0},
-            h->L + 1);
-        // columns: x[j] = sum over column j's terminals of V[l] * TIN[p]
-        run(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), reinterpret_cast<const float*>(a + h->V), nullptr, 0,
-                     0, 0, static_cast<float*>(x), 0},
-            h->L + 2);
-        cuda_ok(cudaGetLastError(), "left kernel launch");
-        h->launches = launches;
+        std::vector<StepLaunch> steps = left_steps(h, y, x);
+        if (steps.empty()) {
+            h->launches = 0;
+            return;
+        }
+        if (!h->exec) {
+            // first product: the chain of kernel nodes, in step order
+            cuda_ok(cudaGraphCreate(&h->graph, 0), "left graph create");
+            for (StepLaunch& l : steps) {
+                void* args[4];
+                const cudaKernelNodeParams kp = node_params(l, args);
+                cudaGraphNode_t node = nullptr;
+                const cudaGraphNode_t* dep = h->nodes.empty() ? nullptr : &h->nodes.back();
+                cuda_ok(cudaGraphAddKernelNode(&node, h->graph, dep, dep ? 1 : 0, &kp), "left graph node");
+                h->nodes.push_back(node);
+                h->node_set.push_back(l.set);
+            }
+            cuda_ok(cudaGraphInstantiate(&h->exec, h->graph, 0), "left graph instantiate");
+        } else if (y != h->y_last || x != h->x_last) {
+            // new y or x: the seed and column nodes take the new pointers
+            for (size_t i = 0; i < steps.size(); ++i)
+                if (steps[i].set == 0 || steps[i].set == h->L + 2) {
+                    if (h->node_set[i] != steps[i].set) fail(GC_ERR_ARG, "left graph does not match its steps");
+                    void* args[4];
+                    const cudaKernelNodeParams kp = node_params(steps[i], args);
+                    cuda_ok(cudaGraphExecKernelNodeSetParams(h->exec, h->nodes[i], &kp), "left graph update");
+                }
+        }
+        h->y_last = y;
+        h->x_last = x;
+        cuda_ok(cudaGraphLaunch(h->exec, st), "left graph launch");
+        h->launches = (int64_t)steps.size();
     });
 }
 

@@ -364,11 +364,14 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
  *   aligned, at least arena_bytes, outliving the handle), enqueued on stream,
  *   and synchronises the stream. The grammar may be freed afterwards.
  * gc_left_matvec -- x = M^T y, asynchronous on stream: y device float[n], x
- *   device float[m], fully written (a column no row uses gets 0); L + 3
- *   kernel launches in stream order. One product at a time per handle (W is
- *   shared). x and y must not overlap the arena.
- * gc_left_launch_count -- kernel launches of the last gc_left_matvec.
- * gc_free_left_handle -- host object only; not the arena.
+ *   device float[m], fully written (a column no row uses gets 0). The L + 3
+ *   steps (fewer when a step has nothing to sum) run as one CUDA graph of the
+ *   handle, a chain of kernel nodes built by the first call; a call with new
+ *   y or x pointers updates the two nodes that use them. One product at a
+ *   time per handle, from one host thread (the graph and W are shared). x and
+ *   y must not overlap the arena.
+ * gc_left_launch_count -- kernels the last gc_left_matvec ran.
+ * gc_free_left_handle -- host object and its graph; not the arena.
  */
 gc_status gc_left_layout(const gc_grammar* g, gc_arena_layout* out);
 gc_status gc_left_upload(const gc_grammar* g, void* arena, int64_t arena_bytes, void* stream,

@@ -106,3 +106,24 @@ def test_left_argument_errors(gcs, torch):
     eng = gcs.LeftEngine(G)
     with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
         gcs.capi.gc_left_matvec(eng._h, None, torch.zeros(30, device="cuda"))
+
+
+def test_left_graph_follows_new_pointers(gcs, torch):
+    # the steps run as one graph built on the first call; later calls with
+    # other y / x buffers must read and write those, in any order
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    G = gcs.Grammar(300, cfg["m"], rp, c, v)
+    eng = gcs.LeftEngine(G)
+    ys = [gcsynth.beta(300, seed=s) for s in (1, 2)]
+    yd = [torch.from_numpy(y).cuda() for y in ys]
+    xd = [torch.full((cfg["m"],), float("nan"), device="cuda") for _ in range(2)]
+    want = []
+    for y in ys:
+        x_ref, b = direct.left_matvec_f64(rp, c, v, y, cfg["m"])
+        want.append((x_ref, b))
+    for i, j in [(0, 0), (1, 1), (0, 1), (1, 0), (1, 0)]:
+        xd[j].fill_(float("nan"))
+        eng.matvec(yd[i], xd[j])
+        x = xd[j].cpu().numpy()
+        assert direct.within_tolerance(x, *want[i], TOL)[0], (i, j)
