@@ -81,31 +81,56 @@ __device__ __forceinline__ float left_init(const LeftStep& s, int32_t g) {
     return (s.init && r >= 0 && r < s.init_count) ? s.init[r + s.init_shift] : 0.0f;
 }
 
+// A warp's tasks are t0 + w, t0 + w + warps, ...; the next task's header and
+// segment offsets are loaded before the current task is summed, so their
+// latency hides behind its gathers.
+struct TaskHead {
+    int32_t first, cnt, q0, q1;
+};
+
+__device__ __forceinline__ TaskHead load_head(const LeftStep& s, const int32_t* __restrict__ task, int64_t t,
+                                              int64_t t1, int lane) {
+    TaskHead h{0, 0, 0, 0};
+    if (t < t1) {
+        h.first = __ldg(task + 2 * t);
+        h.cnt = __ldg(task + 2 * t + 1);
+        // LIGHT: lane's own segment; HEAVY: the one segment
+        const int32_t g = h.cnt > 0 ? h.first + lane : h.first;
+        if (h.cnt < 0 || lane < h.cnt) {
+            h.q0 = __ldg(s.off + g);
+            h.q1 = __ldg(s.off + g + 1);
+        }
+    }
+    return h;
+}
+
 __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep s, const int32_t* __restrict__ task,
                                                                  int64_t t0, int64_t t1) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kLeftThreads / 32);
-    for (int64_t t = t0 + (int64_t)blockIdx.x * (kLeftThreads / 32) + (threadIdx.x >> 5); t < t1; t += warps) {
-        const int32_t first = __ldg(task + 2 * t), cnt = __ldg(task + 2 * t + 1);
-        if (cnt > 0) {   // LIGHT: one segment per lane
-            const int32_t g = first + lane;
-            const int32_t q0 = lane < cnt ? __ldg(s.off + g) : 0, q1 = lane < cnt ? __ldg(s.off + g + 1) : 0;
-            if (lane < cnt && q1 - q0 <= kLeftLightMax) {
+    int64_t t = t0 + (int64_t)blockIdx.x * (kLeftThreads / 32) + (threadIdx.x >> 5);
+    TaskHead h = load_head(s, task, t, t1, lane);
+    while (t < t1) {
+        const TaskHead c = h;
+        t += warps;
+        h = load_head(s, task, t, t1, lane);
+        if (c.cnt > 0) {   // LIGHT: one segment per lane
+            const int32_t g = c.first + lane;
+            if (lane < c.cnt && c.q1 - c.q0 <= kLeftLightMax) {
                 float acc = left_init(s, g);
-                int32_t q = q0;
-                for (; q + 4 <= q1; q += 4) {
+                int32_t q = c.q0;
+                for (; q + 4 <= c.q1; q += 4) {
                     const float v0 = left_item(s, q), v1 = left_item(s, q + 1), v2 = left_item(s, q + 2),
                                 v3 = left_item(s, q + 3);
                     acc = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(acc, v0), v1), v2), v3);
                 }
-                for (; q < q1; ++q) acc = __fadd_rn(acc, left_item(s, q));
+                for (; q < c.q1; ++q) acc = __fadd_rn(acc, left_item(s, q));
                 s.out[g - s.out_base] = acc;
             }
-        } else {         // HEAVY: one segment over the warp
-            const int32_t g = first;
-            const int32_t q1 = __ldg(s.off + g + 1);
+        } else {           // HEAVY: one segment over the warp
+            const int32_t g = c.first;
             float acc = 0.0f;
-            for (int32_t q = __ldg(s.off + g) + lane; q < q1; q += 32) acc = __fadd_rn(acc, left_item(s, q));
+            for (int32_t q = c.q0 + lane; q < c.q1; q += 32) acc = __fadd_rn(acc, left_item(s, q));
 #pragma unroll
             for (int msk = 16; msk >= 1; msk >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, msk));
             if (lane == 0) s.out[g - s.out_base] = __fadd_rn(left_init(s, g), acc);
