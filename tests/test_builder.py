@@ -421,3 +421,31 @@ def test_left_layout_sizes(gcs):
     # W holds one float per layered node; RS one per root slot and terminal
     assert lay["scratch_bytes"] >= 4 * (st["n_nodes"] + st["n_roots"] + 2 * st["n_terminals"])
     assert lay["arena_bytes"] == lay["grammar_bytes"] + lay["scratch_bytes"] and lay["staging_bytes"] == 0
+
+
+def test_corrupted_grammar_file_is_rejected(gcs, tmp_path):
+    # a child reference pointed past its level below: gc_load's validation
+    # must refuse the file (no device is ever handed such a grammar)
+    d = gcsynth.genotype_dense(n=40, m=120, founders=4, switch=0.02, mutation=0.01, seed=2)
+    rp, c, v = gcsynth.dense_to_csr(d)
+    G = gcs.Grammar(40, 120, rp, c, v)
+    ex = export_all(G)
+    p = str(tmp_path / "g.bin")
+    G.save(p)
+    raw = bytearray(open(p, "rb").read())
+    nodes = ex["nodes"].astype(np.int32)
+    at = bytes(raw).find(nodes.tobytes())
+    assert at >= 0 and ex["lvl_off"][-2] > ex["lvl_off"][2]     # found, and there is a level >= 2
+    k2 = int(ex["lvl_off"][2])                                  # first node of level 2
+    bad = nodes.copy()
+    bad[2 * k2] = 1 << 30                                       # its first child: far outside level 1
+    raw[at:at + len(nodes.tobytes())] = bad.tobytes()
+    q = str(tmp_path / "bad.bin")
+    open(q, "wb").write(bytes(raw))
+    with pytest.raises(gcs.GcError, match="GC_ERR_INVALID_GRAMMAR"):
+        gcs.Grammar.load(q)
+    raw2 = bytearray(open(p, "rb").read())
+    raw2[0] ^= 0xFF                                             # not the file's magic
+    open(q, "wb").write(bytes(raw2))
+    with pytest.raises(gcs.GcError, match="GC_ERR_IO"):
+        gcs.Grammar.load(q)
