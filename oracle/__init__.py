@@ -13,7 +13,8 @@ pages) that it follows.
 Modules
   direct   O1: y = Mx straight from the uncompressed rows (fp64 / exact int /
            boolean OR / float32 min-plus), plus the error scale b = |M||x|;
-           the left product x = M^T y with b = |M|^T |y|.
+           the left product x = M^T y (float64 with b = |M|^T |y|, exact
+           int64, Boolean OR, float32 min-plus).
   grammar  CSRV encoding, a naive RePair, decompression, the W-array grammar
            evaluation (sum and min-plus), the top-down left product, levels
            (Eq. 3.1), pass-through

@@ -117,6 +117,43 @@ def left_matvec_f64(row_ptr, col, val, y, m):
     return x, b
 
 
+def left_matvec_i64(row_ptr, col, val, y, m):
+    """Exact integer left product x = M^T y (int64): x[j] = sum of M[i][j] * y[i]."""
+    y = np.asarray(y, dtype=np.int64)
+    v_all = np.asarray(val)
+    if not np.all(np.floor(v_all) == v_all):
+        raise ValueError("integer product needs integer matrix values")
+    x = np.zeros(m, dtype=np.int64)
+    for i in range(len(row_ptr) - 1):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        np.add.at(x, np.asarray(col[s:e], dtype=np.int64), v_all[s:e].astype(np.int64) * y[i])
+    return x
+
+
+def left_matvec_or(row_ptr, col, y, m):
+    """Boolean left product (Sec. 5 semiring): x[j] = OR of y[i] over the
+    stored entries (i, j); with y a frontier of 64-bit source sets, one
+    forward step along the edges i -> j."""
+    y = np.asarray(y, dtype=np.uint64)
+    x = np.zeros(m, dtype=np.uint64)
+    for i in range(len(row_ptr) - 1):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        np.bitwise_or.at(x, np.asarray(col[s:e], dtype=np.int64), y[i])
+    return x
+
+
+def left_matvec_minplus(row_ptr, col, val, y, m):
+    """Tropical left product: x[j] = min of M[i][j] + y[i] over the stored
+    entries (i, j), each sum rounded to float32, +inf for a column no row
+    uses; with y distances, one forward Bellman-Ford relaxation."""
+    y = np.asarray(y, dtype=np.float32)
+    x = np.full(m, np.inf, dtype=np.float32)
+    for i in range(len(row_ptr) - 1):
+        s, e = int(row_ptr[i]), int(row_ptr[i + 1])
+        np.minimum.at(x, np.asarray(col[s:e], dtype=np.int64), np.asarray(val[s:e], dtype=np.float32) + y[i])
+    return x
+
+
 def within_tolerance(y, y_ref, b, tol):
     """The float32 acceptance rule: |y - y_ref| <= tol * b elementwise, and
     y exactly 0 where b is 0 (an all-zero row or all-zero x support)."""

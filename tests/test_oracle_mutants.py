@@ -130,6 +130,30 @@ def _eval_left_forward_order(g, V, y, m):
     return _orig_eval_left(g2, V, y, m)
 
 
+def _left_or_and(row_ptr, col, y, m):
+    y = np.asarray(y, dtype=np.uint64)
+    x = np.full(m, np.uint64(2**64 - 1), dtype=np.uint64)
+    seen = np.zeros(m, bool)
+    for i in range(len(row_ptr) - 1):
+        for e in range(int(row_ptr[i]), int(row_ptr[i + 1])):
+            x[col[e]] &= y[i]
+            seen[col[e]] = True
+    x[~seen] = 0
+    return x
+
+
+def _left_minplus_max(row_ptr, col, val, y, m):
+    y = np.asarray(y, dtype=np.float32)
+    x = np.full(m, np.inf, dtype=np.float32)
+    seen = np.zeros(m, bool)
+    for i in range(len(row_ptr) - 1):
+        for e in range(int(row_ptr[i]), int(row_ptr[i + 1])):
+            t = np.float32(val[e]) + y[i]
+            x[col[e]] = t if not seen[col[e]] else max(x[col[e]], t)
+            seen[col[e]] = True
+    return x
+
+
 _orig_eval_w = grammar.eval_w
 _orig_eval_left = grammar.eval_left
 _orig_csrv = grammar.csrv
@@ -160,6 +184,10 @@ MUTANTS = [
      ["test_left_matches_dense_transposed_matmul", "test_left_closed_forms_on_worked_example"]),
     ("left grammar sweep children first", grammar, "eval_left", _eval_left_forward_order,
      ["test_left_grammar_sweep_matches_dense"]),
+    ("Boolean left product uses AND", direct, "left_matvec_or", _left_or_and,
+     ["test_left_products_equal_right_products_of_the_transpose", "test_left_boolean_and_minplus_brute_force"]),
+    ("tropical left product uses max", direct, "left_matvec_minplus", _left_minplus_max,
+     ["test_left_products_equal_right_products_of_the_transpose", "test_left_boolean_and_minplus_brute_force"]),
     ("shortest-path fixpoint drops min(x, .)", reach, "sssp_fixpoint", _sssp_without_keeping_x,
      ["test_sssp_matches_scipy_dijkstra", "test_sssp_iterations_on_a_path"]),
 ]

@@ -423,3 +423,48 @@ def test_left_grammar_sweep_matches_dense(worked):
         g = grammar.repair(rows)
         y = np.random.default_rng(seed + 5).standard_normal(dense.shape[0])
         np.testing.assert_allclose(grammar.eval_left(g, V, y, dense.shape[1]), dense.T @ y, rtol=0, atol=1e-12)
+
+
+def _transpose_csr(rp, c, v, n, m):
+    T = sp.csr_matrix((np.asarray(v, np.float64), np.asarray(c), np.asarray(rp)), shape=(n, m)).T.tocsr()
+    T.sort_indices()
+    return T.indptr.astype(np.int64), T.indices.astype(np.int32), T.data
+
+
+def test_left_products_equal_right_products_of_the_transpose():
+    # every left product is the right product of M^T, built by scipy; the
+    # right products are pinned above
+    for seed, rp, c, v, dense in _minplus_cases():
+        n, m = dense.shape
+        trp, tc, tv = _transpose_csr(rp, c, v, n, m)
+        g = np.random.default_rng(seed + 31)
+        y = g.standard_normal(n)
+        np.testing.assert_allclose(direct.left_matvec_f64(rp, c, v, y, m)[0], direct.matvec_f64(trp, tc, tv, y)[0],
+                                   rtol=1e-12, atol=1e-12)
+        yi = g.integers(-1000, 1000, n)
+        vi = np.round(np.asarray(v) * 2)
+        trp2, tc2, tv2 = _transpose_csr(rp, c, vi, n, m)
+        assert np.array_equal(direct.left_matvec_i64(rp, c, vi, yi, m), direct.matvec_i64(trp2, tc2, tv2, yi))
+        yb = g.integers(0, 2**63, n, dtype=np.uint64)
+        assert np.array_equal(direct.left_matvec_or(rp, c, yb, m), direct.matvec_or(trp, tc, yb))
+        yf = (g.standard_normal(n) * 10.0 ** g.uniform(-4, 4, n)).astype(np.float32)
+        assert np.array_equal(direct.left_matvec_minplus(rp, c, v, yf, m).view(np.uint32),
+                              direct.matvec_minplus(trp, tc, tv, yf).view(np.uint32))
+
+
+def test_left_boolean_and_minplus_brute_force():
+    for seed, rp, c, v, dense in _minplus_cases():
+        n, m = dense.shape
+        nz = dense != 0
+        g = np.random.default_rng(seed + 41)
+        yb = g.integers(0, 2**63, n, dtype=np.uint64)
+        want = np.zeros(m, np.uint64)
+        yf = g.standard_normal(n).astype(np.float32)
+        wantf = np.full(m, np.inf, np.float32)
+        for i in range(n):
+            for j in range(m):
+                if nz[i, j]:
+                    want[j] |= yb[i]
+                    wantf[j] = min(wantf[j], np.float32(dense[i, j]) + yf[i])
+        assert np.array_equal(direct.left_matvec_or(rp, c, yb, m), want)
+        assert np.array_equal(direct.left_matvec_minplus(rp, c, v, yf, m), wantf)
