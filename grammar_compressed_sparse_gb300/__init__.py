@@ -179,26 +179,34 @@ class Engine:
 
 
 class LeftEngine:
-    """The left product x = M^T y of a grammar resident on a CUDA device
-    (float32, one right-hand side; gc_left_* of the C ABI). The arena is one
-    torch uint8 tensor; the library allocates no device memory itself."""
+    """The left product x = M^T y of a grammar resident on a CUDA device (one
+    right-hand side; gc_left_* of the C ABI), under the policy "f32", "i64",
+    "or" or "minplus". The arena is one torch uint8 tensor; the library
+    allocates no device memory itself."""
 
-    def __init__(self, grammar: Grammar, device="cuda", stream=None):
+    def __init__(self, grammar: Grammar, policy="f32", device="cuda", stream=None):
         import torch
 
         st = grammar.stats()
         self.n, self.m = st["n"], st["m"]
-        self.layout = _capi().gc_left_layout(grammar._p)
+        self.policy = policy
+        self.layout = _capi().gc_left_layout(grammar._p, policy)
         self.device = torch.device(device)
         self.arena = torch.empty(max(self.layout["arena_bytes"], 256), dtype=torch.uint8, device=self.device)
         self._stream = stream if stream is not None else torch.cuda.current_stream(self.device)
-        self._h = _capi().gc_left_upload(grammar._p, self.arena, self.arena.numel(), self._stream)
+        self._h = _capi().gc_left_upload(grammar._p, policy, self.arena, self.arena.numel(), self._stream)
+
+    @property
+    def dtype(self):
+        import torch
+        return {"f32": torch.float32, "i64": torch.int64, "or": torch.int64, "minplus": torch.float32}[self.policy]
 
     def matvec(self, y, x=None, stream=None):
-        """x = M^T y for a device float32 tensor y of shape (n,)."""
+        """x = M^T y for a device tensor y of shape (n,) (the policy's dtype;
+        int64 bit patterns for "or")."""
         import torch
         if x is None:
-            x = torch.empty(self.m, dtype=torch.float32, device=y.device)
+            x = torch.empty(self.m, dtype=self.dtype, device=y.device)
         _capi().gc_left_matvec(self._h, y, x, stream if stream is not None else self._stream)
         return x
 

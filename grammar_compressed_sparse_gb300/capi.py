@@ -93,8 +93,8 @@ _sig = {
     "gc_builder_finish": ([_vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_builder_free": ([_vp], None),
     "gc_free_handle": ([_vp], None),
-    "gc_left_layout": ([_vp, ctypes.POINTER(ArenaLayout)], ctypes.c_int),
-    "gc_left_upload": ([_vp, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
+    "gc_left_layout": ([_vp, ctypes.c_int, ctypes.POINTER(ArenaLayout)], ctypes.c_int),
+    "gc_left_upload": ([_vp, ctypes.c_int, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_left_matvec": ([_vp, _vp, _vp, _vp], ctypes.c_int),
     "gc_left_launch_count": ([_vp, ctypes.POINTER(_i64)], ctypes.c_int),
     "gc_free_left_handle": ([_vp], None),
@@ -283,15 +283,16 @@ def gc_free_handle(h):
     _lib.gc_free_handle(h)
 
 
-def gc_left_layout(g) -> dict:
+def gc_left_layout(g, policy="f32") -> dict:
     lay = ArenaLayout()
-    _check(_lib.gc_left_layout(g, ctypes.byref(lay)), "gc_left_layout")
+    _check(_lib.gc_left_layout(g, POLICIES[policy], ctypes.byref(lay)), "gc_left_layout")
     return {f: getattr(lay, f) for f, _ in ArenaLayout._fields_}
 
 
-def gc_left_upload(g, arena, arena_bytes, stream=None) -> int:
+def gc_left_upload(g, policy, arena, arena_bytes, stream=None) -> int:
     h = _vp()
-    _check(_lib.gc_left_upload(g, _addr(arena), arena_bytes, _stream(stream), ctypes.byref(h)), "gc_left_upload")
+    _check(_lib.gc_left_upload(g, POLICIES[policy], _addr(arena), arena_bytes, _stream(stream), ctypes.byref(h)),
+           "gc_left_upload")
     return h.value
 
 

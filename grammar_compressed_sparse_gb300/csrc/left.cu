@@ -11,8 +11,14 @@
 // from its initial value (items loaded four at a time, added in order; a
 // segment too long for one lane is left to its HEAVY task); a HEAVY task sums
 // one segment over the warp (lane l takes items l, l + 32, ... in order, then
-// a fixed xor butterfly) and adds it to the initial value. Float32, each
-// addition and product rounded separately.
+// a fixed xor butterfly) and adds it to the initial value.
+//
+// Policies (Sec. 5's semirings, as for the right product): the float32 sum
+// (each addition and product rounded separately), the exact int64 sum,
+// Boolean OR on 64-bit source sets, and tropical min-plus in float32. The
+// weights are (+)-sums of y over occurrences in every policy; the column
+// step applies the leaf map: V[l] * weight, or V[l] + weight for min-plus
+// (+ distributes over min), or the weight itself for OR (every entry is 1).
 //
 // The L + 3 steps are one CUDA graph per handle, a chain of kernel nodes
 // built on the first product; later products update the two nodes that read
@@ -28,6 +34,8 @@
 #include "left.hpp"
 
 struct gc_left_handle {
+    gc_policy policy = GC_F32_SUM;
+    int64_t elem = 4;   // bytes of a value
     int64_t n = 0, m = 0, L = 0, N = 0, rho = 0, alpha = 0;
     std::vector<int64_t> lvl_off, lvl_roots, root_off, task_off;
     char* arena = nullptr;
@@ -55,30 +63,65 @@ constexpr int kLeftThreads = 256;
 
 // What one step reads and writes: segment g covers references
 // ref[off[g] .. off[g+1]) (ref == nullptr: the references are the indices
-// themselves); item i is scale(i) * src[i] (scale only for the columns).
+// themselves); item i is src[i], or leaf(V[vidx[i]], src[i]) in the column
+// step. Value arrays are untyped here; the kernel's policy gives their type.
 struct LeftStep {
     const int32_t* off;
     const int32_t* ref;
-    const float* src;
+    const void* src;
     const int32_t* vidx;   // columns: terminal -> value index, else nullptr
-    const float* V;
-    // initial value of segment g: init[g - init_base] when init_base <= g <
-    // init_base + init_count, else 0
-    const float* init;
+    const void* V;
+    // initial value of segment g: init[g - init_base + init_shift] when
+    // init_base <= g < init_base + init_count, else the identity
+    const void* init;
     int64_t init_base, init_count, init_shift;
-    float* out;            // out[g - out_base]
+    void* out;             // out[g - out_base]
     int64_t out_base;
 };
 
-__device__ __forceinline__ float left_item(const LeftStep& s, int32_t q) {
+// The combine, its identity and the column step's leaf map of each policy.
+struct LeftSum {
+    using V = float;
+    using Leaf = float;
+    __device__ __forceinline__ static V identity() { return 0.0f; }
+    __device__ __forceinline__ static V combine(V a, V b) { return __fadd_rn(a, b); }
+    __device__ __forceinline__ static V leaf(Leaf v, V w) { return __fmul_rn(v, w); }
+};
+struct LeftI64 {
+    using V = long long;
+    using Leaf = long long;
+    __device__ __forceinline__ static V identity() { return 0; }
+    __device__ __forceinline__ static V combine(V a, V b) { return a + b; }
+    __device__ __forceinline__ static V leaf(Leaf v, V w) { return v * w; }
+};
+struct LeftOr {
+    using V = unsigned long long;
+    using Leaf = unsigned long long;   // every stored entry is 1: AND with all ones
+    __device__ __forceinline__ static V identity() { return 0ull; }
+    __device__ __forceinline__ static V combine(V a, V b) { return a | b; }
+    __device__ __forceinline__ static V leaf(Leaf, V w) { return w; }
+};
+struct LeftMinPlus {
+    using V = float;
+    using Leaf = float;
+    __device__ __forceinline__ static V identity() { return __int_as_float(0x7f800000); }
+    __device__ __forceinline__ static V combine(V a, V b) { return fminf(a, b); }
+    __device__ __forceinline__ static V leaf(Leaf v, V w) { return __fadd_rn(v, w); }
+};
+
+template <class Op>
+__device__ __forceinline__ typename Op::V left_item(const LeftStep& s, int32_t q) {
+    using V = typename Op::V;
     const int32_t i = s.ref ? __ldg(s.ref + q) : q;
-    const float v = s.src[i];
-    return s.vidx ? __fmul_rn(__ldg(s.V + __ldg(s.vidx + i)), v) : v;
+    const V v = static_cast<const V*>(s.src)[i];
+    return s.vidx ? Op::leaf(__ldg(static_cast<const typename Op::Leaf*>(s.V) + __ldg(s.vidx + i)), v) : v;
 }
 
-__device__ __forceinline__ float left_init(const LeftStep& s, int32_t g) {
+template <class Op>
+__device__ __forceinline__ typename Op::V left_init(const LeftStep& s, int32_t g) {
     const int64_t r = (int64_t)g - s.init_base;
-    return (s.init && r >= 0 && r < s.init_count) ? s.init[r + s.init_shift] : 0.0f;
+    return (s.init && r >= 0 && r < s.init_count) ? static_cast<const typename Op::V*>(s.init)[r + s.init_shift]
+                                                  : Op::identity();
 }
 
 // A warp's tasks are t0 + w, t0 + w + warps, ...; the next task's header and
@@ -104,9 +147,12 @@ __device__ __forceinline__ TaskHead load_head(const LeftStep& s, const int32_t* 
     return h;
 }
 
+template <class Op>
 __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep s, const int32_t* __restrict__ task,
                                                                  int64_t t0, int64_t t1) {
+    using V = typename Op::V;
     const int lane = threadIdx.x & 31;
+    V* const out = static_cast<V*>(s.out);
     const int64_t warps = (int64_t)gridDim.x * (kLeftThreads / 32);
     int64_t t = t0 + (int64_t)blockIdx.x * (kLeftThreads / 32) + (threadIdx.x >> 5);
     TaskHead h = load_head(s, task, t, t1, lane);
@@ -117,23 +163,23 @@ __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep 
         if (c.cnt > 0) {   // LIGHT: one segment per lane
             const int32_t g = c.first + lane;
             if (lane < c.cnt && c.q1 - c.q0 <= kLeftLightMax) {
-                float acc = left_init(s, g);
+                V acc = left_init<Op>(s, g);
                 int32_t q = c.q0;
                 for (; q + 4 <= c.q1; q += 4) {
-                    const float v0 = left_item(s, q), v1 = left_item(s, q + 1), v2 = left_item(s, q + 2),
-                                v3 = left_item(s, q + 3);
-                    acc = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(acc, v0), v1), v2), v3);
+                    const V v0 = left_item<Op>(s, q), v1 = left_item<Op>(s, q + 1), v2 = left_item<Op>(s, q + 2),
+                            v3 = left_item<Op>(s, q + 3);
+                    acc = Op::combine(Op::combine(Op::combine(Op::combine(acc, v0), v1), v2), v3);
                 }
-                for (; q < c.q1; ++q) acc = __fadd_rn(acc, left_item(s, q));
-                s.out[g - s.out_base] = acc;
+                for (; q < c.q1; ++q) acc = Op::combine(acc, left_item<Op>(s, q));
+                out[g - s.out_base] = acc;
             }
         } else {           // HEAVY: one segment over the warp
             const int32_t g = c.first;
-            float acc = 0.0f;
-            for (int32_t q = c.q0 + lane; q < c.q1; q += 32) acc = __fadd_rn(acc, left_item(s, q));
+            V acc = Op::identity();
+            for (int32_t q = c.q0 + lane; q < c.q1; q += 32) acc = Op::combine(acc, left_item<Op>(s, q));
 #pragma unroll
-            for (int msk = 16; msk >= 1; msk >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, msk));
-            if (lane == 0) s.out[g - s.out_base] = __fadd_rn(left_init(s, g), acc);
+            for (int msk = 16; msk >= 1; msk >>= 1) acc = Op::combine(acc, __shfl_xor_sync(0xffffffffu, acc, msk));
+            if (lane == 0) out[g - s.out_base] = Op::combine(left_init<Op>(s, g), acc);
         }
     }
 }
@@ -143,7 +189,8 @@ void cuda_ok(cudaError_t e, const char* what) {
 }
 
 // Arena parts, 256-byte aligned: the plan's arrays (read-only), then the
-// seed sums RS, the node weights W and the terminal sums TIN.
+// seed sums RS, the node weights W and the terminal sums TIN (h.elem bytes a
+// value).
 void left_layout(const LeftPlan& p, gc_left_handle& h) {
     int64_t o = 0;
     auto take = [&](int64_t bytes) {
@@ -159,12 +206,12 @@ void left_layout(const LeftPlan& p, gc_left_handle& h) {
     h.tref = take(4 * (int64_t)p.tref.size());
     h.coff = take(4 * (int64_t)p.coff.size());
     h.vidx = take(4 * (int64_t)p.term_vidx.size());
-    h.V = take(4 * (int64_t)p.V.size());
+    h.V = take(h.elem * (int64_t)p.V.size());
     h.task = take(4 * (int64_t)p.task.size());
     h.grammar_bytes = o;
-    h.RS = take(4 * (p.rho + p.alpha));
-    h.W = take(4 * p.N);
-    h.TIN = take(4 * p.alpha);
+    h.RS = take(h.elem * (p.rho + p.alpha));
+    h.W = take(h.elem * p.N);
+    h.TIN = take(h.elem * p.alpha);
     h.total = o;
 }
 
@@ -180,7 +227,7 @@ struct StepLaunch {
 std::vector<StepLaunch> left_steps(const gc_left_handle* h, const void* y, void* x) {
     char* a = h->arena;
     auto I = [&](int64_t off) { return reinterpret_cast<const int32_t*>(a + off); };
-    auto F = [&](int64_t off) { return reinterpret_cast<float*>(a + off); };
+    auto F = [&](int64_t off) { return static_cast<void*>(a + off); };
     std::vector<StepLaunch> out;
     auto add = [&](const LeftStep& s, int64_t set) {
         const int64_t t0 = h->task_off[set], t1 = h->task_off[set + 1];
@@ -190,8 +237,7 @@ std::vector<StepLaunch> left_steps(const gc_left_handle* h, const void* y, void*
         out.push_back(StepLaunch{s, I(h->task), t0, t1, set, (unsigned)grid});
     };
     // seed: RS[s] = sum of y over C's references to s
-    add(LeftStep{I(h->soff), I(h->srow), static_cast<const float*>(y), nullptr, nullptr, nullptr, 0, 0, 0, F(h->RS), 0},
-        0);
+    add(LeftStep{I(h->soff), I(h->srow), y, nullptr, nullptr, nullptr, 0, 0, 0, F(h->RS), 0}, 0);
     // levels, top first: W[u] = RS[root slot] (roots) + sum of the parents' W
     for (int64_t k = h->L; k >= 1; --k)
         add(LeftStep{I(h->poff), I(h->pref), F(h->W), nullptr, nullptr, F(h->RS), h->lvl_off[k], h->lvl_roots[k],
@@ -201,21 +247,30 @@ std::vector<StepLaunch> left_steps(const gc_left_handle* h, const void* y, void*
     add(LeftStep{I(h->toff), I(h->tref), F(h->W), nullptr, nullptr, F(h->RS), 0, h->alpha, h->rho, F(h->TIN), 0},
         h->L + 1);
     // columns: x[j] = sum over column j's terminals of V[l] * TIN[p]
-    add(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), reinterpret_cast<const float*>(a + h->V), nullptr, 0, 0,
-                 0, static_cast<float*>(x), 0},
-        h->L + 2);
+    add(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), F(h->V), nullptr, 0, 0, 0, x, 0}, h->L + 2);
     return out;
 }
 
 // Kernel-node parameters of a step; args holds the argument pointers and
 // must live until the call that takes the parameters returns.
-cudaKernelNodeParams node_params(StepLaunch& l, void* (&args)[4]) {
+// The step kernel of a policy.
+void* step_kernel(gc_policy p) {
+    switch (p) {
+        case GC_F32_SUM: return reinterpret_cast<void*>(left_step_kernel<LeftSum>);
+        case GC_I64_SUM: return reinterpret_cast<void*>(left_step_kernel<LeftI64>);
+        case GC_BOOL_OR: return reinterpret_cast<void*>(left_step_kernel<LeftOr>);
+        case GC_F32_MIN_PLUS: return reinterpret_cast<void*>(left_step_kernel<LeftMinPlus>);
+    }
+    fail(GC_ERR_ARG, "unknown policy");
+}
+
+cudaKernelNodeParams node_params(gc_policy p, StepLaunch& l, void* (&args)[4]) {
     args[0] = &l.s;
     args[1] = &l.task;
     args[2] = &l.t0;
     args[3] = &l.t1;
     cudaKernelNodeParams kp{};
-    kp.func = reinterpret_cast<void*>(left_step_kernel);
+    kp.func = step_kernel(p);
     kp.gridDim = dim3(l.grid);
     kp.blockDim = dim3(kLeftThreads);
     kp.sharedMemBytes = 0;
@@ -237,13 +292,15 @@ using namespace gcs;
 
 extern "C" {
 
-gc_status gc_left_layout(const gc_grammar* gg, gc_arena_layout* out) {
+gc_status gc_left_layout(const gc_grammar* gg, gc_policy policy, gc_arena_layout* out) {
     return guard([&] {
         if (!gg || !out) fail(GC_ERR_ARG, "null argument");
         const Grammar& g = gg->g;
+        check_policy(g, policy, 1);
         validate_packed(g);
         const LeftPlan p = plan_left(g);
         gc_left_handle h;
+        h.elem = policy_elem_bytes(policy);
         left_layout(p, h);
         gc_arena_layout l{};
         l.arena_bytes = h.total;
@@ -251,21 +308,25 @@ gc_status gc_left_layout(const gc_grammar* gg, gc_arena_layout* out) {
         l.scratch_bytes = h.total - h.grammar_bytes;
         l.staging_bytes = 0;
         const int64_t rp = g.nnz >= INT32_MAX ? 8 * (g.n + 1) : 4 * (g.n + 1);
-        l.csr_bytes = 8 * g.nnz + rp + 4 * (g.n + g.m);
+        l.csr_bytes = 8 * g.nnz + rp + h.elem * (g.n + g.m);
         *out = l;
     });
 }
 
-gc_status gc_left_upload(const gc_grammar* gg, void* arena, int64_t arena_bytes, void* stream, gc_left_handle** out) {
+gc_status gc_left_upload(const gc_grammar* gg, gc_policy policy, void* arena, int64_t arena_bytes, void* stream,
+                         gc_left_handle** out) {
     return guard([&] {
         if (!gg || !out) fail(GC_ERR_ARG, "null grammar or output pointer");
         if (!arena) fail(GC_ERR_ARG, "null arena");
         if (reinterpret_cast<uintptr_t>(arena) % 256 != 0) fail(GC_ERR_ARG, "arena must be 256-byte aligned");
         const Grammar& g = gg->g;
+        check_policy(g, policy, 1);
         validate_packed(g);
         const LeftPlan p = plan_left(g);
         validate_left_plan(p);
         auto h = std::make_unique<gc_left_handle>();
+        h->policy = policy;
+        h->elem = policy_elem_bytes(policy);
         left_layout(p, *h);
         if (arena_bytes < h->total) fail(GC_ERR_ARG, "arena smaller than gc_left_layout().arena_bytes");
         h->n = p.n;
@@ -292,7 +353,13 @@ gc_status gc_left_upload(const gc_grammar* gg, void* arena, int64_t arena_bytes,
         put(st, a, h->tref, p.tref);
         put(st, a, h->coff, p.coff);
         put(st, a, h->vidx, p.term_vidx);
-        put(st, a, h->V, p.V);
+        if (policy_is_f32(policy)) {
+            put(st, a, h->V, p.V);
+        } else {   // exact integers, or all-ones masks for OR
+            std::vector<long long> v(p.V.size());
+            for (size_t i = 0; i < v.size(); ++i) v[i] = policy == GC_BOOL_OR ? ~0ll : (long long)p.V[i];
+            put(st, a, h->V, v);
+        }
         put(st, a, h->task, p.task);
         cuda_ok(cudaStreamSynchronize(st), "left upload synchronize");
         *out = h.release();
@@ -314,7 +381,7 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
             cuda_ok(cudaGraphCreate(&h->graph, 0), "left graph create");
             for (StepLaunch& l : steps) {
                 void* args[4];
-                const cudaKernelNodeParams kp = node_params(l, args);
+                const cudaKernelNodeParams kp = node_params(h->policy, l, args);
                 cudaGraphNode_t node = nullptr;
                 const cudaGraphNode_t* dep = h->nodes.empty() ? nullptr : &h->nodes.back();
                 cuda_ok(cudaGraphAddKernelNode(&node, h->graph, dep, dep ? 1 : 0, &kp), "left graph node");
@@ -328,7 +395,7 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
                 if (steps[i].set == 0 || steps[i].set == h->L + 2) {
                     if (h->node_set[i] != steps[i].set) fail(GC_ERR_ARG, "left graph does not match its steps");
                     void* args[4];
-                    const cudaKernelNodeParams kp = node_params(steps[i], args);
+                    const cudaKernelNodeParams kp = node_params(h->policy, steps[i], args);
                     cuda_ok(cudaGraphExecKernelNodeSetParams(h->exec, h->nodes[i], &kp), "left graph update");
                 }
         }

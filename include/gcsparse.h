@@ -339,20 +339,26 @@ gc_status gc_debug_inject(gc_handle* h, int32_t what, int64_t timeout_cycles);
 gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void* stream);
 
 /*
- * Left product x^T = y^T M, i.e. x = M^T y, in float32 (one right-hand side):
- * the dual of gc_matvec over the same grammar. The pages name left
+ * Left product x^T = y^T M, i.e. x = M^T y (one right-hand side): the dual
+ * of gc_matvec over the same grammar, under the same policies at k = 1:
+ * GC_F32_SUM (float32), GC_I64_SUM (exact), GC_BOOL_OR (x[j] = OR of y[i]
+ * over the entries (i, j): one forward step of a frontier) and
+ * GC_F32_MIN_PLUS (x[j] = min of M[i][j] + y[i], float32, +inf for an
+ * unused column: one forward Bellman-Ford relaxation). The pages name left
  * multiplication by pull-based reduction as future work (Sec. 8); here it is
  * a top-down sweep over the properly layered grammar in which every value is
  * a sum its reader gathers, in a fixed order (no atomics):
- *   RS[s]  = sum of y[r] over row r's references to s in C (root slots and
+ *   RS[s]  = (+) of y[r] over row r's references to s in C (root slots and
  *            terminals),
- *   W[u]   = RS[u's slot] (roots) + sum of W over u's parents, level L first
+ *   W[u]   = RS[u's slot] (roots) (+) the W of u's parents, level L first
  *            (every parent of a level-k node is at level k + 1, Def. 3.2),
- *   x[j]   = sum over the terminals <l, j> of V[l] * (RS + sum of W over the
- *            nodes naming the terminal).
+ *   x[j]   = (+) over the terminals <l, j> of V[l] (x) (RS (+) the W of the
+ *            nodes naming the terminal),
+ * with (+) the policy's combine (sum, OR or min) and (x) its leaf map.
  * Long sums run over a warp with a fixed butterfly, so each is at most about
  * 64 + count / 32 + 5 additions deep. Deterministic: the same y gives the
- * same x bit for bit.
+ * same x bit for bit. Values: float, int64_t, uint64_t or float, by policy;
+ * the policy's value checks are those of gc_layout (GC_ERR_UNSUPPORTED).
  *
  * gc_left_layout -- device bytes a left handle needs (grammar_bytes: the
  *   parent, seed and column lists and the task tables; scratch_bytes: RS, W
@@ -363,8 +369,9 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
  *   task), then copies it into a caller-owned arena (device, 256-byte
  *   aligned, at least arena_bytes, outliving the handle), enqueued on stream,
  *   and synchronises the stream. The grammar may be freed afterwards.
- * gc_left_matvec -- x = M^T y, asynchronous on stream: y device float[n], x
- *   device float[m], fully written (a column no row uses gets 0). The L + 3
+ * gc_left_matvec -- x = M^T y, asynchronous on stream: y device [n], x
+ *   device [m] of the policy's type, fully written (a column no row uses gets
+ *   the identity: 0, or +inf for GC_F32_MIN_PLUS). The L + 3
  *   steps (fewer when a step has nothing to sum) run as one CUDA graph of the
  *   handle, a chain of kernel nodes built by the first call; a call with new
  *   y or x pointers updates the two nodes that use them. One product at a
@@ -373,8 +380,8 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
  * gc_left_launch_count -- kernels the last gc_left_matvec ran.
  * gc_free_left_handle -- host object and its graph; not the arena.
  */
-gc_status gc_left_layout(const gc_grammar* g, gc_arena_layout* out);
-gc_status gc_left_upload(const gc_grammar* g, void* arena, int64_t arena_bytes, void* stream,
+gc_status gc_left_layout(const gc_grammar* g, gc_policy policy, gc_arena_layout* out);
+gc_status gc_left_upload(const gc_grammar* g, gc_policy policy, void* arena, int64_t arena_bytes, void* stream,
                          gc_left_handle** out);
 gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream);
 gc_status gc_left_launch_count(const gc_left_handle* h, int64_t* launches);

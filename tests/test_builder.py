@@ -416,11 +416,17 @@ def test_left_plan_replays_to_the_transpose(gcs, tmp_path):
 def test_left_layout_sizes(gcs):
     d = gcsynth.genotype_dense(n=120, m=300, founders=5, switch=0.01, mutation=0.005, seed=4)
     G = gcs.Grammar(120, 300, *gcsynth.dense_to_csr(d))
-    lay = gcs.capi.gc_left_layout(G._p)
+    lay = gcs.capi.gc_left_layout(G._p, "f32")
     st = G.stats()
     # W holds one float per layered node; RS one per root slot and terminal
     assert lay["scratch_bytes"] >= 4 * (st["n_nodes"] + st["n_roots"] + 2 * st["n_terminals"])
     assert lay["arena_bytes"] == lay["grammar_bytes"] + lay["scratch_bytes"] and lay["staging_bytes"] == 0
+    # 8-byte policies double the scratch; OR needs a 0/1 pattern
+    lay8 = gcs.capi.gc_left_layout(G._p, "i64")
+    assert lay8["scratch_bytes"] >= 2 * lay["scratch_bytes"] - 3 * 256
+    assert gcs.capi.gc_left_layout(G._p, "minplus")["arena_bytes"] == lay["arena_bytes"]
+    with pytest.raises(gcs.GcError, match="UNSUPPORTED"):
+        gcs.capi.gc_left_layout(G._p, "or")
 
 
 def test_corrupted_grammar_file_is_rejected(gcs, tmp_path):

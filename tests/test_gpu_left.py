@@ -1,10 +1,12 @@
-"""GPU parity for the left product x = M^T y (gc_left_* through the C ABI).
+"""GPU parity for the left product x = M^T y (gc_left_* through the C ABI),
+under every policy.
 
 The pages name left multiplication by pull-based reduction as future work
 (Sec. 8). Tolerance as for the right product: |x_j - x_ref_j| <= 1e-4 *
 (|M|^T |y|)_j with x_j exactly 0 where that bound is 0, x_ref in float64
-(oracle.direct.left_matvec_f64). Determinism: the same y gives the same x
-bit for bit.
+(oracle.direct.left_matvec_f64). The exact, Boolean and tropical left
+products match the oracle bit for bit. Determinism: the same y gives the
+same x bit for bit.
 """
 import numpy as np
 import pytest
@@ -97,15 +99,17 @@ def test_edge_cases_left(gcs, torch):
 def test_left_argument_errors(gcs, torch):
     rp, c, v, _ = gcsynth.random_sparse(20, 30, 0.5, [1.0, 2.0], 0)
     G = gcs.Grammar(20, 30, rp, c, v)
-    lay = gcs.capi.gc_left_layout(G._p)
+    lay = gcs.capi.gc_left_layout(G._p, "f32")
     arena = torch.empty(lay["arena_bytes"] + 512, dtype=torch.uint8, device="cuda")
     with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
-        gcs.capi.gc_left_upload(G._p, arena.data_ptr() + 16, arena.numel() - 16)    # misaligned
+        gcs.capi.gc_left_upload(G._p, "f32", arena.data_ptr() + 16, arena.numel() - 16)    # misaligned
     with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
-        gcs.capi.gc_left_upload(G._p, arena, 256)                                   # too small
+        gcs.capi.gc_left_upload(G._p, "f32", arena, 256)                                   # too small
     eng = gcs.LeftEngine(G)
     with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
         gcs.capi.gc_left_matvec(eng._h, None, torch.zeros(30, device="cuda"))
+    with pytest.raises(gcs.GcError, match="GC_ERR_UNSUPPORTED"):
+        gcs.LeftEngine(G, "or")                        # OR needs every stored entry to be 1
 
 
 def test_left_graph_follows_new_pointers(gcs, torch):
@@ -127,3 +131,43 @@ def test_left_graph_follows_new_pointers(gcs, torch):
         eng.matvec(yd[i], xd[j])
         x = xd[j].cpu().numpy()
         assert direct.within_tolerance(x, *want[i], TOL)[0], (i, j)
+
+
+def _policy_cases():
+    rp, c, v, _ = gcsynth.random_sparse(30, 41, 0.4, [1.0, 2.0, -3.0], 3)
+    yield "rand30x41", 30, 41, rp, c, v
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    yield "geno300", 300, cfg["m"], *gcsynth.genotype_csr(**cfg)
+    N = 3000
+    grp, gcol = gcsynth.copy_model_graph(nodes=N, n0=20, d0=15, p_edit=0.05, seed=1)
+    yield "graph3000", N, N, grp, gcol, gcsynth.target_lengths(gcol, N, seed=2)
+    d = np.zeros((3000, 64), np.float32)
+    d[:, 7] = 1.0
+    d[::2, 11] = 2.0
+    yield "longlists", 3000, 64, *dense_to_csr(d, np.float32)
+
+
+POLICY_CASES = list(_policy_cases())
+
+
+@pytest.mark.parametrize("name,n,m,rp,c,v", POLICY_CASES, ids=[s[0] for s in POLICY_CASES])
+def test_left_policies_bit_exact(gcs, torch, name, n, m, rp, c, v):
+    G = gcs.Grammar(n, m, rp, c, v)
+    g = np.random.default_rng(8)
+    # tropical: float32 min-plus, +inf for unused columns
+    yf = g.standard_normal(n).astype(np.float32)
+    yf[g.random(n) < 0.2] = np.inf
+    xf = gcs.LeftEngine(G, "minplus").matvec(torch.from_numpy(yf).cuda()).cpu().numpy()
+    assert np.array_equal(xf.view(np.uint32), direct.left_matvec_minplus(rp, c, v, yf, m).view(np.uint32))
+    # exact integer sums (integer-valued matrices)
+    if np.all(np.floor(v) == v):
+        yi = g.integers(-10**6, 10**6, n)
+        xi = gcs.LeftEngine(G, "i64").matvec(torch.from_numpy(yi).cuda()).cpu().numpy()
+        assert np.array_equal(xi, direct.left_matvec_i64(rp, c, v, yi, m))
+    # Boolean OR on the 0/1 pattern: one forward step of 64 source sets
+    Gb = gcs.Grammar(n, m, rp, c, None)
+    yb = g.integers(0, 2**63, n, dtype=np.uint64)
+    eng = gcs.LeftEngine(Gb, "or")
+    xb = eng.matvec(torch.from_numpy(yb.view(np.int64)).cuda()).cpu().numpy().view(np.uint64)
+    assert np.array_equal(xb, direct.left_matvec_or(rp, c, yb, m))
+    assert np.array_equal(eng.matvec(torch.from_numpy(yb.view(np.int64)).cuda()).cpu().numpy().view(np.uint64), xb)
