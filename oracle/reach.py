@@ -1,4 +1,6 @@
-"""Boolean-semiring reachability (Sec. 5 "Beyond (+,x)").
+"""Boolean-semiring reachability and tropical shortest paths (Sec. 5 "Beyond
+(+,x)"), in both directions: with right products (towards the sources) and
+with left products (away from them).
 
 One (OR, AND) product expands a BFS frontier by one step; the pages measure a
 single pass and name the iteration to the fixpoint as the next step
@@ -20,7 +22,7 @@ from collections import deque
 
 import numpy as np
 
-from .direct import matvec_minplus, matvec_or
+from .direct import left_matvec_minplus, left_matvec_or, matvec_minplus, matvec_or
 
 
 def fixpoint(row_ptr, col, x0, max_iter=1000):
@@ -47,6 +49,36 @@ def sssp_fixpoint(row_ptr, col, val, x0, max_iter=1000):
     x = np.asarray(x0, dtype=np.float32).copy()
     for it in range(1, max_iter + 1):
         nxt = np.minimum(x, matvec_minplus(row_ptr, col, val, x))
+        if np.array_equal(nxt, x):
+            return x, it
+        x = nxt
+    raise RuntimeError("fixpoint not reached")
+
+
+def forward_fixpoint(row_ptr, col, x0, max_iter=1000):
+    """The forward direction with left products: x <- x | (M^T (x) x), i.e.
+    x[j] gains the sets of every i with an edge i -> j, until nothing changes.
+    Bit b of the fixpoint at j is set iff s_b reaches j (reflexively).
+    Returns (x, iterations) as fixpoint() does."""
+    x = np.asarray(x0, dtype=np.uint64).copy()
+    n = len(x)
+    for it in range(1, max_iter + 1):
+        nxt = x | left_matvec_or(row_ptr, col, x, n)
+        if np.array_equal(nxt, x):
+            return x, it
+        x = nxt
+    raise RuntimeError("fixpoint not reached")
+
+
+def forward_sssp_fixpoint(row_ptr, col, val, x0, max_iter=1000):
+    """Forward shortest paths with left products: x <- min(x, M^T (x) x), so
+    x[j] = min over edges i -> j of x[i] + M[i][j] at the fixpoint: the
+    distance from the nearest source (x0 = 0 there, +inf elsewhere) along
+    out-edges, float32 as sssp_fixpoint."""
+    x = np.asarray(x0, dtype=np.float32).copy()
+    n = len(x)
+    for it in range(1, max_iter + 1):
+        nxt = np.minimum(x, left_matvec_minplus(row_ptr, col, val, x, n))
         if np.array_equal(nxt, x):
             return x, it
         x = nxt

@@ -154,6 +154,12 @@ def _left_minplus_max(row_ptr, col, val, y, m):
     return x
 
 
+def _forward_uses_right_products(row_ptr, col, x0, max_iter=1000):
+    # the reverse direction: x <- x | (M (x) x)
+    return _orig_fixpoint(row_ptr, col, x0, max_iter)
+
+
+_orig_fixpoint = reach.fixpoint
 _orig_eval_w = grammar.eval_w
 _orig_eval_left = grammar.eval_left
 _orig_csrv = grammar.csrv
@@ -188,6 +194,8 @@ MUTANTS = [
      ["test_left_products_equal_right_products_of_the_transpose", "test_left_boolean_and_minplus_brute_force"]),
     ("tropical left product uses max", direct, "left_matvec_minplus", _left_minplus_max,
      ["test_left_products_equal_right_products_of_the_transpose", "test_left_boolean_and_minplus_brute_force"]),
+    ("forward fixpoint runs towards the sources", reach, "forward_fixpoint", _forward_uses_right_products,
+     ["test_forward_fixpoints_match_scipy"]),
     ("shortest-path fixpoint drops min(x, .)", reach, "sssp_fixpoint", _sssp_without_keeping_x,
      ["test_sssp_matches_scipy_dijkstra", "test_sssp_iterations_on_a_path"]),
 ]

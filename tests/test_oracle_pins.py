@@ -468,3 +468,37 @@ def test_left_boolean_and_minplus_brute_force():
                     wantf[j] = min(wantf[j], np.float32(dense[i, j]) + yf[i])
         assert np.array_equal(direct.left_matvec_or(rp, c, yb, m), want)
         assert np.array_equal(direct.left_matvec_minplus(rp, c, v, yf, m), wantf)
+
+
+def test_forward_fixpoints_match_scipy():
+    # left-product fixpoints run along out-edges from the sources: scipy's
+    # BFS and Dijkstra on the graph itself (not its transpose)
+    for seed in range(5):
+        n = 70
+        rp, col, w = _weighted_graph(n, 3, seed)
+        srcs = np.random.default_rng(seed + 9).choice(n, 5, replace=False)
+        A = sp.csr_matrix((w.astype(np.float64), col, rp), shape=(n, n))
+        want = np.zeros(n, dtype=np.uint64)
+        for b, s in enumerate(srcs):
+            nodes = breadth_first_order(A, int(s), directed=True, return_predecessors=False)
+            want[nodes] |= np.uint64(1) << np.uint64(b)
+        xs, _ = reach.forward_fixpoint(rp, col, gcsynth.frontier(n, srcs))
+        assert np.array_equal(xs, want)
+        d0 = np.full(n, np.inf, np.float32)
+        d0[srcs] = 0.0
+        ds, _ = reach.forward_sssp_fixpoint(rp, col, w, d0)
+        assert np.array_equal(ds.astype(np.float64), dijkstra(A, directed=True, indices=srcs, min_only=True))
+
+
+def test_forward_iterations_on_a_path():
+    # 0 -> 1 -> ... -> n-1 from source 0: n-1 products reach n-1, one more changes nothing
+    n = 9
+    rp = np.concatenate([np.arange(n, dtype=np.int64), [n - 1]])
+    col = np.arange(1, n, dtype=np.int32)
+    xs, iters = reach.forward_fixpoint(rp, col, gcsynth.frontier(n, np.array([0])))
+    assert iters == n and np.all(xs == 1)
+    w = np.arange(1, n, dtype=np.float32)
+    d0 = np.full(n, np.inf, np.float32)
+    d0[0] = 0.0
+    ds, iters = reach.forward_sssp_fixpoint(rp, col, w, d0)
+    assert iters == n and np.array_equal(ds, np.concatenate([[0], np.cumsum(w)]).astype(np.float32))
