@@ -210,6 +210,23 @@ class LeftEngine:
         _capi().gc_left_matvec(self._h, y, x, stream if stream is not None else self._stream)
         return x
 
+    def reach(self, x0, max_iter=1000, stream=None):
+        """Forward Boolean fixpoint (policy "or") from an int64/uint64 bitset
+        tensor: what the sources reach; returns (x, iterations, status)."""
+        return self._fixpoint(_capi().gc_left_reach, x0, max_iter, stream)
+
+    def sssp(self, x0, max_iter=1000, stream=None):
+        """Forward tropical fixpoint (policy "minplus") from float32 distances
+        (0 at the sources, +inf elsewhere); returns (x, iterations, status)."""
+        return self._fixpoint(_capi().gc_left_sssp, x0, max_iter, stream)
+
+    def _fixpoint(self, fn, x0, max_iter, stream):
+        import torch
+        x = torch.empty_like(x0)
+        iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
+        rc = fn(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        return x, int(iters.item()), rc
+
     def launch_count(self) -> int:
         return _capi().gc_left_launch_count(self._h)
 

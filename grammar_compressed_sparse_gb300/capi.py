@@ -97,6 +97,8 @@ _sig = {
     "gc_left_upload": ([_vp, ctypes.c_int, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_left_matvec": ([_vp, _vp, _vp, _vp], ctypes.c_int),
     "gc_left_launch_count": ([_vp, ctypes.POINTER(_i64)], ctypes.c_int),
+    "gc_left_reach": ([_vp, _vp, _vp, _i32, _vp, _vp], ctypes.c_int),
+    "gc_left_sssp": ([_vp, _vp, _vp, _i32, _vp, _vp], ctypes.c_int),
     "gc_free_left_handle": ([_vp], None),
 }
 for _name, (_args, _res) in _sig.items():
@@ -304,6 +306,22 @@ def gc_left_launch_count(h) -> int:
     v = _i64()
     _check(_lib.gc_left_launch_count(h, ctypes.byref(v)), "gc_left_launch_count")
     return v.value
+
+
+def gc_left_reach(h, x0, x, max_iter, iters, stream=None) -> int:
+    """Returns the status (GC_OK or GC_ERR_NOT_CONVERGED); raises on anything else."""
+    rc = _lib.gc_left_reach(h, _addr(x0), _addr(x), max_iter, _addr(iters), _stream(stream))
+    if rc not in (GC_OK, GC_ERR_NOT_CONVERGED):
+        raise GcError(rc, "gc_left_reach")
+    return rc
+
+
+def gc_left_sssp(h, x0, x, max_iter, iters, stream=None) -> int:
+    """Returns the status (GC_OK or GC_ERR_NOT_CONVERGED); raises on anything else."""
+    rc = _lib.gc_left_sssp(h, _addr(x0), _addr(x), max_iter, _addr(iters), _stream(stream))
+    if rc not in (GC_OK, GC_ERR_NOT_CONVERGED):
+        raise GcError(rc, "gc_left_sssp")
+    return rc
 
 
 def gc_free_left_handle(h):

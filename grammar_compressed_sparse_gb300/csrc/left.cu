@@ -42,7 +42,7 @@ struct gc_left_handle {
     int sms = 1;
     int64_t launches = 0;
     // arena offsets
-    int64_t soff, srow, poff, pref, toff, tref, coff, vidx, V, task, RS, W, TIN, total, grammar_bytes;
+    int64_t soff, srow, poff, pref, toff, tref, coff, vidx, V, task, RS, W, TIN, tmp, flag, total, grammar_bytes;
     // the steps as a graph: its kernel nodes and the step set of each
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -184,6 +184,23 @@ __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep 
     }
 }
 
+// x = x (+) t elementwise (OR, or min); sets *changed if any element changed
+// (one step of a forward fixpoint).
+template <class Op>
+__global__ void __launch_bounds__(kLeftThreads)
+left_update_kernel(typename Op::V* __restrict__ x, const typename Op::V* __restrict__ t, int64_t n,
+                   int32_t* __restrict__ changed) {
+    int ch = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const typename Op::V u = x[i], v = Op::combine(u, t[i]);
+        if (v != u) {
+            x[i] = v;
+            ch = 1;
+        }
+    }
+    if (__syncthreads_or(ch) && threadIdx.x == 0) *changed = 1;
+}
+
 void cuda_ok(cudaError_t e, const char* what) {
     if (e != cudaSuccess) fail(GC_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
@@ -212,6 +229,8 @@ void left_layout(const LeftPlan& p, gc_left_handle& h) {
     h.RS = take(h.elem * (p.rho + p.alpha));
     h.W = take(h.elem * p.N);
     h.TIN = take(h.elem * p.alpha);
+    h.tmp = take(h.elem * p.m);   // the fixpoints' M^T x
+    h.flag = take(256);           // the fixpoints' changed flag
     h.total = o;
 }
 
@@ -283,6 +302,82 @@ template <class T>
 void put(cudaStream_t st, char* arena, int64_t off, const std::vector<T>& v) {
     if (v.empty()) return;
     cuda_ok(cudaMemcpyAsync(arena + off, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice, st), "left upload copy");
+}
+
+// One left product on stream st: the handle's graph, built on the first
+// call; a call with other y or x pointers updates the seed and column nodes.
+void left_run(gc_left_handle* h, const void* y, void* x, cudaStream_t st) {
+    std::vector<StepLaunch> steps = left_steps(h, y, x);
+    if (steps.empty()) {
+        h->launches = 0;
+        return;
+    }
+    if (!h->exec) {
+        // first product: the chain of kernel nodes, in step order
+        cuda_ok(cudaGraphCreate(&h->graph, 0), "left graph create");
+        for (StepLaunch& l : steps) {
+            void* args[4];
+            const cudaKernelNodeParams kp = node_params(h->policy, l, args);
+            cudaGraphNode_t node = nullptr;
+            const cudaGraphNode_t* dep = h->nodes.empty() ? nullptr : &h->nodes.back();
+            cuda_ok(cudaGraphAddKernelNode(&node, h->graph, dep, dep ? 1 : 0, &kp), "left graph node");
+            h->nodes.push_back(node);
+            h->node_set.push_back(l.set);
+        }
+        cuda_ok(cudaGraphInstantiate(&h->exec, h->graph, 0), "left graph instantiate");
+    } else if (y != h->y_last || x != h->x_last) {
+        // new y or x: the seed and column nodes take the new pointers
+        for (size_t i = 0; i < steps.size(); ++i)
+            if (steps[i].set == 0 || steps[i].set == h->L + 2) {
+                if (h->node_set[i] != steps[i].set) fail(GC_ERR_ARG, "left graph does not match its steps");
+                void* args[4];
+                const cudaKernelNodeParams kp = node_params(h->policy, steps[i], args);
+                cuda_ok(cudaGraphExecKernelNodeSetParams(h->exec, h->nodes[i], &kp), "left graph update");
+            }
+    }
+    h->y_last = y;
+    h->x_last = x;
+    cuda_ok(cudaGraphLaunch(h->exec, st), "left graph launch");
+    h->launches = (int64_t)steps.size();
+}
+
+// x <- x (+) (M^T x) from x0 until nothing changes, at most max_iter products;
+// M^T x goes to the arena's tmp. Writes the product count (or -1) to iters
+// on the device; false if max_iter was reached first.
+template <class Op>
+bool left_fixpoint(gc_left_handle* h, const typename Op::V* x0, typename Op::V* x, int32_t max_iter, int32_t* iters,
+                   cudaStream_t st) {
+    using V = typename Op::V;
+    const int64_t n = h->n;
+    V* t = reinterpret_cast<V*>(h->arena + h->tmp);
+    int32_t* changed = reinterpret_cast<int32_t*>(h->arena + h->flag);
+    if (x != x0 && n > 0) cuda_ok(cudaMemcpyAsync(x, x0, n * sizeof(V), cudaMemcpyDeviceToDevice, st), "x0 copy");
+    int32_t it = 0, done = 0;
+    int64_t launches = 0;
+    while (it < max_iter) {
+        ++it;
+        cuda_ok(cudaMemsetAsync(changed, 0, 4, st), "flag clear");
+        left_run(h, x, t, st);
+        launches += h->launches;
+        if (n > 0) {
+            const int64_t grid = std::min<int64_t>((n + kLeftThreads - 1) / kLeftThreads, (int64_t)h->sms * 8);
+            left_update_kernel<Op><<<(unsigned)std::max<int64_t>(grid, 1), kLeftThreads, 0, st>>>(x, t, n, changed);
+            ++launches;
+        }
+        cuda_ok(cudaGetLastError(), "kernel launch");
+        int32_t c = 0;
+        cuda_ok(cudaMemcpyAsync(&c, changed, 4, cudaMemcpyDeviceToHost, st), "flag read");
+        cuda_ok(cudaStreamSynchronize(st), "stream synchronize");
+        if (!c) {
+            done = 1;
+            break;
+        }
+    }
+    h->launches = launches;
+    const int32_t result = done ? it : -1;
+    cuda_ok(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
+    cuda_ok(cudaStreamSynchronize(st), "stream synchronize");
+    return done != 0;
 }
 
 }  // namespace
@@ -370,40 +465,42 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
     return guard([&] {
         if (!h) fail(GC_ERR_ARG, "null handle");
         if ((!y && h->n > 0) || (!x && h->m > 0)) fail(GC_ERR_ARG, "null y or x");
-        cudaStream_t st = static_cast<cudaStream_t>(stream);
-        std::vector<StepLaunch> steps = left_steps(h, y, x);
-        if (steps.empty()) {
-            h->launches = 0;
-            return;
-        }
-        if (!h->exec) {
-            // first product: the chain of kernel nodes, in step order
-            cuda_ok(cudaGraphCreate(&h->graph, 0), "left graph create");
-            for (StepLaunch& l : steps) {
-                void* args[4];
-                const cudaKernelNodeParams kp = node_params(h->policy, l, args);
-                cudaGraphNode_t node = nullptr;
-                const cudaGraphNode_t* dep = h->nodes.empty() ? nullptr : &h->nodes.back();
-                cuda_ok(cudaGraphAddKernelNode(&node, h->graph, dep, dep ? 1 : 0, &kp), "left graph node");
-                h->nodes.push_back(node);
-                h->node_set.push_back(l.set);
-            }
-            cuda_ok(cudaGraphInstantiate(&h->exec, h->graph, 0), "left graph instantiate");
-        } else if (y != h->y_last || x != h->x_last) {
-            // new y or x: the seed and column nodes take the new pointers
-            for (size_t i = 0; i < steps.size(); ++i)
-                if (steps[i].set == 0 || steps[i].set == h->L + 2) {
-                    if (h->node_set[i] != steps[i].set) fail(GC_ERR_ARG, "left graph does not match its steps");
-                    void* args[4];
-                    const cudaKernelNodeParams kp = node_params(h->policy, steps[i], args);
-                    cuda_ok(cudaGraphExecKernelNodeSetParams(h->exec, h->nodes[i], &kp), "left graph update");
-                }
-        }
-        h->y_last = y;
-        h->x_last = x;
-        cuda_ok(cudaGraphLaunch(h->exec, st), "left graph launch");
-        h->launches = (int64_t)steps.size();
+        left_run(h, y, x, static_cast<cudaStream_t>(stream));
     });
+}
+
+gc_status gc_left_reach(gc_left_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter, int32_t* iters,
+                        void* stream) {
+    gc_status rc = GC_OK;
+    gc_status g = guard([&] {
+        if (!h || !x0 || !x || !iters) fail(GC_ERR_ARG, "null argument");
+        if (h->policy != GC_BOOL_OR) fail(GC_ERR_ARG, "gc_left_reach needs the GC_BOOL_OR policy");
+        if (h->n != h->m) fail(GC_ERR_ARG, "gc_left_reach needs a square matrix");
+        if (max_iter < 1) fail(GC_ERR_ARG, "max_iter must be >= 1");
+        if (!left_fixpoint<LeftOr>(h, reinterpret_cast<const unsigned long long*>(x0),
+                                   reinterpret_cast<unsigned long long*>(x), max_iter, iters,
+                                   static_cast<cudaStream_t>(stream)))
+            rc = GC_ERR_NOT_CONVERGED;
+    });
+    if (g != GC_OK) return g;
+    if (rc != GC_OK) set_last_error("gc_left_reach: max_iter reached before the fixpoint");
+    return rc;
+}
+
+gc_status gc_left_sssp(gc_left_handle* h, const float* x0, float* x, int32_t max_iter, int32_t* iters,
+                       void* stream) {
+    gc_status rc = GC_OK;
+    gc_status g = guard([&] {
+        if (!h || !x0 || !x || !iters) fail(GC_ERR_ARG, "null argument");
+        if (h->policy != GC_F32_MIN_PLUS) fail(GC_ERR_ARG, "gc_left_sssp needs the GC_F32_MIN_PLUS policy");
+        if (h->n != h->m) fail(GC_ERR_ARG, "gc_left_sssp needs a square matrix");
+        if (max_iter < 1) fail(GC_ERR_ARG, "max_iter must be >= 1");
+        if (!left_fixpoint<LeftMinPlus>(h, x0, x, max_iter, iters, static_cast<cudaStream_t>(stream)))
+            rc = GC_ERR_NOT_CONVERGED;
+    });
+    if (g != GC_OK) return g;
+    if (rc != GC_OK) set_last_error("gc_left_sssp: max_iter reached before the fixpoint");
+    return rc;
 }
 
 gc_status gc_left_launch_count(const gc_left_handle* h, int64_t* launches) {

@@ -361,8 +361,8 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
  * the policy's value checks are those of gc_layout (GC_ERR_UNSUPPORTED).
  *
  * gc_left_layout -- device bytes a left handle needs (grammar_bytes: the
- *   parent, seed and column lists and the task tables; scratch_bytes: RS, W
- *   and the terminal sums; staging_bytes 0; csr_bytes as in gc_layout for
+ *   parent, seed and column lists and the task tables; scratch_bytes: RS, W,
+ *   the terminal sums and the fixpoints' buffer and flag; staging_bytes 0; csr_bytes as in gc_layout for
  *   k = 1). Builds the plan on the host to size it.
  * gc_left_upload -- builds and checks the plan on the host (every reference
  *   within its list, every parent one level up, every segment in exactly one
@@ -384,6 +384,24 @@ gc_status gc_left_layout(const gc_grammar* g, gc_policy policy, gc_arena_layout*
 gc_status gc_left_upload(const gc_grammar* g, gc_policy policy, void* arena, int64_t arena_bytes, void* stream,
                          gc_left_handle** out);
 gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream);
+/*
+ * gc_left_reach / gc_left_sssp -- the forward fixpoints with left products:
+ * x <- x OR (M^T (x) x) (GC_BOOL_OR; bit b of x[j] ends set iff a node whose
+ * bit b is set in x0 reaches j along out-edges, reflexively) and
+ * x <- min(x, M^T (x) x) (GC_F32_MIN_PLUS; x[j] ends as the shortest path
+ * length from a node s to j plus x0[s], minimised over s, float32 at every
+ * relaxation). The reverse direction of gc_reach / gc_sssp (Sec. 5's BFS and
+ * Bellman-Ford; the pages stop at one pass, Sec. 7 item 4). Requires n == m.
+ *   x0, x    device uint64_t[n] / float[n]; x may equal x0 (in place).
+ *   iters    device int32_t[1]: products performed, the last of which
+ *            changed nothing; -1 if max_iter was reached first.
+ * Returns GC_ERR_NOT_CONVERGED if max_iter products did not reach the
+ * fixpoint. Synchronises the stream once per product to read the changed
+ * flag; uses the handle's graph and scratch (one call at a time per handle).
+ */
+gc_status gc_left_reach(gc_left_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter, int32_t* iters,
+                        void* stream);
+gc_status gc_left_sssp(gc_left_handle* h, const float* x0, float* x, int32_t max_iter, int32_t* iters, void* stream);
 gc_status gc_left_launch_count(const gc_left_handle* h, int64_t* launches);
 void gc_free_left_handle(gc_left_handle* h);
 

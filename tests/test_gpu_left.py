@@ -171,3 +171,47 @@ def test_left_policies_bit_exact(gcs, torch, name, n, m, rp, c, v):
     xb = eng.matvec(torch.from_numpy(yb.view(np.int64)).cuda()).cpu().numpy().view(np.uint64)
     assert np.array_equal(xb, direct.left_matvec_or(rp, c, yb, m))
     assert np.array_equal(eng.matvec(torch.from_numpy(yb.view(np.int64)).cuda()).cpu().numpy().view(np.uint64), xb)
+
+
+def test_forward_fixpoints(gcs, torch):
+    # reachability from the sources and distances from them, by left
+    # products, against the oracle and scipy's BFS / Dijkstra on the graph
+    scipy_sparse = pytest.importorskip("scipy.sparse")
+    from scipy.sparse.csgraph import breadth_first_order, dijkstra
+    from oracle import reach
+    N = 3000
+    rp, col = gcsynth.copy_model_graph(nodes=N, n0=20, d0=15, p_edit=0.05, seed=1)
+    w = gcsynth.target_lengths(col, N, seed=2)
+    srcs = gcsynth.sources(N, 64, seed=0)
+    A = scipy_sparse.csr_matrix((w.astype(np.float64), col, rp), shape=(N, N))
+    # Boolean: 64 source sets at once
+    eng = gcs.LeftEngine(gcs.Grammar(N, N, rp, col, None), "or")
+    x0 = gcsynth.frontier(N, srcs)
+    xs, iters, rc = eng.reach(torch.from_numpy(x0.view(np.int64)).cuda())
+    assert rc == 0
+    want, want_iters = reach.forward_fixpoint(rp, col, x0)
+    assert iters == want_iters
+    got = xs.cpu().numpy().view(np.uint64)
+    assert np.array_equal(got, want)
+    for b in (0, 17, 63):
+        nodes = breadth_first_order(A, int(srcs[b]), directed=True, return_predecessors=False)
+        assert np.array_equal(np.nonzero((got >> np.uint64(b)) & np.uint64(1))[0], np.sort(nodes))
+    _, it1, rc1 = eng.reach(torch.from_numpy(x0.view(np.int64)).cuda(), max_iter=1)
+    assert rc1 == gcs.capi.GC_ERR_NOT_CONVERGED and it1 == -1
+    # tropical: distances from the nearest of 8 sources
+    engm = gcs.LeftEngine(gcs.Grammar(N, N, rp, col, w), "minplus")
+    d0 = gcsynth.frontier_distances(N, srcs[:8])
+    ds, diters, drc = engm.sssp(torch.from_numpy(d0).cuda())
+    assert drc == 0
+    dwant, dwant_iters = reach.forward_sssp_fixpoint(rp, col, w, d0)
+    assert diters == dwant_iters
+    dgot = ds.cpu().numpy()
+    assert np.array_equal(dgot.view(np.uint32), dwant.view(np.uint32))
+    np.testing.assert_array_equal(dgot.astype(np.float64), dijkstra(A, directed=True, indices=srcs[:8], min_only=True))
+    # in place, and the wrong policy refused
+    xin = torch.from_numpy(d0).cuda()
+    it = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert gcs.capi.gc_left_sssp(engm._h, xin, xin, 1000, it) == 0
+    assert np.array_equal(xin.cpu().numpy().view(np.uint32), dwant.view(np.uint32))
+    with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
+        gcs.capi.gc_left_reach(engm._h, xin, xin, 10, it)
