@@ -51,7 +51,8 @@ typedef enum {
 } gc_status;
 
 /* Leaf / combine / emit policy of the sweep (Sec. 5: any monoid homomorphism).
- *   GC_F32_SUM       (+, x) in float32; k = 1 or k = 16 right-hand sides
+ *   GC_F32_SUM       (+, x) in float32; k = 1, 4, 8, 16, 32, 64, 128 or 256
+ *                    right-hand sides (Appendix A's batched product)
  *   GC_I64_SUM       (+, x) in exact int64; matrix values must be integers; k = 1
  *   GC_BOOL_OR       (OR, AND) on uint64 bitsets (64 sources per word); every
  *                    stored entry must be 1 (an edge); k = 1
@@ -188,8 +189,9 @@ gc_status gc_export(const gc_grammar* g, gc_array which, void* dst, int64_t dst_
 
 /*
  * gc_layout -- device bytes needed to serve products under a policy with up
- * to k_max right-hand sides (k_max = 1 or 16 for GC_F32_SUM and
- * GC_F32_MIN_PLUS, 1 otherwise).
+ * to k_max right-hand sides (k_max one of GC_F32_SUM's widths above, 1 or 16
+ * for GC_F32_MIN_PLUS, 1 otherwise). The level buffers hold k_max values a
+ * node, so the scratch grows with k_max.
  * GC_ERR_UNSUPPORTED if the grammar's values do not fit the policy (non-
  * integer values for GC_I64_SUM, values other than 1 for GC_BOOL_OR).
  */
@@ -221,8 +223,9 @@ gc_status gc_upload(const gc_grammar* g, gc_policy policy, int32_t k_max, void* 
  *   y   device, n*k elements, row-major, same element type; fully written
  *       (a row with no non-zeros gets the combine identity: 0, or +inf for
  *       GC_F32_MIN_PLUS)
- *   k   1, or 16 with GC_F32_SUM / GC_F32_MIN_PLUS when the handle was
- *       uploaded with k_max 16
+ *   k   a width the policy supports, at most the handle's k_max (a k_max = 64
+ *       handle also serves k = 1, 4, 8, 16, 32); x and y hold k values per
+ *       column / row (4k bytes: k / 4 float4 lanes)
  * x and y must not overlap the arena. Deterministic: the same x gives the same
  * y bit for bit (fixed summation order, no atomics).
  */
