@@ -291,6 +291,23 @@ def cpu_oracle_rates(workload, seconds, steps=1):
     return [(r["rows"] / n) / r["seconds"] for r in recs], recs
 
 
+def grammar_sweep_rates(G, gen, seconds):
+    """Theorem 2.3's W-array sweep over the same grammar on the host cores
+    (oracle/wsweep.c, float64), sequential and on every core the process may
+    use: the CPU grammar baseline, reported beside the oracle."""
+    from oracle.wsweep import GrammarSweep
+    t0 = time.perf_counter()
+    sw = GrammarSweep.from_grammar(G)
+    prep = time.perf_counter() - t0
+    x = gcsynth.beta(gen["m"], seed=0).astype(np.float64)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    seq = sw.rate(x, 1, seconds / 2)
+    par = sw.rate(x, cores, seconds / 2)
+    return {"kind": "grammar sweep (Theorem 2.3 W-array over the same grammar, float64, C + OpenMP)",
+            "unit": "matvec/s", "sequential": seq, "parallel": par, "cores": cores,
+            "prepare_seconds": round(prep, 2)}
+
+
 def oracle_sample_text(workload):
     wl = WORKLOADS[workload]
     minplus = wl.get("policy") == "minplus"
@@ -568,6 +585,14 @@ def run_ours(args):
                "sample": f"{recs[0]['rows']} rows ({recs[0]['rows'] / gen['n']:.3f} products) of the same "
                          f"matrix in {recs[0]['seconds']:.1f} s: {oracle_sample_text(args.workload)}, "
                          "one BLAS thread"}
+    # the CPU grammar sweep (genotype workloads, float32 sum, one vector);
+    # reported only, and never allowed to cost the line
+    cpu_sweep = None
+    if not args.no_cpu_baseline and not graph and not left and policy == "f32" and k == 1:
+        try:
+            cpu_sweep = grammar_sweep_rates(G, gen, max(2.0, args.cpu_seconds / 2))
+        except Exception as e:  # noqa: BLE001
+            cpu_sweep = {"error": f"{type(e).__name__}: {e}"[:200]}
     line = {
         "metric": METRIC, "value": value, "unit": "matvec/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
@@ -586,6 +611,7 @@ def run_ours(args):
                      "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": bytes_step},
         "cpu_baseline": cpu,
+        "cpu_grammar_sweep": cpu_sweep,
         "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": elem * k * n_in,
                 "d2h_bytes_per_step": elem * k * n_out},
         "vectors_per_s": value * k,

@@ -455,3 +455,18 @@ def test_corrupted_grammar_file_is_rejected(gcs, tmp_path):
     open(q, "wb").write(bytes(raw2))
     with pytest.raises(gcs.GcError, match="GC_ERR_IO"):
         gcs.Grammar.load(q)
+
+
+def test_cpu_grammar_sweep_on_the_builders_grammar(gcs):
+    # the CPU baseline's W-array sweep reads the library's exported raw
+    # grammar: it must give the direct product
+    from oracle.wsweep import GrammarSweep
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    G = gcs.Grammar(300, cfg["m"], rp, c, v)
+    sw = GrammarSweep.from_grammar(G)
+    x = gcsynth.beta(cfg["m"], seed=2).astype(np.float64)
+    y_ref, b = direct.matvec_f64(rp, c, v, x)
+    y = sw(x, 1)
+    assert direct.within_tolerance(y, y_ref, b, 1e-12)[0]
+    assert np.array_equal(sw(x, 4), y)

@@ -502,3 +502,24 @@ def test_forward_iterations_on_a_path():
     d0[0] = 0.0
     ds, iters = reach.forward_sssp_fixpoint(rp, col, w, d0)
     assert iters == n and np.array_equal(ds, np.concatenate([[0], np.cumsum(w)]).astype(np.float32))
+
+
+def test_cpu_grammar_sweep_matches_dense_and_thread_counts():
+    # the C W-array sweep over the oracle's own RePair grammar (same symbol
+    # encoding as the library's export): equal to the dense product, and the
+    # same bits with any number of threads
+    from oracle.wsweep import GrammarSweep
+    for seed, rp, c, v, dense in _random_cases():
+        V, rows = grammar.csrv(rp, c, v)
+        if not len(V):
+            continue
+        g = grammar.repair(rows)
+        R = np.asarray(g["R"], dtype=np.int64).reshape(-1, 2)
+        c_off = np.concatenate([[0], np.cumsum([len(r) for r in g["C"]])])
+        c_sym = np.array([s for r in g["C"] for s in r], dtype=np.int64)
+        sw = GrammarSweep(R, grammar.levels(g["R"]) if len(R) else np.zeros(0, np.int64), c_off, c_sym,
+                          g["term_j"], g["term_l"], V)
+        x = np.random.default_rng(seed).standard_normal(dense.shape[1])
+        y1 = sw(x, 1)
+        np.testing.assert_allclose(y1, dense @ x, rtol=1e-12, atol=1e-12)
+        assert np.array_equal(sw(x, 3), y1)
