@@ -294,18 +294,23 @@ def cpu_oracle_rates(workload, seconds, steps=1):
 def grammar_sweep_rates(G, gen, seconds):
     """Theorem 2.3's W-array sweep over the same grammar on the host cores
     (oracle/wsweep.c, float64), sequential and on every core the process may
-    use: the CPU grammar baseline, reported beside the oracle."""
-    from oracle.wsweep import GrammarSweep
+    use: the CPU grammar baseline, reported beside the oracle; and the direct
+    CSR product of the same matrix the same two ways."""
+    from oracle.wsweep import CsrProduct, GrammarSweep
     t0 = time.perf_counter()
     sw = GrammarSweep.from_grammar(G)
     prep = time.perf_counter() - t0
     x = gcsynth.beta(gen["m"], seed=0).astype(np.float64)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
-    seq = sw.rate(x, 1, seconds / 2)
-    par = sw.rate(x, cores, seconds / 2)
-    return {"kind": "grammar sweep (Theorem 2.3 W-array over the same grammar, float64, C + OpenMP)",
-            "unit": "matvec/s", "sequential": seq, "parallel": par, "cores": cores,
-            "prepare_seconds": round(prep, 2)}
+    seq = sw.rate(x, 1, seconds / 4)
+    par = sw.rate(x, cores, seconds / 4)
+    out = {"kind": "grammar sweep (Theorem 2.3 W-array over the same grammar, float64, C + OpenMP)",
+           "unit": "matvec/s", "sequential": seq, "parallel": par, "cores": cores, "prepare_seconds": round(prep, 2)}
+    del sw
+    csr = CsrProduct(*make_csr(gen)[2:5])
+    out["csr"] = {"kind": "direct CSR product of the same matrix (float64, C + OpenMP)",
+                  "sequential": csr.rate(x, 1, seconds / 4), "parallel": csr.rate(x, cores, seconds / 4)}
+    return out
 
 
 def oracle_sample_text(workload):

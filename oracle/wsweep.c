@@ -51,3 +51,23 @@ int ws_sweep(int64_t n_rules, const int32_t* rule_a, const int32_t* rule_b, cons
     }
     return 0;
 }
+
+/*
+ * The same product from the uncompressed CSR matrix, float64: y[i] = sum of
+ * val[e] * x[col[e]] over row i, rows in parallel. The CSR CPU baseline
+ * (the direct product of Sec. 2, on every host core).
+ */
+int ws_csr(int64_t n, const int64_t* row_ptr, const int32_t* col, const float* val, const double* x, double* y,
+           int threads) {
+    if (threads < 1) return -1;
+#ifdef _OPENMP
+    omp_set_num_threads(threads);
+#endif
+#pragma omp parallel for schedule(dynamic, 16) if (threads > 1)
+    for (int64_t i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int64_t e = row_ptr[i]; e < row_ptr[i + 1]; ++e) acc += (double)val[e] * x[col[e]];
+        y[i] = acc;
+    }
+    return 0;
+}

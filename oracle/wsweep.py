@@ -1,5 +1,6 @@
-"""CPU grammar sweep (Theorem 2.3's W-array evaluation, ``wsweep.c``) as a
-reported CPU baseline: sequential and OpenMP over the machine's host cores.
+"""CPU baselines in C (``wsweep.c``), reported beside the GPU figures:
+Theorem 2.3's W-array grammar sweep and the direct CSR product, each
+sequential and OpenMP over the machine's host cores.
 
 TEST INFRASTRUCTURE, like the rest of this package: only tests and
 bench.py's CPU-baseline leg use it. The C source is compiled with gcc on
@@ -36,6 +37,8 @@ def _load():
     lib.ws_sweep.argtypes = [ctypes.c_int64, p, p, p, p, ctypes.c_int64, ctypes.c_int64, p, p, ctypes.c_int64, p, p, p,
                              p, p, p, p, ctypes.c_int]
     lib.ws_sweep.restype = ctypes.c_int
+    lib.ws_csr.argtypes = [ctypes.c_int64, p, p, p, p, p, ctypes.c_int]
+    lib.ws_csr.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -92,3 +95,23 @@ class GrammarSweep:
             el = time.perf_counter() - t0
             if el >= seconds:
                 return done / el
+
+
+class CsrProduct:
+    """y = M x from the uncompressed CSR (int64 row_ptr, int32 col, float32
+    val) in float64, rows in parallel: the CSR CPU baseline."""
+
+    def __init__(self, row_ptr, col, val):
+        self.rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+        self.col = np.ascontiguousarray(col, dtype=np.int32)
+        self.val = np.ascontiguousarray(val, dtype=np.float32)
+        self.n = len(self.rp) - 1
+
+    def __call__(self, x, threads=1):
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        y = np.empty(self.n, dtype=np.float64)
+        if _load().ws_csr(self.n, _ptr(self.rp), _ptr(self.col), _ptr(self.val), _ptr(x), _ptr(y), int(threads)) != 0:
+            raise ValueError("bad thread count")
+        return y
+
+    rate = GrammarSweep.rate

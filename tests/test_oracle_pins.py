@@ -523,3 +523,13 @@ def test_cpu_grammar_sweep_matches_dense_and_thread_counts():
         y1 = sw(x, 1)
         np.testing.assert_allclose(y1, dense @ x, rtol=1e-12, atol=1e-12)
         assert np.array_equal(sw(x, 3), y1)
+
+
+def test_cpu_csr_product_matches_dense():
+    from oracle.wsweep import CsrProduct
+    for seed, rp, c, v, dense in _random_cases():
+        x = np.random.default_rng(seed + 2).standard_normal(dense.shape[1])
+        p = CsrProduct(rp, c, v)
+        y = p(x, 1)
+        np.testing.assert_allclose(y, dense @ x, rtol=1e-12, atol=1e-12)
+        assert np.array_equal(p(x, 3), y)
