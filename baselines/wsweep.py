@@ -2,9 +2,10 @@
 Theorem 2.3's W-array grammar sweep and the direct CSR product, each
 sequential and OpenMP over the machine's host cores.
 
-TEST INFRASTRUCTURE, like the rest of this package: only tests and
-bench.py's CPU-baseline leg use it. The C source is compiled with gcc on
-first use into ``oracle/_build/`` (no part of the product's build).
+Timed baselines only (no part of the product, and not the oracle): bench.py's
+CPU-baseline leg and the tests that pin these C routines use it. The C source
+is compiled with gcc on first use into ``baselines/_build/`` (no part of the
+product's build).
 """
 from __future__ import annotations
 

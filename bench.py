@@ -291,12 +291,37 @@ def cpu_oracle_rates(workload, seconds, steps=1):
     return [(r["rows"] / n) / r["seconds"] for r in recs], recs
 
 
+def cpu_oracle_all_cores(workload, seconds):
+    """The same oracle sample on every host core the process may use: one
+    child process per core (one BLAS thread each), all running at once for
+    ``seconds``; products per second summed over the children."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", workload,
+           "--cpu-seconds", str(seconds), "--steps", "1"]
+    procs = [subprocess.Popen(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+             for _ in range(cores)]
+    wl = WORKLOADS[workload]
+    n = wl["graph"]["nodes"] if "graph" in wl else wl["gen"]["n"]
+    rows = secs = 0.0
+    total = 0.0
+    for p in procs:
+        out, _ = p.communicate()
+        if p.returncode != 0:
+            raise RuntimeError("oracle sample child failed")
+        r = json.loads(out.strip().splitlines()[-1])[0]
+        total += (r["rows"] / n) / r["seconds"]
+        rows += r["rows"]
+        secs = max(secs, r["seconds"])
+    return total, cores, rows
+
+
 def grammar_sweep_rates(G, gen, seconds):
     """Theorem 2.3's W-array sweep over the same grammar on the host cores
-    (oracle/wsweep.c, float64), sequential and on every core the process may
+    (baselines/wsweep.c, float64), sequential and on every core the process may
     use: the CPU grammar baseline, reported beside the oracle; and the direct
     CSR product of the same matrix the same two ways."""
-    from oracle.wsweep import CsrProduct, GrammarSweep
+    from baselines.wsweep import CsrProduct, GrammarSweep
     t0 = time.perf_counter()
     sw = GrammarSweep.from_grammar(G)
     prep = time.perf_counter() - t0
@@ -581,15 +606,28 @@ def run_ours(args):
     achieved = bytes_step / mean_s / 1e9
     lay = eng.layout
     footprint = lay["grammar_bytes"] + lay["scratch_bytes"] + elem * k * (gen["m"] + gen["n"])
-    kernel_name = ("whole left product: left_step_kernel x (depth + 3)" if left else
-                   "whole product: sweep_kernel + slice_kernel" if launches_per_step == 2 else "whole product: sweep_kernel")
-    cpu = None
+    if left:
+        kernel_name = "whole left product: left_step_kernel x (depth + 3)"
+    elif eng.schedule == "dataflow":
+        kernel_name = "whole product: flow_kernel + " + ("slice_kernel" if not graph else "emit_kernel (rows)")
+    else:
+        kernel_name = "whole product: sweep_kernel" + (" + slice_kernel" if launches_per_step == 2 else "")
+    cpu = cpu_all = None
     if not args.no_cpu_baseline:
         rates, recs = cpu_oracle_rates(args.workload, args.cpu_seconds)
         cpu = {"value": rates[0], "unit": "matvec/s", "cores": 1, "kind": "oracle",
                "sample": f"{recs[0]['rows']} rows ({recs[0]['rows'] / gen['n']:.3f} products) of the same "
                          f"matrix in {recs[0]['seconds']:.1f} s: {oracle_sample_text(args.workload)}, "
                          "one BLAS thread"}
+        # the same oracle on every host core (one process a core), reported beside it
+        try:
+            v_all, cores_all, rows_all = cpu_oracle_all_cores(args.workload, max(2.0, args.cpu_seconds / 3))
+            cpu_all = {"value": v_all, "unit": "matvec/s", "cores": cores_all, "kind": "oracle",
+                       "sample": f"{int(rows_all)} rows in all over {cores_all} processes, each "
+                                 f"{max(2.0, args.cpu_seconds / 3):.1f} s of {oracle_sample_text(args.workload)}, "
+                                 "one BLAS thread each; products per second summed"}
+        except Exception as e:  # noqa: BLE001
+            cpu_all = {"error": f"{type(e).__name__}: {e}"[:200]}
     # the CPU grammar sweep (genotype workloads, float32 sum, one vector);
     # reported only, and never allowed to cost the line
     cpu_sweep = None
@@ -616,6 +654,7 @@ def run_ours(args):
                      "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": bytes_step},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "cpu_grammar_sweep": cpu_sweep,
         "e2e": {"value": e2e, "unit": "matvec/s", "h2d_bytes_per_step": elem * k * n_in,
                 "d2h_bytes_per_step": elem * k * n_out},

@@ -162,11 +162,13 @@ class Engine:
 
     @property
     def schedule(self) -> str:
-        return "persistent" if _capi().gc_get_schedule(self._h) == 0 else "per_level"
+        """"persistent" (grid barriers), "per_level" (a launch per level) or
+        "dataflow" (per-block ready flags; handles with k_max = 1)."""
+        return {0: "persistent", 1: "per_level", 2: "dataflow"}[_capi().gc_get_schedule(self._h)]
 
     @schedule.setter
     def schedule(self, name: str):
-        _capi().gc_set_schedule(self._h, {"persistent": 0, "per_level": 1}[name])
+        _capi().gc_set_schedule(self._h, {"persistent": 0, "per_level": 1, "dataflow": 2}[name])
 
     def __del__(self):
         h = getattr(self, "_h", None)

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libgcsparse.so")
 
 HOST_SOURCES = ["csrv.cpp", "repair.cpp", "layer.cpp", "capi_host.cpp"]
 CUDA_SOURCES = ["engine.cu", "left.cu"]
-HEADERS = ["common.hpp", "layout.hpp", "policy.cuh", "left.hpp"]
+HEADERS = ["common.hpp", "layout.hpp", "flow.hpp", "policy.cuh", "left.hpp"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 _lock = threading.Lock()

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "GC_OK", -1: "GC_ERR_ARG", -2: "GC_ERR_OOM", -3: "GC_ERR_CUDA
                 -7: "GC_ERR_NOT_CONVERGED", -8: "GC_ERR_IO"}
 
 GC_F32_SUM, GC_I64_SUM, GC_BOOL_OR, GC_F32_MIN_PLUS = 0, 1, 2, 3
-GC_SCHED_PERSISTENT, GC_SCHED_PER_LEVEL = 0, 1
+GC_SCHED_PERSISTENT, GC_SCHED_PER_LEVEL, GC_SCHED_DATAFLOW = 0, 1, 2
 POLICIES = {"f32": GC_F32_SUM, "i64": GC_I64_SUM, "or": GC_BOOL_OR, "minplus": GC_F32_MIN_PLUS}
 
 ARRAYS = {  # gc_array enum -> numpy dtype

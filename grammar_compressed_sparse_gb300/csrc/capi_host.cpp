@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "common.hpp"
+#include "flow.hpp"
 #include "layout.hpp"
 
 #ifdef _OPENMP
@@ -337,7 +338,13 @@ gc_status gc_layout(const gc_grammar* gg, gc_policy policy, int32_t k_max, gc_ar
         if (!gg || !out) fail(GC_ERR_ARG, "null argument");
         const Grammar& g = gg->g;
         check_policy(g, policy, k_max);
-        const DevLayout d = device_layout(device_view(g, emit_mode(g, k_max) == EMIT_LEVEL), policy, k_max);
+        DevLayout d;
+        if (uses_flow(k_max)) {
+            const FlowCounts fc = flow_counts(*flow_plan_for(gg, policy_elem_bytes(policy)));
+            d = device_layout(g, policy, k_max, &fc);
+        } else {
+            d = device_layout(device_view(g, emit_mode(g, k_max) == EMIT_LEVEL), policy, k_max);
+        }
         gc_arena_layout l{};
         l.arena_bytes = d.total;
         l.grammar_bytes = d.grammar_bytes;

@@ -3,6 +3,8 @@
 
 #include <algorithm>
 #include <chrono>
+#include <memory>
+#include <mutex>
 #include <cstdint>
 #include <new>
 #include <stdexcept>
@@ -121,4 +123,8 @@ gc_status guard(F&& f) {
 
 struct gc_grammar {
     gcs::Grammar g;
+    // dataflow block plans of this grammar for 4- and 8-byte values, made on
+    // first use by gc_layout / gc_upload (flow.hpp) and kept with the grammar
+    mutable std::mutex flow_mu;
+    mutable std::shared_ptr<const void> flow_plan[2];
 };

@@ -46,6 +46,7 @@
 #include <mutex>
 
 #include "common.hpp"
+#include "flow.hpp"
 #include "layout.hpp"
 #include "policy.cuh"
 
@@ -57,6 +58,7 @@ struct gc_handle {
     char* arena = nullptr;
     gcs::DevLayout lay{};
     int sms = 1;
+    int device = 0;               // the device the arena lives on (current at gc_upload)
     int emit_group = 32;          // row emit: threads per row (0 in the chunked emits)
     int schedule = 0;             // 0 persistent (if cooperative launch works), 1 per level
     int coop = 0;                 // device supports cooperative launch
@@ -66,6 +68,12 @@ struct gc_handle {
     long long timeout_cycles = 4000000000LL;
     int32_t inject = 0;           // test-only: 1 = CTA 0 skips its first barrier arrival
     int64_t launches = 0;
+    // dataflow sweep (one value a node): block plan counts and the product
+    // number its ready flags and level counters are stamped with
+    bool flow = false;
+    int64_t nblocks = 0, final_k0 = 0;
+    std::vector<int64_t> lvl_blk;   // first block of each level (L+2)
+    uint32_t epoch = 0;
 };
 
 namespace gcs {
@@ -96,17 +104,23 @@ struct Chunk {
 };
 
 // ---------------------------------------------------------------- PTX helpers
+// Every .global-qualified instruction below takes a global-window address:
+// the generic pointer (always into the caller's arena, the fixed scratch
+// array or x / y) is converted with cvta.to.global first, as the PTX state
+// spaces require, instead of relying on the generic and global windows
+// coinciding.
+__device__ __forceinline__ size_t gaddr(const void* p) { return __cvta_generic_to_global(p); }
 __device__ __forceinline__ void red_add_release(unsigned long long* p, unsigned long long v) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(gaddr(p)), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
     unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(gaddr(p)) : "memory");
     return v;
 }
 __device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(gaddr(p))); }
 
 __device__ __forceinline__ uint64_t l2_evict_last() {
     uint64_t pol;
@@ -115,18 +129,18 @@ __device__ __forceinline__ uint64_t l2_evict_last() {
 }
 // stores that ask L2 to keep the line (root values, read again by the emit)
 __device__ __forceinline__ void st_keep(float* p, float v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(gaddr(p)), "f"(v), "l"(pol) : "memory");
 }
 __device__ __forceinline__ void st_keep(float4* p, float4 v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(gaddr(p)), "f"(v.x), "f"(v.y),
                  "f"(v.z), "f"(v.w), "l"(pol)
                  : "memory");
 }
 __device__ __forceinline__ void st_keep(long long* p, long long v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(pol) : "memory");
+    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(gaddr(p)), "l"(v), "l"(pol) : "memory");
 }
 __device__ __forceinline__ void st_keep(unsigned long long* p, unsigned long long v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(pol) : "memory");
+    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(gaddr(p)), "l"(v), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ float shfl_x(float v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
@@ -954,6 +968,351 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
     }
 }
 
+// ---------------------------------------------------------------- dataflow sweep
+// One value a node (flow.hpp has the block plan). A CTA per SM: warp 0
+// stages blocks into a ring of shared-memory buffers -- it waits for a
+// block's dependencies (the producers' ready flags, and level k-2 finished
+// before level k overwrites its buffer), then copies the block's node pairs,
+// windows and outlier granules with bulk copies that complete on the stage's
+// mbarrier -- while 16 compute warps evaluate the previously staged blocks:
+// every child is a shared-memory value, the identity or a leaf evaluated in
+// place; values go to the level buffer (and RV for roots); the block's flag is
+// then released. Blocks are dealt to CTAs round robin (b = CTA, CTA + grid,
+// ...), and a CTA works through its blocks in order; every dependency is an
+// earlier block, so the earliest unfinished block can always proceed (all
+// CTAs are resident: cooperative launch). The final block (the narrow top
+// levels) takes every staging buffer of its CTA and computes its levels one
+// after the other in shared memory.
+constexpr int kFlowCW = 16;                   // compute warps of a CTA
+constexpr int kFlowCT = 32 * kFlowCW;         // compute threads
+constexpr int kFlowThreads = kFlowCT + 32;    // and the staging warp
+constexpr int kNS = (int)kFlowStages;
+constexpr int kSB = (int)kFlowStageBytes;
+constexpr int LV_NBLK = 9;                    // level table: regular blocks of level k
+static_assert(LV_NBLK < LV_ROWS, "level table rows");
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bulk copy global -> this CTA's shared memory, completing on bar (16-byte
+// aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(gaddr(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(gaddr(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// generic-proxy writes and async-proxy (bulk copy) reads of the level buffers
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gaddr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(int32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gaddr(p)), "r"(v) : "memory");
+}
+
+template <class P>
+struct FlowArgs {
+    using V = typename P::V;
+    const int2* pairs;        // block-local child references
+    const int32_t* blk;       // kFlowBlkInts per block
+    const int32_t* deps;
+    const int32_t* gran;
+    const int64_t* lv;        // level table
+    int32_t L2;               // its row stride
+    int32_t b_begin, b_end;   // blocks of this launch
+    int32_t final_block;      // id of the final block, or -1
+    int32_t waits;            // 1: one launch for all blocks, wait for dependencies
+    int32_t write_t;          // write T in front of RV
+    int64_t TB, alpha;
+    const typename P::Leaf* Vd;
+    const int32_t* leaf;
+    int32_t vbits;
+    const V* x;
+    V* rv;
+    V* fb0;                   // level k is written to buffer k % 3
+    V* fb1;
+    V* fb2;
+    int32_t* flags;           // per block: the product number once it is ready
+    unsigned long long* done; // per level: blocks finished over all products
+    uint32_t epoch;           // this product's number
+    int32_t* status;
+    long long timeout;
+    int32_t inject;
+
+    __device__ __forceinline__ int64_t lvl(int row, int k) const { return __ldg(lv + (int64_t)row * L2 + k); }
+    __device__ __forceinline__ V* buf(int k) const { return k % 3 == 0 ? fb0 : k % 3 == 1 ? fb1 : fb2; }
+};
+
+template <class P>
+__device__ __forceinline__ typename P::V flow_leaf(const FlowArgs<P>& a, uint32_t q) {
+    return P::leaf(__ldg(a.Vd + (q & ((1u << a.vbits) - 1u))), __ldg(a.x + (q >> a.vbits)));
+}
+
+// Bounded waits: each gives up after a.timeout cycles, or as soon as another
+// wait has reported a timeout, and then returns false.
+template <class P>
+__device__ __forceinline__ bool wait_give_up(const FlowArgs<P>& a, long long t0) {
+    if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return true;
+    if (clock64() - t0 > a.timeout) {
+        atomicCAS(a.status, 0, (int32_t)GC_ERR_TIMEOUT);
+        return true;
+    }
+    return false;
+}
+template <class P>
+__device__ bool wait_flag(const int32_t* p, uint32_t want, const FlowArgs<P>& a) {
+    const long long t0 = clock64();
+    for (unsigned n = 0;; ++n) {
+        if (ld_acquire_u32(p) == want) return true;
+        if ((n & 15u) == 15u && wait_give_up(a, t0)) return false;
+    }
+}
+template <class P>
+__device__ bool wait_count(const unsigned long long* p, unsigned long long want, const FlowArgs<P>& a) {
+    const long long t0 = clock64();
+    for (unsigned n = 0;; ++n) {
+        if (ld_acquire(p) >= want) return true;
+        if ((n & 15u) == 15u && wait_give_up(a, t0)) return false;
+    }
+}
+template <class P>
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FlowArgs<P>& a) {
+    const long long t0 = clock64();
+    for (unsigned n = 0;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 63u && wait_give_up(a, t0)) return false;
+    }
+}
+
+// Warp 0: stages this CTA's blocks in order. On a failed wait it records the
+// first iteration it did not stage in *stop and returns; nothing it did not
+// issue is in flight.
+template <class P>
+__device__ void flow_stage(const FlowArgs<P>& a, unsigned char* fsm, uint64_t* full, uint64_t* empty,
+                           volatile int* stop) {
+    using V = typename P::V;
+    constexpr int G = 16 / (int)sizeof(V);
+    const int lane = threadIdx.x & 31;
+    const uint64_t first = l2_evict_first();
+    int it = 0;
+    // before the warp leaves, the copies it issued (uses it-kNS .. it-1 of
+    // the stages) have landed: nothing is in flight when the CTA exits
+    auto drain = [&]() {
+        if (lane == 0)
+            for (int i = it > kNS ? it - kNS : 0; i < it; ++i)
+                if (!mbar_wait(&full[i % kNS], (uint32_t)(i / kNS) & 1u, a)) break;
+        __syncwarp();
+    };
+    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
+        const int s = it % kNS;
+        const int32_t fv = lane < (int)kFlowBlkInts ? __ldg(a.blk + (int64_t)b * kFlowBlkInts + lane) : 0;
+        auto F = [&](int i) { return __shfl_sync(0xffffffffu, fv, i); };
+        const int k0 = F(FB_K0);
+        const bool fin = b == a.final_block;
+        bool ok = true;
+        // the staging buffer is free once the compute warps released its last
+        // use (the final block needs every buffer)
+        if (lane == 0) {
+            if (fin)
+                for (int i = it > kNS ? it - kNS : 0; i < it && ok; ++i) ok = mbar_wait(&empty[i % kNS], (uint32_t)(i / kNS) & 1u, a);
+            else if (it >= kNS)
+                ok = mbar_wait(&empty[s], (uint32_t)(it / kNS - 1) & 1u, a);
+        }
+        if (a.waits) {
+            const int doff = F(FB_DOFF), nd = F(FB_NDEP);
+            for (int j = lane; j < nd && ok; j += 32) ok = wait_flag(a.flags + __ldg(a.deps + doff + j), a.epoch, a);
+            if (lane == 0 && ok && !fin && k0 >= 3)
+                ok = wait_count(a.done + (k0 - 2), (unsigned long long)a.epoch * (unsigned long long)a.lvl(LV_NBLK, k0 - 2), a);
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) *stop = it;
+            drain();
+            return;
+        }
+        fence_proxy_async_global();
+        unsigned char* base = fin ? fsm : fsm + s * kSB;
+        // every lane reads every field here: F is a full-warp shuffle, so it
+        // is never called inside a lane-dependent branch
+        const int pb = F(FB_PB), wl1 = F(FB_WL1), wl2 = F(FB_WL2), ng = F(FB_NGRAN), goff = F(FB_GOFF);
+        const int node0 = F(FB_NODE0), ws1 = F(FB_WS1), ws2 = F(FB_WS2);
+        if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)pb + (uint32_t)(wl1 + wl2 + ng * G) * (uint32_t)sizeof(V));
+        __syncwarp();
+        const V* prev = a.buf(k0 + 2);   // level k0 - 1
+        V* vals = reinterpret_cast<V*>(base + pb);
+        if (lane == 0) bulk_g2s_hint(base, a.pairs + node0, (uint32_t)pb, &full[s], first);
+        if (lane == 1 && wl1 > 0) bulk_g2s(vals, prev + ws1, (uint32_t)(wl1 * sizeof(V)), &full[s]);
+        if (lane == 2 && wl2 > 0) bulk_g2s(vals + wl1, prev + ws2, (uint32_t)(wl2 * sizeof(V)), &full[s]);
+        for (int j = lane; j < ng; j += 32)
+            bulk_g2s(vals + wl1 + wl2 + j * G, prev + __ldg(a.gran + goff + j), 16u, &full[s]);
+    }
+    drain();
+}
+
+// Warps 1..16: evaluate this CTA's staged blocks in order. They synchronise
+// among themselves on the mbarrier cbar (every compute thread arrives; the
+// waits are bounded, so a thread that gave up cannot leave the others stuck).
+template <class P>
+__device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, uint64_t* full, uint64_t* empty,
+                             uint64_t* cbar, volatile int* stop) {
+    using V = typename P::V;
+    constexpr int G = 16 / (int)sizeof(V);
+    constexpr int U = 4;   // nodes a thread evaluates together
+    const int ct = (int)threadIdx.x - 32;
+    const uint64_t keep = l2_evict_last();
+    uint32_t cphase = 0;
+    auto csync = [&]() {
+        mbar_arrive(cbar);
+        return mbar_wait(cbar, cphase++ & 1u, a);
+    };
+    int it = 0;
+    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
+        const int s = it % kNS;
+        {
+            // wait for the stage; the staging warp's own waits are bounded, so
+            // a stage it never issues shows up in *stop
+            const long long t0 = clock64();
+            for (unsigned n = 0;; ++n) {
+                if (mbar_try_wait(&full[s], (uint32_t)(it / kNS) & 1u)) break;
+                if ((n & 63u) == 63u) {
+                    if (*stop <= it) return;
+                    if (clock64() - t0 > 4 * a.timeout) {
+                        atomicCAS(a.status, 0, (int32_t)GC_ERR_TIMEOUT);
+                        return;
+                    }
+                }
+            }
+        }
+        const int32_t* f = a.blk + (int64_t)b * kFlowBlkInts;
+        const int k0 = __ldg(f + FB_K0), pb = __ldg(f + FB_PB);
+        const bool fin = b == a.final_block;
+        unsigned char* base = fin ? fsm : fsm + s * kSB;
+        const int2* pr = reinterpret_cast<const int2*>(base);
+        V* vals = reinterpret_cast<V*>(base + pb);
+        auto child = [&](int32_t c) -> V {
+            return c >= 0 ? vals[c] : c == -1 ? P::identity() : flow_leaf<P>(a, (uint32_t)(-2 - c));
+        };
+        if (!fin) {
+            const int nn = __ldg(f + FB_NNODES), slot0 = __ldg(f + FB_SLOT0);
+            const int64_t nroots = a.lvl(LV_ROOTS, k0);
+            const int nr = (int)(nroots - slot0 < 0 ? 0 : nroots - slot0 < nn ? nroots - slot0 : nn);
+            V* out = a.buf(k0) + slot0;
+            V* rvo = a.rv + a.TB + a.lvl(LV_ROFF, k0) + slot0;
+            for (int i0 = ct; i0 < nn; i0 += U * kFlowCT) {
+                int2 c[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) c[u] = i0 + u * kFlowCT < nn ? pr[i0 + u * kFlowCT] : make_int2(-1, -1);
+                V va[U], vb[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    va[u] = child(c[u].x);
+                    vb[u] = child(c[u].y);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = i0 + u * kFlowCT;
+                    if (i < nn) {
+                        const V v = P::combine(va[u], vb[u]);
+                        out[i] = v;
+                        if (i < nr) st_keep(rvo + i, v, keep);
+                    }
+                }
+            }
+        } else {
+            // levels k0..k1 one after the other; level k's values follow the
+            // window (and the levels before it) in shared memory
+            const int k1 = __ldg(f + FB_K1);
+            int own = __ldg(f + FB_WL1);
+            const int64_t start0 = a.lvl(LV_START, k0);
+            for (int k = k0; k <= k1; ++k) {
+                const int w = (int)a.lvl(LV_W, k), nr = (int)a.lvl(LV_ROOTS, k);
+                const int p0 = (int)(a.lvl(LV_START, k) - start0);
+                V* rvo = a.rv + a.TB + a.lvl(LV_ROFF, k);
+                for (int i = ct; i < w; i += kFlowCT) {
+                    const int2 c = pr[p0 + i];
+                    const V v = P::combine(child(c.x), child(c.y));
+                    vals[own + i] = v;
+                    if (i < nr) st_keep(rvo + i, v, keep);
+                }
+                own += (w + G - 1) / G * G;
+                if (!csync()) return;
+            }
+        }
+        if (!csync()) return;
+        if (ct == 0) {
+            // publish: every compute thread's writes of this block are ordered
+            // before the flag by the barrier above (arrive releases, wait acquires) (test-only injection: CTA 0
+            // never publishes its first block)
+            if (!(a.inject == 1 && a.waits && blockIdx.x == 0 && it == 0)) {
+                fence_proxy_async_global();
+                __threadfence();
+                st_release_u32(a.flags + b, a.epoch);
+                if (!fin) red_add_release(a.done + k0, 1ull);
+            }
+            mbar_arrive(&empty[s]);
+        }
+    }
+}
+
+template <class P>
+__global__ void __launch_bounds__(kFlowThreads, 1) flow_kernel(const FlowArgs<P> a) {
+    using V = typename P::V;
+    extern __shared__ __align__(128) unsigned char fsm[];
+    __shared__ __align__(8) uint64_t full[kNS], empty[kNS], cbar;
+    __shared__ volatile int s_stop;
+    // an unread earlier timeout: do nothing
+    if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&cbar, kFlowCT);
+        s_stop = 0x7fffffff;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // T[0] = identity, T[p+1] = V[l_p] (x) x[j_p] in front of RV (the emit's
+    // terminals), grid-stride
+    if (a.write_t) {
+        const int64_t nt = (int64_t)gridDim.x * blockDim.x;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= a.alpha; i += nt)
+            a.rv[i] = i == 0 ? P::identity() : flow_leaf<P>(a, (uint32_t)__ldg(a.leaf + (i - 1)));
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) flow_stage<P>(a, fsm, full, empty, &s_stop);
+    else flow_compute<P>(a, fsm, full, empty, &cbar, &s_stop);
+}
+
 // ---------------------------------------------------------------- per-level schedule
 template <class P, bool kC>
 __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a, int k) {
@@ -1204,11 +1563,141 @@ int64_t launch_product_as(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, 
     return launches;
 }
 
+// Scratch of a dataflow product: the three level buffers, the ready flags
+// and level counters, and the product number they are stamped with.
+struct FlowScratch {
+    char* fb0;
+    char* fb1;
+    char* fb2;
+    int32_t* flags;
+    unsigned long long* done;
+    uint32_t epoch;
+};
+
+template <class P>
+FlowArgs<P> make_flow_args(const gc_handle* h, const SweepArgs<P>& a, const FlowScratch& fs) {
+    using V = typename P::V;
+    const DevLayout& d = h->lay;
+    char* ar = h->arena;
+    FlowArgs<P> f{};
+    f.pairs = reinterpret_cast<const int2*>(ar + d.nodes);
+    f.blk = reinterpret_cast<const int32_t*>(ar + d.fblk);
+    f.deps = reinterpret_cast<const int32_t*>(ar + d.fdeps);
+    f.gran = reinterpret_cast<const int32_t*>(ar + d.fgran);
+    f.lv = a.lv;
+    f.L2 = a.L2;
+    f.final_block = h->final_k0 <= h->L ? (int32_t)(h->nblocks - 1) : -1;
+    f.TB = a.TB;
+    f.alpha = a.alpha;
+    f.Vd = a.Vd;
+    f.leaf = a.leaf;
+    f.vbits = a.vbits;
+    f.x = a.x;
+    f.rv = a.rv;
+    f.fb0 = reinterpret_cast<V*>(fs.fb0);
+    f.fb1 = reinterpret_cast<V*>(fs.fb1);
+    f.fb2 = reinterpret_cast<V*>(fs.fb2);
+    f.flags = fs.flags;
+    f.done = fs.done;
+    f.epoch = fs.epoch;
+    f.status = a.status;
+    f.timeout = a.timeout;
+    f.inject = a.inject;
+    return f;
+}
+
+// One dataflow product: the sweep (one cooperative launch, or one launch per
+// level without waits for the per-level schedule), then the emit from RV
+// (slice emit with its row pass, or the row emit).
+template <class P>
+int64_t launch_flow(const gc_handle* h, SweepArgs<P>& a, const FlowScratch& fs, cudaStream_t st,
+                    unsigned long long* arrivals) {
+    FlowArgs<P> f = make_flow_args<P>(h, a, fs);
+    const size_t smem = (size_t)kNS * kSB;
+    cuda_check(cudaFuncSetAttribute((const void*)flow_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+               "dataflow shared memory");
+    int64_t launches = 0;
+    *arrivals = 0;
+    int grid = 0;
+    if (h->schedule != GC_SCHED_PER_LEVEL && h->coop) {
+        int per_sm = 0;
+        cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, flow_kernel<P>, kFlowThreads, smem),
+                   "dataflow occupancy");
+        grid = per_sm >= 1 ? h->sms : 0;
+    }
+    if (grid > 0) {
+        f.b_begin = 0;
+        f.b_end = (int32_t)h->nblocks;
+        f.waits = 1;
+        f.write_t = 1;
+        void* args[] = {&f};
+        cuda_check(cudaLaunchCooperativeKernel((const void*)flow_kernel<P>, dim3(grid), dim3(kFlowThreads), args, smem, st),
+                   "dataflow launch");
+        launches = 1;
+    } else {
+        // Listing 1's order: one launch per level (the final block last);
+        // the launches order the levels, so nothing waits
+        f.waits = 0;
+        f.write_t = 1;
+        auto one = [&](int64_t b0, int64_t b1) {
+            f.b_begin = (int32_t)b0;
+            f.b_end = (int32_t)b1;
+            const int g = (int)std::max<int64_t>(1, std::min<int64_t>(b1 - b0, (int64_t)h->sms));
+            flow_kernel<P><<<g, kFlowThreads, smem, st>>>(f);
+            f.write_t = 0;
+            ++launches;
+        };
+        const int64_t kreg = std::min<int64_t>(h->final_k0, h->L + 1);   // first level without regular blocks
+        for (int64_t k = 1; k < kreg; ++k)
+            if (h->lvl_blk[k + 1] > h->lvl_blk[k]) one(h->lvl_blk[k], h->lvl_blk[k + 1]);
+        if (h->final_k0 <= h->L) one(h->nblocks - 1, h->nblocks);
+        if (launches == 0) one(0, 0);   // no levels: the leaf table only
+    }
+    if (h->n > 0) {
+        if (h->lay.emit == EMIT_SLICE) {
+            if constexpr (kScalarPolicy<P>) {
+                const int grid2 = grid > 0 ? slice_grid<P, false>(h) : 0;
+                a.tail_group = 1;
+                a.tail_solo = h->L + 1;
+                if (grid2 > 0) {
+                    int coop = 1;
+                    void* args2[] = {&a, &coop};
+                    cuda_check(cudaLaunchCooperativeKernel((const void*)slice_kernel<P, false>, dim3(grid2),
+                                                           dim3(kSliceThreads), args2, (size_t)slice_smem<P>(h), st),
+                               "slice launch");
+                    *arrivals = (unsigned long long)grid2;
+                    ++launches;
+                } else {
+                    const int64_t ss = slice_smem<P>(h);
+                    cuda_check(cudaFuncSetAttribute((const void*)slice_kernel<P, false>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss),
+                               "slice shared memory");
+                    const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>(h->lay.n_slices, h->sms));
+                    slice_kernel<P, false><<<g2, kSliceThreads, (size_t)ss, st>>>(a, 0);
+                    emit_kernel<P><<<grid_for(h->n, kWarps, h->sms, 4), kThreads, 0, st>>>(a, 1);
+                    launches += 2;
+                }
+            }
+        } else {
+            emit_kernel<P><<<grid_for(h->n, kWarps * (32 / h->emit_group), h->sms, 4), kThreads, 0, st>>>(a, 0);
+            ++launches;
+        }
+    }
+    cuda_check(cudaGetLastError(), "kernel launch");
+    return launches;
+}
+
 // Carry slots exist only for the device view of 16-wide handles (the float32
-// policies); the other policies are built without them.
+// policies); the other policies are built without them. Handles with one
+// value a node run the dataflow sweep (fs: its scratch).
 template <class P>
 int64_t launch_product(const gc_handle* h, SweepArgs<P>& a, cudaStream_t st, unsigned long long* arrivals,
-                       unsigned long long* tail_arrivals) {
+                       unsigned long long* tail_arrivals, const FlowScratch* fs) {
+    if (h->flow) {
+        *tail_arrivals = 0;
+        if constexpr (kScalarPolicy<P>) return launch_flow<P>(h, a, *fs, st, arrivals);
+        fail(GC_ERR_ARG, "a multi-vector product on a one-vector handle");
+    }
     if constexpr (std::is_same<typename P::Leaf, float>::value)
         if (h->n_carry > 0) return launch_product_as<P, true>(h, a, st, arrivals, tail_arrivals);
     if (h->n_carry > 0) fail(GC_ERR_UNSUPPORTED, "carry slots for a policy built without them");
@@ -1219,7 +1708,18 @@ template <class P>
 void run_product(gc_handle* h, const void* x, void* y, cudaStream_t st) {
     SweepArgs<P> a = make_args<P>(h, x, y);
     unsigned long long arrivals = 0, tail_arrivals = 0;
-    h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals);
+    FlowScratch fs{};
+    if (h->flow) {
+        const DevLayout& d = h->lay;
+        fs.fb0 = h->arena + d.fb0;
+        fs.fb1 = h->arena + d.fb1;
+        fs.fb2 = h->arena + d.fb2;
+        fs.flags = reinterpret_cast<int32_t*>(h->arena + d.fflags);
+        fs.done = reinterpret_cast<unsigned long long*>(h->arena + d.fdone);
+        if (++h->epoch == 0) ++h->epoch;   // flags start at 0: never stamp 0
+        fs.epoch = h->epoch;
+    }
+    h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals, h->flow ? &fs : nullptr);
     h->bar_base += arrivals;
     h->tbar_base += tail_arrivals;
 }
@@ -1261,6 +1761,16 @@ void dispatch_product(gc_handle* h, const void* x, void* y, int32_t k, cudaStrea
 void check_k(const gc_handle* h, int32_t k) {
     if (!policy_width_ok(h->policy, k)) fail(GC_ERR_ARG, "k is not a width this policy supports");
     if (k > h->k_max) fail(GC_ERR_ARG, "k exceeds the k_max the handle was uploaded with");
+}
+
+// Products run on the current device; the handle's arena (and the fixed
+// scratch picked for the current device) must be on that same device.
+void check_device(const gc_handle* h) {
+    int dev = 0;
+    cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev != h->device)
+        fail(GC_ERR_ARG, "the current device (" + std::to_string(dev) + ") is not the device the handle was uploaded on (" +
+                             std::to_string(h->device) + ")");
 }
 
 template <class T>
@@ -1345,6 +1855,7 @@ unsigned char* static_scratch_on_current_device() {
 // sums or RV, then the status block.
 struct StaticParts {
     int64_t buf0, buf1, esum, tbuf, carry, rv, status, total;
+    int64_t fb0, fb1, fb2, fflags, fdone;   // dataflow handles
 };
 StaticParts static_parts(const gc_handle* h, int32_t k) {
     const DevLayout& d = h->lay;
@@ -1356,6 +1867,20 @@ StaticParts static_parts(const gc_handle* h, int32_t k) {
         o = align256(o + bytes);
         return at;
     };
+    if (h->flow) {
+        // the three level buffers, RV and the emit's sums, then the flags,
+        // level counters and status block back to back (cleared by every call)
+        s.fb0 = take(vb * d.fbuf_values);
+        s.fb1 = take(vb * d.fbuf_values);
+        s.fb2 = take(vb * d.fbuf_values);
+        if (d.chunked()) s.esum = take(vb * d.n_esum);
+        if (d.has_rv()) s.rv = take(vb * (d.TB + h->n_roots));
+        s.fflags = take(4 * std::max<int64_t>(1, h->nblocks));
+        s.fdone = take(8 * (h->L + 2));
+        s.status = take(256);
+        s.total = o;
+        return s;
+    }
     s.buf0 = take(vb * (d.TB + h->max_width));
     s.buf1 = take(vb * (d.TB + h->max_width));
     s.tbuf = take(vb * d.tail_total);
@@ -1390,10 +1915,22 @@ void run_product_static(gc_handle* h, const void* x, void* y, cudaStream_t st, u
     a.tbar_base = 0;
     a.inject = 0;
     // the array keeps the previous call's contents: start from a clear status
-    // word and barrier counter
-    cuda_check(cudaMemsetAsync(scratch + sp.status, 0, 256, st), "fixed scratch clear");
+    // word and barrier counter (and, for the dataflow sweep, clear ready
+    // flags and level counters, with product number 1)
+    FlowScratch fs{};
+    if (h->flow) {
+        fs.fb0 = reinterpret_cast<char*>(scratch + sp.fb0);
+        fs.fb1 = reinterpret_cast<char*>(scratch + sp.fb1);
+        fs.fb2 = reinterpret_cast<char*>(scratch + sp.fb2);
+        fs.flags = reinterpret_cast<int32_t*>(scratch + sp.fflags);
+        fs.done = reinterpret_cast<unsigned long long*>(scratch + sp.fdone);
+        fs.epoch = 1;
+        cuda_check(cudaMemsetAsync(scratch + sp.fflags, 0, (size_t)(sp.total - sp.fflags), st), "fixed scratch clear");
+    } else {
+        cuda_check(cudaMemsetAsync(scratch + sp.status, 0, 256, st), "fixed scratch clear");
+    }
     unsigned long long arrivals = 0, tail_arrivals = 0;
-    h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals);
+    h->launches = launch_product<P>(h, a, st, &arrivals, &tail_arrivals, h->flow ? &fs : nullptr);
 }
 
 template <class P>
@@ -1418,9 +1955,22 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         if (reinterpret_cast<uintptr_t>(arena) % 256 != 0) fail(GC_ERR_ARG, "arena must be 256-byte aligned");
         check_policy(gg->g, policy, k_max);
         validate_packed(gg->g);
-        const Grammar g = device_view(gg->g, emit_mode(gg->g, k_max) == EMIT_LEVEL);   // carry slots for 16-wide values
-        validate_device_view(g);
-        const DevLayout d = device_layout(g, policy, k_max);
+        // one value a node: the dataflow sweep over the layered grammar itself;
+        // wider values: the device view (carry slots for the level emit)
+        const bool flow = uses_flow(k_max);
+        std::shared_ptr<const FlowPlan> fp;
+        FlowCounts fc;
+        Grammar view;
+        if (flow) {
+            fp = flow_plan_for(gg, policy_elem_bytes(policy));
+            validate_flow_plan(*fp, gg->g);
+            fc = flow_counts(*fp);
+        } else {
+            view = device_view(gg->g, emit_mode(gg->g, k_max) == EMIT_LEVEL);   // carry slots for 16-wide values
+            validate_device_view(view);
+        }
+        const Grammar& g = flow ? gg->g : view;
+        const DevLayout d = device_layout(g, policy, k_max, flow ? &fc : nullptr);
         if (arena_bytes < d.total) fail(GC_ERR_ARG, "arena smaller than gc_layout().arena_bytes");
         cudaStream_t st = static_cast<cudaStream_t>(stream);
         auto h = std::make_unique<gc_handle>();
@@ -1436,6 +1986,13 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         h->n_carry = g.n_carry;
         h->arena = static_cast<char*>(arena);
         h->lay = d;
+        h->flow = flow;
+        if (flow) {
+            h->nblocks = fp->nblocks;
+            h->final_k0 = fp->final_k0;
+            h->lvl_blk = fp->lvl_blk;
+            h->schedule = GC_SCHED_DATAFLOW;
+        }
         // row emit (rows average < 128 symbols): G lanes per row, so that a
         // lane loads about one batch of a row's symbols (4 one-lane values, 2
         // four-lane ones) and a warp reduces 32 / G rows at a time
@@ -1459,7 +2016,9 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             return kCarryBase + (int32_t)carry_slot(c, A);
         };
         h->lv.assign((size_t)(LV_ROWS * (L + 2)), 0);
-        std::vector<int32_t> nodes((size_t)(2 * d.n_nodes_padded), 0);
+        std::vector<int32_t> nodes;
+        if (flow) nodes = fp->pairs;
+        else nodes.assign((size_t)(2 * d.n_nodes_padded), 0);
         int64_t start = 0;
         for (int64_t k = 1; k <= L; ++k) {
             const int64_t w = g.lvl_off[k + 1] - g.lvl_off[k];
@@ -1468,6 +2027,11 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             h->lv[LV_ROOTS * (L + 2) + k] = g.lvl_roots[k];
             h->lv[LV_ROFF * (L + 2) + k] = g.root_off[k];
             h->lv[LV_TOFF * (L + 2) + k] = toff[k];
+            if (flow) {
+                h->lv[LV_NBLK * (L + 2) + k] = k < fp->final_k0 ? fp->lvl_blk[k + 1] - fp->lvl_blk[k] : 0;
+                start += pad_nodes(w);
+                continue;   // the plan's block-local references are the node array
+            }
             h->lv[LV_CR * (L + 2) + k] = g.carry_roots[k];
             h->lv[LV_CN * (L + 2) + k] = g.carry_rest[k];
             h->lv[LV_COFF * (L + 2) + k] = g.carry_off[k];
@@ -1507,6 +2071,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         // every host-side array is built and checked; now the device
         int dev = 0;
         cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+        h->device = dev;
         cuda_check(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
         cuda_check(cudaDeviceGetAttribute(&h->coop, cudaDevAttrCooperativeLaunch, dev), "cooperative attribute");
         char* a = h->arena;
@@ -1541,6 +2106,13 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             put(st, a, d.c_off, co.data(), co.size());
             put(st, a, d.c_ref, cref.data(), cref.size());
         }
+        if (flow) {
+            put(st, a, d.fblk, fp->blk.data(), fp->blk.size());
+            put(st, a, d.fdeps, fp->deps.data(), fp->deps.size());
+            put(st, a, d.fgran, fp->gran.data(), fp->gran.size());
+            cuda_check(cudaMemsetAsync(a + d.fflags, 0, 4 * std::max<int64_t>(1, d.n_fblocks), st), "flags clear");
+            cuda_check(cudaMemsetAsync(a + d.fdone, 0, 8 * (L + 2), st), "level counters clear");
+        }
         cuda_check(cudaMemsetAsync(a + d.status, 0, 256, st), "status clear");
         cuda_check(cudaStreamSynchronize(st), "upload synchronize");
         *out = h.release();
@@ -1552,6 +2124,7 @@ gc_status gc_matvec(gc_handle* h, const void* x, void* y, int32_t k, void* strea
         if (!h) fail(GC_ERR_ARG, "null handle");
         if ((!x && h->m > 0) || (!y && h->n > 0)) fail(GC_ERR_ARG, "null x or y");
         check_k(h, k);
+        check_device(h);
         dispatch_product(h, x, y, k, static_cast<cudaStream_t>(stream));
     });
 }
@@ -1561,6 +2134,7 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
         if (!h) fail(GC_ERR_ARG, "null handle");
         if ((!x_host && h->m > 0) || (!y_host && h->n > 0)) fail(GC_ERR_ARG, "null x or y");
         check_k(h, k);
+        check_device(h);
         cudaStream_t st = static_cast<cudaStream_t>(stream);
         const int64_t eb = policy_elem_bytes(h->policy) * k;
         char* xs = h->arena + h->lay.xs;
@@ -1578,6 +2152,7 @@ gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_it
     gc_status g = guard([&] {
         if (!h || !x0 || !x || !iters) fail(GC_ERR_ARG, "null argument");
         if (h->policy != GC_BOOL_OR) fail(GC_ERR_ARG, "gc_reach needs the GC_BOOL_OR policy");
+        check_device(h);
         if (h->n != h->m) fail(GC_ERR_ARG, "gc_reach needs a square matrix");
         if (max_iter < 1) fail(GC_ERR_ARG, "max_iter must be >= 1");
         if (!run_fixpoint<OrUpdate>(h, reinterpret_cast<const unsigned long long*>(x0),
@@ -1595,6 +2170,7 @@ gc_status gc_sssp(gc_handle* h, const float* x0, float* x, int32_t max_iter, int
     gc_status g = guard([&] {
         if (!h || !x0 || !x || !iters) fail(GC_ERR_ARG, "null argument");
         if (h->policy != GC_F32_MIN_PLUS) fail(GC_ERR_ARG, "gc_sssp needs the GC_F32_MIN_PLUS policy");
+        check_device(h);
         if (h->n != h->m) fail(GC_ERR_ARG, "gc_sssp needs a square matrix");
         if (max_iter < 1) fail(GC_ERR_ARG, "max_iter must be >= 1");
         if (!run_fixpoint<MinUpdate>(h, x0, x, max_iter, iters, static_cast<cudaStream_t>(stream)))
@@ -1617,6 +2193,12 @@ gc_status gc_check(gc_handle* h, void* stream) {
         if (s != 0) {
             // a failed launch leaves the barrier counter part-way: restart it
             cuda_check(cudaMemsetAsync(h->arena + h->lay.status, 0, 256, st), "status clear");
+            if (h->flow) {   // a failed dataflow product leaves flags and counters part-way
+                cuda_check(cudaMemsetAsync(h->arena + h->lay.fflags, 0, 4 * std::max<int64_t>(1, h->nblocks), st),
+                           "flags clear");
+                cuda_check(cudaMemsetAsync(h->arena + h->lay.fdone, 0, 8 * (h->L + 2), st), "level counters clear");
+                h->epoch = 0;
+            }
             cuda_check(cudaStreamSynchronize(st), "stream synchronize");
             h->bar_base = 0;
             h->tbar_base = 0;
@@ -1638,15 +2220,19 @@ gc_status gc_launch_count(const gc_handle* h, int64_t* launches) {
 gc_status gc_set_schedule(gc_handle* h, int32_t schedule) {
     return guard([&] {
         if (!h) fail(GC_ERR_ARG, "null handle");
-        if (schedule != GC_SCHED_PERSISTENT && schedule != GC_SCHED_PER_LEVEL) fail(GC_ERR_ARG, "unknown schedule");
-        h->schedule = schedule;
+        if (schedule != GC_SCHED_PERSISTENT && schedule != GC_SCHED_PER_LEVEL && schedule != GC_SCHED_DATAFLOW)
+            fail(GC_ERR_ARG, "unknown schedule");
+        if (schedule == GC_SCHED_DATAFLOW && !h->flow)
+            fail(GC_ERR_UNSUPPORTED, "the dataflow schedule serves handles with one value a node (k_max = 1)");
+        // on a dataflow handle the persistent schedule is the dataflow sweep
+        h->schedule = h->flow && schedule == GC_SCHED_PERSISTENT ? GC_SCHED_DATAFLOW : schedule;
     });
 }
 
 gc_status gc_get_schedule(const gc_handle* h, int32_t* schedule) {
     return guard([&] {
         if (!h || !schedule) fail(GC_ERR_ARG, "null argument");
-        *schedule = (h->schedule == GC_SCHED_PERSISTENT && h->coop) ? GC_SCHED_PERSISTENT : GC_SCHED_PER_LEVEL;
+        *schedule = (h->schedule != GC_SCHED_PER_LEVEL && h->coop) ? h->schedule : GC_SCHED_PER_LEVEL;
     });
 }
 
@@ -1666,6 +2252,7 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
         if (!h) fail(GC_ERR_ARG, "null handle");
         if ((!x && h->m > 0) || (!y && h->n > 0)) fail(GC_ERR_ARG, "null x or y");
         check_k(h, k);
+        check_device(h);
         const int64_t need = static_scratch_need(h, k);
         if (need > kStaticScratchBytes)
             fail(GC_ERR_UNSUPPORTED, "gc_matvec_static: this grammar needs " + std::to_string(need) +

@@ -4,10 +4,11 @@
 //   read-only grammar   nodes     int2[sum of padded widths]  child references,
 //                                 each level starting on a 16-node (128 B)
 //                                 boundary and padded to a multiple of 16
-//                       levels    int64[9 (L+2)]   per level k: padded start,
+//                       levels    int64[10 (L+2)]  per level k: padded start,
 //                                 width, roots, first RV slot, first emit chunk,
 //                                 offset in the tail buffer, carried roots,
-//                                 carried other nodes, first carry slot
+//                                 carried other nodes, first carry slot,
+//                                 dataflow blocks of the level
 //                       V         policy[|V|]      value dictionary
 //                       leaf      int32[alpha]     leaf code of terminal p
 //     level emit:       cref      int32[early]     C without the references to
@@ -40,6 +41,11 @@
 //     slice / row:      RVX       value[TB + rho]  leaf table T, then root values
 //                       status    256 B            status word, fixpoint flag, grid-
 //                                                  barrier and tail-group arrival counters
+//   dataflow sweep (one value a node, flow.hpp): nodes holds the block-local
+//   child references; fblk int32[16 blocks] block records, fdeps / fgran
+//   int32 dependency and outlier-granule lists; scratch fb0..fb2 value[buf]
+//   three level buffers, fflags int32[blocks] ready flags, fdone
+//   uint64[L+2] finished blocks per level; no tail and no buf0 / buf1
 //   staging             xs        value[m]         x / y copies for the
 //                       ys        value[n]         host-buffer entry point
 // "value" is k_max elements of the policy's type (float, int64, uint64);
@@ -90,7 +96,8 @@ namespace gcs {
 constexpr int64_t kNodeAlign = 16;        // nodes per 128-byte granule
 constexpr int64_t kEmitChunkSyms = 512;   // references per emit chunk
 constexpr int64_t kLongRowAvg = 128;      // average |C| per row for chunked emits
-constexpr int64_t kLevelRows = 9;         // rows of the level table
+constexpr int64_t kLevelRows = 10;        // rows of the level table
+constexpr int64_t kFlowBlkBytes = 64;     // bytes of a dataflow block record (flow.hpp)
 
 enum EmitMode : int32_t { EMIT_LEVEL = 0, EMIT_SLICE = 1, EMIT_ROWS = 2 };
 
@@ -121,6 +128,12 @@ struct DevLayout {
     int64_t TB;            // leaf-table block length in values
     int32_t vbits;         // bits of the value index inside a leaf code
     EmitMode emit;
+    // dataflow sweep (flow.hpp): one value a node; replaces the tail and the
+    // two level buffers with three level buffers, block records and flags
+    bool flow = false;
+    int64_t fblk, fdeps, fgran;           // grammar part: block records, dependencies, granules
+    int64_t fb0, fb1, fb2, fflags, fdone; // scratch: level buffers, ready flags, per-level counters
+    int64_t n_fblocks, n_fdeps, n_fgran, fbuf_values, final_k0;
 
     bool chunked() const { return emit != EMIT_ROWS; }   // chunk or segment sums, esum
     bool has_rv() const { return emit != EMIT_LEVEL; }
@@ -808,17 +821,32 @@ inline EmitCounts count_level_emit(const Grammar& g, int64_t Lg) {
     return t;
 }
 
-// Sizes of the arena for the device view g (device_view) of a grammar.
-inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
+// Counts of a dataflow block plan (flow.hpp) that size the arena.
+struct FlowCounts {
+    int64_t nblocks = 0, ndeps = 0, ngran = 0, buf_values = 0, final_k0 = 0;
+};
+
+// Sizes of the arena for the device view g (device_view) of a grammar; with
+// fc, for the dataflow sweep of that block plan (every level is swept by the
+// blocks, so there is no tail: grid_levels = L).
+inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max, const FlowCounts* fc = nullptr) {
     DevLayout d{};
     const int64_t L = g.L, C = (int64_t)g.c_ref.size(), A = g.alpha();
     d.value_bytes = policy_elem_bytes(p) * k_max;
     d.vbits = value_bits((int64_t)g.V.size());
     d.TB = leaf_block(A);
     d.emit = emit_mode(g, k_max);
+    d.flow = fc != nullptr;
     d.tail_nodes = d.emit == EMIT_SLICE ? kSliceTailNodes : tail_width(k_max);
-    d.grid_levels = grid_level_count(g, d.tail_nodes);
+    d.grid_levels = d.flow ? L : grid_level_count(g, d.tail_nodes);
     d.tail_total = tail_offsets(g, d.grid_levels)[L + 1];
+    if (d.flow) {
+        d.n_fblocks = fc->nblocks;
+        d.n_fdeps = fc->ndeps;
+        d.n_fgran = fc->ngran;
+        d.fbuf_values = fc->buf_values;
+        d.final_k0 = fc->final_k0;
+    }
     d.n_nodes_padded = 0;
     for (int64_t k = 1; k <= L; ++k) d.n_nodes_padded += pad_nodes(g.lvl_off[k + 1] - g.lvl_off[k]);
     EmitCounts ec;
@@ -847,6 +875,11 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     };
     d.nodes = take(8 * d.n_nodes_padded);
     d.levels = take(8 * kLevelRows * (L + 2));
+    if (d.flow) {
+        d.fblk = take(kFlowBlkBytes * d.n_fblocks);
+        d.fdeps = take(4 * d.n_fdeps);
+        d.fgran = take(4 * d.n_fgran);
+    }
     d.V = take(policy_elem_bytes(p) * std::max<int64_t>(1, (int64_t)g.V.size()));
     d.leaf = take(4 * A);
     if (d.emit == EMIT_LEVEL) {
@@ -871,10 +904,19 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max) {
     }
     d.grammar_bytes = o;
     const int64_t w = g.max_width();
-    d.buf0 = take(d.value_bytes * (d.TB + w));
-    d.buf1 = take(d.value_bytes * (d.TB + w));
-    d.tbuf = take(d.value_bytes * d.tail_total);
-    d.carry = take(d.value_bytes * std::max<int64_t>(1, g.n_carry));
+    if (d.flow) {
+        d.fb0 = take(d.value_bytes * d.fbuf_values);
+        d.fb1 = take(d.value_bytes * d.fbuf_values);
+        d.fb2 = take(d.value_bytes * d.fbuf_values);
+        d.fflags = take(4 * std::max<int64_t>(1, d.n_fblocks));
+        d.fdone = take(8 * (L + 2));
+        d.buf0 = d.buf1 = d.tbuf = d.carry = take(0);
+    } else {
+        d.buf0 = take(d.value_bytes * (d.TB + w));
+        d.buf1 = take(d.value_bytes * (d.TB + w));
+        d.tbuf = take(d.value_bytes * d.tail_total);
+        d.carry = take(d.value_bytes * std::max<int64_t>(1, g.n_carry));
+    }
     if (d.chunked()) d.esum = take(d.value_bytes * d.n_esum);
     if (d.has_rv()) d.RV = take(d.value_bytes * (d.TB + g.n_roots));
     d.status = take(256);

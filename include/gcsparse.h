@@ -228,6 +228,9 @@ gc_status gc_upload(const gc_grammar* g, gc_policy policy, int32_t k_max, void* 
  *       column / row (4k bytes: k / 4 float4 lanes)
  * x and y must not overlap the arena. Deterministic: the same x gives the same
  * y bit for bit (fixed summation order, no atomics).
+ * The device current at the call must be the one that was current at
+ * gc_upload (the arena's device); otherwise GC_ERR_ARG. The same rule holds
+ * for gc_matvec_host, gc_matvec_static, gc_reach and gc_sssp.
  */
 gc_status gc_matvec(gc_handle* h, const void* x, void* y, int32_t k, void* stream);
 
@@ -289,11 +292,24 @@ gc_status gc_launch_count(const gc_handle* h, int64_t* launches);
 
 /* Schedules of the sweep (the same values either way, bit for bit):
  *   GC_SCHED_PERSISTENT  one cooperative kernel per product, levels separated
- *                        by a grid barrier with bounded waits (default; used
- *                        when the device supports cooperative launch)
- *   GC_SCHED_PER_LEVEL   one kernel per level plus one emit kernel, the
- *                        launch sequence of Listing 1 of the pages          */
-enum { GC_SCHED_PERSISTENT = 0, GC_SCHED_PER_LEVEL = 1 };
+ *                        by a grid barrier with bounded waits (default for
+ *                        handles with k_max > 1; used when the device
+ *                        supports cooperative launch)
+ *   GC_SCHED_PER_LEVEL   one kernel per level plus the emit kernels, the
+ *                        launch sequence of Listing 1 of the pages
+ *   GC_SCHED_DATAFLOW    handles with k_max = 1 (one value a node) only, and
+ *                        their default: the levels are cut into blocks of
+ *                        consecutive nodes; one cooperative kernel stages
+ *                        each block's node pairs and the slices of the level
+ *                        below that hold its children in shared memory (bulk
+ *                        copies), and starts a block once the blocks it reads
+ *                        have raised their ready flags (bounded waits), so no
+ *                        grid barrier separates the levels (Lemma 3.3's
+ *                        dependency, block by block); the narrow top levels
+ *                        run as one block in shared memory. Then the emit.
+ *                        On such a handle GC_SCHED_PERSISTENT selects this
+ *                        schedule; on other handles it is GC_ERR_UNSUPPORTED. */
+enum { GC_SCHED_PERSISTENT = 0, GC_SCHED_PER_LEVEL = 1, GC_SCHED_DATAFLOW = 2 };
 gc_status gc_set_schedule(gc_handle* h, int32_t schedule);
 /* The schedule products actually use (PER_LEVEL when cooperative launch is
  * unavailable).                                                             */

@@ -224,6 +224,51 @@ def test_device_plans_pass_host_checks(gcs, k_max):
                 gcs.capi.gc_upload(G._p, pol, k_max, 256, lay["arena_bytes"])
 
 
+def test_dataflow_block_plan(gcs, tmp_path):
+    # tests/native/flow_plan_check.cpp builds the dataflow sweep's block plan
+    # (windows, outlier granules, dependencies, final block) for 4- and 8-byte
+    # values, runs the host checks gc_upload runs, and replays the blocks on
+    # the CPU through their staged-value references, against the direct product
+    import struct
+    import subprocess
+    from grammar_compressed_sparse_gb300 import build as gbuild
+    gbuild.build()
+    objs = [os.path.join(gbuild.BUILD, f + ".o") for f in gbuild.HOST_SOURCES]
+    exe = str(tmp_path / "flow_plan_check")
+    subprocess.run(["g++", "-O2", "-std=c++17", "-fopenmp", "-I", gbuild.INCLUDE, "-I", gbuild.CSRC,
+                    os.path.join(ROOT, "tests", "native", "flow_plan_check.cpp"), *objs, "-o", exe],
+                   check=True, capture_output=True)
+    files = []
+
+    def dump(name, n, m, rp, c, v):
+        path = str(tmp_path / name)
+        with open(path, "wb") as f:
+            f.write(struct.pack("qqq", n, m, int(rp[-1])))
+            f.write(np.asarray(rp, np.int64).tobytes())
+            f.write(np.asarray(c, np.int32).tobytes())
+            f.write(np.asarray(v, np.float32).tobytes())
+        files.append(path)
+
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    dump("slice300.bin", 300, cfg["m"], *gcsynth.genotype_csr(**cfg))                  # many blocks a level
+    dump("small.bin", 1000, 2000, *gcsynth.genotype_csr(**gcsynth.GENO_SMALL))
+    rp, c, v, _ = gcsynth.random_sparse(40, 3000, 0.4, [1.0, -1.0, 0.5], 8)
+    dump("heavy.bin", 40, 3000, rp, c, v)                                               # one final block
+    rp, col = gcsynth.copy_model_graph(nodes=3000, n0=20, d0=15, p_edit=0.05, seed=1)
+    dump("graph.bin", 3000, 3000, rp, col, np.ones(len(col), np.float32))
+    d = np.zeros((9, 700), np.float32)
+    d[:, ::3] = 1.0
+    d[4, 1::3] = 2.0
+    dump("dense.bin", 9, 700, *dense_to_csr(d, np.float32))
+    dump("one.bin", 1, 1, *dense_to_csr(np.full((1, 1), 3.0, np.float32), np.float32))   # no rules
+    out = subprocess.run([exe, *files], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.strip().endswith("OK")
+    # the 300-row slice has regular blocks with windows and granules below its final block
+    first = [ln for ln in out.stdout.splitlines() if ln.startswith("flow vb=4")][0]
+    assert "granules 0 " not in first and "(final from level 1)" not in first
+
+
 def test_slice_plan_and_tile_reduction(gcs, tmp_path):
     # tests/native/slice_plan_check.cpp rebuilds the slice emit's plan for each
     # matrix and replays the device's tile reduction on the CPU (lane runs and
@@ -460,7 +505,7 @@ def test_corrupted_grammar_file_is_rejected(gcs, tmp_path):
 def test_cpu_grammar_sweep_on_the_builders_grammar(gcs):
     # the CPU baseline's W-array sweep reads the library's exported raw
     # grammar: it must give the direct product
-    from oracle.wsweep import GrammarSweep
+    from baselines.wsweep import GrammarSweep
     cfg = dict(gcsynth.GENO_MEDIUM, n=300)
     rp, c, v = gcsynth.genotype_csr(**cfg)
     G = gcs.Grammar(300, cfg["m"], rp, c, v)

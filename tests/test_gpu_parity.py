@@ -210,6 +210,52 @@ def test_schedules_agree_bit_for_bit(gcs, torch):
     assert_f32_parity(y_p, rp, c, v, gcsynth.beta(cfg["m"], seed=3))
 
 
+@pytest.mark.parametrize("policy", ["f32", "i64", "or", "minplus"])
+def test_dataflow_and_per_level_agree(gcs, torch, policy):
+    # one value a node: the dataflow sweep (one cooperative launch, blocks
+    # started by ready flags) and its per-level launch sequence give the same
+    # bits, and both match the oracle; slice emit (long rows) and row emit
+    cfg = dict(gcsynth.GENO_MEDIUM, n=300)
+    rp, c, v = gcsynth.genotype_csr(**cfg)
+    rp2, col2 = gcsynth.copy_model_graph(nodes=3000, n0=20, d0=15, p_edit=0.05, seed=1)
+    for n, m, rp_, c_, v_ in ((300, cfg["m"], rp, c, v), (3000, 3000, rp2, col2, np.ones(len(col2), np.float32))):
+        if policy == "or":
+            v_ = np.ones_like(v_)
+        G = gcs.Grammar(n, m, rp_, c_, v_)
+        eng = gcs.Engine(G, policy, 1)
+        assert eng.schedule == "dataflow"
+        rng = np.random.default_rng(n)
+        if policy == "f32":
+            x = gcsynth.beta(m, seed=9)
+        elif policy == "minplus":
+            x = rng.integers(0, 40, m).astype(np.float32)
+        else:
+            x = rng.integers(-500, 500, m).astype(np.int64) if policy == "i64" else \
+                rng.integers(0, 2**63, m, dtype=np.int64)
+        xd = _dev(torch, x)
+        y_d = eng.matvec(xd).cpu().numpy()
+        assert eng.check() == 0
+        launches_d = eng.launch_count()
+        eng.schedule = "per_level"
+        y_l = eng.matvec(xd).cpu().numpy()
+        assert eng.launch_count() > launches_d
+        eng.schedule = "persistent"              # on this handle: the dataflow schedule
+        assert eng.schedule == "dataflow"
+        np.testing.assert_array_equal(y_d.view(np.uint8), y_l.view(np.uint8))
+        if policy == "f32":
+            assert_f32_parity(y_d, rp_, c_, v_, x)
+        elif policy == "minplus":
+            np.testing.assert_array_equal(y_d.view(np.uint32), direct.matvec_minplus(rp_, c_, v_, x).view(np.uint32))
+        elif policy == "i64":
+            np.testing.assert_array_equal(y_d, direct.matvec_i64(rp_, c_, v_, x))
+        else:
+            np.testing.assert_array_equal(y_d.view(np.uint64), direct.matvec_or(rp_, c_, x.view(np.uint64)))
+        # repeated products on the same handle (the ready flags carry the product number)
+        for _ in range(3):
+            np.testing.assert_array_equal(eng.matvec(xd).cpu().numpy().view(np.uint8), y_d.view(np.uint8))
+        assert eng.check() == 0
+
+
 def test_barrier_timeout_is_reported_not_hung(gcs, torch):
     # CTA 0 skips its first barrier arrival; every other CTA's bounded wait
     # runs out (about a millisecond), the kernel returns with GC_ERR_TIMEOUT

@@ -508,7 +508,7 @@ def test_cpu_grammar_sweep_matches_dense_and_thread_counts():
     # the C W-array sweep over the oracle's own RePair grammar (same symbol
     # encoding as the library's export): equal to the dense product, and the
     # same bits with any number of threads
-    from oracle.wsweep import GrammarSweep
+    from baselines.wsweep import GrammarSweep
     for seed, rp, c, v, dense in _random_cases():
         V, rows = grammar.csrv(rp, c, v)
         if not len(V):
@@ -526,7 +526,7 @@ def test_cpu_grammar_sweep_matches_dense_and_thread_counts():
 
 
 def test_cpu_csr_product_matches_dense():
-    from oracle.wsweep import CsrProduct
+    from baselines.wsweep import CsrProduct
     for seed, rp, c, v, dense in _random_cases():
         x = np.random.default_rng(seed + 2).standard_normal(dense.shape[1])
         p = CsrProduct(rp, c, v)

@@ -1,9 +1,13 @@
 """gc_matvec_static: the product for callers that cannot allocate device memory
 where it runs (their device memory is reserved up front, or they only receive
-input and output buffers). Its scratch is a fixed array inside the library;
-the test checks, through the C ABI, that two calls in a row give what
-gc_matvec gives, within the float32 tolerance of the other parity tests, and
-that a product too large for the array is refused with a clear error.
+input and output buffers). Its scratch is a fixed array inside the library.
+
+Through the C ABI, two calls in a row (the array keeps the previous call's
+contents) must give what gc_matvec gives, bit for bit -- both run the same
+kernels in the same order -- and what the oracle gives: within the float32
+tolerance of the other parity tests for the float32 sum, bit for bit for the
+exact, Boolean and tropical policies. A product too large for the array is
+refused with a clear error.
 
 Kept in its own file so pytest collects it last.
 """
@@ -26,34 +30,65 @@ def torch():
     return t
 
 
-def _within(y_a, y_b, b):
-    return np.all(np.abs(y_a.astype(np.float64) - y_b.astype(np.float64)) <= TOL * b)
+def _inputs(policy, m, k, seed):
+    """x for the policy (numpy), the torch dtype it travels in."""
+    rng = np.random.default_rng(seed)
+    if policy == "f32":
+        return gcsynth.beta(m, seed=seed, k=k)
+    if policy == "minplus":
+        x = rng.integers(0, 50, size=(m,) if k == 1 else (m, k)).astype(np.float32)
+        x[rng.random(x.shape) < 0.1] = np.inf
+        return x
+    if policy == "i64":
+        return rng.integers(-1000, 1000, size=m).astype(np.int64)
+    return rng.integers(0, 2**63, size=m, dtype=np.int64)   # "or": 64 bit lanes
 
 
-@pytest.mark.parametrize("rows,k", [(None, 1), (None, 16), (600, 1)])
-def test_static_scratch_matches_matvec(gcs, torch, rows, k):
-    if rows is None:
-        cfg = gcsynth.GENO_SMALL
+def _oracle_check(policy, rp, c, v, x_np, y):
+    if policy == "f32":
+        y_ref, bound = direct.matvec_f64(rp, c, v, x_np.astype(np.float64))
+        ok, worst = direct.within_tolerance(y, y_ref, bound, TOL)
+        assert ok, worst
+    elif policy == "minplus":
+        assert np.array_equal(y.view(np.uint32), direct.matvec_minplus(rp, c, v, x_np).view(np.uint32))
+    elif policy == "i64":
+        assert np.array_equal(y, direct.matvec_i64(rp, c, v.astype(np.int64), x_np))
     else:
-        cfg = dict(gcsynth.GENO_MEDIUM, n=rows)
+        assert np.array_equal(y.view(np.uint64), direct.matvec_or(rp, c, x_np.view(np.uint64)))
+
+
+CASES = [
+    ("small", "f32", 1, 1), ("small", "f32", 16, 16), ("small", "f32", 16, 4),
+    ("rows600", "f32", 1, 1),
+    ("small", "i64", 1, 1), ("small", "or", 1, 1),
+    ("small", "minplus", 1, 1), ("small", "minplus", 16, 16),
+]
+
+
+@pytest.mark.parametrize("mat,policy,k_max,k", CASES)
+def test_static_scratch_matches_matvec(gcs, torch, mat, policy, k_max, k):
+    cfg = gcsynth.GENO_SMALL if mat == "small" else dict(gcsynth.GENO_MEDIUM, n=600)
     rp, c, v = gcsynth.genotype_csr(**cfg)
+    if policy == "or":
+        v = np.ones_like(v)
     G = gcs.Grammar(cfg["n"], cfg["m"], rp, c, v)
-    eng = gcs.Engine(G, "f32", k)
+    eng = gcs.Engine(G, policy, k_max)
     capi = gcs.capi
     stream = torch.cuda.current_stream()
     shape = (cfg["n"],) if k == 1 else (cfg["n"], k)
+    tdt = torch.float32 if policy in ("f32", "minplus") else torch.int64
     for seed in (11, 12):                       # two calls in a row share the array
-        x_np = gcsynth.beta(cfg["m"], seed=seed, k=k)
+        x_np = _inputs(policy, cfg["m"], k, seed)
         x = torch.from_numpy(x_np).cuda()
-        y_ref = torch.empty(shape, device="cuda")
+        y_ref = torch.empty(shape, dtype=tdt, device="cuda")
         capi.gc_matvec(eng._h, x, y_ref, k, stream)
-        y_st = torch.full(shape, float("nan"), device="cuda")
+        y_st = torch.full(shape, -7, dtype=tdt, device="cuda")
         capi.gc_matvec_static(eng._h, x, y_st, k, stream)
         torch.cuda.synchronize()
         a, b_ = y_st.cpu().numpy(), y_ref.cpu().numpy()
-        assert not np.isnan(a).any()
-        _, bound = direct.matvec_f64(rp, c, v, x_np)
-        assert _within(a, b_, bound)
+        # same kernels, same order of evaluation: the same bits
+        assert np.array_equal(a.view(np.uint8), b_.view(np.uint8))
+        _oracle_check(policy, rp, c, v, x_np, a)
     assert eng.check() == 0
 
 
