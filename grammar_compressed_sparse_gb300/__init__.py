@@ -245,7 +245,7 @@ class LeftEngine:
 def _builder_fingerprint() -> str:
     from . import build as _b
     h = hashlib.sha256()
-    for f in _b.HOST_SOURCES + _b.HEADERS:
+    for f in _b.BUILDER_FILES:
         with open(os.path.join(_b.CSRC, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -22,6 +22,8 @@ LIB = os.path.join(PKG, "libgcsparse.so")
 HOST_SOURCES = ["csrv.cpp", "repair.cpp", "layer.cpp", "capi_host.cpp"]
 CUDA_SOURCES = ["engine.cu", "left.cu"]
 HEADERS = ["common.hpp", "layout.hpp", "flow.hpp", "policy.cuh", "left.hpp"]
+# what a saved grammar depends on (the builder and its file format)
+BUILDER_FILES = HOST_SOURCES + ["common.hpp", "layout.hpp"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 _lock = threading.Lock()

@@ -74,6 +74,7 @@ struct gc_handle {
     int64_t nblocks = 0, final_k0 = 0;
     std::vector<int64_t> lvl_blk;   // first block of each level (L+2)
     uint32_t epoch = 0;
+    const int32_t* conv = nullptr;   // during a device-side fixpoint loop: its converged word
 };
 
 namespace gcs {
@@ -217,6 +218,7 @@ struct SweepArgs {
     int32_t tail_solo;               //   first tail level CTA 0 runs alone (L + 1: none)
     long long timeout;
     int32_t inject;
+    const int32_t* conv;      // fixpoint loop: nonzero once it has converged (then skip), or nullptr
 
     __device__ __forceinline__ int64_t lvl(int row, int k) const { return __ldg(lv + (int64_t)row * L2 + k); }
 };
@@ -941,6 +943,12 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
     using V = typename P::V;
     extern __shared__ __align__(16) unsigned char slice_smem[];
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
+    // a converged fixpoint loop skips the product (one arrival at the grid
+    // barrier, as if the launch had passed it)
+    if (a.conv != nullptr && ld_volatile(a.conv) != 0) {
+        if (coop && threadIdx.x == 0) red_add_release(a.bar, 1ull);
+        return;
+    }
     const bool tail = coop && a.grid_levels < a.L;
     // the first tail_group CTAs run the tail (all of them when the grid is
     // that small), the others the slices
@@ -976,8 +984,10 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
 // windows and outlier granules with bulk copies that complete on the stage's
 // mbarrier -- while 16 compute warps evaluate the previously staged blocks:
 // every child is a shared-memory value, the identity or a leaf evaluated in
-// place; values go to the level buffer (and RV for roots); the block's flag is
-// then released. Blocks are dealt to CTAs round robin (b = CTA, CTA + grid,
+// place; values go to the level buffer (and RV for roots). A warp reports on
+// the stage's `computed` barrier and goes on to the next staged block; warp
+// 17 then releases the block's flag and frees the stage, so the fence and the
+// release stay off the compute path. Blocks are dealt to CTAs round robin (b = CTA, CTA + grid,
 // ...), and a CTA works through its blocks in order; every dependency is an
 // earlier block, so the earliest unfinished block can always proceed (all
 // CTAs are resident: cooperative launch). The final block (the narrow top
@@ -985,7 +995,7 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
 // after the other in shared memory.
 constexpr int kFlowCW = 16;                   // compute warps of a CTA
 constexpr int kFlowCT = 32 * kFlowCW;         // compute threads
-constexpr int kFlowThreads = kFlowCT + 32;    // and the staging warp
+constexpr int kFlowThreads = kFlowCT + 32 * ((int)kFlowStages + 1);   // and kNS staging warps, one publishing warp
 constexpr int kNS = (int)kFlowStages;
 constexpr int kSB = (int)kFlowStageBytes;
 constexpr int LV_NBLK = 9;                    // level table: regular blocks of level k
@@ -995,8 +1005,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)_
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+// 16 bytes from global memory through L2 only (never a stale L1 line)
+__device__ __forceinline__ int4 ld_cg16(const void* p) {
+    int4 v;
+    asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(gaddr(p)));
+    return v;
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
@@ -1040,6 +1058,14 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t* p) {
 __device__ __forceinline__ void st_release_u32(int32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gaddr(p)), "r"(v) : "memory");
 }
+// one fence, then relaxed writes: together a release of both writes
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed_u32(int32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(gaddr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_add(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(gaddr(p)), "l"(v) : "memory");
+}
 
 template <class P>
 struct FlowArgs {
@@ -1069,6 +1095,8 @@ struct FlowArgs {
     int32_t* status;
     long long timeout;
     int32_t inject;
+    const int32_t* conv;      // fixpoint loop: nonzero once it has converged (then skip), or nullptr
+    int32_t nblocks;          // all blocks of the plan
 
     __device__ __forceinline__ int64_t lvl(int row, int k) const { return __ldg(lv + (int64_t)row * L2 + k); }
     __device__ __forceinline__ V* buf(int k) const { return k % 3 == 0 ? fb0 : k % 3 == 1 ? fb1 : fb2; }
@@ -1115,106 +1143,190 @@ __device__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FlowArgs<P>& a) 
     }
 }
 
-// Warp 0: stages this CTA's blocks in order. On a failed wait it records the
-// first iteration it did not stage in *stop and returns; nothing it did not
-// issue is in flight.
+// shared-memory counters: release / acquire at CTA scope
+__device__ __forceinline__ void red_release_cta(int* p, int v) {
+    asm volatile("red.release.cta.shared::cta.add.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// What the compute warps need of a staged block, written by its staging
+// warp (so the compute path reads no block record or level table).
+struct FlowHead {
+    long long out;   // level-buffer address of the block's first node (regular blocks)
+    long long rvo;   // RV address of the block's first node
+    long long prev;  // level buffer of k0 - 1 (regular blocks read their children there)
+    int k0, k1, pb, nn, nr, wl1;
+};
+
+// Per-CTA pipeline state in shared memory.
+struct FlowSync {
+    FlowHead head[kNS];
+    uint64_t full[kNS];    // stage s filled (bulk-copy bytes)
+    uint64_t empty[kNS];   // stage s read by every compute warp (one arrival a warp)
+    uint64_t cbar;         // the compute warps between the final block's levels
+    int done[kNS];         // compute warps finished with stage s, over all its uses
+    int stop;              // first iteration that will never be staged (a wait gave up)
+    int pub;               // blocks published so far
+};
+
+// Staging warp w (w < kNS) owns stage w and stages this CTA's iterations
+// it = w, w + kNS, ...: once its stage is free (every compute warp has read
+// its previous use) it starts the bulk copy of the block's node pairs, then
+// waits for the block's dependencies (the producers' ready flags; level k0 - 2
+// finished, once a level); the final block also waits for every earlier block
+// of the CTA to be published and copies the level below into the stage area.
+// Lane 0's arrival on the stage's barrier, after the waits, lets the phase
+// complete once the copies have landed: the compute warps' child gathers are
+// ordered after the producers' releases (flag acquire, then the barrier). On a
+// failed wait it lowers sy.stop to this iteration, arrives (so the copies it
+// issued can complete), waits for them (bounded) and leaves.
 template <class P>
-__device__ void flow_stage(const FlowArgs<P>& a, unsigned char* fsm, uint64_t* full, uint64_t* empty,
-                           volatile int* stop) {
+__device__ void flow_stage(const FlowArgs<P>& a, unsigned char* fsm, FlowSync& sy, int w) {
     using V = typename P::V;
-    constexpr int G = 16 / (int)sizeof(V);
     const int lane = threadIdx.x & 31;
     const uint64_t first = l2_evict_first();
-    int it = 0;
-    // before the warp leaves, the copies it issued (uses it-kNS .. it-1 of
-    // the stages) have landed: nothing is in flight when the CTA exits
+    int lvl_ok = -1;      // highest level k found finished (levels only grow)
+    int last = -1;        // last iteration this warp issued
     auto drain = [&]() {
-        if (lane == 0)
-            for (int i = it > kNS ? it - kNS : 0; i < it; ++i)
-                if (!mbar_wait(&full[i % kNS], (uint32_t)(i / kNS) & 1u, a)) break;
+        if (lane == 0 && last >= 0) mbar_wait(&sy.full[w], (uint32_t)(last / kNS) & 1u, a);
         __syncwarp();
     };
-    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
-        const int s = it % kNS;
+    int it = w;
+    for (int b = a.b_begin + (int)blockIdx.x + w * (int)gridDim.x; b < a.b_end; b += kNS * (int)gridDim.x, it += kNS) {
         const int32_t fv = lane < (int)kFlowBlkInts ? __ldg(a.blk + (int64_t)b * kFlowBlkInts + lane) : 0;
+        // every lane reads every field here: F is a full-warp shuffle, so it
+        // is never called inside a lane-dependent branch
         auto F = [&](int i) { return __shfl_sync(0xffffffffu, fv, i); };
-        const int k0 = F(FB_K0);
+        const int k0 = F(FB_K0), doff = F(FB_DOFF), nd = F(FB_NDEP), pb = F(FB_PB), wl1 = F(FB_WL1);
+        const int node0 = F(FB_NODE0), k1 = F(FB_K1), nn = F(FB_NNODES), slot0 = F(FB_SLOT0);
         const bool fin = b == a.final_block;
-        bool ok = true;
-        // the staging buffer is free once the compute warps released its last
-        // use (the final block needs every buffer)
-        if (lane == 0) {
-            if (fin)
-                for (int i = it > kNS ? it - kNS : 0; i < it && ok; ++i) ok = mbar_wait(&empty[i % kNS], (uint32_t)(i / kNS) & 1u, a);
-            else if (it >= kNS)
-                ok = mbar_wait(&empty[s], (uint32_t)(it / kNS - 1) & 1u, a);
-        }
-        if (a.waits) {
-            const int doff = F(FB_DOFF), nd = F(FB_NDEP);
-            for (int j = lane; j < nd && ok; j += 32) ok = wait_flag(a.flags + __ldg(a.deps + doff + j), a.epoch, a);
-            if (lane == 0 && ok && !fin && k0 >= 3)
-                ok = wait_count(a.done + (k0 - 2), (unsigned long long)a.epoch * (unsigned long long)a.lvl(LV_NBLK, k0 - 2), a);
+        // (ok is the same in every lane before each branch that holds a shuffle)
+        bool ok = __all_sync(0xffffffffu, ld_volatile(&sy.stop) > it);
+        // the stage is free once every compute warp has read its previous use
+        // (this warp issued that use itself, so the phase is not ambiguous);
+        // the final block takes every stage: every earlier block of the CTA
+        // must have been published (so computed)
+        if (lane == 0 && ok && it >= kNS) ok = mbar_wait(&sy.empty[w], (uint32_t)(it / kNS - 1) & 1u, a);
+        if (lane == 0 && ok && fin) {
+            const long long t0 = clock64();
+            for (unsigned n = 0; ld_acquire_cta(&sy.pub) < it; ++n)
+                if ((n & 63u) == 63u && (ld_volatile(&sy.stop) <= it || wait_give_up(a, t0))) {
+                    ok = false;
+                    break;
+                }
         }
         if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) *stop = it;
+            if (lane == 0) atomicMin(&sy.stop, it);
             drain();
             return;
         }
-        fence_proxy_async_global();
-        unsigned char* base = fin ? fsm : fsm + s * kSB;
-        // every lane reads every field here: F is a full-warp shuffle, so it
-        // is never called inside a lane-dependent branch
-        const int pb = F(FB_PB), wl1 = F(FB_WL1), wl2 = F(FB_WL2), ng = F(FB_NGRAN), goff = F(FB_GOFF);
-        const int node0 = F(FB_NODE0), ws1 = F(FB_WS1), ws2 = F(FB_WS2);
-        if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)pb + (uint32_t)(wl1 + wl2 + ng * G) * (uint32_t)sizeof(V));
-        __syncwarp();
-        const V* prev = a.buf(k0 + 2);   // level k0 - 1
-        V* vals = reinterpret_cast<V*>(base + pb);
-        if (lane == 0) bulk_g2s_hint(base, a.pairs + node0, (uint32_t)pb, &full[s], first);
-        if (lane == 1 && wl1 > 0) bulk_g2s(vals, prev + ws1, (uint32_t)(wl1 * sizeof(V)), &full[s]);
-        if (lane == 2 && wl2 > 0) bulk_g2s(vals + wl1, prev + ws2, (uint32_t)(wl2 * sizeof(V)), &full[s]);
-        for (int j = lane; j < ng; j += 32)
-            bulk_g2s(vals + wl1 + wl2 + j * G, prev + __ldg(a.gran + goff + j), 16u, &full[s]);
+        unsigned char* base = fin ? fsm : fsm + w * kSB;
+        if (lane == 0) {
+            FlowHead& h = sy.head[w];
+            h.k0 = k0;
+            h.k1 = k1;
+            h.pb = pb;
+            h.nn = nn;
+            h.wl1 = wl1;
+            if (!fin) {
+                const int64_t nroots = a.lvl(LV_ROOTS, k0);
+                h.nr = (int)(nroots - slot0 < 0 ? 0 : nroots - slot0 < nn ? nroots - slot0 : nn);
+                h.out = (long long)(a.buf(k0) + slot0);
+                h.rvo = (long long)(a.rv + a.TB + a.lvl(LV_ROFF, k0) + slot0);
+                h.prev = (long long)a.buf(k0 + 2);   // level k0 - 1
+            }
+            fence_proxy_async_shared();   // earlier generic reads of the stage before the copies' writes
+            mbar_expect_tx_only(&sy.full[w], (uint32_t)pb + (uint32_t)(fin ? wl1 * (int)sizeof(V) : 0));
+            bulk_g2s_hint(base, a.pairs + node0, (uint32_t)pb, &sy.full[w], first);
+        }
+        last = it;
+        if (a.waits) {
+            for (int j = lane; j < nd && ok; j += 32) ok = wait_flag(a.flags + __ldg(a.deps + doff + j), a.epoch, a);
+            if (lane == 0 && ok && !fin && k0 >= 3 && k0 - 2 > lvl_ok) {
+                ok = wait_count(a.done + (k0 - 2), (unsigned long long)a.epoch * (unsigned long long)a.lvl(LV_NBLK, k0 - 2), a);
+                if (ok) lvl_ok = k0 - 2;
+            }
+            lvl_ok = __shfl_sync(0xffffffffu, lvl_ok, 0);
+        }
+        __syncwarp();   // every lane's flag acquires before lane 0's arrival below
+        const bool all_ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0) {
+            if (!all_ok) atomicMin(&sy.stop, it);
+            else if (fin && wl1 > 0) {
+                fence_proxy_async_global();   // the producers' values (acquired above) before the copy reads them
+                bulk_g2s(base + pb, a.buf(k0 + 2), (uint32_t)(wl1 * sizeof(V)), &sy.full[w]);
+            }
+            // (on a failed wait the final block's window is not copied: its
+            // bytes stay expected, the phase never completes, and the drain
+            // below gives up after its bounded wait with nothing in flight)
+            mbar_arrive(&sy.full[w]);
+        }
+        if (!all_ok) {
+            drain();
+            return;
+        }
     }
     drain();
 }
 
-// Warps 1..16: evaluate this CTA's staged blocks in order. They synchronise
-// among themselves on the mbarrier cbar (every compute thread arrives; the
-// waits are bounded, so a thread that gave up cannot leave the others stuck).
+// Lane 0 of a warp waits (bounded) for phase `parity` of bar, giving up when
+// sy.stop says the stage will never be filled (stop_at: this block's
+// iteration; -1: do not look at stop); the whole warp gets the answer.
 template <class P>
-__device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, uint64_t* full, uint64_t* empty,
-                             uint64_t* cbar, volatile int* stop) {
-    using V = typename P::V;
-    constexpr int G = 16 / (int)sizeof(V);
-    constexpr int U = 4;   // nodes a thread evaluates together
-    const int ct = (int)threadIdx.x - 32;
-    const uint64_t keep = l2_evict_last();
-    uint32_t cphase = 0;
-    auto csync = [&]() {
-        mbar_arrive(cbar);
-        return mbar_wait(cbar, cphase++ & 1u, a);
-    };
-    int it = 0;
-    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
-        const int s = it % kNS;
-        {
-            // wait for the stage; the staging warp's own waits are bounded, so
-            // a stage it never issues shows up in *stop
-            const long long t0 = clock64();
-            for (unsigned n = 0;; ++n) {
-                if (mbar_try_wait(&full[s], (uint32_t)(it / kNS) & 1u)) break;
-                if ((n & 63u) == 63u) {
-                    if (*stop <= it) return;
-                    if (clock64() - t0 > 4 * a.timeout) {
-                        atomicCAS(a.status, 0, (int32_t)GC_ERR_TIMEOUT);
-                        return;
-                    }
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const FlowSync& sy, int stop_at,
+                                          long long limit, const FlowArgs<P>& a) {
+    const int lane = threadIdx.x & 31;
+    int ok = 1;
+    if (lane == 0) {
+        const long long t0 = clock64();
+        for (unsigned n = 0;; ++n) {
+            if (mbar_try_wait(bar, parity)) break;
+            if ((n & 63u) == 63u) {
+                if (stop_at >= 0 && ld_volatile(&sy.stop) <= stop_at) {
+                    ok = 0;
+                    break;
+                }
+                if (clock64() - t0 > limit) {
+                    atomicCAS(a.status, 0, (int32_t)GC_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
                 }
             }
         }
-        const int32_t* f = a.blk + (int64_t)b * kFlowBlkInts;
-        const int k0 = __ldg(f + FB_K0), pb = __ldg(f + FB_PB);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();   // orders the other lanes' reads after lane 0's acquire
+    return ok != 0;
+}
+
+// The compute warps (16): evaluate this CTA's staged blocks in order. Each
+// warp takes its share of a block's nodes, then reports -- an arrival on the
+// stage's `empty` barrier (the staging warp may refill it) and a count in
+// sy.done (the publishing warp may release the block) -- and moves on to the
+// next staged block at once; warps of one CTA may be on different blocks.
+// Only the final block's levels need the compute warps together, on cbar.
+template <class P>
+__device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, FlowSync& sy, int ct) {
+    using V = typename P::V;
+    constexpr int G = 16 / (int)sizeof(V);
+    constexpr int U = 8;   // nodes a thread evaluates together (their child loads in flight at once)
+    const int lane = (int)threadIdx.x & 31;
+    const uint64_t keep = l2_evict_last();
+    uint32_t cphase = 0;
+    int it = 0;
+    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
+        const int s = it % kNS;
+        if (!warp_wait(&sy.full[s], (uint32_t)(it / kNS) & 1u, sy, it, 4 * a.timeout, a)) return;
+        const FlowHead& h = sy.head[s];
+        const int k0 = h.k0, pb = h.pb;
         const bool fin = b == a.final_block;
         unsigned char* base = fin ? fsm : fsm + s * kSB;
         const int2* pr = reinterpret_cast<const int2*>(base);
@@ -1223,11 +1335,14 @@ __device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, uint64_t*
             return c >= 0 ? vals[c] : c == -1 ? P::identity() : flow_leaf<P>(a, (uint32_t)(-2 - c));
         };
         if (!fin) {
-            const int nn = __ldg(f + FB_NNODES), slot0 = __ldg(f + FB_SLOT0);
-            const int64_t nroots = a.lvl(LV_ROOTS, k0);
-            const int nr = (int)(nroots - slot0 < 0 ? 0 : nroots - slot0 < nn ? nroots - slot0 : nn);
-            V* out = a.buf(k0) + slot0;
-            V* rvo = a.rv + a.TB + a.lvl(LV_ROFF, k0) + slot0;
+            const int nn = h.nn, nr = h.nr;
+            V* out = reinterpret_cast<V*>(h.out);
+            V* rvo = reinterpret_cast<V*>(h.rvo);
+            const V* prev = reinterpret_cast<const V*>(h.prev);
+            // children: slots of level k0 - 1 in its level buffer (through L1/L2)
+            auto gchild = [&](int32_t c) -> V {
+                return c >= 0 ? prev[c] : c == -1 ? P::identity() : flow_leaf<P>(a, (uint32_t)(-2 - c));
+            };
             for (int i0 = ct; i0 < nn; i0 += U * kFlowCT) {
                 int2 c[U];
 #pragma unroll
@@ -1235,8 +1350,8 @@ __device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, uint64_t*
                 V va[U], vb[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    va[u] = child(c[u].x);
-                    vb[u] = child(c[u].y);
+                    va[u] = gchild(c[u].x);
+                    vb[u] = gchild(c[u].y);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -1250,9 +1365,10 @@ __device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, uint64_t*
             }
         } else {
             // levels k0..k1 one after the other; level k's values follow the
-            // window (and the levels before it) in shared memory
-            const int k1 = __ldg(f + FB_K1);
-            int own = __ldg(f + FB_WL1);
+            // window (and the levels before it) in shared memory; between
+            // levels every compute warp reports on cbar and waits for the rest
+            const int k1 = h.k1;
+            int own = h.wl1;
             const int64_t start0 = a.lvl(LV_START, k0);
             for (int k = k0; k <= k1; ++k) {
                 const int w = (int)a.lvl(LV_W, k), nr = (int)a.lvl(LV_ROOTS, k);
@@ -1265,22 +1381,46 @@ __device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, uint64_t*
                     if (i < nr) st_keep(rvo + i, v, keep);
                 }
                 own += (w + G - 1) / G * G;
-                if (!csync()) return;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sy.cbar);
+                if (!warp_wait(&sy.cbar, cphase++ & 1u, sy, -1, a.timeout, a)) return;
             }
         }
-        if (!csync()) return;
-        if (ct == 0) {
-            // publish: every compute thread's writes of this block are ordered
-            // before the flag by the barrier above (arrive releases, wait acquires) (test-only injection: CTA 0
-            // never publishes its first block)
-            if (!(a.inject == 1 && a.waits && blockIdx.x == 0 && it == 0)) {
-                fence_proxy_async_global();
-                __threadfence();
-                st_release_u32(a.flags + b, a.epoch);
-                if (!fin) red_add_release(a.done + k0, 1ull);
-            }
-            mbar_arrive(&empty[s]);
+        __syncwarp();   // the warp's reads and writes before lane 0's report
+        if (lane == 0) {
+            mbar_arrive(&sy.empty[s]);
+            red_release_cta(&sy.done[s], 1);
         }
+    }
+}
+
+// The publishing warp, one lane: releases this CTA's blocks in order once
+// every compute warp has counted it done -- the block's ready flag (and its
+// level's count) -- off the compute warps' path.
+template <class P>
+__device__ void flow_publish(const FlowArgs<P>& a, FlowSync& sy) {
+    if ((threadIdx.x & 31) != 0) return;
+    int it = 0;
+    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
+        const int s = it % kNS, want = kFlowCW * (it / kNS + 1);   // sy.done only grows
+        const long long t0 = clock64();
+        for (unsigned n = 0; ld_acquire_cta(&sy.done[s]) < want; ++n)
+            if ((n & 63u) == 63u) {
+                if (ld_volatile(&sy.stop) <= it) return;
+                if (clock64() - t0 > 4 * a.timeout) {
+                    atomicCAS(a.status, 0, (int32_t)GC_ERR_TIMEOUT);
+                    return;
+                }
+            }
+        // (test-only injection: CTA 0 never publishes its first block)
+        if (!(a.inject == 1 && a.waits && blockIdx.x == 0 && it == 0)) {
+            // one gpu-scope fence releases the block's values (ordered before
+            // it by the compute warps' counts, acquired above) with both writes
+            fence_acq_rel_gpu();
+            st_relaxed_u32(a.flags + b, a.epoch);
+            if (b != a.final_block) red_relaxed_add(a.done + __ldg(a.blk + (int64_t)b * kFlowBlkInts + FB_K0), 1ull);
+        }
+        st_release_cta(&sy.pub, it + 1);   // the final block's staging warp waits on it
     }
 }
 
@@ -1288,17 +1428,33 @@ template <class P>
 __global__ void __launch_bounds__(kFlowThreads, 1) flow_kernel(const FlowArgs<P> a) {
     using V = typename P::V;
     extern __shared__ __align__(128) unsigned char fsm[];
-    __shared__ __align__(8) uint64_t full[kNS], empty[kNS], cbar;
-    __shared__ volatile int s_stop;
+    __shared__ __align__(8) FlowSync sy;
     // an unread earlier timeout: do nothing
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
+    // a converged fixpoint loop skips the product; the level counters still
+    // advance by the blocks of this launch, as if they had run, so that the
+    // next product's waits stay consistent
+    if (a.conv != nullptr && ld_volatile(a.conv) != 0) {
+        if (blockIdx.x == 0 && a.waits) {
+            for (int k = (int)threadIdx.x; k < a.L2; k += (int)blockDim.x) {
+                const int64_t nb = k >= 1 && k < a.L2 - 1 ? a.lvl(LV_NBLK, k) : 0;
+                if (nb > 0) red_add_release(a.done + k, (unsigned long long)nb);
+            }
+        } else if (blockIdx.x == 0 && threadIdx.x == 0 && a.b_end > a.b_begin && a.b_begin != a.final_block) {
+            red_add_release(a.done + __ldg(a.blk + (int64_t)a.b_begin * kFlowBlkInts + FB_K0),
+                            (unsigned long long)(a.b_end - a.b_begin));
+        }
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&sy.full[s], 1);
+            mbar_init(&sy.empty[s], kFlowCW);
+            sy.done[s] = 0;
         }
-        mbar_init(&cbar, kFlowCT);
-        s_stop = 0x7fffffff;
+        mbar_init(&sy.cbar, kFlowCW);
+        sy.stop = 0x7fffffff;
+        sy.pub = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // T[0] = identity, T[p+1] = V[l_p] (x) x[j_p] in front of RV (the emit's
@@ -1309,8 +1465,10 @@ __global__ void __launch_bounds__(kFlowThreads, 1) flow_kernel(const FlowArgs<P>
             a.rv[i] = i == 0 ? P::identity() : flow_leaf<P>(a, (uint32_t)__ldg(a.leaf + (i - 1)));
     }
     __syncthreads();
-    if (threadIdx.x < 32) flow_stage<P>(a, fsm, full, empty, &s_stop);
-    else flow_compute<P>(a, fsm, full, empty, &cbar, &s_stop);
+    const int warp = (int)threadIdx.x >> 5;
+    if (warp < kNS) flow_stage<P>(a, fsm, sy, warp);
+    else if (warp < kNS + kFlowCW) flow_compute<P>(a, fsm, sy, (int)threadIdx.x - 32 * kNS);
+    else flow_publish<P>(a, sy);
 }
 
 // ---------------------------------------------------------------- per-level schedule
@@ -1347,6 +1505,7 @@ __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a
 // phase 1: the chunked emits' row sums
 template <class P>
 __global__ void __launch_bounds__(kThreads, 1) emit_kernel(const SweepArgs<P> a, int phase) {
+    if (a.conv != nullptr && ld_volatile(a.conv) != 0) return;   // a converged fixpoint loop
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (a.emode == EMIT_ROWS) {
@@ -1370,6 +1529,10 @@ struct MinUpdate {
     __device__ __forceinline__ static T apply(T u, T v) { return fminf(u, v); }
 };
 
+// Fixpoint control words (in the status block): ctl[0] changed in this
+// step, ctl[1] converged, ctl[2] CTAs of this step finished, ctl[3] the
+// product count at convergence. With ctl[1] set every later step (and, in the
+// dataflow products, every later product) does nothing.
 template <class U>
 __global__ void __launch_bounds__(kThreads)
 update_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y, int64_t n,
@@ -1383,6 +1546,42 @@ update_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y
         }
     }
     if (__syncthreads_or(ch) && threadIdx.x == 0) *changed = 1;
+}
+
+// The same step for a loop that runs on without the host: the last CTA to
+// finish reads the changed word; if nothing changed, the loop has converged
+// at product `it` (recorded in ctl[3]); it then clears the step's words.
+template <class U>
+__global__ void __launch_bounds__(kThreads)
+update_loop_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y, int64_t n,
+                   int32_t* __restrict__ ctl, int32_t it) {
+    __shared__ int s_last;
+    if (ld_volatile(ctl + 1) != 0) return;   // converged at an earlier step
+    int ch = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const typename U::T u = x[i], v = U::apply(u, y[i]);
+        if (v != u) {
+            x[i] = v;
+            ch = 1;
+        }
+    }
+    const int any = __syncthreads_or(ch);
+    if (threadIdx.x == 0) {
+        if (any) atomicOr(ctl, 1);
+        __threadfence();
+        s_last = atomicAdd(ctl + 2, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last && threadIdx.x == 0) {
+        __threadfence();
+        if (ld_volatile(ctl) == 0) {
+            ctl[3] = it;
+            ctl[1] = 1;
+        }
+        ctl[0] = 0;
+        ctl[2] = 0;
+        __threadfence();
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1444,6 +1643,7 @@ SweepArgs<P> make_args(gc_handle* h, const void* x, void* y) {
     a.bar_base = h->bar_base;
     a.timeout = h->timeout_cycles;
     a.inject = h->inject;
+    a.conv = h->conv;
     a.tail_group = 1;
     a.tail_solo = h->L + 1;
     return a;
@@ -1603,6 +1803,8 @@ FlowArgs<P> make_flow_args(const gc_handle* h, const SweepArgs<P>& a, const Flow
     f.status = a.status;
     f.timeout = a.timeout;
     f.inject = a.inject;
+    f.conv = a.conv;
+    f.nblocks = (int32_t)h->nblocks;
     return f;
 }
 
@@ -1795,6 +1997,45 @@ bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32
         cuda_check(cudaMemcpyAsync(x, x0, n * sizeof(T), cudaMemcpyDeviceToDevice, st), "x0 copy");
     int32_t it = 0, done = 0;
     int64_t launches = 0;
+    if (h->flow) {
+        // the loop runs on the device: products are enqueued in batches of 1,
+        // 2, 4, 8, ... without a host round trip in between; the update
+        // kernel decides convergence (ctl, in the status block) and every
+        // kernel enqueued after it returns at once. One stream synchronise
+        // per batch reads the converged word.
+        int32_t* ctl = status + 4;
+        cuda_check(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
+        h->conv = ctl + 1;
+        int32_t batch = 1, result = -1;
+        while (it < max_iter && !done) {
+            const int32_t nb = std::min(batch, max_iter - it);
+            for (int32_t j = 0; j < nb; ++j) {
+                ++it;
+                dispatch_product(h, x, yv, 1, st);
+                launches += h->launches;
+                update_loop_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, ctl, it);
+                ++launches;
+            }
+            cuda_check(cudaGetLastError(), "kernel launch");
+            int32_t w[4] = {0, 0, 0, 0};
+            cuda_check(cudaMemcpyAsync(w, ctl, 16, cudaMemcpyDeviceToHost, st), "loop words read");
+            cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+            if (w[1]) {
+                done = 1;
+                result = w[3];
+            }
+            batch = std::min(batch * 2, 8);
+        }
+        h->conv = nullptr;
+        h->launches = launches;
+        cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
+        if (!done) {
+            int32_t sw = GC_ERR_NOT_CONVERGED;
+            cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
+        }
+        cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+        return done != 0;
+    }
     while (it < max_iter) {
         ++it;
         cuda_check(cudaMemsetAsync(changed, 0, 4, st), "flag clear");

@@ -3,29 +3,22 @@
 //
 // The level-synchronous sweep of Sec. 4.3 evaluates level k from level k-1
 // only (Lemma 3.3), and any order within a level is correct (Lemma 3.1). The
-// packed order sorts each level by the first column of a node's expansion
-// (roots first), so the children of a run of consecutive level-k nodes lie
-// in two narrow slot ranges of level k-1: one among its roots, one among its
-// other nodes. The dataflow sweep cuts every level into blocks of consecutive
-// nodes and gives each block
-//   * up to two windows: slot ranges of level k-1 that hold almost all of its
-//     children, copied into shared memory with one bulk copy each;
-//   * outlier granules: 16-byte pieces of level k-1 around the few children
-//     outside the windows, copied the same way;
-//   * its dependencies: the level k-1 blocks that write any of those slots.
-// A block starts once its dependencies have published their values (per-block
-// ready flags instead of a grid barrier per level). Every child reference of
-// the block is re-encoded as an index into the block's staged values, so a
-// node reads its two children from shared memory.
+// dataflow sweep cuts every level into blocks of consecutive nodes (4,096 at
+// most) and gives each block the list of blocks of level k-1 that write its
+// children's slots: its dependencies. A block starts once its dependencies
+// have published their values (per-block ready flags instead of a grid
+// barrier per level); its node pairs are staged in shared memory by one bulk
+// copy, and its nodes gather their children from the level buffer of k-1.
 //
 // The narrow top levels form one final block: the whole level below them is
-// its window, and the block computes its levels one after the other inside
-// shared memory, where the top levels' values stay.
+// copied into shared memory, and the block computes its levels one after the
+// other there, where the top levels' values stay.
 //
 // Node references in the uploaded pair array (one int2 per padded node, the
 // layout of the packed grammar):
-//   c >= 0   index into the block's staged values (window 1, window 2, outlier
-//            granules, then in the final block its own levels' values)
+//   c >= 0   regular block: slot c of level k-1 (in its level buffer);
+//            final block: index into its staged values (the level below,
+//            then its own levels' values)
 //   c == -1  the combine identity (second child of a pass-through, Sec. 4.2)
 //   c <= -2  a terminal, as its leaf code q = -c - 2 = column << vbits | value
 //            index, evaluated in place as V[l] (x) x[j]
@@ -43,11 +36,8 @@
 namespace gcs {
 
 constexpr int64_t kFlowStages = 4;              // staging buffers per CTA
-constexpr int64_t kFlowStageBytes = 48 << 10;   // shared memory of one staging buffer
-constexpr int64_t kFlowMaxNodes = 2048;         // nodes of a regular block
-constexpr int64_t kFlowMaxGran = 256;           // outlier granules of a block
-constexpr int64_t kFlowMinNodes = 16;           // smallest block when windows do not fit
-constexpr double kFlowCover = 0.98;             // share of a region's children a window holds
+constexpr int64_t kFlowMaxNodes = 4096;         // nodes of a regular block (a multiple of 16)
+constexpr int64_t kFlowStageBytes = 8 * kFlowMaxNodes;   // a staging buffer: one block's node pairs
 constexpr int64_t kFlowBlkInts = 16;            // ints per block record
 
 // Fields of a block record (int32 each).
@@ -114,26 +104,8 @@ inline int64_t flow_final_level(const Grammar& g, int64_t value_bytes) {
     return k0;
 }
 
-// Shortest run of sorted v holding at least ceil(q * n) of its entries: [lo, hi].
-inline void flow_cover(const std::vector<int32_t>& v, double q, int64_t& lo, int64_t& hi) {
-    const int64_t n = (int64_t)v.size();
-    if (n == 0) {
-        lo = 0;
-        hi = -1;
-        return;
-    }
-    int64_t need = (int64_t)std::ceil(q * (double)n);
-    need = std::min(std::max<int64_t>(need, 1), n);
-    int64_t best = 0;
-    for (int64_t i = 0; i + need - 1 < n; ++i)
-        if (v[i + need - 1] - v[i] < v[best + need - 1] - v[best]) best = i;
-    lo = v[best];
-    hi = v[best + need - 1];
-}
-
 inline FlowPlan plan_flow(const Grammar& g, int64_t value_bytes) {
     const int64_t L = g.L, G = flow_granule(value_bytes);
-    auto rdn = [&](int64_t s) { return s / G * G; };
     auto rup = [&](int64_t s) { return (s + G - 1) / G * G; };
     auto width = [&](int64_t k) { return g.lvl_off[k + 1] - g.lvl_off[k]; };
     auto rup2 = [](int64_t s) { return (s + 1) / 2 * 2; };
@@ -151,112 +123,31 @@ inline FlowPlan plan_flow(const Grammar& g, int64_t value_bytes) {
         const int64_t q = ((int64_t)g.term_col[t] << vbits) | g.term_vidx[t];
         return (int32_t)(-2 - q);
     };
-    std::vector<int64_t> prev_slot0, cur_slot0;   // first slot of each block of level k-1, k
-    int64_t prev_b0 = 0;                          // first block id of level k-1
-    std::vector<int32_t> r, o, gr, dl;
+    std::vector<int32_t> dl;
     for (int64_t k = 1; k <= L; ++k) {
         p.lvl_blk[k] = p.nblocks;
         if (k >= p.final_k0) break;
-        const int64_t w = width(k), R = k > 1 ? g.lvl_roots[k - 1] : 0, wprev = k > 1 ? width(k - 1) : 0;
+        const int64_t w = width(k), b_prev = k > 1 ? p.lvl_blk[k - 1] : 0;
         const int32_t* kids = g.nodes.data() + 2 * g.lvl_off[k];
-        cur_slot0.clear();
-        // producer blocks of level k-1 for the slots [a, b)
-        auto deps_of = [&](int64_t a, int64_t b) {
-            a = std::max<int64_t>(a, 0);
-            b = std::min(b, wprev);
-            if (a >= b) return;
-            int64_t i = std::upper_bound(prev_slot0.begin(), prev_slot0.end(), a) - prev_slot0.begin() - 1;
-            for (; i < (int64_t)prev_slot0.size() && prev_slot0[i] < b; ++i) dl.push_back((int32_t)(prev_b0 + i));
-        };
-        for (int64_t i = 0; i < w;) {
-            int64_t S = std::min(kFlowMaxNodes, w - i);
-            int64_t ws1 = 0, we1 = 0, ws2 = 0, we2 = 0, bytes = 0;
-            for (;;) {
-                r.clear();
-                o.clear();
-                for (int64_t t = 2 * i; t < 2 * (i + S); ++t) {
-                    const int32_t c = kids[t];
-                    if (c >= 0) (c < R ? r : o).push_back(c);
-                }
-                std::sort(r.begin(), r.end());
-                std::sort(o.begin(), o.end());
-                int64_t lo, hi;
-                flow_cover(r, kFlowCover, lo, hi);
-                ws1 = rdn(lo);
-                we1 = hi >= lo ? rup(hi + 1) : ws1;
-                flow_cover(o, kFlowCover, lo, hi);
-                ws2 = rdn(lo);
-                we2 = hi >= lo ? rup(hi + 1) : ws2;
-                if (we1 > ws2 && we2 > ws1) {   // rounding made them meet: one window
-                    ws1 = std::min(ws1, ws2);
-                    we1 = std::max(we1, we2);
-                    ws2 = we2 = 0;
-                }
-                auto outside = [&](int64_t c) { return !(c >= ws1 && c < we1) && !(c >= ws2 && c < we2); };
-                gr.clear();
-                for (int32_t c : r)
-                    if (outside(c)) gr.push_back((int32_t)rdn(c));
-                for (int32_t c : o)
-                    if (outside(c)) gr.push_back((int32_t)rdn(c));
-                std::sort(gr.begin(), gr.end());
-                gr.erase(std::unique(gr.begin(), gr.end()), gr.end());
-                const int64_t vals = (we1 - ws1) + (we2 - ws2) + (int64_t)gr.size() * G;
-                bytes = rup2(S) * 8 + vals * value_bytes;
-                if ((bytes <= kFlowStageBytes && (int64_t)gr.size() <= kFlowMaxGran) || S <= kFlowMinNodes) break;
-                S = std::max<int64_t>(kFlowMinNodes, S / 2 / kNodeAlign * kNodeAlign);
-            }
-            if (bytes > kFlowStageBytes || (int64_t)gr.size() > kFlowMaxGran) {
-                // the smallest block still does not fit: no windows, every child a granule
-                ws1 = we1 = ws2 = we2 = 0;
-                gr.clear();
-                for (int64_t t = 2 * i; t < 2 * (i + S); ++t)
-                    if (kids[t] >= 0) gr.push_back((int32_t)rdn(kids[t]));
-                std::sort(gr.begin(), gr.end());
-                gr.erase(std::unique(gr.begin(), gr.end()), gr.end());
-                bytes = rup2(S) * 8 + (int64_t)gr.size() * G * value_bytes;
-                if (bytes > kFlowStageBytes || (int64_t)gr.size() > kFlowMaxGran)
-                    fail(GC_ERR_UNSUPPORTED, "dataflow plan: a block does not fit its staging buffer");
-            }
-            // dependencies
+        for (int64_t i = 0; i < w; i += kFlowMaxNodes) {
+            const int64_t S = std::min(kFlowMaxNodes, w - i);
             dl.clear();
-            deps_of(ws1, we1);
-            deps_of(ws2, we2);
-            for (int32_t s : gr) deps_of(s, s + G);
-            std::sort(dl.begin(), dl.end());
-            dl.erase(std::unique(dl.begin(), dl.end()), dl.end());
-            // re-encode the block's child references
-            const int64_t W1 = we1 - ws1, W2 = we2 - ws2;
             for (int64_t t = 2 * i; t < 2 * (i + S); ++t) {
                 const int32_t c = kids[t];
-                int32_t e;
-                if (c == -1) {
-                    e = -1;
-                } else if (c <= -2) {
-                    e = leaf_ref(c);
-                } else if (c >= ws1 && c < we1) {
-                    e = (int32_t)(c - ws1);
-                } else if (c >= ws2 && c < we2) {
-                    e = (int32_t)(W1 + c - ws2);
-                } else {
-                    const int64_t j = std::lower_bound(gr.begin(), gr.end(), (int32_t)rdn(c)) - gr.begin();
-                    e = (int32_t)(W1 + W2 + j * G + (c - rdn(c)));
-                }
-                p.pairs[2 * p.lvl_start[k] + t] = e;
+                // a child slot c of level k-1 is written by that level's block c / kFlowMaxNodes
+                if (c >= 0) dl.push_back((int32_t)(b_prev + c / kFlowMaxNodes));
+                p.pairs[2 * p.lvl_start[k] + t] = c <= -2 ? leaf_ref(c) : c;
             }
+            std::sort(dl.begin(), dl.end());
+            dl.erase(std::unique(dl.begin(), dl.end()), dl.end());
             const int32_t rec[kFlowBlkInts] = {
                 (int32_t)(p.lvl_start[k] + i), (int32_t)rup2(S), (int32_t)k, (int32_t)k, (int32_t)i,
-                (int32_t)ws1, (int32_t)W1, (int32_t)ws2, (int32_t)W2,
-                (int32_t)p.gran.size(), (int32_t)gr.size(), (int32_t)p.deps.size(), (int32_t)dl.size(),
-                (int32_t)(rup2(S) * 8), (int32_t)bytes, (int32_t)S};
+                0, 0, 0, 0, (int32_t)p.gran.size(), 0, (int32_t)p.deps.size(), (int32_t)dl.size(),
+                (int32_t)(rup2(S) * 8), (int32_t)(rup2(S) * 8), (int32_t)S};
             p.blk.insert(p.blk.end(), rec, rec + kFlowBlkInts);
-            p.gran.insert(p.gran.end(), gr.begin(), gr.end());
             p.deps.insert(p.deps.end(), dl.begin(), dl.end());
-            cur_slot0.push_back(i);
             ++p.nblocks;
-            i += S;
         }
-        prev_slot0.swap(cur_slot0);
-        prev_b0 = p.lvl_blk[k];
     }
     if (p.final_k0 <= L) {
         const int64_t k0 = p.final_k0;
@@ -368,10 +259,21 @@ inline void validate_flow_plan(const FlowPlan& p, const Grammar& g) {
             if (p.lvl_start[k0] + f[FB_SLOT0] != f[FB_NODE0] || f[FB_NNODES] > f[FB_PAIRS] || f[FB_PAIRS] > f[FB_NNODES] + 1)
                 bad("block nodes");
             covered[k0] += f[FB_NNODES];
+            if (vals_staged != 0) bad("a regular block with staged values");
+            const int32_t* d0 = p.deps.data() + f[FB_DOFF];
             for (int64_t t = 0; t < 2 * f[FB_NNODES]; ++t) {
                 const int64_t c = p.pairs[2 * (int64_t)f[FB_NODE0] + t];
-                if (c >= 0 ? c >= vals_staged : c == -1 ? (t & 1) == 0 : !leaf_ok(-c - 2))
+                if (c >= 0) {
+                    // a slot of level k0-1, whose producer is among the dependencies
+                    if (k0 < 2 || c >= width(k0 - 1)) bad("child reference outside the level below");
+                    const int32_t pbk = (int32_t)(p.lvl_blk[k0 - 1] + c / kFlowMaxNodes);
+                    if (!std::binary_search(d0, d0 + f[FB_NDEP], pbk)) bad("a child's producer is not a dependency");
+                    const int32_t* fp = p.blk.data() + (int64_t)pbk * kFlowBlkInts;
+                    if (fp[FB_K0] != k0 - 1 || c < fp[FB_SLOT0] || c >= fp[FB_SLOT0] + fp[FB_NNODES])
+                        bad("a child's producer does not hold its slot");
+                } else if (c == -1 ? (t & 1) == 0 : !leaf_ok(-c - 2)) {
                     bad("child reference outside the block");
+                }
             }
         } else {
             if (b != NB - 1 || k0 != p.final_k0 || k1 != L || f[FB_NODE0] != p.lvl_start[k0] ||

@@ -253,7 +253,12 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
  *            nothing; -1 if max_iter was reached first.
  * Returns GC_ERR_NOT_CONVERGED (and records it in the status word, which
  * gc_check reports once) if max_iter products did not reach the fixpoint.
- * Synchronises the stream once per product to read the changed flag.
+ * On handles with k_max = 1 (the dataflow schedule) the loop runs on the
+ * device: products and update steps are enqueued in batches of 1, 2, 4, 8,
+ * 8, ... with no host round trip inside a batch; the last update step to
+ * finish records convergence, after which the kernels of the products
+ * already enqueued return at once (x is unchanged by them). The stream is
+ * synchronised once per batch. Other handles synchronise once per product.
  */
 gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
                    int32_t* iters, void* stream);
@@ -274,8 +279,9 @@ gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_it
  *   iters    device int32_t[1]: products performed, the last of which changed
  *            nothing; -1 if max_iter was reached first.
  * Returns GC_ERR_NOT_CONVERGED (also recorded in the status word) if
- * max_iter products did not reach the fixpoint. Synchronises the stream once
- * per product to read the changed flag.
+ * max_iter products did not reach the fixpoint. The loop runs on the device
+ * as described for gc_reach (handles with k_max = 1; a k_max = 16 handle
+ * synchronises once per product).
  */
 gc_status gc_sssp(gc_handle* h, const float* x0, float* x, int32_t max_iter, int32_t* iters,
                   void* stream);

@@ -2,12 +2,11 @@
 //
 // For each input matrix and value width (4 and 8 bytes) it builds the plan the
 // library uploads, runs its host checks, and replays the blocks in order the
-// way the device runs them: each block's windows and outlier granules are
-// copied out of the three level buffers into a staging array, every node reads
-// its two children through the block's re-encoded references (staged value,
-// identity or leaf code evaluated from x), writes its value to buffer k % 3
-// and, if it is a root, to RV; the final block keeps its levels in its own
-// staging array. y is then the sum of each row's C references (T for bare
+// way the device runs them: every node of a regular block reads its two
+// children from the level buffer of the level below (or the identity, or a
+// leaf code evaluated from x), writes its value to buffer k % 3 and, if it is
+// a root, to RV; the final block copies the level below into its staging
+// array and keeps its own levels there. y is then the sum of each row's C references (T for bare
 // terminals, RV for roots), compared with the direct product of the input CSR
 // matrix in float64.
 //
@@ -49,12 +48,15 @@ static int check_flow(const Grammar& g, int64_t vb, const std::vector<int64_t>& 
             for (int64_t s = p.gran[f[FB_GOFF] + j]; s < p.gran[f[FB_GOFF] + j] + G; ++s) st.push_back(prev[s]);
         staged += (int64_t)st.size();
         ngran += f[FB_NGRAN];
+        const bool fin = k0 >= p.final_k0;
+        // a regular block reads its children from the level buffer of k0-1,
+        // the final block from its staged values
         auto child = [&](int32_t c) -> double {
-            if (c >= 0) return st.at((size_t)c);
+            if (c >= 0) return fin ? st.at((size_t)c) : prev.at((size_t)c);
             if (c == -1) return 0.0;
             return leaf(-(int64_t)c - 2);
         };
-        if (k0 >= p.final_k0) {
+        if (fin) {
             ++finals;
             for (int64_t k = k0; k <= k1; ++k) {
                 const int64_t w = g.lvl_off[k + 1] - g.lvl_off[k];
