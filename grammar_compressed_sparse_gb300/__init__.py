@@ -80,8 +80,12 @@ class Grammar:
     def export(self, which: str) -> np.ndarray:
         return _capi().gc_export(self._p, which)
 
-    def layout(self, policy="f32", k_max=1) -> dict:
-        return _capi().gc_layout(self._p, policy, k_max)
+    def layout(self, policy="f32", k_max=1, schedule="persistent") -> dict:
+        """Device bytes for products under ``policy`` with up to ``k_max``
+        right-hand sides; ``schedule="dataflow"`` sizes the dataflow layout."""
+        if schedule == "persistent":
+            return _capi().gc_layout(self._p, policy, k_max)
+        return _capi().gc_layout_ex(self._p, policy, k_max, schedule)
 
     def __del__(self):
         p = getattr(self, "_p", None)
@@ -100,18 +104,21 @@ class Engine:
     the library never allocates device memory itself.
     """
 
-    def __init__(self, grammar: Grammar, policy="f32", k_max=1, device="cuda", stream=None):
+    def __init__(self, grammar: Grammar, policy="f32", k_max=1, device="cuda", stream=None, schedule="persistent"):
+        """``schedule``: "persistent" (default), "per_level", or "dataflow"
+        (k_max = 1; the dataflow sweep's own layout)."""
         import torch
 
         self.policy, self.k_max = policy, k_max
         st = grammar.stats()
         self.n, self.m = st["n"], st["m"]
-        self.layout = grammar.layout(policy, k_max)
+        self.layout = grammar.layout(policy, k_max, schedule)
         self.device = torch.device(device)
         self.arena = torch.empty(max(self.layout["arena_bytes"], 256), dtype=torch.uint8,
                                  device=self.device)
         self._stream = stream if stream is not None else torch.cuda.current_stream(self.device)
-        self._h = _capi().gc_upload(grammar._p, policy, k_max, self.arena, self.arena.numel(), self._stream)
+        self._h = _capi().gc_upload_ex(grammar._p, policy, k_max, schedule, self.arena, self.arena.numel(),
+                                       self._stream)
         self._stream.synchronize()
 
     @property

@@ -75,6 +75,8 @@ _sig = {
     "gc_export": ([_vp, ctypes.c_int, _vp, _i64], ctypes.c_int),
     "gc_layout": ([_vp, ctypes.c_int, _i32, ctypes.POINTER(ArenaLayout)], ctypes.c_int),
     "gc_upload": ([_vp, ctypes.c_int, _i32, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
+    "gc_layout_ex": ([_vp, ctypes.c_int, _i32, _i32, ctypes.POINTER(ArenaLayout)], ctypes.c_int),
+    "gc_upload_ex": ([_vp, ctypes.c_int, _i32, _i32, _vp, _i64, _vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_matvec": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
     "gc_matvec_host": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
     "gc_matvec_static": ([_vp, _vp, _vp, _i32, _vp], ctypes.c_int),
@@ -184,6 +186,22 @@ def gc_upload(g, policy, k_max, arena, arena_bytes, stream=None) -> int:
     out = _vp()
     _check(_lib.gc_upload(g, POLICIES[policy], k_max, _addr(arena), arena_bytes, _stream(stream),
                           ctypes.byref(out)), "gc_upload")
+    return out.value
+
+
+SCHEDULES = {"persistent": GC_SCHED_PERSISTENT, "per_level": GC_SCHED_PER_LEVEL, "dataflow": GC_SCHED_DATAFLOW}
+
+
+def gc_layout_ex(g, policy="f32", k_max=1, schedule="persistent") -> dict:
+    lay = ArenaLayout()
+    _check(_lib.gc_layout_ex(g, POLICIES[policy], k_max, SCHEDULES[schedule], ctypes.byref(lay)), "gc_layout_ex")
+    return {f: getattr(lay, f) for f, _ in ArenaLayout._fields_}
+
+
+def gc_upload_ex(g, policy, k_max, schedule, arena, arena_bytes, stream=None) -> int:
+    out = _vp()
+    _check(_lib.gc_upload_ex(g, POLICIES[policy], k_max, SCHEDULES[schedule], _addr(arena), arena_bytes,
+                             _stream(stream), ctypes.byref(out)), "gc_upload_ex")
     return out.value
 
 

@@ -333,13 +333,14 @@ gc_status gc_export(const gc_grammar* gg, gc_array which, void* dst, int64_t dst
     });
 }
 
-gc_status gc_layout(const gc_grammar* gg, gc_policy policy, int32_t k_max, gc_arena_layout* out) {
+gc_status gc_layout_ex(const gc_grammar* gg, gc_policy policy, int32_t k_max, int32_t schedule, gc_arena_layout* out) {
     return guard([&] {
         if (!gg || !out) fail(GC_ERR_ARG, "null argument");
         const Grammar& g = gg->g;
         check_policy(g, policy, k_max);
+        const bool flow = wants_flow(schedule, k_max);
         DevLayout d;
-        if (uses_flow(k_max)) {
+        if (flow) {
             const FlowCounts fc = flow_counts(*flow_plan_for(gg, policy_elem_bytes(policy)));
             d = device_layout(g, policy, k_max, &fc);
         } else {
@@ -354,6 +355,10 @@ gc_status gc_layout(const gc_grammar* gg, gc_policy policy, int32_t k_max, gc_ar
         l.csr_bytes = 8 * g.nnz + rp + d.value_bytes * (g.n + g.m);
         *out = l;
     });
+}
+
+gc_status gc_layout(const gc_grammar* gg, gc_policy policy, int32_t k_max, gc_arena_layout* out) {
+    return gc_layout_ex(gg, policy, k_max, GC_SCHED_PERSISTENT, out);
 }
 
 gc_status gc_save(const gc_grammar* gg, const char* path) {

@@ -231,18 +231,16 @@ __device__ __forceinline__ typename P::V leaf_value(int32_t code, int part, cons
     return P::leaf(__ldg(a.Vd + vi), ldg_value(a.x + (int64_t)col * P::LPN + part));
 }
 
-// The leaf-table copies in front of buf0, buf1 (and RV in the row emit), grid-stride.
+// The leaf table in front of RV (slice and row emits: C's bare terminals),
+// grid-stride. The sweep itself evaluates terminals where it reads them.
 template <class P>
 __device__ void write_leaf_tables(const SweepArgs<P>& a, int64_t tid, int64_t nthreads) {
-    using V = typename P::V;
+    if (a.emode == EMIT_LEVEL) return;   // no RV: the level emit evaluates its terminals too
     const int64_t total = (a.alpha + 1) * P::LPN;
     for (int64_t i = tid; i < total; i += nthreads) {
         const int64_t p = i / P::LPN;
         const int part = (int)(i % P::LPN);
-        const V v = p == 0 ? P::identity() : leaf_value<P>(__ldg(a.leaf + (p - 1)), part, a);
-        a.buf0[i] = v;
-        a.buf1[i] = v;
-        if (a.emode != EMIT_LEVEL) a.rv[i] = v;   // RV exists in the chunk and row emits
+        a.rv[i] = p == 0 ? P::identity() : leaf_value<P>(__ldg(a.leaf + (p - 1)), part, a);
     }
 }
 
@@ -274,10 +272,10 @@ __device__ __forceinline__ void load_chunk_staged(const SweepArgs<P>& a, int k, 
     }
 }
 
-// Combines chunk c of level k from its prefetched child pairs. prev is the
-// [T | level k-1] index space; with kTail, references past T into level k-1
-// come from prev_tail instead (a narrow level kept in the tail buffers). The
-// values go to cur[t]; roots also to rv[t] when rv is given.
+// Combines chunk c of level k from its prefetched child pairs. prev holds
+// level k-1; with kTail, its slots come from prev_tail instead when that
+// level is one of the narrow ones kept in the tail buffers. The values go to
+// cur[t]; roots also to rv[t] when rv is given.
 template <class P, bool kTail, bool kC>
 __device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int64_t c, const int2 (&ab)[Chunk<P>::U],
                                               const typename P::V* prev, const typename P::V* prev_tail,
@@ -297,11 +295,16 @@ __device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int6
         }
     } else {
         // a child is a carry slot (index >= kCarryBase), a slot of level k-1
-        // (in the tail buffer with kTail, past T), or a T entry
+        // (in the tail buffer with kTail when that level is there), the
+        // identity (-1), or a terminal by its leaf code (-2 - code),
+        // evaluated here
         auto child = [&](int32_t x) -> V {
             if (kC && x >= kCarryBase) return a.carry[(int64_t)(x - kCarryBase) * P::LPN + part];
-            if (kTail && prev_tail != nullptr && x >= a.TB) return prev_tail[(int64_t)(x - a.TB) * P::LPN + part];
-            return prev[(int64_t)x * P::LPN + part];
+            if (x >= 0) {
+                if (kTail && prev_tail != nullptr) return prev_tail[(int64_t)x * P::LPN + part];
+                return prev[(int64_t)x * P::LPN + part];
+            }
+            return x == -1 ? P::identity() : leaf_value<P>(-2 - x, part, a);
         };
 #pragma unroll
         for (int u = 0; u < Chunk<P>::U; ++u) {
@@ -336,7 +339,7 @@ __device__ __forceinline__ void combine_chunk(const SweepArgs<P>& a, int k, int6
     }
 }
 
-// Buffer pointers of grid level k: [T | level k-1] in, level k's values out.
+// Buffer pointers of grid level k: level k-1 in, level k's values out.
 template <class P>
 struct LevelIO {
     const typename P::V* prev;
@@ -347,14 +350,13 @@ template <class P>
 __device__ __forceinline__ LevelIO<P> level_io(const SweepArgs<P>& a, int k) {
     LevelIO<P> io;
     io.prev = (k & 1) ? a.buf0 : a.buf1;
-    io.cur = ((k & 1) ? a.buf1 : a.buf0) + a.TB * P::LPN;
+    io.cur = (k & 1) ? a.buf1 : a.buf0;
     io.rv = a.emode != EMIT_LEVEL ? a.rv + (a.TB + a.lvl(LV_ROFF, k)) * P::LPN : nullptr;
     return io;
 }
 
-// Buffer pointers of tail level k > Lg: T from either full buffer, level k-1
-// from its full buffer (k-1 == Lg) or from the tail buffer, level k's values
-// into the tail buffer.
+// Buffer pointers of tail level k > Lg: level k-1 from its full buffer
+// (k-1 == Lg) or from the tail buffer, level k's values into the tail buffer.
 template <class P>
 struct TailIO {
     const typename P::V* prev;
@@ -430,8 +432,9 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
 // one row (and one level, in the level emit), len <= kEmitChunk. A warp takes
 // 32/LPN references at a time, LPN lanes each; lane (slot, part) sums part
 // `part` of references slot, slot + 32/LPN, ... in order, the warp reduces the
-// slots by a fixed butterfly, and the sum goes to esum[id]. base is the index
-// space of the references: [T | level buffer] or [T | RV].
+// slots by a fixed butterfly, and the sum goes to esum[id]. base is the
+// level's buffer: a reference is one of its root slots, or a bare terminal
+// of C by its leaf code (-2 - code), evaluated here.
 constexpr int kEmitChunk = (int)kEmitChunkSyms;
 
 template <class P>
@@ -449,12 +452,13 @@ __device__ __forceinline__ void emit_chunk(const SweepArgs<P>& a, int64_t j, con
 #pragma unroll
         for (int u = 0; u < B; ++u) {
             const int idx = (u0 + u) * NS + slot;
-            r[u] = idx < ch.y ? __ldcs(a.cref + ch.x + idx) : 0;
+            r[u] = idx < ch.y ? __ldcs(a.cref + ch.x + idx) : -1;   // padding: the identity
         }
         V v[B];
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            v[u] = base[(int64_t)r[u] * P::LPN + part];
+            v[u] = r[u] >= 0 ? base[(int64_t)r[u] * P::LPN + part]
+                   : r[u] == -1 ? P::identity() : leaf_value<P>(-2 - r[u], part, a);
         }
 #pragma unroll
         for (int u = 0; u < B; ++u) acc = P::combine(acc, v[u]);
@@ -682,6 +686,14 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
     // an unread earlier timeout left the barrier counter part-way: do nothing
     if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
     const int Lg = a.grid_levels;
+    // a converged fixpoint loop skips the product: the CTA's arrivals at the
+    // launch's grid barriers (one a level after the first; before the tail
+    // and the emit unless the slice kernel takes them) in one addition
+    if (a.conv != nullptr && ld_volatile(a.conv) != 0) {
+        if (threadIdx.x == 0)
+            red_add_release(a.bar, (unsigned long long)((Lg > 1 ? Lg - 1 : 0) + (a.emode == EMIT_SLICE ? 0 : 2)));
+        return;
+    }
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const uint64_t keep = l2_evict_last();
@@ -946,7 +958,14 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
     // a converged fixpoint loop skips the product (one arrival at the grid
     // barrier, as if the launch had passed it)
     if (a.conv != nullptr && ld_volatile(a.conv) != 0) {
-        if (coop && threadIdx.x == 0) red_add_release(a.bar, 1ull);
+        if (coop && threadIdx.x == 0) {
+            red_add_release(a.bar, 1ull);
+            // the tail group's CTAs pass one group barrier a tail level up to tail_solo
+            const bool tl = a.grid_levels < a.L;
+            const int64_t grp = !tl ? 0 : gridDim.x > a.tail_group ? a.tail_group : gridDim.x;
+            const int64_t per = (a.tail_solo < a.L ? a.tail_solo : a.L) - a.grid_levels - 1;
+            if (grp > 1 && blockIdx.x < grp && per > 0) red_add_release(a.tbar, (unsigned long long)per);
+        }
         return;
     }
     const bool tail = coop && a.grid_levels < a.L;
@@ -1072,11 +1091,12 @@ struct FlowArgs {
     using V = typename P::V;
     const int2* pairs;        // block-local child references
     const int32_t* blk;       // kFlowBlkInts per block
+    const int32_t* order;     // blocks in processing order; a launch takes positions [b_begin, b_end)
     const int32_t* deps;
     const int32_t* gran;
     const int64_t* lv;        // level table
     int32_t L2;               // its row stride
-    int32_t b_begin, b_end;   // blocks of this launch
+    int32_t b_begin, b_end;   // positions in the processing order of this launch
     int32_t final_block;      // id of the final block, or -1
     int32_t waits;            // 1: one launch for all blocks, wait for dependencies
     int32_t write_t;          // write T in front of RV
@@ -1200,7 +1220,8 @@ __device__ void flow_stage(const FlowArgs<P>& a, unsigned char* fsm, FlowSync& s
         __syncwarp();
     };
     int it = w;
-    for (int b = a.b_begin + (int)blockIdx.x + w * (int)gridDim.x; b < a.b_end; b += kNS * (int)gridDim.x, it += kNS) {
+    for (int q = a.b_begin + (int)blockIdx.x + w * (int)gridDim.x; q < a.b_end; q += kNS * (int)gridDim.x, it += kNS) {
+        const int b = __ldg(a.order + q);
         const int32_t fv = lane < (int)kFlowBlkInts ? __ldg(a.blk + (int64_t)b * kFlowBlkInts + lane) : 0;
         // every lane reads every field here: F is a full-warp shuffle, so it
         // is never called inside a lane-dependent branch
@@ -1322,7 +1343,8 @@ __device__ void flow_compute(const FlowArgs<P>& a, unsigned char* fsm, FlowSync&
     const uint64_t keep = l2_evict_last();
     uint32_t cphase = 0;
     int it = 0;
-    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
+    for (int q = a.b_begin + (int)blockIdx.x; q < a.b_end; q += (int)gridDim.x, ++it) {
+        const int b = __ldg(a.order + q);
         const int s = it % kNS;
         if (!warp_wait(&sy.full[s], (uint32_t)(it / kNS) & 1u, sy, it, 4 * a.timeout, a)) return;
         const FlowHead& h = sy.head[s];
@@ -1401,7 +1423,8 @@ template <class P>
 __device__ void flow_publish(const FlowArgs<P>& a, FlowSync& sy) {
     if ((threadIdx.x & 31) != 0) return;
     int it = 0;
-    for (int b = a.b_begin + (int)blockIdx.x; b < a.b_end; b += (int)gridDim.x, ++it) {
+    for (int q = a.b_begin + (int)blockIdx.x; q < a.b_end; q += (int)gridDim.x, ++it) {
+        const int b = __ldg(a.order + q);
         const int s = it % kNS, want = kFlowCW * (it / kNS + 1);   // sy.done only grows
         const long long t0 = clock64();
         for (unsigned n = 0; ld_acquire_cta(&sy.done[s]) < want; ++n)
@@ -1440,9 +1463,11 @@ __global__ void __launch_bounds__(kFlowThreads, 1) flow_kernel(const FlowArgs<P>
                 const int64_t nb = k >= 1 && k < a.L2 - 1 ? a.lvl(LV_NBLK, k) : 0;
                 if (nb > 0) red_add_release(a.done + k, (unsigned long long)nb);
             }
-        } else if (blockIdx.x == 0 && threadIdx.x == 0 && a.b_end > a.b_begin && a.b_begin != a.final_block) {
-            red_add_release(a.done + __ldg(a.blk + (int64_t)a.b_begin * kFlowBlkInts + FB_K0),
-                            (unsigned long long)(a.b_end - a.b_begin));
+        } else if (blockIdx.x == 0 && threadIdx.x == 0 && a.b_end > a.b_begin) {
+            const int b0 = __ldg(a.order + a.b_begin);   // a launch of one level's blocks
+            if (b0 != a.final_block)
+                red_add_release(a.done + __ldg(a.blk + (int64_t)b0 * kFlowBlkInts + FB_K0),
+                                (unsigned long long)(a.b_end - a.b_begin));
         }
         return;
     }
@@ -1474,6 +1499,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1) flow_kernel(const FlowArgs<P>
 // ---------------------------------------------------------------- per-level schedule
 template <class P, bool kC>
 __global__ void __launch_bounds__(kThreads, 2) level_kernel(const SweepArgs<P> a, int k) {
+    if (a.conv != nullptr && ld_volatile(a.conv) != 0) return;   // a converged fixpoint loop
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const uint64_t keep = l2_evict_last();
@@ -1533,23 +1559,8 @@ struct MinUpdate {
 // step, ctl[1] converged, ctl[2] CTAs of this step finished, ctl[3] the
 // product count at convergence. With ctl[1] set every later step (and, in the
 // dataflow products, every later product) does nothing.
-template <class U>
-__global__ void __launch_bounds__(kThreads)
-update_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y, int64_t n,
-              int32_t* __restrict__ changed) {
-    int ch = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const typename U::T u = x[i], v = U::apply(u, y[i]);
-        if (v != u) {
-            x[i] = v;
-            ch = 1;
-        }
-    }
-    if (__syncthreads_or(ch) && threadIdx.x == 0) *changed = 1;
-}
-
-// The same step for a loop that runs on without the host: the last CTA to
-// finish reads the changed word; if nothing changed, the loop has converged
+// One step of a fixpoint loop that runs on without the host, x = x (+) y:
+// the last CTA to finish reads the changed word; if nothing changed, the loop has converged
 // at product `it` (recorded in ctl[3]); it then clears the step's words.
 template <class U>
 __global__ void __launch_bounds__(kThreads)
@@ -1782,6 +1793,7 @@ FlowArgs<P> make_flow_args(const gc_handle* h, const SweepArgs<P>& a, const Flow
     FlowArgs<P> f{};
     f.pairs = reinterpret_cast<const int2*>(ar + d.nodes);
     f.blk = reinterpret_cast<const int32_t*>(ar + d.fblk);
+    f.order = reinterpret_cast<const int32_t*>(ar + d.forder);
     f.deps = reinterpret_cast<const int32_t*>(ar + d.fdeps);
     f.gran = reinterpret_cast<const int32_t*>(ar + d.fgran);
     f.lv = a.lv;
@@ -1982,9 +1994,15 @@ void put(cudaStream_t st, char* arena, int64_t off, const T* p, size_t count) {
 }
 
 // x <- x (+) (M (x) x) from x0 until nothing changes, at most max_iter
-// products; the product's y lives in the arena's staging area. Writes the
-// product count (or -1) to iters on the device. Returns false if max_iter
-// was reached first (the status word then says GC_ERR_NOT_CONVERGED).
+// products; the product's y lives in the arena's staging area. The loop runs
+// on the device: products and update steps are enqueued in batches of 1, 2,
+// 4, 8, 8, ... with no host round trip inside a batch; the update step's last
+// CTA records convergence (ctl, in the status block) and every kernel
+// enqueued after it returns at once, keeping the barrier counters and level
+// counters consistent. One stream synchronise a batch reads the converged
+// word. Writes the product count (or -1) to iters on the device. Returns
+// false if max_iter was reached first (the status word then says
+// GC_ERR_NOT_CONVERGED).
 template <class U>
 bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32_t max_iter, int32_t* iters,
                   cudaStream_t st) {
@@ -1992,77 +2010,42 @@ bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32
     const int64_t n = h->n;
     T* yv = reinterpret_cast<T*>(h->arena + h->lay.ys);
     int32_t* status = reinterpret_cast<int32_t*>(h->arena + h->lay.status);
-    int32_t* changed = status + 1;
+    int32_t* ctl = status + 4;   // changed, converged, CTAs done, product count (bytes 16..31)
     if (x != x0 && n > 0)
         cuda_check(cudaMemcpyAsync(x, x0, n * sizeof(T), cudaMemcpyDeviceToDevice, st), "x0 copy");
-    int32_t it = 0, done = 0;
+    cuda_check(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
+    int32_t it = 0, batch = 1, result = -1;
+    bool done = false;
     int64_t launches = 0;
-    if (h->flow) {
-        // the loop runs on the device: products are enqueued in batches of 1,
-        // 2, 4, 8, ... without a host round trip in between; the update
-        // kernel decides convergence (ctl, in the status block) and every
-        // kernel enqueued after it returns at once. One stream synchronise
-        // per batch reads the converged word.
-        int32_t* ctl = status + 4;
-        cuda_check(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
-        h->conv = ctl + 1;
-        int32_t batch = 1, result = -1;
-        while (it < max_iter && !done) {
-            const int32_t nb = std::min(batch, max_iter - it);
-            for (int32_t j = 0; j < nb; ++j) {
-                ++it;
-                dispatch_product(h, x, yv, 1, st);
-                launches += h->launches;
-                update_loop_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, ctl, it);
-                ++launches;
-            }
-            cuda_check(cudaGetLastError(), "kernel launch");
-            int32_t w[4] = {0, 0, 0, 0};
-            cuda_check(cudaMemcpyAsync(w, ctl, 16, cudaMemcpyDeviceToHost, st), "loop words read");
-            cuda_check(cudaStreamSynchronize(st), "stream synchronize");
-            if (w[1]) {
-                done = 1;
-                result = w[3];
-            }
-            batch = std::min(batch * 2, 8);
-        }
-        h->conv = nullptr;
-        h->launches = launches;
-        cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
-        if (!done) {
-            int32_t sw = GC_ERR_NOT_CONVERGED;
-            cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
-        }
-        cuda_check(cudaStreamSynchronize(st), "stream synchronize");
-        return done != 0;
-    }
-    while (it < max_iter) {
-        ++it;
-        cuda_check(cudaMemsetAsync(changed, 0, 4, st), "flag clear");
-        dispatch_product(h, x, yv, 1, st);
-        launches += h->launches;
-        if (n > 0) {
-            update_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, changed);
+    h->conv = ctl + 1;
+    while (it < max_iter && !done) {
+        const int32_t nb = std::min(batch, max_iter - it);
+        for (int32_t j = 0; j < nb; ++j) {
+            ++it;
+            dispatch_product(h, x, yv, 1, st);
+            launches += h->launches;
+            update_loop_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, ctl, it);
             ++launches;
         }
         cuda_check(cudaGetLastError(), "kernel launch");
-        int32_t c = 0;
-        cuda_check(cudaMemcpyAsync(&c, changed, 4, cudaMemcpyDeviceToHost, st), "flag read");
+        int32_t w[4] = {0, 0, 0, 0};
+        cuda_check(cudaMemcpyAsync(w, ctl, 16, cudaMemcpyDeviceToHost, st), "loop words read");
         cuda_check(cudaStreamSynchronize(st), "stream synchronize");
-        if (!c) {
-            done = 1;
-            break;
+        if (w[1]) {
+            done = true;
+            result = w[3];
         }
+        batch = std::min(batch * 2, 8);
     }
+    h->conv = nullptr;
     h->launches = launches;
-    int32_t result = done ? it : -1;
     cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
     if (!done) {
         int32_t sw = GC_ERR_NOT_CONVERGED;
         cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
     }
     cuda_check(cudaStreamSynchronize(st), "stream synchronize");
-    return done != 0;
+    return done;
 }
 
 // ---------------------------------------------------------------- fixed scratch
@@ -2122,8 +2105,8 @@ StaticParts static_parts(const gc_handle* h, int32_t k) {
         s.total = o;
         return s;
     }
-    s.buf0 = take(vb * (d.TB + h->max_width));
-    s.buf1 = take(vb * (d.TB + h->max_width));
+    s.buf0 = take(vb * std::max<int64_t>(1, h->max_width));
+    s.buf1 = take(vb * std::max<int64_t>(1, h->max_width));
     s.tbuf = take(vb * d.tail_total);
     s.carry = take(vb * std::max<int64_t>(1, h->n_carry));
     if (d.chunked()) s.esum = take(vb * d.n_esum);
@@ -2188,8 +2171,8 @@ using namespace gcs;
 
 extern "C" {
 
-gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void* arena, int64_t arena_bytes,
-                    void* stream, gc_handle** out) {
+gc_status gc_upload_ex(const gc_grammar* gg, gc_policy policy, int32_t k_max, int32_t schedule, void* arena,
+                       int64_t arena_bytes, void* stream, gc_handle** out) {
     return guard([&] {
         if (!gg || !out) fail(GC_ERR_ARG, "null grammar or output pointer");
         if (!arena) fail(GC_ERR_ARG, "null arena");
@@ -2198,7 +2181,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         validate_packed(gg->g);
         // one value a node: the dataflow sweep over the layered grammar itself;
         // wider values: the device view (carry slots for the level emit)
-        const bool flow = uses_flow(k_max);
+        const bool flow = wants_flow(schedule, k_max);
         std::shared_ptr<const FlowPlan> fp;
         FlowCounts fc;
         Grammar view;
@@ -2233,6 +2216,8 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             h->final_k0 = fp->final_k0;
             h->lvl_blk = fp->lvl_blk;
             h->schedule = GC_SCHED_DATAFLOW;
+        } else if (schedule == GC_SCHED_PER_LEVEL) {
+            h->schedule = GC_SCHED_PER_LEVEL;
         }
         // row emit (rows average < 128 symbols): G lanes per row, so that a
         // lane loads about one batch of a row's symbols (4 one-lane values, 2
@@ -2251,9 +2236,9 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         auto leaf_code = [&](int32_t p) { return (int32_t)(((int64_t)g.term_col[p] << d.vbits) | g.term_vidx[p]); };
         const int64_t A = g.alpha();
         auto ref = [&](int32_t c) -> int32_t {   // device-view reference -> device index
-            if (c >= 0) return (int32_t)(d.TB + c);
-            if (c == -1) return 0;
-            if (c >= -(A + 1)) return -c - 1;      // terminal p = -c-2 -> T[p+1]
+            if (c >= 0) return c;                   // slot of the level below
+            if (c == -1) return -1;                 // identity
+            if (c >= -(A + 1)) return -2 - leaf_code(-c - 2);   // terminal p = -c-2, by its leaf code
             return kCarryBase + (int32_t)carry_slot(c, A);
         };
         h->lv.assign((size_t)(LV_ROWS * (L + 2)), 0);
@@ -2290,11 +2275,11 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         SlicePlan sp;
         std::vector<int32_t> cref, co;
         if (d.emit == EMIT_LEVEL) {
-            plan = plan_level_emit(g, d.TB, d.grid_levels);
+            plan = plan_level_emit(g, d.grid_levels);
             if ((int64_t)plan.echunk.size() != 4 * d.n_echunks || (int64_t)plan.late_ref.size() != d.n_late ||
                 (int64_t)plan.cref.size() != d.n_early)
                 fail(GC_ERR_INVALID_GRAMMAR, "emit plan does not match the layout");
-            validate_emit_plan(plan, g, d.TB, d.grid_levels);
+            validate_emit_plan(plan, g, d.grid_levels);
             for (int64_t k = 0; k <= L + 1; ++k) h->lv[LV_ECH * (L + 2) + k] = plan.ech[k];
         } else if (d.emit == EMIT_SLICE) {
             sp = plan_slice_emit(g, d.TB, d.grid_levels, d.slice);
@@ -2304,7 +2289,12 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
             validate_slice_plan(sp, g, d.TB, d.grid_levels);
         } else {
             cref.resize(g.c_ref.size());
-            for (size_t e = 0; e < cref.size(); ++e) cref[e] = ref(g.c_ref[e]);
+            // row emit: C's references index [T | RV] (root slot s at TB + s,
+            // terminal p at T[p + 1])
+            for (size_t e = 0; e < cref.size(); ++e) {
+                const int32_t c = g.c_ref[e];
+                cref[e] = c >= 0 ? (int32_t)(d.TB + c) : -c - 1;
+            }
             co.resize(g.slp.c_off.size());
             for (size_t r = 0; r < co.size(); ++r) co[r] = (int32_t)g.slp.c_off[r];
         }
@@ -2349,6 +2339,7 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         }
         if (flow) {
             put(st, a, d.fblk, fp->blk.data(), fp->blk.size());
+            put(st, a, d.forder, fp->order.data(), fp->order.size());
             put(st, a, d.fdeps, fp->deps.data(), fp->deps.size());
             put(st, a, d.fgran, fp->gran.data(), fp->gran.size());
             cuda_check(cudaMemsetAsync(a + d.fflags, 0, 4 * std::max<int64_t>(1, d.n_fblocks), st), "flags clear");
@@ -2358,6 +2349,11 @@ gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void*
         cuda_check(cudaStreamSynchronize(st), "upload synchronize");
         *out = h.release();
     });
+}
+
+gc_status gc_upload(const gc_grammar* gg, gc_policy policy, int32_t k_max, void* arena, int64_t arena_bytes,
+                    void* stream, gc_handle** out) {
+    return gc_upload_ex(gg, policy, k_max, GC_SCHED_PERSISTENT, arena, arena_bytes, stream, out);
 }
 
 gc_status gc_matvec(gc_handle* h, const void* x, void* y, int32_t k, void* stream) {

@@ -67,6 +67,7 @@ struct FlowPlan {
     std::vector<int32_t> gran;      // first slot of each outlier granule, per block
     std::vector<int64_t> lvl_blk;   // L+2: first block of level k; [L+1] = blocks
     std::vector<int64_t> lvl_start; // L+2: first padded node of level k
+    std::vector<int32_t> order;     // the blocks in processing order (see plan_flow)
     int64_t nblocks = 0;
     int64_t final_k0 = 0;           // first level of the final block (L+1: none)
     int64_t buf_values = 0;         // values per level buffer
@@ -182,6 +183,30 @@ inline FlowPlan plan_flow(const Grammar& g, int64_t value_bytes) {
         for (int64_t k = k0 + 1; k <= L; ++k) p.lvl_blk[k] = p.lvl_blk[k0];
     }
     p.lvl_blk[L + 1] = p.nblocks;
+    // Processing order: level after level (every dependency lies in the level
+    // below, so this is a topological order), and within a level by the
+    // position of the block's latest dependency in the order, then by id. A
+    // block's children span both halves of the level below (roots first,
+    // then the other nodes, each sorted by column), so by id the first blocks
+    // of a level would wait for the last of the one below; in this order
+    // they wait for the earliest ones.
+    std::vector<int32_t> pos((size_t)p.nblocks, 0);
+    std::vector<std::pair<int64_t, int32_t>> key;
+    for (int64_t k = 1; k < std::min(p.final_k0, L + 1); ++k) {
+        key.clear();
+        for (int64_t b = p.lvl_blk[k]; b < p.lvl_blk[k + 1]; ++b) {
+            const int32_t* f = p.blk.data() + b * kFlowBlkInts;
+            int64_t latest = -1;
+            for (int32_t j = 0; j < f[FB_NDEP]; ++j) latest = std::max<int64_t>(latest, pos[p.deps[f[FB_DOFF] + j]]);
+            key.push_back({latest, (int32_t)b});
+        }
+        std::sort(key.begin(), key.end());
+        for (const auto& kb : key) {
+            pos[kb.second] = (int32_t)p.order.size();
+            p.order.push_back(kb.second);
+        }
+    }
+    if (p.final_k0 <= L) p.order.push_back((int32_t)(p.nblocks - 1));   // the final block last
     return p;
 }
 
@@ -299,6 +324,22 @@ inline void validate_flow_plan(const FlowPlan& p, const Grammar& g) {
     }
     for (int64_t k = 1; k <= L; ++k)
         if (covered[k] != width(k)) bad("a level not covered by its blocks");
+    // the processing order: a permutation that keeps each level's blocks in
+    // that level's id range and puts every dependency before its block
+    if ((int64_t)p.order.size() != NB) bad("processing order size");
+    std::vector<int64_t> pos((size_t)NB, -1);
+    for (int64_t q = 0; q < NB; ++q) {
+        const int64_t b = p.order[q];
+        if (b < 0 || b >= NB || pos[b] >= 0) bad("processing order is not a permutation");
+        pos[b] = q;
+    }
+    for (int64_t b = 0; b < NB; ++b) {
+        const int32_t* f = p.blk.data() + b * kFlowBlkInts;
+        const int64_t k0 = f[FB_K0];
+        if (pos[b] < p.lvl_blk[k0] || pos[b] >= (k0 >= p.final_k0 ? NB : p.lvl_blk[k0 + 1])) bad("processing order mixes levels");
+        for (int64_t j = 0; j < f[FB_NDEP]; ++j)
+            if (pos[p.deps[f[FB_DOFF] + j]] >= pos[b]) bad("a dependency after its block in the processing order");
+    }
 }
 
 // The plan of gg's grammar for values of value_bytes, made on first use and
@@ -320,7 +361,14 @@ inline FlowCounts flow_counts(const FlowPlan& p) {
     return c;
 }
 
-// Handles with one value a node (k_max = 1) run the dataflow sweep.
-inline bool uses_flow(int32_t k_max) { return k_max == 1; }
+// The dataflow layout is made on request (schedule GC_SCHED_DATAFLOW at
+// upload) for handles with one value a node; anything else is refused.
+inline bool wants_flow(int32_t schedule, int32_t k_max) {
+    if (schedule != GC_SCHED_PERSISTENT && schedule != GC_SCHED_PER_LEVEL && schedule != GC_SCHED_DATAFLOW)
+        fail(GC_ERR_ARG, "unknown schedule");
+    if (schedule == GC_SCHED_DATAFLOW && k_max != 1)
+        fail(GC_ERR_UNSUPPORTED, "the dataflow schedule serves handles with one value a node (k_max = 1)");
+    return schedule == GC_SCHED_DATAFLOW;
+}
 
 }  // namespace gcs

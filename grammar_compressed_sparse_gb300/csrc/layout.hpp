@@ -30,8 +30,8 @@
 //                       late_ref  int32[late]      narrow top levels (tail indices)
 //     row emit:         c_off     int32[n+1]
 //                       c_ref     int32[|C|]       C in row order (RV slots / T)
-//   scratch             buf0X     value[TB + w*]   leaf table T, then a level's
-//                       buf1X     value[TB + w*]   values (the two streaming buffers)
+//   scratch             buf0X     value[w*]        a level's values (the two
+//                       buf1X     value[w*]        streaming buffers)
 //                       tbuf      value[tail]      the narrow top levels' values,
 //                                                  level after level
 //                       carry     value[carried]   values of the nodes read two or
@@ -42,8 +42,8 @@
 //                       status    256 B            status word, fixpoint flag, grid-
 //                                                  barrier and tail-group arrival counters
 //   dataflow sweep (one value a node, flow.hpp): nodes holds the block-local
-//   child references; fblk int32[16 blocks] block records, fdeps / fgran
-//   int32 dependency and outlier-granule lists; scratch fb0..fb2 value[buf]
+//   child references; fblk int32[16 blocks] block records, forder int32[blocks]
+//   the processing order, fdeps / fgran int32 dependency and outlier-granule lists; scratch fb0..fb2 value[buf]
 //   three level buffers, fflags int32[blocks] ready flags, fdone
 //   uint64[L+2] finished blocks per level; no tail and no buf0 / buf1
 //   staging             xs        value[m]         x / y copies for the
@@ -51,15 +51,18 @@
 // "value" is k_max elements of the policy's type (float, int64, uint64);
 // TB = alpha + 1 rounded up to a multiple of 64 values.
 //
-// Leaf table: T[0] is the combine identity and T[p+1] = V[l_p] (x) x[j_p] for
-// terminal p = <l_p, j_p> (Sec. 4.3's T). Its copies sit in front of each
-// buffer, so that one index space covers both: a child or C reference is
-//   0            the identity (second child of a pass-through)
-//   p + 1        terminal p
-//   TB + s       slot s of a level's buffer (or root slot s of RV)
-// and every read is a single load, without a branch. Level 1, whose children
-// are all terminals, instead stores leaf codes (column << vbits | value index)
-// and evaluates its leaves in the sweep while the T copies are being written.
+// Terminals are evaluated where the sweep reads them (Sec. 4.3's leaf values
+// V[l_p] (x) x[j_p], without a leaf table in front of the level buffers, so
+// the buffers hold w* values at every batch width): a child reference of a
+// level k >= 2 node, and a C reference of the level emit, is
+//   c >= 0       slot c of the level below (of its own level for C), or a
+//                carry slot (kCarryBase + s, the device view's carried rules)
+//   -1           the identity (second child of a pass-through)
+//   -2 - q       a terminal by its leaf code q = column << vbits | value index
+// and level 1, whose children are all terminals, stores the leaf codes
+// themselves. The slice and row emits read C's bare terminals from a leaf
+// table in front of RV: T[0] the identity, T[p+1] = V[l_p] (x) x[j_p] for
+// terminal p, and root slot s at TB + s.
 //
 // Levels 1..Lg are wide and use the whole grid; the narrow levels above them
 // (each at most tail_nodes wide, two or more of them) form the tail, computed
@@ -131,7 +134,7 @@ struct DevLayout {
     // dataflow sweep (flow.hpp): one value a node; replaces the tail and the
     // two level buffers with three level buffers, block records and flags
     bool flow = false;
-    int64_t fblk, fdeps, fgran;           // grammar part: block records, dependencies, granules
+    int64_t fblk, fdeps, fgran, forder;   // grammar part: block records, dependencies, granules, order
     int64_t fb0, fb1, fb2, fflags, fdone; // scratch: level buffers, ready flags, per-level counters
     int64_t n_fblocks, n_fdeps, n_fgran, fbuf_values, final_k0;
 
@@ -391,10 +394,11 @@ inline void plan_late(const Grammar& g, int64_t Lg, std::vector<int32_t>& off, s
     }
 }
 
-inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
+inline EmitPlan plan_level_emit(const Grammar& g, int64_t Lg) {
     const int64_t L = g.L, n = g.n;
     const std::vector<int64_t>& co = g.slp.c_off;
     const size_t C = g.c_ref.size();
+    const int32_t vbits = value_bits((int64_t)g.V.size());
     EmitPlan p;
     plan_late(g, Lg, p.late_off, p.late_ref);
     std::vector<int32_t> lev(C), pos(C);
@@ -402,8 +406,10 @@ inline EmitPlan plan_level_emit(const Grammar& g, int64_t TB, int64_t Lg) {
         const int32_t c = g.c_ref[e];
         const int64_t k = ref_level(g, c);
         lev[e] = (int32_t)k;
-        pos[e] = c < 0 ? -c - 1                                   // terminal p = -c-2 -> T[p+1]
-                       : (int32_t)(TB + c - g.root_off[k]);
+        // a terminal p = -c-2 as -2 - its leaf code (evaluated where it is
+        // read); a root as its slot in its level's buffer
+        pos[e] = c < 0 ? (int32_t)(-2 - (((int64_t)g.term_col[-c - 2] << vbits) | g.term_vidx[-c - 2]))
+                       : (int32_t)(c - g.root_off[k]);
     }
     // counting sort of the early references by level, stable in row-major order
     std::vector<int64_t> cnt((size_t)Lg + 2, 0);
@@ -715,7 +721,7 @@ inline void check_late(const std::vector<int32_t>& off, const std::vector<int32_
         if (t < 0 || t >= toff[g.L + 1]) bad("tail reference outside the tail buffer");
 }
 
-inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, int64_t Lg) {
+inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t Lg) {
     const int64_t n = g.n, L = g.L, nch = (int64_t)p.echunk.size() / 4;
     auto bad = [](const char* what) { fail(GC_ERR_INVALID_GRAMMAR, std::string("emit plan: ") + what); };
     if ((int64_t)p.ech.size() != L + 2 || p.ech[0] != 0 || p.ech[L + 1] != nch) bad("level chunk ranges");
@@ -724,10 +730,13 @@ inline void validate_emit_plan(const EmitPlan& p, const Grammar& g, int64_t TB, 
     std::vector<char> seen((size_t)nch, 0);
     for (int64_t k = 0; k <= L; ++k) {
         if (p.ech[k + 1] < p.ech[k] || (k > Lg && p.ech[k + 1] != p.ech[k])) bad("level chunk ranges");
-        // terminals (level 0) or level k's roots in its buffer
-        const int64_t t_hi = k == 0 ? g.alpha() + 1 : 0;
-        const int64_t r_hi = TB + (k == 0 ? 0 : g.lvl_roots[k]);
-        auto ok = [&](int64_t v) { return (v >= 0 && v < t_hi) || (v >= TB && v < r_hi); };
+        // terminals (level 0: -2 - a leaf code) or level k's roots (their slots)
+        const int32_t vbits = value_bits((int64_t)g.V.size());
+        const int64_t nv = (int64_t)g.V.size(), leaf_max = (int64_t)g.m << vbits;
+        auto ok = [&](int64_t v) {
+            if (k == 0) return v <= -2 && -v - 2 < leaf_max && ((-v - 2) & ((1 << vbits) - 1)) < nv;
+            return v >= 0 && v < g.lvl_roots[k];
+        };
         for (int64_t j = p.ech[k]; j < p.ech[k + 1]; ++j) {
             const int64_t st = p.echunk[4 * j], len = p.echunk[4 * j + 1], id = p.echunk[4 * j + 2];
             if (st < 0 || len < 1 || len > kEmitChunkSyms || st + len > (int64_t)p.cref.size()) bad("chunk extent");
@@ -877,6 +886,7 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max, con
     d.levels = take(8 * kLevelRows * (L + 2));
     if (d.flow) {
         d.fblk = take(kFlowBlkBytes * d.n_fblocks);
+        d.forder = take(4 * d.n_fblocks);
         d.fdeps = take(4 * d.n_fdeps);
         d.fgran = take(4 * d.n_fgran);
     }
@@ -912,8 +922,8 @@ inline DevLayout device_layout(const Grammar& g, gc_policy p, int32_t k_max, con
         d.fdone = take(8 * (L + 2));
         d.buf0 = d.buf1 = d.tbuf = d.carry = take(0);
     } else {
-        d.buf0 = take(d.value_bytes * (d.TB + w));
-        d.buf1 = take(d.value_bytes * (d.TB + w));
+        d.buf0 = take(d.value_bytes * std::max<int64_t>(1, w));
+        d.buf1 = take(d.value_bytes * std::max<int64_t>(1, w));
         d.tbuf = take(d.value_bytes * d.tail_total);
         d.carry = take(d.value_bytes * std::max<int64_t>(1, g.n_carry));
     }

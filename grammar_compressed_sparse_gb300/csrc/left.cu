@@ -77,6 +77,7 @@ struct LeftStep {
     int64_t init_base, init_count, init_shift;
     void* out;             // out[g - out_base]
     int64_t out_base;
+    const int32_t* conv;   // nonzero while a converged fixpoint loop skips the rest of its products
 };
 
 // The combine, its identity and the column step's leaf map of each policy.
@@ -151,6 +152,7 @@ template <class Op>
 __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep s, const int32_t* __restrict__ task,
                                                                  int64_t t0, int64_t t1) {
     using V = typename Op::V;
+    if (*reinterpret_cast<const volatile int32_t*>(s.conv) != 0) return;
     const int lane = threadIdx.x & 31;
     V* const out = static_cast<V*>(s.out);
     const int64_t warps = (int64_t)gridDim.x * (kLeftThreads / 32);
@@ -184,12 +186,18 @@ __global__ void __launch_bounds__(kLeftThreads) left_step_kernel(const LeftStep 
     }
 }
 
-// x = x (+) t elementwise (OR, or min); sets *changed if any element changed
-// (one step of a forward fixpoint).
+// One step of a forward fixpoint loop that runs on without the host, x = x
+// (+) t elementwise (OR, or min). ctl: changed in this step, converged, CTAs
+// of this step finished, product count at convergence. The last CTA to
+// finish reads the changed word; if nothing changed the loop has converged
+// at product `it`; it then clears the step's words. Once converged, every
+// later step (and product) does nothing.
 template <class Op>
 __global__ void __launch_bounds__(kLeftThreads)
-left_update_kernel(typename Op::V* __restrict__ x, const typename Op::V* __restrict__ t, int64_t n,
-                   int32_t* __restrict__ changed) {
+left_update_loop_kernel(typename Op::V* __restrict__ x, const typename Op::V* __restrict__ t, int64_t n,
+                        int32_t* __restrict__ ctl, int32_t it) {
+    __shared__ int s_last;
+    if (*reinterpret_cast<const volatile int32_t*>(ctl + 1) != 0) return;
     int ch = 0;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const typename Op::V u = x[i], v = Op::combine(u, t[i]);
@@ -198,7 +206,23 @@ left_update_kernel(typename Op::V* __restrict__ x, const typename Op::V* __restr
             ch = 1;
         }
     }
-    if (__syncthreads_or(ch) && threadIdx.x == 0) *changed = 1;
+    const int any = __syncthreads_or(ch);
+    if (threadIdx.x == 0) {
+        if (any) atomicOr(ctl, 1);
+        __threadfence();
+        s_last = atomicAdd(ctl + 2, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last && threadIdx.x == 0) {
+        __threadfence();
+        if (*reinterpret_cast<volatile int32_t*>(ctl) == 0) {
+            ctl[3] = it;
+            ctl[1] = 1;
+        }
+        ctl[0] = 0;
+        ctl[2] = 0;
+        __threadfence();
+    }
 }
 
 void cuda_ok(cudaError_t e, const char* what) {
@@ -248,25 +272,28 @@ std::vector<StepLaunch> left_steps(const gc_left_handle* h, const void* y, void*
     auto I = [&](int64_t off) { return reinterpret_cast<const int32_t*>(a + off); };
     auto F = [&](int64_t off) { return static_cast<void*>(a + off); };
     std::vector<StepLaunch> out;
-    auto add = [&](const LeftStep& s, int64_t set) {
+    const int32_t* conv = I(h->flag) + 1;   // the fixpoint loop's converged word (0 outside a loop)
+    auto add = [&](LeftStep s, int64_t set) {
         const int64_t t0 = h->task_off[set], t1 = h->task_off[set + 1];
         if (t1 <= t0) return;
+        s.conv = conv;
         const int64_t wpb = kLeftThreads / 32;
         const int64_t grid = std::min<int64_t>((t1 - t0 + wpb - 1) / wpb, (int64_t)h->sms * 8);
         out.push_back(StepLaunch{s, I(h->task), t0, t1, set, (unsigned)grid});
     };
     // seed: RS[s] = sum of y over C's references to s
-    add(LeftStep{I(h->soff), I(h->srow), y, nullptr, nullptr, nullptr, 0, 0, 0, F(h->RS), 0}, 0);
+    add(LeftStep{I(h->soff), I(h->srow), y, nullptr, nullptr, nullptr, 0, 0, 0, F(h->RS), 0, nullptr}, 0);
     // levels, top first: W[u] = RS[root slot] (roots) + sum of the parents' W
     for (int64_t k = h->L; k >= 1; --k)
         add(LeftStep{I(h->poff), I(h->pref), F(h->W), nullptr, nullptr, F(h->RS), h->lvl_off[k], h->lvl_roots[k],
-                     h->root_off[k], F(h->W), 0},
+                     h->root_off[k], F(h->W), 0, nullptr},
             k);
     // terminals: TIN[p] = RS[rho + p] + sum of the W of the nodes naming p
-    add(LeftStep{I(h->toff), I(h->tref), F(h->W), nullptr, nullptr, F(h->RS), 0, h->alpha, h->rho, F(h->TIN), 0},
+    add(LeftStep{I(h->toff), I(h->tref), F(h->W), nullptr, nullptr, F(h->RS), 0, h->alpha, h->rho, F(h->TIN), 0,
+                 nullptr},
         h->L + 1);
     // columns: x[j] = sum over column j's terminals of V[l] * TIN[p]
-    add(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), F(h->V), nullptr, 0, 0, 0, x, 0}, h->L + 2);
+    add(LeftStep{I(h->coff), nullptr, F(h->TIN), I(h->vidx), F(h->V), nullptr, 0, 0, 0, x, 0, nullptr}, h->L + 2);
     return out;
 }
 
@@ -342,42 +369,50 @@ void left_run(gc_left_handle* h, const void* y, void* x, cudaStream_t st) {
 }
 
 // x <- x (+) (M^T x) from x0 until nothing changes, at most max_iter products;
-// M^T x goes to the arena's tmp. Writes the product count (or -1) to iters
-// on the device; false if max_iter was reached first.
+// M^T x goes to the arena's tmp. The loop runs on the device: products (the
+// handle's graph) and update steps are enqueued in batches of 1, 2, 4, 8, 8,
+// ... with no host round trip inside a batch; the update step's last CTA
+// records convergence and the kernels enqueued after it return at once; one
+// stream synchronise a batch. The loop's words are cleared at the end, so
+// later products run. Writes the product count (or -1) to iters on the
+// device; false if max_iter was reached first.
 template <class Op>
 bool left_fixpoint(gc_left_handle* h, const typename Op::V* x0, typename Op::V* x, int32_t max_iter, int32_t* iters,
                    cudaStream_t st) {
     using V = typename Op::V;
     const int64_t n = h->n;
     V* t = reinterpret_cast<V*>(h->arena + h->tmp);
-    int32_t* changed = reinterpret_cast<int32_t*>(h->arena + h->flag);
+    int32_t* ctl = reinterpret_cast<int32_t*>(h->arena + h->flag);
     if (x != x0 && n > 0) cuda_ok(cudaMemcpyAsync(x, x0, n * sizeof(V), cudaMemcpyDeviceToDevice, st), "x0 copy");
-    int32_t it = 0, done = 0;
+    cuda_ok(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
+    int32_t it = 0, batch = 1, result = -1;
+    bool done = false;
     int64_t launches = 0;
-    while (it < max_iter) {
-        ++it;
-        cuda_ok(cudaMemsetAsync(changed, 0, 4, st), "flag clear");
-        left_run(h, x, t, st);
-        launches += h->launches;
-        if (n > 0) {
-            const int64_t grid = std::min<int64_t>((n + kLeftThreads - 1) / kLeftThreads, (int64_t)h->sms * 8);
-            left_update_kernel<Op><<<(unsigned)std::max<int64_t>(grid, 1), kLeftThreads, 0, st>>>(x, t, n, changed);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((n + kLeftThreads - 1) / kLeftThreads, (int64_t)h->sms * 8));
+    while (it < max_iter && !done) {
+        const int32_t nb = std::min(batch, max_iter - it);
+        for (int32_t j = 0; j < nb; ++j) {
+            ++it;
+            left_run(h, x, t, st);
+            launches += h->launches;
+            left_update_loop_kernel<Op><<<(unsigned)grid, kLeftThreads, 0, st>>>(x, t, n, ctl, it);
             ++launches;
         }
         cuda_ok(cudaGetLastError(), "kernel launch");
-        int32_t c = 0;
-        cuda_ok(cudaMemcpyAsync(&c, changed, 4, cudaMemcpyDeviceToHost, st), "flag read");
+        int32_t w[4] = {0, 0, 0, 0};
+        cuda_ok(cudaMemcpyAsync(w, ctl, 16, cudaMemcpyDeviceToHost, st), "loop words read");
         cuda_ok(cudaStreamSynchronize(st), "stream synchronize");
-        if (!c) {
-            done = 1;
-            break;
+        if (w[1]) {
+            done = true;
+            result = w[3];
         }
+        batch = std::min(batch * 2, 8);
     }
     h->launches = launches;
-    const int32_t result = done ? it : -1;
+    cuda_ok(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");   // later products run again
     cuda_ok(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
     cuda_ok(cudaStreamSynchronize(st), "stream synchronize");
-    return done != 0;
+    return done;
 }
 
 }  // namespace
@@ -456,6 +491,9 @@ gc_status gc_left_upload(const gc_grammar* gg, gc_policy policy, void* arena, in
             put(st, a, h->V, v);
         }
         put(st, a, h->task, p.task);
+        // the fixpoint loop's words: clear, so products run (a nonzero
+        // converged word makes every step return at once)
+        cuda_ok(cudaMemsetAsync(a + h->flag, 0, 256, st), "loop words clear");
         cuda_ok(cudaStreamSynchronize(st), "left upload synchronize");
         *out = h.release();
     });

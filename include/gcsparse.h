@@ -215,6 +215,26 @@ gc_status gc_upload(const gc_grammar* g, gc_policy policy, int32_t k_max, void* 
                     int64_t arena_bytes, void* stream, gc_handle** out);
 
 /*
+ * gc_layout_ex / gc_upload_ex -- the same with the schedule chosen at upload:
+ * GC_SCHED_PERSISTENT or GC_SCHED_PER_LEVEL (the layout of gc_layout /
+ * gc_upload; the handle starts with that schedule), or GC_SCHED_DATAFLOW
+ * (k_max = 1 only, else GC_ERR_UNSUPPORTED): the dataflow sweep's own layout
+ * -- the levels cut into blocks with their dependency lists, three level
+ * buffers, per-block ready flags -- on which the products run that schedule
+ * (or its per-level launch sequence, GC_SCHED_PER_LEVEL). Its arena differs
+ * from gc_layout's, so size it with gc_layout_ex and the same schedule. The
+ * layout is the pages' level-synchronous sweep (Lemma 3.3) with the barrier
+ * between levels replaced by per-block dependencies; on the 10,000 x 50,000
+ * genotype grammar it measured slower than the persistent sweep (the latency
+ * of a dependency hop exceeds that of a grid barrier there), so it is not
+ * the default. Unknown schedules: GC_ERR_ARG.
+ */
+gc_status gc_layout_ex(const gc_grammar* g, gc_policy policy, int32_t k_max, int32_t schedule,
+                       gc_arena_layout* out);
+gc_status gc_upload_ex(const gc_grammar* g, gc_policy policy, int32_t k_max, int32_t schedule, void* arena,
+                       int64_t arena_bytes, void* stream, gc_handle** out);
+
+/*
  * gc_matvec -- y = M x on the device (Lemmas 2.1-2.2, Theorem 2.3, Sec. 4.3,
  * Appendix A for k > 1). Asynchronous on stream.
  *   x   device, m*k elements, row-major (x[j*k + c] is column j of input c)
@@ -253,12 +273,11 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
  *            nothing; -1 if max_iter was reached first.
  * Returns GC_ERR_NOT_CONVERGED (and records it in the status word, which
  * gc_check reports once) if max_iter products did not reach the fixpoint.
- * On handles with k_max = 1 (the dataflow schedule) the loop runs on the
- * device: products and update steps are enqueued in batches of 1, 2, 4, 8,
- * 8, ... with no host round trip inside a batch; the last update step to
- * finish records convergence, after which the kernels of the products
- * already enqueued return at once (x is unchanged by them). The stream is
- * synchronised once per batch. Other handles synchronise once per product.
+ * The loop runs on the device: products and update steps are enqueued in
+ * batches of 1, 2, 4, 8, 8, ... with no host round trip inside a batch; the
+ * last update step to finish records convergence, after which the kernels of
+ * the products already enqueued return at once (x is unchanged by them). The
+ * stream is synchronised once per batch.
  */
 gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
                    int32_t* iters, void* stream);
@@ -280,8 +299,7 @@ gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_it
  *            nothing; -1 if max_iter was reached first.
  * Returns GC_ERR_NOT_CONVERGED (also recorded in the status word) if
  * max_iter products did not reach the fixpoint. The loop runs on the device
- * as described for gc_reach (handles with k_max = 1; a k_max = 16 handle
- * synchronises once per product).
+ * as described for gc_reach.
  */
 gc_status gc_sssp(gc_handle* h, const float* x0, float* x, int32_t max_iter, int32_t* iters,
                   void* stream);
@@ -303,18 +321,17 @@ gc_status gc_launch_count(const gc_handle* h, int64_t* launches);
  *                        supports cooperative launch)
  *   GC_SCHED_PER_LEVEL   one kernel per level plus the emit kernels, the
  *                        launch sequence of Listing 1 of the pages
- *   GC_SCHED_DATAFLOW    handles with k_max = 1 (one value a node) only, and
- *                        their default: the levels are cut into blocks of
- *                        consecutive nodes; one cooperative kernel stages
- *                        each block's node pairs and the slices of the level
- *                        below that hold its children in shared memory (bulk
- *                        copies), and starts a block once the blocks it reads
- *                        have raised their ready flags (bounded waits), so no
- *                        grid barrier separates the levels (Lemma 3.3's
- *                        dependency, block by block); the narrow top levels
- *                        run as one block in shared memory. Then the emit.
- *                        On such a handle GC_SCHED_PERSISTENT selects this
- *                        schedule; on other handles it is GC_ERR_UNSUPPORTED. */
+ *   GC_SCHED_DATAFLOW    handles uploaded for it (gc_upload_ex): the levels
+ *                        are cut into blocks of consecutive nodes; one
+ *                        cooperative kernel stages each block's node pairs in
+ *                        shared memory (a bulk copy) and starts the block once
+ *                        the blocks that write its children have raised their
+ *                        ready flags (bounded waits), so no grid barrier
+ *                        separates the levels (Lemma 3.3's dependency, block by
+ *                        block); the narrow top levels run as one block in
+ *                        shared memory. Then the emit. On such a handle
+ *                        GC_SCHED_PERSISTENT selects this schedule; on other
+ *                        handles GC_SCHED_DATAFLOW is GC_ERR_UNSUPPORTED.      */
 enum { GC_SCHED_PERSISTENT = 0, GC_SCHED_PER_LEVEL = 1, GC_SCHED_DATAFLOW = 2 };
 gc_status gc_set_schedule(gc_handle* h, int32_t schedule);
 /* The schedule products actually use (PER_LEVEL when cooperative launch is

@@ -37,7 +37,8 @@ static int check_flow(const Grammar& g, int64_t vb, const std::vector<int64_t>& 
     std::vector<std::vector<double>> buf(3, std::vector<double>((size_t)p.buf_values, 1e300));
     std::vector<double> rv((size_t)g.n_roots, 1e300);
     int64_t regular = 0, finals = 0, staged = 0, nodes = 0, ngran = 0;
-    for (int64_t b = 0; b < p.nblocks; ++b) {
+    for (int64_t q = 0; q < p.nblocks; ++q) {   // in the processing order
+        const int64_t b = p.order[q];
         const int32_t* f = p.blk.data() + b * kFlowBlkInts;
         const int64_t k0 = f[FB_K0], k1 = f[FB_K1];
         const std::vector<double>& prev = buf[(k0 + 2) % 3];

@@ -222,6 +222,13 @@ def test_device_plans_pass_host_checks(gcs, k_max):
             lay = G.layout(pol, k_max)
             with pytest.raises(gcs.GcError, match="GC_ERR_CUDA"):
                 gcs.capi.gc_upload(G._p, pol, k_max, 256, lay["arena_bytes"])
+            if k_max == 1:   # the dataflow layout: block plan and its checks
+                lay = G.layout(pol, 1, "dataflow")
+                with pytest.raises(gcs.GcError, match="GC_ERR_CUDA"):
+                    gcs.capi.gc_upload_ex(G._p, pol, 1, "dataflow", 256, lay["arena_bytes"])
+            else:
+                with pytest.raises(gcs.GcError, match="GC_ERR_UNSUPPORTED"):
+                    G.layout(pol, k_max, "dataflow")
 
 
 def test_dataflow_block_plan(gcs, tmp_path):

@@ -7,8 +7,9 @@ two ways: by gc_build with block_rows (blocks compressed one after the other
 in one call) and by the streaming builder (Grammar.from_row_blocks, blocks
 compressed concurrently as they are generated). Both must be the same grammar
 (blocks merged level by level, rules numbered block after block), and every
-row of y = M x must match the float64 oracle at k = 1 (dataflow sweep, slice
-emit) and k = 16 (level emit), with the two builds giving the same bits.
+row of y = M x must match the float64 oracle at k = 1 (persistent sweep and
+the dataflow schedule, slice emit) and k = 16 (level emit), with the two builds
+giving the same bits.
 """
 import numpy as np
 import pytest
@@ -58,13 +59,18 @@ def test_blocked_every_row(gcs, torch, blocked, k):
     ys = []
     for G in (G1, G2):
         eng = gcs.Engine(G, "f32", k)
-        if k == 1:
-            assert eng.schedule == "dataflow"
+        assert eng.schedule == "persistent"
         Y = eng.matvec(torch.from_numpy(X).cuda()).cpu().numpy()
         assert eng.check() == 0
         ok, worst = direct.within_tolerance(Y, y_ref, b, TOL)
         assert ok, f"k={k}: max scaled error {worst:.3e}"
         ys.append(Y)
+        if k == 1:   # the dataflow schedule's own layout: the same bits
+            eng_d = gcs.Engine(G, "f32", 1, schedule="dataflow")
+            Yd = eng_d.matvec(torch.from_numpy(X).cuda()).cpu().numpy()
+            assert eng_d.check() == 0
+            ok, worst = direct.within_tolerance(Yd, y_ref, b, TOL)
+            assert ok, f"dataflow: max scaled error {worst:.3e}"
         lay = G.layout("f32", k)
         if k == 1:
             assert lay["grammar_bytes"] + lay["scratch_bytes"] < lay["csr_bytes"]

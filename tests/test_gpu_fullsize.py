@@ -1,7 +1,7 @@
 """Full-size parity, in the launch configuration bench.py times.
 
 * 10,000 x 50,000 genotype matrix (2.3e8 non-zeros, one grammar): every row of
-  y = G beta against the float64 oracle, dataflow schedule; every row of a
+  y = G beta against the float64 oracle, persistent schedule; every row of a
   16-wide product.
 * 2,000,000-node copy-model graph (about 2e8 edges): the Boolean product and the
   reachability fixpoint from 64 sources, bit for bit against the oracle.
@@ -46,7 +46,7 @@ def test_medium_single_vector_all_rows(gcs, torch, medium):
     st = G.stats()
     assert st["nnz"] == rp[-1] and st["depth"] >= 10
     eng = gcs.Engine(G, "f32", 1)
-    assert eng.schedule == "dataflow"
+    assert eng.schedule == "persistent"
     for seed in (0, 99):
         x = gcsynth.beta(gen["m"], seed=seed)
         y = eng.matvec(torch.from_numpy(x).cuda()).cpu().numpy()

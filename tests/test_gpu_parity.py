@@ -222,7 +222,8 @@ def test_dataflow_and_per_level_agree(gcs, torch, policy):
         if policy == "or":
             v_ = np.ones_like(v_)
         G = gcs.Grammar(n, m, rp_, c_, v_)
-        eng = gcs.Engine(G, policy, 1)
+        assert gcs.Engine(G, policy, 1).schedule == "persistent"     # the default layout
+        eng = gcs.Engine(G, policy, 1, schedule="dataflow")
         assert eng.schedule == "dataflow"
         rng = np.random.default_rng(n)
         if policy == "f32":
@@ -254,6 +255,46 @@ def test_dataflow_and_per_level_agree(gcs, torch, policy):
         for _ in range(3):
             np.testing.assert_array_equal(eng.matvec(xd).cpu().numpy().view(np.uint8), y_d.view(np.uint8))
         assert eng.check() == 0
+
+
+def test_dataflow_fixpoints_and_timeout(gcs, torch):
+    # the Boolean and tropical fixpoints on dataflow handles (device-side
+    # loop), against the oracle; then a dependency wait that runs out (CTA 0
+    # never publishes its first block) is reported, not hung, and the handle
+    # computes correctly after gc_check
+    rp, col = gcsynth.copy_model_graph(nodes=20000, n0=40, d0=20, p_edit=0.05, seed=3)
+    n = 20000
+    ones = np.ones(len(col), np.float32)
+    G = gcs.Grammar(n, n, rp, col, ones)
+    srcs = gcsynth.sources(n, 64, 3)
+    eng = gcs.Engine(G, "or", 1, schedule="dataflow")
+    x0 = gcsynth.frontier(n, srcs)
+    x, iters, rc = eng.reach(_dev(torch, x0.view(np.int64)))
+    assert rc == 0 and iters >= 2
+    want, want_iters = reach.fixpoint(rp, col, x0)
+    np.testing.assert_array_equal(x.cpu().numpy().view(np.uint64), want)
+    assert iters == want_iters
+    mp = gcs.Engine(G, "minplus", 1, schedule="dataflow")
+    d0 = gcsynth.frontier_distances(n, srcs)
+    d, it2, rc2 = mp.sssp(_dev(torch, d0))
+    assert rc2 == 0
+    want_d, want_it = reach.sssp_fixpoint(rp, col, ones, d0)
+    np.testing.assert_array_equal(d.cpu().numpy().view(np.uint32), want_d.view(np.uint32))
+    assert it2 == want_it
+    # the injected timeout
+    cfg = dict(gcsynth.GENO_MEDIUM, n=200)
+    rp3, c3, v3 = gcsynth.genotype_csr(**cfg)
+    G3 = gcs.Grammar(200, cfg["m"], rp3, c3, v3)
+    e3 = gcs.Engine(G3, "f32", 1, schedule="dataflow")
+    xg = _dev(torch, gcsynth.beta(cfg["m"], seed=5))
+    y_ok = e3.matvec(xg).cpu().numpy()
+    gcs.capi.gc_debug_inject(e3._h, 1, 2_000_000)
+    e3.matvec(xg)
+    torch.cuda.synchronize()
+    assert e3.check() == gcs.capi.GC_ERR_TIMEOUT
+    gcs.capi.gc_debug_inject(e3._h, 0, 4_000_000_000)
+    np.testing.assert_array_equal(e3.matvec(xg).cpu().numpy(), y_ok)
+    assert e3.check() == 0
 
 
 def test_barrier_timeout_is_reported_not_hung(gcs, torch):

@@ -58,21 +58,22 @@ def _oracle_check(policy, rp, c, v, x_np, y):
 
 
 CASES = [
-    ("small", "f32", 1, 1), ("small", "f32", 16, 16), ("small", "f32", 16, 4),
-    ("rows600", "f32", 1, 1),
-    ("small", "i64", 1, 1), ("small", "or", 1, 1),
-    ("small", "minplus", 1, 1), ("small", "minplus", 16, 16),
+    ("small", "f32", 1, 1, "persistent"), ("small", "f32", 16, 16, "persistent"),
+    ("small", "f32", 16, 4, "persistent"), ("rows600", "f32", 1, 1, "persistent"),
+    ("small", "i64", 1, 1, "persistent"), ("small", "or", 1, 1, "persistent"),
+    ("small", "minplus", 1, 1, "persistent"), ("small", "minplus", 16, 16, "persistent"),
+    ("small", "f32", 1, 1, "dataflow"), ("rows600", "or", 1, 1, "dataflow"),
 ]
 
 
-@pytest.mark.parametrize("mat,policy,k_max,k", CASES)
-def test_static_scratch_matches_matvec(gcs, torch, mat, policy, k_max, k):
+@pytest.mark.parametrize("mat,policy,k_max,k,schedule", CASES)
+def test_static_scratch_matches_matvec(gcs, torch, mat, policy, k_max, k, schedule):
     cfg = gcsynth.GENO_SMALL if mat == "small" else dict(gcsynth.GENO_MEDIUM, n=600)
     rp, c, v = gcsynth.genotype_csr(**cfg)
     if policy == "or":
         v = np.ones_like(v)
     G = gcs.Grammar(cfg["n"], cfg["m"], rp, c, v)
-    eng = gcs.Engine(G, policy, k_max)
+    eng = gcs.Engine(G, policy, k_max, schedule=schedule)
     capi = gcs.capi
     stream = torch.cuda.current_stream()
     shape = (cfg["n"],) if k == 1 else (cfg["n"], k)
