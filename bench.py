@@ -68,6 +68,11 @@ WORKLOADS = {
     # the same products under the dataflow schedule (its own layout)
     "geno_10k_50k_dataflow": dict(gen=gcsynth.GENO_MEDIUM, k=1, schedule="dataflow"),
     "graph_2m_dataflow": dict(graph=gcsynth.GRAPH, k=1, schedule="dataflow"),
+    # the same matrices over the height-balanced (AVL) grammar
+    "geno_10k_50k_balanced": dict(gen=gcsynth.GENO_MEDIUM, k=1, balance=True),
+    "geno_10k_50k_k16_balanced": dict(gen=gcsynth.GENO_MEDIUM, k=16, balance=True),
+    "geno_50k_200k_balanced": dict(gen=gcsynth.GENO_LARGE, k=1, balance=True),
+    "graph_2m_balanced": dict(graph=gcsynth.GRAPH, k=1, balance=True),
 }
 L2_FLUSH_BYTES = 512 << 20
 
@@ -454,13 +459,20 @@ def run_ours(args):
     if graph:
         gp = wl["graph"]
         gen = dict(n=gp["nodes"], m=gp["nodes"])
-        G = gcs.cached_grammar(f"graph:{sorted(gp.items())}", lambda: make_graph(gp))
+        key = f"graph:{sorted(gp.items())}"
+        load = lambda: gcs.cached_grammar(key, lambda: make_graph(gp))  # noqa: E731
     else:
         gen = wl["gen"]
+        key = f"genotype:{sorted(gen.items())}"
         if "block_rows" in gen:
-            G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", None, build=lambda: make_blocked(gcs, gen))
+            load = lambda: gcs.cached_grammar(key, None, build=lambda: make_blocked(gcs, gen))  # noqa: E731
         else:
-            G = gcs.cached_grammar(f"genotype:{sorted(gen.items())}", lambda: make_csr(gen))
+            load = lambda: gcs.cached_grammar(key, lambda: make_csr(gen))  # noqa: E731
+    if wl.get("balance"):
+        G = gcs.cached_grammar(key + ":balanced", None, build=lambda: load().balanced(),
+                               extra_sources=("balance.cpp",))
+    else:
+        G = load()
     build_s = time.perf_counter() - t0
     st = G.stats()
     policy, elem, dtype_name = workload_policy(wl)
@@ -663,6 +675,7 @@ def run_ours(args):
                    **({"graph": "copy model, unit edge lengths" if minplus else "copy model, 64-bit source bitsets"}
                       if graph else
                       {"founders": gen["founders"], "switch": gen["switch"], "mutation": gen["mutation"]}),
+                   "grammar": "RePair, AVL height-balanced" if wl.get("balance") else "RePair",
                    "l2": "flushed before every step (512 MB write, outside the events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

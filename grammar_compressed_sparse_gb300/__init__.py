@@ -77,6 +77,12 @@ class Grammar:
     def widths(self) -> np.ndarray:
         return _capi().gc_widths(self._p)
 
+    def balanced(self) -> "Grammar":
+        """The same expansions as an AVL-balanced grammar (a new Grammar;
+        products over it equal this one's, the level count L drops to about
+        1.44 log2 of the longest rule expansion)."""
+        return Grammar(_ptr=_capi().gc_balance(self._p))
+
     def export(self, which: str) -> np.ndarray:
         return _capi().gc_export(self._p, which)
 
@@ -249,28 +255,29 @@ class LeftEngine:
             self._h = None
 
 
-def _builder_fingerprint() -> str:
+def _builder_fingerprint(extra=()) -> str:
     from . import build as _b
     h = hashlib.sha256()
-    for f in _b.BUILDER_FILES:
+    for f in list(_b.BUILDER_FILES) + list(extra):
         with open(os.path.join(_b.CSRC, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def cached_grammar(key: str, make_csr, cache_dir=None, build=None, **build_kwargs) -> Grammar:
+def cached_grammar(key: str, make_csr, cache_dir=None, build=None, extra_sources=(), **build_kwargs) -> Grammar:
     """Build a grammar, reusing a saved copy when one exists.
 
     ``make_csr()`` returns (n, m, row_ptr, col, val); alternatively
     ``build()`` returns the Grammar itself (a streaming build). The file name
     combines ``key``, the build options and a hash of the builder's sources,
-    so a changed builder never reuses an old file. A file that fails to load
+    so a changed builder never reuses an old file (``extra_sources`` names
+    further csrc files the build depends on). A file that fails to load
     or validate is rebuilt. Set GCSPARSE_NO_CACHE=1 to always rebuild.
     """
     cache_dir = cache_dir or os.environ.get("GCSPARSE_CACHE",
                                             os.path.join(os.path.expanduser("~"), ".cache", "gcsparse"))
     tag = hashlib.sha256(repr((key, sorted(build_kwargs.items()))).encode()).hexdigest()[:16]
-    path = os.path.join(cache_dir, f"{tag}-{_builder_fingerprint()}.gcg")
+    path = os.path.join(cache_dir, f"{tag}-{_builder_fingerprint(extra_sources)}.gcg")
     if os.environ.get("GCSPARSE_NO_CACHE") != "1" and os.path.exists(path):
         try:
             return Grammar.load(path)

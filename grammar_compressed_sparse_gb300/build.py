@@ -19,11 +19,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgcsparse.so")
 
-HOST_SOURCES = ["csrv.cpp", "repair.cpp", "layer.cpp", "capi_host.cpp"]
+HOST_SOURCES = ["csrv.cpp", "repair.cpp", "layer.cpp", "balance.cpp", "capi_host.cpp"]
 CUDA_SOURCES = ["engine.cu", "left.cu"]
 HEADERS = ["common.hpp", "layout.hpp", "flow.hpp", "policy.cuh", "left.hpp"]
-# what a saved grammar depends on (the builder and its file format)
-BUILDER_FILES = HOST_SOURCES + ["common.hpp", "layout.hpp"]
+# what a saved grammar depends on (the builder and its file format); a
+# balanced grammar adds balance.cpp (cached_grammar's extra_sources)
+BUILDER_FILES = ["csrv.cpp", "repair.cpp", "layer.cpp", "capi_host.cpp", "common.hpp", "layout.hpp"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 _lock = threading.Lock()

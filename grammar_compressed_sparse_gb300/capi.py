@@ -70,6 +70,7 @@ _sig = {
     "gc_version": ([], ctypes.c_char_p),
     "gc_build": ([_i64, _i64, _vp, _vp, _vp, ctypes.POINTER(BuildOpts), ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_stats": ([_vp, ctypes.POINTER(GrammarStats)], ctypes.c_int),
+    "gc_balance": ([_vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_widths": ([_vp, _vp, _i64], ctypes.c_int),
     "gc_export_size": ([_vp, ctypes.c_int, ctypes.POINTER(_i64)], ctypes.c_int),
     "gc_export": ([_vp, ctypes.c_int, _vp, _i64], ctypes.c_int),
@@ -151,6 +152,12 @@ def gc_build(n, m, row_ptr, col, val=None, block_rows=0, threads=0, order=0) -> 
     opts = BuildOpts(block_rows, threads, order)
     _check(_lib.gc_build(n, m, _addr(row_ptr), _addr(col), _addr(val), ctypes.byref(opts),
                          ctypes.byref(out)), "gc_build")
+    return out.value
+
+
+def gc_balance(g):
+    out = _vp()
+    _check(_lib.gc_balance(g, ctypes.byref(out)), "gc_balance")
     return out.value
 
 

@@ -273,6 +273,29 @@ gc_status gc_build(int64_t n, int64_t m, const int64_t* row_ptr, const int32_t* 
     });
 }
 
+gc_status gc_balance(const gc_grammar* gg, gc_grammar** out) {
+    return guard([&] {
+        if (!gg || !out) fail(GC_ERR_ARG, "null argument");
+        *out = nullptr;
+        const Grammar& g = gg->g;
+        const double t0 = now_seconds();
+        auto G = std::make_unique<gc_grammar>();
+        Grammar& b = G->g;
+        b.n = g.n;
+        b.m = g.m;
+        b.nnz = g.nnz;
+        b.V = g.V;
+        b.term_col = g.term_col;
+        b.term_vidx = g.term_vidx;
+        b.n_blocks = g.n_blocks;
+        b.slp = balance_slp(g.slp);
+        b.repair_seconds = g.repair_seconds + (now_seconds() - t0);
+        layer_and_pack(b, 0);
+        validate_packed(b);
+        *out = G.release();
+    });
+}
+
 gc_status gc_stats(const gc_grammar* gg, gc_grammar_stats* out) {
     return guard([&] {
         if (!gg || !out) fail(GC_ERR_ARG, "null argument");

@@ -97,6 +97,10 @@ void layer_and_pack(Grammar& g, int order);
 // Host-side validation of the packed arrays (bounds of every reference).
 void validate_packed(const Grammar& g);
 
+// Sec. 4.2 pre-balancing: the same expansions as an AVL grammar (children's
+// heights differ by at most one), rules in creation order, C remapped.
+Slp balance_slp(const Slp& s);
+
 // Runs f at the C ABI boundary: maps exceptions to a status and records the
 // message for gc_last_error().
 template <class F>

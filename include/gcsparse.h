@@ -174,6 +174,21 @@ gc_status gc_builder_add_rows(gc_builder* b, int64_t r0, int64_t rows, const int
 gc_status gc_builder_finish(gc_builder* b, gc_grammar** out);
 void gc_builder_free(gc_builder* b);
 
+/*
+ * gc_balance -- height balancing of a built grammar (Sec. 4.2 names
+ * pre-balancing to a logarithmic height; Sec. 8 leaves it to future work).
+ * The pages give no construction; this one rebuilds the rules bottom-up as an
+ * AVL grammar: each rule becomes the join of its children's balanced forms,
+ * so the two children of every rule differ in height by at most one and the
+ * depth L is at most about 1.44 log2 of the longest expansion. Rules with the
+ * same (left, right) pair are made once; rules C no longer reaches are
+ * dropped. Expansions are unchanged, so products over the result equal the
+ * original's. The result is layered and packed like gc_build's (default
+ * order); *out is a new library-owned grammar (gc_free_grammar). Host memory
+ * only. Errors: GC_ERR_ARG, GC_ERR_UNSUPPORTED (over 2^31-1 rules).
+ */
+gc_status gc_balance(const gc_grammar* g, gc_grammar** out);
+
 /* Structural figures of a built grammar (Table 4.1's |R|, L, w*, +pt).      */
 gc_status gc_stats(const gc_grammar* g, gc_grammar_stats* out);
 

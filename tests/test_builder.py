@@ -27,7 +27,7 @@ def _cases():
 CASES = list(_cases())
 
 
-def check_grammar(G, rp, c, v, n, m, block_rows=0):
+def check_grammar(G, rp, c, v, n, m, block_rows=0, repair_end_state=True):
     ex = export_all(G)
     st = G.stats()
     og = oracle_grammar(ex)
@@ -44,7 +44,7 @@ def check_grammar(G, rp, c, v, n, m, block_rows=0):
         for i in range(len(row) - 1):
             key = (blk, row[i], row[i + 1])
             seen[key] = seen.get(key, 0) + 1
-    assert all(cnt < 2 for cnt in seen.values())
+    assert all(cnt < 2 for cnt in seen.values()) or not repair_end_state
     for i, (a, b) in enumerate(og["R"]):
         assert (a < 0 or a < i) and (b < 0 or b < i)
     # O4: Eq. 3.1 levels, live-set widths, pass-through count
@@ -522,3 +522,28 @@ def test_cpu_grammar_sweep_on_the_builders_grammar(gcs):
     y = sw(x, 1)
     assert direct.within_tolerance(y, y_ref, b, 1e-12)[0]
     assert np.array_equal(sw(x, 4), y)
+
+
+@pytest.mark.parametrize("name,rp,c,v", CASES[-4:], ids=[cs[0] for cs in CASES[-4:]])
+def test_balanced_grammar(gcs, name, rp, c, v):
+    """Sec. 4.2 pre-balancing (an AVL grammar): same decompression, same
+    products, children's heights within one of each other, and depth within
+    the AVL bound 1.4405 log2(len + 2) of the longest expansion."""
+    n, m = len(rp) - 1, int(c.max()) + 3
+    G = gcs.Grammar(n, m, rp, c, v)
+    B = G.balanced()
+    ex = check_grammar(B, rp, c, v, n, m, repair_end_state=False)
+    og = oracle_grammar(ex)
+    lvl = grammar.levels(og["R"])
+    h = lambda s: 0 if s < 0 else int(lvl[s])
+    assert all(abs(h(a) - h(b)) <= 1 for a, b in og["R"])
+    lens = np.zeros(len(og["R"]), np.int64)
+    for i, (a, b) in enumerate(og["R"]):
+        lens[i] = (1 if a < 0 else lens[a]) + (1 if b < 0 else lens[b])
+    longest = int(lens.max()) if len(lens) else 1
+    assert B.stats()["depth"] <= 1.4405 * np.log2(longest + 2)
+    assert B.stats()["depth"] <= G.stats()["depth"]
+    # balancing a balanced grammar changes nothing
+    ex2 = export_all(B.balanced())
+    for key in ("nodes", "lvl_off", "c_ref"):
+        np.testing.assert_array_equal(ex2[key], ex[key])
