@@ -30,6 +30,15 @@ def _capi():
     return importlib.import_module(".capi", __name__)
 
 
+def _sync(stream):
+    """Wait for the work on ``stream`` (a torch stream, else the device)."""
+    import torch
+    if hasattr(stream, "synchronize"):
+        stream.synchronize()
+    else:
+        torch.cuda.synchronize()
+
+
 class Grammar:
     """A built grammar (host). ``Grammar(n, m, row_ptr, col, val)`` runs
     CSRV + RePair + levels + pass-through completion + packing."""
@@ -155,7 +164,9 @@ class Engine:
         import torch
         x = torch.empty_like(x0)
         iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
-        rc = _capi().gc_reach(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        st = stream if stream is not None else self._stream
+        rc = _capi().gc_reach(self._h, x0, x, max_iter, iters, st)
+        _sync(st)   # the call returns before its last batch and the iters write end
         return x, int(iters.item()), rc
 
     def sssp(self, x0, max_iter=1000, stream=None):
@@ -164,7 +175,9 @@ class Engine:
         import torch
         x = torch.empty_like(x0)
         iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
-        rc = _capi().gc_sssp(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        st = stream if stream is not None else self._stream
+        rc = _capi().gc_sssp(self._h, x0, x, max_iter, iters, st)
+        _sync(st)   # the call returns before its last batch and the iters write end
         return x, int(iters.item()), rc
 
     def check(self, stream=None) -> int:
@@ -239,7 +252,9 @@ class LeftEngine:
         import torch
         x = torch.empty_like(x0)
         iters = torch.zeros(1, dtype=torch.int32, device=x0.device)
-        rc = fn(self._h, x0, x, max_iter, iters, stream if stream is not None else self._stream)
+        st = stream if stream is not None else self._stream
+        rc = fn(self._h, x0, x, max_iter, iters, st)
+        _sync(st)   # the call returns before its last batch and the iters write end
         return x, int(iters.item()), rc
 
     def launch_count(self) -> int:

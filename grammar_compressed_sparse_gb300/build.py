@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libgcsparse.so")
 
 HOST_SOURCES = ["csrv.cpp", "repair.cpp", "layer.cpp", "balance.cpp", "capi_host.cpp"]
 CUDA_SOURCES = ["engine.cu", "left.cu"]
-HEADERS = ["common.hpp", "layout.hpp", "flow.hpp", "policy.cuh", "left.hpp"]
+HEADERS = ["common.hpp", "layout.hpp", "flow.hpp", "loop.hpp", "policy.cuh", "left.hpp"]
 # what a saved grammar depends on (the builder and its file format); a
 # balanced grammar adds balance.cpp (cached_grammar's extra_sources)
 BUILDER_FILES = ["csrv.cpp", "repair.cpp", "layer.cpp", "capi_host.cpp", "common.hpp", "layout.hpp"]

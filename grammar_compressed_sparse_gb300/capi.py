@@ -70,6 +70,7 @@ _sig = {
     "gc_version": ([], ctypes.c_char_p),
     "gc_build": ([_i64, _i64, _vp, _vp, _vp, ctypes.POINTER(BuildOpts), ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_stats": ([_vp, ctypes.POINTER(GrammarStats)], ctypes.c_int),
+    "gc_update": ([ctypes.c_int, _vp, _vp, ctypes.c_int64, _vp, _vp], ctypes.c_int),
     "gc_balance": ([_vp, ctypes.POINTER(_vp)], ctypes.c_int),
     "gc_widths": ([_vp, _vp, _i64], ctypes.c_int),
     "gc_export_size": ([_vp, ctypes.c_int, ctypes.POINTER(_i64)], ctypes.c_int),
@@ -233,6 +234,10 @@ def gc_reach(h, x0, x, max_iter, iters, stream=None) -> int:
     if rc not in (GC_OK, GC_ERR_NOT_CONVERGED):
         raise GcError(rc, "gc_reach")
     return rc
+
+
+def gc_update(policy, x, y, n, changed, stream=None):
+    _check(_lib.gc_update(POLICIES[policy], _addr(x), _addr(y), n, _addr(changed), _stream(stream)), "gc_update")
 
 
 def gc_sssp(h, x0, x, max_iter, iters, stream=None) -> int:

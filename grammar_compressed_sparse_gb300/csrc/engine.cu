@@ -48,6 +48,7 @@
 #include "common.hpp"
 #include "flow.hpp"
 #include "layout.hpp"
+#include "loop.hpp"
 #include "policy.cuh"
 
 struct gc_handle {
@@ -75,6 +76,7 @@ struct gc_handle {
     std::vector<int64_t> lvl_blk;   // first block of each level (L+2)
     uint32_t epoch = 0;
     const int32_t* conv = nullptr;   // during a device-side fixpoint loop: its converged word
+    gcs::LoopHost loop;              // the fixpoint loop's pinned words and events
 };
 
 namespace gcs {
@@ -1027,14 +1029,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
 __device__ __forceinline__ void mbar_expect_tx_only(uint64_t* b, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
 }
-// 16 bytes from global memory through L2 only (never a stale L1 line)
-__device__ __forceinline__ int4 ld_cg16(const void* p) {
-    int4 v;
-    asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(gaddr(p)));
-    return v;
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
@@ -1073,9 +1067,6 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(gaddr(p)) : "memory");
     return v;
-}
-__device__ __forceinline__ void st_release_u32(int32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(gaddr(p)), "r"(v) : "memory");
 }
 // one fence, then relaxed writes: together a release of both writes
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -1555,6 +1546,24 @@ struct MinUpdate {
     __device__ __forceinline__ static T apply(T u, T v) { return fminf(u, v); }
 };
 
+// One fixpoint step on rows a caller holds (a rank's share of a row-sharded
+// fixpoint): x = x (+) y; *changed = 1 if any element changed (untouched
+// otherwise: every writer stores the same value).
+template <class U>
+__global__ void __launch_bounds__(kThreads)
+update_rows_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y, int64_t n,
+                   int32_t* __restrict__ changed) {
+    int ch = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const typename U::T u = x[i], v = U::apply(u, y[i]);
+        if (v != u) {
+            x[i] = v;
+            ch = 1;
+        }
+    }
+    if (__syncthreads_or(ch) && threadIdx.x == 0) *changed = 1;
+}
+
 // Fixpoint control words (in the status block): ctl[0] changed in this
 // step, ctl[1] converged, ctl[2] CTAs of this step finished, ctl[3] the
 // product count at convergence. With ctl[1] set every later step (and, in the
@@ -1995,14 +2004,13 @@ void put(cudaStream_t st, char* arena, int64_t off, const T* p, size_t count) {
 
 // x <- x (+) (M (x) x) from x0 until nothing changes, at most max_iter
 // products; the product's y lives in the arena's staging area. The loop runs
-// on the device: products and update steps are enqueued in batches of 1, 2,
-// 4, 8, 8, ... with no host round trip inside a batch; the update step's last
-// CTA records convergence (ctl, in the status block) and every kernel
-// enqueued after it returns at once, keeping the barrier counters and level
-// counters consistent. One stream synchronise a batch reads the converged
-// word. Writes the product count (or -1) to iters on the device. Returns
-// false if max_iter was reached first (the status word then says
-// GC_ERR_NOT_CONVERGED).
+// on the device (drive_fixpoint): products and update steps are enqueued in
+// batches of 1, 2, 4, 8, 8, ..., one batch ahead of the one the host waits
+// for; the update step's last CTA records convergence (ctl, in the status
+// block) and every kernel enqueued after it returns at once, keeping the
+// barrier counters and level counters consistent. Writes the product count
+// (or -1) to iters on the device. Returns false if max_iter was reached first
+// (the status word then says GC_ERR_NOT_CONVERGED).
 template <class U>
 bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32_t max_iter, int32_t* iters,
                   cudaStream_t st) {
@@ -2011,40 +2019,35 @@ bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32
     T* yv = reinterpret_cast<T*>(h->arena + h->lay.ys);
     int32_t* status = reinterpret_cast<int32_t*>(h->arena + h->lay.status);
     int32_t* ctl = status + 4;   // changed, converged, CTAs done, product count (bytes 16..31)
+    after_last_loop(h->loop, st, cuda_check);
     if (x != x0 && n > 0)
         cuda_check(cudaMemcpyAsync(x, x0, n * sizeof(T), cudaMemcpyDeviceToDevice, st), "x0 copy");
     cuda_check(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
-    int32_t it = 0, batch = 1, result = -1;
-    bool done = false;
+    int32_t result = -1;
     int64_t launches = 0;
     h->conv = ctl + 1;
-    while (it < max_iter && !done) {
-        const int32_t nb = std::min(batch, max_iter - it);
-        for (int32_t j = 0; j < nb; ++j) {
-            ++it;
+    bool done = false;
+    try {
+        done = drive_fixpoint(h->loop, ctl, max_iter, st, cuda_check, [&](int32_t it) {
             dispatch_product(h, x, yv, 1, st);
             launches += h->launches;
             update_loop_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, ctl, it);
             ++launches;
-        }
-        cuda_check(cudaGetLastError(), "kernel launch");
-        int32_t w[4] = {0, 0, 0, 0};
-        cuda_check(cudaMemcpyAsync(w, ctl, 16, cudaMemcpyDeviceToHost, st), "loop words read");
-        cuda_check(cudaStreamSynchronize(st), "stream synchronize");
-        if (w[1]) {
-            done = true;
-            result = w[3];
-        }
-        batch = std::min(batch * 2, 8);
+        }, &result);
+    } catch (...) {
+        h->conv = nullptr;
+        if (h->loop.end && cudaEventRecord(h->loop.end, st) == cudaSuccess) h->loop.ended = true;
+        throw;
     }
     h->conv = nullptr;
     h->launches = launches;
+    // pageable sources: both copies take their value before they return
     cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
     if (!done) {
         int32_t sw = GC_ERR_NOT_CONVERGED;
         cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
     }
-    cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+    mark_loop_end(h->loop, st, cuda_check);
     return done;
 }
 
@@ -2362,6 +2365,7 @@ gc_status gc_matvec(gc_handle* h, const void* x, void* y, int32_t k, void* strea
         if ((!x && h->m > 0) || (!y && h->n > 0)) fail(GC_ERR_ARG, "null x or y");
         check_k(h, k);
         check_device(h);
+        after_last_loop(h->loop, static_cast<cudaStream_t>(stream), cuda_check);
         dispatch_product(h, x, y, k, static_cast<cudaStream_t>(stream));
     });
 }
@@ -2373,6 +2377,7 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
         check_k(h, k);
         check_device(h);
         cudaStream_t st = static_cast<cudaStream_t>(stream);
+        after_last_loop(h->loop, st, cuda_check);
         const int64_t eb = policy_elem_bytes(h->policy) * k;
         char* xs = h->arena + h->lay.xs;
         char* ys = h->arena + h->lay.ys;
@@ -2425,6 +2430,7 @@ gc_status gc_check(gc_handle* h, void* stream) {
         cudaStream_t st = static_cast<cudaStream_t>(stream);
         int32_t* status = reinterpret_cast<int32_t*>(h->arena + h->lay.status);
         int32_t s = 0;
+        after_last_loop(h->loop, st, cuda_check);
         cuda_check(cudaMemcpyAsync(&s, status, 4, cudaMemcpyDeviceToHost, st), "status read");
         cuda_check(cudaStreamSynchronize(st), "stream synchronize");
         if (s != 0) {
@@ -2445,6 +2451,29 @@ gc_status gc_check(gc_handle* h, void* stream) {
     if (g != GC_OK) return g;
     if (rc != GC_OK) set_last_error("device status word reported an error");
     return rc;
+}
+
+gc_status gc_update(gc_policy policy, void* x, const void* y, int64_t n, int32_t* changed, void* stream) {
+    return guard([&] {
+        if (policy != GC_BOOL_OR && policy != GC_F32_MIN_PLUS)
+            fail(GC_ERR_ARG, "gc_update needs the GC_BOOL_OR or GC_F32_MIN_PLUS policy");
+        if (n < 0 || !changed || (n > 0 && (!x || !y))) fail(GC_ERR_ARG, "null argument or negative n");
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cuda_check(cudaMemsetAsync(changed, 0, sizeof(int32_t), st), "changed clear");
+        if (n == 0) return;
+        int dev = 0, sms = 1;
+        cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+        cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+        const int grid = grid_for(n, kThreads, sms, 8);
+        if (policy == GC_BOOL_OR)
+            update_rows_kernel<OrUpdate><<<grid, kThreads, 0, st>>>(static_cast<unsigned long long*>(x),
+                                                                   static_cast<const unsigned long long*>(y), n,
+                                                                   changed);
+        else
+            update_rows_kernel<MinUpdate><<<grid, kThreads, 0, st>>>(static_cast<float*>(x),
+                                                                    static_cast<const float*>(y), n, changed);
+        cuda_check(cudaGetLastError(), "kernel launch");
+    });
 }
 
 gc_status gc_launch_count(const gc_handle* h, int64_t* launches) {
@@ -2496,6 +2525,7 @@ gc_status gc_matvec_static(gc_handle* h, const void* x, void* y, int32_t k, void
                                          " bytes of scratch; the fixed array holds " +
                                          std::to_string(kStaticScratchBytes));
         cudaStream_t st = static_cast<cudaStream_t>(stream);
+        after_last_loop(h->loop, st, cuda_check);
         unsigned char* scratch = static_scratch_on_current_device();
         switch (h->policy) {
             case GC_F32_SUM: for_f32_width<RunStatic>(k, h, x, y, st, scratch); break;

@@ -32,6 +32,7 @@
 #include "common.hpp"
 #include "layout.hpp"
 #include "left.hpp"
+#include "loop.hpp"
 
 struct gc_left_handle {
     gc_policy policy = GC_F32_SUM;
@@ -46,11 +47,13 @@ struct gc_left_handle {
     // the steps as a graph: its kernel nodes and the step set of each
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
+    gcs::LoopHost loop;   // the fixpoint loop's pinned words and events
     std::vector<cudaGraphNode_t> nodes;
     std::vector<int64_t> node_set;
     const void* y_last = nullptr;
     void* x_last = nullptr;
     ~gc_left_handle() {
+        if (loop.ended) (void)cudaEventSynchronize(loop.end);   // a fixpoint's last batch may still run
         if (exec) cudaGraphExecDestroy(exec);
         if (graph) cudaGraphDestroy(graph);
     }
@@ -369,13 +372,13 @@ void left_run(gc_left_handle* h, const void* y, void* x, cudaStream_t st) {
 }
 
 // x <- x (+) (M^T x) from x0 until nothing changes, at most max_iter products;
-// M^T x goes to the arena's tmp. The loop runs on the device: products (the
-// handle's graph) and update steps are enqueued in batches of 1, 2, 4, 8, 8,
-// ... with no host round trip inside a batch; the update step's last CTA
-// records convergence and the kernels enqueued after it return at once; one
-// stream synchronise a batch. The loop's words are cleared at the end, so
-// later products run. Writes the product count (or -1) to iters on the
-// device; false if max_iter was reached first.
+// M^T x goes to the arena's tmp. The loop runs on the device
+// (drive_fixpoint): products (the handle's graph) and update steps are
+// enqueued in batches of 1, 2, 4, 8, 8, ..., one batch ahead of the one the
+// host waits for; the update step's last CTA records convergence and the
+// kernels enqueued after it return at once. The loop's words are cleared at
+// the end, so later products run. Writes the product count (or -1) to iters
+// on the device; false if max_iter was reached first.
 template <class Op>
 bool left_fixpoint(gc_left_handle* h, const typename Op::V* x0, typename Op::V* x, int32_t max_iter, int32_t* iters,
                    cudaStream_t st) {
@@ -383,35 +386,29 @@ bool left_fixpoint(gc_left_handle* h, const typename Op::V* x0, typename Op::V* 
     const int64_t n = h->n;
     V* t = reinterpret_cast<V*>(h->arena + h->tmp);
     int32_t* ctl = reinterpret_cast<int32_t*>(h->arena + h->flag);
+    after_last_loop(h->loop, st, cuda_ok);
     if (x != x0 && n > 0) cuda_ok(cudaMemcpyAsync(x, x0, n * sizeof(V), cudaMemcpyDeviceToDevice, st), "x0 copy");
     cuda_ok(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
-    int32_t it = 0, batch = 1, result = -1;
-    bool done = false;
+    int32_t result = -1;
     int64_t launches = 0;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((n + kLeftThreads - 1) / kLeftThreads, (int64_t)h->sms * 8));
-    while (it < max_iter && !done) {
-        const int32_t nb = std::min(batch, max_iter - it);
-        for (int32_t j = 0; j < nb; ++j) {
-            ++it;
+    bool done = false;
+    try {
+        done = drive_fixpoint(h->loop, ctl, max_iter, st, cuda_ok, [&](int32_t it) {
             left_run(h, x, t, st);
             launches += h->launches;
             left_update_loop_kernel<Op><<<(unsigned)grid, kLeftThreads, 0, st>>>(x, t, n, ctl, it);
             ++launches;
-        }
-        cuda_ok(cudaGetLastError(), "kernel launch");
-        int32_t w[4] = {0, 0, 0, 0};
-        cuda_ok(cudaMemcpyAsync(w, ctl, 16, cudaMemcpyDeviceToHost, st), "loop words read");
-        cuda_ok(cudaStreamSynchronize(st), "stream synchronize");
-        if (w[1]) {
-            done = true;
-            result = w[3];
-        }
-        batch = std::min(batch * 2, 8);
+        }, &result);
+    } catch (...) {
+        if (h->loop.end && cudaEventRecord(h->loop.end, st) == cudaSuccess) h->loop.ended = true;
+        throw;
     }
     h->launches = launches;
     cuda_ok(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");   // later products run again
+    // a pageable source: the copy takes its value before it returns
     cuda_ok(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
-    cuda_ok(cudaStreamSynchronize(st), "stream synchronize");
+    mark_loop_end(h->loop, st, cuda_ok);
     return done;
 }
 
@@ -503,6 +500,7 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
     return guard([&] {
         if (!h) fail(GC_ERR_ARG, "null handle");
         if ((!y && h->n > 0) || (!x && h->m > 0)) fail(GC_ERR_ARG, "null y or x");
+        after_last_loop(h->loop, static_cast<cudaStream_t>(stream), cuda_ok);
         left_run(h, y, x, static_cast<cudaStream_t>(stream));
     });
 }

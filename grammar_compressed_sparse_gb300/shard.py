@@ -8,9 +8,13 @@ tropical fixpoints exchange once per iteration: every rank gathers the new
 vector (the next product reads all of x) and the ranks agree on whether
 anything changed (an all-reduce of the changed flag).
 
-The product itself is a callable, so the same logic runs with an Engine on a
-GPU (NCCL) and with a CPU stand-in in tests (gloo). Nothing here computes any
-part of the product.
+``ShardedEngine`` is the GPU path: each rank builds the grammar of its own
+row blocks, uploads it to its GPU and runs the library's products; the
+fixpoints' update step (x = x OR y, or min) runs in the library too
+(``gc_update``), and the exchanges go over the process group (NCCL). The loop
+itself (``sharded_fixpoint``) takes the product and the update as callables,
+so its exchange logic also runs with CPU stand-ins (gloo) in tests. Nothing
+here computes any part of the product.
 """
 from __future__ import annotations
 
@@ -58,9 +62,10 @@ def sharded_fixpoint(product, x0, shards, update, max_iter=1000, group=None):
     """x <- update(x, M x) to the fixpoint, M's rows sharded over the ranks.
 
     ``product(x)`` returns this rank's rows of M x for the whole vector x;
-    ``update(old_rows, new_rows)`` returns (rows, changed: bool) -- OR for
-    reachability, min for shortest paths. Each iteration gathers the rows of
-    every rank and all-reduces the changed flag (MAX of 0/1), so every rank
+    ``update(old_rows, new_rows)`` returns (rows, changed) -- OR for
+    reachability, min for shortest paths -- with changed a bool or a one-
+    element int32 tensor on x's device (0 or 1). Each iteration gathers the
+    rows of every rank and all-reduces the changed flag (MAX), so every rank
     stops at the same iteration. Returns (x, iterations) with iterations
     counting the products, the last of which changed nothing, or -1 if
     max_iter was reached first.
@@ -73,7 +78,10 @@ def sharded_fixpoint(product, x0, shards, update, max_iter=1000, group=None):
     x = x0.clone()
     for it in range(1, max_iter + 1):
         rows, changed = update(x[r0:r1], product(x))
-        flag = torch.tensor([1 if changed else 0], dtype=torch.int32, device=x.device)
+        if isinstance(changed, torch.Tensor):
+            flag = changed.to(device=x.device, dtype=torch.int32).reshape(1)
+        else:
+            flag = torch.tensor([1 if changed else 0], dtype=torch.int32, device=x.device)
         dist.all_reduce(flag, op=dist.ReduceOp.MAX, group=group)
         x = gather_rows(rows, shards, group)
         if int(flag.item()) == 0:
@@ -81,17 +89,75 @@ def sharded_fixpoint(product, x0, shards, update, max_iter=1000, group=None):
     return x, -1
 
 
-def or_update(old, new):
-    """Reachability step on this rank's rows: old | new, and whether it changed."""
-    out = old | new
-    return out, bool((out != old).any())
+def library_update(policy: str, stream=None):
+    """The fixpoint step of ``policy`` ("or" or "minplus") on a rank's rows,
+    in the library (gc_update): old rows updated in place, changed flag left
+    on the device."""
+    from . import _capi
+
+    def update(old, new):
+        import torch
+        changed = torch.empty(1, dtype=torch.int32, device=old.device)
+        st = stream if stream is not None else torch.cuda.current_stream(old.device)
+        _capi().gc_update(policy, old, new, old.numel(), changed, st)
+        return old, changed
+    return update
 
 
-def min_update(old, new):
-    """Shortest-path step on this rank's rows: min(old, new), and whether it changed."""
-    import torch
-    out = torch.minimum(old, new)
-    return out, bool((out != old).any())
+class ShardedEngine:
+    """This rank's share of a row-sharded matrix on its GPU.
+
+    ``rows_csr(r0, r1)`` returns the CSR (row_ptr from 0, col, val or None) of
+    rows [r0, r1); each rank builds and uploads the grammar of its own rows
+    (whole ``block_rows`` blocks when given). ``matvec`` returns the whole y
+    on every rank (one all-gather); ``matvec_rows`` only this rank's rows
+    (no exchange). ``reach`` / ``sssp`` run the fixpoints with one all-gather
+    and one all-reduce per iteration. Requires an initialised process group
+    whose backend handles device tensors (NCCL).
+    """
+
+    def __init__(self, n, m, rows_csr, policy="f32", k_max=1, block_rows=0, group=None, device=None,
+                 balance=False, threads=0):
+        import torch
+        import torch.distributed as dist
+        from . import Engine, Grammar
+
+        self.n, self.m, self.policy, self.group = n, m, policy, group
+        self.shards = row_shards(n, dist.get_world_size(group), block_rows)
+        self.r0, self.r1 = self.shards[dist.get_rank(group)]
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.engine = None
+        if self.r1 > self.r0:
+            rp, col, val = rows_csr(self.r0, self.r1)
+            g = Grammar(self.r1 - self.r0, m, rp, col, val, block_rows=block_rows, threads=threads)
+            if balance:
+                g = g.balanced()
+            self.engine = Engine(g, policy, k_max, device=self.device)
+
+    def matvec_rows(self, x, stream=None):
+        """This rank's rows of M x (x: the whole vector on this rank's device)."""
+        import torch
+        if self.engine is None:
+            shape = (0,) if x.dim() == 1 else (0, x.shape[1])
+            return torch.empty(shape, dtype=x.dtype, device=x.device)
+        return self.engine.matvec(x, stream=stream)
+
+    def matvec(self, x, stream=None):
+        """The whole M x on every rank."""
+        return gather_rows(self.matvec_rows(x, stream), self.shards, self.group)
+
+    def reach(self, x0, max_iter=1000):
+        """Boolean fixpoint x <- x OR (M (x) x) over the ranks; (x, iterations)."""
+        if self.policy != "or":
+            raise ValueError("reach needs the 'or' policy")
+        return sharded_fixpoint(self.matvec_rows, x0, self.shards, library_update("or"), max_iter, self.group)
+
+    def sssp(self, x0, max_iter=1000):
+        """Tropical fixpoint x <- min(x, M (x) x) over the ranks; (x, iterations)."""
+        if self.policy != "minplus":
+            raise ValueError("sssp needs the 'minplus' policy")
+        return sharded_fixpoint(self.matvec_rows, x0, self.shards, library_update("minplus"), max_iter,
+                                self.group)
 
 
 def local_rows(row_ptr, col, val, r0, r1):

@@ -292,10 +292,30 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
  * batches of 1, 2, 4, 8, 8, ... with no host round trip inside a batch; the
  * last update step to finish records convergence, after which the kernels of
  * the products already enqueued return at once (x is unchanged by them). The
- * stream is synchronised once per batch.
+ * host keeps one batch enqueued ahead of the one whose convergence words it
+ * waits for (an event on the stream), so the device does not idle between
+ * batches. The call returns once convergence (or max_iter) is known; the
+ * last batch's early-return kernels and the iters write may still be on the
+ * stream: synchronise it before reading x or iters on the host. Every later
+ * call on the handle (products, gc_check, another fixpoint), on any stream,
+ * is ordered after them. The first call pins 32 bytes of host memory and
+ * makes three events, released by gc_free_handle.
  */
 gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
                    int32_t* iters, void* stream);
+
+/*
+ * gc_update -- one fixpoint step on rows the caller holds: x[i] = x[i] OR y[i]
+ * (GC_BOOL_OR, uint64_t) or x[i] = min(x[i], y[i]) (GC_F32_MIN_PLUS, float),
+ * i < n, for a rank's share of a row-sharded fixpoint (Sec. 5's iteration,
+ * rows split over GPUs: each rank updates its own rows, then the ranks gather
+ * the new vector and agree on the changed flag).
+ *   x, y     device arrays of n values (x updated in place; no overlap)
+ *   changed  device int32_t[1]: set to 0, then to 1 if any element changed
+ * Stream-ordered and asynchronous; no handle, no allocation. Errors:
+ * GC_ERR_ARG (other policies, null pointers, n < 0), GC_ERR_CUDA.
+ */
+gc_status gc_update(gc_policy policy, void* x, const void* y, int64_t n, int32_t* changed, void* stream);
 
 /*
  * gc_sssp -- tropical-semiring fixpoint x <- min(x, M (x) x) from x0 until it
@@ -453,8 +473,9 @@ gc_status gc_left_matvec(gc_left_handle* h, const void* y, void* x, void* stream
  *   iters    device int32_t[1]: products performed, the last of which
  *            changed nothing; -1 if max_iter was reached first.
  * Returns GC_ERR_NOT_CONVERGED if max_iter products did not reach the
- * fixpoint. Synchronises the stream once per product to read the changed
- * flag; uses the handle's graph and scratch (one call at a time per handle).
+ * fixpoint. The loop runs on the device as described for gc_reach (batches,
+ * one batch ahead, later calls ordered after the last batch); uses the
+ * handle's graph and scratch (one call at a time per handle).
  */
 gc_status gc_left_reach(gc_left_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter, int32_t* iters,
                         void* stream);

@@ -365,3 +365,44 @@ def test_batch_widths(gcs, torch, k):
         assert direct.within_tolerance(Yn, y_ref, b, TOL)[0]
     with pytest.raises(gcs.GcError, match="GC_ERR_ARG"):
         eng.matvec(torch.zeros((m, 12), device="cuda"))
+
+
+def test_fixpoint_loop_edges_and_streams(gcs, torch):
+    # the loop keeps one batch enqueued ahead: max_iter at and just below
+    # the product count, a product on another stream straight after the
+    # call returns (ordered after the loop's last batch), and a handle freed
+    # with the last batch still on the stream
+    N = 3000
+    rp, col = gcsynth.copy_model_graph(nodes=N, n0=20, d0=15, p_edit=0.05, seed=3)
+    G = gcs.Grammar(N, N, rp, col, None)
+    x0 = gcsynth.frontier(N, gcsynth.sources(N, 64, seed=1))
+    want, want_iters = reach.fixpoint(rp, col, x0)
+    assert want_iters >= 3
+    for sched in ("persistent", "dataflow"):
+        eng = gcs.Engine(G, "or", 1, schedule=sched)
+        x0d = _dev(torch, x0.view(np.int64))
+        xs, iters, rc = eng.reach(x0d, max_iter=want_iters)
+        assert rc == 0 and iters == want_iters
+        np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint64), want)
+        xs, iters, rc = eng.reach(x0d, max_iter=want_iters - 1)
+        assert rc == gcs.capi.GC_ERR_NOT_CONVERGED and iters == -1
+        assert eng.check() == gcs.capi.GC_ERR_NOT_CONVERGED
+        assert eng.check() == 0
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        xr = torch.empty_like(x0d)
+        it = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        assert gcs.capi.gc_reach(eng._h, x0d, xr, 1000, it, s1) == 0
+        xv = _dev(torch, want.view(np.int64))
+        yv = torch.empty_like(xv)
+        torch.cuda.synchronize()
+        eng.matvec(xv, yv, stream=s2)
+        s2.synchronize()
+        s1.synchronize()
+        np.testing.assert_array_equal(yv.cpu().numpy().view(np.uint64), direct.matvec_or(rp, col, want))
+        np.testing.assert_array_equal(xr.cpu().numpy().view(np.uint64), want)
+        assert int(it.item()) == want_iters
+        assert gcs.capi.gc_reach(eng._h, x0d, xr, 1000, it, s1) == 0
+        del eng                          # freed with the last batch possibly still running
+        s1.synchronize()
+        np.testing.assert_array_equal(xr.cpu().numpy().view(np.uint64), want)

@@ -3,9 +3,11 @@ grammar_compressed_sparse_gb300.shard, with no GPU.
 
 Each rank builds the grammar of its own rows (whole 64-row blocks) with the
 host builder, evaluates its rows of the product with the CPU emulator of the
-packed layout (a stand-in for the device sweep), and the ranks gather the
-rows; the fixpoints gather the new vector and all-reduce the changed flag
-once per iteration. Everything is compared with the oracle on the whole
+packed layout (a stand-in for the device sweep) and updates them with CPU
+stand-ins of the library's update step, and the ranks gather the rows; the
+fixpoints gather the new vector and all-reduce the changed flag (a bool from
+one stand-in, a tensor from the other) once per iteration. The GPU path
+(ShardedEngine, gc_update) is tested on one rank in test_gpu_shard.py. Everything is compared with the oracle on the whole
 matrix, on every rank.
 """
 import os
@@ -47,8 +49,16 @@ def _rank_main(rank, world, port, errors):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         import grammar_compressed_sparse_gb300 as gcs
-        from grammar_compressed_sparse_gb300.shard import (gather_rows, local_rows, min_update, or_update,
-                                                           row_shards, sharded_fixpoint)
+        from grammar_compressed_sparse_gb300.shard import gather_rows, local_rows, row_shards, sharded_fixpoint
+
+        # CPU stand-ins of the library's update step (gc_update runs on the GPU)
+        def or_update(old, new):
+            out = old | new
+            return out, bool((out != old).any())
+
+        def min_update(old, new):
+            out = torch.minimum(old, new)
+            return out, torch.tensor([int((out != old).any())], dtype=torch.int32)
         # genotype rows: y = G beta, rows sharded by 64-row blocks
         cfg = dict(gcsynth.GENO_SMALL, n=300, m=900)
         rp, c, v = gcsynth.genotype_csr(**cfg)
