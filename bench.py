@@ -3,8 +3,9 @@
 
 Workload (default): 10,000 individuals x 50,000 variants, genotypes in
 {0,1,2} from a 100-founder mosaic (switch = mutation = 1e-3, seed 0), one
-grammar built once, then K timed products with fresh beta ~ N(0,1) float32.
-A step is one whole product (leaf gather, every level, row emit).
+grammar built once (RePair, then height-balanced: --grammar repair keeps
+RePair's grammar as built), then K timed products with fresh beta ~ N(0,1)
+float32. A step is one whole product (leaf gather, every level, row emit).
 
 Timing: W warm-up steps, then K steps, each timed with CUDA events on the
 launching stream; the L2 cache (129 MB) is flushed by writing a 512 MB buffer
@@ -52,27 +53,25 @@ if ROOT not in sys.path:
 import gcsynth  # noqa: E402
 
 METRIC = "matvecs/s and effective HBM GB/s (% of roofline) for y=Gβ on one GB300"
+# k = 1 products run over the height-balanced grammar (faster on every one
+# measured); the wide batches keep RePair's (the balanced grammar has more
+# rules, and their values dominate a wide product's traffic)
 WORKLOADS = {
-    "geno_10k_50k": dict(gen=gcsynth.GENO_MEDIUM, k=1),
+    "geno_10k_50k": dict(gen=gcsynth.GENO_MEDIUM, k=1, grammar="balanced"),
     "geno_10k_50k_k16": dict(gen=gcsynth.GENO_MEDIUM, k=16),
     "geno_10k_50k_k64": dict(gen=gcsynth.GENO_MEDIUM, k=64),
     "geno_10k_50k_k256": dict(gen=gcsynth.GENO_MEDIUM, k=256),
-    "geno_1k_2k": dict(gen=gcsynth.GENO_SMALL, k=1),
-    "geno_50k_200k": dict(gen=gcsynth.GENO_LARGE, k=1),
-    "graph_2m": dict(graph=gcsynth.GRAPH, k=1),
+    "geno_1k_2k": dict(gen=gcsynth.GENO_SMALL, k=1, grammar="balanced"),
+    "geno_50k_200k": dict(gen=gcsynth.GENO_LARGE, k=1, grammar="balanced"),
+    "graph_2m": dict(graph=gcsynth.GRAPH, k=1, grammar="balanced"),
     # tropical (min, +): one Bellman-Ford relaxation per product
-    "geno_10k_50k_minplus": dict(gen=gcsynth.GENO_MEDIUM, k=1, policy="minplus"),
+    "geno_10k_50k_minplus": dict(gen=gcsynth.GENO_MEDIUM, k=1, policy="minplus", grammar="balanced"),
     # the left product x = M^T y (float32, one vector)
-    "geno_10k_50k_left": dict(gen=gcsynth.GENO_MEDIUM, k=1, op="left"),
-    "graph_2m_minplus": dict(graph=gcsynth.GRAPH, k=1, policy="minplus"),
+    "geno_10k_50k_left": dict(gen=gcsynth.GENO_MEDIUM, k=1, op="left", grammar="balanced"),
+    "graph_2m_minplus": dict(graph=gcsynth.GRAPH, k=1, policy="minplus", grammar="balanced"),
     # the same products under the dataflow schedule (its own layout)
     "geno_10k_50k_dataflow": dict(gen=gcsynth.GENO_MEDIUM, k=1, schedule="dataflow"),
     "graph_2m_dataflow": dict(graph=gcsynth.GRAPH, k=1, schedule="dataflow"),
-    # the same matrices over the height-balanced (AVL) grammar
-    "geno_10k_50k_balanced": dict(gen=gcsynth.GENO_MEDIUM, k=1, balance=True),
-    "geno_10k_50k_k16_balanced": dict(gen=gcsynth.GENO_MEDIUM, k=16, balance=True),
-    "geno_50k_200k_balanced": dict(gen=gcsynth.GENO_LARGE, k=1, balance=True),
-    "graph_2m_balanced": dict(graph=gcsynth.GRAPH, k=1, balance=True),
 }
 L2_FLUSH_BYTES = 512 << 20
 
@@ -84,6 +83,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="geno_10k_50k", choices=sorted(WORKLOADS))
+    ap.add_argument("--grammar", default=None, choices=["repair", "balanced"],
+                    help="RePair's grammar as built, or its AVL height-balanced form (default: the workload's)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -468,7 +469,8 @@ def run_ours(args):
             load = lambda: gcs.cached_grammar(key, None, build=lambda: make_blocked(gcs, gen))  # noqa: E731
         else:
             load = lambda: gcs.cached_grammar(key, lambda: make_csr(gen))  # noqa: E731
-    if wl.get("balance"):
+    balanced = (args.grammar or wl.get("grammar", "repair")) == "balanced"
+    if balanced:
         G = gcs.cached_grammar(key + ":balanced", None, build=lambda: load().balanced(),
                                extra_sources=("balance.cpp",))
     else:
@@ -588,6 +590,7 @@ def run_ours(args):
         fixpoint = {"kind": "shortest paths, unit lengths" if minplus else "reachability, 64-bit source bitsets",
                     "iterations": iters, "seconds": round(wall_fp, 5), "device_ms": round(dev_ms, 4),
                     "per_iteration_ms": round(dev_ms / max(1, iters), 4),
+                    "vs_iterations_x_product": round(dev_ms / max(1e-9, iters * 1e3 * total_s / args.steps), 3),
                     "vs_iterations_x_hot_product": round(dev_ms / max(1e-9, iters * hot_ms), 3),
                     "status": rc}
 
@@ -678,12 +681,12 @@ def run_ours(args):
                    **({"graph": "copy model, unit edge lengths" if minplus else "copy model, 64-bit source bitsets"}
                       if graph else
                       {"founders": gen["founders"], "switch": gen["switch"], "mutation": gen["mutation"]}),
-                   "grammar": "RePair, AVL height-balanced" if wl.get("balance") else "RePair",
+                   "grammar": "RePair, AVL height-balanced" if balanced else "RePair",
                    "l2": "flushed before every step (512 MB write, outside the events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
-                     "traffic": profile_traffic(f"sweep:{args.workload}"),
+                     "traffic": profile_traffic(f"sweep:{args.workload}" + (":balanced" if balanced else "")),
                      "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": bytes_step},
         "cpu_baseline": cpu,

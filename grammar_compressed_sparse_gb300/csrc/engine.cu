@@ -122,6 +122,7 @@ __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long lon
     return v;
 }
 __device__ __forceinline__ int ld_volatile(const int32_t* p) { return *reinterpret_cast<const volatile int32_t*>(p); }
+__device__ __forceinline__ void st_volatile(int32_t* p, int32_t v) { *reinterpret_cast<volatile int32_t*>(p) = v; }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(gaddr(p))); }
 
@@ -212,6 +213,8 @@ struct SweepArgs {
     int32_t emode;            // EmitMode
     int32_t emit_group;       // row emit: G lanes per row
     int32_t* status;
+    int32_t* fix;             // a fixpoint in one launch (see sweep_fixpoint), else nullptr
+    int32_t fix_max;          //   at most this many products
     unsigned long long* bar;
     unsigned long long bar_base;
     unsigned long long* tbar;        // slice emit: the tail group's arrival counter
@@ -230,7 +233,10 @@ template <class P>
 __device__ __forceinline__ typename P::V leaf_value(int32_t code, int part, const SweepArgs<P>& a) {
     const uint32_t q = (uint32_t)code;
     const uint32_t col = q >> a.vbits, vi = q & ((1u << a.vbits) - 1u);
-    return P::leaf(__ldg(a.Vd + vi), ldg_value(a.x + (int64_t)col * P::LPN + part));
+    const typename P::V* xp = a.x + (int64_t)col * P::LPN + part;
+    if constexpr (kFixpointPolicy<P>)
+        if (a.fix != nullptr) return P::leaf(__ldg(a.Vd + vi), *xp);   // x changes inside the launch
+    return P::leaf(__ldg(a.Vd + vi), ldg_value(xp));
 }
 
 // The leaf table in front of RV (slice and row emits: C's bare terminals),
@@ -383,7 +389,7 @@ __device__ __forceinline__ TailIO<P> tail_io(const SweepArgs<P>& a, int k, typen
 // Lane (slot, part) sums part `part` of the row's symbols q = s+slot,
 // s+slot+S, ... in order, then the group reduces the slots by a fixed butterfly.
 template <class P, int G>
-__device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
+__device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblocks, int* changed) {
     using V = typename P::V;
     constexpr int S = G < 32 / P::LPN ? G : 32 / P::LPN;
     constexpr int GG = S * P::LPN;                     // lanes per row
@@ -423,7 +429,20 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
         }
 #pragma unroll
         for (int msk = GG / 2; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
-        if (row < a.n && slot == 0) a.y[row * P::LPN + part] = acc;
+        if (row < a.n && slot == 0) {
+            bool stored = false;
+            if constexpr (kFixpointPolicy<P>)
+                if (changed != nullptr) {   // a fixpoint step: x = x (+) y in place (x is no longer read)
+                    V* x = const_cast<V*>(a.x);
+                    const V u = x[row], v = P::combine(u, acc);
+                    if (v != u) {
+                        x[row] = v;
+                        *changed = 1;
+                    }
+                    stored = true;
+                }
+            if (!stored) a.y[row * P::LPN + part] = acc;
+        }
         row = nrow;
         s = ns;
         e = ne;
@@ -611,14 +630,16 @@ __device__ void finish_rows(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps
 
 // Row emit: groups of G lanes per row (emit_group = G).
 template <class P>
-__device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
+// With changed given (a fixpoint in one launch), each row's sum goes into x
+// instead, x[r] = x[r] (+) y[r], and *changed is set if any x[r] changed.
+__device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks, int* changed = nullptr) {
     switch (a.emit_group) {
-        case 1: emit_groups<P, 1>(a, block, nblocks); break;
-        case 2: emit_groups<P, 2>(a, block, nblocks); break;
-        case 4: emit_groups<P, 4>(a, block, nblocks); break;
-        case 8: emit_groups<P, 8>(a, block, nblocks); break;
-        case 16: emit_groups<P, 16>(a, block, nblocks); break;
-        default: emit_groups<P, 32>(a, block, nblocks); break;
+        case 1: emit_groups<P, 1>(a, block, nblocks, changed); break;
+        case 2: emit_groups<P, 2>(a, block, nblocks, changed); break;
+        case 4: emit_groups<P, 4>(a, block, nblocks, changed); break;
+        case 8: emit_groups<P, 8>(a, block, nblocks, changed); break;
+        case 16: emit_groups<P, 16>(a, block, nblocks, changed); break;
+        default: emit_groups<P, 32>(a, block, nblocks, changed); break;
     }
 }
 
@@ -683,19 +704,15 @@ __device__ __forceinline__ void arrive_on(unsigned long long* bar) {
 }
 
 // ---------------------------------------------------------------- persistent sweep
+// One product of the persistent sweep, this CTA's share: leaf tables, the
+// wide levels, then (unless the slice kernel takes over) the tail and the
+// emit. nbar counts the launch's grid barriers passed so far. With changed
+// given, the row emit folds its sums into x (a fixpoint step, emit_rows).
+// False if a barrier timed out (the status word says so).
 template <class P, bool kC>
-__global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a) {
-    // an unread earlier timeout left the barrier counter part-way: do nothing
-    if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
+__device__ __forceinline__ bool sweep_product(const SweepArgs<P>& a, unsigned long long& nbar,
+                                              int* changed = nullptr) {
     const int Lg = a.grid_levels;
-    // a converged fixpoint loop skips the product: the CTA's arrivals at the
-    // launch's grid barriers (one a level after the first; before the tail
-    // and the emit unless the slice kernel takes them) in one addition
-    if (a.conv != nullptr && ld_volatile(a.conv) != 0) {
-        if (threadIdx.x == 0)
-            red_add_release(a.bar, (unsigned long long)((Lg > 1 ? Lg - 1 : 0) + (a.emode == EMIT_SLICE ? 0 : 2)));
-        return;
-    }
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const uint64_t keep = l2_evict_last();
@@ -724,9 +741,8 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
     norm(kn, cn);
     int2 nab[Chunk<P>::U];
     if (kn <= Lg) load_chunk<P>(a, kn, cn, nab);
-    unsigned long long nbar = 0;
     for (int k = 1; k <= Lg; ++k) {
-        if (k > 1 && !grid_sync(a, nbar++)) return;
+        if (k > 1 && !grid_sync(a, nbar++)) return false;
         const LevelIO<P> io = level_io<P>(a, k);
         while (kn == k) {
             int2 ab[Chunk<P>::U];
@@ -744,8 +760,8 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
         }
     }
     // slice emit: the second kernel takes the tail, the emit and the row pass
-    if (a.emode == EMIT_SLICE) return;
-    if (!grid_sync(a, nbar++)) return;
+    if (a.emode == EMIT_SLICE) return true;
+    if (!grid_sync(a, nbar++)) return false;
     // while CTA 0 runs the tail, the others reduce what is left of the level
     // emit (level Lg, and the terminals if no phase took them)
     const int64_t skip = (tail && gridDim.x > 1) ? kWarps : 0;
@@ -768,9 +784,75 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
             __syncthreads();
         }
     }
-    if (!grid_sync(a, nbar++)) return;
+    if (!grid_sync(a, nbar++)) return false;
     if (a.emode != EMIT_ROWS) emit_final<P>(a, gw, GW);
-    else emit_rows<P>(a, blockIdx.x, gridDim.x);
+    else emit_rows<P>(a, blockIdx.x, gridDim.x, changed);
+    return true;
+}
+
+// A whole fixpoint x = x (+) (M (x) x) in one launch (handles whose product is
+// this kernel alone: no slice kernel). With the row emit, the product's emit
+// folds each row's sum into x (nothing reads x after the levels); with the
+// level emit, the product goes into y, a grid barrier, then x = x (+) y over
+// the grid. Either way a changed flag, a grid barrier, and every CTA reads
+// the flag. fix[0] / fix[1] are the changed flags of the even / odd products
+// (a product's flag is cleared by CTA 0 during the product before it, after
+// every CTA has read it), fix[2] = 1 and fix[3] = the product count on
+// convergence; both stay 0 if a.fix_max products did not converge. Each
+// product passes sweep_barriers + 1 grid barriers (+ 2 with the level emit).
+template <class P, bool kC>
+__device__ void sweep_fixpoint(const SweepArgs<P>& a, unsigned long long& nbar) {
+    using V = typename P::V;
+    V* x = const_cast<V*>(a.x);   // x is the fixpoint's iterate, updated in place
+    int32_t* fx = a.fix;
+    const bool rows = a.emode == EMIT_ROWS;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nth = (int64_t)gridDim.x * blockDim.x;
+    for (int32_t it = 1; it <= a.fix_max; ++it) {
+        int ch = 0;
+        if (!sweep_product<P, kC>(a, nbar, rows ? &ch : nullptr)) return;
+        if (!rows) {
+            if (!grid_sync(a, nbar++)) return;   // every row of y is written and x no longer read
+            for (int64_t i = tid; i < a.n; i += nth) {
+                const V u = x[i], v = P::combine(u, a.y[i]);
+                if (v != u) {
+                    x[i] = v;
+                    ch = 1;
+                }
+            }
+        }
+        if (__syncthreads_or(ch) && threadIdx.x == 0) st_volatile(fx + (it & 1), 1);
+        if (blockIdx.x == 0 && threadIdx.x == 0) st_volatile(fx + ((it + 1) & 1), 0);
+        if (!grid_sync(a, nbar++)) return;
+        if (ld_volatile(fx + (it & 1)) == 0) {   // nothing changed: converged at product it
+            if (blockIdx.x == 0 && threadIdx.x == 0) {
+                fx[3] = it;
+                fx[2] = 1;
+            }
+            return;
+        }
+    }
+}
+
+template <class P, bool kC>
+__global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a) {
+    // an unread earlier timeout left the barrier counter part-way: do nothing
+    if (ld_volatile(a.status) == (int32_t)GC_ERR_TIMEOUT) return;
+    const int Lg = a.grid_levels;
+    // a converged fixpoint loop skips the product: the CTA's arrivals at the
+    // launch's grid barriers (one a level after the first; before the tail
+    // and the emit unless the slice kernel takes them) in one addition
+    if (a.conv != nullptr && ld_volatile(a.conv) != 0) {
+        if (threadIdx.x == 0)
+            red_add_release(a.bar, (unsigned long long)((Lg > 1 ? Lg - 1 : 0) + (a.emode == EMIT_SLICE ? 0 : 2)));
+        return;
+    }
+    unsigned long long nbar = 0;
+    if constexpr (kFixpointPolicy<P>)
+        if (a.fix != nullptr) {
+            sweep_fixpoint<P, kC>(a, nbar);
+            return;
+        }
+    sweep_product<P, kC>(a, nbar);
 }
 
 // ---------------------------------------------------------------- slice emit
@@ -998,22 +1080,25 @@ __global__ void __launch_bounds__(kSliceThreads, 1) slice_kernel(const SweepArgs
 }
 
 // ---------------------------------------------------------------- dataflow sweep
-// One value a node (flow.hpp has the block plan). A CTA per SM: warp 0
-// stages blocks into a ring of shared-memory buffers -- it waits for a
-// block's dependencies (the producers' ready flags, and level k-2 finished
-// before level k overwrites its buffer), then copies the block's node pairs,
-// windows and outlier granules with bulk copies that complete on the stage's
-// mbarrier -- while 16 compute warps evaluate the previously staged blocks:
-// every child is a shared-memory value, the identity or a leaf evaluated in
-// place; values go to the level buffer (and RV for roots). A warp reports on
-// the stage's `computed` barrier and goes on to the next staged block; warp
-// 17 then releases the block's flag and frees the stage, so the fence and the
-// release stay off the compute path. Blocks are dealt to CTAs round robin (b = CTA, CTA + grid,
-// ...), and a CTA works through its blocks in order; every dependency is an
-// earlier block, so the earliest unfinished block can always proceed (all
-// CTAs are resident: cooperative launch). The final block (the narrow top
-// levels) takes every staging buffer of its CTA and computes its levels one
-// after the other in shared memory.
+// One value a node (flow.hpp has the block plan). A CTA per SM, three roles:
+// kNS staging warps, warp s owning stage s of a ring of shared-memory
+// buffers -- it waits until its stage is free, copies the next block's node
+// pairs in with one bulk copy completing on the stage's mbarrier, and waits
+// for the block's dependencies (the producers' ready flags, and level k-2
+// finished before level k overwrites its buffer); 16 compute warps evaluate
+// the staged blocks in order, gathering each child from the level buffer of
+// the level below through L1/L2 (the flag acquire and the stage's mbarrier
+// order the gathers after the producers' writes), the identity, or a leaf
+// evaluated in place, and write the values to the level buffer (and RV for
+// roots); a publishing warp, once all compute warps have reported a block,
+// sets its ready flag (one gpu-scope fence, then relaxed stores) and adds it
+// to its level's done counter, so the fence stays off the compute path.
+// Blocks are dealt to CTAs round robin over a processing order sorted by
+// readiness, and a CTA works through its blocks in that order; every
+// dependency comes earlier in the order, so the earliest unfinished block can
+// always proceed (all CTAs are resident: cooperative launch). The final block
+// (the narrow top levels) takes every staging buffer of its CTA and computes
+// its levels one after the other in shared memory. Every wait is bounded.
 constexpr int kFlowCW = 16;                   // compute warps of a CTA
 constexpr int kFlowCT = 32 * kFlowCW;         // compute threads
 constexpr int kFlowThreads = kFlowCT + 32 * ((int)kFlowStages + 1);   // and kNS staging warps, one publishing warp
@@ -1539,10 +1624,12 @@ __global__ void __launch_bounds__(kThreads, 1) emit_kernel(const SweepArgs<P> a,
 // sets *changed if any element changed (one fixpoint step).
 struct OrUpdate {
     using T = unsigned long long;
+    using Pol = PolOr;
     __device__ __forceinline__ static T apply(T u, T v) { return u | v; }
 };
 struct MinUpdate {
     using T = float;
+    using Pol = PolMinPlus;
     __device__ __forceinline__ static T apply(T u, T v) { return fminf(u, v); }
 };
 
@@ -1574,9 +1661,12 @@ update_rows_kernel(typename U::T* __restrict__ x, const typename U::T* __restric
 template <class U>
 __global__ void __launch_bounds__(kThreads)
 update_loop_kernel(typename U::T* __restrict__ x, const typename U::T* __restrict__ y, int64_t n,
-                   int32_t* __restrict__ ctl, int32_t it) {
+                   int32_t* __restrict__ ctl, int32_t it, int32_t max_it, int32_t* __restrict__ status) {
     __shared__ int s_last;
     if (ld_volatile(ctl + 1) != 0) return;   // converged at an earlier step
+    // a product that timed out wrote no y: no step, no convergence (the loop
+    // runs out at max_it and the status word keeps the timeout)
+    if (ld_volatile(status) == (int32_t)GC_ERR_TIMEOUT) return;
     int ch = 0;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const typename U::T u = x[i], v = U::apply(u, y[i]);
@@ -1597,6 +1687,8 @@ update_loop_kernel(typename U::T* __restrict__ x, const typename U::T* __restric
         if (ld_volatile(ctl) == 0) {
             ctl[3] = it;
             ctl[1] = 1;
+        } else if (it == max_it) {
+            atomicCAS(status, 0, (int32_t)GC_ERR_NOT_CONVERGED);
         }
         ctl[0] = 0;
         ctl[2] = 0;
@@ -2003,14 +2095,63 @@ void put(cudaStream_t st, char* arena, int64_t off, const T* p, size_t count) {
 }
 
 // x <- x (+) (M (x) x) from x0 until nothing changes, at most max_iter
-// products; the product's y lives in the arena's staging area. The loop runs
-// on the device (drive_fixpoint): products and update steps are enqueued in
-// batches of 1, 2, 4, 8, 8, ..., one batch ahead of the one the host waits
-// for; the update step's last CTA records convergence (ctl, in the status
-// block) and every kernel enqueued after it returns at once, keeping the
-// barrier counters and level counters consistent. Writes the product count
-// (or -1) to iters on the device. Returns false if max_iter was reached first
-// (the status word then says GC_ERR_NOT_CONVERGED).
+// products; the product's y lives in the arena's staging area. Handles whose
+// product is the persistent sweep alone run it in one launch
+// (fused_fixpoint). Otherwise the loop runs on the device (drive_fixpoint):
+// products and update steps are enqueued in batches of 1, 2, 4, 8, 8, ...,
+// one batch ahead of the one the host waits for; the update step's last CTA
+// records convergence (ctl, in the status block) and every kernel enqueued
+// after it returns at once, keeping the barrier counters and level counters
+// consistent. Writes the product count (or -1) to iters on the device.
+// Returns false if max_iter was reached first (the status word then says
+// GC_ERR_NOT_CONVERGED, unless a barrier timed out: GC_ERR_TIMEOUT).
+// The whole fixpoint as one launch of the persistent sweep (sweep_fixpoint):
+// for handles whose product is that kernel alone (persistent schedule, no
+// slice kernel, no dataflow layout). Sets *result to the product count (or
+// -1) and returns whether it converged; synchronises the stream.
+template <class P, bool kC>
+bool fused_fixpoint(gc_handle* h, typename P::V* x, int32_t max_iter, int32_t* result, cudaStream_t st) {
+    int32_t* status = reinterpret_cast<int32_t*>(h->arena + h->lay.status);
+    int32_t* fix = status + 8;   // bytes 32..47 of the status block
+    const int grid = sweep_grid<P, kC>(h);
+    if (!h->loop.words) {
+        void* p = nullptr;
+        cuda_check(cudaHostAlloc(&p, 8 * sizeof(int32_t), cudaHostAllocDefault), "loop words (pinned)");
+        h->loop.words = static_cast<int32_t*>(p);
+    }
+    cuda_check(cudaMemsetAsync(fix, 0, 4 * sizeof(int32_t), st), "fixpoint words clear");
+    SweepArgs<P> a = make_args<P>(h, x, h->arena + h->lay.ys);
+    a.fix = fix;
+    a.fix_max = max_iter;
+    a.conv = nullptr;
+    void* args[] = {&a};
+    cuda_check(cudaLaunchCooperativeKernel((const void*)sweep_kernel<P, kC>, dim3(grid), dim3(kThreads), args, 0, st),
+               "fixpoint launch");
+    h->launches = 1;
+    int32_t* w = h->loop.words;   // status word, then the fixpoint's four
+    cuda_check(cudaMemcpyAsync(w, status, sizeof(int32_t), cudaMemcpyDeviceToHost, st), "status read");
+    cuda_check(cudaMemcpyAsync(w + 4, fix, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, st), "fixpoint words read");
+    cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+    const bool done = w[0] == 0 && w[6] != 0;
+    *result = done ? w[7] : -1;
+    // the launch's grid barriers: sweep_barriers + 1 a product, + 2 with the
+    // level emit (sweep_fixpoint; a timed-out
+    // launch leaves the counter part-way; gc_check restarts it)
+    const int64_t products = done ? w[7] : max_iter;
+    if (w[0] == 0)
+        h->bar_base += (unsigned long long)products *
+                       (unsigned long long)(sweep_barriers(h) + (h->lay.emit == EMIT_ROWS ? 1 : 2)) *
+                       (unsigned long long)grid;
+    return done;
+}
+
+template <class P>
+bool fused_fixpoint_ok(const gc_handle* h) {
+    if (h->schedule != 0 || !h->coop || h->flow || h->lay.emit == EMIT_SLICE) return false;
+    if (h->n_carry > 0) return false;
+    return sweep_grid<P, false>(h) > 0;
+}
+
 template <class U>
 bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32_t max_iter, int32_t* iters,
                   cudaStream_t st) {
@@ -2022,6 +2163,16 @@ bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32
     after_last_loop(h->loop, st, cuda_check);
     if (x != x0 && n > 0)
         cuda_check(cudaMemcpyAsync(x, x0, n * sizeof(T), cudaMemcpyDeviceToDevice, st), "x0 copy");
+    if (fused_fixpoint_ok<typename U::Pol>(h)) {
+        int32_t result = -1;
+        const bool done = fused_fixpoint<typename U::Pol, false>(h, x, max_iter, &result, st);
+        cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
+        if (!done && h->loop.words[0] == 0) {
+            int32_t sw = GC_ERR_NOT_CONVERGED;
+            cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
+        }
+        return done;
+    }
     cuda_check(cudaMemsetAsync(ctl, 0, 16, st), "loop words clear");
     int32_t result = -1;
     int64_t launches = 0;
@@ -2031,7 +2182,8 @@ bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32
         done = drive_fixpoint(h->loop, ctl, max_iter, st, cuda_check, [&](int32_t it) {
             dispatch_product(h, x, yv, 1, st);
             launches += h->launches;
-            update_loop_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, ctl, it);
+            update_loop_kernel<U><<<grid_for(n, kThreads, h->sms, 8), kThreads, 0, st>>>(x, yv, n, ctl, it, max_iter,
+                                                                                         status);
             ++launches;
         }, &result);
     } catch (...) {
@@ -2041,12 +2193,9 @@ bool run_fixpoint(gc_handle* h, const typename U::T* x0, typename U::T* x, int32
     }
     h->conv = nullptr;
     h->launches = launches;
-    // pageable sources: both copies take their value before they return
+    // a pageable source: the copy takes its value before it returns (the
+    // last update step records GC_ERR_NOT_CONVERGED in the status word)
     cuda_check(cudaMemcpyAsync(iters, &result, 4, cudaMemcpyHostToDevice, st), "iters write");
-    if (!done) {
-        int32_t sw = GC_ERR_NOT_CONVERGED;
-        cuda_check(cudaMemcpyAsync(status, &sw, 4, cudaMemcpyHostToDevice, st), "status write");
-    }
     mark_loop_end(h->loop, st, cuda_check);
     return done;
 }

@@ -18,6 +18,8 @@
 // child.
 #pragma once
 
+#include <type_traits>
+
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -117,5 +119,10 @@ struct PolMinPlusx16 {
         return make_float4(__fadd_rn(s, x.x), __fadd_rn(s, x.y), __fadd_rn(s, x.z), __fadd_rn(s, x.w));
     }
 };
+
+// The policies the fixpoints run in, x = x (+) (M (x) x) with one value a
+// node: reachability (OR) and shortest paths (min); (+) is P::combine.
+template <class P>
+constexpr bool kFixpointPolicy = std::is_same<P, PolOr>::value || std::is_same<P, PolMinPlus>::value;
 
 }  // namespace gcs

@@ -288,18 +288,27 @@ gc_status gc_matvec_host(gc_handle* h, const void* x_host, void* y_host, int32_t
  *            nothing; -1 if max_iter was reached first.
  * Returns GC_ERR_NOT_CONVERGED (and records it in the status word, which
  * gc_check reports once) if max_iter products did not reach the fixpoint.
- * The loop runs on the device: products and update steps are enqueued in
- * batches of 1, 2, 4, 8, 8, ... with no host round trip inside a batch; the
- * last update step to finish records convergence, after which the kernels of
- * the products already enqueued return at once (x is unchanged by them). The
- * host keeps one batch enqueued ahead of the one whose convergence words it
- * waits for (an event on the stream), so the device does not idle between
- * batches. The call returns once convergence (or max_iter) is known; the
- * last batch's early-return kernels and the iters write may still be on the
- * stream: synchronise it before reading x or iters on the host. Every later
- * call on the handle (products, gc_check, another fixpoint), on any stream,
- * is ordered after them. The first call pins 32 bytes of host memory and
- * makes three events, released by gc_free_handle.
+ * The loop runs on the device. Where the handle's product is one persistent
+ * launch (the persistent schedule with the row or level emit: matrices with
+ * short rows, such as graphs), the whole fixpoint is that one launch: each
+ * product is followed, inside the kernel, by a grid barrier, the update
+ * x = x OR y over the grid with a changed flag, and a second grid barrier
+ * after which every CTA reads the flag; the call then synchronises the
+ * stream once. Otherwise (the slice emit, the per-level and dataflow
+ * schedules) products and update steps are enqueued in batches of 1, 2, 4,
+ * 8, 8, ... with no host round trip inside a batch; the last update step to
+ * finish records convergence, after which the kernels of the products
+ * already enqueued return at once (x is unchanged by them). The host keeps
+ * one batch enqueued ahead of the one whose convergence words it waits for
+ * (an event on the stream), so the device does not idle between batches,
+ * and returns once convergence (or max_iter) is known; the last batch's
+ * early-return kernels and the iters write may still be on the stream:
+ * synchronise it before reading x or iters on the host. Every later call on
+ * the handle (products, gc_check, another fixpoint), on any stream, is
+ * ordered after them. The first call pins 32 bytes of host memory and makes
+ * three events, released by gc_free_handle. A grid barrier that times out
+ * ends the call with GC_ERR_NOT_CONVERGED (iters -1) and leaves
+ * GC_ERR_TIMEOUT in the status word for gc_check.
  */
 gc_status gc_reach(gc_handle* h, const uint64_t* x0, uint64_t* x, int32_t max_iter,
                    int32_t* iters, void* stream);

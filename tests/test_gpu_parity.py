@@ -406,3 +406,53 @@ def test_fixpoint_loop_edges_and_streams(gcs, torch):
         del eng                          # freed with the last batch possibly still running
         s1.synchronize()
         np.testing.assert_array_equal(xr.cpu().numpy().view(np.uint64), want)
+
+
+def test_fixpoint_in_one_launch_and_its_timeout(gcs, torch):
+    # row-emit handles (the graph) run the whole fixpoint in one persistent
+    # launch; a handle with the slice emit (long rows) keeps the batched loop.
+    # Both against the oracle; then an injected barrier timeout inside the
+    # one-launch fixpoint is reported, and the handle recovers after gc_check
+    N = 3000
+    rp, col = gcsynth.copy_model_graph(nodes=N, n0=20, d0=15, p_edit=0.05, seed=5)
+    G = gcs.Grammar(N, N, rp, col, None)
+    eng = gcs.Engine(G, "or", 1)
+    x0 = gcsynth.frontier(N, gcsynth.sources(N, 64, seed=2))
+    want, want_iters = reach.fixpoint(rp, col, x0)
+    xs, iters, rc = eng.reach(_dev(torch, x0.view(np.int64)))
+    assert rc == 0 and iters == want_iters and eng.launch_count() == 1
+    np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint64), want)
+    # products after the fixpoint still compute (barrier counters consistent)
+    xv = _dev(torch, want.view(np.int64))
+    np.testing.assert_array_equal(eng.matvec(xv).cpu().numpy().view(np.uint64), direct.matvec_or(rp, col, want))
+    gcs.capi.gc_debug_inject(eng._h, 1, 2_000_000)
+    _, iters_t, rc_t = eng.reach(_dev(torch, x0.view(np.int64)))
+    assert rc_t == gcs.capi.GC_ERR_NOT_CONVERGED and iters_t == -1
+    assert eng.check() == gcs.capi.GC_ERR_TIMEOUT
+    gcs.capi.gc_debug_inject(eng._h, 0, 4_000_000_000)
+    xs, iters, rc = eng.reach(_dev(torch, x0.view(np.int64)))
+    assert rc == 0 and iters == want_iters
+    np.testing.assert_array_equal(xs.cpu().numpy().view(np.uint64), want)
+    assert eng.check() == 0
+    # a square matrix with long rows: the slice emit, the batched loop
+    n = 800
+    rp2, c2, v2, _ = gcsynth.random_sparse(n, n, 0.5, [1.0, 2.0, 3.0], 9)   # |C| / n about 193
+    G2 = gcs.Grammar(n, n, rp2, c2, v2)
+    mp = gcs.Engine(G2, "minplus", 1)
+    d0 = np.full(n, np.inf, np.float32)
+    d0[[3, 77]] = 0.0
+    d, it2, rc2 = mp.sssp(_dev(torch, d0))
+    want_d, want_it = reach.sssp_fixpoint(rp2, c2, v2, d0)
+    assert rc2 == 0 and it2 == want_it and mp.launch_count() > 1
+    np.testing.assert_array_equal(d.cpu().numpy().view(np.uint32), want_d.view(np.uint32))
+    # a barrier timeout inside the batched loop: not converged, the status
+    # word keeps the timeout, and the handle recovers after gc_check
+    gcs.capi.gc_debug_inject(mp._h, 1, 2_000_000)
+    _, it3, rc3 = mp.sssp(_dev(torch, d0), max_iter=5)
+    assert rc3 == gcs.capi.GC_ERR_NOT_CONVERGED and it3 == -1
+    assert mp.check() == gcs.capi.GC_ERR_TIMEOUT
+    gcs.capi.gc_debug_inject(mp._h, 0, 4_000_000_000)
+    d, it2, rc2 = mp.sssp(_dev(torch, d0))
+    assert rc2 == 0 and it2 == want_it
+    np.testing.assert_array_equal(d.cpu().numpy().view(np.uint32), want_d.view(np.uint32))
+    assert mp.check() == 0
