@@ -389,7 +389,7 @@ __device__ __forceinline__ TailIO<P> tail_io(const SweepArgs<P>& a, int k, typen
 // Lane (slot, part) sums part `part` of the row's symbols q = s+slot,
 // s+slot+S, ... in order, then the group reduces the slots by a fixed butterfly.
 template <class P, int G>
-__device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblocks, int* changed) {
+__device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     using V = typename P::V;
     constexpr int S = G < 32 / P::LPN ? G : 32 / P::LPN;
     constexpr int GG = S * P::LPN;                     // lanes per row
@@ -429,20 +429,7 @@ __device__ void emit_groups(const SweepArgs<P>& a, int64_t block, int64_t nblock
         }
 #pragma unroll
         for (int msk = GG / 2; msk >= P::LPN; msk >>= 1) acc = P::combine(acc, shfl_x(acc, msk));
-        if (row < a.n && slot == 0) {
-            bool stored = false;
-            if constexpr (kFixpointPolicy<P>)
-                if (changed != nullptr) {   // a fixpoint step: x = x (+) y in place (x is no longer read)
-                    V* x = const_cast<V*>(a.x);
-                    const V u = x[row], v = P::combine(u, acc);
-                    if (v != u) {
-                        x[row] = v;
-                        *changed = 1;
-                    }
-                    stored = true;
-                }
-            if (!stored) a.y[row * P::LPN + part] = acc;
-        }
+        if (row < a.n && slot == 0) a.y[row * P::LPN + part] = acc;
         row = nrow;
         s = ns;
         e = ne;
@@ -630,16 +617,14 @@ __device__ void finish_rows(const SweepArgs<P>& a, int64_t gwarp, int64_t nwarps
 
 // Row emit: groups of G lanes per row (emit_group = G).
 template <class P>
-// With changed given (a fixpoint in one launch), each row's sum goes into x
-// instead, x[r] = x[r] (+) y[r], and *changed is set if any x[r] changed.
-__device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks, int* changed = nullptr) {
+__device__ void emit_rows(const SweepArgs<P>& a, int64_t block, int64_t nblocks) {
     switch (a.emit_group) {
-        case 1: emit_groups<P, 1>(a, block, nblocks, changed); break;
-        case 2: emit_groups<P, 2>(a, block, nblocks, changed); break;
-        case 4: emit_groups<P, 4>(a, block, nblocks, changed); break;
-        case 8: emit_groups<P, 8>(a, block, nblocks, changed); break;
-        case 16: emit_groups<P, 16>(a, block, nblocks, changed); break;
-        default: emit_groups<P, 32>(a, block, nblocks, changed); break;
+        case 1: emit_groups<P, 1>(a, block, nblocks); break;
+        case 2: emit_groups<P, 2>(a, block, nblocks); break;
+        case 4: emit_groups<P, 4>(a, block, nblocks); break;
+        case 8: emit_groups<P, 8>(a, block, nblocks); break;
+        case 16: emit_groups<P, 16>(a, block, nblocks); break;
+        default: emit_groups<P, 32>(a, block, nblocks); break;
     }
 }
 
@@ -706,12 +691,10 @@ __device__ __forceinline__ void arrive_on(unsigned long long* bar) {
 // ---------------------------------------------------------------- persistent sweep
 // One product of the persistent sweep, this CTA's share: leaf tables, the
 // wide levels, then (unless the slice kernel takes over) the tail and the
-// emit. nbar counts the launch's grid barriers passed so far. With changed
-// given, the row emit folds its sums into x (a fixpoint step, emit_rows).
-// False if a barrier timed out (the status word says so).
+// emit. nbar counts the launch's grid barriers passed so far. False if a
+// barrier timed out (the status word says so).
 template <class P, bool kC>
-__device__ __forceinline__ bool sweep_product(const SweepArgs<P>& a, unsigned long long& nbar,
-                                              int* changed = nullptr) {
+__device__ __forceinline__ bool sweep_product(const SweepArgs<P>& a, unsigned long long& nbar) {
     const int Lg = a.grid_levels;
     const int64_t GW = (int64_t)gridDim.x * kWarps;
     const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -786,38 +769,34 @@ __device__ __forceinline__ bool sweep_product(const SweepArgs<P>& a, unsigned lo
     }
     if (!grid_sync(a, nbar++)) return false;
     if (a.emode != EMIT_ROWS) emit_final<P>(a, gw, GW);
-    else emit_rows<P>(a, blockIdx.x, gridDim.x, changed);
+    else emit_rows<P>(a, blockIdx.x, gridDim.x);
     return true;
 }
 
 // A whole fixpoint x = x (+) (M (x) x) in one launch (handles whose product is
-// this kernel alone: no slice kernel). With the row emit, the product's emit
-// folds each row's sum into x (nothing reads x after the levels); with the
-// level emit, the product goes into y, a grid barrier, then x = x (+) y over
-// the grid. Either way a changed flag, a grid barrier, and every CTA reads
-// the flag. fix[0] / fix[1] are the changed flags of the even / odd products
-// (a product's flag is cleared by CTA 0 during the product before it, after
-// every CTA has read it), fix[2] = 1 and fix[3] = the product count on
-// convergence; both stay 0 if a.fix_max products did not converge. Each
-// product passes sweep_barriers + 1 grid barriers (+ 2 with the level emit).
+// this kernel alone: no slice kernel): product it into y, a grid barrier, then
+// x = x (+) y over the grid with a changed flag, a grid barrier, and every CTA
+// reads the flag. fix[0] / fix[1] are the changed flags of the even / odd
+// products (a product's flag is cleared by CTA 0 during the product before
+// it, after every CTA has read it), fix[2] = 1 and fix[3] = the product
+// count on convergence; both stay 0 if a.fix_max products did not converge.
+// Each product passes sweep_barriers + 2 grid barriers. (Folding the update
+// into the row emit instead, one barrier fewer, measured slower.)
 template <class P, bool kC>
 __device__ void sweep_fixpoint(const SweepArgs<P>& a, unsigned long long& nbar) {
     using V = typename P::V;
     V* x = const_cast<V*>(a.x);   // x is the fixpoint's iterate, updated in place
     int32_t* fx = a.fix;
-    const bool rows = a.emode == EMIT_ROWS;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nth = (int64_t)gridDim.x * blockDim.x;
     for (int32_t it = 1; it <= a.fix_max; ++it) {
+        if (!sweep_product<P, kC>(a, nbar)) return;
+        if (!grid_sync(a, nbar++)) return;   // every row of y is written and x no longer read
         int ch = 0;
-        if (!sweep_product<P, kC>(a, nbar, rows ? &ch : nullptr)) return;
-        if (!rows) {
-            if (!grid_sync(a, nbar++)) return;   // every row of y is written and x no longer read
-            for (int64_t i = tid; i < a.n; i += nth) {
-                const V u = x[i], v = P::combine(u, a.y[i]);
-                if (v != u) {
-                    x[i] = v;
-                    ch = 1;
-                }
+        for (int64_t i = tid; i < a.n; i += nth) {
+            const V u = x[i], v = P::combine(u, a.y[i]);
+            if (v != u) {
+                x[i] = v;
+                ch = 1;
             }
         }
         if (__syncthreads_or(ch) && threadIdx.x == 0) st_volatile(fx + (it & 1), 1);
@@ -847,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 2) sweep_kernel(const SweepArgs<P> a
         return;
     }
     unsigned long long nbar = 0;
-    if constexpr (kFixpointPolicy<P>)
+    if constexpr (kFixpointPolicy<P> && !kC)   // the one-launch fixpoint runs without carry slots
         if (a.fix != nullptr) {
             sweep_fixpoint<P, kC>(a, nbar);
             return;
@@ -2134,13 +2113,12 @@ bool fused_fixpoint(gc_handle* h, typename P::V* x, int32_t max_iter, int32_t* r
     cuda_check(cudaStreamSynchronize(st), "stream synchronize");
     const bool done = w[0] == 0 && w[6] != 0;
     *result = done ? w[7] : -1;
-    // the launch's grid barriers: sweep_barriers + 1 a product, + 2 with the
-    // level emit (sweep_fixpoint; a timed-out
+    // the launch's grid barriers: sweep_barriers + 2 a product (sweep_fixpoint; a timed-out
     // launch leaves the counter part-way; gc_check restarts it)
     const int64_t products = done ? w[7] : max_iter;
     if (w[0] == 0)
         h->bar_base += (unsigned long long)products *
-                       (unsigned long long)(sweep_barriers(h) + (h->lay.emit == EMIT_ROWS ? 1 : 2)) *
+                       (unsigned long long)(sweep_barriers(h) + 2) *
                        (unsigned long long)grid;
     return done;
 }
