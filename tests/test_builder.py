@@ -524,7 +524,7 @@ def test_cpu_grammar_sweep_on_the_builders_grammar(gcs):
     assert np.array_equal(sw(x, 4), y)
 
 
-@pytest.mark.parametrize("name,rp,c,v", CASES[-4:], ids=[cs[0] for cs in CASES[-4:]])
+@pytest.mark.parametrize("name,rp,c,v", CASES, ids=[cs[0] for cs in CASES])
 def test_balanced_grammar(gcs, name, rp, c, v):
     """Sec. 4.2 pre-balancing (an AVL grammar): same decompression, same
     products, children's heights within one of each other, and depth within
@@ -547,3 +547,25 @@ def test_balanced_grammar(gcs, name, rp, c, v):
     ex2 = export_all(B.balanced())
     for key in ("nodes", "lvl_off", "c_ref"):
         np.testing.assert_array_equal(ex2[key], ex[key])
+
+
+def test_balanced_degenerate_grammars(gcs):
+    # no rules at all, all rows empty, a 1 x 1 matrix, one long repeated row
+    # (a deep right comb that balancing must flatten to about log2 of its
+    # length): the same products and a valid packed grammar
+    cases = [
+        (2, 4, np.array([0, 2, 4], np.int64), np.array([0, 1, 2, 3], np.int32), np.array([1, 2, 3, 4], np.float32)),
+        (3, 5, np.zeros(4, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32)),
+        (1, 1, np.array([0, 1], np.int64), np.array([0], np.int32), np.array([-2.5], np.float32)),
+    ]
+    m = 4096
+    row = np.arange(m, dtype=np.int32)
+    rep = 6
+    cases.append((rep, m, np.arange(rep + 1, dtype=np.int64) * m, np.tile(row, rep),
+                  np.tile(np.where(row % 3 == 0, 1.0, 2.0).astype(np.float32), rep)))
+    for n, m, rp, c, v in cases:
+        G = gcs.Grammar(n, m, rp, c, v)
+        B = G.balanced()
+        check_grammar(B, rp, c, v, n, m, repair_end_state=False)
+        assert B.stats()["depth"] <= max(1, G.stats()["depth"])
+    assert B.stats()["depth"] <= 1.4405 * np.log2(m + 2)
