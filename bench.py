@@ -393,9 +393,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def engine_code_hash(text: str) -> str:
+    """sha256 prefix of a CUDA/C++ source with its comments, blank lines and
+    trailing spaces removed: equal exactly when the code is equal."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':   # string literal: kept whole (a "//" inside is not a comment)
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    code = "\n".join(ln for ln in lines if ln)
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def profile_traffic(kernel_key):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the current kernel code (comments aside; else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -405,9 +431,9 @@ def profile_traffic(kernel_key):
     if not rec:
         return None
     src = os.path.join(ROOT, "grammar_compressed_sparse_gb300", "csrc", "engine.cu")
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec.get("dram_bytes_per_launch") if rec.get("engine_sha") == h else None
+    with open(src, encoding="utf-8") as f:
+        h = engine_code_hash(f.read())
+    return rec.get("dram_bytes_per_launch") if rec.get("engine_code_sha") == h else None
 
 
 class LeftAdapter:

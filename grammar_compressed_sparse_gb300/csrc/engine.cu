@@ -88,7 +88,7 @@ constexpr int LV_START = 0, LV_W = 1, LV_ROOTS = 2, LV_ROFF = 3, LV_ECH = 4, LV_
 constexpr int LV_CR = 6, LV_CN = 7, LV_COFF = 8;   // carried roots, carried others, first carry slot
 constexpr int LV_ROWS = (int)kLevelRows;
 static_assert(LV_COFF < LV_ROWS, "level table rows");
-// device index of carry slot s: kCarryBase + s (above every [T | buffer] index)
+// device index of carry slot s: kCarryBase + s (above every slot of a level buffer)
 constexpr int32_t kCarryBase = 1 << 30;
 
 
@@ -187,7 +187,7 @@ struct SweepArgs {
     int32_t vbits;
     const V* x;
     V* y;
-    V* buf0;                  // [T | level values]
+    V* buf0;                  // level values (the two buffers alternate by level)
     V* buf1;
     V* rv;                    // row emit: [T | root values]
     const int32_t* c_off;     // row emit: C in row order
@@ -2362,7 +2362,8 @@ gc_status gc_upload_ex(const gc_grammar* gg, gc_policy policy, int32_t k_max, in
         h->grid_levels = (int)d.grid_levels;
         const std::vector<int64_t> toff = tail_offsets(g, d.grid_levels);
 
-        // level table; level 1 with leaf codes, later levels with indices into [T | buffer]
+        // level table; node children as slots of the level below, the identity (-1), terminals as
+        // -2 - leaf code, or carry slots
         auto leaf_code = [&](int32_t p) { return (int32_t)(((int64_t)g.term_col[p] << d.vbits) | g.term_vidx[p]); };
         const int64_t A = g.alpha();
         auto ref = [&](int32_t c) -> int32_t {   // device-view reference -> device index

@@ -359,11 +359,11 @@ inline std::vector<int64_t> tail_offsets(const Grammar& g, int64_t Lg) {
 }
 
 // Level emit: chunks of C's early references (terminals and levels 1..Lg),
-// grouped by the level of their symbol and indexed into that level's
-// [T | buffer] space, in chunks of one (level, row). References to the tail
-// levels are kept per row as tail-buffer indices.
+// grouped by the level of their symbol, in chunks of one (level, row): a root
+// slot of that level's buffer, or a terminal as -2 - its leaf code. References
+// to the tail levels are kept per row as tail-buffer indices.
 struct EmitPlan {
-    std::vector<int32_t> cref;      // grouped by (level, row), as [T | buffer] indices
+    std::vector<int32_t> cref;      // grouped by (level, row): root slots, or -2 - leaf code
     std::vector<int32_t> echunk;    // 4 per chunk: start, length, id, 0 (level-major)
     std::vector<int64_t> ech;       // L+2: chunk range of level k
     std::vector<int32_t> row_ech;   // n+1

@@ -40,3 +40,26 @@ def test_our_arm_needs_a_gpu():
     r = _bench("--steps", "1", "--warmup", "1", "--no-cpu-baseline")
     assert r.returncode != 0
     assert "CUDA" in (r.stdout + r.stderr)
+
+
+def test_traffic_record_follows_the_kernel_code():
+    # the bench line's DRAM traffic comes from profiles/traffic.json only while
+    # engine.cu's code (comments aside) is the code the counters were taken on
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    src = 'int f(int a) { // add one\n  return a + 1; /* done */ }\nconst char* s = "x // y";\n'
+    h = b.engine_code_hash(src)
+    assert b.engine_code_hash(src.replace("// add one", "// plus one")) == h
+    assert b.engine_code_hash(src + "\n\n// trailing note\n") == h
+    assert b.engine_code_hash(src.replace("a + 1", "a + 2")) != h
+    assert b.engine_code_hash(src.replace('"x // y"', '"x // z"')) != h   # strings are code
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        recs = json.load(f)
+    with open(os.path.join(ROOT, "grammar_compressed_sparse_gb300", "csrc", "engine.cu"), encoding="utf-8") as f:
+        cur = b.engine_code_hash(f.read())
+    for key, rec in recs.items():
+        assert rec["dram_bytes_per_launch"] > 0 and os.path.exists(os.path.join(ROOT, rec["source"]))
+        got = b.profile_traffic(key)
+        assert got == (rec["dram_bytes_per_launch"] if rec["engine_code_sha"] == cur else None)
