@@ -431,8 +431,11 @@ def profile_traffic(kernel_key):
     if not rec:
         return None
     src = os.path.join(ROOT, "grammar_compressed_sparse_gb300", "csrc", "engine.cu")
-    with open(src, encoding="utf-8") as f:
-        h = engine_code_hash(f.read())
+    try:
+        with open(src, encoding="utf-8") as f:
+            h = engine_code_hash(f.read())
+    except (OSError, UnicodeDecodeError):
+        return None
     return rec.get("dram_bytes_per_launch") if rec.get("engine_code_sha") == h else None
 
 
